@@ -1,0 +1,348 @@
+#!/usr/bin/env python3
+"""Benchmark: chunked Gated DeltaNet forward + backward on GB300.
+
+One step = one forward (o, S_T) and one backward (dq, dk, dv, dg, dbeta) of the
+H=32, T=8192, d=128 bf16 prefill workload through the C ABI, inputs resident in
+HBM.  Prints ONE JSON line (rank 0).  See --help for the options.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gb300|reference]
+
+Timing: W untimed warm-up steps; K timed steps, each bracketed by CUDA events on
+the launch stream, with an L2 flush (a 256 MB write) before every step that is
+outside the events; barrier + synchronize around the timed loop; max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN chunked fwd+bwd tokens/s (bf16, d=128) on 1 GB300; % of HBM roofline"
+DEFAULT_WORKLOAD = "prefill_h32_t8192"
+
+
+# ----------------------------------------------------------------------------- accounting
+def algorithmic_bytes(w, x):
+    """Bytes the method must move (per call), per the roofline accounting:
+    forward 2*(dk+dk+dv)*e + 8 + dv*e per token-head (q, k, v, g, beta in; o out) plus
+    4*d^2 per (sequence, head) for S0 in / S_T out; backward q, k, v, dO, g, beta in and
+    dq, dk, dv, dg, dbeta out plus the state terms."""
+    e = 2 if x["dtype"] == "bf16" else 4
+    D = x["D"]
+    tokens = x["q"].shape[0] * x["q"].shape[1]
+    th = tokens * x["H"]
+    sh = x["N"] * x["H"]
+    st = 4 * D * D
+    fwd = th * (3 * D * e + 8 + D * e) + sh * st * ((x["S0"] is not None) + 1)
+    bwd = th * (4 * D * e + 8 + 3 * D * e + 8) + sh * st * ((x["S0"] is not None) * 2 + (x["dST"] is not None))
+    per_kernel = {
+        "fwd_chunk": fwd,
+        "fwd_states": th * (3 * D * e + 8),        # q, k, v, g, beta in (state copies are workspace)
+        "bwd_chain": th * (3 * D * e + 8),         # q, k, dO, g, beta in
+        "bwd_local": th * (4 * D * e + 8 + 3 * D * e + 8),
+    }
+    return fwd, bwd, per_kernel
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1901.0)), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle legs
+def cpu_oracle_sample(wname, heads=None, tokens=None):
+    """Time the fp64 oracle (fwd + bwd) on a bounded sample of the workload: the
+    first `heads` heads (default: one per core) over `tokens` tokens per sequence.
+    Returns (tokens/s scaled to the whole workload's head count, cores, description)."""
+    import torch
+
+    import oracle
+    from gdn_inputs import WORKLOADS, make_inputs
+    w = WORKLOADS[wname]
+    cores = os.cpu_count() or 1
+    Hs = min(w.H, heads or cores)
+    T = tokens or (w.T if w.T else 4096)
+    x = make_inputs(w, "cpu", H=Hs, T=T, B=1)
+    t0 = time.perf_counter()
+    oracle.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], scale=x["scale"], l2norm=x["l2norm"],
+               nthreads=cores)
+    oracle.bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["dO"], x["S0"], None, scale=x["scale"],
+               l2norm=x["l2norm"], nthreads=cores)
+    dt = time.perf_counter() - t0
+    # the workload's tokens/s: T tokens of all H heads cost H/Hs times the sample
+    tps = T * (Hs / w.H) / dt
+    return tps, min(cores, Hs), f"fwd+bwd of {Hs} of {w.H} heads x {T} tokens (B=1), {dt:.2f} s"
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle as it stands, on the host cores (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    times, tps_all = [], []
+    desc, cores = "", 1
+    from gdn_inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    for i in range(args.warmup + args.steps):
+        tps, cores, desc = cpu_oracle_sample(args.workload, tokens=args.ref_tokens)
+        if i >= args.warmup:
+            tps_all.append(tps)
+    value = statistics.median(tps_all)
+    tokens_per_step = (w.B * w.T) if w.T else 135168
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000.0 * tokens_per_step / value, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": args.workload, "B": w.B, "T": w.T, "H": w.H, "d": w.D},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-tokens", type=int, default=None, help="tokens per sequence in the reference sample")
+    ap.add_argument("--seg-chunks", type=int, default=0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    # CPU baseline first (before heavy GPU work), rank 0 at N=1 only
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tps, cores, desc = cpu_oracle_sample(args.workload)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    import __graft_entry__
+    __graft_entry__.build_library()
+    import gated_deltanet_linear_15_gb300 as g
+    from gdn_inputs import WORKLOADS, make_inputs
+
+    w = WORKLOADS[args.workload]
+    x = make_inputs(w, dev, seed=w.seed + 1000 * rank)
+    shape = g.make_shape(x["q"], x["v"], cu_seqlens=x["cu_seqlens"], scale=x["scale"], l2norm=x["l2norm"],
+                         seg_chunks=args.seg_chunks)
+    plan = g.gdn_plan_query(shape)
+    ws_bytes = max(g.gdn_fwd_workspace_size(shape), g.gdn_bwd_workspace_size(shape))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    o = torch.empty_like(x["v"])
+    N, H, D = x["N"], x["H"], x["D"]
+    ST = torch.empty(N, H, D, D, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"])
+    dg, db = torch.empty_like(x["g"]), torch.empty_like(x["beta"])
+    dS0 = torch.empty_like(x["S0"]) if x["S0"] is not None else None
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def fwd():
+        rc = g.gdn_chunk_fwd(shape, x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], o, ST, ws, ws_bytes, stream)
+        assert rc == 0, g._lib.last_error()
+
+    def bwd():
+        rc = g.gdn_chunk_bwd(shape, x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], x["dO"], x["dST"], dq, dk,
+                             dv, dg, db, dS0, ws, ws_bytes, stream)
+        assert rc == 0, g._lib.last_error()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    g.gdn_profile_report(reset=True)
+    g.gdn_profile_enable(True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        fwd()
+        evs[i][1].record(stream)
+        bwd()
+        evs[i][2].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    g.gdn_profile_enable(False)
+    clk = clocks.stop()
+    prof = g.gdn_profile_report(reset=True)
+    fwd_ms = [a.elapsed_time(b) for a, b, c in evs]
+    bwd_ms = [b.elapsed_time(c) for a, b, c in evs]
+    step_ms = sum(fwd_ms) + sum(bwd_ms)
+    t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    tokens_per_step = x["q"].shape[0] * x["q"].shape[1]
+    value = world * tokens_per_step * args.steps / (total_ms / 1000.0)
+
+    # ---- roofline of the dominant kernel, from the live per-launch events
+    hbm_peak, bf16_peak, peak_kind = load_peaks()
+    fwd_b, bwd_b, per_kernel = algorithmic_bytes(w, x)
+    kern = {k: v for k, v in prof.items()}
+    dom = max(kern, key=lambda k: kern[k][1]) if kern else None
+    roof = None
+    if dom:
+        cnt, ms = kern[dom]
+        avg_s = ms / cnt / 1000.0
+        alg = per_kernel.get(dom)
+        if alg is not None:
+            ach = alg / avg_s / 1e9
+            roof = {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
+                    "frac": round(ach / hbm_peak, 4), "peak_kind": peak_kind, "traffic": None,
+                    "avg_launch_us": round(avg_s * 1e6, 2), "algorithmic_bytes_per_launch": alg}
+    launches = sum(c for c, _ in kern.values())
+    fwd_s = statistics.mean(fwd_ms) / 1000.0
+    bwd_s = statistics.mean(bwd_ms) / 1000.0
+    kernel_table = {k: {"launches": c, "total_ms": round(ms, 4), "share": round(ms / max(1e-9, sum(
+        m for _, m in kern.values())), 4)} for k, (c, ms) in sorted(kern.items(), key=lambda kv: -kv[1][1])}
+
+    # ---- end-to-end through the public API with host buffers
+    e2e = None
+    if rank == 0:
+        host_in = {k: x[k].cpu().pin_memory() for k in ("q", "k", "v", "g", "beta", "dO")}
+        dev_in = {k: torch.empty_like(x[k]) for k in host_in}
+        host_out = {"o": torch.empty_like(o, device="cpu").pin_memory(),
+                    "dq": torch.empty_like(dq, device="cpu").pin_memory(),
+                    "dk": torch.empty_like(dk, device="cpu").pin_memory(),
+                    "dv": torch.empty_like(dv, device="cpu").pin_memory(),
+                    "dg": torch.empty_like(dg, device="cpu").pin_memory(),
+                    "dbeta": torch.empty_like(db, device="cpu").pin_memory()}
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+        def e2e_step():
+            for k in host_in:
+                dev_in[k].copy_(host_in[k], non_blocking=True)
+            rc = g.gdn_chunk_fwd(shape, dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"],
+                                 x["S0"], o, ST, ws, ws_bytes, stream)
+            assert rc == 0
+            rc = g.gdn_chunk_bwd(shape, dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"], x["S0"],
+                                 dev_in["dO"], x["dST"], dq, dk, dv, dg, db, dS0, ws, ws_bytes, stream)
+            assert rc == 0
+            for k, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv), ("dg", dg), ("dbeta", db)):
+                host_out[k].copy_(t, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(3, min(args.steps, 10))
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a0.elapsed_time(a1) / n_e2e
+        e2e = {"value": tokens_per_step / (e2e_ms / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if x["dtype"] == "bf16" else "fp32",
+            "data": "synthetic (seeded gdn_inputs; q,k raw Gaussian with in-kernel L2 norm)",
+            "config": {"workload": args.workload, "B": x["q"].shape[0], "T": x["q"].shape[1], "H": H, "d": D,
+                       "chunk": 64, "l2norm_in_kernel": x["l2norm"], "initial_state": x["S0"] is not None,
+                       "seg_chunks": plan["seg_chunks"], "l2": "256 MB flush before every step, outside the events",
+                       "parallelism": f"replica x{world}"},
+            "fwd_ms": round(1000 * fwd_s, 4), "bwd_ms": round(1000 * bwd_s, 4),
+            "fwd_hbm_frac": round(fwd_b / fwd_s / 1e9 / hbm_peak, 4),
+            "bwd_hbm_frac": round(bwd_b / bwd_s / 1e9 / hbm_peak, 4),
+            "fwdbwd_hbm_frac": round((fwd_b + bwd_b) / (fwd_s + bwd_s) / 1e9 / hbm_peak, 4),
+            "roofline": roof, "kernels": kernel_table, "gpu_launches": launches, "cpu_baseline": cpu, "e2e": e2e,
+            "clocks": clk, "wall_s": round(wall, 3),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,195 @@
+"""GB300 (sm_103a) chunked Gated DeltaNet: Python binding of the C ABI in include/gdn.h.
+
+Every step of the forward and backward runs in the library's CUDA kernels;
+this module only marshals arguments (tensor pointers, the current stream,
+workspace tensors from PyTorch's allocator).  If the library is not built the
+calls raise: there is no CPU or PyTorch fallback.
+
+Low-level (same names as the C entry points): ``gdn_chunk_fwd``,
+``gdn_chunk_bwd``, ``gdn_fwd_workspace_size``, ``gdn_bwd_workspace_size``,
+``gdn_plan_query``, ``gdn_get_device_status``.
+High-level: ``chunk_gated_delta_rule_fwd/_bwd`` (allocate outputs) and
+``chunk_gated_delta_rule`` (autograd).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Optional
+
+import torch
+
+from . import _lib
+from ._lib import (GDN_BF16, GDN_FP32, GDN_L2NORM_QK, GDN_SP_OFF, GDN_WINDOW_OFF, GdnShape)
+
+__all__ = ["GdnShape", "make_shape", "gdn_chunk_fwd", "gdn_chunk_bwd", "gdn_fwd_workspace_size",
+           "gdn_bwd_workspace_size", "gdn_plan_query", "gdn_get_device_status", "gdn_profile_enable",
+           "gdn_profile_report",
+           "chunk_gated_delta_rule_fwd", "chunk_gated_delta_rule_bwd", "chunk_gated_delta_rule",
+           "GDN_L2NORM_QK", "GDN_SP_OFF", "GDN_WINDOW_OFF"]
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        lib = _lib.load()
+        raise RuntimeError(f"{what}: {lib.gdn_status_string(rc).decode()} ({_lib.last_error()})")
+
+
+def make_shape(q: torch.Tensor, v: torch.Tensor, *, cu_seqlens: Optional[torch.Tensor] = None,
+               scale: Optional[float] = None, l2norm: bool = False, sp: bool = True, window: bool = True,
+               seg_chunks: int = 0) -> GdnShape:
+    B, T, H, Dk = q.shape
+    s = GdnShape()
+    s.B, s.T, s.H, s.Dk, s.Dv = B, T, H, Dk, v.shape[-1]
+    if cu_seqlens is not None:
+        s.cu_seqlens = cu_seqlens.data_ptr()
+        s.num_seqs = cu_seqlens.numel() - 1
+    s.dtype = GDN_BF16 if q.dtype == torch.bfloat16 else GDN_FP32
+    s.scale = 1.0 / math.sqrt(Dk) if scale is None else float(scale)
+    s.flags = (GDN_L2NORM_QK if l2norm else 0) | (0 if sp else GDN_SP_OFF) | (0 if window else GDN_WINDOW_OFF)
+    s.seg_chunks = int(seg_chunks)
+    return s
+
+
+# ------------------------------------------------------------------ C entry points
+def gdn_fwd_workspace_size(shape: GdnShape) -> int:
+    return int(_lib.load().gdn_fwd_workspace_size(ctypes.byref(shape)))
+
+
+def gdn_bwd_workspace_size(shape: GdnShape) -> int:
+    return int(_lib.load().gdn_bwd_workspace_size(ctypes.byref(shape)))
+
+
+def gdn_plan_query(shape: GdnShape):
+    a, b, c = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(_lib.load().gdn_plan_query(ctypes.byref(shape), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)),
+           "gdn_plan_query")
+    return dict(seg_chunks=a.value, max_segments=b.value, max_chunks=c.value)
+
+
+def gdn_chunk_fwd(shape: GdnShape, q, k, v, g, beta, S0, o, S_T, workspace, workspace_bytes: int = None,
+                  stream=None) -> int:
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    return _lib.load().gdn_chunk_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                     _ptr(S0), _ptr(o), _ptr(S_T), _ptr(workspace), int(workspace_bytes),
+                                     _stream(stream))
+
+
+def gdn_chunk_bwd(shape: GdnShape, q, k, v, g, beta, S0, dO, dS_T, dq, dk, dv, dg, dbeta, dS0, workspace,
+                  workspace_bytes: int = None, stream=None) -> int:
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    return _lib.load().gdn_chunk_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                     _ptr(S0), _ptr(dO), _ptr(dS_T), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg),
+                                     _ptr(dbeta), _ptr(dS0), _ptr(workspace), int(workspace_bytes),
+                                     _stream(stream))
+
+
+def gdn_profile_enable(on: bool) -> None:
+    _check(_lib.load().gdn_profile_enable(int(bool(on))), "gdn_profile_enable")
+
+
+def gdn_profile_report(reset: bool = True) -> dict:
+    """{kernel: (launches, total_ms)} since the last reset."""
+    lib = _lib.load()
+    n = lib.gdn_profile_report(None, 0, 0)
+    buf = ctypes.create_string_buffer(n + 1)
+    lib.gdn_profile_report(buf, n + 1, int(bool(reset)))
+    out = {}
+    for line in buf.value.decode().splitlines():
+        name, cnt, ms = line.split()
+        out[name] = (int(cnt), float(ms))
+    return out
+
+
+def gdn_get_device_status(shape: GdnShape, workspace, stream=None) -> int:
+    return int(_lib.load().gdn_get_device_status(ctypes.byref(shape), _ptr(workspace), _stream(stream)))
+
+
+# ------------------------------------------------------------------ allocation helpers
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def _contig(*ts):
+    for t in ts:
+        if t is not None and not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+
+
+def chunk_gated_delta_rule_fwd(q, k, v, g, beta, initial_state=None, output_final_state=True, cu_seqlens=None,
+                               scale=None, use_qk_l2norm_in_kernel=False, sp=True, window=True, seg_chunks=0,
+                               workspace=None):
+    """o, S_T (S_T None unless output_final_state)."""
+    _contig(q, k, v, g, beta, initial_state)
+    shape = make_shape(q, v, cu_seqlens=cu_seqlens, scale=scale, l2norm=use_qk_l2norm_in_kernel, sp=sp,
+                       window=window, seg_chunks=seg_chunks)
+    N = shape.num_seqs if cu_seqlens is not None else q.shape[0]
+    o = torch.empty_like(v)
+    S_T = torch.empty(N, q.shape[2], v.shape[-1], q.shape[-1], dtype=torch.float32, device=q.device) \
+        if output_final_state else None
+    need = gdn_fwd_workspace_size(shape)
+    if need == 0:
+        _check(_lib.GDN_ERR_INVALID_ARG, "gdn_fwd_workspace_size")
+    ws = workspace if workspace is not None and workspace.numel() >= need else _workspace(need, q.device)
+    _check(gdn_chunk_fwd(shape, q, k, v, g, beta, initial_state, o, S_T, ws), "gdn_chunk_fwd")
+    return o, S_T
+
+
+def chunk_gated_delta_rule_bwd(q, k, v, g, beta, dO, initial_state=None, dS_T=None, cu_seqlens=None, scale=None,
+                               use_qk_l2norm_in_kernel=False, sp=True, window=True, seg_chunks=0, workspace=None):
+    """dq, dk, dv, dg, dbeta, dS0 (dS0 None without an initial state)."""
+    _contig(q, k, v, g, beta, dO, initial_state, dS_T)
+    shape = make_shape(q, v, cu_seqlens=cu_seqlens, scale=scale, l2norm=use_qk_l2norm_in_kernel, sp=sp,
+                       window=window, seg_chunks=seg_chunks)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dg, db = torch.empty_like(g), torch.empty_like(beta)
+    dS0 = torch.empty_like(initial_state) if initial_state is not None else None
+    need = gdn_bwd_workspace_size(shape)
+    if need == 0:
+        _check(_lib.GDN_ERR_INVALID_ARG, "gdn_bwd_workspace_size")
+    ws = workspace if workspace is not None and workspace.numel() >= need else _workspace(need, q.device)
+    _check(gdn_chunk_bwd(shape, q, k, v, g, beta, initial_state, dO, dS_T, dq, dk, dv, dg, db, dS0, ws),
+           "gdn_chunk_bwd")
+    return dq, dk, dv, dg, db, dS0
+
+
+class ChunkGatedDeltaRuleFunction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, g, beta, initial_state, cu_seqlens, scale, l2norm):
+        o, S_T = chunk_gated_delta_rule_fwd(q, k, v, g, beta, initial_state, True, cu_seqlens, scale, l2norm)
+        ctx.save_for_backward(q, k, v, g, beta, initial_state, cu_seqlens)
+        ctx.scale, ctx.l2norm = scale, l2norm
+        return o, S_T
+
+    @staticmethod
+    def backward(ctx, dO, dS_T):
+        q, k, v, g, beta, S0, cu = ctx.saved_tensors
+        dq, dk, dv, dg, db, dS0 = chunk_gated_delta_rule_bwd(
+            q, k, v, g, beta, dO.contiguous(), S0, None if dS_T is None else dS_T.contiguous(), cu, ctx.scale,
+            ctx.l2norm)
+        return dq, dk, dv, dg, db, dS0, None, None, None
+
+
+def chunk_gated_delta_rule(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=None,
+                           use_qk_l2norm_in_kernel=False):
+    """Autograd entry: returns (o, final_state)."""
+    return ChunkGatedDeltaRuleFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, scale,
+                                             use_qk_l2norm_in_kernel)

@@ -1,0 +1,521 @@
+// C ABI of the library: argument validation, workspace layout, segment-length
+// choice and the launch sequence of the forward and backward passes.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/gdn.h"
+#include "kernels.h"
+
+using namespace gdn;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int num_sms() {
+  static std::mutex mu;
+  static std::vector<int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  std::lock_guard<std::mutex> lk(mu);
+  if ((int)cache.size() <= dev) cache.resize(dev + 1, 0);
+  if (cache[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+    cache[dev] = v;
+  }
+  return cache[dev];
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct Layout {
+  int N = 0, H = 0, D = 0, Tseq = 0;  // Tseq: per-sequence length for uniform batches, 0 for packed
+  long Ttot = 0;
+  int CH_max = 0, S_max = 0, Lseg = 1;
+  bool sp = false;  // more than one segment possible for some sequence
+  size_t esize = 2;
+  size_t off_status = 0, off_plan = 0, off_gsum = 0;
+  size_t off_E = 0, off_M = 0, off_S = 0;     // forward fix-up buffers
+  size_t off_states = 0, off_dstates = 0;   // backward per-chunk states
+  size_t off_F = 0, off_R = 0, off_dS = 0;  // reverse fix-up buffers
+  size_t fwd_total = 0, bwd_total = 0;
+};
+
+// Chunks per segment.  One CTA per (segment, head) runs a serial chain over its
+// chunks, so with few (sequence, head) pairs the sequences are split until the
+// work items fill the SMs (onedev.kr FlashQLA talk summary, paragraph on
+// parallelism: one head per SM leaves most of a >100-SM card idle).  Estimated
+// time ~ waves(items) * (chunks per segment + ~2 warm-up chunks).
+int choose_lseg(const gdn_shape &s, int N, int maxc, int CH_max) {
+  if (maxc <= 0) return 1;
+  if (s.flags & GDN_SP_OFF) return maxc;
+  if (s.seg_chunks > 0) return s.seg_chunks;
+  const int slots = num_sms();
+  if ((long)N * s.H >= slots) return maxc;
+  int best = maxc;
+  double best_cost = 1e300;
+  for (int L = 1; L <= maxc; ++L) {
+    double items;
+    if (s.cu_seqlens) items = (double)s.H * ((double)CH_max / L + 0.5 * N);
+    else items = (double)N * s.H * ((maxc + L - 1) / L);
+    const double waves = std::ceil(items / slots);
+    const double cost = waves * (L + (L < maxc ? 2.0 : 0.0));
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = L;
+    }
+  }
+  return best;
+}
+
+int make_layout(const gdn_shape *s, Layout &L) {
+  if (!s) return fail(GDN_ERR_INVALID_ARG, "shape is NULL");
+  if (s->reserved[0] || s->reserved[1] || s->reserved[2]) return fail(GDN_ERR_INVALID_ARG, "reserved fields must be 0");
+  if (s->B < 1 || s->T < 0 || s->H < 1) return fail(GDN_ERR_INVALID_ARG, "need B >= 1, T >= 0, H >= 1");
+  if (s->Dk != s->Dv) return fail(GDN_ERR_UNSUPPORTED, "d_k != d_v is not supported");
+  if (s->Dk != 64 && s->Dk != 128) return fail(GDN_ERR_UNSUPPORTED, "d must be 64 or 128 (got %d)", s->Dk);
+  if (s->dtype != GDN_BF16 && s->dtype != GDN_FP32) return fail(GDN_ERR_INVALID_ARG, "unknown dtype");
+  if (s->dtype == GDN_FP32 && s->Dk != 64) return fail(GDN_ERR_UNSUPPORTED, "fp32 mode supports d = 64 only");
+  if (s->seg_chunks < 0) return fail(GDN_ERR_INVALID_ARG, "seg_chunks must be >= 0");
+  if (!std::isfinite(s->scale) || s->scale == 0.f) return fail(GDN_ERR_INVALID_ARG, "scale must be finite and non-zero");
+  if (s->cu_seqlens) {
+    if (s->B != 1) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens requires B == 1");
+    if (s->num_seqs < 1) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens requires num_seqs >= 1");
+    L.N = s->num_seqs;
+    L.Tseq = 0;
+  } else {
+    L.N = s->B;
+    L.Tseq = s->T;
+  }
+  if ((long)s->B * s->T > (long)INT32_MAX / 2) return fail(GDN_ERR_UNSUPPORTED, "too many tokens");
+  L.H = s->H;
+  L.D = s->Dk;
+  L.Ttot = (long)s->B * s->T;
+  L.esize = s->dtype == GDN_BF16 ? 2 : 4;
+  int maxc;
+  if (s->cu_seqlens) {
+    L.CH_max = (int)((L.Ttot + (long)(CH - 1) * L.N) / CH);
+    maxc = (int)((L.Ttot + CH - 1) / CH);
+  } else {
+    maxc = (s->T + CH - 1) / CH;
+    L.CH_max = L.N * maxc;
+  }
+  L.Lseg = std::max(1, choose_lseg(*s, L.N, maxc, L.CH_max));
+  if (s->cu_seqlens) L.S_max = L.CH_max / L.Lseg + 2 * L.N + 1;
+  else L.S_max = L.N * std::max(1, (maxc + L.Lseg - 1) / L.Lseg);
+  L.sp = L.Lseg < maxc;
+  const size_t DD = (size_t)L.D * L.D;
+  const size_t nplan = 5 * (size_t)L.N + L.S_max + L.CH_max + 2;
+  size_t off = 0;
+  L.off_status = off;
+  off += 256;
+  L.off_plan = off;
+  off = align256(off + nplan * 4);
+  L.off_gsum = off;
+  off = align256(off + (size_t)L.CH_max * L.H * 4);
+  const size_t spbuf = L.sp ? align256((size_t)L.S_max * L.H * DD * 4) : 0;
+  L.off_E = off;
+  off += spbuf;
+  L.off_M = off;
+  off += spbuf;
+  L.off_S = off;
+  off += spbuf;
+  L.fwd_total = off;
+  L.off_states = off;
+  off = align256(off + (size_t)L.CH_max * L.H * DD * L.esize);
+  L.off_dstates = off;
+  off = align256(off + (size_t)L.CH_max * L.H * DD * L.esize);
+  L.off_F = off;
+  off += spbuf;
+  L.off_R = off;
+  off += spbuf;
+  L.off_dS = off;
+  off += spbuf;
+  L.bwd_total = off;
+  return GDN_OK;
+}
+
+Plan plan_of(const Layout &L, char *ws) {
+  int *p = reinterpret_cast<int *>(ws + L.off_plan);
+  Plan pl;
+  pl.seq_bos = p;
+  pl.seq_len = p + L.N;
+  pl.seq_chunk0 = p + 2 * L.N;
+  pl.seq_seg0 = p + 3 * L.N;
+  pl.seq_nseg = p + 4 * L.N;
+  pl.seg_seq = p + 5 * L.N;
+  pl.chunk_seq = pl.seg_seq + L.S_max;
+  pl.totals = pl.chunk_seq + L.CH_max;
+  return pl;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int check_ptrs(std::initializer_list<std::pair<const void *, const char *>> req,
+               std::initializer_list<std::pair<const void *, const char *>> opt) {
+  for (auto &x : req) {
+    if (!x.first) return fail(GDN_ERR_INVALID_ARG, "%s is NULL", x.second);
+    if (!aligned16(x.first)) return fail(GDN_ERR_INVALID_ARG, "%s is not 16-byte aligned", x.second);
+  }
+  for (auto &x : opt)
+    if (x.first && !aligned16(x.first)) return fail(GDN_ERR_INVALID_ARG, "%s is not 16-byte aligned", x.second);
+  return GDN_OK;
+}
+
+// ------------------------------------------------------------------ profiler
+// Optional per-launch CUDA-event timing (diagnostics for benchmarks): when
+// enabled, every kernel launch is bracketed by two events from a fixed pool on
+// the launch stream; gdn_profile_report() sums the durations per kernel name.
+struct ProfRec {
+  const char *name;
+  int ev0, ev1;
+};
+struct Profiler {
+  std::mutex mu;
+  bool on = false;
+  std::vector<cudaEvent_t> pool;
+  int used = 0;
+  std::vector<ProfRec> recs;
+  std::vector<std::string> names;
+  std::vector<double> total_ms;
+  std::vector<long> count;
+};
+Profiler g_prof;
+
+struct ProfScope {
+  int idx = -1;
+  cudaStream_t st;
+  const char *name;
+  ProfScope(const char *n, cudaStream_t s) : st(s), name(n) {
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    if (!g_prof.on || g_prof.used + 2 > (int)g_prof.pool.size()) return;
+    idx = g_prof.used;
+    g_prof.used += 2;
+    cudaEventRecord(g_prof.pool[idx], st);
+  }
+  ~ProfScope() {
+    if (idx < 0) return;
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    cudaEventRecord(g_prof.pool[idx + 1], st);
+    g_prof.recs.push_back({name, idx, idx + 1});
+  }
+};
+
+void prof_drain_locked() {
+  for (auto &r : g_prof.recs) {
+    float ms = 0.f;
+    cudaEventSynchronize(g_prof.pool[r.ev1]);
+    cudaEventElapsedTime(&ms, g_prof.pool[r.ev0], g_prof.pool[r.ev1]);
+    size_t i = 0;
+    for (; i < g_prof.names.size(); ++i)
+      if (g_prof.names[i] == r.name) break;
+    if (i == g_prof.names.size()) {
+      g_prof.names.push_back(r.name);
+      g_prof.total_ms.push_back(0.0);
+      g_prof.count.push_back(0);
+    }
+    g_prof.total_ms[i] += ms;
+    g_prof.count[i] += 1;
+  }
+  g_prof.recs.clear();
+  g_prof.used = 0;
+}
+
+#define PROF(name) ProfScope _prof_scope(name, st)
+
+#define CK(expr)                                                                                  \
+  do {                                                                                            \
+    int _e = (expr);                                                                              \
+    if (_e != 0) return fail(GDN_ERR_CUDA, "%s failed: %s", #expr, cudaGetErrorString((cudaError_t)_e)); \
+  } while (0)
+
+// plan + gate scan, shared by both directions
+int prologue(const gdn_shape *s, const Layout &L, char *ws, const float *g, cudaStream_t st, Plan &pl) {
+  pl = plan_of(L, ws);
+  int *status = reinterpret_cast<int *>(ws + L.off_status);
+  CK((int)cudaMemsetAsync(status, 0, 4, st));
+  {
+    PROF("plan");
+    CK(launch_plan(pl, s->cu_seqlens, L.N, s->cu_seqlens ? s->T : L.Tseq, L.Lseg, L.S_max, L.CH_max, status, st));
+  }
+  {
+    PROF("gate_scan");
+    CK(launch_gate_scan(pl, g, L.H, L.CH_max, reinterpret_cast<float *>(ws + L.off_gsum), status, st));
+  }
+  return GDN_OK;
+}
+
+// Forward state pass: pass A + fix-up when segments exist, then `pass` (1: outputs, 2: states).
+int forward_passes(const gdn_shape *s, const Layout &L, char *ws, FwdArgs fa, int pass, cudaStream_t st) {
+  const bool bf = s->dtype == GDN_BF16;
+  if (L.sp) {
+    fa.pass = 0;
+    {
+      PROF("fwd_segment_pass_a");
+      CK(launch_fwd_chunk(fa, bf, L.D, dim3(L.S_max, L.H, 2), st));
+    }
+    FixupArgs fx;
+    fx.plan = fa.plan;
+    fx.gsum = fa.gsum;
+    fx.E = fa.Ebuf;
+    fx.M = fa.Mbuf;
+    fx.out = fa.Sstart;
+    fx.H = L.H;
+    fx.D = L.D;
+    fx.Lseg = L.Lseg;
+    fx.flags = fa.flags;
+    fx.reverse = 0;
+    PROF("fixup_fwd");
+    CK(launch_fixup(fx, L.N, st));
+  }
+  fa.pass = pass;
+  PROF(pass == 1 ? "fwd_chunk" : "fwd_states");
+  CK(launch_fwd_chunk(fa, bf, L.D, dim3(L.S_max, L.H, 1), st));
+  return GDN_OK;
+}
+
+FwdArgs fwd_args(const gdn_shape *s, const Layout &L, char *ws, const Plan &pl) {
+  FwdArgs fa;
+  std::memset(&fa, 0, sizeof fa);
+  fa.plan = pl;
+  fa.gsum = reinterpret_cast<const float *>(ws + L.off_gsum);
+  fa.status = reinterpret_cast<int *>(ws + L.off_status);
+  if (L.sp) {
+    fa.Ebuf = reinterpret_cast<float *>(ws + L.off_E);
+    fa.Mbuf = reinterpret_cast<float *>(ws + L.off_M);
+    fa.Sstart = reinterpret_cast<float *>(ws + L.off_S);
+  }
+  fa.H = L.H;
+  fa.Lseg = L.Lseg;
+  fa.scale = s->scale;
+  fa.flags = s->flags;
+  return fa;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t gdn_fwd_workspace_size(const gdn_shape *shape) {
+  Layout L;
+  if (make_layout(shape, L) != GDN_OK) return 0;
+  return L.fwd_total;
+}
+
+size_t gdn_bwd_workspace_size(const gdn_shape *shape) {
+  Layout L;
+  if (make_layout(shape, L) != GDN_OK) return 0;
+  return L.bwd_total;
+}
+
+int gdn_chunk_fwd(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g, const float *beta,
+                  const float *S0, void *o, float *S_T, void *workspace, size_t workspace_bytes,
+                  gdn_stream_t stream) {
+  g_last_error.clear();
+  Layout L;
+  int rc = make_layout(s, L);
+  if (rc) return rc;
+  if (L.Ttot > 0 || S_T) {
+    rc = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {g, "g"}, {beta, "beta"}, {o, "o"}},
+                    {{S0, "S0"}, {S_T, "S_T"}, {s->cu_seqlens, "cu_seqlens"}});
+    if (rc) return rc;
+  }
+  if (!workspace || workspace_bytes < L.fwd_total)
+    return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", L.fwd_total,
+                workspace ? workspace_bytes : (size_t)0);
+  if (!aligned16(workspace)) return fail(GDN_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(workspace);
+  Plan pl;
+  if ((rc = prologue(s, L, ws, g, st, pl))) return rc;
+  FwdArgs fa = fwd_args(s, L, ws, pl);
+  fa.q = q;
+  fa.k = k;
+  fa.v = v;
+  fa.g = g;
+  fa.beta = beta;
+  fa.S0 = S0;
+  fa.o = o;
+  fa.ST = S_T;
+  return forward_passes(s, L, ws, fa, 1, st);
+}
+
+int gdn_chunk_bwd(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g, const float *beta,
+                  const float *S0, const void *dO, const float *dS_T, void *dq, void *dk, void *dv, float *dg,
+                  float *dbeta, float *dS0, void *workspace, size_t workspace_bytes, gdn_stream_t stream) {
+  g_last_error.clear();
+  Layout L;
+  int rc = make_layout(s, L);
+  if (rc) return rc;
+  if (S0 && !dS0) return fail(GDN_ERR_INVALID_ARG, "dS0 is required when S0 is given");
+  rc = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {g, "g"}, {beta, "beta"}, {dO, "dO"}, {dq, "dq"}, {dk, "dk"},
+                   {dv, "dv"}, {dg, "dg"}, {dbeta, "dbeta"}},
+                  {{S0, "S0"}, {dS_T, "dS_T"}, {dS0, "dS0"}, {s->cu_seqlens, "cu_seqlens"}});
+  if (rc) return rc;
+  if (!workspace || workspace_bytes < L.bwd_total)
+    return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", L.bwd_total,
+                workspace ? workspace_bytes : (size_t)0);
+  if (!aligned16(workspace)) return fail(GDN_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(workspace);
+  const bool bf = s->dtype == GDN_BF16;
+  Plan pl;
+  if ((rc = prologue(s, L, ws, g, st, pl))) return rc;
+  // 1. forward states at every chunk start
+  FwdArgs fa = fwd_args(s, L, ws, pl);
+  fa.q = q;
+  fa.k = k;
+  fa.v = v;
+  fa.g = g;
+  fa.beta = beta;
+  fa.S0 = S0;
+  fa.states = ws + L.off_states;
+  if ((rc = forward_passes(s, L, ws, fa, 2, st))) return rc;
+  // 2. reverse chain: dS at every chunk end (and dS0)
+  BwdArgs ba;
+  std::memset(&ba, 0, sizeof ba);
+  ba.q = q;
+  ba.k = k;
+  ba.v = v;
+  ba.dO = dO;
+  ba.g = g;
+  ba.beta = beta;
+  ba.dST = dS_T;
+  ba.dq = dq;
+  ba.dk = dk;
+  ba.dv = dv;
+  ba.dg = dg;
+  ba.dbeta = dbeta;
+  ba.dS0 = dS0;
+  ba.plan = pl;
+  ba.gsum = reinterpret_cast<const float *>(ws + L.off_gsum);
+  ba.status = reinterpret_cast<int *>(ws + L.off_status);
+  if (L.sp) {
+    ba.Fbuf = reinterpret_cast<float *>(ws + L.off_F);
+    ba.Rbuf = reinterpret_cast<float *>(ws + L.off_R);
+    ba.dSend = reinterpret_cast<float *>(ws + L.off_dS);
+  }
+  ba.states = ws + L.off_states;
+  ba.dstates = ws + L.off_dstates;
+  ba.H = L.H;
+  ba.Lseg = L.Lseg;
+  ba.scale = s->scale;
+  ba.flags = s->flags;
+  if (L.sp) {
+    ba.pass = 0;
+    {
+      PROF("bwd_chain_pass_a");
+      CK(launch_bwd_chain(ba, bf, L.D, dim3(L.S_max, L.H, 2), st));
+    }
+    FixupArgs fx;
+    fx.plan = pl;
+    fx.gsum = ba.gsum;
+    fx.E = ba.Fbuf;
+    fx.M = ba.Rbuf;
+    fx.out = ba.dSend;
+    fx.H = L.H;
+    fx.D = L.D;
+    fx.Lseg = L.Lseg;
+    fx.flags = s->flags;
+    fx.reverse = 1;
+    PROF("fixup_bwd");
+    CK(launch_fixup(fx, L.N, st));
+  }
+  ba.pass = 1;
+  {
+    PROF("bwd_chain");
+    CK(launch_bwd_chain(ba, bf, L.D, dim3(L.S_max, L.H, 1), st));
+  }
+  // 3. local gradients, every (chunk, head) in parallel
+  {
+    PROF("bwd_local");
+    CK(launch_bwd_local(ba, bf, L.D, L.CH_max, st));
+  }
+  return GDN_OK;
+}
+
+int gdn_get_device_status(const gdn_shape *shape, const void *workspace, gdn_stream_t stream) {
+  (void)shape;
+  if (!workspace) return -1;
+  int v = 0;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&v, workspace, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess) return -1;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return -1;
+  return v;
+}
+
+int gdn_plan_query(const gdn_shape *shape, int *seg_chunks, int *max_segments, int *max_chunks) {
+  Layout L;
+  int rc = make_layout(shape, L);
+  if (rc) return rc;
+  if (seg_chunks) *seg_chunks = L.Lseg;
+  if (max_segments) *max_segments = L.S_max;
+  if (max_chunks) *max_chunks = L.CH_max;
+  return GDN_OK;
+}
+
+int gdn_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (on && g_prof.pool.empty()) {
+    g_prof.pool.resize(8192);
+    for (auto &e : g_prof.pool)
+      if (cudaEventCreate(&e) != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaEventCreate failed");
+  }
+  if (!on) prof_drain_locked();
+  g_prof.on = on != 0;
+  return GDN_OK;
+}
+
+int gdn_profile_report(char *buf, size_t len, int reset) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  prof_drain_locked();
+  std::string out;
+  char line[256];
+  for (size_t i = 0; i < g_prof.names.size(); ++i) {
+    snprintf(line, sizeof line, "%s %ld %.6f\n", g_prof.names[i].c_str(), g_prof.count[i], g_prof.total_ms[i]);
+    out += line;
+  }
+  if (reset) {
+    g_prof.names.clear();
+    g_prof.total_ms.clear();
+    g_prof.count.clear();
+  }
+  if (buf && len) {
+    const size_t n = std::min(len - 1, out.size());
+    memcpy(buf, out.data(), n);
+    buf[n] = 0;
+  }
+  return (int)out.size();
+}
+
+const char *gdn_status_string(int status) {
+  switch (status) {
+    case GDN_OK: return "ok";
+    case GDN_ERR_INVALID_ARG: return "invalid argument";
+    case GDN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case GDN_ERR_WORKSPACE: return "workspace missing or too small";
+    case GDN_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+const char *gdn_last_error_string(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

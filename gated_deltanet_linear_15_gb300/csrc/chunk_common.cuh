@@ -1,0 +1,156 @@
+// Per-chunk building blocks shared by the forward and backward chunk kernels:
+// tile loads, in-kernel L2 normalisation, gate prefix sums, and the unit
+// lower-triangular inverse of the WY stage.
+#pragma once
+#include "common.cuh"
+
+namespace gdn {
+
+// Load a CH x D tile of a [tokens, H, D] tensor: row r = token tok0 + r of head h,
+// rows r >= nvalid are zero-filled.
+template <typename E, int D>
+__device__ __forceinline__ void load_tile(E *dst, int ld, const E *base, int H, int h, long tok0, int nvalid) {
+  constexpr int EPV = 16 / sizeof(E);  // elements per 16-byte piece
+  constexpr int VPR = D / EPV;
+  for (int e = threadIdx.x; e < CH * VPR; e += NTHREADS) {
+    const int r = e / VPR, cidx = e % VPR;
+    const bool valid = r < nvalid;
+    const E *src = base + ((size_t)(tok0 + (valid ? r : 0)) * H + h) * D + cidx * EPV;
+    cp_async16(dst + r * ld + cidx * EPV, src, valid);
+  }
+}
+
+// Load CH scalars x[(tok0 + r) * H + h] (zero for r >= nvalid) into dst[0..CH).
+__device__ __forceinline__ void load_scalars(float *dst, const float *base, int H, int h, long tok0, int nvalid,
+                                             int thread0) {
+  const int r = threadIdx.x - thread0;
+  if (r >= 0 && r < CH) {
+    const bool valid = r < nvalid;
+    cp_async4(dst + r, base + (size_t)(tok0 + (valid ? r : 0)) * H + h, valid);
+  }
+}
+
+// In-place row normalisation x <- x * mul / sqrt(sum x^2 + 1e-6), one warp per row.
+// Optionally records the norm used per row.
+template <typename E, int D>
+__device__ __forceinline__ void l2norm_rows(E *t, int ld, float mul, float *norm_out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int r = warp; r < CH; r += NWARPS) {
+    float ss = 0.f;
+#pragma unroll
+    for (int c = lane; c < D; c += 32) {
+      const float x = tof(t[r * ld + c]);
+      ss += x * x;
+    }
+    ss = warp_sum(ss);
+    const float nrm = sqrtf(ss + 1e-6f);
+    const float f = mul / nrm;
+#pragma unroll
+    for (int c = lane; c < D; c += 32) t[r * ld + c] = fromf<E>(tof(t[r * ld + c]) * f);
+    if (norm_out && lane == 0) norm_out[r] = nrm;
+  }
+}
+
+// Gate quantities of one chunk from the raw log-gates g[0..CH) (one warp).
+//   G_r   = sum_{i<=r} g_i                 (in-chunk inclusive prefix)
+//   gam_r = exp(G_r)                       (decay from the chunk start)
+//   gp_r  = exp(G_r - G_mid), rgp_r = exp(G_mid - G_r)   (gamma factoring, centred)
+//   cdec_r = exp(G_last - G_r)             (decay from token r to the chunk end)
+// Each exponential is taken once per token (onedev.kr FlashQLA talk summary,
+// paragraph on SFU load: the diagonal scaling is pulled out of the inverse).
+// Returns true in lane 0 if |G_r - G_mid| exceeds the factoring range.
+struct Gates {
+  float G[CH], gam[CH], gp[CH], rgp[CH], cdec[CH];
+  float gamC;  // exp(G_last)
+};
+
+__device__ __forceinline__ bool gate_prefix(const float *g, Gates &gt) {
+  const int lane = threadIdx.x & 31;
+  float a = g[lane], b = g[lane + 32];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float ya = __shfl_up_sync(0xffffffffu, a, o);
+    const float yb = __shfl_up_sync(0xffffffffu, b, o);
+    if (lane >= o) {
+      a += ya;
+      b += yb;
+    }
+  }
+  const float Gmid = __shfl_sync(0xffffffffu, a, 31);
+  b += Gmid;
+  const float Glast = __shfl_sync(0xffffffffu, b, 31);
+  gt.G[lane] = a;
+  gt.G[lane + 32] = b;
+  gt.gam[lane] = expf(a);
+  gt.gam[lane + 32] = expf(b);
+  gt.gp[lane] = expf(a - Gmid);
+  gt.gp[lane + 32] = expf(b - Gmid);
+  gt.rgp[lane] = expf(Gmid - a);
+  gt.rgp[lane + 32] = expf(Gmid - b);
+  gt.cdec[lane] = expf(Glast - a);
+  gt.cdec[lane + 32] = expf(Glast - b);
+  if (lane == 0) gt.gamC = expf(Glast);
+  float rng = fmaxf(fabsf(a - Gmid), fabsf(b - Gmid));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) rng = fmaxf(rng, __shfl_xor_sync(0xffffffffu, rng, o));
+  return rng > FACTOR_RANGE;
+}
+
+// Inverse of the unit lower-triangular T = I + diag(beta) N, N = strict_tril(K K^T),
+// in fp32.  `nf` (CH x ldn floats) holds N in its strictly lower triangle on entry;
+// on exit its strictly upper triangle holds Ahat^T (Ahat[r][i] at nf[i][r], i < r);
+// the lower triangle is left intact.  Diagonal 16x16 blocks are inverted by
+// forward substitution (one column per lane), then the off-diagonal blocks
+// follow by distance: Ahat_IJ = -Ahat_II sum_{K=J}^{I-1} T_IK Ahat_KJ.
+// `ys` is 768 floats of scratch.  Ends with __syncthreads().
+__device__ __forceinline__ float ahat_at(const float *nf, int ldn, int a, int b) {
+  return a == b ? 1.f : (a > b ? nf[b * ldn + a] : 0.f);
+}
+
+static __device__ __noinline__ void tril_inverse(float *nf, int ldn, const float *beta, float *ys) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp < 4 && lane < 16) {
+    const int b = warp * 16, jj = lane;
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float acc = (r == jj) ? 1.f : 0.f;
+      const float br = beta[b + r];
+#pragma unroll
+      for (int i = 0; i < r; ++i) acc -= br * nf[(b + r) * ldn + b + i] * x[i];
+      x[r] = acc;
+    }
+#pragma unroll
+    for (int r = 1; r < 16; ++r)
+      if (r > jj) nf[(b + jj) * ldn + b + r] = x[r];
+  }
+  __syncthreads();
+  for (int d = 1; d <= 3; ++d) {
+    const int nb = 4 - d;
+    for (int e = threadIdx.x; e < nb * 256; e += NTHREADS) {
+      const int bi = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+      const int I = d + bi, J = I - d;
+      const int row = 16 * I + r, col = 16 * J + cc;
+      const float br = beta[row];
+      float acc = 0.f;
+      for (int kb = J; kb < I; ++kb) {
+#pragma unroll
+        for (int t = 0; t < 16; ++t) acc += nf[row * ldn + 16 * kb + t] * ahat_at(nf, ldn, 16 * kb + t, col);
+      }
+      ys[e] = br * acc;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < nb * 256; e += NTHREADS) {
+      const int bi = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+      const int I = d + bi, J = I - d;
+      float acc = 0.f;
+#pragma unroll
+      for (int t = 0; t < 16; ++t)
+        if (t <= r) acc += ahat_at(nf, ldn, 16 * I + r, 16 * I + t) * ys[(bi << 8) + (t << 4) + cc];
+      nf[(16 * J + cc) * ldn + 16 * I + r] = -acc;
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace gdn

@@ -1,0 +1,306 @@
+// Fused chunked forward of the gated delta rule over one segment of one
+// (sequence, head): WY stage, chunk-to-chunk state pass and output in one
+// kernel, so W, U, the corrected values and the per-chunk state never reach
+// HBM (onedev.kr FlashQLA talk summary, paragraph on the WY representation:
+// four steps, of which FLA writes W, U, S to HBM between operators).
+//
+// Per chunk (C = 64 tokens, S is d_v x d_k, G = in-chunk prefix of g):
+//   N    = strict_tril(K K^T);  Ahat = (I + diag(beta) N)^{-1}      (fp32)
+//   W    = diag(gam) Ahat diag(beta) K;   U = diag(gp) Ahat diag(beta rgp) V
+//   Ut   = U - W S0^T                                    (corrected values)
+//   O    = diag(gam) Q S0^T + P Ut,  P = diag(gp) tril_incl(Q K^T) diag(rgp)
+//   S_C  = gam_C S0 + Ut^T diag(cdec) K
+// The state lives in fp32 registers for the whole segment; its bf16 copy in
+// shared memory is the MMA operand of the next chunk.
+//
+// Passes (one CTA per (segment, head[, role])):
+//   pass A: segments whose successor needs a corrected start: run from the
+//           segment's own start (initial state, warm-up, or zero) and store the
+//           end state E; role 1 runs the same recurrence with v = 0 from I to
+//           give the d_k x d_k transition M (onedev.kr talk summary, paragraph
+//           on parallelism: zero-state recursion plus one d_k x d_k correction).
+//   pass B: every segment from its exact start, writing O (and S_T).
+//   pass S: as pass B but writing the bf16 state at every chunk start instead
+//           of O (input of the backward).
+#include "chunk_common.cuh"
+#include "kernels.h"
+
+namespace gdn {
+
+template <typename E, int D> struct FwdSmem {
+  static constexpr int LD = D + Pad<E>::v;
+  static constexpr int LC = CH + Pad<E>::v;
+  static constexpr int LN = CH + 4;
+  E q[CH * LD], k[CH * LD], v[CH * LD], kt[CH * LD], w[CH * LD], ut[CH * LD];
+  E s[D * LD];
+  E p[CH * LC], x1[CH * LC], x2[CH * LC];
+  float nf[CH * LN];
+  float g[CH], beta[CH];
+  Gates gt;
+  float ys[768];
+};
+
+template <typename E, int D>
+__global__ void __launch_bounds__(NTHREADS, 1) fwd_chunk_kernel(FwdArgs a) {
+  using SM = FwdSmem<E, D>;
+  constexpr int LD = SM::LD, LC = SM::LC, LN = SM::LN;
+  constexpr int SWM = D / 4, SWN = D / 2;  // state / output warp tile
+  extern __shared__ __align__(128) unsigned char smraw[];
+  SM &sm = *reinterpret_cast<SM *>(smraw);
+
+  const int s = blockIdx.x, h = blockIdx.y, role = blockIdx.z;
+  const int H = a.H;
+  const int n = a.plan.seg_seq[s];
+  if (n < 0) return;
+  const int j = s - a.plan.seq_seg0[n], nseg = a.plan.seq_nseg[n];
+  const int len = a.plan.seq_len[n], chunk0 = a.plan.seq_chunk0[n];
+  const long bos = a.plan.seq_bos[n];
+  const int nchunks = (len + CH - 1) / CH;
+  const int cbeg = j * a.Lseg, cend = min(cbeg + a.Lseg, nchunks);
+  const bool window = !(a.flags & kFlagWindowOff);
+  int w = 0;
+  const int mode = fwd_start_mode(a.gsum, H, h, chunk0, cbeg, j, window, &w);
+  bool transition = false;
+  if (a.pass == 0) {
+    if (j >= nseg - 1) return;
+    int w2;
+    if (fwd_start_mode(a.gsum, H, h, chunk0, cend, j + 1, window, &w2) != START_FIXUP) return;
+    if (role == 1) {
+      if (mode != START_FIXUP) return;
+      transition = true;
+    }
+  } else if (role != 0) {
+    return;
+  }
+  const bool outputs = (a.pass == 1);
+  const bool states = (a.pass == 2);
+  const bool need_v = !transition;
+  const bool l2 = (a.flags & kFlagL2Norm) != 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wr = warp >> 1, wc = warp & 1;
+
+  const E *qg = static_cast<const E *>(a.q);
+  const E *kg = static_cast<const E *>(a.k);
+  const E *vg = static_cast<const E *>(a.v);
+  const size_t DD = (size_t)D * D;
+  const size_t sh_idx = (size_t)s * H + h;
+
+  int cfirst = cbeg;
+  if (mode == START_WARMUP && !transition) cfirst = cbeg - w;
+
+  auto issue_loads = [&](int c) {
+    const long tok0 = bos + (long)c * CH;
+    const int nvalid = min(CH, len - c * CH);
+    load_tile<E, D>(sm.k, LD, kg, H, h, tok0, nvalid);
+    if (need_v) load_tile<E, D>(sm.v, LD, vg, H, h, tok0, nvalid);
+    if (outputs && c >= cbeg) load_tile<E, D>(sm.q, LD, qg, H, h, tok0, nvalid);
+    load_scalars(sm.g, a.g, H, h, tok0, nvalid, 0);
+    load_scalars(sm.beta, a.beta, H, h, tok0, nvalid, 64);
+    cp_async_commit();
+  };
+
+  issue_loads(cfirst);
+
+  // ---- initial state into registers (fp32) and its E copy
+  Acc<SWM, SWN> Sacc;
+  {
+    const float *src = nullptr;
+    if (transition) {
+      src = nullptr;
+    } else if (mode == START_INIT) {
+      src = a.S0 ? a.S0 + ((size_t)n * H + h) * DD : nullptr;
+    } else if (mode == START_FIXUP && a.pass != 0) {
+      src = a.Sstart + sh_idx * DD;
+    }
+    const int m0 = wr * SWM, n0 = wc * SWN;
+    Sacc.pairs([&](int r, int c, float &v0, float &v1) {
+      const int row = m0 + r, col = n0 + c;
+      if (src) {
+        const float2 t = *reinterpret_cast<const float2 *>(src + (size_t)row * D + col);
+        v0 = t.x;
+        v1 = t.y;
+      } else if (transition) {
+        v0 = (row == col) ? 1.f : 0.f;
+        v1 = (row == col + 1) ? 1.f : 0.f;
+      } else {
+        v0 = v1 = 0.f;
+      }
+      st2(&sm.s[row * LD + col], v0, v1);
+    });
+  }
+
+  Acc<32, SWN> X;  // U / Ut (warps 0-3) or the output (warps 4-7)
+
+  for (int c = cfirst; c < cend; ++c) {
+    const bool emit = outputs && c >= cbeg;
+    const long tok0 = bos + (long)c * CH;
+    const int nvalid = min(CH, len - c * CH);
+    cp_async_wait_all();
+    __syncthreads();  // tiles of chunk c landed; state copy of S0 complete
+
+    if (states && c >= cbeg) {
+      // bf16/fp32 copy of the state at the chunk start, for the backward
+      E *dst = static_cast<E *>(a.states) + ((size_t)(chunk0 + c) * H + h) * DD;
+      constexpr int EPV = 16 / sizeof(E);
+      for (int e = threadIdx.x; e < D * D / EPV; e += NTHREADS) {
+        const int r = e / (D / EPV), cc = (e % (D / EPV)) * EPV;
+        *reinterpret_cast<uint4 *>(dst + (size_t)r * D + cc) = *reinterpret_cast<const uint4 *>(&sm.s[r * LD + cc]);
+      }
+    }
+    if (l2) {
+      l2norm_rows<E, D>(sm.k, LD, 1.f, nullptr);
+      if (emit) l2norm_rows<E, D>(sm.q, LD, a.scale, nullptr);
+    } else if (emit && a.scale != 1.f) {
+      for (int e = threadIdx.x; e < CH * D; e += NTHREADS) {
+        const int r = e / D, cc = e % D;
+        sm.q[r * LD + cc] = fromf<E>(tof(sm.q[r * LD + cc]) * a.scale);
+      }
+    }
+    if (warp == 0) {
+      if (gate_prefix(sm.g, sm.gt) && lane == 0 && a.status) atomicOr(a.status, 1);
+    }
+    __syncthreads();
+
+    // ---- K~ = diag(cdec) K, and [K; Q] K^T  ->  N (fp32) and P (E)
+    for (int e = threadIdx.x; e < CH * D; e += NTHREADS) {
+      const int r = e / D, cc = e % D;
+      sm.kt[r * LD + cc] = fromf<E>(tof(sm.k[r * LD + cc]) * sm.gt.cdec[r]);
+    }
+    if (warp < 4 || emit) {
+      Acc<32, 32> acc;
+      acc.zero();
+      const E *A = (warp < 4) ? sm.k : sm.q;
+      const int m0 = (wr & 1) * 32, n0 = wc * 32;
+      warp_mma<32, 32, false, false>(acc, A, LD, sm.k, LD, m0, n0, D);
+      if (warp < 4) {
+        acc.each([&](int r, int cc, float &v) {
+          const int row = m0 + r, col = n0 + cc;
+          if (col < row) sm.nf[row * LN + col] = v;
+        });
+      } else {
+        acc.each([&](int r, int cc, float &v) {
+          const int row = m0 + r, col = n0 + cc;
+          sm.p[row * LC + col] = fromf<E>(col <= row ? v * sm.gt.gp[row] * sm.gt.rgp[col] : 0.f);
+        });
+      }
+    }
+    __syncthreads();
+
+    tril_inverse(sm.nf, LN, sm.beta, sm.ys);
+
+    // ---- X1 = Ahat diag(beta), X2 = Ahat diag(beta * rgp)
+    for (int e = threadIdx.x; e < CH * CH; e += NTHREADS) {
+      const int r = e / CH, i = e % CH;
+      const float ah = ahat_at(sm.nf, LN, r, i);
+      const float b = sm.beta[i];
+      sm.x1[r * LC + i] = fromf<E>(ah * b);
+      sm.x2[r * LC + i] = fromf<E>(ah * b * sm.gt.rgp[i]);
+    }
+    __syncthreads();
+
+    // ---- U (warps 0-3, registers) and -W (warps 4-7, shared)
+    {
+      const int ww = warp & 3;
+      const int m0 = (ww >> 1) * 32, n0 = (ww & 1) * SWN;
+      if (warp < 4) {
+        X.zero();
+        if (need_v) {
+          warp_mma<32, SWN, false, true>(X, sm.x2, LC, sm.v, LD, m0, n0, CH);
+          X.each([&](int r, int cc, float &v) { v *= sm.gt.gp[m0 + r]; });
+        }
+      } else {
+        Acc<32, SWN> acc;
+        acc.zero();
+        warp_mma<32, SWN, false, true>(acc, sm.x1, LC, sm.k, LD, m0, n0, CH);
+        acc.pairs([&](int r, int cc, float &v0, float &v1) {
+          const float gm = -sm.gt.gam[m0 + r];
+          st2(&sm.w[(m0 + r) * LD + n0 + cc], v0 * gm, v1 * gm);
+        });
+      }
+    }
+    __syncthreads();
+
+    // ---- Ut = U + (-W) S0^T (warps 0-3);  O1 = Q S0^T (warps 4-7)
+    {
+      const int ww = warp & 3;
+      const int m0 = (ww >> 1) * 32, n0 = (ww & 1) * SWN;
+      if (warp < 4) {
+        warp_mma<32, SWN, false, false>(X, sm.w, LD, sm.s, LD, m0, n0, D);
+      } else if (emit) {
+        X.zero();
+        warp_mma<32, SWN, false, false>(X, sm.q, LD, sm.s, LD, m0, n0, D);
+      }
+    }
+    __syncthreads();
+
+    if (c + 1 < cend) issue_loads(c + 1);  // Q, K, V, g, beta are free now
+
+    if (warp < 4) {
+      const int m0 = (warp >> 1) * 32, n0 = (warp & 1) * SWN;
+      X.pairs([&](int r, int cc, float &v0, float &v1) { st2(&sm.ut[(m0 + r) * LD + n0 + cc], v0, v1); });
+    }
+    __syncthreads();
+
+    // ---- S_C = gam_C S0 + Ut^T K~ (all warps);  O = diag(gam) O1 + P Ut (warps 4-7)
+    {
+      const float gC = sm.gt.gamC;
+      Sacc.each([&](int r, int cc, float &v) { v *= gC; });
+      warp_mma<SWM, SWN, true, true>(Sacc, sm.ut, LD, sm.kt, LD, wr * SWM, wc * SWN, CH);
+      if (warp >= 4 && emit) {
+        const int ww = warp & 3;
+        const int m0 = (ww >> 1) * 32, n0 = (ww & 1) * SWN;
+        X.each([&](int r, int cc, float &v) { v *= sm.gt.gam[m0 + r]; });
+        warp_mma<32, SWN, false, true>(X, sm.p, LC, sm.ut, LD, m0, n0, CH);
+        X.pairs([&](int r, int cc, float &v0, float &v1) { st2(&sm.w[(m0 + r) * LD + n0 + cc], v0, v1); });
+      }
+    }
+    __syncthreads();
+
+    // ---- state copy for the next chunk, output rows to HBM
+    Sacc.pairs([&](int r, int cc, float &v0, float &v1) { st2(&sm.s[(wr * SWM + r) * LD + wc * SWN + cc], v0, v1); });
+    if (emit) {
+      E *og = static_cast<E *>(a.o);
+      constexpr int EPV = 16 / sizeof(E);
+      constexpr int VPR = D / EPV;
+      for (int e = threadIdx.x; e < CH * VPR; e += NTHREADS) {
+        const int r = e / VPR, cc = (e % VPR) * EPV;
+        if (r < nvalid)
+          *reinterpret_cast<uint4 *>(og + ((size_t)(tok0 + r) * H + h) * D + cc) =
+              *reinterpret_cast<const uint4 *>(&sm.w[r * LD + cc]);
+      }
+    }
+  }
+
+  // ---- end-of-segment state
+  float *dst = nullptr;
+  if (a.pass == 0) {
+    dst = (transition ? a.Mbuf : a.Ebuf) + sh_idx * DD;
+  } else if (j == nseg - 1 && a.ST) {
+    dst = a.ST + ((size_t)n * H + h) * DD;
+  }
+  if (dst) {
+    const int m0 = wr * SWM, n0 = wc * SWN;
+    Sacc.pairs([&](int r, int cc, float &v0, float &v1) {
+      *reinterpret_cast<float2 *>(dst + (size_t)(m0 + r) * D + n0 + cc) = make_float2(v0, v1);
+    });
+  }
+}
+
+template <typename E, int D> static int launch_fwd(const FwdArgs &a, dim3 grid, cudaStream_t st) {
+  const size_t smem = sizeof(FwdSmem<E, D>);
+  static_assert(sizeof(FwdSmem<E, D>) <= 232448, "shared memory budget");
+  auto kern = fwd_chunk_kernel<E, D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return (int)e;
+  kern<<<grid, NTHREADS, smem, st>>>(a);
+  return (int)cudaGetLastError();
+}
+
+int launch_fwd_chunk(const FwdArgs &a, bool is_bf16, int D, dim3 grid, cudaStream_t st) {
+  if (is_bf16 && D == 128) return launch_fwd<bf16, 128>(a, grid, st);
+  if (is_bf16 && D == 64) return launch_fwd<bf16, 64>(a, grid, st);
+  if (!is_bf16 && D == 64) return launch_fwd<float, 64>(a, grid, st);
+  return -1;
+}
+
+}  // namespace gdn

@@ -1,0 +1,65 @@
+// Host-visible launch descriptors of the chunk kernels (internal to the library).
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "common.cuh"
+
+namespace gdn {
+
+constexpr unsigned kFlagL2Norm = 1u;
+constexpr unsigned kFlagSpOff = 2u;
+constexpr unsigned kFlagWindowOff = 4u;
+
+struct FwdArgs {
+  const void *q, *k, *v;
+  const float *g, *beta, *S0;
+  void *o;
+  float *ST;
+  Plan plan;
+  const float *gsum;  // [CH_max, H] per-chunk sum of g
+  int *status;
+  float *Ebuf, *Mbuf, *Sstart;  // [S_max, H, D, D]
+  void *states;                 // [CH_max, H, D, D] element type of q
+  int H, Lseg;
+  float scale;
+  unsigned flags;
+  int pass;  // 0: segment end states / transitions, 1: outputs, 2: per-chunk states
+};
+
+struct BwdArgs {
+  const void *q, *k, *v, *dO;
+  const float *g, *beta, *dST;
+  void *dq, *dk, *dv;
+  float *dg, *dbeta, *dS0;
+  Plan plan;
+  const float *gsum;
+  int *status;
+  float *Fbuf, *Rbuf, *dSend;  // [S_max, H, D, D]
+  const void *states;          // [CH_max, H, D, D] forward state at each chunk start
+  void *dstates;               // [CH_max, H, D, D] dS at each chunk end
+  int H, Lseg;
+  float scale;
+  unsigned flags;
+  int pass;  // reverse chain: 0 segment starts / transitions, 1 per-chunk dS
+};
+
+struct FixupArgs {
+  Plan plan;
+  const float *gsum;
+  const float *E, *M;  // end states / transitions per (segment, head)
+  float *out;          // corrected start (forward) or end (reverse) states
+  int H, D, Lseg;
+  unsigned flags;
+  int reverse;
+};
+
+int launch_plan(const Plan &p, const int *cu, int N, int T, int Lseg, int S_max, int CH_max, int *status,
+                cudaStream_t st);
+int launch_gate_scan(const Plan &p, const float *g, int H, int CH_max, float *gsum, int *status, cudaStream_t st);
+int launch_fixup(const FixupArgs &a, int N, cudaStream_t st);
+int launch_fwd_chunk(const FwdArgs &a, bool is_bf16, int D, dim3 grid, cudaStream_t st);
+int launch_bwd_chain(const BwdArgs &a, bool is_bf16, int D, dim3 grid, cudaStream_t st);
+int launch_bwd_local(const BwdArgs &a, bool is_bf16, int D, int CH_max, cudaStream_t st);
+
+}  // namespace gdn

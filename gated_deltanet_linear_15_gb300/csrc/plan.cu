@@ -1,0 +1,247 @@
+// Segment plan, gate scan and the sequential start-state fix-up.
+//
+// Gate scan: "one light kernel scanning the gate distribution" decides which
+// segment starts lie inside an effective sliding window (onedev.kr FlashQLA
+// talk summary, paragraph on the effective sliding window).  Here it stores
+// the log-decay sum of every (chunk, head); the chunk kernels derive from it
+// the warm-up length of each segment start: the smallest w <= 8 chunks whose
+// summed log-decay is <= ln(2^-24).  Because |I - beta k k^T|_2 <= 1 for unit
+// keys and beta in [0, 1], starting w chunks early from a zero state leaves a
+// start-state error below 2^-24 |S|, so that segment needs no correction.
+//
+// Fix-up: segments that are not inside a window get their exact start state
+// from the composition S_start(j+1) = S_start(j) M_j + E_j over the segments of
+// the sequence (onedev.kr talk summary, paragraph on parallelism).  Rows of the
+// state are independent in this composition, so CTAs split the rows.
+#include "kernels.h"
+
+namespace gdn {
+
+// One block.  Builds the per-sequence and per-segment tables; a malformed
+// cu_seqlens (not starting at 0, decreasing, or not ending at T) sets status
+// bit 1 and leaves every sequence empty, so the chunk kernels do nothing.
+__global__ void plan_kernel(Plan p, const int *cu, int N, int T, int Lseg, int S_max, int CH_max, int *status) {
+  __shared__ int carry_c, carry_s, bad;
+  __shared__ int wsum_c[32], wsum_s[32];
+  const int tid = threadIdx.x, nt = blockDim.x;
+  if (tid == 0) {
+    carry_c = 0;
+    carry_s = 0;
+    bad = 0;
+    if (cu && (cu[0] != 0 || cu[N] != T)) bad = 1;
+  }
+  __syncthreads();
+  if (cu) {
+    for (int n = tid; n < N; n += nt)
+      if (cu[n + 1] < cu[n]) atomicOr(&bad, 1);
+  }
+  __syncthreads();
+  const bool isbad = bad != 0;
+  if (isbad && tid == 0 && status) atomicOr(status, 2);
+  for (int base = 0; base < N; base += nt) {
+    const int n = base + tid;
+    int len = 0, bos = 0;
+    if (n < N && !isbad) {
+      bos = cu ? cu[n] : n * T;
+      len = cu ? cu[n + 1] - cu[n] : T;
+    }
+    const int nc = (len + CH - 1) / CH;
+    // an empty sequence still gets one (chunk-less) segment: it passes S0 to S_T
+    const int ns = (n < N && !isbad) ? max(1, (nc + Lseg - 1) / Lseg) : 0;
+    // block-wide exclusive scans of nc and ns
+    const int lane = tid & 31, warp = tid >> 5;
+    int ic = nc, is = ns;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int yc = __shfl_up_sync(0xffffffffu, ic, o), ys = __shfl_up_sync(0xffffffffu, is, o);
+      if (lane >= o) {
+        ic += yc;
+        is += ys;
+      }
+    }
+    if (lane == 31) {
+      wsum_c[warp] = ic;
+      wsum_s[warp] = is;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const int nw = nt / 32;
+      int vc = lane < nw ? wsum_c[lane] : 0, vs = lane < nw ? wsum_s[lane] : 0;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int yc = __shfl_up_sync(0xffffffffu, vc, o), ys = __shfl_up_sync(0xffffffffu, vs, o);
+        if (lane >= o) {
+          vc += yc;
+          vs += ys;
+        }
+      }
+      if (lane < nw) {
+        wsum_c[lane] = vc;
+        wsum_s[lane] = vs;
+      }
+    }
+    __syncthreads();
+    const int pre_c = carry_c + (warp ? wsum_c[warp - 1] : 0) + ic - nc;
+    const int pre_s = carry_s + (warp ? wsum_s[warp - 1] : 0) + is - ns;
+    if (n < N) {
+      p.seq_bos[n] = bos;
+      p.seq_len[n] = len;
+      p.seq_chunk0[n] = pre_c;
+      p.seq_seg0[n] = pre_s;
+      p.seq_nseg[n] = ns;
+    }
+    __syncthreads();
+    if (tid == nt - 1) {
+      carry_c = pre_c + nc;
+      carry_s = pre_s + ns;
+    }
+    __syncthreads();
+  }
+  const int tot_c = carry_c, tot_s = carry_s;
+  if (tid == 0) {
+    p.totals[0] = tot_c;
+    p.totals[1] = tot_s;
+    if ((tot_c > CH_max || tot_s > S_max) && status) atomicOr(status, 2);
+  }
+  // owner sequence of every chunk and segment: the last sequence whose prefix is
+  // <= the index (an empty sequence shares its prefix with the next one, so the
+  // search never lands on it for an index below the total)
+  for (int c = tid; c < CH_max; c += nt) {
+    int owner = -1;
+    if (c < tot_c && tot_c <= CH_max) {
+      int lo = 0, hi = N - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.seq_chunk0[mid] <= c) lo = mid; else hi = mid - 1;
+      }
+      owner = lo;
+    }
+    p.chunk_seq[c] = owner;
+  }
+  for (int s = tid; s < S_max; s += nt) {
+    int owner = -1;
+    if (s < tot_s && tot_s <= S_max) {
+      int lo = 0, hi = N - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.seq_seg0[mid] <= s) lo = mid; else hi = mid - 1;
+      }
+      owner = lo;
+    }
+    p.seg_seq[s] = owner;
+  }
+}
+
+int launch_plan(const Plan &p, const int *cu, int N, int T, int Lseg, int S_max, int CH_max, int *status,
+                cudaStream_t st) {
+  plan_kernel<<<1, 1024, 0, st>>>(p, cu, N, T, Lseg, S_max, CH_max, status);
+  return (int)cudaGetLastError();
+}
+
+// One block per global chunk, one warp per head (looping): gsum[c, h] = sum of g
+// over the chunk's tokens; status bit 0 if the centred in-chunk prefix leaves
+// the range of the gamma factoring.
+__global__ void gate_scan_kernel(Plan p, const float *g, int H, float *gsum, int *status) {
+  const int c = blockIdx.x;
+  const int n = p.chunk_seq[c];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (n < 0) {
+    for (int h = threadIdx.x; h < H; h += blockDim.x) gsum[(size_t)c * H + h] = 0.f;
+    return;
+  }
+  const int lc = c - p.seq_chunk0[n];
+  const long tok0 = (long)p.seq_bos[n] + (long)lc * CH;
+  const int nvalid = min(CH, p.seq_len[n] - lc * CH);
+  for (int h = warp; h < H; h += blockDim.x / 32) {
+    float a = lane < nvalid ? g[(size_t)(tok0 + lane) * H + h] : 0.f;
+    float b = lane + 32 < nvalid ? g[(size_t)(tok0 + lane + 32) * H + h] : 0.f;
+    for (int o = 1; o < 32; o <<= 1) {
+      const float ya = __shfl_up_sync(0xffffffffu, a, o), yb = __shfl_up_sync(0xffffffffu, b, o);
+      if (lane >= o) {
+        a += ya;
+        b += yb;
+      }
+    }
+    const float Gmid = __shfl_sync(0xffffffffu, a, 31);
+    b += Gmid;
+    const float Glast = __shfl_sync(0xffffffffu, b, 31);
+    float rng = fmaxf(fabsf(a - Gmid), fabsf(b - Gmid));
+    for (int o = 16; o > 0; o >>= 1) rng = fmaxf(rng, __shfl_xor_sync(0xffffffffu, rng, o));
+    if (lane == 0) {
+      gsum[(size_t)c * H + h] = Glast;
+      if (rng > FACTOR_RANGE && status) atomicOr(status, 1);
+    }
+  }
+}
+
+int launch_gate_scan(const Plan &p, const float *g, int H, int CH_max, float *gsum, int *status, cudaStream_t st) {
+  if (CH_max == 0) return 0;
+  gate_scan_kernel<<<CH_max, 256, 0, st>>>(p, g, H, gsum, status);
+  return (int)cudaGetLastError();
+}
+
+// grid (D / FIX_ROWS, H, N); FIX_ROWS rows of the state per CTA, 256 threads.
+constexpr int FIX_ROWS = 8;
+
+template <int D>
+__global__ void __launch_bounds__(256) fixup_kernel(FixupArgs a) {
+  __shared__ float cur[FIX_ROWS][D];
+  const int rb = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+  const int H = a.H;
+  const int nseg = a.plan.seq_nseg[n];
+  if (nseg <= 1) return;
+  const int seg0 = a.plan.seq_seg0[n], chunk0 = a.plan.seq_chunk0[n];
+  const int nchunks = (a.plan.seq_len[n] + CH - 1) / CH;
+  const bool window = !(a.flags & kFlagWindowOff);
+  const size_t DD = (size_t)D * D;
+  constexpr int CPT = D / 32;  // columns per thread
+  const int r = threadIdx.x >> 5;
+  const int c0 = (threadIdx.x & 31) * CPT;
+  const int row = rb * FIX_ROWS + r;
+  for (int step = 0; step < nseg - 1; ++step) {
+    int jt, js, mt, ms, w;
+    if (!a.reverse) {
+      jt = step + 1;
+      js = jt - 1;
+      mt = fwd_start_mode(a.gsum, H, h, chunk0, jt * a.Lseg, jt, window, &w);
+      if (mt != START_FIXUP) continue;
+      ms = fwd_start_mode(a.gsum, H, h, chunk0, js * a.Lseg, js, window, &w);
+    } else {
+      jt = nseg - 2 - step;
+      js = jt + 1;
+      mt = bwd_start_mode(a.gsum, H, h, chunk0, min((jt + 1) * a.Lseg, nchunks), nchunks, jt, nseg, window, &w);
+      if (mt != START_FIXUP) continue;
+      ms = bwd_start_mode(a.gsum, H, h, chunk0, min((js + 1) * a.Lseg, nchunks), nchunks, js, nseg, window, &w);
+    }
+    const size_t src = ((size_t)(seg0 + js) * H + h) * DD;
+    float acc[CPT];
+#pragma unroll
+    for (int t = 0; t < CPT; ++t) acc[t] = a.E[src + (size_t)row * D + c0 + t];
+    if (ms == START_FIXUP) {
+      // cur holds the corrected state of segment js (computed in the previous step)
+      const float *M = a.M + src;
+      for (int k = 0; k < D; ++k) {
+        const float x = cur[r][k];
+#pragma unroll
+        for (int t = 0; t < CPT; ++t) acc[t] = fmaf(x, M[(size_t)k * D + c0 + t], acc[t]);
+      }
+    }
+    __syncthreads();
+    float *out = a.out + ((size_t)(seg0 + jt) * H + h) * DD + (size_t)row * D;
+#pragma unroll
+    for (int t = 0; t < CPT; ++t) {
+      cur[r][c0 + t] = acc[t];
+      out[c0 + t] = acc[t];
+    }
+    __syncthreads();
+  }
+}
+
+int launch_fixup(const FixupArgs &a, int N, cudaStream_t st) {
+  if (N == 0) return 0;
+  dim3 grid(a.D / FIX_ROWS, a.H, N);
+  if (a.D == 128) fixup_kernel<128><<<grid, 256, 0, st>>>(a);
+  else if (a.D == 64) fixup_kernel<64><<<grid, 256, 0, st>>>(a);
+  else return -1;
+  return (int)cudaGetLastError();
+}
+
+}  // namespace gdn

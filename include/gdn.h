@@ -1,0 +1,142 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) chunked Gated DeltaNet library.
+ *
+ * The operation is the gated delta-rule recurrence
+ *
+ *     S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+ *     o_t = S_t q_t,                      alpha_t = exp(g_t),
+ *
+ * with a d_v x d_k state per (sequence, head), evaluated in chunks of 64 tokens
+ * with the WY representation (onedev.kr summary of the FlashQLA AICon 2026
+ * talk, paragraph on the WY representation: intra-chunk K K^T and its inverse,
+ * W and U, the chunk-to-chunk state pass, the output).  Background for the
+ * recurrence itself: same page, paragraphs on the linear-attention background
+ * (d x d state, O(N d^2)) and on the effective sliding window (alpha in (0,1),
+ * L2-normalised keys).
+ *
+ * Conventions for every entry point
+ *  - All tensor pointers are DEVICE pointers, contiguous, 16-byte aligned.
+ *  - q, k [B, T, H, d_k]; v, o, dO [B, T, H, d_v] (token-major, then head,
+ *    then feature).  With cu_seqlens != NULL the batch is packed: B == 1 and
+ *    sequence n occupies tokens cu_seqlens[n] .. cu_seqlens[n+1]-1.
+ *  - g, beta, dg, dbeta: fp32 [B, T, H].
+ *  - States S0, S_T, dS_T, dS0: fp32 [N, H, d_v, d_k] row-major, N = number of
+ *    sequences (B, or num_seqs when packed).  Row index = value feature.
+ *  - The caller owns all memory.  The library never allocates: scratch memory
+ *    is the caller's `workspace`, sized by the *_workspace_size queries.
+ *  - Calls are asynchronous on `stream` and never synchronise the host.
+ *  - Argument errors are detected on the host before any launch and return
+ *    GDN_ERR_INVALID_ARG / GDN_ERR_UNSUPPORTED / GDN_ERR_WORKSPACE; a failed
+ *    launch returns GDN_ERR_CUDA.  gdn_last_error_string() (thread-local)
+ *    gives a one-line reason.
+ *  - Results are deterministic (no floating-point atomics).
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *gdn_stream_t; /* same type as cudaStream_t; NULL = default stream */
+
+typedef enum { GDN_BF16 = 0, GDN_FP32 = 1 } gdn_dtype;
+
+enum {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = 1, /* bad pointer, shape, stride or alignment                 */
+  GDN_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. d not in {64, 128})      */
+  GDN_ERR_WORKSPACE = 3,   /* workspace NULL or smaller than the size query          */
+  GDN_ERR_CUDA = 4         /* a CUDA call or kernel launch failed                     */
+};
+
+enum {
+  GDN_L2NORM_QK = 1u,  /* normalise q and k per token in-kernel: x / sqrt(|x|^2 + 1e-6)   */
+  GDN_SP_OFF = 2u,     /* no intra-card sequence parallelism: one segment per sequence    */
+  GDN_WINDOW_OFF = 4u  /* never skip the segment-start correction (always exact path)     */
+};
+
+/* Problem description shared by the forward, the backward and the size queries. */
+typedef struct {
+  int B, T, H;                /* with cu_seqlens: B == 1 and T = total packed tokens     */
+  int Dk, Dv;                 /* d_k == d_v, 64 or 128                                   */
+  const int32_t *cu_seqlens;  /* device [num_seqs + 1], or NULL                          */
+  int num_seqs;               /* number of sequences when cu_seqlens != NULL             */
+  gdn_dtype dtype;            /* dtype of q, k, v, o, dO, dq, dk, dv                     */
+  float scale;                /* o_t = S_t (scale * q_t), applied after normalisation    */
+  unsigned flags;             /* GDN_L2NORM_QK | GDN_SP_OFF | GDN_WINDOW_OFF             */
+  int seg_chunks;             /* chunks per segment for sequence parallelism; 0 = auto   */
+  int reserved[3];            /* must be 0                                               */
+} gdn_shape;
+
+/* Workspace bytes needed by gdn_chunk_fwd / gdn_chunk_bwd for this shape on the
+ * current device (the segment plan depends on its SM count).  0 on error. */
+size_t gdn_fwd_workspace_size(const gdn_shape *shape);
+size_t gdn_bwd_workspace_size(const gdn_shape *shape);
+
+/*
+ * Forward.  Computes o (and S_T if non-NULL) from q, k, v, g, beta and the
+ * initial state S0 (NULL = zero state).
+ *
+ * Steps (all in sm_103a kernels on `stream`): segment plan from cu_seqlens;
+ * gate scan (per-chunk log-decay sums, which mark segment starts inside an
+ * effective sliding window -- onedev.kr talk summary, paragraph on the
+ * effective sliding window); pass A over segments whose start must be
+ * corrected (state from zero plus the composed d_k x d_k transition --
+ * paragraph on parallelism); the sequential start-state fix-up; pass B, the
+ * fused WY + state pass + output over every segment.
+ */
+int gdn_chunk_fwd(const gdn_shape *shape,
+                  const void *q, const void *k, const void *v,
+                  const float *g, const float *beta,
+                  const float *S0, /* nullable */
+                  void *o, float *S_T, /* S_T nullable */
+                  void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+
+/*
+ * Backward (stateless: recomputes everything from the inputs).  Given dO and
+ * dS_T (NULL = zero), writes dq, dk, dv (input dtype), dg, dbeta (fp32) and,
+ * when S0 != NULL, dS0 (fp32; required then).  Gradients of q and k are with
+ * respect to the raw inputs (through the optional normalisation and scale).
+ * The WY backward forms dA and dA^T into one symmetric matrix multiplied with
+ * K once (onedev.kr talk summary, paragraph on SFU load, last sentence).
+ */
+int gdn_chunk_bwd(const gdn_shape *shape,
+                  const void *q, const void *k, const void *v,
+                  const float *g, const float *beta,
+                  const float *S0,   /* nullable */
+                  const void *dO,
+                  const float *dS_T, /* nullable */
+                  void *dq, void *dk, void *dv, float *dg, float *dbeta,
+                  float *dS0,        /* required iff S0 != NULL */
+                  void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+
+/* Reads the device status word that the kernels of the last call on `stream`
+ * set (synchronises the stream).  Bit 0: a chunk's in-chunk log-decay span
+ * exceeded the range of the gamma factoring (|G_r - G_mid| > 80), so its
+ * results are not reliable.  Returns -1 on a CUDA error.  `workspace` is the
+ * one passed to that call. */
+int gdn_get_device_status(const gdn_shape *shape, const void *workspace, gdn_stream_t stream);
+
+/* The segment plan for this shape on the current device: chunks per segment,
+ * an upper bound on the number of segments, and on the number of chunks. */
+int gdn_plan_query(const gdn_shape *shape, int *seg_chunks, int *max_segments, int *max_chunks);
+
+/* Diagnostics for benchmarks: when enabled, every kernel launch of the library
+ * is bracketed by CUDA events (from a pool created on the first enable) on its
+ * stream.  gdn_profile_report() waits for the recorded events and writes one
+ * line "<kernel> <launches> <total_ms>" per kernel into buf (truncated to len),
+ * returning the full report length; reset != 0 clears the totals. */
+int gdn_profile_enable(int on);
+int gdn_profile_report(char *buf, size_t len, int reset);
+
+const char *gdn_status_string(int status);
+const char *gdn_last_error_string(void); /* thread-local, "" if none */
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDN_H_ */

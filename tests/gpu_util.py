@@ -1,0 +1,54 @@
+"""Shared helpers of the GPU parity tests (CUDA path vs the CPU oracle)."""
+import numpy as np
+import torch
+
+import gated_deltanet_linear_15_gb300 as g
+import oracle
+
+# max |x - ref| / rms(ref), per output tensor: bf16 inputs with fp32 accumulation, and fp32 mode
+TOL = {"bf16": 2e-2, "fp32": 1e-4}
+
+
+def rel_err(x, ref):
+    ref = np.asarray(ref, dtype=np.float64)
+    x = x.detach().float().cpu().numpy().astype(np.float64) if hasattr(x, "detach") else np.asarray(x, np.float64)
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    if rms == 0.0:
+        return float(np.max(np.abs(x)))
+    return float(np.max(np.abs(x - ref))) / rms
+
+
+def run_gpu(x, *, bwd=True, sp=True, window=True, seg_chunks=0, with_final=True):
+    o, ST = g.chunk_gated_delta_rule_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], with_final,
+                                         x["cu_seqlens"], x["scale"], x["l2norm"], sp=sp, window=window,
+                                         seg_chunks=seg_chunks)
+    out = dict(o=o, S_T=ST)
+    if bwd:
+        dq, dk, dv, dg, db, dS0 = g.chunk_gated_delta_rule_bwd(
+            x["q"], x["k"], x["v"], x["g"], x["beta"], x["dO"], x["S0"], x["dST"], x["cu_seqlens"], x["scale"],
+            x["l2norm"], sp=sp, window=window, seg_chunks=seg_chunks)
+        out.update(dq=dq, dk=dk, dv=dv, dg=dg, dbeta=db, dS0=dS0)
+    torch.cuda.synchronize()
+    return out
+
+
+def run_oracle(x, *, bwd=True):
+    cu = x["cu_seqlens"]
+    o, ST = oracle.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], cu, scale=x["scale"],
+                       l2norm=x["l2norm"])
+    out = dict(o=o, S_T=ST)
+    if bwd:
+        out.update(oracle.bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["dO"], x["S0"], x["dST"], cu,
+                              scale=x["scale"], l2norm=x["l2norm"]))
+    return out
+
+
+def compare(got, ref, tol, keys=None):
+    errs = {}
+    for key in keys or ref.keys():
+        if got.get(key) is None or ref.get(key) is None:
+            continue
+        errs[key] = rel_err(got[key], ref[key])
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, f"errors above {tol}: {bad} (all: {errs})"
+    return errs

@@ -1,0 +1,123 @@
+"""CPU checks of the C ABI: the library loads, exports every declared symbol, and
+rejects bad arguments on the host with the documented status codes (these
+paths return before any CUDA launch, so no GPU is needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+from gated_deltanet_linear_15_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build_library()
+    return _lib.load()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_]+)\s*\(", src)))
+
+
+def test_header_and_binding_agree():
+    assert _declared() == sorted(_lib.EXPORTS)
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def _shape(**kw):
+    s = _lib.GdnShape()
+    s.B, s.T, s.H, s.Dk, s.Dv = 1, 128, 2, 128, 128
+    s.dtype, s.scale, s.flags = _lib.GDN_BF16, 1.0, 0
+    for k, v in kw.items():
+        setattr(s, k, v)
+    return s
+
+
+def _fwd(lib, s, ptr=0x10000, ws_bytes=1 << 40, q=None):
+    p = ptr if q is None else q
+    return lib.gdn_chunk_fwd(ctypes.byref(s), p, ptr, ptr, ptr, ptr, None, ptr, None, ptr, ws_bytes, None)
+
+
+def test_status_strings(lib):
+    assert lib.gdn_status_string(0) == b"ok"
+    assert lib.gdn_status_string(2) == b"unsupported configuration"
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Dk=96, Dv=96), _lib.GDN_ERR_UNSUPPORTED),
+    (dict(Dk=128, Dv=64), _lib.GDN_ERR_UNSUPPORTED),
+    (dict(dtype=_lib.GDN_FP32), _lib.GDN_ERR_UNSUPPORTED),      # fp32 needs d = 64
+    (dict(H=0), _lib.GDN_ERR_INVALID_ARG),
+    (dict(B=0), _lib.GDN_ERR_INVALID_ARG),
+    (dict(T=-1), _lib.GDN_ERR_INVALID_ARG),
+    (dict(dtype=7), _lib.GDN_ERR_INVALID_ARG),
+    (dict(seg_chunks=-2), _lib.GDN_ERR_INVALID_ARG),
+])
+def test_bad_shapes_rejected(lib, kw, code):
+    s = _shape(**kw)
+    assert _fwd(lib, s) == code
+    assert lib.gdn_last_error_string() != b""
+    assert lib.gdn_fwd_workspace_size(ctypes.byref(s)) == 0
+
+
+def test_reserved_must_be_zero(lib):
+    s = _shape()
+    s.reserved[1] = 3
+    assert _fwd(lib, s) == _lib.GDN_ERR_INVALID_ARG
+
+
+def test_null_and_misaligned_pointers(lib):
+    s = _shape()
+    assert _fwd(lib, s, q=0) == _lib.GDN_ERR_INVALID_ARG
+    assert b"q is NULL" in lib.gdn_last_error_string()
+    assert _fwd(lib, s, q=0x10008) == _lib.GDN_ERR_INVALID_ARG
+    assert b"aligned" in lib.gdn_last_error_string()
+
+
+def test_workspace_checks(lib):
+    s = _shape()
+    need = lib.gdn_fwd_workspace_size(ctypes.byref(s))
+    assert need > 0
+    assert _fwd(lib, s, ws_bytes=need - 1) == _lib.GDN_ERR_WORKSPACE
+    assert lib.gdn_bwd_workspace_size(ctypes.byref(s)) > need   # per-chunk states for the backward
+
+
+def test_cu_seqlens_requires_B1(lib):
+    s = _shape(B=2, cu_seqlens=0x10000, num_seqs=2)
+    assert _fwd(lib, s) == _lib.GDN_ERR_INVALID_ARG
+
+
+def test_bwd_requires_dS0_with_S0(lib):
+    s = _shape()
+    p = 0x10000
+    rc = lib.gdn_chunk_bwd(ctypes.byref(s), p, p, p, p, p, p, p, None, p, p, p, p, p, None, p, 1 << 40, None)
+    assert rc == _lib.GDN_ERR_INVALID_ARG
+    assert b"dS0" in lib.gdn_last_error_string()
+
+
+def test_plan_query_sp_policy(lib):
+    """The segment plan: SP off gives one segment per sequence; forced segment length is honoured;
+    with many (sequence, head) pairs no split happens."""
+    a, b, c = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    s = _shape(T=8192, H=32, flags=_lib.GDN_SP_OFF)
+    assert lib.gdn_plan_query(ctypes.byref(s), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)) == 0
+    assert (a.value, b.value, c.value) == (128, 1, 128)
+    s = _shape(T=8192, H=32, seg_chunks=10)
+    lib.gdn_plan_query(ctypes.byref(s), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c))
+    assert (a.value, b.value) == (10, 13)
+    s = _shape(B=64, T=4096, H=32)
+    lib.gdn_plan_query(ctypes.byref(s), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c))
+    assert a.value == 64 and b.value == 64
+    s = _shape(T=65536, H=8)           # long context, few heads: split
+    lib.gdn_plan_query(ctypes.byref(s), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c))
+    assert 1 < a.value < 1024 and b.value * 8 >= 100
