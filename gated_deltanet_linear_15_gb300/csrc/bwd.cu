@@ -6,9 +6,9 @@
 //   dS0   = gam_C dS + (diag(gam) dO)^T Q - dUt^T W           (reverse chain)
 //   dQ    = diag(gam) dO S0 + dPm K,  dPm = diag(gp) tril_incl(dO Ut^T) diag(rgp)
 //   dK    = diag(cdec) Ut dS + dPm^T Q + diag(beta) Ahat^T dW' + (dN + dN^T) K
-//   dV    = diag(beta rgp) Ahat^T dU'
-//   with dU' = diag(gp) dUt, dW' = diag(gam) dW = -gam_mid dU' S0,
-//   dAhat = dW' (diag(beta) K)^T + dU' (diag(beta rgp) V)^T,
+//   dV    = X2^T dUt,  X2 = diag(gp) Ahat diag(beta rgp)  (the forward's bounded operand)
+//   with dW' = diag(gam) dW = -diag(gam) dUt S0,
+//   dAhat = (dW' K^T + Gamma * (dUt V^T)) diag(beta),  Gamma_ri = gp_r rgp_i (i <= r),
 //   dT = -Ahat^T dAhat Ahat^T,  dN = strict_tril(diag(beta) dT).
 // The last line forms dA and dA^T as one symmetric matrix multiplied with K
 // once (onedev.kr FlashQLA talk summary, paragraph on SFU load, last sentence).
@@ -41,8 +41,9 @@ template <typename E, int D> struct ChainSmem {
   float ys[768];
 };
 
-template <typename E, int D>
+template <typename I, int D>
 __global__ void __launch_bounds__(NTHREADS, 1) bwd_chain_kernel(BwdArgs a) {
+  using E = typename OpType<I>::T;
   using SM = ChainSmem<E, D>;
   constexpr int LD = SM::LD, LC = SM::LC, LN = SM::LN;
   constexpr int SWM = D / 4, SWN = D / 2;
@@ -77,9 +78,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_chain_kernel(BwdArgs a) {
   const bool l2 = (a.flags & kFlagL2Norm) != 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wr = warp >> 1, wc = warp & 1;
-  const E *qg = static_cast<const E *>(a.q);
-  const E *kg = static_cast<const E *>(a.k);
-  const E *dog = static_cast<const E *>(a.dO);
+  const I *qg = static_cast<const I *>(a.q);
+  const I *kg = static_cast<const I *>(a.k);
+  const I *dog = static_cast<const I *>(a.dO);
   const size_t DD = (size_t)D * D;
   const size_t sh_idx = (size_t)s * H + h;
 
@@ -89,10 +90,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_chain_kernel(BwdArgs a) {
   auto issue_loads = [&](int c) {
     const long tok0 = bos + (long)c * CH;
     const int nvalid = min(CH, len - c * CH);
-    load_tile<E, D>(sm.k, LD, kg, H, h, tok0, nvalid);
+    load_tile<I, D>(sm.k, LD, kg, H, h, tok0, nvalid);
     if (!transition) {
-      load_tile<E, D>(sm.q, LD, qg, H, h, tok0, nvalid);
-      load_tile<E, D>(sm.dob, LD, dog, H, h, tok0, nvalid);
+      load_tile<I, D>(sm.q, LD, qg, H, h, tok0, nvalid);
+      load_tile<I, D>(sm.dob, LD, dog, H, h, tok0, nvalid);
     }
     load_scalars(sm.g, a.g, H, h, tok0, nvalid, 0);
     load_scalars(sm.beta, a.beta, H, h, tok0, nvalid, 64);
@@ -135,14 +136,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_chain_kernel(BwdArgs a) {
         *reinterpret_cast<uint4 *>(dst + (size_t)r * D + cc) = *reinterpret_cast<const uint4 *>(&sm.ds[r * LD + cc]);
       }
     }
-    if (l2) {
-      l2norm_rows<E, D>(sm.k, LD, 1.f, nullptr);
-      if (!transition) l2norm_rows<E, D>(sm.q, LD, a.scale, nullptr);
-    } else if (!transition && a.scale != 1.f) {
-      for (int e = threadIdx.x; e < CH * D; e += NTHREADS) {
-        const int r = e / D, cc = e % D;
-        sm.q[r * LD + cc] = fromf<E>(tof(sm.q[r * LD + cc]) * a.scale);
-      }
+    prep_rows<I, E, D>(sm.k, LD, 1.f, l2, nullptr);
+    if (!transition) {
+      prep_rows<I, E, D>(sm.q, LD, a.scale, l2, nullptr);
+      prep_rows<I, E, D>(sm.dob, LD, 1.f, false, nullptr);
     }
     if (warp == 0) gate_prefix(sm.g, sm.gt);
     __syncthreads();
@@ -234,7 +231,7 @@ template <typename E, int D> struct LocalSmem {
   static constexpr int LN = CH + 4;
   E q[CH * LD], k[CH * LD], v[CH * LD], dob[CH * LD];
   E s0[D * LD];
-  E ds[D * LD];  // dS, later reused for dU'
+  E ds[D * LD];  // dS, later reused for dUt
   E ut[CH * LD], w[CH * LD];
   E p[CH * LC], x1[CH * LC], x2[CH * LC];  // p later holds dPm, then Sigma; x2 later holds Ahat
   float nf[CH * LN];
@@ -247,8 +244,9 @@ template <typename E, int D> struct LocalSmem {
   float red[NWARPS];
 };
 
-template <typename E, int D>
+template <typename I, int D>
 __global__ void __launch_bounds__(NTHREADS, 1) bwd_local_kernel(BwdArgs a) {
+  using E = typename OpType<I>::T;
   using SM = LocalSmem<E, D>;
   constexpr int LD = SM::LD, LC = SM::LC, LN = SM::LN;
   constexpr int WN = D / 2;
@@ -269,10 +267,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_local_kernel(BwdArgs a) {
   const size_t st_idx = ((size_t)gc * H + h) * DD;
 
   // ---- loads
-  load_tile<E, D>(sm.q, LD, static_cast<const E *>(a.q), H, h, tok0, nvalid);
-  load_tile<E, D>(sm.k, LD, static_cast<const E *>(a.k), H, h, tok0, nvalid);
-  load_tile<E, D>(sm.v, LD, static_cast<const E *>(a.v), H, h, tok0, nvalid);
-  load_tile<E, D>(sm.dob, LD, static_cast<const E *>(a.dO), H, h, tok0, nvalid);
+  load_tile<I, D>(sm.q, LD, static_cast<const I *>(a.q), H, h, tok0, nvalid);
+  load_tile<I, D>(sm.k, LD, static_cast<const I *>(a.k), H, h, tok0, nvalid);
+  load_tile<I, D>(sm.v, LD, static_cast<const I *>(a.v), H, h, tok0, nvalid);
+  load_tile<I, D>(sm.dob, LD, static_cast<const I *>(a.dO), H, h, tok0, nvalid);
   load_scalars(sm.g, a.g, H, h, tok0, nvalid, 0);
   load_scalars(sm.beta, a.beta, H, h, tok0, nvalid, 64);
   {
@@ -288,15 +286,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_local_kernel(BwdArgs a) {
   cp_async_commit();
   cp_async_wait_all();
   __syncthreads();
-  if (l2) {
-    l2norm_rows<E, D>(sm.k, LD, 1.f, sm.nk);
-    l2norm_rows<E, D>(sm.q, LD, a.scale, sm.nq);
-  } else if (a.scale != 1.f) {
-    for (int e = threadIdx.x; e < CH * D; e += NTHREADS) {
-      const int r = e / D, cc = e % D;
-      sm.q[r * LD + cc] = fromf<E>(tof(sm.q[r * LD + cc]) * a.scale);
-    }
-  }
+  prep_rows<I, E, D>(sm.k, LD, 1.f, l2, sm.nk);
+  prep_rows<I, E, D>(sm.q, LD, a.scale, l2, sm.nq);
+  prep_rows<I, E, D>(sm.v, LD, 1.f, false, nullptr);
+  prep_rows<I, E, D>(sm.dob, LD, 1.f, false, nullptr);
   if (warp == 0) gate_prefix(sm.g, sm.gt);
   __syncthreads();
 
@@ -326,7 +319,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_local_kernel(BwdArgs a) {
     const float ah = ahat_at(sm.nf, LN, r, i);
     const float b = sm.beta[i];
     sm.x1[r * LC + i] = fromf<E>(ah * b);
-    sm.x2[r * LC + i] = fromf<E>(ah * b * sm.gt.rgp[i]);
+    sm.x2[r * LC + i] = fromf<E>(i <= r ? ah * b * (sm.gt.gp[r] * sm.gt.rgp[i]) : 0.f);
   }
   __syncthreads();
 
@@ -346,13 +339,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_local_kernel(BwdArgs a) {
     Acc<16, WN> acc;
     acc.zero();
     warp_mma<16, WN, false, true>(acc, sm.x2, LC, sm.v, LD, m0, n0, CH);
-    acc.each([&](int r, int cc, float &v) { v *= sm.gt.gp[m0 + r]; });
     warp_mma<16, WN, false, false>(acc, sm.w, LD, sm.s0, LD, m0, n0, D);
     acc.pairs([&](int r, int cc, float &v0, float &v1) { st2(&sm.ut[(m0 + r) * LD + n0 + cc], v0, v1); });
   }
   __syncthreads();
 
-  // ---- Y = K dS^T: y-terms; dUt = diag(cdec) Y + P^T dO; <dUt, Ut>; dU' = diag(gp) dUt (into regs)
+  // ---- Y = K dS^T: y-terms; dUt = diag(cdec) Y + P^T dO; <dUt, Ut>
   Acc<16, WN> dU;
   {
     dU.zero();
@@ -392,12 +384,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_local_kernel(BwdArgs a) {
     if (lane == 0) sm.red[warp] = acc;
   }
   __syncthreads();  // everyone done with sm.ds (dS)
-  E *du = sm.ds;   // dU' = diag(gp) dUt   (CH x LD; dS is no longer needed)
-  E *dw = sm.dob;  // dW' = -gam_mid dU' S0 (written after the last read of dO)
-  dU.pairs([&](int r, int cc, float &v0, float &v1) {
-    const float gp = sm.gt.gp[m0 + r];
-    st2(&du[(m0 + r) * LD + n0 + cc], v0 * gp, v1 * gp);
-  });
+  E *du = sm.ds;   // dUt   (CH x LD; dS is no longer needed)
+  E *dw = sm.dob;  // dW' = -diag(gam) dUt S0 (written after the last read of dO)
+  dU.pairs([&](int r, int cc, float &v0, float &v1) { st2(&du[(m0 + r) * LD + n0 + cc], v0, v1); });
   // ---- dP = dO Ut^T  ->  Z = dP * P sums, dPm (written over P, element by element)
   E *dpm = sm.p;
   {
@@ -464,7 +453,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_local_kernel(BwdArgs a) {
     }
     __syncthreads();
     // dq = scale * dq^ (no norm), or (scale dq^ - Q^ (Q^ . dq^) / scale) / |q|
-    E *dqg = static_cast<E *>(a.dq);
+    I *dqg = static_cast<I *>(a.dq);
     acc.pairs([&](int r, int cc, float &v0, float &v1) {
       const int row = m0 + r;
       if (row >= nvalid) return;
@@ -481,25 +470,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_local_kernel(BwdArgs a) {
       st2(dqg + ((size_t)(tok0 + row) * H + h) * D + n0 + cc, o0, o1);
     });
   }
-  // ---- dW' = -gam_mid dU' S0
+  // ---- dW' = -diag(gam) dUt S0
   {
     Acc<16, WN> acc;
     acc.zero();
     warp_mma<16, WN, false, true>(acc, du, LD, sm.s0, LD, m0, n0, D);
-    const float gmid = -sm.gt.gam[31];
-    acc.pairs([&](int r, int cc, float &v0, float &v1) { st2(&dw[(m0 + r) * LD + n0 + cc], v0 * gmid, v1 * gmid); });
+    acc.pairs([&](int r, int cc, float &v0, float &v1) {
+      const float gm = -sm.gt.gam[m0 + r];
+      st2(&dw[(m0 + r) * LD + n0 + cc], v0 * gm, v1 * gm);
+    });
   }
   __syncthreads();
   // ---- dK += dPm^T Q + X1^T dW'
   warp_mma<16, WN, true, true>(dK, dpm, LC, sm.q, LD, m0, n0, CH);
   warp_mma<16, WN, true, true>(dK, sm.x1, LC, dw, LD, m0, n0, CH);
-  // ---- dV = X2^T dU'
+  // ---- dV = X2^T dUt
   {
     Acc<16, WN> acc;
     acc.zero();
     warp_mma<16, WN, true, true>(acc, sm.x2, LC, du, LD, m0, n0, CH);
     float rv[2] = {0.f, 0.f};
-    E *dvg = static_cast<E *>(a.dv);
+    I *dvg = static_cast<I *>(a.dv);
     acc.pairs([&](int r, int cc, float &v0, float &v1) {
       const int row = m0 + r;
       rv[r >> 3] += v0 * tof(sm.v[row * LD + n0 + cc]) + v1 * tof(sm.v[row * LD + n0 + cc + 1]);
@@ -512,7 +503,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_local_kernel(BwdArgs a) {
       sm.part[12 + wc][m0 + (lane >> 2) + 8] = rv[1];
     }
   }
-  // ---- dAhat = (dW' K^T) diag(beta) + (dU' V^T) diag(beta rgp); beta column terms
+  // ---- dAhat = (dW' K^T + Gamma * (dUt V^T)) diag(beta); beta column terms
   {
     Acc<16, 32> a1, a2;
     a1.zero();
@@ -523,7 +514,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_local_kernel(BwdArgs a) {
     float cs[4][2];
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) cs[jj][0] = cs[jj][1] = 0.f;
-    // element (r, i): a1 = <dW'_r, k_i>, a2 = <dU'_r, v_i>
+    // element (r, i): a1 = <dW'_r, k_i>, a2 = <dUt_r, v_i>; the V term carries
+    // Gamma_ri = gp_r rgp_i <= 1 for i <= r (entries above the diagonal do not
+    // reach the strictly lower part of dT and are dropped)
     {
       const int lr = lane >> 2, lcc = 2 * (lane & 3);
 #pragma unroll
@@ -532,7 +525,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_local_kernel(BwdArgs a) {
         for (int e = 0; e < 4; ++e) {
           const int row = pm0 + lr + 8 * (e >> 1), col = pn0 + 8 * jj + lcc + (e & 1);
           const float ah = ahat_at(sm.nf, LN, row, col);
-          const float x1 = a1.c[0][jj][e], x2 = a2.c[0][jj][e] * sm.gt.rgp[col];
+          const float x1 = a1.c[0][jj][e];
+          const float x2 = col <= row ? a2.c[0][jj][e] * (sm.gt.gp[row] * sm.gt.rgp[col]) : 0.f;
           cs[jj][e & 1] += ah * (x1 + x2);
           a1.c[0][jj][e] = sm.beta[col] * (x1 + x2);
         }
@@ -610,7 +604,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_local_kernel(BwdArgs a) {
   }
   __syncthreads();
   {
-    E *dkg = static_cast<E *>(a.dk);
+    I *dkg = static_cast<I *>(a.dk);
     dK.pairs([&](int r, int cc, float &v0, float &v1) {
       const int row = m0 + r;
       if (row >= nvalid) return;
@@ -673,20 +667,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_local_kernel(BwdArgs a) {
 }
 
 // ================================================================== launchers
-template <typename E, int D> static int launch_chain(const BwdArgs &a, dim3 grid, cudaStream_t st) {
+template <typename I, int D> static int launch_chain(const BwdArgs &a, dim3 grid, cudaStream_t st) {
+  using E = typename OpType<I>::T;
   const size_t smem = sizeof(ChainSmem<E, D>);
   static_assert(sizeof(ChainSmem<E, D>) <= 232448, "shared memory budget");
-  auto kern = bwd_chain_kernel<E, D>;
+  auto kern = bwd_chain_kernel<I, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
   kern<<<grid, NTHREADS, smem, st>>>(a);
   return (int)cudaGetLastError();
 }
-template <typename E, int D> static int launch_local(const BwdArgs &a, int CH_max, cudaStream_t st) {
+template <typename I, int D> static int launch_local(const BwdArgs &a, int CH_max, cudaStream_t st) {
+  using E = typename OpType<I>::T;
   const size_t smem = sizeof(LocalSmem<E, D>);
   static_assert(sizeof(LocalSmem<E, D>) <= 232448, "shared memory budget");
-  
-  auto kern = bwd_local_kernel<E, D>;
+  auto kern = bwd_local_kernel<I, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
   kern<<<dim3(CH_max, a.H), NTHREADS, smem, st>>>(a);

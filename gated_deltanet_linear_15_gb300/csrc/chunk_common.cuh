@@ -6,17 +6,20 @@
 
 namespace gdn {
 
-// Load a CH x D tile of a [tokens, H, D] tensor: row r = token tok0 + r of head h,
-// rows r >= nvalid are zero-filled.
-template <typename E, int D>
-__device__ __forceinline__ void load_tile(E *dst, int ld, const E *base, int H, int h, long tok0, int nvalid) {
-  constexpr int EPV = 16 / sizeof(E);  // elements per 16-byte piece
+// Load a CH x D tile of a [tokens, H, D] input tensor (element type I) into a
+// shared tile of the same element size: row r = token tok0 + r of head h, rows
+// r >= nvalid zero-filled.  The raw input bits land in the tile; prep_rows()
+// converts them to the operand type in place.
+template <typename I, int D>
+__device__ __forceinline__ void load_tile(void *dst, int ld, const I *base, int H, int h, long tok0, int nvalid) {
+  constexpr int EPV = 16 / sizeof(I);  // elements per 16-byte piece
   constexpr int VPR = D / EPV;
+  I *d = static_cast<I *>(dst);
   for (int e = threadIdx.x; e < CH * VPR; e += NTHREADS) {
     const int r = e / VPR, cidx = e % VPR;
     const bool valid = r < nvalid;
-    const E *src = base + ((size_t)(tok0 + (valid ? r : 0)) * H + h) * D + cidx * EPV;
-    cp_async16(dst + r * ld + cidx * EPV, src, valid);
+    const I *src = base + ((size_t)(tok0 + (valid ? r : 0)) * H + h) * D + cidx * EPV;
+    cp_async16(d + r * ld + cidx * EPV, src, valid);
   }
 }
 
@@ -30,24 +33,33 @@ __device__ __forceinline__ void load_scalars(float *dst, const float *base, int 
   }
 }
 
-// In-place row normalisation x <- x * mul / sqrt(sum x^2 + 1e-6), one warp per row.
-// Optionally records the norm used per row.
-template <typename E, int D>
-__device__ __forceinline__ void l2norm_rows(E *t, int ld, float mul, float *norm_out) {
+// In place, one warp per row: raw input values x (type I) become operand values
+// (type E)  x * mul / sqrt(sum x^2 + 1e-6)  when `l2`, else  x * mul.  The
+// normalisation's row reduction uses warp shuffles; `norm_out` (optional)
+// receives the norm of each row.
+template <typename I, typename E, int D>
+__device__ __forceinline__ void prep_rows(E *t, int ld, float mul, bool l2, float *norm_out) {
+  static_assert(sizeof(I) == sizeof(E), "in-place conversion needs equal element sizes");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const I *src = reinterpret_cast<const I *>(t);
   for (int r = warp; r < CH; r += NWARPS) {
+    float x[D / 32];
     float ss = 0.f;
 #pragma unroll
-    for (int c = lane; c < D; c += 32) {
-      const float x = tof(t[r * ld + c]);
-      ss += x * x;
+    for (int i = 0; i < D / 32; ++i) {
+      x[i] = tof(src[r * ld + lane + 32 * i]);
+      ss += x[i] * x[i];
     }
-    ss = warp_sum(ss);
-    const float nrm = sqrtf(ss + 1e-6f);
-    const float f = mul / nrm;
+    float f = mul;
+    if (l2) {
+      ss = warp_sum(ss);
+      const float nrm = sqrtf(ss + 1e-6f);
+      f = mul / nrm;
+      if (norm_out && lane == 0) norm_out[r] = nrm;
+    }
+    __syncwarp();
 #pragma unroll
-    for (int c = lane; c < D; c += 32) t[r * ld + c] = fromf<E>(tof(t[r * ld + c]) * f);
-    if (norm_out && lane == 0) norm_out[r] = nrm;
+    for (int i = 0; i < D / 32; ++i) t[r * ld + lane + 32 * i] = fromf<E>(x[i] * f);
   }
 }
 

@@ -2,13 +2,14 @@
 //
 // Tiles live in shared memory, row-major with a padded row stride.  The block
 // GEMM helpers compute one warp's output tile of C = op(A) op(B) with
-// mma.sync m16n8k16 (bf16 operands, fp32 accumulation) when the element type
-// is bf16, and with the same fragment ownership on CUDA cores when it is fp32
+// mma.sync m16n8k16 (fp16 operands, fp32 accumulation) when the element type
+// is fp16, and with the same fragment ownership on CUDA cores when it is fp32
 // (the fp32 mode needs full fp32 products, which the bf16/tf32 tensor paths do
 // not give).  The fragment layout is the PTX one for m16n8: thread `lane` owns
 // rows lane/4 and lane/4 + 8, columns 2*(lane%4) + {0, 1} of every 16x8 atom.
 #pragma once
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -19,20 +20,37 @@ constexpr int NTHREADS = 256; // threads per CTA in the chunk kernels
 constexpr int NWARPS = NTHREADS / 32;
 
 typedef __nv_bfloat16 bf16;
+typedef __half f16;
+
+// Operand precision of the tensor-core products.  bf16 inputs are widened to
+// fp16 in shared memory (exact inside fp16's range) and every computed operand
+// is rounded to fp16: 11 significant bits instead of bf16's 8, at the same MMA
+// rate.  Every computed operand is formed so that it stays bounded (decay
+// ratios gamma_r / gamma_i <= 1 are applied before rounding).  fp32 inputs keep
+// fp32 operands (CUDA-core products).
+template <typename I> struct OpType;
+template <> struct OpType<bf16> { typedef f16 T; };
+template <> struct OpType<float> { typedef float T; };
 
 template <typename E> struct Pad;
 template <> struct Pad<bf16> { static constexpr int v = 8; };
+template <> struct Pad<f16> { static constexpr int v = 8; };
 template <> struct Pad<float> { static constexpr int v = 4; };
 
 __device__ __forceinline__ float tof(bf16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float tof(f16 x) { return __half2float(x); }
 __device__ __forceinline__ float tof(float x) { return x; }
 template <typename E> __device__ __forceinline__ E fromf(float x);
 template <> __device__ __forceinline__ bf16 fromf<bf16>(float x) { return __float2bfloat16_rn(x); }
+template <> __device__ __forceinline__ f16 fromf<f16>(float x) { return __float2half_rn(x); }
 template <> __device__ __forceinline__ float fromf<float>(float x) { return x; }
 
 // store two adjacent values (columns c, c+1)
 __device__ __forceinline__ void st2(bf16 *p, float a, float b) {
   *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(a, b);
+}
+__device__ __forceinline__ void st2(f16 *p, float a, float b) {
+  *reinterpret_cast<__half2 *>(p) = __floats2half2_rn(a, b);
 }
 __device__ __forceinline__ void st2(float *p, float a, float b) {
   *reinterpret_cast<float2 *>(p) = make_float2(a, b);
@@ -67,7 +85,7 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void *p) {
 }
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};\n"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
@@ -111,7 +129,7 @@ template <int WM, int WN> struct Acc {
 //  AT == false: A stored [m][k] (row stride lda);  AT == true: A stored [k][m].
 //  BT == false: B stored [n][k] (row stride ldb);  BT == true: B stored [k][n].
 template <int WM, int WN, bool AT, bool BT>
-__device__ __forceinline__ void warp_mma(Acc<WM, WN> &acc, const bf16 *A, int lda, const bf16 *B, int ldb, int m0,
+__device__ __forceinline__ void warp_mma(Acc<WM, WN> &acc, const f16 *A, int lda, const f16 *B, int ldb, int m0,
                                          int n0, int K) {
   static_assert(WN % 16 == 0, "WN must be a multiple of 16");
   const int lane = threadIdx.x & 31;
@@ -122,10 +140,10 @@ __device__ __forceinline__ void warp_mma(Acc<WM, WN> &acc, const bf16 *A, int ld
 #pragma unroll
     for (int i = 0; i < WM / 16; ++i) {
       if (!AT) {
-        const bf16 *p = A + (size_t)(m0 + 16 * i + (lane & 15)) * lda + k0 + (lane >> 4) * 8;
+        const f16 *p = A + (size_t)(m0 + 16 * i + (lane & 15)) * lda + k0 + (lane >> 4) * 8;
         ldsm_x4(af[i], p);
       } else {
-        const bf16 *p = A + (size_t)(k0 + r8 + 8 * (mi >> 1)) * lda + m0 + 16 * i + 8 * (mi & 1);
+        const f16 *p = A + (size_t)(k0 + r8 + 8 * (mi >> 1)) * lda + m0 + 16 * i + 8 * (mi & 1);
         ldsm_x4_t(af[i], p);
       }
     }
@@ -133,10 +151,10 @@ __device__ __forceinline__ void warp_mma(Acc<WM, WN> &acc, const bf16 *A, int ld
     for (int j = 0; j < WN / 16; ++j) {
       uint32_t bfr[4];
       if (!BT) {
-        const bf16 *p = B + (size_t)(n0 + 16 * j + r8 + 8 * (mi >> 1)) * ldb + k0 + 8 * (mi & 1);
+        const f16 *p = B + (size_t)(n0 + 16 * j + r8 + 8 * (mi >> 1)) * ldb + k0 + 8 * (mi & 1);
         ldsm_x4(bfr, p);
       } else {
-        const bf16 *p = B + (size_t)(k0 + r8 + 8 * (mi & 1)) * ldb + n0 + 16 * j + 8 * (mi >> 1);
+        const f16 *p = B + (size_t)(k0 + r8 + 8 * (mi & 1)) * ldb + n0 + 16 * j + 8 * (mi >> 1);
         ldsm_x4_t(bfr, p);
       }
 #pragma unroll

@@ -6,7 +6,7 @@
 //
 // Per chunk (C = 64 tokens, S is d_v x d_k, G = in-chunk prefix of g):
 //   N    = strict_tril(K K^T);  Ahat = (I + diag(beta) N)^{-1}      (fp32)
-//   W    = diag(gam) Ahat diag(beta) K;   U = diag(gp) Ahat diag(beta rgp) V
+//   W    = diag(gam) Ahat diag(beta) K;   U = (diag(gp) Ahat diag(beta rgp)) V
 //   Ut   = U - W S0^T                                    (corrected values)
 //   O    = diag(gam) Q S0^T + P Ut,  P = diag(gp) tril_incl(Q K^T) diag(rgp)
 //   S_C  = gam_C S0 + Ut^T diag(cdec) K
@@ -40,8 +40,9 @@ template <typename E, int D> struct FwdSmem {
   float ys[768];
 };
 
-template <typename E, int D>
+template <typename I, int D>
 __global__ void __launch_bounds__(NTHREADS, 1) fwd_chunk_kernel(FwdArgs a) {
+  using E = typename OpType<I>::T;
   using SM = FwdSmem<E, D>;
   constexpr int LD = SM::LD, LC = SM::LC, LN = SM::LN;
   constexpr int SWM = D / 4, SWN = D / 2;  // state / output warp tile
@@ -79,9 +80,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_chunk_kernel(FwdArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wr = warp >> 1, wc = warp & 1;
 
-  const E *qg = static_cast<const E *>(a.q);
-  const E *kg = static_cast<const E *>(a.k);
-  const E *vg = static_cast<const E *>(a.v);
+  const I *qg = static_cast<const I *>(a.q);
+  const I *kg = static_cast<const I *>(a.k);
+  const I *vg = static_cast<const I *>(a.v);
   const size_t DD = (size_t)D * D;
   const size_t sh_idx = (size_t)s * H + h;
 
@@ -91,9 +92,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_chunk_kernel(FwdArgs a) {
   auto issue_loads = [&](int c) {
     const long tok0 = bos + (long)c * CH;
     const int nvalid = min(CH, len - c * CH);
-    load_tile<E, D>(sm.k, LD, kg, H, h, tok0, nvalid);
-    if (need_v) load_tile<E, D>(sm.v, LD, vg, H, h, tok0, nvalid);
-    if (outputs && c >= cbeg) load_tile<E, D>(sm.q, LD, qg, H, h, tok0, nvalid);
+    load_tile<I, D>(sm.k, LD, kg, H, h, tok0, nvalid);
+    if (need_v) load_tile<I, D>(sm.v, LD, vg, H, h, tok0, nvalid);
+    if (outputs && c >= cbeg) load_tile<I, D>(sm.q, LD, qg, H, h, tok0, nvalid);
     load_scalars(sm.g, a.g, H, h, tok0, nvalid, 0);
     load_scalars(sm.beta, a.beta, H, h, tok0, nvalid, 64);
     cp_async_commit();
@@ -147,15 +148,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_chunk_kernel(FwdArgs a) {
         *reinterpret_cast<uint4 *>(dst + (size_t)r * D + cc) = *reinterpret_cast<const uint4 *>(&sm.s[r * LD + cc]);
       }
     }
-    if (l2) {
-      l2norm_rows<E, D>(sm.k, LD, 1.f, nullptr);
-      if (emit) l2norm_rows<E, D>(sm.q, LD, a.scale, nullptr);
-    } else if (emit && a.scale != 1.f) {
-      for (int e = threadIdx.x; e < CH * D; e += NTHREADS) {
-        const int r = e / D, cc = e % D;
-        sm.q[r * LD + cc] = fromf<E>(tof(sm.q[r * LD + cc]) * a.scale);
-      }
-    }
+    prep_rows<I, E, D>(sm.k, LD, 1.f, l2, nullptr);
+    if (emit) prep_rows<I, E, D>(sm.q, LD, a.scale, l2, nullptr);
+    if (need_v) prep_rows<I, E, D>(sm.v, LD, 1.f, false, nullptr);
     if (warp == 0) {
       if (gate_prefix(sm.g, sm.gt) && lane == 0 && a.status) atomicOr(a.status, 1);
     }
@@ -188,13 +183,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_chunk_kernel(FwdArgs a) {
 
     tril_inverse(sm.nf, LN, sm.beta, sm.ys);
 
-    // ---- X1 = Ahat diag(beta), X2 = Ahat diag(beta * rgp)
+    // ---- X1 = Ahat diag(beta), X2 = diag(gp) Ahat diag(beta rgp) (entries <= |Ahat beta|)
     for (int e = threadIdx.x; e < CH * CH; e += NTHREADS) {
       const int r = e / CH, i = e % CH;
       const float ah = ahat_at(sm.nf, LN, r, i);
       const float b = sm.beta[i];
       sm.x1[r * LC + i] = fromf<E>(ah * b);
-      sm.x2[r * LC + i] = fromf<E>(ah * b * sm.gt.rgp[i]);
+      sm.x2[r * LC + i] = fromf<E>(i <= r ? ah * b * (sm.gt.gp[r] * sm.gt.rgp[i]) : 0.f);
     }
     __syncthreads();
 
@@ -204,10 +199,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_chunk_kernel(FwdArgs a) {
       const int m0 = (ww >> 1) * 32, n0 = (ww & 1) * SWN;
       if (warp < 4) {
         X.zero();
-        if (need_v) {
-          warp_mma<32, SWN, false, true>(X, sm.x2, LC, sm.v, LD, m0, n0, CH);
-          X.each([&](int r, int cc, float &v) { v *= sm.gt.gp[m0 + r]; });
-        }
+        if (need_v) warp_mma<32, SWN, false, true>(X, sm.x2, LC, sm.v, LD, m0, n0, CH);
       } else {
         Acc<32, SWN> acc;
         acc.zero();
@@ -251,7 +243,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_chunk_kernel(FwdArgs a) {
         const int m0 = (ww >> 1) * 32, n0 = (ww & 1) * SWN;
         X.each([&](int r, int cc, float &v) { v *= sm.gt.gam[m0 + r]; });
         warp_mma<32, SWN, false, true>(X, sm.p, LC, sm.ut, LD, m0, n0, CH);
-        X.pairs([&](int r, int cc, float &v0, float &v1) { st2(&sm.w[(m0 + r) * LD + n0 + cc], v0, v1); });
+        I *ostage = reinterpret_cast<I *>(sm.w);  // output staging in the input dtype
+        X.pairs([&](int r, int cc, float &v0, float &v1) { st2(&ostage[(m0 + r) * LD + n0 + cc], v0, v1); });
       }
     }
     __syncthreads();
@@ -259,14 +252,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_chunk_kernel(FwdArgs a) {
     // ---- state copy for the next chunk, output rows to HBM
     Sacc.pairs([&](int r, int cc, float &v0, float &v1) { st2(&sm.s[(wr * SWM + r) * LD + wc * SWN + cc], v0, v1); });
     if (emit) {
-      E *og = static_cast<E *>(a.o);
-      constexpr int EPV = 16 / sizeof(E);
+      I *og = static_cast<I *>(a.o);
+      const I *ostage = reinterpret_cast<const I *>(sm.w);
+      constexpr int EPV = 16 / sizeof(I);
       constexpr int VPR = D / EPV;
       for (int e = threadIdx.x; e < CH * VPR; e += NTHREADS) {
         const int r = e / VPR, cc = (e % VPR) * EPV;
         if (r < nvalid)
           *reinterpret_cast<uint4 *>(og + ((size_t)(tok0 + r) * H + h) * D + cc) =
-              *reinterpret_cast<const uint4 *>(&sm.w[r * LD + cc]);
+              *reinterpret_cast<const uint4 *>(&ostage[r * LD + cc]);
       }
     }
   }
@@ -286,10 +280,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_chunk_kernel(FwdArgs a) {
   }
 }
 
-template <typename E, int D> static int launch_fwd(const FwdArgs &a, dim3 grid, cudaStream_t st) {
+template <typename I, int D> static int launch_fwd(const FwdArgs &a, dim3 grid, cudaStream_t st) {
+  using E = typename OpType<I>::T;
   const size_t smem = sizeof(FwdSmem<E, D>);
   static_assert(sizeof(FwdSmem<E, D>) <= 232448, "shared memory budget");
-  auto kern = fwd_chunk_kernel<E, D>;
+  auto kern = fwd_chunk_kernel<I, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
   kern<<<grid, NTHREADS, smem, st>>>(a);
