@@ -22,7 +22,7 @@ import torch
 from . import _lib
 from ._lib import (GDN_BF16, GDN_FP32, GDN_L2NORM_QK, GDN_SP_OFF, GDN_WINDOW_OFF, GdnShape)
 
-__all__ = ["GdnShape", "make_shape", "gdn_chunk_fwd", "gdn_chunk_bwd", "gdn_fwd_workspace_size",
+__all__ = ["GdnShape", "make_shape", "gdn_chunk_fwd", "gdn_chunk_fwd_static", "gdn_chunk_bwd", "gdn_fwd_workspace_size",
            "gdn_bwd_workspace_size", "gdn_plan_query", "gdn_get_device_status", "gdn_profile_enable",
            "gdn_profile_report",
            "chunk_gated_delta_rule_fwd", "chunk_gated_delta_rule_bwd", "chunk_gated_delta_rule",
@@ -90,6 +90,13 @@ def gdn_chunk_fwd(shape: GdnShape, q, k, v, g, beta, S0, o, S_T, workspace, work
     return _lib.load().gdn_chunk_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                                      _ptr(S0), _ptr(o), _ptr(S_T), _ptr(workspace), int(workspace_bytes),
                                      _stream(stream))
+
+
+def gdn_chunk_fwd_static(shape: GdnShape, q, k, v, g, beta, S0, o, S_T, stream=None) -> int:
+    """Forward whose scratch is the library's fixed device array (no allocation
+    anywhere); for callers that cannot allocate device memory.  See gdn.h."""
+    return _lib.load().gdn_chunk_fwd_static(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                            _ptr(S0), _ptr(o), _ptr(S_T), _stream(stream))
 
 
 def gdn_chunk_bwd(shape: GdnShape, q, k, v, g, beta, S0, dO, dS_T, dq, dk, dv, dg, dbeta, dS0, workspace,

@@ -10,9 +10,11 @@ from . import build as _build
 GDN_BF16, GDN_FP32 = 0, 1
 GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE, GDN_ERR_CUDA = 0, 1, 2, 3, 4
 GDN_L2NORM_QK, GDN_SP_OFF, GDN_WINDOW_OFF = 1, 2, 4
+GDN_STATIC_SCRATCH_BYTES = 16 << 20
 
 # every symbol include/gdn.h declares
-EXPORTS = ("gdn_fwd_workspace_size", "gdn_bwd_workspace_size", "gdn_chunk_fwd", "gdn_chunk_bwd",
+EXPORTS = ("gdn_fwd_workspace_size", "gdn_bwd_workspace_size", "gdn_chunk_fwd", "gdn_chunk_fwd_static",
+           "gdn_chunk_bwd",
            "gdn_get_device_status", "gdn_plan_query", "gdn_profile_enable", "gdn_profile_report",
            "gdn_status_string", "gdn_last_error_string")
 
@@ -51,6 +53,8 @@ def load():
         lib.gdn_bwd_workspace_size.restype = ctypes.c_size_t
         lib.gdn_chunk_fwd.argtypes = [S, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
         lib.gdn_chunk_fwd.restype = ctypes.c_int
+        lib.gdn_chunk_fwd_static.argtypes = [S, P, P, P, P, P, P, P, P, P]
+        lib.gdn_chunk_fwd_static.restype = ctypes.c_int
         lib.gdn_chunk_bwd.argtypes = [S, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
         lib.gdn_chunk_bwd.restype = ctypes.c_int
         lib.gdn_get_device_status.argtypes = [S, P, P]

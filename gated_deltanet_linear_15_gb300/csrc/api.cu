@@ -357,6 +357,58 @@ int gdn_chunk_fwd(const gdn_shape *s, const void *q, const void *k, const void *
   return forward_passes(s, L, ws, fa, 1, st);
 }
 
+}  // extern "C"
+
+// ------------------------------------------------------------ no-allocation forward
+// Scratch for gdn_chunk_fwd_static: a fixed array in device memory that every
+// GPU loading this library holds until the process exits.  Host code only sees
+// a host-side stand-in under this name; its device address comes from
+// cudaGetSymbolAddress, taken once per device with that device current.
+namespace {
+constexpr size_t kStaticScratchBytes = (size_t)GDN_STATIC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void *g_static_ptr[kMaxDevices] = {};
+}  // namespace
+
+extern "C" {
+
+int gdn_chunk_fwd_static(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,
+                         const float *beta, const float *S0, void *o, float *S_T, gdn_stream_t stream) {
+  g_last_error.clear();
+  Layout L;
+  int rc = make_layout(s, L);
+  if (rc) return rc;
+  gdn_shape sh = *s;
+  if (L.fwd_total > kStaticScratchBytes && !(sh.flags & GDN_SP_OFF)) {
+    // the sequence-parallel buffers do not fit: run one segment per sequence
+    sh.flags |= GDN_SP_OFF;
+    if ((rc = make_layout(&sh, L))) return rc;
+  }
+  if (L.fwd_total > kStaticScratchBytes)
+    return fail(GDN_ERR_WORKSPACE,
+                "gdn_chunk_fwd_static: this shape needs %zu bytes of scratch, the static scratch holds %zu "
+                "(use gdn_chunk_fwd with a caller-provided workspace)",
+                L.fwd_total, kStaticScratchBytes);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return fail(GDN_ERR_CUDA, "gdn_chunk_fwd_static: no usable current device");
+  void *ptr = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (!g_static_ptr[dev]) {
+      void *p = nullptr;
+      const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+      if (e != cudaSuccess || !p)
+        return fail(GDN_ERR_CUDA, "gdn_chunk_fwd_static: cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
+      g_static_ptr[dev] = p;
+    }
+    ptr = g_static_ptr[dev];
+  }
+  return gdn_chunk_fwd(&sh, q, k, v, g, beta, S0, o, S_T, ptr, kStaticScratchBytes, stream);
+}
+
 int gdn_chunk_bwd(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g, const float *beta,
                   const float *S0, const void *dO, const float *dS_T, void *dq, void *dk, void *dv, float *dg,
                   float *dbeta, float *dS0, void *workspace, size_t workspace_bytes, gdn_stream_t stream) {

@@ -97,6 +97,33 @@ int gdn_chunk_fwd(const gdn_shape *shape,
                   void *workspace, size_t workspace_bytes, gdn_stream_t stream);
 
 /*
+ * Forward without any memory allocation by the caller or the library: the same
+ * computation as gdn_chunk_fwd, with its scratch taken from a fixed device
+ * array of GDN_STATIC_SCRATCH_BYTES that the library declares (the paper has no
+ * counterpart; this serves callers that cannot call cudaMalloc, such as code
+ * running inside another runtime's allocator-free region, a plugin host that
+ * forbids device allocations, or a process whose memory pool is fully
+ * reserved).  The caller still passes every input and output.
+ *  - Every GPU that loads the library holds the array until the process exits.
+ *  - The first call on a device looks the array's device address up (once per
+ *    device, with that device current); make that first call before any stream
+ *    capture.
+ *  - If the shape's scratch with sequence parallelism does not fit, the call
+ *    runs one segment per sequence (as with GDN_SP_OFF); if it still does not
+ *    fit, it returns GDN_ERR_WORKSPACE and launches nothing.
+ *  - All calls share the one array: calls that overlap on the GPU (other
+ *    streams, other threads) race and must be serialised by the caller.
+ *  - No cudaMalloc, cudaFree or allocating library routine is called.
+ */
+#define GDN_STATIC_SCRATCH_BYTES (16u << 20)
+int gdn_chunk_fwd_static(const gdn_shape *shape,
+                         const void *q, const void *k, const void *v,
+                         const float *g, const float *beta,
+                         const float *S0, /* nullable */
+                         void *o, float *S_T, /* S_T nullable */
+                         gdn_stream_t stream);
+
+/*
  * Backward (stateless: recomputes everything from the inputs).  Given dO and
  * dS_T (NULL = zero), writes dq, dk, dv (input dtype), dg, dbeta (fp32) and,
  * when S0 != NULL, dS0 (fp32; required then).  Gradients of q and k are with
