@@ -262,6 +262,54 @@ int prologue(const gdn_shape *s, const Layout &L, char *ws, const float *g, cuda
   return GDN_OK;
 }
 
+// ------------------------------------------------------------------ TMA tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// [tokens, H, 128] bf16 tensor, box = 64 features x 1 head x 64 tokens, 128-byte swizzle
+int qkv_map(CUtensorMap *m, const void *ptr, long tokens, int H) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)tokens};
+  cuuint64_t strides[2] = {128 * 2, (cuuint64_t)H * 128 * 2};
+  cuuint32_t box[3] = {64, 1, 64};
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return GDN_OK;
+}
+
+// The chunk forward kernel for this problem: tcgen05 for bf16 with d = 128, the
+// mma.sync/CUDA-core kernel otherwise (d = 64, fp32 inputs, empty batches).
+int launch_forward_kernel(const Layout &L, const gdn_shape *s, const FwdArgs &fa, dim3 grid, cudaStream_t st) {
+  const bool bf = s->dtype == GDN_BF16;
+  if (bf && L.D == 128 && L.Ttot > 0) {
+    CUtensorMap tq, tk, tv;
+    int rc;
+    if ((rc = qkv_map(&tk, fa.k, L.Ttot, L.H))) return rc;
+    if ((rc = qkv_map(&tv, fa.v, L.Ttot, L.H))) return rc;
+    if ((rc = qkv_map(&tq, fa.q ? fa.q : fa.k, L.Ttot, L.H))) return rc;
+    return launch_fwd_tc(fa, tq, tk, tv, grid, st);
+  }
+  return launch_fwd_chunk(fa, bf, L.D, grid, st);
+}
+
 // Forward state pass: pass A + fix-up when segments exist, then `pass` (1: outputs, 2: states).
 int forward_passes(const gdn_shape *s, const Layout &L, char *ws, FwdArgs fa, int pass, cudaStream_t st) {
   const bool bf = s->dtype == GDN_BF16;
@@ -269,7 +317,7 @@ int forward_passes(const gdn_shape *s, const Layout &L, char *ws, FwdArgs fa, in
     fa.pass = 0;
     {
       PROF("fwd_segment_pass_a");
-      CK(launch_fwd_chunk(fa, bf, L.D, dim3(L.S_max, L.H, 2), st));
+      CK(launch_forward_kernel(L, s, fa, dim3(L.S_max, L.H, 2), st));
     }
     FixupArgs fx;
     fx.plan = fa.plan;
@@ -287,7 +335,7 @@ int forward_passes(const gdn_shape *s, const Layout &L, char *ws, FwdArgs fa, in
   }
   fa.pass = pass;
   PROF(pass == 1 ? "fwd_chunk" : "fwd_states");
-  CK(launch_fwd_chunk(fa, bf, L.D, dim3(L.S_max, L.H, 1), st));
+  CK(launch_forward_kernel(L, s, fa, dim3(L.S_max, L.H, 1), st));
   return GDN_OK;
 }
 

@@ -38,7 +38,7 @@ template <typename E, int D> struct ChainSmem {
   float nf[CH * LN];
   float g[CH], beta[CH];
   Gates gt;
-  float ys[768];
+  float ys[1024];
 };
 
 template <typename I, int D>
@@ -237,7 +237,7 @@ template <typename E, int D> struct LocalSmem {
   float nf[CH * LN];
   float g[CH], beta[CH], nq[CH], nk[CH];
   Gates gt;
-  float ys[768];
+  float ys[1024];
   float part[14][CH];   // gate-gradient partials (see the final sum)
   float bpart[6][CH];   // beta-gradient partials
   float rdot[2][CH];    // row dots for the normalisation Jacobians

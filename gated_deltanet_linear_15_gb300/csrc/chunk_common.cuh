@@ -109,14 +109,45 @@ __device__ __forceinline__ bool gate_prefix(const float *g, Gates &gt) {
 }
 
 // Inverse of the unit lower-triangular T = I + diag(beta) N, N = strict_tril(K K^T),
-// in fp32.  `nf` (CH x ldn floats) holds N in its strictly lower triangle on entry;
-// on exit its strictly upper triangle holds Ahat^T (Ahat[r][i] at nf[i][r], i < r);
-// the lower triangle is left intact.  Diagonal 16x16 blocks are inverted by
-// forward substitution (one column per lane), then the off-diagonal blocks
-// follow by distance: Ahat_IJ = -Ahat_II sum_{K=J}^{I-1} T_IK Ahat_KJ.
-// `ys` is 768 floats of scratch.  Ends with __syncthreads().
+// in fp32 accuracy.  `nf` (CH x ldn floats) holds N in its strictly lower triangle
+// on entry; on exit its strictly upper triangle holds Ahat^T (Ahat[r][i] at
+// nf[i][r], i < r); the lower triangle is left intact.  The four diagonal 16x16
+// blocks are inverted by forward substitution (one column per lane); the
+// off-diagonal blocks follow by distance, Ahat_IJ = -Ahat_II sum_{K=J}^{I-1}
+// T_IK Ahat_KJ, as 16 x 8 x 8 tensor-core products in 3xTF32 (each fp32
+// operand split into a tf32 high part and a tf32 remainder; the three leading
+// products restore fp32 accuracy).  `ys` holds >= 6 * 16 * 9 floats of scratch.
+// Ends with __syncthreads().
 __device__ __forceinline__ float ahat_at(const float *nf, int ldn, int a, int b) {
   return a == b ? 1.f : (a > b ? nf[b * ldn + a] : 0.f);
+}
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(x));
+  return r;
+}
+// x ~ hi + lo, both tf32
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+  hi = to_tf32(x);
+  lo = to_tf32(x - __uint_as_float(hi));
+}
+__device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+// c += a * b with fp32 operands given as values: 3xTF32
+__device__ __forceinline__ void mma_3xtf32(float (&c)[4], const float (&a)[4], const float (&b)[2]) {
+  uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) split_tf32(a[i], ah[i], al[i]);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) split_tf32(b[i], bh[i], bl[i]);
+  mma_tf32(c, al, bh);
+  mma_tf32(c, ah, bl);
+  mma_tf32(c, ah, bh);
 }
 
 static __device__ __noinline__ void tril_inverse(float *nf, int ldn, const float *beta, float *ys) {
@@ -126,40 +157,61 @@ static __device__ __noinline__ void tril_inverse(float *nf, int ldn, const float
     float x[16];
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
-      float acc = (r == jj) ? 1.f : 0.f;
-      const float br = beta[b + r];
+      float s0 = 0.f, s1 = 0.f;  // two partial sums for instruction-level parallelism
 #pragma unroll
-      for (int i = 0; i < r; ++i) acc -= br * nf[(b + r) * ldn + b + i] * x[i];
-      x[r] = acc;
+      for (int i = 0; i < r; ++i) {
+        if (i & 1) s1 += nf[(b + r) * ldn + b + i] * x[i];
+        else s0 += nf[(b + r) * ldn + b + i] * x[i];
+      }
+      x[r] = ((r == jj) ? 1.f : 0.f) - beta[b + r] * (s0 + s1);
     }
 #pragma unroll
     for (int r = 1; r < 16; ++r)
       if (r > jj) nf[(b + jj) * ldn + b + r] = x[r];
   }
   __syncthreads();
+  const int gr = lane >> 2, gc = lane & 3;
   for (int d = 1; d <= 3; ++d) {
     const int nb = 4 - d;
-    for (int e = threadIdx.x; e < nb * 256; e += NTHREADS) {
-      const int bi = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+    if (warp < 2 * nb) {
+      const int bi = warp >> 1, nh = warp & 1;
       const int I = d + bi, J = I - d;
-      const int row = 16 * I + r, col = 16 * J + cc;
-      const float br = beta[row];
-      float acc = 0.f;
-      for (int kb = J; kb < I; ++kb) {
+      const int n0 = 16 * J + 8 * nh;  // global column of this 16 x 8 slice
+      const int ra = 16 * I + gr;
+      const float b0 = beta[ra], b1 = beta[ra + 8];
+      float y[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int K = J; K < I; ++K) {
 #pragma unroll
-        for (int t = 0; t < 16; ++t) acc += nf[row * ldn + 16 * kb + t] * ahat_at(nf, ldn, 16 * kb + t, col);
+        for (int ks = 0; ks < 2; ++ks) {
+          const int k0 = 16 * K + 8 * ks;
+          const float av[4] = {b0 * nf[ra * ldn + k0 + gc], b1 * nf[(ra + 8) * ldn + k0 + gc],
+                               b0 * nf[ra * ldn + k0 + gc + 4], b1 * nf[(ra + 8) * ldn + k0 + gc + 4]};
+          const float bv[2] = {ahat_at(nf, ldn, k0 + gc, n0 + gr), ahat_at(nf, ldn, k0 + gc + 4, n0 + gr)};
+          mma_3xtf32(y, av, bv);
+        }
       }
-      ys[e] = br * acc;
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < nb * 256; e += NTHREADS) {
-      const int bi = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-      const int I = d + bi, J = I - d;
-      float acc = 0.f;
+      float *Ys = ys + warp * 16 * 9;  // [16][9]
+      Ys[gr * 9 + 2 * gc] = y[0];
+      Ys[gr * 9 + 2 * gc + 1] = y[1];
+      Ys[(gr + 8) * 9 + 2 * gc] = y[2];
+      Ys[(gr + 8) * 9 + 2 * gc + 1] = y[3];
+      __syncwarp();
+      float x[4] = {0.f, 0.f, 0.f, 0.f};
+      const int rr = 16 * I;
 #pragma unroll
-      for (int t = 0; t < 16; ++t)
-        if (t <= r) acc += ahat_at(nf, ldn, 16 * I + r, 16 * I + t) * ys[(bi << 8) + (t << 4) + cc];
-      nf[(16 * J + cc) * ldn + 16 * I + r] = -acc;
+      for (int ks = 0; ks < 2; ++ks) {
+        const int kl = 8 * ks;
+        const float av[4] = {ahat_at(nf, ldn, rr + gr, rr + kl + gc), ahat_at(nf, ldn, rr + gr + 8, rr + kl + gc),
+                             ahat_at(nf, ldn, rr + gr, rr + kl + gc + 4),
+                             ahat_at(nf, ldn, rr + gr + 8, rr + kl + gc + 4)};
+        const float bv[2] = {Ys[(kl + gc) * 9 + gr], Ys[(kl + gc + 4) * 9 + gr]};
+        mma_3xtf32(x, av, bv);
+      }
+      const int R = 16 * I + gr, Cc = n0 + 2 * gc;
+      nf[Cc * ldn + R] = -x[0];
+      nf[(Cc + 1) * ldn + R] = -x[1];
+      nf[Cc * ldn + R + 8] = -x[2];
+      nf[(Cc + 1) * ldn + R + 8] = -x[3];
     }
     __syncthreads();
   }

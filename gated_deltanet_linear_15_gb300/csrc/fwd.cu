@@ -37,7 +37,7 @@ template <typename E, int D> struct FwdSmem {
   float nf[CH * LN];
   float g[CH], beta[CH];
   Gates gt;
-  float ys[768];
+  float ys[1024];
 };
 
 template <typename I, int D>

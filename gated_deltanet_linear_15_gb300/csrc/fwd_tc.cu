@@ -1,0 +1,517 @@
+// Blackwell-native fused forward (bf16 inputs, d = 128): TMA tile loads,
+// tcgen05.mma with every accumulator in tensor memory (TMEM), the recurrent
+// state resident in TMEM for the whole segment.
+//
+// Every chunk product is an M = 128 MMA with the feature dimension on the
+// TMEM lanes (transposed where that is what puts d = 128 on M):
+//   [K; Q] K^T     -> N = strict_tril(K K^T) (rows 0-63), Q K^T (rows 64-127)
+//   W^T = K^T X1^T, U^T = V^T X2^T      X1 = Ahat diag(beta), X2 = diag(gp) Ahat diag(beta rgp)
+//   Ut^T = U^T - S0 W^T (negated-A MMA accumulating on U^T),   O^T = S0 Qg^T
+//   S   = gam_C S0 + Ut^T Kc                Kc = diag(cdec) K (MN-major operand)
+//   O^T += Ut^T P^T                         P = diag(gp) tril_incl(Q K^T) diag(rgp)
+// with Qg = diag(gam) Q, W^T's columns scaled by gam at read-out, and
+// Ahat = (I + diag(beta) N)^{-1} computed on CUDA cores in fp32 (onedev.kr
+// FlashQLA talk summary, paragraph on the WY representation for the four
+// steps; paragraph on SFU load for pulling the diagonal gamma scaling out of
+// the inverse).  Operands are fp16 in 128-byte-swizzled shared memory (see
+// umma.cuh); the state is kept in fp32 in TMEM and copied to fp16 once per
+// chunk as the operand of the next products.
+//
+// One CTA of 256 threads per (segment, head); thread 0 issues TMA and MMA,
+// both warpgroups read TMEM (each covers lanes 0-127) and do the CUDA-core
+// work.  Inputs of chunk c+1 are loaded by TMA while chunk c is computed.
+#include "chunk_common.cuh"
+#include "kernels.h"
+#include "umma.cuh"
+
+namespace gdn {
+
+using namespace umma;
+
+namespace {
+
+constexpr int D = 128;
+constexpr int HT = 8192;  // one 64 x 64 fp16 half-tile, 128B-swizzled
+
+// TMEM columns
+constexpr uint32_t TM_S = 0, TM_KQ = 128, TM_W = 192, TM_U = 256, TM_O = 320, TM_COLS = 512;
+
+struct __align__(1024) TcSmem {
+  // input ring, 2 stages: [K0 | Q0 | K1 | Q1 | V0 | V1] half-tiles (0/1 = feature block)
+  uint8_t ring[2][6 * HT];
+  uint8_t kc[2 * HT];   // diag(cdec) K        (MN-major B operand: rows = token)
+  uint8_t qg[2 * HT];   // diag(gam) Q          (K-major B operand: rows = token)
+  uint8_t x1[HT], x2[HT], p[HT];
+  uint8_t wu[2 * HT];   // W^T (MN-major B, rows = d_k), later Ut^T (K-major A, rows = d_v)
+  uint8_t s0[4 * HT];   // S0 fp16 (K-major A: rows = d_v, two k-blocks of 128 rows)
+  float nf[CH * (CH + 4)];
+  float g[2][CH], beta[2][CH];  // per ring stage
+  Gates gt;
+  float ys[1024];
+  uint64_t bar_tma[2];
+  uint64_t bar_mma;
+  uint32_t tmem_base;
+};
+
+constexpr int LN = CH + 4;
+
+__device__ __forceinline__ uint32_t u32(const void *p) { return smem_u32(p); }
+
+// store 8 fp32 values as one 16-byte fp16 chunk
+__device__ __forceinline__ void st_chunk_f16(uint8_t *dst, const float *v) {
+  __half2 h[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+  *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<uint4 *>(h);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv) {
+  extern __shared__ unsigned char smraw[];
+  TcSmem &sm = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+
+  const int s = blockIdx.x, h = blockIdx.y, role = blockIdx.z;
+  const int H = a.H;
+  const int n = a.plan.seg_seq[s];
+  if (n < 0) return;
+  const int j = s - a.plan.seq_seg0[n], nseg = a.plan.seq_nseg[n];
+  const int len = a.plan.seq_len[n], chunk0 = a.plan.seq_chunk0[n];
+  const int bos = a.plan.seq_bos[n];
+  const int nchunks = (len + CH - 1) / CH;
+  const int cbeg = j * a.Lseg, cend = min(cbeg + a.Lseg, nchunks);
+  const bool window = !(a.flags & kFlagWindowOff);
+  int w = 0;
+  const int mode = fwd_start_mode(a.gsum, H, h, chunk0, cbeg, j, window, &w);
+  bool transition = false;
+  if (a.pass == 0) {
+    if (j >= nseg - 1) return;
+    int w2;
+    if (fwd_start_mode(a.gsum, H, h, chunk0, cend, j + 1, window, &w2) != START_FIXUP) return;
+    if (role == 1) {
+      if (mode != START_FIXUP) return;
+      transition = true;
+    }
+  } else if (role != 0) {
+    return;
+  }
+  const bool outputs = (a.pass == 1);
+  const bool states = (a.pass == 2);
+  const bool need_v = !transition;
+  const bool l2 = (a.flags & kFlagL2Norm) != 0;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int wg = warp >> 2;                      // warpgroup 0 / 1
+  const int row = ((warp & 3) << 5) | lane;      // TMEM lane this thread reads
+  const size_t DD = (size_t)D * D;
+  const size_t sh_idx = (size_t)s * H + h;
+  int cfirst = cbeg;
+  if (mode == START_WARMUP && !transition) cfirst = cbeg - w;
+
+  // ---------------------------------------------------------------- set-up
+  if (tid == 0) {
+    mbar_init(u32(&sm.bar_tma[0]), 1);
+    mbar_init(u32(&sm.bar_tma[1]), 1);
+    mbar_init(u32(&sm.bar_mma), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
+    tma_prefetch_desc(&tmq);
+  }
+  if (warp == 0) {
+    tmem_alloc(u32(&sm.tmem_base), TM_COLS);
+    tmem_relinquish();
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tm = sm.tmem_base;
+  const uint32_t tm_lane = (uint32_t)((warp & 3) * 32) << 16;
+
+  auto issue_tma = [&](int c, int stage) {
+    const int tok0 = bos + c * CH;
+    const bool wq = outputs && c >= cbeg;
+    const uint32_t bytes = (2 + (wq ? 2 : 0) + (need_v ? 2 : 0)) * HT;
+    const uint32_t bar = u32(&sm.bar_tma[stage]);
+    uint8_t *st = sm.ring[stage];
+    mbar_expect_tx(bar, bytes);
+    tma_load_3d(u32(st + 0 * HT), &tmk, 0, h, tok0, bar);
+    tma_load_3d(u32(st + 2 * HT), &tmk, 64, h, tok0, bar);
+    if (wq) {
+      tma_load_3d(u32(st + 1 * HT), &tmq, 0, h, tok0, bar);
+      tma_load_3d(u32(st + 3 * HT), &tmq, 64, h, tok0, bar);
+    }
+    if (need_v) {
+      tma_load_3d(u32(st + 4 * HT), &tmv, 0, h, tok0, bar);
+      tma_load_3d(u32(st + 5 * HT), &tmv, 64, h, tok0, bar);
+    }
+  };
+  auto issue_gb = [&](int c, int stage) {  // cp.async of g, beta for chunk c (threads 0-127)
+    const int tok0 = bos + c * CH;
+    const int nvalid = min(CH, len - c * CH);
+    load_scalars(sm.g[stage], a.g, H, h, tok0, nvalid, 0);
+    load_scalars(sm.beta[stage], a.beta, H, h, tok0, nvalid, 64);
+    cp_async_commit();
+  };
+  if (tid == 0 && cfirst < cend) issue_tma(cfirst, 0);
+  if (cfirst < cend) issue_gb(cfirst, 0);
+
+  // ---------------------------------------------------------------- initial state -> TMEM
+  {
+    const float *src = nullptr;
+    if (!transition) {
+      if (mode == START_INIT) src = a.S0 ? a.S0 + ((size_t)n * H + h) * DD : nullptr;
+      else if (mode == START_FIXUP && a.pass != 0) src = a.Sstart + sh_idx * DD;
+    }
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int c0 = wg * 64 + half * 32;
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int col = c0 + i;
+        v[i] = src ? src[(size_t)row * D + col] : (transition && col == row ? 1.f : 0.f);
+      }
+      tmem_st32(tm + tm_lane + TM_S + c0, v);
+    }
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+
+  int *err = a.status;
+  uint32_t mma_phase = 0;
+  bool failed = false;
+  auto mma_wait = [&]() {
+    const bool ok = mbar_wait(u32(&sm.bar_mma), mma_phase, err, 4);
+    mma_phase ^= 1;
+    fence_after();
+    return ok;
+  };
+
+  for (int c = cfirst; c < cend && !failed; ++c) {
+    const int it = c - cfirst;
+    const int stage = it & 1;
+    const bool emit = outputs && c >= cbeg;
+    const int tok0 = bos + c * CH;
+    const int nvalid = min(CH, len - c * CH);
+    uint8_t *st = sm.ring[stage];
+
+    float *gbeta = sm.beta[stage];
+    // g, beta of this chunk (issued one chunk ahead) must have landed before the next prefetch reuses cp.async
+    cp_async_wait_all();
+    // prefetch the next chunk into the other stage (its previous contents were consumed)
+    if (tid == 0 && c + 1 < cend) issue_tma(c + 1, stage ^ 1);
+    if (c + 1 < cend) issue_gb(c + 1, stage ^ 1);
+    const bool tma_ok = mbar_wait(u32(&sm.bar_tma[stage]), (it >> 1) & 1, err, 8);
+    if (__syncthreads_or(!tma_ok)) {
+      failed = true;
+      break;
+    }
+    if (warp == 0) {
+      if (gate_prefix(sm.g[stage], sm.gt) && lane == 0 && err) atomicOr(err, 1);
+    }
+    __syncthreads();
+
+    // ---- prep: bf16 -> fp16 in place, L2 norm of q/k rows, Kc = cdec*K, Qg = gam*Q; rows >= nvalid zeroed.
+    // One thread per half-row (64 features = one 128-byte swizzled row); the two halves of a row
+    // sit in adjacent lanes and combine their squared norms with one shuffle.
+    for (int task = tid; task < 3 * 2 * CH; task += NTHREADS) {
+      const int t = task >> 7;  // 0: K, 1: Q, 2: V
+      if (t == 1 && !emit) continue;
+      if (t == 2 && !need_v) continue;
+      const int r = (task >> 1) & 63, hb = task & 1;
+      uint8_t *rowp = st + (t == 0 ? 0 : t == 1 ? HT : 4 * HT) + hb * (t == 2 ? HT : 2 * HT) + r * 128;
+      float x[64];
+#pragma unroll
+      for (int chk = 0; chk < 8; ++chk) {
+        const uint4 raw = *reinterpret_cast<const uint4 *>(rowp + ((chk ^ (r & 7)) * 16));
+        const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(b2[i]);
+          x[chk * 8 + 2 * i] = f.x;
+          x[chk * 8 + 2 * i + 1] = f.y;
+        }
+      }
+      float mul = (t == 1) ? a.scale : 1.f;
+      if (l2 && t < 2) {
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) ss += x[i] * x[i];
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        mul = mul / sqrtf(ss + 1e-6f);
+      }
+      if (r >= nvalid) mul = 0.f;
+      const float sc2 = t == 0 ? sm.gt.cdec[r] : sm.gt.gam[r];
+      uint8_t *row2 = (t == 0 ? sm.kc : sm.qg) + hb * HT + r * 128;
+#pragma unroll
+      for (int chk = 0; chk < 8; ++chk) {
+        float y[8], z[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          y[i] = x[chk * 8 + i] * mul;
+          z[i] = y[i] * sc2;
+        }
+        const int off = (chk ^ (r & 7)) * 16;
+        st_chunk_f16(rowp + off, y);
+        if (t < 2) st_chunk_f16(row2 + off, z);
+      }
+    }
+    fence_async_smem();
+    __syncthreads();
+
+    // ---- MMA 1: [K; Q] K^T  (M = 128, N = 64, K = 128)
+    if (tid == 0) {
+      fence_after();
+      const uint32_t idesc = idesc_f16(128, 64, false, false);
+      const uint32_t base = u32(st);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t koff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
+        mma_f16(tm + TM_KQ, sdesc(base + koff, 16, 1024), sdesc(base + koff, 16, 1024), idesc, kk > 0);
+      }
+      mma_commit(u32(&sm.bar_mma));
+    }
+    __syncwarp();
+    if (__syncthreads_or(!mma_wait())) {
+      failed = true;
+      break;
+    }
+
+    // ---- read-out: N (fp32, rows 0-63) and P (fp16, rows 64-127); each warpgroup takes 32 columns
+    if (row < 64 || emit) {
+      float v[32];
+      const int c0 = wg * 32;
+      tmem_ld32(tm + tm_lane + TM_KQ + c0, v);
+      if (row < 64) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sm.nf[row * LN + c0 + i] = v[i];
+      } else {
+        const int r = row - 64;
+        const float gr = sm.gt.gp[r];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          float y[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int col = c0 + q4 * 8 + i;
+            y[i] = col <= r ? v[q4 * 8 + i] * gr * sm.gt.rgp[col] : 0.f;
+          }
+          const int chk = (c0 >> 3) + q4;
+          st_chunk_f16(sm.p + r * 128 + ((chk ^ (r & 7)) * 16), y);
+        }
+      }
+    }
+    fence_before();
+    __syncthreads();
+
+    // ---- Ahat (fp32, CUDA cores), then X1, X2 (fp16, K-major: rows = r)
+    tril_inverse(sm.nf, LN, gbeta, sm.ys);
+    for (int e = tid; e < CH * 8; e += NTHREADS) {
+      const int r = e & 63, chk = e >> 6;  // consecutive lanes: consecutive rows (conflict-free reads of Ahat^T)
+      float y1[8], y2[8];
+      const float gr = sm.gt.gp[r];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int col = chk * 8 + i;
+        const float ah = ahat_at(sm.nf, LN, r, col);
+        const float b = gbeta[col];
+        y1[i] = ah * b;
+        y2[i] = col <= r ? ah * b * (gr * sm.gt.rgp[col]) : 0.f;
+      }
+      const uint32_t off = r * 128 + ((chk ^ (r & 7)) * 16);
+      st_chunk_f16(sm.x1 + off, y1);
+      st_chunk_f16(sm.x2 + off, y2);
+    }
+    fence_async_smem();
+    __syncthreads();
+
+    // ---- MMA 2: W^T = K^T X1^T, U^T = V^T X2^T  (M = 128, N = 64, K = 64)
+    if (tid == 0) {
+      fence_after();
+      const uint32_t idesc = idesc_f16(128, 64, true, false);
+      const uint32_t kb = u32(st), vb = u32(st + 4 * HT), x1b = u32(sm.x1), x2b = u32(sm.x2);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        mma_f16(tm + TM_W, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(x1b + kk * 32, 16, 1024), idesc, kk > 0);
+      }
+      if (need_v) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f16(tm + TM_U, sdesc(vb + kk * 2048, HT, 1024), sdesc(x2b + kk * 32, 16, 1024), idesc, kk > 0);
+      }
+      mma_commit(u32(&sm.bar_mma));
+    }
+    __syncwarp();
+    // meanwhile: S0 -> fp16 operand copy, gam_C * S0 back into TMEM (state copy for the backward)
+    {
+      const float gC = sm.gt.gamC;
+      f16 *stg = states && c >= cbeg
+                     ? static_cast<f16 *>(a.states) + ((size_t)(chunk0 + c) * H + h) * DD + (size_t)row * D
+                     : nullptr;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int c0 = wg * 64 + half * 32;
+        float v[32];
+        tmem_ld32(tm + tm_lane + TM_S + c0, v);
+        const int kb = c0 >> 6;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int chk = ((c0 & 63) >> 3) + q4;
+          uint8_t *dst = sm.s0 + kb * 2 * HT + row * 128 + ((chk ^ (row & 7)) * 16);
+          st_chunk_f16(dst, v + q4 * 8);
+          if (stg) *reinterpret_cast<uint4 *>(stg + c0 + q4 * 8) = *reinterpret_cast<const uint4 *>(dst);
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= gC;
+        tmem_st32(tm + tm_lane + TM_S + c0, v);
+      }
+    }
+    if (__syncthreads_or(!mma_wait())) {
+      failed = true;
+      break;
+    }
+
+    // ---- W^T read-out: columns scaled by gam -> fp16 MN-major B (rows = d_k)
+    {
+      const int c0 = wg * 32;
+      float v[32];
+      tmem_ld32(tm + tm_lane + TM_W + c0, v);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float y[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) y[i] = v[q4 * 8 + i] * sm.gt.gam[c0 + q4 * 8 + i];
+        const int chk = (c0 >> 3) + q4;
+        st_chunk_f16(sm.wu + row * 128 + ((chk ^ (row & 7)) * 16), y);
+      }
+    }
+    fence_before();
+    fence_async_smem();
+    __syncthreads();
+
+    // ---- MMA 3: Ut^T = U^T - S0 W^T;  O^T = S0 Qg^T   (M = 128, N = 64, K = 128)
+    if (tid == 0) {
+      fence_after();
+      const uint32_t s0b = u32(sm.s0), wb = u32(sm.wu), qb = u32(sm.qg);
+      const uint32_t id_u = idesc_f16(128, 64, false, true, /*neg_a=*/true);
+      const uint32_t id_o = idesc_f16(128, 64, false, false);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
+        mma_f16(tm + TM_U, sdesc(s0b + aoff, 16, 1024), sdesc(wb + kk * 2048, 2 * HT, 1024), id_u,
+                need_v || kk > 0);
+      }
+      if (emit) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
+          const uint32_t boff = (kk >> 2) * HT + (kk & 3) * 32;
+          mma_f16(tm + TM_O, sdesc(s0b + aoff, 16, 1024), sdesc(qb + boff, 16, 1024), id_o, kk > 0);
+        }
+      }
+      mma_commit(u32(&sm.bar_mma));
+    }
+    __syncwarp();
+    if (__syncthreads_or(!mma_wait())) {
+      failed = true;
+      break;
+    }
+
+    // ---- Ut^T read-out -> fp16 K-major A (rows = d_v, k = token)
+    {
+      const int c0 = wg * 32;
+      float v[32];
+      tmem_ld32(tm + tm_lane + TM_U + c0, v);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int chk = (c0 >> 3) + q4;
+        st_chunk_f16(sm.wu + row * 128 + ((chk ^ (row & 7)) * 16), v + q4 * 8);
+      }
+    }
+    fence_before();
+    fence_async_smem();
+    __syncthreads();
+
+    // ---- MMA 4: S += Ut^T Kc (N = 128, K = 64);  O^T += Ut^T P^T (N = 64, K = 64)
+    if (tid == 0) {
+      fence_after();
+      const uint32_t ub = u32(sm.wu), kcb = u32(sm.kc), pb = u32(sm.p);
+      const uint32_t id_s = idesc_f16(128, 128, false, true);
+      const uint32_t id_o = idesc_f16(128, 64, false, false);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_f16(tm + TM_S, sdesc(ub + kk * 32, 16, 1024), sdesc(kcb + kk * 2048, HT, 1024), id_s, true);
+      if (emit) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f16(tm + TM_O, sdesc(ub + kk * 32, 16, 1024), sdesc(pb + kk * 32, 16, 1024), id_o, true);
+      }
+      mma_commit(u32(&sm.bar_mma));
+    }
+    __syncwarp();
+    if (__syncthreads_or(!mma_wait())) {
+      failed = true;
+      break;
+    }
+
+    // ---- O^T read-out -> bf16 [token][d_v] staging in qg (free now) -> coalesced rows of o
+    if (emit) {
+      const int c0 = wg * 32;
+      float v[32];
+      tmem_ld32(tm + tm_lane + TM_O + c0, v);
+      bf16 *stg = reinterpret_cast<bf16 *>(sm.qg);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) stg[(c0 + i) * D + row] = __float2bfloat16_rn(v[i]);
+    }
+    fence_before();
+    __syncthreads();
+    if (emit) {
+      const uint4 *stg = reinterpret_cast<const uint4 *>(sm.qg);
+      bf16 *og = static_cast<bf16 *>(a.o);
+      for (int e = tid; e < CH * (D / 8); e += NTHREADS) {
+        const int r = e >> 4, cc = e & 15;
+        if (r < nvalid) *reinterpret_cast<uint4 *>(og + ((size_t)(tok0 + r) * H + h) * D + cc * 8) = stg[e];
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- end-of-segment state
+  if (!failed) {
+    float *dst = nullptr;
+    if (a.pass == 0) dst = (transition ? a.Mbuf : a.Ebuf) + sh_idx * DD;
+    else if (j == nseg - 1 && a.ST) dst = a.ST + ((size_t)n * H + h) * DD;
+    if (dst) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int c0 = wg * 64 + half * 32;
+        float v[32];
+        tmem_ld32(tm + tm_lane + TM_S + c0, v);
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4)
+          *reinterpret_cast<float4 *>(dst + (size_t)row * D + c0 + 4 * q4) =
+              make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+      }
+    }
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp == 0) tmem_dealloc(tm, TM_COLS);
+}
+
+size_t fwd_tc_smem_bytes() { return sizeof(TcSmem) + 1024; }
+
+int launch_fwd_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, dim3 grid,
+                  cudaStream_t st) {
+  const size_t smem = fwd_tc_smem_bytes();
+  static_assert(sizeof(TcSmem) + 1024 <= 232448, "shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return (int)e;
+  fwd_tc_kernel<<<grid, NTHREADS, smem, st>>>(a, tq, tk, tv);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -1,5 +1,6 @@
 // Host-visible launch descriptors of the chunk kernels (internal to the library).
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 
@@ -59,6 +60,9 @@ int launch_plan(const Plan &p, const int *cu, int N, int T, int Lseg, int S_max,
 int launch_gate_scan(const Plan &p, const float *g, int H, int CH_max, float *gsum, int *status, cudaStream_t st);
 int launch_fixup(const FixupArgs &a, int N, cudaStream_t st);
 int launch_fwd_chunk(const FwdArgs &a, bool is_bf16, int D, dim3 grid, cudaStream_t st);
+// tcgen05 forward for bf16 inputs and d = 128; q, k, v tensor maps over [tokens, H, 128] with a 64 x 1 x 64 box
+int launch_fwd_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, dim3 grid,
+                  cudaStream_t st);
 int launch_bwd_chain(const BwdArgs &a, bool is_bf16, int D, dim3 grid, cudaStream_t st);
 int launch_bwd_local(const BwdArgs &a, bool is_bf16, int D, int CH_max, cudaStream_t st);
 
