@@ -295,6 +295,21 @@ int qkv_map(CUtensorMap *m, const void *ptr, long tokens, int H) {
   return GDN_OK;
 }
 
+// fp16 per-chunk states [rows, 128] (row-major), box = 64 columns x 128 rows, 128-byte swizzle
+int state_map(CUtensorMap *m, const void *ptr, long rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[3] = {128, (cuuint64_t)rows, 1};
+  cuuint64_t strides[2] = {128 * 2, (cuuint64_t)rows * 128 * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return GDN_OK;
+}
+
 // The chunk forward kernel for this problem: tcgen05 for bf16 with d = 128, the
 // mma.sync/CUDA-core kernel otherwise (d = 64, fp32 inputs, empty batches).
 int launch_forward_kernel(const Layout &L, const gdn_shape *s, const FwdArgs &fa, dim3 grid, cudaStream_t st) {
@@ -546,7 +561,17 @@ int gdn_chunk_bwd(const gdn_shape *s, const void *q, const void *k, const void *
   // 3. local gradients, every (chunk, head) in parallel
   {
     PROF("bwd_local");
-    CK(launch_bwd_local(ba, bf, L.D, L.CH_max, st));
+    if (bf && L.D == 128 && L.Ttot > 0) {
+      CUtensorMap maps[6];
+      if ((rc = qkv_map(&maps[0], q, L.Ttot, L.H)) || (rc = qkv_map(&maps[1], k, L.Ttot, L.H)) ||
+          (rc = qkv_map(&maps[2], v, L.Ttot, L.H)) || (rc = qkv_map(&maps[3], dO, L.Ttot, L.H)) ||
+          (rc = state_map(&maps[4], ws + L.off_states, (long)L.CH_max * L.H * 128)) ||
+          (rc = state_map(&maps[5], ws + L.off_dstates, (long)L.CH_max * L.H * 128)))
+        return rc;
+      CK(launch_bwd_local_tc(ba, maps, L.CH_max, st));
+    } else {
+      CK(launch_bwd_local(ba, bf, L.D, L.CH_max, st));
+    }
   }
   return GDN_OK;
 }

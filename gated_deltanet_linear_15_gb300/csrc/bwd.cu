@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_chain_kernel(BwdArgs a) {
       }
     }
     __syncthreads();
-    tril_inverse(sm.nf, LN, sm.beta, sm.ys);
+    tril_inverse<std::is_same<E, float>::value>(sm.nf, LN, sm.beta, sm.ys);
     for (int e = threadIdx.x; e < CH * CH; e += NTHREADS) {
       const int r = e / CH, i = e % CH;
       sm.x1[r * LC + i] = fromf<E>(ahat_at(sm.nf, LN, r, i) * sm.beta[i]);
@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_local_kernel(BwdArgs a) {
     }
   }
   __syncthreads();
-  tril_inverse(sm.nf, LN, sm.beta, sm.ys);
+  tril_inverse<std::is_same<E, float>::value>(sm.nf, LN, sm.beta, sm.ys);
   for (int e = threadIdx.x; e < CH * CH; e += NTHREADS) {
     const int r = e / CH, i = e % CH;
     const float ah = ahat_at(sm.nf, LN, r, i);

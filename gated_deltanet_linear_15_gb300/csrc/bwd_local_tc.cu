@@ -1,0 +1,738 @@
+// Blackwell-native local-gradient kernel of the chunked backward (bf16 inputs,
+// d = 128): one CTA per (chunk, head), given the forward state S0 at the chunk
+// start and dS at its end (fp16, from the two serial passes).  Every product
+// is a tcgen05 MMA with fp32 accumulation in TMEM; the 64 x 64 products use
+// M = 128 with the upper 64 rows unused.  The algebra is the hand-derived
+// chunk backward (see bwd.cu); the WY part forms dA and dA^T as one symmetric
+// matrix multiplied with K once (onedev.kr FlashQLA talk summary, paragraph on
+// SFU load, last sentence).
+//
+// Rounds (MMA group -> read-out), TMEM regions T0..T7 of 64 columns:
+//   P1 [K;Q]K^T->T0          R1: N (fp32), P;  inverse; X1, X2, Ahat (fp16)
+//   P2 W^T->T1, U^T->T2      R2: W^T (gam-scaled columns)
+//   P3 Ut^T = U^T - S0 W^T   R3: Ut^T
+//   P4 Y = dS K^T->T3, Z = dO^T P->T4, Qa = S0^T dO^T->T5
+//                            R4: dUt^T = cdec*Y + Z; sums <Ut,Y>, <dUt,Ut>
+//   P5 dP = dO Ut^T->T0, dW'^T = -S0^T dUt^T->T1, dV^T = dUt^T X2->T6
+//                            R5: dPm (over P), dP*P sums; dW'^T tile; dv out, <dV,v>
+//   P6 Qb = K^T dPm^T->T7, M1 = dW' K^T->T3, M2 = dUt V^T->T4
+//                            R6: dq out (+ <dQ1,q>); dAhat tile, beta column sums
+//   P7 Y1 = Ahat^T dAhat->T0 R7: Y1 tile
+//   P8 dT = -Y1 Ahat^T->T1   R8: Sigma = dN + dN^T tile, beta row sums
+//   P9 Ka = Q^T dPm + dW'^T X1 + K^T Sigma->T3, Kb = dS^T Ut^T->T4
+//                            R9: dk out;  dg (reverse cumsum), dbeta
+#include "chunk_common.cuh"
+#include "kernels.h"
+#include "umma.cuh"
+
+namespace gdn {
+
+using namespace umma;
+
+namespace {
+
+constexpr int D = 128;
+constexpr int HT = 8192;
+constexpr int LN = CH + 4;
+constexpr uint32_t T0 = 0, T1 = 64, T2 = 128, T3 = 192, T4 = 256, T5 = 320, T6 = 384, T7 = 448;
+
+struct __align__(1024) LocalTcSmem {
+  uint8_t kq[4 * HT];   // [K0 | Q0 | K1 | Q1] half-tiles (feature blocks 0/1), rows = token
+  uint8_t v[2 * HT];    // V, later Y1 (first half) and Sigma (second half)
+  uint8_t dob[2 * HT];  // dO, later output staging (bf16 [token][128])
+  uint8_t s0[4 * HT];   // S0 [k-block][128 rows = d_v][64], later dW'^T [d_k][token]
+  uint8_t ds[4 * HT];   // dS, same layout
+  uint8_t p[HT];        // P, then dPm (in place)
+  uint8_t x1[HT];
+  uint8_t x2[HT];       // X2, later dAhat
+  uint8_t ah[HT];       // Ahat (fp16)
+  uint8_t wt[2 * HT];   // W^T [d_k][token], later dUt^T [d_v][token]
+  uint8_t ut[2 * HT];   // Ut^T [d_v][token]
+  float nf[CH * LN];
+  float g[CH], beta[CH], nq[CH], nk[CH];  // nq, nk hold reciprocal norms
+  Gates gt;
+  float ys[1024];
+  float part[16][CH];   // per-token partial sums (4 warps x 4 kinds, reused per round)
+  float acc[12][CH];    // assembled per-token terms
+  float red[NWARPS];
+  uint64_t bar_tma, bar_mma;
+  uint32_t tmem_base;
+};
+
+__device__ __forceinline__ uint32_t u32(const void *p) { return smem_u32(p); }
+
+__device__ __forceinline__ void st_chunk_f16(uint8_t *dst, const float *v) {
+  __half2 h[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+  *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<uint4 *>(h);
+}
+// fp16 element (row, col) of a [rows][64]-per-half-tile swizzled operand whose
+// feature blocks sit `blk` bytes apart
+__device__ __forceinline__ float ld_f16(const uint8_t *t, int row, int col, int blk) {
+  const uint8_t *p = t + (col >> 6) * blk + sw128_offset(row, col & 63);
+  return __half2float(*reinterpret_cast<const __half *>(p));
+}
+__device__ __forceinline__ void st_f16(uint8_t *t, int row, int col, int blk, float x) {
+  *reinterpret_cast<__half *>(t + (col >> 6) * blk + sw128_offset(row, col & 63)) = __float2half_rn(x);
+}
+
+// v[32] per lane (one lane per feature) -> lane l holds the sum over the warp's
+// lanes of v[l] (transpose-reduce, 31 shuffles)
+__device__ __forceinline__ float colsum32(float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+#pragma unroll
+    for (int i = 0; i < s; ++i) {
+      const bool up = (lane & s) != 0;
+      const float send = up ? v[i] : v[i + s];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, s);
+      v[i] = (up ? v[i + s] : v[i]) + recv;
+    }
+  }
+  return v[0];
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    bwd_local_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                        const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
+                        const __grid_constant__ CUtensorMap tms0, const __grid_constant__ CUtensorMap tmds) {
+  extern __shared__ unsigned char smraw[];
+  LocalTcSmem &sm =
+      *reinterpret_cast<LocalTcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+  const int gc = blockIdx.x, h = blockIdx.y;
+  const int H = a.H;
+  const int n = a.plan.chunk_seq[gc];
+  if (n < 0) return;
+  const int lc = gc - a.plan.seq_chunk0[n];
+  const int len = a.plan.seq_len[n];
+  const int tok0 = a.plan.seq_bos[n] + lc * CH;
+  const int nvalid = min(CH, len - lc * CH);
+  const bool l2 = (a.flags & kFlagL2Norm) != 0;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int wg = warp >> 2, wq = warp & 3;
+  const int row = (wq << 5) | lane;  // TMEM lane of this thread
+  const int c0 = wg * 32;            // this warpgroup's 32 columns of a 64-column region
+  int *err = a.status;
+
+  if (tid == 0) {
+    mbar_init(u32(&sm.bar_tma), 1);
+    mbar_init(u32(&sm.bar_mma), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if (warp == 0) {
+    tmem_alloc(u32(&sm.tmem_base), 512);
+    tmem_relinquish();
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tm = sm.tmem_base;
+  const uint32_t tl = (uint32_t)(wq * 32) << 16;
+
+  // ---- loads: TMA for the six tiles, plain loads for g, beta
+  if (tid == 0) {
+    const uint32_t bar = u32(&sm.bar_tma);
+    mbar_expect_tx(bar, 16 * HT);
+    tma_load_3d(u32(sm.kq + 0 * HT), &tmk, 0, h, tok0, bar);
+    tma_load_3d(u32(sm.kq + 2 * HT), &tmk, 64, h, tok0, bar);
+    tma_load_3d(u32(sm.kq + 1 * HT), &tmq, 0, h, tok0, bar);
+    tma_load_3d(u32(sm.kq + 3 * HT), &tmq, 64, h, tok0, bar);
+    tma_load_3d(u32(sm.v), &tmv, 0, h, tok0, bar);
+    tma_load_3d(u32(sm.v + HT), &tmv, 64, h, tok0, bar);
+    tma_load_3d(u32(sm.dob), &tmdo, 0, h, tok0, bar);
+    tma_load_3d(u32(sm.dob + HT), &tmdo, 64, h, tok0, bar);
+    const int srow = (gc * H + h) * D;
+    tma_load_3d(u32(sm.s0), &tms0, 0, srow, 0, bar);
+    tma_load_3d(u32(sm.s0 + 2 * HT), &tms0, 64, srow, 0, bar);
+    tma_load_3d(u32(sm.ds), &tmds, 0, srow, 0, bar);
+    tma_load_3d(u32(sm.ds + 2 * HT), &tmds, 64, srow, 0, bar);
+  }
+  if (tid < 64) sm.g[tid] = tid < nvalid ? a.g[(size_t)(tok0 + tid) * H + h] : 0.f;
+  else if (tid < 128) sm.beta[tid - 64] = (tid - 64) < nvalid ? a.beta[(size_t)(tok0 + tid - 64) * H + h] : 0.f;
+  bool ok = mbar_wait(u32(&sm.bar_tma), 0, err, 8);
+  uint32_t phase = 0;
+  auto mma_done = [&]() {
+    const bool r = mbar_wait(u32(&sm.bar_mma), phase, err, 4);
+    phase ^= 1;
+    fence_after();
+    return r;
+  };
+  if (__syncthreads_or(!ok)) goto out;
+  if (warp == 0) gate_prefix(sm.g, sm.gt);
+  {  // <dS, S0> over the whole state (both tiles share one layout, so compare byte positions)
+    float acc = 0.f;
+    const uint4 *A4 = reinterpret_cast<const uint4 *>(sm.s0), *B4 = reinterpret_cast<const uint4 *>(sm.ds);
+    for (int e = tid; e < 4 * HT / 16; e += NTHREADS) {
+      const uint4 x = A4[e], y = B4[e];
+      const __half2 *xh = reinterpret_cast<const __half2 *>(&x), *yh = reinterpret_cast<const __half2 *>(&y);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 fx = __half22float2(xh[i]), fy = __half22float2(yh[i]);
+        acc += fx.x * fy.x + fx.y * fy.y;
+      }
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) sm.red[warp] = acc;
+  }
+
+  // ---- prep: bf16 -> fp16 in place; q, k normalised (norms kept for the Jacobians); rows >= nvalid zero
+  for (int task = tid; task < 4 * 2 * CH; task += NTHREADS) {
+    const int t = task >> 7;  // 0 K, 1 Q, 2 V, 3 dO
+    const int r = (task >> 1) & 63, hb = task & 1;
+    uint8_t *rowp = (t == 0 ? sm.kq : t == 1 ? sm.kq + HT : t == 2 ? sm.v : sm.dob) +
+                    hb * (t < 2 ? 2 * HT : HT) + r * 128;
+    float x[64];
+#pragma unroll
+    for (int chk = 0; chk < 8; ++chk) {
+      const uint4 raw = *reinterpret_cast<const uint4 *>(rowp + ((chk ^ (r & 7)) * 16));
+      const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(b2[i]);
+        x[chk * 8 + 2 * i] = f.x;
+        x[chk * 8 + 2 * i + 1] = f.y;
+      }
+    }
+    float mul = (t == 1) ? a.scale : 1.f;
+    if (l2 && t < 2) {
+      float ss = 0.f;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) ss += x[i] * x[i];
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      const float rn = 1.f / sqrtf(ss + 1e-6f);
+      mul = mul * rn;
+      if (hb == 0) (t == 0 ? sm.nk : sm.nq)[r] = rn;
+    }
+    if (r >= nvalid) mul = 0.f;
+#pragma unroll
+    for (int chk = 0; chk < 8; ++chk) {
+      float y[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) y[i] = x[chk * 8 + i] * mul;
+      st_chunk_f16(rowp + ((chk ^ (r & 7)) * 16), y);
+    }
+  }
+  fence_async_smem();
+  __syncthreads();
+
+  // ---- P1: [K; Q] K^T -> T0
+  if (tid == 0) {
+    fence_after();
+    const uint32_t id = idesc_f16(128, 64, false, false), kb = u32(sm.kq);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint32_t off = (kk >> 2) * 2 * HT + (kk & 3) * 32;
+      mma_f16(tm + T0, sdesc(kb + off, 16, 1024), sdesc(kb + off, 16, 1024), id, kk > 0);
+    }
+    mma_commit(u32(&sm.bar_mma));
+  }
+  __syncwarp();
+  if (__syncthreads_or(!mma_done())) goto out;
+  // R1: rows 0-63 -> N (fp32), rows 64-127 -> P (fp16, [r][i])
+  {
+    float v[32];
+    tmem_ld32(tm + tl + T0 + c0, v);
+    if (row < 64) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) sm.nf[row * LN + c0 + i] = v[i];
+    } else {
+      const int r = row - 64;
+      const float gr = sm.gt.gp[r];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float y[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int col = c0 + q4 * 8 + i;
+          y[i] = col <= r ? v[q4 * 8 + i] * gr * sm.gt.rgp[col] : 0.f;
+        }
+        st_chunk_f16(sm.p + r * 128 + ((((c0 >> 3) + q4) ^ (r & 7)) * 16), y);
+      }
+    }
+  }
+  fence_before();
+  __syncthreads();
+  tril_inverse<false>(sm.nf, LN, sm.beta, sm.ys);
+  for (int e = tid; e < CH * 8; e += NTHREADS) {
+    const int r = e & 63, chk = e >> 6;
+    float y1[8], y2[8], y3[8];
+    const float gr = sm.gt.gp[r];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int col = chk * 8 + i;
+      const float ah = ahat_at(sm.nf, LN, r, col);
+      const float b = sm.beta[col];
+      y1[i] = ah * b;
+      y2[i] = col <= r ? ah * b * (gr * sm.gt.rgp[col]) : 0.f;
+      y3[i] = ah;
+    }
+    const uint32_t off = r * 128 + ((chk ^ (r & 7)) * 16);
+    st_chunk_f16(sm.x1 + off, y1);
+    st_chunk_f16(sm.x2 + off, y2);
+    st_chunk_f16(sm.ah + off, y3);
+  }
+  fence_async_smem();
+  __syncthreads();
+
+  // ---- P2: W^T = K^T X1^T -> T1;  U^T = V^T X2^T -> T2
+  if (tid == 0) {
+    fence_after();
+    const uint32_t id = idesc_f16(128, 64, true, false);
+    const uint32_t kb = u32(sm.kq), vb = u32(sm.v), x1b = u32(sm.x1), x2b = u32(sm.x2);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      mma_f16(tm + T1, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(x1b + kk * 32, 16, 1024), id, kk > 0);
+      mma_f16(tm + T2, sdesc(vb + kk * 2048, HT, 1024), sdesc(x2b + kk * 32, 16, 1024), id, kk > 0);
+    }
+    mma_commit(u32(&sm.bar_mma));
+  }
+  __syncwarp();
+  if (__syncthreads_or(!mma_done())) goto out;
+  {  // R2: W^T (lanes d_k, columns token) * gam -> wt
+    float v[32];
+    tmem_ld32(tm + tl + T1 + c0, v);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      float y[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) y[i] = v[q4 * 8 + i] * sm.gt.gam[c0 + q4 * 8 + i];
+      st_chunk_f16(sm.wt + row * 128 + ((((c0 >> 3) + q4) ^ (row & 7)) * 16), y);
+    }
+  }
+  fence_before();
+  fence_async_smem();
+  __syncthreads();
+
+  // ---- P3: Ut^T = U^T - S0 W^T  (T2)
+  if (tid == 0) {
+    fence_after();
+    const uint32_t id = idesc_f16(128, 64, false, true, true);
+    const uint32_t sb = u32(sm.s0), wb = u32(sm.wt);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      mma_f16(tm + T2, sdesc(sb + (kk >> 2) * 2 * HT + (kk & 3) * 32, 16, 1024), sdesc(wb + kk * 2048, 2 * HT, 1024),
+              id, true);
+    mma_commit(u32(&sm.bar_mma));
+  }
+  __syncwarp();
+  if (__syncthreads_or(!mma_done())) goto out;
+  {  // R3: Ut^T -> ut
+    float v[32];
+    tmem_ld32(tm + tl + T2 + c0, v);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4)
+      st_chunk_f16(sm.ut + row * 128 + ((((c0 >> 3) + q4) ^ (row & 7)) * 16), v + q4 * 8);
+  }
+  fence_before();
+  fence_async_smem();
+  __syncthreads();
+
+  // ---- P4: Y = dS K^T -> T3; Z = dO^T P -> T4; Qa = S0^T dO^T -> T5
+  if (tid == 0) {
+    fence_after();
+    const uint32_t id_kk = idesc_f16(128, 64, false, false);
+    const uint32_t id_mm = idesc_f16(128, 64, true, true);
+    const uint32_t id_mk = idesc_f16(128, 64, true, false);
+    const uint32_t dsb = u32(sm.ds), kb = u32(sm.kq), dob = u32(sm.dob), pb = u32(sm.p), sb = u32(sm.s0);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
+      mma_f16(tm + T3, sdesc(dsb + aoff, 16, 1024), sdesc(kb + aoff, 16, 1024), id_kk, kk > 0);
+      mma_f16(tm + T5, sdesc(sb + kk * 2048, 2 * HT, 1024), sdesc(dob + (kk >> 2) * HT + (kk & 3) * 32, 16, 1024),
+              id_mk, kk > 0);
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_f16(tm + T4, sdesc(dob + kk * 2048, HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id_mm, kk > 0);
+    mma_commit(u32(&sm.bar_mma));
+  }
+  __syncwarp();
+  if (__syncthreads_or(!mma_done())) goto out;
+  {  // R4: dUt^T = cdec*Y + Z -> wt (W^T is dead);  per-token sums <Ut, Y>, <dUt, Ut> over d_v
+    float y[32], z[32], u[32];
+    tmem_ld32(tm + tl + T3 + c0, y);
+    tmem_ld32(tm + tl + T4 + c0, z);
+    tmem_ld32(tm + tl + T2 + c0, u);
+    float s1[32], s2[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float du = sm.gt.cdec[c0 + i] * y[i] + z[i];
+      s1[i] = u[i] * y[i];
+      s2[i] = du * u[i];
+      z[i] = du;
+    }
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4)
+      st_chunk_f16(sm.wt + row * 128 + ((((c0 >> 3) + q4) ^ (row & 7)) * 16), z + q4 * 8);
+    const float t1 = colsum32(s1), t2 = colsum32(s2);
+    sm.part[wq][c0 + lane] = t1;
+    sm.part[4 + wq][c0 + lane] = t2;
+  }
+  fence_before();
+  fence_async_smem();
+  __syncthreads();
+  if (tid < 64) {
+    sm.acc[0][tid] = sm.part[0][tid] + sm.part[1][tid] + sm.part[2][tid] + sm.part[3][tid];  // <Ut, Y>
+    sm.acc[1][tid] = sm.part[4][tid] + sm.part[5][tid] + sm.part[6][tid] + sm.part[7][tid];  // <dUt, Ut>
+  }
+
+  // ---- P5: dP = dO Ut^T -> T0; dW'^T = -S0^T dUt^T -> T1; dV^T = dUt^T X2 -> T6
+  if (tid == 0) {
+    fence_after();
+    const uint32_t id_kmn = idesc_f16(128, 64, false, true);
+    const uint32_t id_mmn_neg = idesc_f16(128, 64, true, true, true);
+    const uint32_t dob = u32(sm.dob), ub = u32(sm.ut), sb = u32(sm.s0), dub = u32(sm.wt), x2b = u32(sm.x2);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      mma_f16(tm + T0, sdesc(dob + (kk >> 2) * HT + (kk & 3) * 32, 16, 1024), sdesc(ub + kk * 2048, 2 * HT, 1024),
+              id_kmn, kk > 0);
+      mma_f16(tm + T1, sdesc(sb + kk * 2048, 2 * HT, 1024), sdesc(dub + kk * 2048, 2 * HT, 1024), id_mmn_neg,
+              kk > 0);
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_f16(tm + T6, sdesc(dub + kk * 32, 16, 1024), sdesc(x2b + kk * 2048, HT, 1024), id_kmn, kk > 0);
+    mma_commit(u32(&sm.bar_mma));
+  }
+  __syncwarp();
+  if (__syncthreads_or(!mma_done())) goto out;
+  {
+    // dP rows (lanes 0-63): Z = dP * P row sums (thread-local) and column sums; dPm over P
+    if (row < 64) {
+      float v[32], zc[32];
+      tmem_ld32(tm + tl + T0 + c0, v);
+      const int r = row;
+      const float gr = sm.gt.gp[r];
+      float rs = 0.f;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint8_t *pp = sm.p + r * 128 + ((((c0 >> 3) + q4) ^ (r & 7)) * 16);
+        const uint4 raw = *reinterpret_cast<const uint4 *>(pp);
+        const __half *ph = reinterpret_cast<const __half *>(&raw);
+        float y[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int col = c0 + q4 * 8 + i;
+          const float dpv = v[q4 * 8 + i];
+          const float zz = dpv * __half2float(ph[i]);
+          rs += zz;
+          zc[q4 * 8 + i] = zz;
+          y[i] = col <= r ? dpv * gr * sm.gt.rgp[col] : 0.f;
+        }
+        st_chunk_f16(pp, y);
+      }
+      sm.part[8 + wg][r] = rs;  // row sums of Z, per column half
+      const float cs = colsum32(zc);
+      sm.part[10 + wq][c0 + lane] = cs;  // column sums of Z, per row quarter (wq 0/1)
+    }
+    // dW'^T (lanes d_k) * gam -> s0 region (S0 is dead)
+    {
+      float v[32];
+      tmem_ld32(tm + tl + T1 + c0, v);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float y[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) y[i] = v[q4 * 8 + i] * sm.gt.gam[c0 + q4 * 8 + i];
+        st_chunk_f16(sm.s0 + row * 128 + ((((c0 >> 3) + q4) ^ (row & 7)) * 16), y);
+      }
+    }
+    // dV^T (lanes d_v, columns token): stage bf16 dv[token][d_v] in dob (dO is dead); <dV, v>
+    {
+      float v[32];
+      tmem_ld32(tm + tl + T6 + c0, v);
+      bf16 *stg = reinterpret_cast<bf16 *>(sm.dob);
+      float sv[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int tkn = c0 + i;
+        stg[tkn * D + row] = __float2bfloat16_rn(v[i]);
+        sv[i] = v[i] * ld_f16(sm.v, tkn, row, HT);
+      }
+      const float t = colsum32(sv);
+      sm.part[12 + wq][c0 + lane] = t;
+    }
+  }
+  fence_before();
+  fence_async_smem();
+  __syncthreads();
+  {
+    bf16 *dvg = static_cast<bf16 *>(a.dv);
+    const uint4 *stg = reinterpret_cast<const uint4 *>(sm.dob);
+    for (int e = tid; e < CH * (D / 8); e += NTHREADS) {
+      const int r = e >> 4, cc = e & 15;
+      if (r < nvalid) *reinterpret_cast<uint4 *>(dvg + ((size_t)(tok0 + r) * H + h) * D + cc * 8) = stg[e];
+    }
+    if (tid < 64) {
+      sm.acc[2][tid] = sm.part[8][tid] + sm.part[9][tid];    // row sums of dP * P
+      sm.acc[3][tid] = sm.part[10][tid] + sm.part[11][tid];  // column sums of dP * P
+      sm.acc[4][tid] = sm.part[12][tid] + sm.part[13][tid] + sm.part[14][tid] + sm.part[15][tid];  // <dV, v>
+    }
+  }
+  __syncthreads();
+
+  // ---- P6: Qb = K^T dPm^T -> T7;  M1 = dW' K^T -> T3;  M2 = dUt V^T -> T4
+  if (tid == 0) {
+    fence_after();
+    const uint32_t id_mk = idesc_f16(128, 64, true, false);
+    const uint32_t kb = u32(sm.kq), pb = u32(sm.p), dwb = u32(sm.s0), dub = u32(sm.wt), vb = u32(sm.v);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_f16(tm + T7, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(pb + kk * 32, 16, 1024), id_mk, kk > 0);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint32_t boff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
+      mma_f16(tm + T3, sdesc(dwb + kk * 2048, 2 * HT, 1024), sdesc(kb + boff, 16, 1024), id_mk, kk > 0);
+      mma_f16(tm + T4, sdesc(dub + kk * 2048, 2 * HT, 1024), sdesc(vb + (kk >> 2) * HT + (kk & 3) * 32, 16, 1024),
+              id_mk, kk > 0);
+    }
+    mma_commit(u32(&sm.bar_mma));
+  }
+  __syncwarp();
+  if (__syncthreads_or(!mma_done())) goto out;
+  {
+    // dq^T = gam*Qa + Qb (lanes d_k): <dQ1, q^> and Jacobian dots over d_k; stage dq^ (fp32 kept in regs)
+    float qa[32], qb[32], s1[32], s2[32], qv[32];
+    tmem_ld32(tm + tl + T5 + c0, qa);
+    tmem_ld32(tm + tl + T7 + c0, qb);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int tkn = c0 + i;
+      qv[i] = ld_f16(sm.kq + HT, tkn, row, 2 * HT);
+      const float a1 = sm.gt.gam[tkn] * qa[i];
+      qb[i] += a1;  // dq^ (w.r.t. the normalised, scaled q)
+      s1[i] = a1 * qv[i];
+      s2[i] = qb[i] * qv[i];
+    }
+    const float t1 = colsum32(s1), t2 = colsum32(s2);
+    sm.part[wq][c0 + lane] = t1;
+    sm.part[4 + wq][c0 + lane] = t2;
+    // M1, M2 (lanes 0-63 = r): dAhat = beta_i (M1 + Gamma M2); beta column sums colsum_i(Ahat (M1 + Gamma M2))
+    if (row < 64) {
+      float m1[32], m2[32];
+      tmem_ld32(tm + tl + T3 + c0, m1);
+      tmem_ld32(tm + tl + T4 + c0, m2);
+      const int r = row;
+      const float gr = sm.gt.gp[r];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int col = c0 + i;
+        const float x = m1[i] + (col <= r ? m2[i] * gr * sm.gt.rgp[col] : 0.f);
+        const float ahv = ahat_at(sm.nf, LN, r, col);
+        m2[i] = ahv * x;
+        m1[i] = sm.beta[col] * x;
+      }
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+        st_chunk_f16(sm.x2 + r * 128 + ((((c0 >> 3) + q4) ^ (r & 7)) * 16), m1 + q4 * 8);
+      const float cs = colsum32(m2);
+      sm.part[8 + wq][c0 + lane] = cs;
+    }
+    __syncthreads();
+    // dq raw = (scale dq^ - q^ (q^ . dq^) / scale) / |q|   (or scale dq^ without normalisation)
+    bf16 *stg = reinterpret_cast<bf16 *>(sm.dob);
+    const float rscale = 1.f / a.scale;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int tkn = c0 + i;
+      float o;
+      if (l2) {
+        const float dot = sm.part[4][tkn] + sm.part[5][tkn] + sm.part[6][tkn] + sm.part[7][tkn];
+        o = (a.scale * qb[i] - qv[i] * dot * rscale) * sm.nq[tkn];
+      } else {
+        o = a.scale * qb[i];
+      }
+      stg[tkn * D + row] = __float2bfloat16_rn(o);
+    }
+  }
+  fence_before();
+  fence_async_smem();
+  __syncthreads();
+  {
+    bf16 *dqg = static_cast<bf16 *>(a.dq);
+    const uint4 *stg = reinterpret_cast<const uint4 *>(sm.dob);
+    for (int e = tid; e < CH * (D / 8); e += NTHREADS) {
+      const int r = e >> 4, cc = e & 15;
+      if (r < nvalid) *reinterpret_cast<uint4 *>(dqg + ((size_t)(tok0 + r) * H + h) * D + cc * 8) = stg[e];
+    }
+    if (tid < 64) {
+      sm.acc[5][tid] = sm.part[0][tid] + sm.part[1][tid] + sm.part[2][tid] + sm.part[3][tid];  // gam <dO S0, q>
+      sm.acc[6][tid] = sm.part[8][tid] + sm.part[9][tid];                                      // beta col terms
+    }
+  }
+  __syncthreads();
+
+  // ---- P7: Y1 = Ahat^T dAhat -> T0
+  if (tid == 0) {
+    fence_after();
+    const uint32_t id = idesc_f16(128, 64, true, true);
+    const uint32_t ab = u32(sm.ah), dab = u32(sm.x2);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_f16(tm + T0, sdesc(ab + kk * 2048, HT, 1024), sdesc(dab + kk * 2048, HT, 1024), id, kk > 0);
+    mma_commit(u32(&sm.bar_mma));
+  }
+  __syncwarp();
+  if (__syncthreads_or(!mma_done())) goto out;
+  if (row < 64) {  // R7: Y1 -> v (first half; V is dead)
+    float v[32];
+    tmem_ld32(tm + tl + T0 + c0, v);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4)
+      st_chunk_f16(sm.v + row * 128 + ((((c0 >> 3) + q4) ^ (row & 7)) * 16), v + q4 * 8);
+  }
+  fence_before();
+  fence_async_smem();
+  __syncthreads();
+
+  // ---- P8: dT = -Y1 Ahat^T -> T1
+  if (tid == 0) {
+    fence_after();
+    const uint32_t id = idesc_f16(128, 64, false, false, true);
+    const uint32_t yb = u32(sm.v), ab = u32(sm.ah);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) mma_f16(tm + T1, sdesc(yb + kk * 32, 16, 1024), sdesc(ab + kk * 32, 16, 1024), id, kk > 0);
+    mma_commit(u32(&sm.bar_mma));
+  }
+  __syncwarp();
+  if (__syncthreads_or(!mma_done())) goto out;
+  if (row < 64) {  // R8: Sigma[r][i] = Sigma[i][r] = beta_r dT_ri (i < r), 0 on the diagonal; beta row sums
+    float v[32];
+    tmem_ld32(tm + tl + T1 + c0, v);
+    const int r = row;
+    const float br = sm.beta[r];
+    uint8_t *sg = sm.v + HT;
+    float rb = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int col = c0 + i;
+      if (col < r) {
+        rb += v[i] * sm.nf[r * LN + col];
+        const float dn = br * v[i];
+        st_f16(sg, r, col, HT, dn);
+        st_f16(sg, col, r, HT, dn);
+      } else if (col == r) {
+        st_f16(sg, r, col, HT, 0.f);
+      }
+    }
+    sm.part[12 + wg][r] = rb;
+  }
+  fence_before();
+  fence_async_smem();
+  __syncthreads();
+
+  // ---- P9: Ka = Q^T dPm + dW'^T X1 + K^T Sigma -> T3;  Kb = dS^T Ut^T -> T4
+  if (tid == 0) {
+    fence_after();
+    const uint32_t id_mm = idesc_f16(128, 64, true, true);
+    const uint32_t id_km = idesc_f16(128, 64, false, true);
+    const uint32_t kb = u32(sm.kq), pb = u32(sm.p), dwb = u32(sm.s0), x1b = u32(sm.x1), sgb = u32(sm.v + HT);
+    const uint32_t dsb = u32(sm.ds), ub = u32(sm.ut);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      mma_f16(tm + T3, sdesc(kb + HT + kk * 2048, 2 * HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id_mm, kk > 0);
+      mma_f16(tm + T3, sdesc(dwb + kk * 32, 16, 1024), sdesc(x1b + kk * 2048, HT, 1024), id_km, true);
+      mma_f16(tm + T3, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(sgb + kk * 2048, HT, 1024), id_mm, true);
+    }
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      mma_f16(tm + T4, sdesc(dsb + kk * 2048, 2 * HT, 1024), sdesc(ub + kk * 2048, 2 * HT, 1024), id_mm, kk > 0);
+    mma_commit(u32(&sm.bar_mma));
+  }
+  __syncwarp();
+  if (__syncthreads_or(!mma_done())) goto out;
+  {  // R9: dk^T = Ka + cdec * Kb (lanes d_k); Jacobian; dk out
+    float ka[32], kbv[32], s2[32];
+    tmem_ld32(tm + tl + T3 + c0, ka);
+    tmem_ld32(tm + tl + T4 + c0, kbv);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int tkn = c0 + i;
+      ka[i] += sm.gt.cdec[tkn] * kbv[i];
+      kbv[i] = ld_f16(sm.kq, tkn, row, 2 * HT);  // k^ (reused below)
+      s2[i] = ka[i] * kbv[i];
+    }
+    const float t2 = colsum32(s2);
+    sm.part[wq][c0 + lane] = t2;
+    __syncthreads();
+    bf16 *stg = reinterpret_cast<bf16 *>(sm.dob);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int tkn = c0 + i;
+      float o = ka[i];
+      if (l2) {
+        const float dot = sm.part[0][tkn] + sm.part[1][tkn] + sm.part[2][tkn] + sm.part[3][tkn];
+        o = (ka[i] - kbv[i] * dot) * sm.nk[tkn];
+      }
+      stg[tkn * D + row] = __float2bfloat16_rn(o);
+    }
+  }
+  fence_before();
+  __syncthreads();
+  {
+    bf16 *dkg = static_cast<bf16 *>(a.dk);
+    const uint4 *stg = reinterpret_cast<const uint4 *>(sm.dob);
+    for (int e = tid; e < CH * (D / 8); e += NTHREADS) {
+      const int r = e >> 4, cc = e & 15;
+      if (r < nvalid) *reinterpret_cast<uint4 *>(dkg + ((size_t)(tok0 + r) * H + h) * D + cc * 8) = stg[e];
+    }
+  }
+  // ---- gate and beta gradients
+  if (warp == 0) {
+    float dGv[2];
+    float sumy = 0.f;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int r = lane + 32 * t;
+      const float y = sm.gt.cdec[r] * sm.acc[0][r];
+      sumy += y;
+      dGv[t] = sm.acc[1][r] + sm.acc[2][r] - sm.acc[3][r] + sm.acc[5][r] - sm.acc[4][r] - y;
+    }
+    sumy = warp_sum(sumy);
+    float red = 0.f;
+    for (int i = 0; i < NWARPS; ++i) red += sm.red[i];
+    if (lane == 31) dGv[1] += sumy + sm.gt.gamC * red;
+    float hi = dGv[1], lo = dGv[0];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float yh = __shfl_down_sync(0xffffffffu, hi, o), yl = __shfl_down_sync(0xffffffffu, lo, o);
+      if (lane + o < 32) {
+        hi += yh;
+        lo += yl;
+      }
+    }
+    lo += __shfl_sync(0xffffffffu, hi, 0);
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int r = lane + 32 * t;
+      if (r < nvalid) {
+        a.dg[(size_t)(tok0 + r) * H + h] = t ? hi : lo;
+        a.dbeta[(size_t)(tok0 + r) * H + h] = sm.acc[6][r] + sm.part[12][r] + sm.part[13][r];
+      }
+    }
+  }
+out:
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp == 0) tmem_dealloc(tm, 512);
+}
+
+size_t bwd_local_tc_smem_bytes() { return sizeof(LocalTcSmem) + 1024; }
+
+int launch_bwd_local_tc(const BwdArgs &a, const CUtensorMap *maps, int CH_max, cudaStream_t st) {
+  if (CH_max == 0) return 0;
+  const size_t smem = bwd_local_tc_smem_bytes();
+  static_assert(sizeof(LocalTcSmem) + 1024 <= 232448, "shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(bwd_local_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return (int)e;
+  bwd_local_tc_kernel<<<dim3(CH_max, a.H), NTHREADS, smem, st>>>(a, maps[0], maps[1], maps[2], maps[3], maps[4],
+                                                                   maps[5]);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -2,6 +2,8 @@
 // tile loads, in-kernel L2 normalisation, gate prefix sums, and the unit
 // lower-triangular inverse of the WY stage.
 #pragma once
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace gdn {
@@ -114,9 +116,9 @@ __device__ __forceinline__ bool gate_prefix(const float *g, Gates &gt) {
 // nf[i][r], i < r); the lower triangle is left intact.  The four diagonal 16x16
 // blocks are inverted by forward substitution (one column per lane); the
 // off-diagonal blocks follow by distance, Ahat_IJ = -Ahat_II sum_{K=J}^{I-1}
-// T_IK Ahat_KJ, as 16 x 8 x 8 tensor-core products in 3xTF32 (each fp32
-// operand split into a tf32 high part and a tf32 remainder; the three leading
-// products restore fp32 accuracy).  `ys` holds >= 6 * 16 * 9 floats of scratch.
+// T_IK Ahat_KJ, as 16 x 8 x 8 tensor-core products in TF32, or in 3xTF32 (each
+// fp32 operand split into a tf32 high part and a tf32 remainder; the three
+// leading products restore fp32 accuracy).  `ys` holds >= 6 * 16 * 9 floats.
 // Ends with __syncthreads().
 __device__ __forceinline__ float ahat_at(const float *nf, int ldn, int a, int b) {
   return a == b ? 1.f : (a > b ? nf[b * ldn + a] : 0.f);
@@ -150,6 +152,10 @@ __device__ __forceinline__ void mma_3xtf32(float (&c)[4], const float (&a)[4], c
   mma_tf32(c, ah, bh);
 }
 
+// PRECISE: 3xTF32 merges (fp32 accuracy, fp32 mode); otherwise single TF32
+// merges (11-bit significand, matching the fp16 operands that X1 and X2 are
+// rounded to afterwards).
+template <bool PRECISE>
 static __device__ __noinline__ void tril_inverse(float *nf, int ldn, const float *beta, float *ys) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp < 4 && lane < 16) {
@@ -171,6 +177,18 @@ static __device__ __noinline__ void tril_inverse(float *nf, int ldn, const float
   }
   __syncthreads();
   const int gr = lane >> 2, gc = lane & 3;
+  auto mma = [&](float(&c)[4], const float(&av)[4], const float(&bv)[2]) {
+    if (PRECISE) {
+      mma_3xtf32(c, av, bv);
+    } else {
+      uint32_t ah[4], bh[2];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ah[i] = to_tf32(av[i]);
+      bh[0] = to_tf32(bv[0]);
+      bh[1] = to_tf32(bv[1]);
+      mma_tf32(c, ah, bh);
+    }
+  };
   for (int d = 1; d <= 3; ++d) {
     const int nb = 4 - d;
     if (warp < 2 * nb) {
@@ -179,7 +197,7 @@ static __device__ __noinline__ void tril_inverse(float *nf, int ldn, const float
       const int n0 = 16 * J + 8 * nh;  // global column of this 16 x 8 slice
       const int ra = 16 * I + gr;
       const float b0 = beta[ra], b1 = beta[ra + 8];
-      float y[4] = {0.f, 0.f, 0.f, 0.f};
+      float y0[4] = {0.f, 0.f, 0.f, 0.f}, y1[4] = {0.f, 0.f, 0.f, 0.f};  // two accumulators: shorter chains
       for (int K = J; K < I; ++K) {
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {
@@ -187,16 +205,17 @@ static __device__ __noinline__ void tril_inverse(float *nf, int ldn, const float
           const float av[4] = {b0 * nf[ra * ldn + k0 + gc], b1 * nf[(ra + 8) * ldn + k0 + gc],
                                b0 * nf[ra * ldn + k0 + gc + 4], b1 * nf[(ra + 8) * ldn + k0 + gc + 4]};
           const float bv[2] = {ahat_at(nf, ldn, k0 + gc, n0 + gr), ahat_at(nf, ldn, k0 + gc + 4, n0 + gr)};
-          mma_3xtf32(y, av, bv);
+          if (ks == 0) mma(y0, av, bv);
+          else mma(y1, av, bv);
         }
       }
       float *Ys = ys + warp * 16 * 9;  // [16][9]
-      Ys[gr * 9 + 2 * gc] = y[0];
-      Ys[gr * 9 + 2 * gc + 1] = y[1];
-      Ys[(gr + 8) * 9 + 2 * gc] = y[2];
-      Ys[(gr + 8) * 9 + 2 * gc + 1] = y[3];
+      Ys[gr * 9 + 2 * gc] = y0[0] + y1[0];
+      Ys[gr * 9 + 2 * gc + 1] = y0[1] + y1[1];
+      Ys[(gr + 8) * 9 + 2 * gc] = y0[2] + y1[2];
+      Ys[(gr + 8) * 9 + 2 * gc + 1] = y0[3] + y1[3];
       __syncwarp();
-      float x[4] = {0.f, 0.f, 0.f, 0.f};
+      float x0[4] = {0.f, 0.f, 0.f, 0.f}, x1[4] = {0.f, 0.f, 0.f, 0.f};
       const int rr = 16 * I;
 #pragma unroll
       for (int ks = 0; ks < 2; ++ks) {
@@ -205,13 +224,14 @@ static __device__ __noinline__ void tril_inverse(float *nf, int ldn, const float
                              ahat_at(nf, ldn, rr + gr, rr + kl + gc + 4),
                              ahat_at(nf, ldn, rr + gr + 8, rr + kl + gc + 4)};
         const float bv[2] = {Ys[(kl + gc) * 9 + gr], Ys[(kl + gc + 4) * 9 + gr]};
-        mma_3xtf32(x, av, bv);
+        if (ks == 0) mma(x0, av, bv);
+        else mma(x1, av, bv);
       }
       const int R = 16 * I + gr, Cc = n0 + 2 * gc;
-      nf[Cc * ldn + R] = -x[0];
-      nf[(Cc + 1) * ldn + R] = -x[1];
-      nf[Cc * ldn + R + 8] = -x[2];
-      nf[(Cc + 1) * ldn + R + 8] = -x[3];
+      nf[Cc * ldn + R] = -(x0[0] + x1[0]);
+      nf[(Cc + 1) * ldn + R] = -(x0[1] + x1[1]);
+      nf[Cc * ldn + R + 8] = -(x0[2] + x1[2]);
+      nf[(Cc + 1) * ldn + R + 8] = -(x0[3] + x1[3]);
     }
     __syncthreads();
   }

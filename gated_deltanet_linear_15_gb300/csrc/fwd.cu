@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_chunk_kernel(FwdArgs a) {
     }
     __syncthreads();
 
-    tril_inverse(sm.nf, LN, sm.beta, sm.ys);
+    tril_inverse<std::is_same<E, float>::value>(sm.nf, LN, sm.beta, sm.ys);
 
     // ---- X1 = Ahat diag(beta), X2 = diag(gp) Ahat diag(beta rgp) (entries <= |Ahat beta|)
     for (int e = threadIdx.x; e < CH * CH; e += NTHREADS) {

@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncthreads();
 
     // ---- Ahat (fp32, CUDA cores), then X1, X2 (fp16, K-major: rows = r)
-    tril_inverse(sm.nf, LN, gbeta, sm.ys);
+    tril_inverse<false>(sm.nf, LN, gbeta, sm.ys);
     for (int e = tid; e < CH * 8; e += NTHREADS) {
       const int r = e & 63, chk = e >> 6;  // consecutive lanes: consecutive rows (conflict-free reads of Ahat^T)
       float y1[8], y2[8];
