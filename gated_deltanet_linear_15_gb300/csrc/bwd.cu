@@ -38,7 +38,7 @@ template <typename E, int D> struct ChainSmem {
   float nf[CH * LN];
   float g[CH], beta[CH];
   Gates gt;
-  float ys[1024];
+  float ys[1152];
 };
 
 template <typename I, int D>
@@ -170,12 +170,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_chain_kernel(BwdArgs a) {
       }
     }
     __syncthreads();
-    tril_inverse<std::is_same<E, float>::value>(sm.nf, LN, sm.beta, sm.ys);
-    for (int e = threadIdx.x; e < CH * CH; e += NTHREADS) {
-      const int r = e / CH, i = e % CH;
-      sm.x1[r * LC + i] = fromf<E>(ahat_at(sm.nf, LN, r, i) * sm.beta[i]);
-    }
-    __syncthreads();
+    wy_inverse<std::is_same<E, float>::value, false>(sm.nf, LN, sm.beta, sm.ys,
+                                                     [&](int r, int c, float a0, float a1) {
+      st2(&sm.x1[r * LC + c], a0 * sm.beta[c], a1 * sm.beta[c + 1]);
+    });
 
     // W = diag(gam) X1 K  (all warps: 64 x D as 4 x 2 tiles of 16 x D/2)
     {
@@ -237,7 +235,7 @@ template <typename E, int D> struct LocalSmem {
   float nf[CH * LN];
   float g[CH], beta[CH], nq[CH], nk[CH];
   Gates gt;
-  float ys[1024];
+  float ys[1152];
   float part[14][CH];   // gate-gradient partials (see the final sum)
   float bpart[6][CH];   // beta-gradient partials
   float rdot[2][CH];    // row dots for the normalisation Jacobians
@@ -313,15 +311,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_local_kernel(BwdArgs a) {
     }
   }
   __syncthreads();
-  tril_inverse<std::is_same<E, float>::value>(sm.nf, LN, sm.beta, sm.ys);
-  for (int e = threadIdx.x; e < CH * CH; e += NTHREADS) {
-    const int r = e / CH, i = e % CH;
-    const float ah = ahat_at(sm.nf, LN, r, i);
-    const float b = sm.beta[i];
-    sm.x1[r * LC + i] = fromf<E>(ah * b);
-    sm.x2[r * LC + i] = fromf<E>(i <= r ? ah * b * (sm.gt.gp[r] * sm.gt.rgp[i]) : 0.f);
-  }
-  __syncthreads();
+  wy_inverse<std::is_same<E, float>::value, true>(sm.nf, LN, sm.beta, sm.ys,
+                                                    [&](int r, int c, float a0, float a1) {
+    const float b0 = sm.beta[c], b1 = sm.beta[c + 1], gr = sm.gt.gp[r];
+    st2(&sm.x1[r * LC + c], a0 * b0, a1 * b1);
+    st2(&sm.x2[r * LC + c], c <= r ? a0 * b0 * (gr * sm.gt.rgp[c]) : 0.f,
+        c + 1 <= r ? a1 * b1 * (gr * sm.gt.rgp[c + 1]) : 0.f);
+  });
 
   const int m0 = wr * 16, n0 = wc * WN;  // 64 x D outputs: 4 x 2 warps of 16 x D/2
   // ---- -W  and  Ut = U - W S0^T

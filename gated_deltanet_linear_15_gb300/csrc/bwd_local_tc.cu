@@ -51,7 +51,7 @@ struct __align__(1024) LocalTcSmem {
   float nf[CH * LN];
   float g[CH], beta[CH], nq[CH], nk[CH];  // nq, nk hold reciprocal norms
   Gates gt;
-  float ys[1024];
+  float ys[1152];
   float part[16][CH];   // per-token partial sums (4 warps x 4 kinds, reused per round)
   float acc[12][CH];    // assembled per-token terms
   float red[NWARPS];
@@ -256,27 +256,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   fence_before();
   __syncthreads();
-  tril_inverse<false>(sm.nf, LN, sm.beta, sm.ys);
-  for (int e = tid; e < CH * 8; e += NTHREADS) {
-    const int r = e & 63, chk = e >> 6;
-    float y1[8], y2[8], y3[8];
-    const float gr = sm.gt.gp[r];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int col = chk * 8 + i;
-      const float ah = ahat_at(sm.nf, LN, r, col);
-      const float b = sm.beta[col];
-      y1[i] = ah * b;
-      y2[i] = col <= r ? ah * b * (gr * sm.gt.rgp[col]) : 0.f;
-      y3[i] = ah;
-    }
-    const uint32_t off = r * 128 + ((chk ^ (r & 7)) * 16);
-    st_chunk_f16(sm.x1 + off, y1);
-    st_chunk_f16(sm.x2 + off, y2);
-    st_chunk_f16(sm.ah + off, y3);
-  }
-  fence_async_smem();
-  __syncthreads();
+  wy_inverse<false, true>(sm.nf, LN, sm.beta, sm.ys, [&](int r, int c, float a0, float a1) {
+    const float b0 = sm.beta[c], b1 = sm.beta[c + 1], gr = sm.gt.gp[r];
+    const uint32_t off = sw128_offset(r, c);
+    *reinterpret_cast<__half2 *>(sm.x1 + off) = __floats2half2_rn(a0 * b0, a1 * b1);
+    *reinterpret_cast<__half2 *>(sm.x2 + off) =
+        __floats2half2_rn(c <= r ? a0 * b0 * (gr * sm.gt.rgp[c]) : 0.f,
+                          c + 1 <= r ? a1 * b1 * (gr * sm.gt.rgp[c + 1]) : 0.f);
+    *reinterpret_cast<__half2 *>(sm.ah + off) = __floats2half2_rn(a0, a1);
+  });
 
   // ---- P2: W^T = K^T X1^T -> T1;  U^T = V^T X2^T -> T2
   if (tid == 0) {

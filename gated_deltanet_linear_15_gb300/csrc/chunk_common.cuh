@@ -110,16 +110,7 @@ __device__ __forceinline__ bool gate_prefix(const float *g, Gates &gt) {
   return rng > FACTOR_RANGE;
 }
 
-// Inverse of the unit lower-triangular T = I + diag(beta) N, N = strict_tril(K K^T),
-// in fp32 accuracy.  `nf` (CH x ldn floats) holds N in its strictly lower triangle
-// on entry; on exit its strictly upper triangle holds Ahat^T (Ahat[r][i] at
-// nf[i][r], i < r); the lower triangle is left intact.  The four diagonal 16x16
-// blocks are inverted by forward substitution (one column per lane); the
-// off-diagonal blocks follow by distance, Ahat_IJ = -Ahat_II sum_{K=J}^{I-1}
-// T_IK Ahat_KJ, as 16 x 8 x 8 tensor-core products in TF32, or in 3xTF32 (each
-// fp32 operand split into a tf32 high part and a tf32 remainder; the three
-// leading products restore fp32 accuracy).  `ys` holds >= 6 * 16 * 9 floats.
-// Ends with __syncthreads().
+// Ahat entry (a, b) from the transposed upper-triangle storage written by wy_inverse<., true>.
 __device__ __forceinline__ float ahat_at(const float *nf, int ldn, int a, int b) {
   return a == b ? 1.f : (a > b ? nf[b * ldn + a] : 0.f);
 }
@@ -152,18 +143,18 @@ __device__ __forceinline__ void mma_3xtf32(float (&c)[4], const float (&a)[4], c
   mma_tf32(c, ah, bh);
 }
 
-// PRECISE: 3xTF32 merges (fp32 accuracy, fp32 mode); otherwise single TF32
-// merges (11-bit significand, matching the fp16 operands that X1 and X2 are
-// rounded to afterwards).
-template <bool PRECISE>
-static __device__ __noinline__ void tril_inverse(float *nf, int ldn, const float *beta, float *ys) {
+__device__ __forceinline__ void umma_fence_proxy() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+
+template <bool PRECISE, bool NF_T, class Out>
+__device__ __forceinline__ void wy_inverse(float *nf, int ldn, const float *beta, float *dinv, Out out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int DL = 17;  // dinv row stride
   if (warp < 4 && lane < 16) {
     const int b = warp * 16, jj = lane;
     float x[16];
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
-      float s0 = 0.f, s1 = 0.f;  // two partial sums for instruction-level parallelism
+      float s0 = 0.f, s1 = 0.f;
 #pragma unroll
       for (int i = 0; i < r; ++i) {
         if (i & 1) s1 += nf[(b + r) * ldn + b + i] * x[i];
@@ -172,11 +163,9 @@ static __device__ __noinline__ void tril_inverse(float *nf, int ldn, const float
       x[r] = ((r == jj) ? 1.f : 0.f) - beta[b + r] * (s0 + s1);
     }
 #pragma unroll
-    for (int r = 1; r < 16; ++r)
-      if (r > jj) nf[(b + jj) * ldn + b + r] = x[r];
+    for (int r = 0; r < 16; ++r) dinv[(warp * 16 + r) * DL + jj] = x[r];
   }
   __syncthreads();
-  const int gr = lane >> 2, gc = lane & 3;
   auto mma = [&](float(&c)[4], const float(&av)[4], const float(&bv)[2]) {
     if (PRECISE) {
       mma_3xtf32(c, av, bv);
@@ -189,52 +178,85 @@ static __device__ __noinline__ void tril_inverse(float *nf, int ldn, const float
       mma_tf32(c, ah, bh);
     }
   };
-  for (int d = 1; d <= 3; ++d) {
-    const int nb = 4 - d;
-    if (warp < 2 * nb) {
-      const int bi = warp >> 1, nh = warp & 1;
-      const int I = d + bi, J = I - d;
-      const int n0 = 16 * J + 8 * nh;  // global column of this 16 x 8 slice
-      const int ra = 16 * I + gr;
-      const float b0 = beta[ra], b1 = beta[ra + 8];
-      float y0[4] = {0.f, 0.f, 0.f, 0.f}, y1[4] = {0.f, 0.f, 0.f, 0.f};  // two accumulators: shorter chains
-      for (int K = J; K < I; ++K) {
+  const int gr = lane >> 2, gc = lane & 3;
+  const int J0 = warp >> 1;               // first row block with non-zero entries in this slice
+  const int cl = 8 * (warp & 1);          // slice column offset inside block J0
+  // B fragment (k = 8*ks + gc (+4), n = gr) of a 16 x 8 block held in accumulator layout
+  auto bfrag = [&](const float(&c)[4], int ks, float(&bv)[2]) {
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-          const int k0 = 16 * K + 8 * ks;
-          const float av[4] = {b0 * nf[ra * ldn + k0 + gc], b1 * nf[(ra + 8) * ldn + k0 + gc],
-                               b0 * nf[ra * ldn + k0 + gc + 4], b1 * nf[(ra + 8) * ldn + k0 + gc + 4]};
-          const float bv[2] = {ahat_at(nf, ldn, k0 + gc, n0 + gr), ahat_at(nf, ldn, k0 + gc + 4, n0 + gr)};
-          if (ks == 0) mma(y0, av, bv);
-          else mma(y1, av, bv);
-        }
-      }
-      float *Ys = ys + warp * 16 * 9;  // [16][9]
-      Ys[gr * 9 + 2 * gc] = y0[0] + y1[0];
-      Ys[gr * 9 + 2 * gc + 1] = y0[1] + y1[1];
-      Ys[(gr + 8) * 9 + 2 * gc] = y0[2] + y1[2];
-      Ys[(gr + 8) * 9 + 2 * gc + 1] = y0[3] + y1[3];
-      __syncwarp();
-      float x0[4] = {0.f, 0.f, 0.f, 0.f}, x1[4] = {0.f, 0.f, 0.f, 0.f};
-      const int rr = 16 * I;
+    for (int h = 0; h < 2; ++h) {
+      const int krow = gc + 4 * h;               // row inside the 8-row half ks
+      const int src = krow * 4 + (gr >> 1);      // lane holding (row krow (+8 ks), col gr)
+      const float e0 = __shfl_sync(0xffffffffu, c[2 * ks + 0], src);
+      const float e1 = __shfl_sync(0xffffffffu, c[2 * ks + 1], src);
+      bv[h] = (gr & 1) ? e1 : e0;
+    }
+  };
+  float X[4][4];
+#pragma unroll
+  for (int I = 0; I < 4; ++I)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) X[I][e] = 0.f;
+  // X_J0 = columns of D_J0^{-1}
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int r = gr + 8 * (e >> 1), c = cl + 2 * gc + (e & 1);
+#pragma unroll
+    for (int I = 0; I < 4; ++I)
+      if (I == J0) X[I][e] = dinv[(I * 16 + r) * DL + c];
+  }
+#pragma unroll
+  for (int I = 1; I < 4; ++I) {
+    if (I <= J0) continue;
+    const int ra = 16 * I + gr;
+    const float b0 = beta[ra], b1 = beta[ra + 8];
+    float y0[4] = {0.f, 0.f, 0.f, 0.f}, y1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int K = 0; K < 3; ++K) {
+      if (K < J0 || K >= I) continue;
 #pragma unroll
       for (int ks = 0; ks < 2; ++ks) {
-        const int kl = 8 * ks;
-        const float av[4] = {ahat_at(nf, ldn, rr + gr, rr + kl + gc), ahat_at(nf, ldn, rr + gr + 8, rr + kl + gc),
-                             ahat_at(nf, ldn, rr + gr, rr + kl + gc + 4),
-                             ahat_at(nf, ldn, rr + gr + 8, rr + kl + gc + 4)};
-        const float bv[2] = {Ys[(kl + gc) * 9 + gr], Ys[(kl + gc + 4) * 9 + gr]};
-        if (ks == 0) mma(x0, av, bv);
-        else mma(x1, av, bv);
+        const int k0 = 16 * K + 8 * ks;
+        const float av[4] = {b0 * nf[ra * ldn + k0 + gc], b1 * nf[(ra + 8) * ldn + k0 + gc],
+                             b0 * nf[ra * ldn + k0 + gc + 4], b1 * nf[(ra + 8) * ldn + k0 + gc + 4]};
+        float bv[2];
+        bfrag(X[K], ks, bv);
+        if (ks == 0) mma(y0, av, bv);
+        else mma(y1, av, bv);
       }
-      const int R = 16 * I + gr, Cc = n0 + 2 * gc;
-      nf[Cc * ldn + R] = -(x0[0] + x1[0]);
-      nf[(Cc + 1) * ldn + R] = -(x0[1] + x1[1]);
-      nf[Cc * ldn + R + 8] = -(x0[2] + x1[2]);
-      nf[(Cc + 1) * ldn + R + 8] = -(x0[3] + x1[3]);
     }
-    __syncthreads();
+    float z[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) z[e] = -(y0[e] + y1[e]);
+    float x0[4] = {0.f, 0.f, 0.f, 0.f}, x1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+      const int kc = 8 * ks;
+      const float av[4] = {dinv[(I * 16 + gr) * DL + kc + gc], dinv[(I * 16 + gr + 8) * DL + kc + gc],
+                           dinv[(I * 16 + gr) * DL + kc + gc + 4], dinv[(I * 16 + gr + 8) * DL + kc + gc + 4]};
+      float bv[2];
+      bfrag(z, ks, bv);
+      if (ks == 0) mma(x0, av, bv);
+      else mma(x1, av, bv);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) X[I][e] = x0[e] + x1[e];
   }
+  // hand out every element of the slice (rows 0..63, columns 8w..8w+7)
+#pragma unroll
+  for (int I = 0; I < 4; ++I)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = 16 * I + gr + 8 * h, c = 8 * warp + 2 * gc;
+      const float a0 = X[I][2 * h], a1 = X[I][2 * h + 1];
+      out(r, c, a0, a1);
+      if (NF_T) {
+        if (c < r) nf[c * ldn + r] = a0;
+        if (c + 1 < r) nf[(c + 1) * ldn + r] = a1;
+      }
+    }
+  umma_fence_proxy();  // shared-memory operands written above are read by the tensor-core async proxy
+  __syncthreads();
 }
 
 }  // namespace gdn

@@ -37,7 +37,7 @@ template <typename E, int D> struct FwdSmem {
   float nf[CH * LN];
   float g[CH], beta[CH];
   Gates gt;
-  float ys[1024];
+  float ys[1152];
 };
 
 template <typename I, int D>
@@ -181,17 +181,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_chunk_kernel(FwdArgs a) {
     }
     __syncthreads();
 
-    tril_inverse<std::is_same<E, float>::value>(sm.nf, LN, sm.beta, sm.ys);
-
-    // ---- X1 = Ahat diag(beta), X2 = diag(gp) Ahat diag(beta rgp) (entries <= |Ahat beta|)
-    for (int e = threadIdx.x; e < CH * CH; e += NTHREADS) {
-      const int r = e / CH, i = e % CH;
-      const float ah = ahat_at(sm.nf, LN, r, i);
-      const float b = sm.beta[i];
-      sm.x1[r * LC + i] = fromf<E>(ah * b);
-      sm.x2[r * LC + i] = fromf<E>(i <= r ? ah * b * (sm.gt.gp[r] * sm.gt.rgp[i]) : 0.f);
-    }
-    __syncthreads();
+    wy_inverse<std::is_same<E, float>::value, false>(sm.nf, LN, sm.beta, sm.ys,
+                                                     [&](int r, int c, float a0, float a1) {
+      const float b0 = sm.beta[c], b1 = sm.beta[c + 1], gr = sm.gt.gp[r];
+      st2(&sm.x1[r * LC + c], a0 * b0, a1 * b1);
+      st2(&sm.x2[r * LC + c], c <= r ? a0 * b0 * (gr * sm.gt.rgp[c]) : 0.f,
+          c + 1 <= r ? a1 * b1 * (gr * sm.gt.rgp[c + 1]) : 0.f);
+    });
 
     // ---- U (warps 0-3, registers) and -W (warps 4-7, shared)
     {

@@ -47,7 +47,7 @@ struct __align__(1024) TcSmem {
   float nf[CH * (CH + 4)];
   float g[2][CH], beta[2][CH];  // per ring stage
   Gates gt;
-  float ys[1024];
+  float ys[1152];
   uint64_t bar_tma[2];
   uint64_t bar_mma;
   uint32_t tmem_base;
@@ -307,26 +307,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     fence_before();
     __syncthreads();
 
-    // ---- Ahat (fp32, CUDA cores), then X1, X2 (fp16, K-major: rows = r)
-    tril_inverse<false>(sm.nf, LN, gbeta, sm.ys);
-    for (int e = tid; e < CH * 8; e += NTHREADS) {
-      const int r = e & 63, chk = e >> 6;  // consecutive lanes: consecutive rows (conflict-free reads of Ahat^T)
-      float y1[8], y2[8];
-      const float gr = sm.gt.gp[r];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int col = chk * 8 + i;
-        const float ah = ahat_at(sm.nf, LN, r, col);
-        const float b = gbeta[col];
-        y1[i] = ah * b;
-        y2[i] = col <= r ? ah * b * (gr * sm.gt.rgp[col]) : 0.f;
-      }
-      const uint32_t off = r * 128 + ((chk ^ (r & 7)) * 16);
-      st_chunk_f16(sm.x1 + off, y1);
-      st_chunk_f16(sm.x2 + off, y2);
-    }
-    fence_async_smem();
-    __syncthreads();
+    // ---- Ahat (fp32 diagonal blocks, TF32 tensor-core merges) -> X1, X2 (fp16, K-major: rows = r)
+    wy_inverse<false, false>(sm.nf, LN, gbeta, sm.ys, [&](int r, int c, float a0, float a1) {
+      const float b0 = gbeta[c], b1 = gbeta[c + 1], gr = sm.gt.gp[r];
+      const uint32_t off = sw128_offset(r, c);
+      *reinterpret_cast<__half2 *>(sm.x1 + off) = __floats2half2_rn(a0 * b0, a1 * b1);
+      *reinterpret_cast<__half2 *>(sm.x2 + off) =
+          __floats2half2_rn(c <= r ? a0 * b0 * (gr * sm.gt.rgp[c]) : 0.f,
+                            c + 1 <= r ? a1 * b1 * (gr * sm.gt.rgp[c + 1]) : 0.f);
+    });
 
     // ---- MMA 2: W^T = K^T X1^T, U^T = V^T X2^T  (M = 128, N = 64, K = 64)
     if (tid == 0) {
