@@ -18,8 +18,8 @@
 //   P6 Qb = K^T dPm^T->T7, M1 = dW' K^T->T3, M2 = dUt V^T->T4
 //                            R6: dq out (+ <dQ1,q>); dAhat tile, beta column sums
 //   P7 Y1 = Ahat^T dAhat->T0 R7: Y1 tile
-//   P8 dT = -Y1 Ahat^T->T1   R8: Sigma = dN + dN^T tile, beta row sums
-//   P9 Ka = Q^T dPm + dW'^T X1 + K^T Sigma->T3, Kb = dS^T Ut^T->T4
+//   P8 dT = -Y1 Ahat^T->T1   R8: dN tile (strictly lower), beta row sums
+//   P9 Ka = Q^T dPm + dW'^T X1 + K^T (dN + dN^T)->T3, Kb = dS^T Ut^T->T4
 //                            R9: dk out;  dg (reverse cumsum), dbeta
 #include "chunk_common.cuh"
 #include "kernels.h"
@@ -38,7 +38,7 @@ constexpr uint32_t T0 = 0, T1 = 64, T2 = 128, T3 = 192, T4 = 256, T5 = 320, T6 =
 
 struct __align__(1024) LocalTcSmem {
   uint8_t kq[4 * HT];   // [K0 | Q0 | K1 | Q1] half-tiles (feature blocks 0/1), rows = token
-  uint8_t v[2 * HT];    // V, later Y1 (first half) and Sigma (second half)
+  uint8_t v[2 * HT];    // V, later Y1 (first half) and dN (second half)
   uint8_t dob[2 * HT];  // dO, later output staging (bf16 [token][128])
   uint8_t s0[4 * HT];   // S0 [k-block][128 rows = d_v][64], later dW'^T [d_k][token]
   uint8_t ds[4 * HT];   // dS, same layout
@@ -55,7 +55,7 @@ struct __align__(1024) LocalTcSmem {
   float part[16][CH];   // per-token partial sums (4 warps x 4 kinds, reused per round)
   float acc[12][CH];    // assembled per-token terms
   float red[NWARPS];
-  uint64_t bar_tma, bar_mma;
+  uint64_t bar_tma, bar_st, bar_mma;
   uint32_t tmem_base;
 };
 
@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (tid == 0) {
     mbar_init(u32(&sm.bar_tma), 1);
+    mbar_init(u32(&sm.bar_st), 1);
     mbar_init(u32(&sm.bar_mma), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
@@ -135,8 +136,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   // ---- loads: TMA for the six tiles, plain loads for g, beta
   if (tid == 0) {
-    const uint32_t bar = u32(&sm.bar_tma);
-    mbar_expect_tx(bar, 16 * HT);
+    const uint32_t bar = u32(&sm.bar_tma), bst = u32(&sm.bar_st);
+    mbar_expect_tx(bar, 8 * HT);
+    mbar_expect_tx(bst, 8 * HT);
     tma_load_3d(u32(sm.kq + 0 * HT), &tmk, 0, h, tok0, bar);
     tma_load_3d(u32(sm.kq + 2 * HT), &tmk, 64, h, tok0, bar);
     tma_load_3d(u32(sm.kq + 1 * HT), &tmq, 0, h, tok0, bar);
@@ -146,10 +148,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tma_load_3d(u32(sm.dob), &tmdo, 0, h, tok0, bar);
     tma_load_3d(u32(sm.dob + HT), &tmdo, 64, h, tok0, bar);
     const int srow = (gc * H + h) * D;
-    tma_load_3d(u32(sm.s0), &tms0, 0, srow, 0, bar);
-    tma_load_3d(u32(sm.s0 + 2 * HT), &tms0, 64, srow, 0, bar);
-    tma_load_3d(u32(sm.ds), &tmds, 0, srow, 0, bar);
-    tma_load_3d(u32(sm.ds + 2 * HT), &tmds, 64, srow, 0, bar);
+    // the states are first needed at P3: their own barrier, waited there
+    tma_load_3d(u32(sm.s0), &tms0, 0, srow, 0, bst);
+    tma_load_3d(u32(sm.s0 + 2 * HT), &tms0, 64, srow, 0, bst);
+    tma_load_3d(u32(sm.ds), &tmds, 0, srow, 0, bst);
+    tma_load_3d(u32(sm.ds + 2 * HT), &tmds, 64, srow, 0, bst);
   }
   if (tid < 64) sm.g[tid] = tid < nvalid ? a.g[(size_t)(tok0 + tid) * H + h] : 0.f;
   else if (tid < 128) sm.beta[tid - 64] = (tid - 64) < nvalid ? a.beta[(size_t)(tok0 + tid - 64) * H + h] : 0.f;
@@ -163,22 +166,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   };
   if (__syncthreads_or(!ok)) goto out;
   if (warp == 0) gate_prefix(sm.g, sm.gt);
-  {  // <dS, S0> over the whole state (both tiles share one layout, so compare byte positions)
-    float acc = 0.f;
-    const uint4 *A4 = reinterpret_cast<const uint4 *>(sm.s0), *B4 = reinterpret_cast<const uint4 *>(sm.ds);
-    for (int e = tid; e < 4 * HT / 16; e += NTHREADS) {
-      const uint4 x = A4[e], y = B4[e];
-      const __half2 *xh = reinterpret_cast<const __half2 *>(&x), *yh = reinterpret_cast<const __half2 *>(&y);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 fx = __half22float2(xh[i]), fy = __half22float2(yh[i]);
-        acc += fx.x * fy.x + fx.y * fy.y;
-      }
-    }
-    acc = warp_sum(acc);
-    if (lane == 0) sm.red[warp] = acc;
-  }
-
   // ---- prep: bf16 -> fp16 in place; q, k normalised (norms kept for the Jacobians); rows >= nvalid zero
   for (int task = tid; task < 4 * 2 * CH; task += NTHREADS) {
     const int t = task >> 7;  // 0 K, 1 Q, 2 V, 3 dO
@@ -256,7 +243,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   fence_before();
   __syncthreads();
-  wy_inverse<false, true>(sm.nf, LN, sm.beta, sm.ys, [&](int r, int c, float a0, float a1) {
+  wy_inverse<false, false>(sm.nf, LN, sm.beta, sm.ys, [&](int r, int c, float a0, float a1) {
     const float b0 = sm.beta[c], b1 = sm.beta[c + 1], gr = sm.gt.gp[r];
     const uint32_t off = sw128_offset(r, c);
     *reinterpret_cast<__half2 *>(sm.x1 + off) = __floats2half2_rn(a0 * b0, a1 * b1);
@@ -294,6 +281,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   fence_before();
   fence_async_smem();
   __syncthreads();
+
+  if (__syncthreads_or(!mbar_wait(u32(&sm.bar_st), 0, err, 8))) goto out;
+  {  // <dS, S0> over the whole state (both tiles share one layout, so compare byte positions)
+    float acc = 0.f;
+    const uint4 *A4 = reinterpret_cast<const uint4 *>(sm.s0), *B4 = reinterpret_cast<const uint4 *>(sm.ds);
+    for (int e = tid; e < 4 * HT / 16; e += NTHREADS) {
+      const uint4 x = A4[e], y = B4[e];
+      const __half2 *xh = reinterpret_cast<const __half2 *>(&x), *yh = reinterpret_cast<const __half2 *>(&y);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 fx = __half22float2(xh[i]), fy = __half22float2(yh[i]);
+        acc += fx.x * fy.x + fx.y * fy.y;
+      }
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) sm.red[warp] = acc;
+  }
 
   // ---- P3: Ut^T = U^T - S0 W^T  (T2)
   if (tid == 0) {
@@ -506,12 +510,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tmem_ld32(tm + tl + T4 + c0, m2);
       const int r = row;
       const float gr = sm.gt.gp[r];
+      float ahr[32];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const uint4 raw = *reinterpret_cast<const uint4 *>(sm.ah + r * 128 + ((((c0 >> 3) + q4) ^ (r & 7)) * 16));
+        const __half2 *hh = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __half22float2(hh[i]);
+          ahr[q4 * 8 + 2 * i] = f.x;
+          ahr[q4 * 8 + 2 * i + 1] = f.y;
+        }
+      }
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const int col = c0 + i;
         const float x = m1[i] + (col <= r ? m2[i] * gr * sm.gt.rgp[col] : 0.f);
-        const float ahv = ahat_at(sm.nf, LN, r, col);
-        m2[i] = ahv * x;
+        m2[i] = ahr[i] * x;
         m1[i] = sm.beta[col] * x;
       }
 #pragma unroll
@@ -588,7 +603,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   __syncwarp();
   if (__syncthreads_or(!mma_done())) goto out;
-  if (row < 64) {  // R8: Sigma[r][i] = Sigma[i][r] = beta_r dT_ri (i < r), 0 on the diagonal; beta row sums
+  if (row < 64) {  // R8: dN[r][i] = beta_r dT_ri (i < r), zero elsewhere; beta row sums of dT * N
     float v[32];
     tmem_ld32(tm + tl + T1 + c0, v);
     const int r = row;
@@ -596,16 +611,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint8_t *sg = sm.v + HT;
     float rb = 0.f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int col = c0 + i;
-      if (col < r) {
-        rb += v[i] * sm.nf[r * LN + col];
-        const float dn = br * v[i];
-        st_f16(sg, r, col, HT, dn);
-        st_f16(sg, col, r, HT, dn);
-      } else if (col == r) {
-        st_f16(sg, r, col, HT, 0.f);
+    for (int q4 = 0; q4 < 4; ++q4) {
+      float y[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int col = c0 + q4 * 8 + i;
+        const float dt = v[q4 * 8 + i];
+        const bool lo = col < r;
+        rb += lo ? dt * sm.nf[r * LN + col] : 0.f;
+        y[i] = lo ? br * dt : 0.f;
       }
+      st_chunk_f16(sg + r * 128 + ((((c0 >> 3) + q4) ^ (r & 7)) * 16), y);
     }
     sm.part[12 + wg][r] = rb;
   }
@@ -618,13 +634,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     fence_after();
     const uint32_t id_mm = idesc_f16(128, 64, true, true);
     const uint32_t id_km = idesc_f16(128, 64, false, true);
+    const uint32_t id_mk = idesc_f16(128, 64, true, false);
     const uint32_t kb = u32(sm.kq), pb = u32(sm.p), dwb = u32(sm.s0), x1b = u32(sm.x1), sgb = u32(sm.v + HT);
     const uint32_t dsb = u32(sm.ds), ub = u32(sm.ut);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       mma_f16(tm + T3, sdesc(kb + HT + kk * 2048, 2 * HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id_mm, kk > 0);
       mma_f16(tm + T3, sdesc(dwb + kk * 32, 16, 1024), sdesc(x1b + kk * 2048, HT, 1024), id_km, true);
+      // K^T (dN + dN^T): the dN tile read once as MN-major (dN) and once as K-major (dN^T)
       mma_f16(tm + T3, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(sgb + kk * 2048, HT, 1024), id_mm, true);
+      mma_f16(tm + T3, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(sgb + kk * 32, 16, 1024), id_mk, true);
     }
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)

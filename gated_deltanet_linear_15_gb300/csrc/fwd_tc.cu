@@ -46,7 +46,7 @@ struct __align__(1024) TcSmem {
   uint8_t s0[4 * HT];   // S0 fp16 (K-major A: rows = d_v, two k-blocks of 128 rows)
   float nf[CH * (CH + 4)];
   float g[2][CH], beta[2][CH];  // per ring stage
-  Gates gt;
+  Gates gt[2];  // per ring stage; the next chunk's gates are computed during this chunk
   float ys[1152];
   uint64_t bar_tma[2];
   uint64_t bar_mma;
@@ -147,15 +147,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tma_load_3d(u32(st + 5 * HT), &tmv, 64, h, tok0, bar);
     }
   };
-  auto issue_gb = [&](int c, int stage) {  // cp.async of g, beta for chunk c (threads 0-127)
+  auto issue_gb = [&](int c, int stage, bool with_g) {  // cp.async of (g and) beta for chunk c
     const int tok0 = bos + c * CH;
     const int nvalid = min(CH, len - c * CH);
-    load_scalars(sm.g[stage], a.g, H, h, tok0, nvalid, 0);
+    if (with_g) load_scalars(sm.g[stage], a.g, H, h, tok0, nvalid, 0);
     load_scalars(sm.beta[stage], a.beta, H, h, tok0, nvalid, 64);
     cp_async_commit();
   };
   if (tid == 0 && cfirst < cend) issue_tma(cfirst, 0);
-  if (cfirst < cend) issue_gb(cfirst, 0);
+  if (cfirst < cend) issue_gb(cfirst, 0, true);
 
   // ---------------------------------------------------------------- initial state -> TMEM
   {
@@ -199,64 +199,93 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint8_t *st = sm.ring[stage];
 
     float *gbeta = sm.beta[stage];
+    float gnext0 = 0.f, gnext1 = 0.f;  // next chunk's log-gates (warp 0), consumed while MMA 4 runs
+    if (warp == 0 && c + 1 < cend) {
+      const int tokn = bos + (c + 1) * CH, nvn = min(CH, len - (c + 1) * CH);
+      if (lane < nvn) gnext0 = a.g[(size_t)(tokn + lane) * H + h];
+      if (lane + 32 < nvn) gnext1 = a.g[(size_t)(tokn + lane + 32) * H + h];
+    }
     // g, beta of this chunk (issued one chunk ahead) must have landed before the next prefetch reuses cp.async
     cp_async_wait_all();
     // prefetch the next chunk into the other stage (its previous contents were consumed)
     if (tid == 0 && c + 1 < cend) issue_tma(c + 1, stage ^ 1);
-    if (c + 1 < cend) issue_gb(c + 1, stage ^ 1);
+    if (c + 1 < cend) issue_gb(c + 1, stage ^ 1, false);
     const bool tma_ok = mbar_wait(u32(&sm.bar_tma[stage]), (it >> 1) & 1, err, 8);
     if (__syncthreads_or(!tma_ok)) {
       failed = true;
       break;
     }
-    if (warp == 0) {
-      if (gate_prefix(sm.g[stage], sm.gt) && lane == 0 && err) atomicOr(err, 1);
+    Gates &G = sm.gt[stage];
+    if (it == 0 && warp == 0) {  // later chunks' gates were computed one chunk ahead
+      if (gate_prefix(sm.g[stage], G) && lane == 0 && err) atomicOr(err, 1);
     }
     __syncthreads();
 
     // ---- prep: bf16 -> fp16 in place, L2 norm of q/k rows, Kc = cdec*K, Qg = gam*Q; rows >= nvalid zeroed.
-    // One thread per half-row (64 features = one 128-byte swizzled row); the two halves of a row
-    // sit in adjacent lanes and combine their squared norms with one shuffle.
-    for (int task = tid; task < 3 * 2 * CH; task += NTHREADS) {
-      const int t = task >> 7;  // 0: K, 1: Q, 2: V
-      if (t == 1 && !emit) continue;
-      if (t == 2 && !need_v) continue;
-      const int r = (task >> 1) & 63, hb = task & 1;
-      uint8_t *rowp = st + (t == 0 ? 0 : t == 1 ? HT : 4 * HT) + hb * (t == 2 ? HT : 2 * HT) + r * 128;
-      float x[64];
+    // Thread t: half-row t of K (t < 128) or of Q (t >= 128): 64 features = one 128-byte swizzled row, the
+    // two halves of a row in adjacent lanes (one shuffle for the squared norm); plus quarter-row t of V.
+    {
+      const bool isq = tid >= 128;
+      if (!isq || emit) {
+        const int r = (tid >> 1) & 63, hb = tid & 1;
+        uint8_t *rowp = st + (isq ? HT : 0) + hb * 2 * HT + r * 128;
+        uint32_t raw[32];
 #pragma unroll
-      for (int chk = 0; chk < 8; ++chk) {
-        const uint4 raw = *reinterpret_cast<const uint4 *>(rowp + ((chk ^ (r & 7)) * 16));
-        const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+        for (int chk = 0; chk < 8; ++chk) {
+          const uint4 q4 = *reinterpret_cast<const uint4 *>(rowp + ((chk ^ (r & 7)) * 16));
+          raw[4 * chk] = q4.x;
+          raw[4 * chk + 1] = q4.y;
+          raw[4 * chk + 2] = q4.z;
+          raw[4 * chk + 3] = q4.w;
+        }
+        float mul = isq ? a.scale : 1.f;
+        if (l2) {
+          float ss = 0.f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __bfloat1622float2(b2[i]);
-          x[chk * 8 + 2 * i] = f.x;
-          x[chk * 8 + 2 * i + 1] = f.y;
+          for (int i = 0; i < 32; ++i) {
+            const float lo = __uint_as_float(raw[i] << 16), hi = __uint_as_float(raw[i] & 0xffff0000u);
+            ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+          }
+          ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+          mul *= rsqrtf(ss + 1e-6f);
+        }
+        if (r >= nvalid) mul = 0.f;
+        const float m2 = mul * (isq ? G.gam[r] : G.cdec[r]);
+        uint8_t *row2 = (isq ? sm.qg : sm.kc) + hb * HT + r * 128;
+#pragma unroll
+        for (int chk = 0; chk < 8; ++chk) {
+          uint32_t y[4], z[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t w = raw[4 * chk + i];
+            const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+            const __half2 a2 = __floats2half2_rn(lo * mul, hi * mul);
+            const __half2 b2 = __floats2half2_rn(lo * m2, hi * m2);
+            y[i] = *reinterpret_cast<const uint32_t *>(&a2);
+            z[i] = *reinterpret_cast<const uint32_t *>(&b2);
+          }
+          const int off = (chk ^ (r & 7)) * 16;
+          *reinterpret_cast<uint4 *>(rowp + off) = make_uint4(y[0], y[1], y[2], y[3]);
+          *reinterpret_cast<uint4 *>(row2 + off) = make_uint4(z[0], z[1], z[2], z[3]);
         }
       }
-      float mul = (t == 1) ? a.scale : 1.f;
-      if (l2 && t < 2) {
-        float ss = 0.f;
+      if (need_v) {  // quarter-row: 4 chunks of V
+        const int r = tid >> 2, qr = tid & 3;
+        uint8_t *rowp = st + 4 * HT + (qr >> 1) * HT + r * 128;
+        const float mul = r < nvalid ? 1.f : 0.f;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) ss += x[i] * x[i];
-        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-        mul = mul / sqrtf(ss + 1e-6f);
-      }
-      if (r >= nvalid) mul = 0.f;
-      const float sc2 = t == 0 ? sm.gt.cdec[r] : sm.gt.gam[r];
-      uint8_t *row2 = (t == 0 ? sm.kc : sm.qg) + hb * HT + r * 128;
+        for (int cc = 0; cc < 4; ++cc) {
+          const int chk = (qr & 1) * 4 + cc;
+          uint4 q4 = *reinterpret_cast<const uint4 *>(rowp + ((chk ^ (r & 7)) * 16));
+          uint32_t *w = reinterpret_cast<uint32_t *>(&q4);
 #pragma unroll
-      for (int chk = 0; chk < 8; ++chk) {
-        float y[8], z[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          y[i] = x[chk * 8 + i] * mul;
-          z[i] = y[i] * sc2;
+          for (int i = 0; i < 4; ++i) {
+            const __half2 a2 = __floats2half2_rn(__uint_as_float(w[i] << 16) * mul,
+                                                 __uint_as_float(w[i] & 0xffff0000u) * mul);
+            w[i] = *reinterpret_cast<const uint32_t *>(&a2);
+          }
+          *reinterpret_cast<uint4 *>(rowp + ((chk ^ (r & 7)) * 16)) = q4;
         }
-        const int off = (chk ^ (r & 7)) * 16;
-        st_chunk_f16(rowp + off, y);
-        if (t < 2) st_chunk_f16(row2 + off, z);
       }
     }
     fence_async_smem();
@@ -290,14 +319,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int i = 0; i < 32; ++i) sm.nf[row * LN + c0 + i] = v[i];
       } else {
         const int r = row - 64;
-        const float gr = sm.gt.gp[r];
+        const float gr = G.gp[r];
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           float y[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int col = c0 + q4 * 8 + i;
-            y[i] = col <= r ? v[q4 * 8 + i] * gr * sm.gt.rgp[col] : 0.f;
+            y[i] = col <= r ? v[q4 * 8 + i] * gr * G.rgp[col] : 0.f;
           }
           const int chk = (c0 >> 3) + q4;
           st_chunk_f16(sm.p + r * 128 + ((chk ^ (r & 7)) * 16), y);
@@ -309,12 +338,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     // ---- Ahat (fp32 diagonal blocks, TF32 tensor-core merges) -> X1, X2 (fp16, K-major: rows = r)
     wy_inverse<false, false>(sm.nf, LN, gbeta, sm.ys, [&](int r, int c, float a0, float a1) {
-      const float b0 = gbeta[c], b1 = gbeta[c + 1], gr = sm.gt.gp[r];
+      const float b0 = gbeta[c], b1 = gbeta[c + 1], gr = G.gp[r];
       const uint32_t off = sw128_offset(r, c);
       *reinterpret_cast<__half2 *>(sm.x1 + off) = __floats2half2_rn(a0 * b0, a1 * b1);
       *reinterpret_cast<__half2 *>(sm.x2 + off) =
-          __floats2half2_rn(c <= r ? a0 * b0 * (gr * sm.gt.rgp[c]) : 0.f,
-                            c + 1 <= r ? a1 * b1 * (gr * sm.gt.rgp[c + 1]) : 0.f);
+          __floats2half2_rn(c <= r ? a0 * b0 * (gr * G.rgp[c]) : 0.f,
+                            c + 1 <= r ? a1 * b1 * (gr * G.rgp[c + 1]) : 0.f);
     });
 
     // ---- MMA 2: W^T = K^T X1^T, U^T = V^T X2^T  (M = 128, N = 64, K = 64)
@@ -336,7 +365,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncwarp();
     // meanwhile: S0 -> fp16 operand copy, gam_C * S0 back into TMEM (state copy for the backward)
     {
-      const float gC = sm.gt.gamC;
+      const float gC = G.gamC;
       f16 *stg = states && c >= cbeg
                      ? static_cast<f16 *>(a.states) + ((size_t)(chunk0 + c) * H + h) * DD + (size_t)row * D
                      : nullptr;
@@ -372,7 +401,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int q4 = 0; q4 < 4; ++q4) {
         float y[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) y[i] = v[q4 * 8 + i] * sm.gt.gam[c0 + q4 * 8 + i];
+        for (int i = 0; i < 8; ++i) y[i] = v[q4 * 8 + i] * G.gam[c0 + q4 * 8 + i];
         const int chk = (c0 >> 3) + q4;
         st_chunk_f16(sm.wu + row * 128 + ((chk ^ (row & 7)) * 16), y);
       }
@@ -441,6 +470,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mma_commit(u32(&sm.bar_mma));
     }
     __syncwarp();
+    if (warp == 0 && c + 1 < cend) {  // gates of the next chunk, overlapping MMA 4
+      float *gn = sm.g[stage ^ 1];
+      gn[lane] = gnext0;
+      gn[lane + 32] = gnext1;
+      __syncwarp();
+      if (gate_prefix(gn, sm.gt[stage ^ 1]) && lane == 0 && err) atomicOr(err, 1);
+    }
     if (__syncthreads_or(!mma_wait())) {
       failed = true;
       break;
