@@ -533,11 +533,20 @@ int gdn_chunk_bwd(const gdn_shape *s, const void *q, const void *k, const void *
   ba.Lseg = L.Lseg;
   ba.scale = s->scale;
   ba.flags = s->flags;
+  // the reverse chain: tcgen05 for bf16 with d = 128, the mma.sync kernel otherwise
+  const bool chain_tc = bf && L.D == 128 && L.Ttot > 0;
+  CUtensorMap cmaps[3];
+  if (chain_tc && ((rc = qkv_map(&cmaps[0], q, L.Ttot, L.H)) || (rc = qkv_map(&cmaps[1], k, L.Ttot, L.H)) ||
+                   (rc = qkv_map(&cmaps[2], dO, L.Ttot, L.H))))
+    return rc;
+  auto chain = [&](dim3 grid) {
+    return chain_tc ? launch_bwd_chain_tc(ba, cmaps, grid, st) : launch_bwd_chain(ba, bf, L.D, grid, st);
+  };
   if (L.sp) {
     ba.pass = 0;
     {
       PROF("bwd_chain_pass_a");
-      CK(launch_bwd_chain(ba, bf, L.D, dim3(L.S_max, L.H, 2), st));
+      CK(chain(dim3(L.S_max, L.H, 2)));
     }
     FixupArgs fx;
     fx.plan = pl;
@@ -556,7 +565,7 @@ int gdn_chunk_bwd(const gdn_shape *s, const void *q, const void *k, const void *
   ba.pass = 1;
   {
     PROF("bwd_chain");
-    CK(launch_bwd_chain(ba, bf, L.D, dim3(L.S_max, L.H, 1), st));
+    CK(chain(dim3(L.S_max, L.H, 1)));
   }
   // 3. local gradients, every (chunk, head) in parallel
   {

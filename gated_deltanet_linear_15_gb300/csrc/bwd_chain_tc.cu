@@ -1,0 +1,464 @@
+// Blackwell-native reverse state chain of the chunked backward (bf16 inputs,
+// d = 128): one CTA per (segment, head), chunks in reverse order, dS (the
+// gradient w.r.t. a chunk's end state) resident in fp32 TMEM.  Per chunk:
+//   [K; Q] K^T            -> N (inverse -> X1 = Ahat diag(beta)), P
+//   W^T = K^T X1^T        (columns scaled by gam at read-out)
+//   dUt^T = dS Kc^T + dO^T P               Kc = diag(cdec) K
+//   dS <- gam_C dS + dO^T Qg - dUt^T W     Qg = diag(gam) Q
+// and the fp16 dS at every chunk end goes to the workspace for the
+// local-gradient kernel.  Pass 0 (reverse sequence parallelism) runs a
+// segment from zero (role 0) or the transition from I with dO = 0 (role 1);
+// pass 1 runs it from its exact end gradient and stores the per-chunk dS
+// (and dS0 for the first segment).  Layouts and primitives as in fwd_tc.cu.
+#include "chunk_common.cuh"
+#include "kernels.h"
+#include "umma.cuh"
+
+namespace gdn {
+
+using namespace umma;
+
+namespace {
+
+constexpr int D = 128;
+constexpr int HT = 8192;
+constexpr int LN = CH + 4;
+constexpr uint32_t TM_S = 0, TM_KQ = 128, TM_W = 192, TM_DU = 256, TM_COLS = 512;
+
+struct __align__(1024) ChainTcSmem {
+  uint8_t ring[2][6 * HT];  // [K0 | Q0 | K1 | Q1 | dO0 | dO1]
+  uint8_t kc[2 * HT];       // diag(cdec) K (K-major B, rows = token); later dUt^T (K-major A, rows = d_v)
+  uint8_t qg[2 * HT];       // diag(gam) Q (MN-major B, rows = token)
+  uint8_t x1[HT], p[HT];
+  uint8_t wt[2 * HT];       // W^T [d_k][token]: MN-major view for nothing, K-major B view for dUt^T W
+  uint8_t ds16[4 * HT];     // dS fp16 (K-major A: rows = d_v, two k-blocks of 128 rows)
+  float nf[CH * LN];
+  float g[2][CH], beta[2][CH];
+  Gates gt[2];
+  float ys[1152];
+  uint64_t bar_tma[2];
+  uint64_t bar_mma;
+  uint32_t tmem_base;
+};
+
+__device__ __forceinline__ uint32_t u32(const void *p) { return smem_u32(p); }
+
+__device__ __forceinline__ void st_chunk_f16(uint8_t *dst, const float *v) {
+  __half2 h[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+  *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<uint4 *>(h);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    bwd_chain_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                        const __grid_constant__ CUtensorMap tmdo) {
+  extern __shared__ unsigned char smraw[];
+  ChainTcSmem &sm =
+      *reinterpret_cast<ChainTcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+  const int s = blockIdx.x, h = blockIdx.y, role = blockIdx.z;
+  const int H = a.H;
+  const int n = a.plan.seg_seq[s];
+  if (n < 0) return;
+  const int j = s - a.plan.seq_seg0[n], nseg = a.plan.seq_nseg[n];
+  const int len = a.plan.seq_len[n], chunk0 = a.plan.seq_chunk0[n];
+  const int bos = a.plan.seq_bos[n];
+  const int nchunks = (len + CH - 1) / CH;
+  const int cbeg = j * a.Lseg, cend = min(cbeg + a.Lseg, nchunks);
+  const bool window = !(a.flags & kFlagWindowOff);
+  int w = 0;
+  const int mode = bwd_start_mode(a.gsum, H, h, chunk0, cend, nchunks, j, nseg, window, &w);
+  bool transition = false;
+  if (a.pass == 0) {
+    if (j == 0) return;
+    int w2;
+    if (bwd_start_mode(a.gsum, H, h, chunk0, cbeg, nchunks, j - 1, nseg, window, &w2) != START_FIXUP) return;
+    if (role == 1) {
+      if (mode != START_FIXUP) return;
+      transition = true;
+    }
+  } else if (role != 0) {
+    return;
+  }
+  const bool store = (a.pass == 1);
+  const bool l2 = (a.flags & kFlagL2Norm) != 0;
+  const bool with_do = !transition;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int wg = warp >> 2;
+  const int row = ((warp & 3) << 5) | lane;
+  const size_t DD = (size_t)D * D;
+  const size_t sh_idx = (size_t)s * H + h;
+  int clast = cend - 1;
+  if (mode == START_WARMUP && !transition) clast = cend - 1 + w;
+
+  if (tid == 0) {
+    mbar_init(u32(&sm.bar_tma[0]), 1);
+    mbar_init(u32(&sm.bar_tma[1]), 1);
+    mbar_init(u32(&sm.bar_mma), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmq);
+    tma_prefetch_desc(&tmdo);
+  }
+  if (warp == 0) {
+    tmem_alloc(u32(&sm.tmem_base), TM_COLS);
+    tmem_relinquish();
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tm = sm.tmem_base;
+  const uint32_t tl = (uint32_t)((warp & 3) * 32) << 16;
+
+  auto issue_tma = [&](int c, int stage) {
+    const int tok0 = bos + c * CH;
+    const uint32_t bar = u32(&sm.bar_tma[stage]);
+    uint8_t *st = sm.ring[stage];
+    mbar_expect_tx(bar, (2 + (with_do ? 4 : 0)) * HT);
+    tma_load_3d(u32(st + 0 * HT), &tmk, 0, h, tok0, bar);
+    tma_load_3d(u32(st + 2 * HT), &tmk, 64, h, tok0, bar);
+    if (with_do) {
+      tma_load_3d(u32(st + 1 * HT), &tmq, 0, h, tok0, bar);
+      tma_load_3d(u32(st + 3 * HT), &tmq, 64, h, tok0, bar);
+      tma_load_3d(u32(st + 4 * HT), &tmdo, 0, h, tok0, bar);
+      tma_load_3d(u32(st + 5 * HT), &tmdo, 64, h, tok0, bar);
+    }
+  };
+  auto issue_gb = [&](int c, int stage, bool with_g) {
+    const int tok0 = bos + c * CH;
+    const int nvalid = min(CH, len - c * CH);
+    if (with_g) load_scalars(sm.g[stage], a.g, H, h, tok0, nvalid, 0);
+    load_scalars(sm.beta[stage], a.beta, H, h, tok0, nvalid, 64);
+    cp_async_commit();
+  };
+  if (clast >= cbeg) {
+    if (tid == 0) issue_tma(clast, 0);
+    issue_gb(clast, 0, true);
+  }
+
+  // initial dS -> TMEM
+  {
+    const float *src = nullptr;
+    if (!transition) {
+      if (mode == START_INIT) src = a.dST ? a.dST + ((size_t)n * H + h) * DD : nullptr;
+      else if (mode == START_FIXUP && a.pass != 0) src = a.dSend + sh_idx * DD;
+    }
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int c0 = wg * 64 + half * 32;
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int col = c0 + i;
+        v[i] = src ? src[(size_t)row * D + col] : (transition && col == row ? 1.f : 0.f);
+      }
+      tmem_st32(tm + tl + TM_S + c0, v);
+    }
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+
+  int *err = a.status;
+  uint32_t mma_phase = 0;
+  bool failed = false;
+  auto mma_wait = [&]() {
+    const bool ok = mbar_wait(u32(&sm.bar_mma), mma_phase, err, 4);
+    mma_phase ^= 1;
+    fence_after();
+    return ok;
+  };
+
+  for (int c = clast; c >= cbeg && !failed; --c) {
+    const int it = clast - c;
+    const int stage = it & 1;
+    const int nvalid = min(CH, len - c * CH);
+    uint8_t *st = sm.ring[stage];
+    float *gbeta = sm.beta[stage];
+    float gnext0 = 0.f, gnext1 = 0.f;  // log-gates of the next (previous in time) chunk
+    if (warp == 0 && c - 1 >= cbeg) {
+      const int tokn = bos + (c - 1) * CH;
+      gnext0 = a.g[(size_t)(tokn + lane) * H + h];
+      gnext1 = a.g[(size_t)(tokn + lane + 32) * H + h];
+    }
+    cp_async_wait_all();
+    if (tid == 0 && c - 1 >= cbeg) issue_tma(c - 1, stage ^ 1);
+    if (c - 1 >= cbeg) issue_gb(c - 1, stage ^ 1, false);
+    const bool tma_ok = mbar_wait(u32(&sm.bar_tma[stage]), (it >> 1) & 1, err, 8);
+    if (__syncthreads_or(!tma_ok)) {
+      failed = true;
+      break;
+    }
+    Gates &G = sm.gt[stage];
+    if (it == 0 && warp == 0) gate_prefix(sm.g[stage], G);
+    __syncthreads();
+
+    // ---- prep: K^, Q^ (normalised, fp16) with Kc = cdec K^, Qg = gam Q^;  dO -> fp16; rows >= nvalid zero
+    {
+      const bool isq = tid >= 128;
+      if (!isq || with_do) {
+        const int r = (tid >> 1) & 63, hb = tid & 1;
+        uint8_t *rowp = st + (isq ? HT : 0) + hb * 2 * HT + r * 128;
+        uint32_t raw[32];
+#pragma unroll
+        for (int chk = 0; chk < 8; ++chk) {
+          const uint4 q4 = *reinterpret_cast<const uint4 *>(rowp + ((chk ^ (r & 7)) * 16));
+          raw[4 * chk] = q4.x;
+          raw[4 * chk + 1] = q4.y;
+          raw[4 * chk + 2] = q4.z;
+          raw[4 * chk + 3] = q4.w;
+        }
+        float mul = isq ? a.scale : 1.f;
+        if (l2) {
+          float ss = 0.f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float lo = __uint_as_float(raw[i] << 16), hi = __uint_as_float(raw[i] & 0xffff0000u);
+            ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+          }
+          ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+          mul *= rsqrtf(ss + 1e-6f);
+        }
+        if (r >= nvalid) mul = 0.f;
+        const float m2 = mul * (isq ? G.gam[r] : G.cdec[r]);
+        uint8_t *row2 = (isq ? sm.qg : sm.kc) + hb * HT + r * 128;
+#pragma unroll
+        for (int chk = 0; chk < 8; ++chk) {
+          uint32_t y[4], z[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t wv = raw[4 * chk + i];
+            const float lo = __uint_as_float(wv << 16), hi = __uint_as_float(wv & 0xffff0000u);
+            const __half2 a2 = __floats2half2_rn(lo * mul, hi * mul);
+            const __half2 b2 = __floats2half2_rn(lo * m2, hi * m2);
+            y[i] = *reinterpret_cast<const uint32_t *>(&a2);
+            z[i] = *reinterpret_cast<const uint32_t *>(&b2);
+          }
+          const int off = (chk ^ (r & 7)) * 16;
+          *reinterpret_cast<uint4 *>(rowp + off) = make_uint4(y[0], y[1], y[2], y[3]);
+          *reinterpret_cast<uint4 *>(row2 + off) = make_uint4(z[0], z[1], z[2], z[3]);
+        }
+      }
+      if (with_do) {
+        const int r = tid >> 2, qr = tid & 3;
+        uint8_t *rowp = st + 4 * HT + (qr >> 1) * HT + r * 128;
+        const float mul = r < nvalid ? 1.f : 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const int chk = (qr & 1) * 4 + cc;
+          uint4 q4 = *reinterpret_cast<const uint4 *>(rowp + ((chk ^ (r & 7)) * 16));
+          uint32_t *wv = reinterpret_cast<uint32_t *>(&q4);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const __half2 a2 = __floats2half2_rn(__uint_as_float(wv[i] << 16) * mul,
+                                                 __uint_as_float(wv[i] & 0xffff0000u) * mul);
+            wv[i] = *reinterpret_cast<const uint32_t *>(&a2);
+          }
+          *reinterpret_cast<uint4 *>(rowp + ((chk ^ (r & 7)) * 16)) = q4;
+        }
+      }
+    }
+    fence_async_smem();
+    __syncthreads();
+
+    // ---- MMA 1: [K; Q] K^T
+    if (tid == 0) {
+      fence_after();
+      const uint32_t idesc = idesc_f16(128, 64, false, false);
+      const uint32_t base = u32(st);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t koff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
+        mma_f16(tm + TM_KQ, sdesc(base + koff, 16, 1024), sdesc(base + koff, 16, 1024), idesc, kk > 0);
+      }
+      mma_commit(u32(&sm.bar_mma));
+    }
+    __syncwarp();
+    if (__syncthreads_or(!mma_wait())) {
+      failed = true;
+      break;
+    }
+    if (row < 64 || with_do) {
+      float v[32];
+      const int c0 = wg * 32;
+      tmem_ld32(tm + tl + TM_KQ + c0, v);
+      if (row < 64) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sm.nf[row * LN + c0 + i] = v[i];
+      } else {
+        const int r = row - 64;
+        const float gr = G.gp[r];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          float y[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int col = c0 + q4 * 8 + i;
+            y[i] = col <= r ? v[q4 * 8 + i] * gr * G.rgp[col] : 0.f;
+          }
+          st_chunk_f16(sm.p + r * 128 + ((((c0 >> 3) + q4) ^ (r & 7)) * 16), y);
+        }
+      }
+    }
+    fence_before();
+    __syncthreads();
+    wy_inverse<false, false>(sm.nf, LN, gbeta, sm.ys, [&](int r, int cc, float a0, float a1) {
+      *reinterpret_cast<__half2 *>(sm.x1 + sw128_offset(r, cc)) = __floats2half2_rn(a0 * gbeta[cc], a1 * gbeta[cc + 1]);
+    });
+
+    // ---- MMA 2: W^T = K^T X1^T;  meanwhile dS -> fp16 operand copy (+ workspace), gam_C dS back to TMEM
+    if (tid == 0) {
+      fence_after();
+      const uint32_t idesc = idesc_f16(128, 64, true, false);
+      const uint32_t kb = u32(st), x1b = u32(sm.x1);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_f16(tm + TM_W, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(x1b + kk * 32, 16, 1024), idesc, kk > 0);
+      mma_commit(u32(&sm.bar_mma));
+    }
+    __syncwarp();
+    {
+      const float gC = G.gamC;
+      f16 *stg = store && c < cend
+                     ? static_cast<f16 *>(a.dstates) + ((size_t)(chunk0 + c) * H + h) * DD + (size_t)row * D
+                     : nullptr;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int c0 = wg * 64 + half * 32;
+        float v[32];
+        tmem_ld32(tm + tl + TM_S + c0, v);
+        const int kb = c0 >> 6;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int chk = ((c0 & 63) >> 3) + q4;
+          uint8_t *dst = sm.ds16 + kb * 2 * HT + row * 128 + ((chk ^ (row & 7)) * 16);
+          st_chunk_f16(dst, v + q4 * 8);
+          if (stg) *reinterpret_cast<uint4 *>(stg + c0 + q4 * 8) = *reinterpret_cast<const uint4 *>(dst);
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= gC;
+        tmem_st32(tm + tl + TM_S + c0, v);
+      }
+    }
+    if (__syncthreads_or(!mma_wait())) {
+      failed = true;
+      break;
+    }
+    {  // W^T read-out, columns scaled by gam
+      const int c0 = wg * 32;
+      float v[32];
+      tmem_ld32(tm + tl + TM_W + c0, v);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float y[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) y[i] = v[q4 * 8 + i] * G.gam[c0 + q4 * 8 + i];
+        st_chunk_f16(sm.wt + row * 128 + ((((c0 >> 3) + q4) ^ (row & 7)) * 16), y);
+      }
+    }
+    fence_before();
+    fence_async_smem();
+    __syncthreads();
+
+    // ---- MMA 3: dUt^T = dS Kc^T + dO^T P   (M = 128, N = 64)
+    if (tid == 0) {
+      fence_after();
+      const uint32_t id_kk = idesc_f16(128, 64, false, false);
+      const uint32_t id_mm = idesc_f16(128, 64, true, true);
+      const uint32_t dsb = u32(sm.ds16), kcb = u32(sm.kc), dob = u32(st + 4 * HT), pb = u32(sm.p);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
+        const uint32_t boff = (kk >> 2) * HT + (kk & 3) * 32;
+        mma_f16(tm + TM_DU, sdesc(dsb + aoff, 16, 1024), sdesc(kcb + boff, 16, 1024), id_kk, kk > 0);
+      }
+      if (with_do) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f16(tm + TM_DU, sdesc(dob + kk * 2048, HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id_mm, true);
+      }
+      mma_commit(u32(&sm.bar_mma));
+    }
+    __syncwarp();
+    if (__syncthreads_or(!mma_wait())) {
+      failed = true;
+      break;
+    }
+    {  // dUt^T -> fp16 K-major A (rows = d_v, k = token) in the Kc space (Kc is dead)
+      const int c0 = wg * 32;
+      float v[32];
+      tmem_ld32(tm + tl + TM_DU + c0, v);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+        st_chunk_f16(sm.kc + row * 128 + ((((c0 >> 3) + q4) ^ (row & 7)) * 16), v + q4 * 8);
+    }
+    fence_before();
+    fence_async_smem();
+    __syncthreads();
+
+    // ---- MMA 4: dS += dO^T Qg - dUt^T W   (M = 128, N = 128)
+    if (tid == 0) {
+      fence_after();
+      const uint32_t id_mm = idesc_f16(128, 128, true, true);
+      const uint32_t id_kk_neg = idesc_f16(128, 128, false, false, true);
+      const uint32_t dob = u32(st + 4 * HT), qgb = u32(sm.qg), dub = u32(sm.kc), wb = u32(sm.wt);
+      if (with_do) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f16(tm + TM_S, sdesc(dob + kk * 2048, HT, 1024), sdesc(qgb + kk * 2048, HT, 1024), id_mm, true);
+      }
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_f16(tm + TM_S, sdesc(dub + kk * 32, 16, 1024), sdesc(wb + kk * 32, 16, 1024), id_kk_neg, true);
+      mma_commit(u32(&sm.bar_mma));
+    }
+    __syncwarp();
+    if (warp == 0 && c - 1 >= cbeg) {  // gates of the next chunk, overlapping MMA 4
+      float *gn = sm.g[stage ^ 1];
+      const int nvn = min(CH, len - (c - 1) * CH);
+      gn[lane] = lane < nvn ? gnext0 : 0.f;
+      gn[lane + 32] = lane + 32 < nvn ? gnext1 : 0.f;
+      __syncwarp();
+      gate_prefix(gn, sm.gt[stage ^ 1]);
+    }
+    if (__syncthreads_or(!mma_wait())) {
+      failed = true;
+      break;
+    }
+  }
+
+  if (!failed) {
+    float *dst = nullptr;
+    if (a.pass == 0) dst = (transition ? a.Rbuf : a.Fbuf) + sh_idx * DD;
+    else if (j == 0 && a.dS0) dst = a.dS0 + ((size_t)n * H + h) * DD;
+    if (dst) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int c0 = wg * 64 + half * 32;
+        float v[32];
+        tmem_ld32(tm + tl + TM_S + c0, v);
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4)
+          *reinterpret_cast<float4 *>(dst + (size_t)row * D + c0 + 4 * q4) =
+              make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+      }
+    }
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp == 0) tmem_dealloc(tm, TM_COLS);
+}
+
+int launch_bwd_chain_tc(const BwdArgs &a, const CUtensorMap *maps, dim3 grid, cudaStream_t st) {
+  const size_t smem = sizeof(ChainTcSmem) + 1024;
+  static_assert(sizeof(ChainTcSmem) + 1024 <= 232448, "shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(bwd_chain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return (int)e;
+  bwd_chain_tc_kernel<<<grid, NTHREADS, smem, st>>>(a, maps[0], maps[1], maps[2]);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace gdn

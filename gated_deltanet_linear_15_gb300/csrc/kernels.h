@@ -64,6 +64,8 @@ int launch_fwd_chunk(const FwdArgs &a, bool is_bf16, int D, dim3 grid, cudaStrea
 int launch_fwd_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, dim3 grid,
                   cudaStream_t st);
 int launch_bwd_chain(const BwdArgs &a, bool is_bf16, int D, dim3 grid, cudaStream_t st);
+// tcgen05 reverse chain (bf16, d = 128); maps: q, k, dO ([tokens, H, 128] bf16, box 64x1x64)
+int launch_bwd_chain_tc(const BwdArgs &a, const CUtensorMap *maps, dim3 grid, cudaStream_t st);
 int launch_bwd_local(const BwdArgs &a, bool is_bf16, int D, int CH_max, cudaStream_t st);
 // tcgen05 local-gradient kernel (bf16, d = 128); maps: q, k, v, dO ([tokens, H, 128] bf16, box 64x1x64) and
 // the fp16 per-chunk states S0 and dS ([rows, 128] as a 3-D map, box 64x128x1)
