@@ -94,6 +94,28 @@ __device__ __forceinline__ float colsum32(float (&v)[32]) {
   return v[0];
 }
 
+// v[8] per lane -> lane l holds the sum over the warp's lanes of v[l % 8]
+__device__ __forceinline__ float colsum8(float (&v)[8]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int s = 4; s >= 1; s >>= 1) {
+#pragma unroll
+    for (int i = 0; i < s; ++i) {
+      const bool up = (lane & s) != 0;
+      const float send = up ? v[i] : v[i + s];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, s);
+      v[i] = (up ? v[i + s] : v[i]) + recv;
+    }
+  }
+  float t = v[0];
+  t += __shfl_xor_sync(0xffffffffu, t, 8);
+  t += __shfl_xor_sync(0xffffffffu, t, 16);
+  return t;
+}
+
+// byte offset of the 16-byte chunk holding columns [cb, cb + 8) of row r in a swizzled tile
+__device__ __forceinline__ uint32_t chunk_off(int r, int cb) { return r * 128 + ((((cb & 63) >> 3) ^ (r & 7)) << 4); }
+
 }  // namespace
 
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -167,40 +189,44 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (__syncthreads_or(!ok)) goto out;
   if (warp == 0) gate_prefix(sm.g, sm.gt);
   // ---- prep: bf16 -> fp16 in place; q, k normalised (norms kept for the Jacobians); rows >= nvalid zero
+#pragma unroll 1
   for (int task = tid; task < 4 * 2 * CH; task += NTHREADS) {
     const int t = task >> 7;  // 0 K, 1 Q, 2 V, 3 dO
     const int r = (task >> 1) & 63, hb = task & 1;
     uint8_t *rowp = (t == 0 ? sm.kq : t == 1 ? sm.kq + HT : t == 2 ? sm.v : sm.dob) +
                     hb * (t < 2 ? 2 * HT : HT) + r * 128;
-    float x[64];
-#pragma unroll
-    for (int chk = 0; chk < 8; ++chk) {
-      const uint4 raw = *reinterpret_cast<const uint4 *>(rowp + ((chk ^ (r & 7)) * 16));
-      const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(b2[i]);
-        x[chk * 8 + 2 * i] = f.x;
-        x[chk * 8 + 2 * i + 1] = f.y;
-      }
-    }
     float mul = (t == 1) ? a.scale : 1.f;
     if (l2 && t < 2) {
       float ss = 0.f;
+#pragma unroll 1
+      for (int chk = 0; chk < 8; ++chk) {
+        const uint4 raw = *reinterpret_cast<const uint4 *>(rowp + ((chk ^ (r & 7)) * 16));
+        const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
 #pragma unroll
-      for (int i = 0; i < 64; ++i) ss += x[i] * x[i];
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(b2[i]);
+          ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+        }
+      }
       ss += __shfl_xor_sync(0xffffffffu, ss, 1);
       const float rn = 1.f / sqrtf(ss + 1e-6f);
       mul = mul * rn;
       if (hb == 0) (t == 0 ? sm.nk : sm.nq)[r] = rn;
     }
     if (r >= nvalid) mul = 0.f;
-#pragma unroll
+#pragma unroll 1
     for (int chk = 0; chk < 8; ++chk) {
+      uint8_t *cp = rowp + ((chk ^ (r & 7)) * 16);
+      const uint4 raw = *reinterpret_cast<const uint4 *>(cp);
+      const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
       float y[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) y[i] = x[chk * 8 + i] * mul;
-      st_chunk_f16(rowp + ((chk ^ (r & 7)) * 16), y);
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(b2[i]);
+        y[2 * i] = f.x * mul;
+        y[2 * i + 1] = f.y * mul;
+      }
+      st_chunk_f16(cp, y);
     }
   }
   fence_async_smem();
@@ -210,7 +236,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (tid == 0) {
     fence_after();
     const uint32_t id = idesc_f16(128, 64, false, false), kb = u32(sm.kq);
-#pragma unroll
+#pragma unroll 1
     for (int kk = 0; kk < 8; ++kk) {
       const uint32_t off = (kk >> 2) * 2 * HT + (kk & 3) * 32;
       mma_f16(tm + T0, sdesc(kb + off, 16, 1024), sdesc(kb + off, 16, 1024), id, kk > 0);
@@ -220,25 +246,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncwarp();
   if (__syncthreads_or(!mma_done())) goto out;
   // R1: rows 0-63 -> N (fp32), rows 64-127 -> P (fp16, [r][i])
-  {
-    float v[32];
-    tmem_ld32(tm + tl + T0 + c0, v);
+#pragma unroll 1
+  for (int q4 = 0; q4 < 4; ++q4) {
+    const int cb = c0 + q4 * 8;
+    float v[8];
+    tmem_ld8(tm + tl + T0 + cb, v);
     if (row < 64) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) sm.nf[row * LN + c0 + i] = v[i];
+      float4 *dst = reinterpret_cast<float4 *>(&sm.nf[row * LN + cb]);
+      dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+      dst[1] = make_float4(v[4], v[5], v[6], v[7]);
     } else {
       const int r = row - 64;
       const float gr = sm.gt.gp[r];
+      float y[8];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        float y[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int col = c0 + q4 * 8 + i;
-          y[i] = col <= r ? v[q4 * 8 + i] * gr * sm.gt.rgp[col] : 0.f;
-        }
-        st_chunk_f16(sm.p + r * 128 + ((((c0 >> 3) + q4) ^ (r & 7)) * 16), y);
-      }
+      for (int i = 0; i < 8; ++i) y[i] = cb + i <= r ? v[i] * gr * sm.gt.rgp[cb + i] : 0.f;
+      st_chunk_f16(sm.p + chunk_off(r, cb), y);
     }
   }
   fence_before();
@@ -258,7 +281,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     fence_after();
     const uint32_t id = idesc_f16(128, 64, true, false);
     const uint32_t kb = u32(sm.kq), vb = u32(sm.v), x1b = u32(sm.x1), x2b = u32(sm.x2);
-#pragma unroll
+#pragma unroll 1
     for (int kk = 0; kk < 4; ++kk) {
       mma_f16(tm + T1, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(x1b + kk * 32, 16, 1024), id, kk > 0);
       mma_f16(tm + T2, sdesc(vb + kk * 2048, HT, 1024), sdesc(x2b + kk * 32, 16, 1024), id, kk > 0);
@@ -267,16 +290,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   __syncwarp();
   if (__syncthreads_or(!mma_done())) goto out;
-  {  // R2: W^T (lanes d_k, columns token) * gam -> wt
-    float v[32];
-    tmem_ld32(tm + tl + T1 + c0, v);
+  // R2: W^T (lanes d_k, columns token) * gam -> wt
+#pragma unroll 1
+  for (int q4 = 0; q4 < 4; ++q4) {
+    const int cb = c0 + q4 * 8;
+    float v[8];
+    tmem_ld8(tm + tl + T1 + cb, v);
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      float y[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) y[i] = v[q4 * 8 + i] * sm.gt.gam[c0 + q4 * 8 + i];
-      st_chunk_f16(sm.wt + row * 128 + ((((c0 >> 3) + q4) ^ (row & 7)) * 16), y);
-    }
+    for (int i = 0; i < 8; ++i) v[i] *= sm.gt.gam[cb + i];
+    st_chunk_f16(sm.wt + chunk_off(row, cb), v);
   }
   fence_before();
   fence_async_smem();
@@ -286,6 +308,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   {  // <dS, S0> over the whole state (both tiles share one layout, so compare byte positions)
     float acc = 0.f;
     const uint4 *A4 = reinterpret_cast<const uint4 *>(sm.s0), *B4 = reinterpret_cast<const uint4 *>(sm.ds);
+#pragma unroll 2
     for (int e = tid; e < 4 * HT / 16; e += NTHREADS) {
       const uint4 x = A4[e], y = B4[e];
       const __half2 *xh = reinterpret_cast<const __half2 *>(&x), *yh = reinterpret_cast<const __half2 *>(&y);
@@ -304,7 +327,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     fence_after();
     const uint32_t id = idesc_f16(128, 64, false, true, true);
     const uint32_t sb = u32(sm.s0), wb = u32(sm.wt);
-#pragma unroll
+#pragma unroll 1
     for (int kk = 0; kk < 8; ++kk)
       mma_f16(tm + T2, sdesc(sb + (kk >> 2) * 2 * HT + (kk & 3) * 32, 16, 1024), sdesc(wb + kk * 2048, 2 * HT, 1024),
               id, true);
@@ -312,12 +335,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   __syncwarp();
   if (__syncthreads_or(!mma_done())) goto out;
-  {  // R3: Ut^T -> ut
-    float v[32];
-    tmem_ld32(tm + tl + T2 + c0, v);
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4)
-      st_chunk_f16(sm.ut + row * 128 + ((((c0 >> 3) + q4) ^ (row & 7)) * 16), v + q4 * 8);
+  // R3: Ut^T -> ut
+#pragma unroll 1
+  for (int q4 = 0; q4 < 4; ++q4) {
+    const int cb = c0 + q4 * 8;
+    float v[8];
+    tmem_ld8(tm + tl + T2 + cb, v);
+    st_chunk_f16(sm.ut + chunk_off(row, cb), v);
   }
   fence_before();
   fence_async_smem();
@@ -330,14 +354,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t id_mm = idesc_f16(128, 64, true, true);
     const uint32_t id_mk = idesc_f16(128, 64, true, false);
     const uint32_t dsb = u32(sm.ds), kb = u32(sm.kq), dob = u32(sm.dob), pb = u32(sm.p), sb = u32(sm.s0);
-#pragma unroll
+#pragma unroll 1
     for (int kk = 0; kk < 8; ++kk) {
       const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
       mma_f16(tm + T3, sdesc(dsb + aoff, 16, 1024), sdesc(kb + aoff, 16, 1024), id_kk, kk > 0);
       mma_f16(tm + T5, sdesc(sb + kk * 2048, 2 * HT, 1024), sdesc(dob + (kk >> 2) * HT + (kk & 3) * 32, 16, 1024),
               id_mk, kk > 0);
     }
-#pragma unroll
+#pragma unroll 1
     for (int kk = 0; kk < 4; ++kk)
       mma_f16(tm + T4, sdesc(dob + kk * 2048, HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id_mm, kk > 0);
     mma_commit(u32(&sm.bar_mma));
@@ -345,22 +369,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncwarp();
   if (__syncthreads_or(!mma_done())) goto out;
   {  // R4: dUt^T = cdec*Y + Z -> wt (W^T is dead);  per-token sums <Ut, Y>, <dUt, Ut> over d_v
-    float y[32], z[32], u[32];
-    tmem_ld32(tm + tl + T3 + c0, y);
-    tmem_ld32(tm + tl + T4 + c0, z);
-    tmem_ld32(tm + tl + T2 + c0, u);
-    float s1[32], s2[32];
+    float t1 = 0.f, t2 = 0.f;
+#pragma unroll 1
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const int cb = c0 + q4 * 8;
+      float y[8], z[8], u[8], s1[8], s2[8];
+      tmem_ld8(tm + tl + T3 + cb, y);
+      tmem_ld8(tm + tl + T4 + cb, z);
+      tmem_ld8(tm + tl + T2 + cb, u);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float du = sm.gt.cdec[c0 + i] * y[i] + z[i];
-      s1[i] = u[i] * y[i];
-      s2[i] = du * u[i];
-      z[i] = du;
+      for (int i = 0; i < 8; ++i) {
+        const float du = sm.gt.cdec[cb + i] * y[i] + z[i];
+        s1[i] = u[i] * y[i];
+        s2[i] = du * u[i];
+        z[i] = du;
+      }
+      st_chunk_f16(sm.wt + chunk_off(row, cb), z);
+      const float a1 = colsum8(s1), a2 = colsum8(s2);
+      if ((lane >> 3) == q4) {
+        t1 = a1;
+        t2 = a2;
+      }
     }
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4)
-      st_chunk_f16(sm.wt + row * 128 + ((((c0 >> 3) + q4) ^ (row & 7)) * 16), z + q4 * 8);
-    const float t1 = colsum32(s1), t2 = colsum32(s2);
     sm.part[wq][c0 + lane] = t1;
     sm.part[4 + wq][c0 + lane] = t2;
   }
@@ -378,14 +408,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t id_kmn = idesc_f16(128, 64, false, true);
     const uint32_t id_mmn_neg = idesc_f16(128, 64, true, true, true);
     const uint32_t dob = u32(sm.dob), ub = u32(sm.ut), sb = u32(sm.s0), dub = u32(sm.wt), x2b = u32(sm.x2);
-#pragma unroll
+#pragma unroll 1
     for (int kk = 0; kk < 8; ++kk) {
       mma_f16(tm + T0, sdesc(dob + (kk >> 2) * HT + (kk & 3) * 32, 16, 1024), sdesc(ub + kk * 2048, 2 * HT, 1024),
               id_kmn, kk > 0);
       mma_f16(tm + T1, sdesc(sb + kk * 2048, 2 * HT, 1024), sdesc(dub + kk * 2048, 2 * HT, 1024), id_mmn_neg,
               kk > 0);
     }
-#pragma unroll
+#pragma unroll 1
     for (int kk = 0; kk < 4; ++kk)
       mma_f16(tm + T6, sdesc(dub + kk * 32, 16, 1024), sdesc(x2b + kk * 2048, HT, 1024), id_kmn, kk > 0);
     mma_commit(u32(&sm.bar_mma));
@@ -395,57 +425,60 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   {
     // dP rows (lanes 0-63): Z = dP * P row sums (thread-local) and column sums; dPm over P
     if (row < 64) {
-      float v[32], zc[32];
-      tmem_ld32(tm + tl + T0 + c0, v);
       const int r = row;
       const float gr = sm.gt.gp[r];
-      float rs = 0.f;
-#pragma unroll
+      float rs = 0.f, cs = 0.f;
+#pragma unroll 1
       for (int q4 = 0; q4 < 4; ++q4) {
-        uint8_t *pp = sm.p + r * 128 + ((((c0 >> 3) + q4) ^ (r & 7)) * 16);
+        const int cb = c0 + q4 * 8;
+        float v[8], zc[8], y[8];
+        tmem_ld8(tm + tl + T0 + cb, v);
+        uint8_t *pp = sm.p + chunk_off(r, cb);
         const uint4 raw = *reinterpret_cast<const uint4 *>(pp);
         const __half *ph = reinterpret_cast<const __half *>(&raw);
-        float y[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int col = c0 + q4 * 8 + i;
-          const float dpv = v[q4 * 8 + i];
+          const float dpv = v[i];
           const float zz = dpv * __half2float(ph[i]);
           rs += zz;
-          zc[q4 * 8 + i] = zz;
-          y[i] = col <= r ? dpv * gr * sm.gt.rgp[col] : 0.f;
+          zc[i] = zz;
+          y[i] = cb + i <= r ? dpv * gr * sm.gt.rgp[cb + i] : 0.f;
         }
         st_chunk_f16(pp, y);
+        const float a = colsum8(zc);
+        if ((lane >> 3) == q4) cs = a;
       }
-      sm.part[8 + wg][r] = rs;  // row sums of Z, per column half
-      const float cs = colsum32(zc);
+      sm.part[8 + wg][r] = rs;           // row sums of Z, per column half
       sm.part[10 + wq][c0 + lane] = cs;  // column sums of Z, per row quarter (wq 0/1)
     }
     // dW'^T (lanes d_k) * gam -> s0 region (S0 is dead)
-    {
-      float v[32];
-      tmem_ld32(tm + tl + T1 + c0, v);
+#pragma unroll 1
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const int cb = c0 + q4 * 8;
+      float v[8];
+      tmem_ld8(tm + tl + T1 + cb, v);
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        float y[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) y[i] = v[q4 * 8 + i] * sm.gt.gam[c0 + q4 * 8 + i];
-        st_chunk_f16(sm.s0 + row * 128 + ((((c0 >> 3) + q4) ^ (row & 7)) * 16), y);
-      }
+      for (int i = 0; i < 8; ++i) v[i] *= sm.gt.gam[cb + i];
+      st_chunk_f16(sm.s0 + chunk_off(row, cb), v);
     }
     // dV^T (lanes d_v, columns token): stage bf16 dv[token][d_v] in dob (dO is dead); <dV, v>
     {
-      float v[32];
-      tmem_ld32(tm + tl + T6 + c0, v);
       bf16 *stg = reinterpret_cast<bf16 *>(sm.dob);
-      float sv[32];
+      float t = 0.f;
+#pragma unroll 1
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int cb = c0 + q4 * 8;
+        float v[8], sv[8];
+        tmem_ld8(tm + tl + T6 + cb, v);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int tkn = c0 + i;
-        stg[tkn * D + row] = __float2bfloat16_rn(v[i]);
-        sv[i] = v[i] * ld_f16(sm.v, tkn, row, HT);
+        for (int i = 0; i < 8; ++i) {
+          const int tkn = cb + i;
+          stg[tkn * D + row] = __float2bfloat16_rn(v[i]);
+          sv[i] = v[i] * ld_f16(sm.v, tkn, row, HT);
+        }
+        const float a = colsum8(sv);
+        if ((lane >> 3) == q4) t = a;
       }
-      const float t = colsum32(sv);
       sm.part[12 + wq][c0 + lane] = t;
     }
   }
@@ -472,10 +505,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     fence_after();
     const uint32_t id_mk = idesc_f16(128, 64, true, false);
     const uint32_t kb = u32(sm.kq), pb = u32(sm.p), dwb = u32(sm.s0), dub = u32(sm.wt), vb = u32(sm.v);
-#pragma unroll
+#pragma unroll 1
     for (int kk = 0; kk < 4; ++kk)
       mma_f16(tm + T7, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(pb + kk * 32, 16, 1024), id_mk, kk > 0);
-#pragma unroll
+#pragma unroll 1
     for (int kk = 0; kk < 8; ++kk) {
       const uint32_t boff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
       mma_f16(tm + T3, sdesc(dwb + kk * 2048, 2 * HT, 1024), sdesc(kb + boff, 16, 1024), id_mk, kk > 0);
@@ -488,68 +521,81 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (__syncthreads_or(!mma_done())) goto out;
   {
     // dq^T = gam*Qa + Qb (lanes d_k): <dQ1, q^> and Jacobian dots over d_k; stage dq^ (fp32 kept in regs)
-    float qa[32], qb[32], s1[32], s2[32], qv[32];
-    tmem_ld32(tm + tl + T5 + c0, qa);
-    tmem_ld32(tm + tl + T7 + c0, qb);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int tkn = c0 + i;
-      qv[i] = ld_f16(sm.kq + HT, tkn, row, 2 * HT);
-      const float a1 = sm.gt.gam[tkn] * qa[i];
-      qb[i] += a1;  // dq^ (w.r.t. the normalised, scaled q)
-      s1[i] = a1 * qv[i];
-      s2[i] = qb[i] * qv[i];
-    }
-    const float t1 = colsum32(s1), t2 = colsum32(s2);
-    sm.part[wq][c0 + lane] = t1;
-    sm.part[4 + wq][c0 + lane] = t2;
-    // M1, M2 (lanes 0-63 = r): dAhat = beta_i (M1 + Gamma M2); beta column sums colsum_i(Ahat (M1 + Gamma M2))
-    if (row < 64) {
-      float m1[32], m2[32];
-      tmem_ld32(tm + tl + T3 + c0, m1);
-      tmem_ld32(tm + tl + T4 + c0, m2);
-      const int r = row;
-      const float gr = sm.gt.gp[r];
-      float ahr[32];
-#pragma unroll
+    {
+      float t1 = 0.f, t2 = 0.f;
+#pragma unroll 1
       for (int q4 = 0; q4 < 4; ++q4) {
-        const uint4 raw = *reinterpret_cast<const uint4 *>(sm.ah + r * 128 + ((((c0 >> 3) + q4) ^ (r & 7)) * 16));
-        const __half2 *hh = reinterpret_cast<const __half2 *>(&raw);
+        const int cb = c0 + q4 * 8;
+        float qa[8], qb[8], s1[8], s2[8];
+        tmem_ld8(tm + tl + T5 + cb, qa);
+        tmem_ld8(tm + tl + T7 + cb, qb);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __half22float2(hh[i]);
-          ahr[q4 * 8 + 2 * i] = f.x;
-          ahr[q4 * 8 + 2 * i + 1] = f.y;
+        for (int i = 0; i < 8; ++i) {
+          const int tkn = cb + i;
+          const float qv = ld_f16(sm.kq + HT, tkn, row, 2 * HT);
+          const float a1 = sm.gt.gam[tkn] * qa[i];
+          s1[i] = a1 * qv;
+          s2[i] = (qb[i] + a1) * qv;  // dq^ (w.r.t. the normalised, scaled q) times q^
+        }
+        const float a1 = colsum8(s1), a2 = colsum8(s2);
+        if ((lane >> 3) == q4) {
+          t1 = a1;
+          t2 = a2;
         }
       }
+      sm.part[wq][c0 + lane] = t1;
+      sm.part[4 + wq][c0 + lane] = t2;
+    }
+    // M1, M2 (lanes 0-63 = r): dAhat = beta_i (M1 + Gamma M2); beta column sums colsum_i(Ahat (M1 + Gamma M2))
+    if (row < 64) {
+      const int r = row;
+      const float gr = sm.gt.gp[r];
+      float cs = 0.f;
+#pragma unroll 1
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int cb = c0 + q4 * 8;
+        float m1[8], m2[8];
+        tmem_ld8(tm + tl + T3 + cb, m1);
+        tmem_ld8(tm + tl + T4 + cb, m2);
+        const uint4 raw = *reinterpret_cast<const uint4 *>(sm.ah + chunk_off(r, cb));
+        const __half *hh = reinterpret_cast<const __half *>(&raw);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int col = c0 + i;
-        const float x = m1[i] + (col <= r ? m2[i] * gr * sm.gt.rgp[col] : 0.f);
-        m2[i] = ahr[i] * x;
-        m1[i] = sm.beta[col] * x;
+        for (int i = 0; i < 8; ++i) {
+          const int col = cb + i;
+          const float x = m1[i] + (col <= r ? m2[i] * gr * sm.gt.rgp[col] : 0.f);
+          m2[i] = __half2float(hh[i]) * x;
+          m1[i] = sm.beta[col] * x;
+        }
+        st_chunk_f16(sm.x2 + chunk_off(r, cb), m1);
+        const float a = colsum8(m2);
+        if ((lane >> 3) == q4) cs = a;
       }
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4)
-        st_chunk_f16(sm.x2 + r * 128 + ((((c0 >> 3) + q4) ^ (r & 7)) * 16), m1 + q4 * 8);
-      const float cs = colsum32(m2);
       sm.part[8 + wq][c0 + lane] = cs;
     }
     __syncthreads();
     // dq raw = (scale dq^ - q^ (q^ . dq^) / scale) / |q|   (or scale dq^ without normalisation)
     bf16 *stg = reinterpret_cast<bf16 *>(sm.dob);
     const float rscale = 1.f / a.scale;
+#pragma unroll 1
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const int cb = c0 + q4 * 8;
+      float qa[8], qb[8];
+      tmem_ld8(tm + tl + T5 + cb, qa);
+      tmem_ld8(tm + tl + T7 + cb, qb);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int tkn = c0 + i;
-      float o;
-      if (l2) {
-        const float dot = sm.part[4][tkn] + sm.part[5][tkn] + sm.part[6][tkn] + sm.part[7][tkn];
-        o = (a.scale * qb[i] - qv[i] * dot * rscale) * sm.nq[tkn];
-      } else {
-        o = a.scale * qb[i];
+      for (int i = 0; i < 8; ++i) {
+        const int tkn = cb + i;
+        const float dq = qb[i] + sm.gt.gam[tkn] * qa[i];
+        float o;
+        if (l2) {
+          const float qv = ld_f16(sm.kq + HT, tkn, row, 2 * HT);
+          const float dot = sm.part[4][tkn] + sm.part[5][tkn] + sm.part[6][tkn] + sm.part[7][tkn];
+          o = (a.scale * dq - qv * dot * rscale) * sm.nq[tkn];
+        } else {
+          o = a.scale * dq;
+        }
+        stg[tkn * D + row] = __float2bfloat16_rn(o);
       }
-      stg[tkn * D + row] = __float2bfloat16_rn(o);
     }
   }
   fence_before();
@@ -574,7 +620,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     fence_after();
     const uint32_t id = idesc_f16(128, 64, true, true);
     const uint32_t ab = u32(sm.ah), dab = u32(sm.x2);
-#pragma unroll
+#pragma unroll 1
     for (int kk = 0; kk < 4; ++kk)
       mma_f16(tm + T0, sdesc(ab + kk * 2048, HT, 1024), sdesc(dab + kk * 2048, HT, 1024), id, kk > 0);
     mma_commit(u32(&sm.bar_mma));
@@ -582,11 +628,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncwarp();
   if (__syncthreads_or(!mma_done())) goto out;
   if (row < 64) {  // R7: Y1 -> v (first half; V is dead)
-    float v[32];
-    tmem_ld32(tm + tl + T0 + c0, v);
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4)
-      st_chunk_f16(sm.v + row * 128 + ((((c0 >> 3) + q4) ^ (row & 7)) * 16), v + q4 * 8);
+#pragma unroll 1
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const int cb = c0 + q4 * 8;
+      float v[8];
+      tmem_ld8(tm + tl + T0 + cb, v);
+      st_chunk_f16(sm.v + chunk_off(row, cb), v);
+    }
   }
   fence_before();
   fence_async_smem();
@@ -597,31 +645,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     fence_after();
     const uint32_t id = idesc_f16(128, 64, false, false, true);
     const uint32_t yb = u32(sm.v), ab = u32(sm.ah);
-#pragma unroll
+#pragma unroll 1
     for (int kk = 0; kk < 4; ++kk) mma_f16(tm + T1, sdesc(yb + kk * 32, 16, 1024), sdesc(ab + kk * 32, 16, 1024), id, kk > 0);
     mma_commit(u32(&sm.bar_mma));
   }
   __syncwarp();
   if (__syncthreads_or(!mma_done())) goto out;
   if (row < 64) {  // R8: dN[r][i] = beta_r dT_ri (i < r), zero elsewhere; beta row sums of dT * N
-    float v[32];
-    tmem_ld32(tm + tl + T1 + c0, v);
     const int r = row;
     const float br = sm.beta[r];
     uint8_t *sg = sm.v + HT;
     float rb = 0.f;
-#pragma unroll
+#pragma unroll 1
     for (int q4 = 0; q4 < 4; ++q4) {
-      float y[8];
+      const int cb = c0 + q4 * 8;
+      float v[8], y[8];
+      tmem_ld8(tm + tl + T1 + cb, v);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const int col = c0 + q4 * 8 + i;
-        const float dt = v[q4 * 8 + i];
+        const int col = cb + i;
         const bool lo = col < r;
-        rb += lo ? dt * sm.nf[r * LN + col] : 0.f;
-        y[i] = lo ? br * dt : 0.f;
+        rb += lo ? v[i] * sm.nf[r * LN + col] : 0.f;
+        y[i] = lo ? br * v[i] : 0.f;
       }
-      st_chunk_f16(sg + r * 128 + ((((c0 >> 3) + q4) ^ (r & 7)) * 16), y);
+      st_chunk_f16(sg + chunk_off(r, cb), y);
     }
     sm.part[12 + wg][r] = rb;
   }
@@ -637,7 +684,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t id_mk = idesc_f16(128, 64, true, false);
     const uint32_t kb = u32(sm.kq), pb = u32(sm.p), dwb = u32(sm.s0), x1b = u32(sm.x1), sgb = u32(sm.v + HT);
     const uint32_t dsb = u32(sm.ds), ub = u32(sm.ut);
-#pragma unroll
+#pragma unroll 1
     for (int kk = 0; kk < 4; ++kk) {
       mma_f16(tm + T3, sdesc(kb + HT + kk * 2048, 2 * HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id_mm, kk > 0);
       mma_f16(tm + T3, sdesc(dwb + kk * 32, 16, 1024), sdesc(x1b + kk * 2048, HT, 1024), id_km, true);
@@ -645,7 +692,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mma_f16(tm + T3, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(sgb + kk * 2048, HT, 1024), id_mm, true);
       mma_f16(tm + T3, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(sgb + kk * 32, 16, 1024), id_mk, true);
     }
-#pragma unroll
+#pragma unroll 1
     for (int kk = 0; kk < 8; ++kk)
       mma_f16(tm + T4, sdesc(dsb + kk * 2048, 2 * HT, 1024), sdesc(ub + kk * 2048, 2 * HT, 1024), id_mm, kk > 0);
     mma_commit(u32(&sm.bar_mma));
@@ -653,29 +700,42 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncwarp();
   if (__syncthreads_or(!mma_done())) goto out;
   {  // R9: dk^T = Ka + cdec * Kb (lanes d_k); Jacobian; dk out
-    float ka[32], kbv[32], s2[32];
-    tmem_ld32(tm + tl + T3 + c0, ka);
-    tmem_ld32(tm + tl + T4 + c0, kbv);
+    if (l2) {
+      float t2 = 0.f;
+#pragma unroll 1
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int cb = c0 + q4 * 8;
+        float ka[8], kbv[8];
+        tmem_ld8(tm + tl + T3 + cb, ka);
+        tmem_ld8(tm + tl + T4 + cb, kbv);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int tkn = c0 + i;
-      ka[i] += sm.gt.cdec[tkn] * kbv[i];
-      kbv[i] = ld_f16(sm.kq, tkn, row, 2 * HT);  // k^ (reused below)
-      s2[i] = ka[i] * kbv[i];
+        for (int i = 0; i < 8; ++i) {
+          const int tkn = cb + i;
+          ka[i] = (ka[i] + sm.gt.cdec[tkn] * kbv[i]) * ld_f16(sm.kq, tkn, row, 2 * HT);
+        }
+        const float a2 = colsum8(ka);
+        if ((lane >> 3) == q4) t2 = a2;
+      }
+      sm.part[wq][c0 + lane] = t2;
     }
-    const float t2 = colsum32(s2);
-    sm.part[wq][c0 + lane] = t2;
     __syncthreads();
     bf16 *stg = reinterpret_cast<bf16 *>(sm.dob);
+#pragma unroll 1
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const int cb = c0 + q4 * 8;
+      float ka[8], kbv[8];
+      tmem_ld8(tm + tl + T3 + cb, ka);
+      tmem_ld8(tm + tl + T4 + cb, kbv);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int tkn = c0 + i;
-      float o = ka[i];
-      if (l2) {
-        const float dot = sm.part[0][tkn] + sm.part[1][tkn] + sm.part[2][tkn] + sm.part[3][tkn];
-        o = (ka[i] - kbv[i] * dot) * sm.nk[tkn];
+      for (int i = 0; i < 8; ++i) {
+        const int tkn = cb + i;
+        float o = ka[i] + sm.gt.cdec[tkn] * kbv[i];
+        if (l2) {
+          const float dot = sm.part[0][tkn] + sm.part[1][tkn] + sm.part[2][tkn] + sm.part[3][tkn];
+          o = (o - ld_f16(sm.kq, tkn, row, 2 * HT) * dot) * sm.nk[tkn];
+        }
+        stg[tkn * D + row] = __float2bfloat16_rn(o);
       }
-      stg[tkn * D + row] = __float2bfloat16_rn(o);
     }
   }
   fence_before();
