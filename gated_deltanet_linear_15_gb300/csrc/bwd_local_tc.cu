@@ -34,6 +34,8 @@ namespace {
 constexpr int D = 128;
 constexpr int HT = 8192;
 constexpr int LN = CH + 4;
+constexpr int LTHREADS = 512;  // 16 warps: four per TMEM lane quarter, 16 columns each per read-out
+constexpr int LWARPS = LTHREADS / 32;
 constexpr uint32_t T0 = 0, T1 = 64, T2 = 128, T3 = 192, T4 = 256, T5 = 320, T6 = 384, T7 = 448;
 
 struct __align__(1024) LocalTcSmem {
@@ -52,9 +54,9 @@ struct __align__(1024) LocalTcSmem {
   float g[CH], beta[CH], nq[CH], nk[CH];  // nq, nk hold reciprocal norms
   Gates gt;
   float ys[1152];
-  float part[16][CH];   // per-token partial sums (4 warps x 4 kinds, reused per round)
+  float part[20][CH];   // per-token partial sums (reused per round)
   float acc[12][CH];    // assembled per-token terms
-  float red[NWARPS];
+  float red[LWARPS];
   uint64_t bar_tma, bar_st, bar_mma;
   uint32_t tmem_base;
 };
@@ -118,7 +120,7 @@ __device__ __forceinline__ uint32_t chunk_off(int r, int cb) { return r * 128 + 
 
 }  // namespace
 
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(LTHREADS, 1)
     bwd_local_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
                         const __grid_constant__ CUtensorMap tms0, const __grid_constant__ CUtensorMap tmds) {
@@ -137,7 +139,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wg = warp >> 2, wq = warp & 3;
   const int row = (wq << 5) | lane;  // TMEM lane of this thread
-  const int c0 = wg * 32;            // this warpgroup's 32 columns of a 64-column region
+  const int c0 = wg * 16;            // this warp's 16 columns of a 64-column region
   int *err = a.status;
 
   if (tid == 0) {
@@ -190,7 +192,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (warp == 0) gate_prefix(sm.g, sm.gt);
   // ---- prep: bf16 -> fp16 in place; q, k normalised (norms kept for the Jacobians); rows >= nvalid zero
 #pragma unroll 1
-  for (int task = tid; task < 4 * 2 * CH; task += NTHREADS) {
+  for (int task = tid; task < 4 * 2 * CH; task += LTHREADS) {
     const int t = task >> 7;  // 0 K, 1 Q, 2 V, 3 dO
     const int r = (task >> 1) & 63, hb = task & 1;
     uint8_t *rowp = (t == 0 ? sm.kq : t == 1 ? sm.kq + HT : t == 2 ? sm.v : sm.dob) +
@@ -247,7 +249,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (__syncthreads_or(!mma_done())) goto out;
   // R1: rows 0-63 -> N (fp32), rows 64-127 -> P (fp16, [r][i])
 #pragma unroll 1
-  for (int q4 = 0; q4 < 4; ++q4) {
+  for (int q4 = 0; q4 < 2; ++q4) {
     const int cb = c0 + q4 * 8;
     float v[8];
     tmem_ld8(tm + tl + T0 + cb, v);
@@ -292,7 +294,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (__syncthreads_or(!mma_done())) goto out;
   // R2: W^T (lanes d_k, columns token) * gam -> wt
 #pragma unroll 1
-  for (int q4 = 0; q4 < 4; ++q4) {
+  for (int q4 = 0; q4 < 2; ++q4) {
     const int cb = c0 + q4 * 8;
     float v[8];
     tmem_ld8(tm + tl + T1 + cb, v);
@@ -309,7 +311,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     float acc = 0.f;
     const uint4 *A4 = reinterpret_cast<const uint4 *>(sm.s0), *B4 = reinterpret_cast<const uint4 *>(sm.ds);
 #pragma unroll 2
-    for (int e = tid; e < 4 * HT / 16; e += NTHREADS) {
+    for (int e = tid; e < 4 * HT / 16; e += LTHREADS) {
       const uint4 x = A4[e], y = B4[e];
       const __half2 *xh = reinterpret_cast<const __half2 *>(&x), *yh = reinterpret_cast<const __half2 *>(&y);
 #pragma unroll
@@ -337,7 +339,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (__syncthreads_or(!mma_done())) goto out;
   // R3: Ut^T -> ut
 #pragma unroll 1
-  for (int q4 = 0; q4 < 4; ++q4) {
+  for (int q4 = 0; q4 < 2; ++q4) {
     const int cb = c0 + q4 * 8;
     float v[8];
     tmem_ld8(tm + tl + T2 + cb, v);
@@ -371,7 +373,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   {  // R4: dUt^T = cdec*Y + Z -> wt (W^T is dead);  per-token sums <Ut, Y>, <dUt, Ut> over d_v
     float t1 = 0.f, t2 = 0.f;
 #pragma unroll 1
-    for (int q4 = 0; q4 < 4; ++q4) {
+    for (int q4 = 0; q4 < 2; ++q4) {
       const int cb = c0 + q4 * 8;
       float y[8], z[8], u[8], s1[8], s2[8];
       tmem_ld8(tm + tl + T3 + cb, y);
@@ -391,8 +393,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         t2 = a2;
       }
     }
-    sm.part[wq][c0 + lane] = t1;
-    sm.part[4 + wq][c0 + lane] = t2;
+    if (lane < 16) sm.part[wq][c0 + lane] = t1;
+    if (lane < 16) sm.part[4 + wq][c0 + lane] = t2;
   }
   fence_before();
   fence_async_smem();
@@ -429,7 +431,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const float gr = sm.gt.gp[r];
       float rs = 0.f, cs = 0.f;
 #pragma unroll 1
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int q4 = 0; q4 < 2; ++q4) {
         const int cb = c0 + q4 * 8;
         float v[8], zc[8], y[8];
         tmem_ld8(tm + tl + T0 + cb, v);
@@ -448,12 +450,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const float a = colsum8(zc);
         if ((lane >> 3) == q4) cs = a;
       }
-      sm.part[8 + wg][r] = rs;           // row sums of Z, per column half
-      sm.part[10 + wq][c0 + lane] = cs;  // column sums of Z, per row quarter (wq 0/1)
+      sm.part[16 + wg][r] = rs;          // row sums of Z, per 16-column block
+      if (lane < 16) sm.part[10 + wq][c0 + lane] = cs;  // column sums of Z, per row quarter (wq 0/1)
     }
     // dW'^T (lanes d_k) * gam -> s0 region (S0 is dead)
 #pragma unroll 1
-    for (int q4 = 0; q4 < 4; ++q4) {
+    for (int q4 = 0; q4 < 2; ++q4) {
       const int cb = c0 + q4 * 8;
       float v[8];
       tmem_ld8(tm + tl + T1 + cb, v);
@@ -466,7 +468,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       bf16 *stg = reinterpret_cast<bf16 *>(sm.dob);
       float t = 0.f;
 #pragma unroll 1
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int q4 = 0; q4 < 2; ++q4) {
         const int cb = c0 + q4 * 8;
         float v[8], sv[8];
         tmem_ld8(tm + tl + T6 + cb, v);
@@ -479,7 +481,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const float a = colsum8(sv);
         if ((lane >> 3) == q4) t = a;
       }
-      sm.part[12 + wq][c0 + lane] = t;
+      if (lane < 16) sm.part[12 + wq][c0 + lane] = t;
     }
   }
   fence_before();
@@ -488,12 +490,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   {
     bf16 *dvg = static_cast<bf16 *>(a.dv);
     const uint4 *stg = reinterpret_cast<const uint4 *>(sm.dob);
-    for (int e = tid; e < CH * (D / 8); e += NTHREADS) {
+    for (int e = tid; e < CH * (D / 8); e += LTHREADS) {
       const int r = e >> 4, cc = e & 15;
       if (r < nvalid) *reinterpret_cast<uint4 *>(dvg + ((size_t)(tok0 + r) * H + h) * D + cc * 8) = stg[e];
     }
     if (tid < 64) {
-      sm.acc[2][tid] = sm.part[8][tid] + sm.part[9][tid];    // row sums of dP * P
+      sm.acc[2][tid] = sm.part[16][tid] + sm.part[17][tid] + sm.part[18][tid] + sm.part[19][tid];  // row sums of dP * P
       sm.acc[3][tid] = sm.part[10][tid] + sm.part[11][tid];  // column sums of dP * P
       sm.acc[4][tid] = sm.part[12][tid] + sm.part[13][tid] + sm.part[14][tid] + sm.part[15][tid];  // <dV, v>
     }
@@ -524,7 +526,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     {
       float t1 = 0.f, t2 = 0.f;
 #pragma unroll 1
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int q4 = 0; q4 < 2; ++q4) {
         const int cb = c0 + q4 * 8;
         float qa[8], qb[8], s1[8], s2[8];
         tmem_ld8(tm + tl + T5 + cb, qa);
@@ -543,8 +545,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           t2 = a2;
         }
       }
-      sm.part[wq][c0 + lane] = t1;
-      sm.part[4 + wq][c0 + lane] = t2;
+      if (lane < 16) sm.part[wq][c0 + lane] = t1;
+      if (lane < 16) sm.part[4 + wq][c0 + lane] = t2;
     }
     // M1, M2 (lanes 0-63 = r): dAhat = beta_i (M1 + Gamma M2); beta column sums colsum_i(Ahat (M1 + Gamma M2))
     if (row < 64) {
@@ -552,7 +554,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const float gr = sm.gt.gp[r];
       float cs = 0.f;
 #pragma unroll 1
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int q4 = 0; q4 < 2; ++q4) {
         const int cb = c0 + q4 * 8;
         float m1[8], m2[8];
         tmem_ld8(tm + tl + T3 + cb, m1);
@@ -570,14 +572,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const float a = colsum8(m2);
         if ((lane >> 3) == q4) cs = a;
       }
-      sm.part[8 + wq][c0 + lane] = cs;
+      if (lane < 16) sm.part[8 + wq][c0 + lane] = cs;
     }
     __syncthreads();
     // dq raw = (scale dq^ - q^ (q^ . dq^) / scale) / |q|   (or scale dq^ without normalisation)
     bf16 *stg = reinterpret_cast<bf16 *>(sm.dob);
     const float rscale = 1.f / a.scale;
 #pragma unroll 1
-    for (int q4 = 0; q4 < 4; ++q4) {
+    for (int q4 = 0; q4 < 2; ++q4) {
       const int cb = c0 + q4 * 8;
       float qa[8], qb[8];
       tmem_ld8(tm + tl + T5 + cb, qa);
@@ -604,7 +606,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   {
     bf16 *dqg = static_cast<bf16 *>(a.dq);
     const uint4 *stg = reinterpret_cast<const uint4 *>(sm.dob);
-    for (int e = tid; e < CH * (D / 8); e += NTHREADS) {
+    for (int e = tid; e < CH * (D / 8); e += LTHREADS) {
       const int r = e >> 4, cc = e & 15;
       if (r < nvalid) *reinterpret_cast<uint4 *>(dqg + ((size_t)(tok0 + r) * H + h) * D + cc * 8) = stg[e];
     }
@@ -629,7 +631,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (__syncthreads_or(!mma_done())) goto out;
   if (row < 64) {  // R7: Y1 -> v (first half; V is dead)
 #pragma unroll 1
-    for (int q4 = 0; q4 < 4; ++q4) {
+    for (int q4 = 0; q4 < 2; ++q4) {
       const int cb = c0 + q4 * 8;
       float v[8];
       tmem_ld8(tm + tl + T0 + cb, v);
@@ -657,7 +659,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint8_t *sg = sm.v + HT;
     float rb = 0.f;
 #pragma unroll 1
-    for (int q4 = 0; q4 < 4; ++q4) {
+    for (int q4 = 0; q4 < 2; ++q4) {
       const int cb = c0 + q4 * 8;
       float v[8], y[8];
       tmem_ld8(tm + tl + T1 + cb, v);
@@ -670,7 +672,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       st_chunk_f16(sg + chunk_off(r, cb), y);
     }
-    sm.part[12 + wg][r] = rb;
+    sm.part[16 + wg][r] = rb;
   }
   fence_before();
   fence_async_smem();
@@ -703,7 +705,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (l2) {
       float t2 = 0.f;
 #pragma unroll 1
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int q4 = 0; q4 < 2; ++q4) {
         const int cb = c0 + q4 * 8;
         float ka[8], kbv[8];
         tmem_ld8(tm + tl + T3 + cb, ka);
@@ -716,12 +718,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const float a2 = colsum8(ka);
         if ((lane >> 3) == q4) t2 = a2;
       }
-      sm.part[wq][c0 + lane] = t2;
+      if (lane < 16) sm.part[wq][c0 + lane] = t2;
     }
     __syncthreads();
     bf16 *stg = reinterpret_cast<bf16 *>(sm.dob);
 #pragma unroll 1
-    for (int q4 = 0; q4 < 4; ++q4) {
+    for (int q4 = 0; q4 < 2; ++q4) {
       const int cb = c0 + q4 * 8;
       float ka[8], kbv[8];
       tmem_ld8(tm + tl + T3 + cb, ka);
@@ -743,7 +745,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   {
     bf16 *dkg = static_cast<bf16 *>(a.dk);
     const uint4 *stg = reinterpret_cast<const uint4 *>(sm.dob);
-    for (int e = tid; e < CH * (D / 8); e += NTHREADS) {
+    for (int e = tid; e < CH * (D / 8); e += LTHREADS) {
       const int r = e >> 4, cc = e & 15;
       if (r < nvalid) *reinterpret_cast<uint4 *>(dkg + ((size_t)(tok0 + r) * H + h) * D + cc * 8) = stg[e];
     }
@@ -761,7 +763,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     sumy = warp_sum(sumy);
     float red = 0.f;
-    for (int i = 0; i < NWARPS; ++i) red += sm.red[i];
+    for (int i = 0; i < LWARPS; ++i) red += sm.red[i];
     if (lane == 31) dGv[1] += sumy + sm.gt.gamC * red;
     float hi = dGv[1], lo = dGv[0];
 #pragma unroll
@@ -778,7 +780,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int r = lane + 32 * t;
       if (r < nvalid) {
         a.dg[(size_t)(tok0 + r) * H + h] = t ? hi : lo;
-        a.dbeta[(size_t)(tok0 + r) * H + h] = sm.acc[6][r] + sm.part[12][r] + sm.part[13][r];
+        a.dbeta[(size_t)(tok0 + r) * H + h] =
+            sm.acc[6][r] + sm.part[16][r] + sm.part[17][r] + sm.part[18][r] + sm.part[19][r];
       }
     }
   }
@@ -797,7 +800,7 @@ int launch_bwd_local_tc(const BwdArgs &a, const CUtensorMap *maps, int CH_max, c
   static_assert(sizeof(LocalTcSmem) + 1024 <= 232448, "shared memory budget");
   cudaError_t e = cudaFuncSetAttribute(bwd_local_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  bwd_local_tc_kernel<<<dim3(CH_max, a.H), NTHREADS, smem, st>>>(a, maps[0], maps[1], maps[2], maps[3], maps[4],
+  bwd_local_tc_kernel<<<dim3(CH_max, a.H), LTHREADS, smem, st>>>(a, maps[0], maps[1], maps[2], maps[3], maps[4],
                                                                    maps[5]);
   return (int)cudaGetLastError();
 }

@@ -178,6 +178,7 @@ __device__ __forceinline__ void wy_inverse(float *nf, int ldn, const float *beta
       mma_tf32(c, ah, bh);
     }
   };
+  if (warp < 8) {  // eight column slices; further warps (if any) only join the barriers
   const int gr = lane >> 2, gc = lane & 3;
   const int J0 = warp >> 1;               // first row block with non-zero entries in this slice
   const int cl = 8 * (warp & 1);          // slice column offset inside block J0
@@ -255,6 +256,7 @@ __device__ __forceinline__ void wy_inverse(float *nf, int ldn, const float *beta
         if (c + 1 < r) nf[(c + 1) * ldn + r] = a1;
       }
     }
+  }
   umma_fence_proxy();  // shared-memory operands written above are read by the tensor-core async proxy
   __syncthreads();
 }
