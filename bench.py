@@ -53,6 +53,27 @@ def algorithmic_bytes(w, x):
     return fwd, bwd, per_kernel
 
 
+# ----------------------------------------------------------------------------- multi-rank host logic
+def replica_seed(seed, rank):
+    """Each rank runs its own replica of the workload, drawn from its own seed."""
+    return seed + 1000 * rank
+
+
+def max_over_ranks(local_ms, world, device=None):
+    """The job's time is the slowest rank's: all-reduce MAX over the process group."""
+    import torch
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(total_ms, world, tokens_per_rank_step, steps):
+    """Whole-job tokens/s: `world` replicas each process `tokens_per_rank_step` per step."""
+    return world * tokens_per_rank_step * steps / (total_ms / 1000.0)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -195,7 +216,7 @@ def main():
     from gdn_inputs import WORKLOADS, make_inputs
 
     w = WORKLOADS[args.workload]
-    x = make_inputs(w, dev, seed=w.seed + 1000 * rank)
+    x = make_inputs(w, dev, seed=replica_seed(w.seed, rank))
     shape = g.make_shape(x["q"], x["v"], cu_seqlens=x["cu_seqlens"], scale=x["scale"], l2norm=x["l2norm"],
                          seg_chunks=args.seg_chunks)
     plan = g.gdn_plan_query(shape)
@@ -253,12 +274,9 @@ def main():
     fwd_ms = [a.elapsed_time(b) for a, b, c in evs]
     bwd_ms = [b.elapsed_time(c) for a, b, c in evs]
     step_ms = sum(fwd_ms) + sum(bwd_ms)
-    t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = max_over_ranks(step_ms, world, dev)
     tokens_per_step = x["q"].shape[0] * x["q"].shape[1]
-    value = world * tokens_per_step * args.steps / (total_ms / 1000.0)
+    value = job_throughput(total_ms, world, tokens_per_step, args.steps)
 
     # ---- roofline of the dominant kernel, from the live per-launch events
     hbm_peak, bf16_peak, peak_kind = load_peaks()

@@ -142,10 +142,17 @@ int gdn_chunk_bwd(const gdn_shape *shape,
                   void *workspace, size_t workspace_bytes, gdn_stream_t stream);
 
 /* Reads the device status word that the kernels of the last call on `stream`
- * set (synchronises the stream).  Bit 0: a chunk's in-chunk log-decay span
- * exceeded the range of the gamma factoring (|G_r - G_mid| > 80), so its
- * results are not reliable.  Returns -1 on a CUDA error.  `workspace` is the
- * one passed to that call. */
+ * set (synchronises the stream).  Every bit means the outputs of that call are
+ * not reliable:
+ *   bit 0 (1): a chunk's in-chunk log-decay span exceeded the range of the
+ *              gamma factoring (|G_r - G_mid| > 80);
+ *   bit 1 (2): cu_seqlens is not non-decreasing, or describes more chunks or
+ *              segments than the workspace was sized for;
+ *   bit 2 (4): a tensor-core completion wait ran past its iteration limit (the
+ *              kernel stopped that work item and returned);
+ *   bit 3 (8): a TMA tile-load wait ran past its iteration limit (likewise).
+ * Returns the word (0 = clean), or -1 on a CUDA error.  `workspace` is the one
+ * passed to that call. */
 int gdn_get_device_status(const gdn_shape *shape, const void *workspace, gdn_stream_t stream);
 
 /* The segment plan for this shape on the current device: chunks per segment,
