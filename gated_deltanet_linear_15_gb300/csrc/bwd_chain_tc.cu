@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncthreads();
     wy_inverse<false, false>(sm.nf, LN, gbeta, sm.ys, [&](int r, int cc, float a0, float a1) {
       *reinterpret_cast<__half2 *>(sm.x1 + sw128_offset(r, cc)) = __floats2half2_rn(a0 * gbeta[cc], a1 * gbeta[cc + 1]);
-    });
+    }, it == 0);
 
     // ---- MMA 2: W^T = K^T X1^T;  meanwhile dS -> fp16 operand copy (+ workspace), gam_C dS back to TMEM
     if (tid == 0) {

@@ -73,10 +73,22 @@ __device__ __forceinline__ void prep_rows(E *t, int ld, float mul, bool l2, floa
 // Each exponential is taken once per token (onedev.kr FlashQLA talk summary,
 // paragraph on SFU load: the diagonal scaling is pulled out of the inverse).
 // Returns true in lane 0 if |G_r - G_mid| exceeds the factoring range.
-struct Gates {
+struct __align__(16) Gates {
   float G[CH], gam[CH], gp[CH], rgp[CH], cdec[CH];
   float gamC;  // exp(G_last)
 };
+
+// 16 consecutive floats from 16-byte aligned shared memory (four vector loads)
+__device__ __forceinline__ void ld16f(const float *p, float (&v)[16]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 t = reinterpret_cast<const float4 *>(p)[q];
+    v[4 * q] = t.x;
+    v[4 * q + 1] = t.y;
+    v[4 * q + 2] = t.z;
+    v[4 * q + 3] = t.w;
+  }
+}
 
 __device__ __forceinline__ bool gate_prefix(const float *g, Gates &gt) {
   const int lane = threadIdx.x & 31;
@@ -145,25 +157,51 @@ __device__ __forceinline__ void mma_3xtf32(float (&c)[4], const float (&a)[4], c
 
 __device__ __forceinline__ void umma_fence_proxy() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
+// Ahat = (I + diag(beta) N)^{-1} for the strictly lower N held in `nf` (row
+// stride ldn; only its strict lower triangle is read, the strict upper
+// triangle serves as scratch).  The four diagonal 16 x 16 blocks are inverted
+// by forward substitution (one column per lane) into `dinv` (>= 64 x 17
+// floats); the off-diagonal part follows in two doubling levels of the block
+// identity  [[A, 0], [C, B]]^{-1} = [[A^-1, 0], [-B^-1 C A^-1, B^-1]]:  16 -> 32
+// (blocks (1,0) and (3,2)) and 32 -> 64 (the lower-left 32 x 32 block), each a
+// pair of m16n8k8 TF32 tensor-core products (3xTF32 when PRECISE).  Every
+// element of Ahat is then handed to out(r, c, Ahat[r][c], Ahat[r][c + 1]) once
+// (c even), the zero upper blocks only when with_zeros; with NF_T the strict
+// lower part is also stored transposed into
+// the strict upper triangle of nf.  Uses warps 0-7 (any further warps only join
+// the barriers); ends with a proxy fence and __syncthreads().
 template <bool PRECISE, bool NF_T, class Out>
-__device__ __forceinline__ void wy_inverse(float *nf, int ldn, const float *beta, float *dinv, Out out) {
+__device__ __forceinline__ void wy_inverse(float *nf, int ldn, const float *beta, float *dinv, Out out,
+                                           bool with_zeros = true) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int DL = 17;  // dinv row stride
-  if (warp < 4 && lane < 16) {
+  if (warp < 4 && lane < 16) {  // column jj of block warp; rows of N read as 16-byte vectors (broadcast)
     const int b = warp * 16, jj = lane;
-    float x[16];
+    float x[16], bt[16];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-      for (int i = 0; i < r; ++i) {
-        if (i & 1) s1 += nf[(b + r) * ldn + b + i] * x[i];
-        else s0 += nf[(b + r) * ldn + b + i] * x[i];
-      }
-      x[r] = ((r == jj) ? 1.f : 0.f) - beta[b + r] * (s0 + s1);
+    for (int q = 0; q < 4; ++q) {
+      const float4 t = *reinterpret_cast<const float4 *>(beta + b + 4 * q);
+      bt[4 * q] = t.x;
+      bt[4 * q + 1] = t.y;
+      bt[4 * q + 2] = t.z;
+      bt[4 * q + 3] = t.w;
     }
 #pragma unroll
-    for (int r = 0; r < 16; ++r) dinv[(warp * 16 + r) * DL + jj] = x[r];
+    for (int r = 0; r < 16; ++r) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int q = 0; q < (r + 3) / 4; ++q) {
+        const float4 n4 = *reinterpret_cast<const float4 *>(nf + (b + r) * ldn + b + 4 * q);
+        const float nv[4] = {n4.x, n4.y, n4.z, n4.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (4 * q + u < r) acc[u] = fmaf(nv[u], x[4 * q + u], acc[u]);
+      }
+      x[r] = ((r == jj) ? 1.f : 0.f) - bt[r] * ((acc[0] + acc[1]) + (acc[2] + acc[3]));
+    }
+    // stored only now, so that no store sits between the row loads above (dinv may alias nf)
+#pragma unroll
+    for (int r = 0; r < 16; ++r) dinv[(b + r) * DL + jj] = x[r];
   }
   __syncthreads();
   auto mma = [&](float(&c)[4], const float(&av)[4], const float(&bv)[2]) {
@@ -178,83 +216,137 @@ __device__ __forceinline__ void wy_inverse(float *nf, int ldn, const float *beta
       mma_tf32(c, ah, bh);
     }
   };
-  if (warp < 8) {  // eight column slices; further warps (if any) only join the barriers
+  // fragment coordinates (m16n8k8): A element i at (gr + 8 (i & 1), gc + 4 (i >> 1)),
+  // B element h at (k = gc + 4 h, n = gr), accumulator e at (gr + 8 (e >> 1), 2 gc + (e & 1))
   const int gr = lane >> 2, gc = lane & 3;
-  const int J0 = warp >> 1;               // first row block with non-zero entries in this slice
-  const int cl = 8 * (warp & 1);          // slice column offset inside block J0
-  // B fragment (k = 8*ks + gc (+4), n = gr) of a 16 x 8 block held in accumulator layout
-  auto bfrag = [&](const float(&c)[4], int ks, float(&bv)[2]) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int krow = gc + 4 * h;               // row inside the 8-row half ks
-      const int src = krow * 4 + (gr >> 1);      // lane holding (row krow (+8 ks), col gr)
-      const float e0 = __shfl_sync(0xffffffffu, c[2 * ks + 0], src);
-      const float e1 = __shfl_sync(0xffffffffu, c[2 * ks + 1], src);
-      bv[h] = (gr & 1) ? e1 : e0;
-    }
-  };
-  float X[4][4];
-#pragma unroll
-  for (int I = 0; I < 4; ++I)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) X[I][e] = 0.f;
-  // X_J0 = columns of D_J0^{-1}
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int r = gr + 8 * (e >> 1), c = cl + 2 * gc + (e & 1);
-#pragma unroll
-    for (int I = 0; I < 4; ++I)
-      if (I == J0) X[I][e] = dinv[(I * 16 + r) * DL + c];
-  }
-#pragma unroll
-  for (int I = 1; I < 4; ++I) {
-    if (I <= J0) continue;
-    const int ra = 16 * I + gr;
-    const float b0 = beta[ra], b1 = beta[ra + 8];
-    float y0[4] = {0.f, 0.f, 0.f, 0.f}, y1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int K = 0; K < 3; ++K) {
-      if (K < J0 || K >= I) continue;
-#pragma unroll
-      for (int ks = 0; ks < 2; ++ks) {
-        const int k0 = 16 * K + 8 * ks;
-        const float av[4] = {b0 * nf[ra * ldn + k0 + gc], b1 * nf[(ra + 8) * ldn + k0 + gc],
-                             b0 * nf[ra * ldn + k0 + gc + 4], b1 * nf[(ra + 8) * ldn + k0 + gc + 4]};
-        float bv[2];
-        bfrag(X[K], ks, bv);
-        if (ks == 0) mma(y0, av, bv);
-        else mma(y1, av, bv);
-      }
-    }
-    float z[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) z[e] = -(y0[e] + y1[e]);
-    float x0[4] = {0.f, 0.f, 0.f, 0.f}, x1[4] = {0.f, 0.f, 0.f, 0.f};
+  // level 1: X_{I,J} = -D_I (T_IJ D_J) for (I, J) = (1, 0), (3, 2); warp w < 4: pair w / 2, columns 8 (w % 2)..
+  // The result stays in registers (x1v) for the hand-out and goes, transposed, to the scratch slot
+  // nf[(16 J + c) * ldn + 16 I + r] for level 2.  (dinv is exactly zero above each block's diagonal.)
+  float x1v[4] = {0.f, 0.f, 0.f, 0.f};
+  if (warp < 4) {
+    const int I = 2 * (warp >> 1) + 1, J = I - 1, nt = warp & 1;
+    float y[4] = {0.f, 0.f, 0.f, 0.f};
+    const float b0 = beta[16 * I + gr], b1 = beta[16 * I + gr + 8];
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
-      const int kc = 8 * ks;
-      const float av[4] = {dinv[(I * 16 + gr) * DL + kc + gc], dinv[(I * 16 + gr + 8) * DL + kc + gc],
-                           dinv[(I * 16 + gr) * DL + kc + gc + 4], dinv[(I * 16 + gr + 8) * DL + kc + gc + 4]};
-      float bv[2];
-      bfrag(z, ks, bv);
-      if (ks == 0) mma(x0, av, bv);
-      else mma(x1, av, bv);
+      const int k0 = 16 * J + 8 * ks;
+      const float av[4] = {b0 * nf[(16 * I + gr) * ldn + k0 + gc], b1 * nf[(16 * I + gr + 8) * ldn + k0 + gc],
+                           b0 * nf[(16 * I + gr) * ldn + k0 + gc + 4], b1 * nf[(16 * I + gr + 8) * ldn + k0 + gc + 4]};
+      const float bv[2] = {dinv[(k0 + gc) * DL + 8 * nt + gr], dinv[(k0 + gc + 4) * DL + 8 * nt + gr]};
+      mma(y, av, bv);
     }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) X[I][e] = x0[e] + x1[e];
+    for (int ks = 0; ks < 2; ++ks) {
+      const int a0 = 16 * I;
+      const float av[4] = {dinv[(a0 + gr) * DL + 8 * ks + gc], dinv[(a0 + gr + 8) * DL + 8 * ks + gc],
+                           dinv[(a0 + gr) * DL + 8 * ks + gc + 4], dinv[(a0 + gr + 8) * DL + 8 * ks + gc + 4]};
+      float bv[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // B element (k = 8 ks + gc + 4 h, n = gr) from the accumulator y
+        const int src = (gc + 4 * h) * 4 + (gr >> 1);
+        const float e0 = __shfl_sync(0xffffffffu, y[2 * ks + 0], src);
+        const float e1 = __shfl_sync(0xffffffffu, y[2 * ks + 1], src);
+        bv[h] = (gr & 1) ? e1 : e0;
+      }
+      mma(x1v, av, bv);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x1v[e] = -x1v[e];
+      const int r = gr + 8 * (e >> 1), c = 8 * nt + 2 * gc + (e & 1);
+      nf[(16 * J + c) * ldn + 16 * I + r] = x1v[e];
+    }
   }
-  // hand out every element of the slice (rows 0..63, columns 8w..8w+7)
+  __syncthreads();
+  // level 2: Y = T_LL E0 (32 x 32, stored transposed in the upper-right quadrant), then X_LL = -E1 Y;
+  // warp (mt, nt) owns the m16n8 tile at rows 16 mt, columns 8 nt.  Block relations are warp-uniform.
+  const int mt = (warp >> 2) & 1, nt = warp & 3;
+  if (warp < 8) {
+    float y[4] = {0.f, 0.f, 0.f, 0.f};
+    const int ra = 32 + 16 * mt;
+    const float b0 = beta[ra + gr], b1 = beta[ra + gr + 8];
 #pragma unroll
-  for (int I = 0; I < 4; ++I)
+    for (int ks = 0; ks < 4; ++ks) {
+      if (ks < nt) continue;  // E0[k][j] = 0 for k < j
+      const int k0 = 8 * ks;
+      const float av[4] = {b0 * nf[(ra + gr) * ldn + k0 + gc], b1 * nf[(ra + gr + 8) * ldn + k0 + gc],
+                           b0 * nf[(ra + gr) * ldn + k0 + gc + 4], b1 * nf[(ra + gr + 8) * ldn + k0 + gc + 4]};
+      float bv[2];
+      if ((ks >> 1) == (nt >> 1)) {  // E0 diagonal block
+        bv[0] = dinv[(k0 + gc) * DL + ((8 * nt + gr) & 15)];
+        bv[1] = dinv[(k0 + gc + 4) * DL + ((8 * nt + gr) & 15)];
+      } else {  // E0 block (1, 0): level-1 scratch
+        bv[0] = nf[(8 * nt + gr) * ldn + k0 + gc];
+        bv[1] = nf[(8 * nt + gr) * ldn + k0 + gc + 4];
+      }
+      mma(y, av, bv);
+    }
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int r = 16 * I + gr + 8 * h, c = 8 * warp + 2 * gc;
-      const float a0 = X[I][2 * h], a1 = X[I][2 * h + 1];
+    for (int e = 0; e < 4; ++e) {  // Y[i][j] -> nf[j * ldn + 32 + i]
+      const int i = 16 * mt + gr + 8 * (e >> 1), j = 8 * nt + 2 * gc + (e & 1);
+      nf[j * ldn + 32 + i] = y[e];
+    }
+  }
+  __syncthreads();
+  float xl[4] = {0.f, 0.f, 0.f, 0.f};
+  if (warp < 8) {
+    const int a0 = 32 + 16 * mt;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      if (ks > 2 * mt + 1) continue;  // E1[i][k] = 0 for k > i
+      const int k0 = 32 + 8 * ks;
+      float av[4];
+      if ((ks >> 1) == mt) {  // E1 diagonal block
+        av[0] = dinv[(a0 + gr) * DL + ((k0 + gc) & 15)];
+        av[1] = dinv[(a0 + gr + 8) * DL + ((k0 + gc) & 15)];
+        av[2] = dinv[(a0 + gr) * DL + ((k0 + gc + 4) & 15)];
+        av[3] = dinv[(a0 + gr + 8) * DL + ((k0 + gc + 4) & 15)];
+      } else {  // E1 block (3, 2): level-1 scratch
+        av[0] = nf[(k0 + gc) * ldn + a0 + gr];
+        av[1] = nf[(k0 + gc) * ldn + a0 + gr + 8];
+        av[2] = nf[(k0 + gc + 4) * ldn + a0 + gr];
+        av[3] = nf[(k0 + gc + 4) * ldn + a0 + gr + 8];
+      }
+      const float bv[2] = {nf[(8 * nt + gr) * ldn + k0 + gc], nf[(8 * nt + gr) * ldn + k0 + gc + 4]};
+      mma(xl, av, bv);
+    }
+  }
+  __syncthreads();  // Y is read; its slots may now take the transposed lower-left block
+  if (warp < 8) {
+    auto give = [&](int r, int c, float a0, float a1) {
       out(r, c, a0, a1);
       if (NF_T) {
         if (c < r) nf[c * ldn + r] = a0;
         if (c + 1 < r) nf[(c + 1) * ldn + r] = a1;
       }
+    };
+    // lower-left 32 x 32 (registers of every warp)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) give(32 + 16 * mt + gr + 8 * h, 8 * nt + 2 * gc, -xl[2 * h], -xl[2 * h + 1]);
+    // blocks (1, 0) and (3, 2) (registers of warps 0-3)
+    if (warp < 4) {
+      const int I = 2 * (warp >> 1) + 1, nt1 = warp & 1;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) give(16 * I + gr + 8 * h, 16 * (I - 1) + 8 * nt1 + 2 * gc, x1v[2 * h], x1v[2 * h + 1]);
+    }
+    // diagonal blocks from dinv: thread t -> block t / 64, rows (t % 64) / 4 and columns 2 (t % 4) + {0, 8}
+    {
+      const int t = threadIdx.x, blk = t >> 6, r = (t & 63) >> 2, cc = 2 * (t & 3);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = cc + 8 * h;
+        give(16 * blk + r, 16 * blk + c, dinv[(16 * blk + r) * DL + c], dinv[(16 * blk + r) * DL + c + 1]);
+      }
+    }
+    // zeros: the six 16 x 16 blocks above the diagonal (768 pairs, three per thread); a caller whose
+    // output tiles keep them from an earlier call passes with_zeros = false
+#pragma unroll
+    for (int i = 0; i < 3 && with_zeros; ++i) {
+      const int pidx = threadIdx.x + 256 * i;  // pair index
+      const int b = pidx >> 7, w = pidx & 127;   // block 0..5, pair within block
+      const int bi = b < 3 ? 0 : (b < 5 ? 1 : 2);
+      const int bj = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
+      out(16 * bi + (w >> 3), 16 * bj + 2 * (w & 7), 0.f, 0.f);
     }
   }
   umma_fence_proxy();  // shared-memory operands written above are read by the tensor-core async proxy

@@ -6,10 +6,11 @@
 // TMEM lanes (transposed where that is what puts d = 128 on M):
 //   [K; Q] K^T     -> N = strict_tril(K K^T) (rows 0-63), Q K^T (rows 64-127)
 //   W^T = K^T X1^T, U^T = V^T X2^T      X1 = Ahat diag(beta), X2 = diag(gp) Ahat diag(beta rgp)
-//   Ut^T = U^T - S0 W^T (negated-A MMA accumulating on U^T),   O^T = S0 Qg^T
-//   S   = gam_C S0 + Ut^T Kc                Kc = diag(cdec) K (MN-major operand)
-//   O^T += Ut^T P^T                         P = diag(gp) tril_incl(Q K^T) diag(rgp)
-// with Qg = diag(gam) Q, W^T's columns scaled by gam at read-out, and
+//   Ut^T = U^T - S0 W^T (negated-A MMA accumulating on U^T),   Oi^T = S0 Q^T
+//   S   = gam_C S0 + (Ut^T diag(cdec)) K    (K as the MN-major operand)
+//   Oa^T = Ut^T P^T                         P = diag(gp) tril_incl(Q K^T) diag(rgp)
+//   O^T = Oi^T diag(gam) + Oa^T             (combined at read-out)
+// with W^T's columns scaled by gam and a cdec-scaled copy of Ut^T made at read-out, and
 // Ahat = (I + diag(beta) N)^{-1} computed on CUDA cores in fp32 (onedev.kr
 // FlashQLA talk summary, paragraph on the WY representation for the four
 // steps; paragraph on SFU load for pulling the diagonal gamma scaling out of
@@ -17,9 +18,11 @@
 // umma.cuh); the state is kept in fp32 in TMEM and copied to fp16 once per
 // chunk as the operand of the next products.
 //
-// One CTA of 256 threads per (segment, head); thread 0 issues TMA and MMA,
-// both warpgroups read TMEM (each covers lanes 0-127) and do the CUDA-core
-// work.  Inputs of chunk c+1 are loaded by TMA while chunk c is computed.
+// One CTA of 512 threads per (segment, head); thread 0 issues TMA and MMA,
+// all 16 warps read TMEM (warp w reaches lanes 32 (w % 4)..; the four warps of
+// a lane quarter split the columns) and do the CUDA-core work.  Inputs of chunk c+1 are loaded by TMA while chunk c is computed, and
+// normalised in place (they need no gates) while chunk c's last two MMA groups
+// run.
 #include "chunk_common.cuh"
 #include "kernels.h"
 #include "umma.cuh"
@@ -32,17 +35,17 @@ namespace {
 
 constexpr int D = 128;
 constexpr int HT = 8192;  // one 64 x 64 fp16 half-tile, 128B-swizzled
+constexpr int FT = 512;   // threads per CTA
 
 // TMEM columns
-constexpr uint32_t TM_S = 0, TM_KQ = 128, TM_W = 192, TM_U = 256, TM_O = 320, TM_COLS = 512;
+constexpr uint32_t TM_S = 0, TM_KQ = 128, TM_W = 192, TM_U = 256, TM_O = 320, TM_OA = 384, TM_COLS = 512;
 
 struct __align__(1024) TcSmem {
   // input ring, 2 stages: [K0 | Q0 | K1 | Q1 | V0 | V1] half-tiles (0/1 = feature block)
   uint8_t ring[2][6 * HT];
-  uint8_t kc[2 * HT];   // diag(cdec) K        (MN-major B operand: rows = token)
-  uint8_t qg[2 * HT];   // diag(gam) Q          (K-major B operand: rows = token)
+  uint8_t uc[2 * HT];   // Ut^T diag(cdec) (K-major A, rows = d_v)
   uint8_t x1[HT], x2[HT], p[HT];
-  uint8_t wu[2 * HT];   // W^T (MN-major B, rows = d_k), later Ut^T (K-major A, rows = d_v)
+  uint8_t wu[2 * HT];   // W^T (MN-major B, rows = d_k), later Ut^T (K-major A, rows = d_v), then O staging
   uint8_t s0[4 * HT];   // S0 fp16 (K-major A: rows = d_v, two k-blocks of 128 rows)
   float nf[CH * (CH + 4)];
   float g[2][CH], beta[2][CH];  // per ring stage
@@ -67,7 +70,10 @@ __device__ __forceinline__ void st_chunk_f16(uint8_t *dst, const float *v) {
 
 }  // namespace
 
-__global__ void __launch_bounds__(NTHREADS, 1)
+// byte offset of the 16-byte chunk holding columns [cb, cb + 8) of row r in a swizzled [rows][64] tile
+__device__ __forceinline__ uint32_t chunk_off(int r, int cb) { return r * 128 + ((((cb & 63) >> 3) ^ (r & 7)) << 4); }
+
+__global__ void __launch_bounds__(FT, 1)
     fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ unsigned char smraw[];
@@ -102,7 +108,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const bool need_v = !transition;
   const bool l2 = (a.flags & kFlagL2Norm) != 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int wg = warp >> 2;                      // warpgroup 0 / 1
+  const int wg = warp >> 2;                      // column group 0..3 within a lane quarter
   const int row = ((warp & 3) << 5) | lane;      // TMEM lane this thread reads
   const size_t DD = (size_t)D * D;
   const size_t sh_idx = (size_t)s * H + h;
@@ -164,9 +170,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (mode == START_INIT) src = a.S0 ? a.S0 + ((size_t)n * H + h) * DD : nullptr;
       else if (mode == START_FIXUP && a.pass != 0) src = a.Sstart + sh_idx * DD;
     }
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int c0 = wg * 64 + half * 32;
+    {
+      const int c0 = wg * 32;
       float v[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
@@ -190,6 +195,69 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     return ok;
   };
 
+  // In-place operand preparation of one ring stage: bf16 -> fp16, L2 norm of the q/k rows (q also
+  // scaled), rows >= nvalid zeroed.  prep_kq: thread t takes quarter-row t % 256 of K (t < 256) or
+  // of Q: 32 features = four 16-byte chunks of one 128-byte swizzled row; the four quarters of a row
+  // sit in adjacent lanes (two shuffles for the squared norm).  prep_v: eighth-row t of V.
+  auto prep_kq = [&](uint8_t *st, int nvalid, bool with_q) {
+    const bool isq = tid >= 256;
+    if (isq && !with_q) return;
+    const int r = (tid >> 2) & 63, qq = tid & 3;
+    uint8_t *rowp = st + (isq ? HT : 0) + (qq >> 1) * 2 * HT + r * 128;
+    const int ch0 = (qq & 1) * 4;
+    uint32_t raw[16];
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      const uint4 q4 = *reinterpret_cast<const uint4 *>(rowp + (((ch0 + cc) ^ (r & 7)) * 16));
+      raw[4 * cc] = q4.x;
+      raw[4 * cc + 1] = q4.y;
+      raw[4 * cc + 2] = q4.z;
+      raw[4 * cc + 3] = q4.w;
+    }
+    float mul = isq ? a.scale : 1.f;
+    if (l2) {
+      float ss = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float lo = __uint_as_float(raw[i] << 16), hi = __uint_as_float(raw[i] & 0xffff0000u);
+        ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+      }
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+      mul *= rsqrtf(ss + 1e-6f);
+    }
+    if (r >= nvalid) mul = 0.f;
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      uint32_t y[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t w = raw[4 * cc + i];
+        const __half2 a2 = __floats2half2_rn(__uint_as_float(w << 16) * mul, __uint_as_float(w & 0xffff0000u) * mul);
+        y[i] = *reinterpret_cast<const uint32_t *>(&a2);
+      }
+      *reinterpret_cast<uint4 *>(rowp + (((ch0 + cc) ^ (r & 7)) * 16)) = make_uint4(y[0], y[1], y[2], y[3]);
+    }
+  };
+  auto prep_v = [&](uint8_t *st, int nvalid) {
+    const int r = tid >> 3, part = tid & 7;
+    uint8_t *rowp = st + 4 * HT + (part >> 2) * HT + r * 128;
+    const float mul = r < nvalid ? 1.f : 0.f;
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      const int chk = (part & 3) * 2 + cc;
+      uint4 q4 = *reinterpret_cast<const uint4 *>(rowp + ((chk ^ (r & 7)) * 16));
+      uint32_t *w = reinterpret_cast<uint32_t *>(&q4);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __half2 a2 =
+            __floats2half2_rn(__uint_as_float(w[i] << 16) * mul, __uint_as_float(w[i] & 0xffff0000u) * mul);
+        w[i] = *reinterpret_cast<const uint32_t *>(&a2);
+      }
+      *reinterpret_cast<uint4 *>(rowp + ((chk ^ (r & 7)) * 16)) = q4;
+    }
+  };
+
   for (int c = cfirst; c < cend && !failed; ++c) {
     const int it = c - cfirst;
     const int stage = it & 1;
@@ -210,85 +278,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // prefetch the next chunk into the other stage (its previous contents were consumed)
     if (tid == 0 && c + 1 < cend) issue_tma(c + 1, stage ^ 1);
     if (c + 1 < cend) issue_gb(c + 1, stage ^ 1, false);
-    const bool tma_ok = mbar_wait(u32(&sm.bar_tma[stage]), (it >> 1) & 1, err, 8);
+    // chunk cfirst: wait for its tiles and normalise them here; later chunks were normalised one
+    // iteration ahead, while MMA 3 and MMA 4 of the previous chunk ran
+    const bool tma_ok = it > 0 || mbar_wait(u32(&sm.bar_tma[stage]), 0, err, 8);
     if (__syncthreads_or(!tma_ok)) {
       failed = true;
       break;
     }
     Gates &G = sm.gt[stage];
-    if (it == 0 && warp == 0) {  // later chunks' gates were computed one chunk ahead
-      if (gate_prefix(sm.g[stage], G) && lane == 0 && err) atomicOr(err, 1);
+    if (it == 0) {
+      if (warp == 0 && gate_prefix(sm.g[stage], G) && lane == 0 && err) atomicOr(err, 1);
+      prep_kq(st, nvalid, emit);
+      if (need_v) prep_v(st, nvalid);
+      fence_async_smem();
     }
-    __syncthreads();
-
-    // ---- prep: bf16 -> fp16 in place, L2 norm of q/k rows, Kc = cdec*K, Qg = gam*Q; rows >= nvalid zeroed.
-    // Thread t: half-row t of K (t < 128) or of Q (t >= 128): 64 features = one 128-byte swizzled row, the
-    // two halves of a row in adjacent lanes (one shuffle for the squared norm); plus quarter-row t of V.
-    {
-      const bool isq = tid >= 128;
-      if (!isq || emit) {
-        const int r = (tid >> 1) & 63, hb = tid & 1;
-        uint8_t *rowp = st + (isq ? HT : 0) + hb * 2 * HT + r * 128;
-        uint32_t raw[32];
-#pragma unroll
-        for (int chk = 0; chk < 8; ++chk) {
-          const uint4 q4 = *reinterpret_cast<const uint4 *>(rowp + ((chk ^ (r & 7)) * 16));
-          raw[4 * chk] = q4.x;
-          raw[4 * chk + 1] = q4.y;
-          raw[4 * chk + 2] = q4.z;
-          raw[4 * chk + 3] = q4.w;
-        }
-        float mul = isq ? a.scale : 1.f;
-        if (l2) {
-          float ss = 0.f;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float lo = __uint_as_float(raw[i] << 16), hi = __uint_as_float(raw[i] & 0xffff0000u);
-            ss = fmaf(lo, lo, fmaf(hi, hi, ss));
-          }
-          ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-          mul *= rsqrtf(ss + 1e-6f);
-        }
-        if (r >= nvalid) mul = 0.f;
-        const float m2 = mul * (isq ? G.gam[r] : G.cdec[r]);
-        uint8_t *row2 = (isq ? sm.qg : sm.kc) + hb * HT + r * 128;
-#pragma unroll
-        for (int chk = 0; chk < 8; ++chk) {
-          uint32_t y[4], z[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t w = raw[4 * chk + i];
-            const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
-            const __half2 a2 = __floats2half2_rn(lo * mul, hi * mul);
-            const __half2 b2 = __floats2half2_rn(lo * m2, hi * m2);
-            y[i] = *reinterpret_cast<const uint32_t *>(&a2);
-            z[i] = *reinterpret_cast<const uint32_t *>(&b2);
-          }
-          const int off = (chk ^ (r & 7)) * 16;
-          *reinterpret_cast<uint4 *>(rowp + off) = make_uint4(y[0], y[1], y[2], y[3]);
-          *reinterpret_cast<uint4 *>(row2 + off) = make_uint4(z[0], z[1], z[2], z[3]);
-        }
-      }
-      if (need_v) {  // quarter-row: 4 chunks of V
-        const int r = tid >> 2, qr = tid & 3;
-        uint8_t *rowp = st + 4 * HT + (qr >> 1) * HT + r * 128;
-        const float mul = r < nvalid ? 1.f : 0.f;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const int chk = (qr & 1) * 4 + cc;
-          uint4 q4 = *reinterpret_cast<const uint4 *>(rowp + ((chk ^ (r & 7)) * 16));
-          uint32_t *w = reinterpret_cast<uint32_t *>(&q4);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const __half2 a2 = __floats2half2_rn(__uint_as_float(w[i] << 16) * mul,
-                                                 __uint_as_float(w[i] & 0xffff0000u) * mul);
-            w[i] = *reinterpret_cast<const uint32_t *>(&a2);
-          }
-          *reinterpret_cast<uint4 *>(rowp + ((chk ^ (r & 7)) * 16)) = q4;
-        }
-      }
-    }
-    fence_async_smem();
     __syncthreads();
 
     // ---- MMA 1: [K; Q] K^T  (M = 128, N = 64, K = 128)
@@ -309,28 +312,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       break;
     }
 
-    // ---- read-out: N (fp32, rows 0-63) and P (fp16, rows 64-127); each warpgroup takes 32 columns
+    // ---- read-out: N (fp32, rows 0-63) and P (fp16, rows 64-127); each warp takes 16 columns
     if (row < 64 || emit) {
-      float v[32];
-      const int c0 = wg * 32;
-      tmem_ld32(tm + tm_lane + TM_KQ + c0, v);
+      const int c0 = wg * 16;
+      float v[16];
+      tmem_ld16(tm + tm_lane + TM_KQ + c0, v);
       if (row < 64) {
+        float4 *dst = reinterpret_cast<float4 *>(&sm.nf[row * LN + c0]);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) sm.nf[row * LN + c0 + i] = v[i];
+        for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
       } else {
         const int r = row - 64;
         const float gr = G.gp[r];
+        float rg[16];
+        ld16f(G.rgp + c0, rg);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          float y[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int col = c0 + q4 * 8 + i;
-            y[i] = col <= r ? v[q4 * 8 + i] * gr * G.rgp[col] : 0.f;
-          }
-          const int chk = (c0 >> 3) + q4;
-          st_chunk_f16(sm.p + r * 128 + ((chk ^ (r & 7)) * 16), y);
-        }
+        for (int i = 0; i < 16; ++i) v[i] = c0 + i <= r ? v[i] * gr * rg[i] : 0.f;
+        st_chunk_f16(sm.p + chunk_off(r, c0), v);
+        st_chunk_f16(sm.p + chunk_off(r, c0 + 8), v + 8);
       }
     }
     fence_before();
@@ -338,13 +337,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     // ---- Ahat (fp32 diagonal blocks, TF32 tensor-core merges) -> X1, X2 (fp16, K-major: rows = r)
     wy_inverse<false, false>(sm.nf, LN, gbeta, sm.ys, [&](int r, int c, float a0, float a1) {
-      const float b0 = gbeta[c], b1 = gbeta[c + 1], gr = G.gp[r];
+      const float2 bb = *reinterpret_cast<const float2 *>(gbeta + c), rg = *reinterpret_cast<const float2 *>(G.rgp + c);
+      const float gr = G.gp[r], x0 = a0 * bb.x, x1 = a1 * bb.y;
       const uint32_t off = sw128_offset(r, c);
-      *reinterpret_cast<__half2 *>(sm.x1 + off) = __floats2half2_rn(a0 * b0, a1 * b1);
+      *reinterpret_cast<__half2 *>(sm.x1 + off) = __floats2half2_rn(x0, x1);
       *reinterpret_cast<__half2 *>(sm.x2 + off) =
-          __floats2half2_rn(c <= r ? a0 * b0 * (gr * G.rgp[c]) : 0.f,
-                            c + 1 <= r ? a1 * b1 * (gr * G.rgp[c + 1]) : 0.f);
-    });
+          __floats2half2_rn(c <= r ? x0 * (gr * rg.x) : 0.f, c + 1 <= r ? x1 * (gr * rg.y) : 0.f);
+    }, it == 0);
 
     // ---- MMA 2: W^T = K^T X1^T, U^T = V^T X2^T  (M = 128, N = 64, K = 64)
     if (tid == 0) {
@@ -369,16 +368,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       f16 *stg = states && c >= cbeg
                      ? static_cast<f16 *>(a.states) + ((size_t)(chunk0 + c) * H + h) * DD + (size_t)row * D
                      : nullptr;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int c0 = wg * 64 + half * 32;
+      {
+        const int c0 = wg * 32;
         float v[32];
         tmem_ld32(tm + tm_lane + TM_S + c0, v);
         const int kb = c0 >> 6;
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          const int chk = ((c0 & 63) >> 3) + q4;
-          uint8_t *dst = sm.s0 + kb * 2 * HT + row * 128 + ((chk ^ (row & 7)) * 16);
+          uint8_t *dst = sm.s0 + kb * 2 * HT + chunk_off(row, c0 + q4 * 8);
           st_chunk_f16(dst, v + q4 * 8);
           if (stg) *reinterpret_cast<uint4 *>(stg + c0 + q4 * 8) = *reinterpret_cast<const uint4 *>(dst);
         }
@@ -394,26 +391,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     // ---- W^T read-out: columns scaled by gam -> fp16 MN-major B (rows = d_k)
     {
-      const int c0 = wg * 32;
-      float v[32];
-      tmem_ld32(tm + tm_lane + TM_W + c0, v);
+      const int c0 = wg * 16;
+      float v[16];
+      tmem_ld16(tm + tm_lane + TM_W + c0, v);
+      float gm[16];
+      ld16f(G.gam + c0, gm);
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        float y[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) y[i] = v[q4 * 8 + i] * G.gam[c0 + q4 * 8 + i];
-        const int chk = (c0 >> 3) + q4;
-        st_chunk_f16(sm.wu + row * 128 + ((chk ^ (row & 7)) * 16), y);
-      }
+      for (int i = 0; i < 16; ++i) v[i] *= gm[i];
+      st_chunk_f16(sm.wu + chunk_off(row, c0), v);
+      st_chunk_f16(sm.wu + chunk_off(row, c0 + 8), v + 8);
     }
     fence_before();
     fence_async_smem();
     __syncthreads();
 
-    // ---- MMA 3: Ut^T = U^T - S0 W^T;  O^T = S0 Qg^T   (M = 128, N = 64, K = 128)
+    // ---- MMA 3: Ut^T = U^T - S0 W^T;  Oi^T = S0 Q^T   (M = 128, N = 64, K = 128)
     if (tid == 0) {
       fence_after();
-      const uint32_t s0b = u32(sm.s0), wb = u32(sm.wu), qb = u32(sm.qg);
+      const uint32_t s0b = u32(sm.s0), wb = u32(sm.wu), qb = u32(st + HT);
       const uint32_t id_u = idesc_f16(128, 64, false, true, /*neg_a=*/true);
       const uint32_t id_o = idesc_f16(128, 64, false, false);
 #pragma unroll
@@ -426,50 +421,65 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
-          const uint32_t boff = (kk >> 2) * HT + (kk & 3) * 32;
-          mma_f16(tm + TM_O, sdesc(s0b + aoff, 16, 1024), sdesc(qb + boff, 16, 1024), id_o, kk > 0);
+          mma_f16(tm + TM_O, sdesc(s0b + aoff, 16, 1024), sdesc(qb + aoff, 16, 1024), id_o, kk > 0);
         }
       }
       mma_commit(u32(&sm.bar_mma));
     }
     __syncwarp();
-    if (__syncthreads_or(!mma_wait())) {
-      failed = true;
-      break;
+    const bool more = c + 1 < cend;
+    const int nvn = more ? min(CH, len - (c + 1) * CH) : 0;
+    uint8_t *stn = sm.ring[stage ^ 1];
+    bool next_ok = true;
+    if (more) {  // the next chunk's tiles (issued at the top of this iteration), normalised while MMA 3 runs
+      next_ok = mbar_wait(u32(&sm.bar_tma[stage ^ 1]), ((it + 1) >> 1) & 1, err, 8);
+      if (next_ok) prep_kq(stn, nvn, outputs && c + 1 >= cbeg);
+    }
+    {
+      const bool mok = mma_wait();
+      if (__syncthreads_or(!mok || !next_ok)) {
+        failed = true;
+        break;
+      }
     }
 
-    // ---- Ut^T read-out -> fp16 K-major A (rows = d_v, k = token)
+    // ---- Ut^T read-out -> fp16 K-major A (rows = d_v, k = token), and Ut^T diag(cdec)
     {
-      const int c0 = wg * 32;
-      float v[32];
-      tmem_ld32(tm + tm_lane + TM_U + c0, v);
+      const int c0 = wg * 16;
+      float v[16];
+      tmem_ld16(tm + tm_lane + TM_U + c0, v);
+      st_chunk_f16(sm.wu + chunk_off(row, c0), v);
+      st_chunk_f16(sm.wu + chunk_off(row, c0 + 8), v + 8);
+      float cd[16];
+      ld16f(G.cdec + c0, cd);
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int chk = (c0 >> 3) + q4;
-        st_chunk_f16(sm.wu + row * 128 + ((chk ^ (row & 7)) * 16), v + q4 * 8);
-      }
+      for (int i = 0; i < 16; ++i) v[i] *= cd[i];
+      st_chunk_f16(sm.uc + chunk_off(row, c0), v);
+      st_chunk_f16(sm.uc + chunk_off(row, c0 + 8), v + 8);
     }
     fence_before();
     fence_async_smem();
     __syncthreads();
 
-    // ---- MMA 4: S += Ut^T Kc (N = 128, K = 64);  O^T += Ut^T P^T (N = 64, K = 64)
+    // ---- MMA 4: S += (Ut^T diag(cdec)) K (N = 128, K = 64);  Oa^T = Ut^T P^T (N = 64, K = 64)
     if (tid == 0) {
       fence_after();
-      const uint32_t ub = u32(sm.wu), kcb = u32(sm.kc), pb = u32(sm.p);
+      const uint32_t ucb = u32(sm.uc), ub = u32(sm.wu), kb = u32(st), pb = u32(sm.p);
       const uint32_t id_s = idesc_f16(128, 128, false, true);
       const uint32_t id_o = idesc_f16(128, 64, false, false);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
-        mma_f16(tm + TM_S, sdesc(ub + kk * 32, 16, 1024), sdesc(kcb + kk * 2048, HT, 1024), id_s, true);
+        mma_f16(tm + TM_S, sdesc(ucb + kk * 32, 16, 1024), sdesc(kb + kk * 2048, 2 * HT, 1024), id_s, true);
       if (emit) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_f16(tm + TM_O, sdesc(ub + kk * 32, 16, 1024), sdesc(pb + kk * 32, 16, 1024), id_o, true);
+          mma_f16(tm + TM_OA, sdesc(ub + kk * 32, 16, 1024), sdesc(pb + kk * 32, 16, 1024), id_o, kk > 0);
       }
       mma_commit(u32(&sm.bar_mma));
     }
     __syncwarp();
+    if (more && need_v) prep_v(stn, nvn);  // the next chunk's V, while MMA 4 runs
+    fence_async_smem();
     if (warp == 0 && c + 1 < cend) {  // gates of the next chunk, overlapping MMA 4
       float *gn = sm.g[stage ^ 1];
       gn[lane] = gnext0;
@@ -482,21 +492,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       break;
     }
 
-    // ---- O^T read-out -> bf16 [token][d_v] staging in qg (free now) -> coalesced rows of o
+    // ---- O^T = Oi^T diag(gam) + Oa^T -> bf16 [token][d_v] staging in wu (free now) -> coalesced rows of o
     if (emit) {
-      const int c0 = wg * 32;
-      float v[32];
-      tmem_ld32(tm + tm_lane + TM_O + c0, v);
-      bf16 *stg = reinterpret_cast<bf16 *>(sm.qg);
+      bf16 *stg = reinterpret_cast<bf16 *>(sm.wu);
+      const int c0 = wg * 16;
+      float v[16], va[16];
+      tmem_ld16x2(tm + tm_lane + TM_O + c0, v, tm + tm_lane + TM_OA + c0, va);
+      float gm[16];
+      ld16f(G.gam + c0, gm);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) stg[(c0 + i) * D + row] = __float2bfloat16_rn(v[i]);
+      for (int i = 0; i < 16; ++i) stg[(c0 + i) * D + row] = __float2bfloat16_rn(fmaf(v[i], gm[i], va[i]));
     }
     fence_before();
     __syncthreads();
     if (emit) {
-      const uint4 *stg = reinterpret_cast<const uint4 *>(sm.qg);
+      const uint4 *stg = reinterpret_cast<const uint4 *>(sm.wu);
       bf16 *og = static_cast<bf16 *>(a.o);
-      for (int e = tid; e < CH * (D / 8); e += NTHREADS) {
+      for (int e = tid; e < CH * (D / 8); e += FT) {
         const int r = e >> 4, cc = e & 15;
         if (r < nvalid) *reinterpret_cast<uint4 *>(og + ((size_t)(tok0 + r) * H + h) * D + cc * 8) = stg[e];
       }
@@ -509,9 +521,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (a.pass == 0) dst = (transition ? a.Mbuf : a.Ebuf) + sh_idx * DD;
     else if (j == nseg - 1 && a.ST) dst = a.ST + ((size_t)n * H + h) * DD;
     if (dst) {
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int c0 = wg * 64 + half * 32;
+      {
+        const int c0 = wg * 32;
         float v[32];
         tmem_ld32(tm + tm_lane + TM_S + c0, v);
 #pragma unroll
@@ -535,7 +546,7 @@ int launch_fwd_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk
   static_assert(sizeof(TcSmem) + 1024 <= 232448, "shared memory budget");
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  fwd_tc_kernel<<<grid, NTHREADS, smem, st>>>(a, tq, tk, tv);
+  fwd_tc_kernel<<<grid, FT, smem, st>>>(a, tq, tk, tv);
   return (int)cudaGetLastError();
 }
 
