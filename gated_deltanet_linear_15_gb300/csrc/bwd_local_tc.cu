@@ -1,6 +1,8 @@
 // Blackwell-native local-gradient kernel of the chunked backward (bf16 inputs,
-// d = 128): one CTA per (chunk, head), given the forward state S0 at the chunk
-// start and dS at its end (fp16, from the two serial passes).  Every product
+// d = 128): persistent CTAs (one per SM, 16 warps) walk the (chunk, head) work
+// items, each given the forward state S0 at the chunk start and dS at its end
+// (fp16, from the two serial passes); the next item's tiles stream in by TMA
+// while the current one finishes.  Every product
 // is a tcgen05 MMA with fp32 accumulation in TMEM; the 64 x 64 products use
 // M = 128 with the upper 64 rows unused.  The algebra is the hand-derived
 // chunk backward (see bwd.cu); the WY part forms dA and dA^T as one symmetric
@@ -57,7 +59,7 @@ struct __align__(1024) LocalTcSmem {
   float part[20][CH];   // per-token partial sums (reused per round)
   float acc[12][CH];    // assembled per-token terms
   float red[LWARPS];
-  uint64_t bar_tma, bar_st, bar_mma;
+  uint64_t bar_a, bar_b, bar_mma;  // TMA: {K, Q, V, S0, dS}, {dO}; tensor-core completion
   uint32_t tmem_base;
 };
 
@@ -75,26 +77,7 @@ __device__ __forceinline__ float ld_f16(const uint8_t *t, int row, int col, int 
   const uint8_t *p = t + (col >> 6) * blk + sw128_offset(row, col & 63);
   return __half2float(*reinterpret_cast<const __half *>(p));
 }
-__device__ __forceinline__ void st_f16(uint8_t *t, int row, int col, int blk, float x) {
-  *reinterpret_cast<__half *>(t + (col >> 6) * blk + sw128_offset(row, col & 63)) = __float2half_rn(x);
-}
 
-// v[32] per lane (one lane per feature) -> lane l holds the sum over the warp's
-// lanes of v[l] (transpose-reduce, 31 shuffles)
-__device__ __forceinline__ float colsum32(float (&v)[32]) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int s = 16; s >= 1; s >>= 1) {
-#pragma unroll
-    for (int i = 0; i < s; ++i) {
-      const bool up = (lane & s) != 0;
-      const float send = up ? v[i] : v[i + s];
-      const float recv = __shfl_xor_sync(0xffffffffu, send, s);
-      v[i] = (up ? v[i + s] : v[i]) + recv;
-    }
-  }
-  return v[0];
-}
 
 // v[8] per lane -> lane l holds the sum over the warp's lanes of v[l % 8]
 __device__ __forceinline__ float colsum8(float (&v)[8]) {
@@ -123,18 +106,12 @@ __device__ __forceinline__ uint32_t chunk_off(int r, int cb) { return r * 128 + 
 __global__ void __launch_bounds__(LTHREADS, 1)
     bwd_local_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
-                        const __grid_constant__ CUtensorMap tms0, const __grid_constant__ CUtensorMap tmds) {
+                        const __grid_constant__ CUtensorMap tms0, const __grid_constant__ CUtensorMap tmds,
+                        int n_items) {
   extern __shared__ unsigned char smraw[];
   LocalTcSmem &sm =
       *reinterpret_cast<LocalTcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
-  const int gc = blockIdx.x, h = blockIdx.y;
   const int H = a.H;
-  const int n = a.plan.chunk_seq[gc];
-  if (n < 0) return;
-  const int lc = gc - a.plan.seq_chunk0[n];
-  const int len = a.plan.seq_len[n];
-  const int tok0 = a.plan.seq_bos[n] + lc * CH;
-  const int nvalid = min(CH, len - lc * CH);
   const bool l2 = (a.flags & kFlagL2Norm) != 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wg = warp >> 2, wq = warp & 3;
@@ -143,8 +120,8 @@ __global__ void __launch_bounds__(LTHREADS, 1)
   int *err = a.status;
 
   if (tid == 0) {
-    mbar_init(u32(&sm.bar_tma), 1);
-    mbar_init(u32(&sm.bar_st), 1);
+    mbar_init(u32(&sm.bar_a), 1);
+    mbar_init(u32(&sm.bar_b), 1);
     mbar_init(u32(&sm.bar_mma), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
@@ -157,30 +134,6 @@ __global__ void __launch_bounds__(LTHREADS, 1)
   fence_after();
   const uint32_t tm = sm.tmem_base;
   const uint32_t tl = (uint32_t)(wq * 32) << 16;
-
-  // ---- loads: TMA for the six tiles, plain loads for g, beta
-  if (tid == 0) {
-    const uint32_t bar = u32(&sm.bar_tma), bst = u32(&sm.bar_st);
-    mbar_expect_tx(bar, 8 * HT);
-    mbar_expect_tx(bst, 8 * HT);
-    tma_load_3d(u32(sm.kq + 0 * HT), &tmk, 0, h, tok0, bar);
-    tma_load_3d(u32(sm.kq + 2 * HT), &tmk, 64, h, tok0, bar);
-    tma_load_3d(u32(sm.kq + 1 * HT), &tmq, 0, h, tok0, bar);
-    tma_load_3d(u32(sm.kq + 3 * HT), &tmq, 64, h, tok0, bar);
-    tma_load_3d(u32(sm.v), &tmv, 0, h, tok0, bar);
-    tma_load_3d(u32(sm.v + HT), &tmv, 64, h, tok0, bar);
-    tma_load_3d(u32(sm.dob), &tmdo, 0, h, tok0, bar);
-    tma_load_3d(u32(sm.dob + HT), &tmdo, 64, h, tok0, bar);
-    const int srow = (gc * H + h) * D;
-    // the states are first needed at P3: their own barrier, waited there
-    tma_load_3d(u32(sm.s0), &tms0, 0, srow, 0, bst);
-    tma_load_3d(u32(sm.s0 + 2 * HT), &tms0, 64, srow, 0, bst);
-    tma_load_3d(u32(sm.ds), &tmds, 0, srow, 0, bst);
-    tma_load_3d(u32(sm.ds + 2 * HT), &tmds, 64, srow, 0, bst);
-  }
-  if (tid < 64) sm.g[tid] = tid < nvalid ? a.g[(size_t)(tok0 + tid) * H + h] : 0.f;
-  else if (tid < 128) sm.beta[tid - 64] = (tid - 64) < nvalid ? a.beta[(size_t)(tok0 + tid - 64) * H + h] : 0.f;
-  bool ok = mbar_wait(u32(&sm.bar_tma), 0, err, 8);
   uint32_t phase = 0;
   auto mma_done = [&]() {
     const bool r = mbar_wait(u32(&sm.bar_mma), phase, err, 4);
@@ -188,7 +141,65 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     fence_after();
     return r;
   };
-  if (__syncthreads_or(!ok)) goto out;
+
+  // Work items (chunk gc, head h) = (item / H, item % H), strided over the persistent CTAs; chunks past
+  // the plan's total are skipped.  The tiles of the next item are loaded by TMA while this one finishes:
+  // dO once the dq staging in its buffer is stored, everything else once the last product (P9) is done.
+  auto next_valid = [&](int item) {
+    while (item < n_items && a.plan.chunk_seq[item / H] < 0) item += gridDim.x;
+    return item;
+  };
+  auto item_tok0 = [&](int item) {
+    const int gc = item / H, n = a.plan.chunk_seq[gc];
+    return a.plan.seq_bos[n] + (gc - a.plan.seq_chunk0[n]) * CH;
+  };
+  auto issue_main = [&](int item) {  // K, Q, V, S0, dS
+    const int hh = item % H, t0 = item_tok0(item), srow = item * D;  // state rows of (chunk, head)
+    const uint32_t bar = u32(&sm.bar_a);
+    mbar_expect_tx(bar, 14 * HT);
+    tma_load_3d(u32(sm.kq + 0 * HT), &tmk, 0, hh, t0, bar);
+    tma_load_3d(u32(sm.kq + 2 * HT), &tmk, 64, hh, t0, bar);
+    tma_load_3d(u32(sm.kq + 1 * HT), &tmq, 0, hh, t0, bar);
+    tma_load_3d(u32(sm.kq + 3 * HT), &tmq, 64, hh, t0, bar);
+    tma_load_3d(u32(sm.v), &tmv, 0, hh, t0, bar);
+    tma_load_3d(u32(sm.v + HT), &tmv, 64, hh, t0, bar);
+    tma_load_3d(u32(sm.s0), &tms0, 0, srow, 0, bar);
+    tma_load_3d(u32(sm.s0 + 2 * HT), &tms0, 64, srow, 0, bar);
+    tma_load_3d(u32(sm.ds), &tmds, 0, srow, 0, bar);
+    tma_load_3d(u32(sm.ds + 2 * HT), &tmds, 64, srow, 0, bar);
+  };
+  auto issue_do = [&](int item) {
+    const int hh = item % H, t0 = item_tok0(item);
+    const uint32_t bar = u32(&sm.bar_b);
+    mbar_expect_tx(bar, 2 * HT);
+    tma_load_3d(u32(sm.dob), &tmdo, 0, hh, t0, bar);
+    tma_load_3d(u32(sm.dob + HT), &tmdo, 64, hh, t0, bar);
+  };
+  int item = next_valid(blockIdx.x);
+  if (tid == 0 && item < n_items) {
+    issue_main(item);
+    issue_do(item);
+  }
+  bool pend_main = item < n_items, pend_do = pend_main, failed = false;
+  uint32_t it = 0;  // parity of the TMA barriers: one completion per item
+  for (; item < n_items; ++it) {
+  const int nitem = next_valid(item + gridDim.x);
+  const int gc = item / H, h = item % H;
+  const int n = a.plan.chunk_seq[gc];
+  const int lc = gc - a.plan.seq_chunk0[n];
+  const int len = a.plan.seq_len[n];
+  const int tok0 = a.plan.seq_bos[n] + lc * CH;
+  const int nvalid = min(CH, len - lc * CH);
+  if (tid < 64) sm.g[tid] = tid < nvalid ? a.g[(size_t)(tok0 + tid) * H + h] : 0.f;
+  else if (tid < 128) sm.beta[tid - 64] = (tid - 64) < nvalid ? a.beta[(size_t)(tok0 + tid - 64) * H + h] : 0.f;
+  {
+    const bool ok = mbar_wait(u32(&sm.bar_a), it & 1, err, 8) && mbar_wait(u32(&sm.bar_b), it & 1, err, 8);
+    pend_main = pend_do = false;
+    if (__syncthreads_or(!ok)) {
+      failed = true;
+      break;
+    }
+  }
   if (warp == 0) gate_prefix(sm.g, sm.gt);
   // ---- prep: bf16 -> fp16 in place; q, k normalised (norms kept for the Jacobians); rows >= nvalid zero
 #pragma unroll 1
@@ -246,7 +257,10 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     mma_commit(u32(&sm.bar_mma));
   }
   __syncwarp();
-  if (__syncthreads_or(!mma_done())) goto out;
+  if (__syncthreads_or(!mma_done())) {
+    failed = true;
+    break;
+  }
   // R1: rows 0-63 -> N (fp32), rows 64-127 -> P (fp16, [r][i])
 #pragma unroll 1
   for (int q4 = 0; q4 < 2; ++q4) {
@@ -291,7 +305,10 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     mma_commit(u32(&sm.bar_mma));
   }
   __syncwarp();
-  if (__syncthreads_or(!mma_done())) goto out;
+  if (__syncthreads_or(!mma_done())) {
+    failed = true;
+    break;
+  }
   // R2: W^T (lanes d_k, columns token) * gam -> wt
 #pragma unroll 1
   for (int q4 = 0; q4 < 2; ++q4) {
@@ -306,7 +323,6 @@ __global__ void __launch_bounds__(LTHREADS, 1)
   fence_async_smem();
   __syncthreads();
 
-  if (__syncthreads_or(!mbar_wait(u32(&sm.bar_st), 0, err, 8))) goto out;
   {  // <dS, S0> over the whole state (both tiles share one layout, so compare byte positions)
     float acc = 0.f;
     const uint4 *A4 = reinterpret_cast<const uint4 *>(sm.s0), *B4 = reinterpret_cast<const uint4 *>(sm.ds);
@@ -336,7 +352,10 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     mma_commit(u32(&sm.bar_mma));
   }
   __syncwarp();
-  if (__syncthreads_or(!mma_done())) goto out;
+  if (__syncthreads_or(!mma_done())) {
+    failed = true;
+    break;
+  }
   // R3: Ut^T -> ut
 #pragma unroll 1
   for (int q4 = 0; q4 < 2; ++q4) {
@@ -369,7 +388,10 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     mma_commit(u32(&sm.bar_mma));
   }
   __syncwarp();
-  if (__syncthreads_or(!mma_done())) goto out;
+  if (__syncthreads_or(!mma_done())) {
+    failed = true;
+    break;
+  }
   {  // R4: dUt^T = cdec*Y + Z -> wt (W^T is dead);  per-token sums <Ut, Y>, <dUt, Ut> over d_v
     float t1 = 0.f, t2 = 0.f;
 #pragma unroll 1
@@ -423,7 +445,10 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     mma_commit(u32(&sm.bar_mma));
   }
   __syncwarp();
-  if (__syncthreads_or(!mma_done())) goto out;
+  if (__syncthreads_or(!mma_done())) {
+    failed = true;
+    break;
+  }
   {
     // dP rows (lanes 0-63): Z = dP * P row sums (thread-local) and column sums; dPm over P
     if (row < 64) {
@@ -520,7 +545,15 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     mma_commit(u32(&sm.bar_mma));
   }
   __syncwarp();
-  if (__syncthreads_or(!mma_done())) goto out;
+  if (__syncthreads_or(!mma_done())) {
+    failed = true;
+    break;
+  }
+  {  // K^ -> wt (dUt^T is dead): R9 reads k^ there, so the K/Q buffer is free once P9 is done
+    const uint4 *src = reinterpret_cast<const uint4 *>(sm.kq);
+    uint4 *dst = reinterpret_cast<uint4 *>(sm.wt);
+    for (int e = tid; e < 2 * HT / 16; e += LTHREADS) dst[e] = src[(e >= HT / 16 ? 2 * HT / 16 : 0) + (e % (HT / 16))];
+  }
   {
     // dq^T = gam*Qa + Qb (lanes d_k): <dQ1, q^> and Jacobian dots over d_k; stage dq^ (fp32 kept in regs)
     {
@@ -615,7 +648,12 @@ __global__ void __launch_bounds__(LTHREADS, 1)
       sm.acc[6][tid] = sm.part[8][tid] + sm.part[9][tid];                                      // beta col terms
     }
   }
+  fence_async_smem();
   __syncthreads();
+  if (nitem < n_items) {  // dO of the next item into its (now free) buffer
+    if (tid == 0) issue_do(nitem);
+    pend_do = true;
+  }
 
   // ---- P7: Y1 = Ahat^T dAhat -> T0
   if (tid == 0) {
@@ -628,7 +666,10 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     mma_commit(u32(&sm.bar_mma));
   }
   __syncwarp();
-  if (__syncthreads_or(!mma_done())) goto out;
+  if (__syncthreads_or(!mma_done())) {
+    failed = true;
+    break;
+  }
   if (row < 64) {  // R7: Y1 -> v (first half; V is dead)
 #pragma unroll 1
     for (int q4 = 0; q4 < 2; ++q4) {
@@ -652,7 +693,10 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     mma_commit(u32(&sm.bar_mma));
   }
   __syncwarp();
-  if (__syncthreads_or(!mma_done())) goto out;
+  if (__syncthreads_or(!mma_done())) {
+    failed = true;
+    break;
+  }
   if (row < 64) {  // R8: dN[r][i] = beta_r dT_ri (i < r), zero elsewhere; beta row sums of dT * N
     const int r = row;
     const float br = sm.beta[r];
@@ -700,7 +744,16 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     mma_commit(u32(&sm.bar_mma));
   }
   __syncwarp();
-  if (__syncthreads_or(!mma_done())) goto out;
+  if (__syncthreads_or(!mma_done())) {
+    failed = true;
+    break;
+  }
+  fence_async_smem();
+  __syncthreads();
+  if (nitem < n_items) {  // K, Q, V, S0, dS of the next item: their buffers are free after P9
+    if (tid == 0) issue_main(nitem);
+    pend_main = true;
+  }
   {  // R9: dk^T = Ka + cdec * Kb (lanes d_k); Jacobian; dk out
     if (l2) {
       float t2 = 0.f;
@@ -713,7 +766,7 @@ __global__ void __launch_bounds__(LTHREADS, 1)
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int tkn = cb + i;
-          ka[i] = (ka[i] + sm.gt.cdec[tkn] * kbv[i]) * ld_f16(sm.kq, tkn, row, 2 * HT);
+          ka[i] = (ka[i] + sm.gt.cdec[tkn] * kbv[i]) * ld_f16(sm.wt, tkn, row, HT);
         }
         const float a2 = colsum8(ka);
         if ((lane >> 3) == q4) t2 = a2;
@@ -721,7 +774,7 @@ __global__ void __launch_bounds__(LTHREADS, 1)
       if (lane < 16) sm.part[wq][c0 + lane] = t2;
     }
     __syncthreads();
-    bf16 *stg = reinterpret_cast<bf16 *>(sm.dob);
+    bf16 *stg = reinterpret_cast<bf16 *>(sm.x2);  // x2 + ah (16 KB, both dead after P8)
 #pragma unroll 1
     for (int q4 = 0; q4 < 2; ++q4) {
       const int cb = c0 + q4 * 8;
@@ -734,7 +787,7 @@ __global__ void __launch_bounds__(LTHREADS, 1)
         float o = ka[i] + sm.gt.cdec[tkn] * kbv[i];
         if (l2) {
           const float dot = sm.part[0][tkn] + sm.part[1][tkn] + sm.part[2][tkn] + sm.part[3][tkn];
-          o = (o - ld_f16(sm.kq, tkn, row, 2 * HT) * dot) * sm.nk[tkn];
+          o = (o - ld_f16(sm.wt, tkn, row, HT) * dot) * sm.nk[tkn];
         }
         stg[tkn * D + row] = __float2bfloat16_rn(o);
       }
@@ -744,7 +797,7 @@ __global__ void __launch_bounds__(LTHREADS, 1)
   __syncthreads();
   {
     bf16 *dkg = static_cast<bf16 *>(a.dk);
-    const uint4 *stg = reinterpret_cast<const uint4 *>(sm.dob);
+    const uint4 *stg = reinterpret_cast<const uint4 *>(sm.x2);
     for (int e = tid; e < CH * (D / 8); e += LTHREADS) {
       const int r = e >> 4, cc = e & 15;
       if (r < nvalid) *reinterpret_cast<uint4 *>(dkg + ((size_t)(tok0 + r) * H + h) * D + cc * 8) = stg[e];
@@ -785,7 +838,13 @@ __global__ void __launch_bounds__(LTHREADS, 1)
       }
     }
   }
-out:
+  __syncthreads();  // the next item rewrites the per-token scratch read above
+  item = nitem;
+  }
+  if (failed) {  // let prefetches already in flight land before the CTA leaves (bounded waits)
+    if (pend_main) mbar_wait(u32(&sm.bar_a), (it + 1) & 1, err, 8);
+    if (pend_do) mbar_wait(u32(&sm.bar_b), (it + 1) & 1, err, 8);
+  }
   fence_before();
   __syncthreads();
   fence_after();
@@ -800,8 +859,16 @@ int launch_bwd_local_tc(const BwdArgs &a, const CUtensorMap *maps, int CH_max, c
   static_assert(sizeof(LocalTcSmem) + 1024 <= 232448, "shared memory budget");
   cudaError_t e = cudaFuncSetAttribute(bwd_local_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  bwd_local_tc_kernel<<<dim3(CH_max, a.H), LTHREADS, smem, st>>>(a, maps[0], maps[1], maps[2], maps[3], maps[4],
-                                                                   maps[5]);
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 1;
+  }
+  const int n_items = CH_max * a.H;
+  const int grid = n_items < sms ? n_items : sms;  // persistent: one CTA per SM
+  bwd_local_tc_kernel<<<grid, LTHREADS, smem, st>>>(a, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
+                                                    n_items);
   return (int)cudaGetLastError();
 }
 
