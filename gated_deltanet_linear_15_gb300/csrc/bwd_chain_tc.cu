@@ -285,19 +285,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int c0 = wg * 32;
       tmem_ld32(tm + tl + TM_KQ + c0, v);
       if (row < 64) {
+        float4 *dst = reinterpret_cast<float4 *>(&sm.nf[row * LN + c0]);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) sm.nf[row * LN + c0 + i] = v[i];
+        for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
       } else {
         const int r = row - 64;
         const float gr = G.gp[r];
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
+          const float4 ga = reinterpret_cast<const float4 *>(G.rgp + c0 + q4 * 8)[0];
+          const float4 gb = reinterpret_cast<const float4 *>(G.rgp + c0 + q4 * 8)[1];
+          const float rg[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
           float y[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int col = c0 + q4 * 8 + i;
-            y[i] = col <= r ? v[q4 * 8 + i] * gr * G.rgp[col] : 0.f;
-          }
+          for (int i = 0; i < 8; ++i) y[i] = c0 + q4 * 8 + i <= r ? v[q4 * 8 + i] * gr * rg[i] : 0.f;
           st_chunk_f16(sm.p + r * 128 + ((((c0 >> 3) + q4) ^ (r & 7)) * 16), y);
         }
       }
@@ -305,7 +306,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     fence_before();
     __syncthreads();
     wy_inverse<false, false>(sm.nf, LN, gbeta, sm.ys, [&](int r, int cc, float a0, float a1) {
-      *reinterpret_cast<__half2 *>(sm.x1 + sw128_offset(r, cc)) = __floats2half2_rn(a0 * gbeta[cc], a1 * gbeta[cc + 1]);
+      const float2 bb = *reinterpret_cast<const float2 *>(gbeta + cc);
+      *reinterpret_cast<__half2 *>(sm.x1 + sw128_offset(r, cc)) = __floats2half2_rn(a0 * bb.x, a1 * bb.y);
     }, it == 0);
 
     // ---- MMA 2: W^T = K^T X1^T;  meanwhile dS -> fp16 operand copy (+ workspace), gam_C dS back to TMEM
@@ -352,9 +354,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tmem_ld32(tm + tl + TM_W + c0, v);
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
+        const float4 ga = reinterpret_cast<const float4 *>(G.gam + c0 + q4 * 8)[0];
+        const float4 gb = reinterpret_cast<const float4 *>(G.gam + c0 + q4 * 8)[1];
+        const float gm[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
         float y[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) y[i] = v[q4 * 8 + i] * G.gam[c0 + q4 * 8 + i];
+        for (int i = 0; i < 8; ++i) y[i] = v[q4 * 8 + i] * gm[i];
         st_chunk_f16(sm.wt + row * 128 + ((((c0 >> 3) + q4) ^ (row & 7)) * 16), y);
       }
     }

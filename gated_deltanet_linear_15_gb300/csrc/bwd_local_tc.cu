@@ -98,6 +98,13 @@ __device__ __forceinline__ float colsum8(float (&v)[8]) {
   return t;
 }
 
+// 8 consecutive floats from 16-byte aligned shared memory (two vector loads, broadcast across the warp)
+__device__ __forceinline__ void ld8f(const float *p, float (&v)[8]) {
+  const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
 // byte offset of the 16-byte chunk holding columns [cb, cb + 8) of row r in a swizzled tile
 __device__ __forceinline__ uint32_t chunk_off(int r, int cb) { return r * 128 + ((((cb & 63) >> 3) ^ (r & 7)) << 4); }
 
@@ -274,9 +281,10 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     } else {
       const int r = row - 64;
       const float gr = sm.gt.gp[r];
-      float y[8];
+      float y[8], rg[8];
+      ld8f(sm.gt.rgp + cb, rg);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) y[i] = cb + i <= r ? v[i] * gr * sm.gt.rgp[cb + i] : 0.f;
+      for (int i = 0; i < 8; ++i) y[i] = cb + i <= r ? v[i] * gr * rg[i] : 0.f;
       st_chunk_f16(sm.p + chunk_off(r, cb), y);
     }
   }
@@ -315,8 +323,10 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     const int cb = c0 + q4 * 8;
     float v[8];
     tmem_ld8(tm + tl + T1 + cb, v);
+    float gm[8];
+    ld8f(sm.gt.gam + cb, gm);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] *= sm.gt.gam[cb + i];
+    for (int i = 0; i < 8; ++i) v[i] *= gm[i];
     st_chunk_f16(sm.wt + chunk_off(row, cb), v);
   }
   fence_before();
@@ -401,9 +411,11 @@ __global__ void __launch_bounds__(LTHREADS, 1)
       tmem_ld8(tm + tl + T3 + cb, y);
       tmem_ld8(tm + tl + T4 + cb, z);
       tmem_ld8(tm + tl + T2 + cb, u);
+      float cd[8];
+      ld8f(sm.gt.cdec + cb, cd);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float du = sm.gt.cdec[cb + i] * y[i] + z[i];
+        const float du = cd[i] * y[i] + z[i];
         s1[i] = u[i] * y[i];
         s2[i] = du * u[i];
         z[i] = du;
@@ -463,13 +475,15 @@ __global__ void __launch_bounds__(LTHREADS, 1)
         uint8_t *pp = sm.p + chunk_off(r, cb);
         const uint4 raw = *reinterpret_cast<const uint4 *>(pp);
         const __half *ph = reinterpret_cast<const __half *>(&raw);
+float rg[8];
+        ld8f(sm.gt.rgp + cb, rg);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float dpv = v[i];
           const float zz = dpv * __half2float(ph[i]);
           rs += zz;
           zc[i] = zz;
-          y[i] = cb + i <= r ? dpv * gr * sm.gt.rgp[cb + i] : 0.f;
+          y[i] = cb + i <= r ? dpv * gr * rg[i] : 0.f;
         }
         st_chunk_f16(pp, y);
         const float a = colsum8(zc);
@@ -484,8 +498,10 @@ __global__ void __launch_bounds__(LTHREADS, 1)
       const int cb = c0 + q4 * 8;
       float v[8];
       tmem_ld8(tm + tl + T1 + cb, v);
+      float gm[8];
+      ld8f(sm.gt.gam + cb, gm);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] *= sm.gt.gam[cb + i];
+      for (int i = 0; i < 8; ++i) v[i] *= gm[i];
       st_chunk_f16(sm.s0 + chunk_off(row, cb), v);
     }
     // dV^T (lanes d_v, columns token): stage bf16 dv[token][d_v] in dob (dO is dead); <dV, v>
@@ -564,11 +580,13 @@ __global__ void __launch_bounds__(LTHREADS, 1)
         float qa[8], qb[8], s1[8], s2[8];
         tmem_ld8(tm + tl + T5 + cb, qa);
         tmem_ld8(tm + tl + T7 + cb, qb);
+        float gm[8];
+        ld8f(sm.gt.gam + cb, gm);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int tkn = cb + i;
           const float qv = ld_f16(sm.kq + HT, tkn, row, 2 * HT);
-          const float a1 = sm.gt.gam[tkn] * qa[i];
+          const float a1 = gm[i] * qa[i];
           s1[i] = a1 * qv;
           s2[i] = (qb[i] + a1) * qv;  // dq^ (w.r.t. the normalised, scaled q) times q^
         }
@@ -594,12 +612,15 @@ __global__ void __launch_bounds__(LTHREADS, 1)
         tmem_ld8(tm + tl + T4 + cb, m2);
         const uint4 raw = *reinterpret_cast<const uint4 *>(sm.ah + chunk_off(r, cb));
         const __half *hh = reinterpret_cast<const __half *>(&raw);
+        float rg[8], bt[8];
+        ld8f(sm.gt.rgp + cb, rg);
+        ld8f(sm.beta + cb, bt);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int col = cb + i;
-          const float x = m1[i] + (col <= r ? m2[i] * gr * sm.gt.rgp[col] : 0.f);
+          const float x = m1[i] + (col <= r ? m2[i] * gr * rg[i] : 0.f);
           m2[i] = __half2float(hh[i]) * x;
-          m1[i] = sm.beta[col] * x;
+          m1[i] = bt[i] * x;
         }
         st_chunk_f16(sm.x2 + chunk_off(r, cb), m1);
         const float a = colsum8(m2);
@@ -617,15 +638,26 @@ __global__ void __launch_bounds__(LTHREADS, 1)
       float qa[8], qb[8];
       tmem_ld8(tm + tl + T5 + cb, qa);
       tmem_ld8(tm + tl + T7 + cb, qb);
+      float gm[8], dt[8], nqv[8];
+      ld8f(sm.gt.gam + cb, gm);
+      if (l2) {
+        float p0[8], p1[8], p2[8], p3[8];
+        ld8f(sm.part[4] + cb, p0);
+        ld8f(sm.part[5] + cb, p1);
+        ld8f(sm.part[6] + cb, p2);
+        ld8f(sm.part[7] + cb, p3);
+        ld8f(sm.nq + cb, nqv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dt[i] = (p0[i] + p1[i]) + (p2[i] + p3[i]);
+      }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int tkn = cb + i;
-        const float dq = qb[i] + sm.gt.gam[tkn] * qa[i];
+        const float dq = qb[i] + gm[i] * qa[i];
         float o;
         if (l2) {
           const float qv = ld_f16(sm.kq + HT, tkn, row, 2 * HT);
-          const float dot = sm.part[4][tkn] + sm.part[5][tkn] + sm.part[6][tkn] + sm.part[7][tkn];
-          o = (a.scale * dq - qv * dot * rscale) * sm.nq[tkn];
+          o = (a.scale * dq - qv * dt[i] * rscale) * nqv[i];
         } else {
           o = a.scale * dq;
         }
@@ -763,10 +795,12 @@ __global__ void __launch_bounds__(LTHREADS, 1)
         float ka[8], kbv[8];
         tmem_ld8(tm + tl + T3 + cb, ka);
         tmem_ld8(tm + tl + T4 + cb, kbv);
+        float cd[8];
+        ld8f(sm.gt.cdec + cb, cd);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int tkn = cb + i;
-          ka[i] = (ka[i] + sm.gt.cdec[tkn] * kbv[i]) * ld_f16(sm.wt, tkn, row, HT);
+          ka[i] = (ka[i] + cd[i] * kbv[i]) * ld_f16(sm.wt, tkn, row, HT);
         }
         const float a2 = colsum8(ka);
         if ((lane >> 3) == q4) t2 = a2;
@@ -781,14 +815,23 @@ __global__ void __launch_bounds__(LTHREADS, 1)
       float ka[8], kbv[8];
       tmem_ld8(tm + tl + T3 + cb, ka);
       tmem_ld8(tm + tl + T4 + cb, kbv);
+      float cd[8], dt[8], nkv[8];
+      ld8f(sm.gt.cdec + cb, cd);
+      if (l2) {
+        float p0[8], p1[8], p2[8], p3[8];
+        ld8f(sm.part[0] + cb, p0);
+        ld8f(sm.part[1] + cb, p1);
+        ld8f(sm.part[2] + cb, p2);
+        ld8f(sm.part[3] + cb, p3);
+        ld8f(sm.nk + cb, nkv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dt[i] = (p0[i] + p1[i]) + (p2[i] + p3[i]);
+      }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int tkn = cb + i;
-        float o = ka[i] + sm.gt.cdec[tkn] * kbv[i];
-        if (l2) {
-          const float dot = sm.part[0][tkn] + sm.part[1][tkn] + sm.part[2][tkn] + sm.part[3][tkn];
-          o = (o - ld_f16(sm.wt, tkn, row, HT) * dot) * sm.nk[tkn];
-        }
+        float o = ka[i] + cd[i] * kbv[i];
+        if (l2) o = (o - ld_f16(sm.wt, tkn, row, HT) * dt[i]) * nkv[i];
         stg[tkn * D + row] = __float2bfloat16_rn(o);
       }
     }
