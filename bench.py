@@ -74,6 +74,34 @@ def job_throughput(total_ms, world, tokens_per_rank_step, steps):
     return world * tokens_per_rank_step * steps / (total_ms / 1000.0)
 
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture,
+# keyed by (profiler name, workload); valid only while the kernel's sources hash to the value
+# recorded with it (otherwise the roofline reports traffic null).  Summaries: profiles/*.md.
+NCU_TRAFFIC = {
+    ("bwd_local", "prefill_h32_t8192"): (717289728, "bwd_local_tc.cu", "b93b3731adc602c6"),
+    ("fwd_states", "prefill_h32_t8192"): (238025472, "fwd_tc.cu", "a09b8ea71e26822d"),
+    ("bwd_chain", "prefill_h32_t8192"): (320992768, "bwd_chain_tc.cu", "acef9b1bbb10a761"),
+}
+KERNEL_COMMON = ["chunk_common.cuh", "umma.cuh", "common.cuh", "kernels.h"]
+
+
+def measured_traffic(kernel, workload):
+    import hashlib
+    ent = NCU_TRAFFIC.get((kernel, workload))
+    if ent is None:
+        return None
+    nbytes, src, digest = ent
+    m = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gated_deltanet_linear_15_gb300", "csrc")
+    try:
+        for f in [src] + KERNEL_COMMON:
+            with open(os.path.join(csrc, f), "rb") as fh:
+                m.update(fh.read())
+    except OSError:
+        return None
+    return nbytes if m.hexdigest()[:16] == digest else None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -138,8 +166,11 @@ def cpu_oracle_sample(wname, heads=None, tokens=None):
     w = WORKLOADS[wname]
     cores = os.cpu_count() or 1
     Hs = min(w.H, heads or cores)
+    if not w.T:  # packed variable-length batch: the drawn lengths (~135k tokens), on fewer heads
+        Hs = max(1, Hs // 4)
     T = tokens or (w.T if w.T else 4096)
     x = make_inputs(w, "cpu", H=Hs, T=T, B=1)
+    T = x["q"].shape[0] * x["q"].shape[1]  # tokens actually in the sample
     t0 = time.perf_counter()
     oracle.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], scale=x["scale"], l2norm=x["l2norm"],
                nthreads=cores)
@@ -148,7 +179,7 @@ def cpu_oracle_sample(wname, heads=None, tokens=None):
     dt = time.perf_counter() - t0
     # the workload's tokens/s: T tokens of all H heads cost H/Hs times the sample
     tps = T * (Hs / w.H) / dt
-    return tps, min(cores, Hs), f"fwd+bwd of {Hs} of {w.H} heads x {T} tokens (B=1), {dt:.2f} s"
+    return tps, min(cores, Hs), f"fwd+bwd of {Hs} of {w.H} heads x {T} tokens, {dt:.2f} s"
 
 
 def run_reference(args):
@@ -291,7 +322,7 @@ def main():
         if alg is not None:
             ach = alg / avg_s / 1e9
             roof = {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
-                    "frac": round(ach / hbm_peak, 4), "peak_kind": peak_kind, "traffic": None,
+                    "frac": round(ach / hbm_peak, 4), "peak_kind": peak_kind, "traffic": measured_traffic(dom, args.workload),
                     "avg_launch_us": round(avg_s * 1e6, 2), "algorithmic_bytes_per_launch": alg}
     launches = sum(c for c, _ in kern.values())
     fwd_s = statistics.mean(fwd_ms) / 1000.0
