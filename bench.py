@@ -207,6 +207,65 @@ def run_reference(args):
     return 0
 
 
+# ----------------------------------------------------------------------------- decode arm
+def run_decode(args):
+    """gdn_recurrent_fwd on B sequences x T tokens (H=32, d=128, bf16, fp32 state updated in place).
+    The step is HBM-bound on the state: algorithmic bytes = state read + write (2 x 4 d^2 per
+    (sequence, head)) + q, k, v, o (4 x 2 d per token-head) + g, beta (8 per token-head)."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build_library()
+    import gated_deltanet_linear_15_gb300 as g
+    from gdn_inputs import make_inputs
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    B, T, H, D = args.decode_batch, args.decode_tokens, 32, 128
+    x = make_inputs("prefill_h32_t8192", dev, T=T, B=B, H=H, with_S0=True, seed=101)
+    S = x["S0"].clone()
+    o = torch.empty_like(x["v"])
+    shape = g.make_shape(x["q"], x["v"], scale=x["scale"], l2norm=x["l2norm"])
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        rc = g.gdn_recurrent_fwd(shape, x["q"], x["k"], x["v"], x["g"], x["beta"], S, o, S, stream)
+        assert rc == 0, g._lib.last_error()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    step_ms = statistics.median(ms)
+    hbm_peak, _, peak_kind = load_peaks()
+    nbytes = B * H * 2 * 4 * D * D + B * T * H * (4 * 2 * D + 8)
+    ach = nbytes / (step_ms / 1000.0) / 1e9
+    line = {"metric": "GDN recurrent decode tokens/s (bf16, d=128, fp32 state) on 1 GB300",
+            "value": B * T / (step_ms / 1000.0), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded gdn_inputs)",
+            "config": {"workload": f"decode_b{B}_h{H}_t{T}", "B": B, "T": T, "H": H, "d": D,
+                       "l2": "256 MB flush before every step, outside the events"},
+            "roofline": {"bound": "hbm", "kernel": "recurrent", "achieved": round(ach, 1), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": round(ach / hbm_peak, 4), "peak_kind": peak_kind, "traffic": None,
+                         "algorithmic_bytes_per_launch": nbytes},
+            "gpu_launches": args.steps, "clocks": clk}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
@@ -218,11 +277,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-tokens", type=int, default=None, help="tokens per sequence in the reference sample")
     ap.add_argument("--seg-chunks", type=int, default=0)
+    ap.add_argument("--decode", action="store_true",
+                    help="time the token-by-token decode entry point instead (B sequences x T tokens)")
+    ap.add_argument("--decode-batch", type=int, default=64)
+    ap.add_argument("--decode-tokens", type=int, default=1)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.decode:
+        return run_decode(args)
 
     import torch
     import torch.distributed as dist

@@ -109,6 +109,12 @@ def gdn_chunk_bwd(shape: GdnShape, q, k, v, g, beta, S0, dO, dS_T, dq, dk, dv, d
                                      _stream(stream))
 
 
+def gdn_recurrent_fwd(shape: GdnShape, q, k, v, g, beta, S_in, o, S_out, stream=None) -> int:
+    """Token-by-token forward (decoding); S_out may be S_in.  See gdn.h."""
+    return _lib.load().gdn_recurrent_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                         _ptr(S_in), _ptr(o), _ptr(S_out), _stream(stream))
+
+
 def gdn_profile_enable(on: bool) -> None:
     _check(_lib.load().gdn_profile_enable(int(bool(on))), "gdn_profile_enable")
 
@@ -158,6 +164,25 @@ def chunk_gated_delta_rule_fwd(q, k, v, g, beta, initial_state=None, output_fina
     ws = workspace if workspace is not None and workspace.numel() >= need else _workspace(need, q.device)
     _check(gdn_chunk_fwd(shape, q, k, v, g, beta, initial_state, o, S_T, ws), "gdn_chunk_fwd")
     return o, S_T
+
+
+def recurrent_gated_delta_rule(q, k, v, g, beta, initial_state=None, scale=None, use_qk_l2norm_in_kernel=False,
+                               inplace=False):
+    """Decode T tokens per sequence: returns (o, S_out).  q, k, v [B, T, H, d]; g, beta [B, T, H];
+    initial_state fp32 [B, H, d, d] or None.  With inplace=True the state is updated in
+    initial_state's own buffer (which is then returned as S_out)."""
+    _contig(q, k, v, g, beta, initial_state)
+    shape = make_shape(q, v, scale=scale, l2norm=use_qk_l2norm_in_kernel)
+    o = torch.empty_like(v)
+    B, _, H, D = q.shape
+    if inplace:
+        if initial_state is None:
+            raise ValueError("inplace=True needs an initial_state buffer")
+        S_out = initial_state
+    else:
+        S_out = torch.empty(B, H, v.shape[-1], D, dtype=torch.float32, device=q.device)
+    _check(gdn_recurrent_fwd(shape, q, k, v, g, beta, initial_state, o, S_out), "gdn_recurrent_fwd")
+    return o, S_out
 
 
 def chunk_gated_delta_rule_bwd(q, k, v, g, beta, dO, initial_state=None, dS_T=None, cu_seqlens=None, scale=None,

@@ -14,7 +14,7 @@ GDN_STATIC_SCRATCH_BYTES = 16 << 20
 
 # every symbol include/gdn.h declares
 EXPORTS = ("gdn_fwd_workspace_size", "gdn_bwd_workspace_size", "gdn_chunk_fwd", "gdn_chunk_fwd_static",
-           "gdn_chunk_bwd",
+           "gdn_chunk_bwd", "gdn_recurrent_fwd",
            "gdn_get_device_status", "gdn_plan_query", "gdn_profile_enable", "gdn_profile_report",
            "gdn_status_string", "gdn_last_error_string")
 
@@ -57,6 +57,8 @@ def load():
         lib.gdn_chunk_fwd_static.restype = ctypes.c_int
         lib.gdn_chunk_bwd.argtypes = [S, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
         lib.gdn_chunk_bwd.restype = ctypes.c_int
+        lib.gdn_recurrent_fwd.argtypes = [S, P, P, P, P, P, P, P, P, P]
+        lib.gdn_recurrent_fwd.restype = ctypes.c_int
         lib.gdn_get_device_status.argtypes = [S, P, P]
         lib.gdn_get_device_status.restype = ctypes.c_int
         lib.gdn_plan_query.argtypes = [S, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),

@@ -585,6 +585,42 @@ int gdn_chunk_bwd(const gdn_shape *s, const void *q, const void *k, const void *
   return GDN_OK;
 }
 
+int gdn_recurrent_fwd(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,
+                      const float *beta, const float *S_in, void *o, float *S_out, gdn_stream_t stream) {
+  g_last_error.clear();
+  if (!s) return fail(GDN_ERR_INVALID_ARG, "shape is NULL");
+  if (s->reserved[0] || s->reserved[1] || s->reserved[2]) return fail(GDN_ERR_INVALID_ARG, "reserved fields must be 0");
+  if (s->B < 1 || s->T < 0 || s->H < 1) return fail(GDN_ERR_INVALID_ARG, "need B >= 1, T >= 0, H >= 1");
+  if (s->cu_seqlens) return fail(GDN_ERR_UNSUPPORTED, "the recurrent form takes B sequences of T tokens (cu_seqlens must be NULL)");
+  if (s->Dk != s->Dv) return fail(GDN_ERR_UNSUPPORTED, "d_k != d_v is not supported");
+  if (s->Dk != 64 && s->Dk != 128) return fail(GDN_ERR_UNSUPPORTED, "d must be 64 or 128 (got %d)", s->Dk);
+  if (s->dtype != GDN_BF16 && s->dtype != GDN_FP32) return fail(GDN_ERR_INVALID_ARG, "unknown dtype");
+  if (!std::isfinite(s->scale) || s->scale == 0.f) return fail(GDN_ERR_INVALID_ARG, "scale must be finite and non-zero");
+  if ((long)s->B * s->H > (long)INT32_MAX / 4 || (long)s->B * s->T > (long)INT32_MAX / 2)
+    return fail(GDN_ERR_UNSUPPORTED, "too many sequences or tokens");
+  int rc = check_ptrs({{S_out, "S_out"}}, {{S_in, "S_in"}});
+  if (rc) return rc;
+  if (s->T > 0 && (rc = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {g, "g"}, {beta, "beta"}, {o, "o"}}, {})))
+    return rc;
+  RecArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.g = g;
+  a.beta = beta;
+  a.S_in = S_in;
+  a.o = o;
+  a.S_out = S_out;
+  a.T = s->T;
+  a.H = s->H;
+  a.scale = s->scale;
+  a.flags = s->flags;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  PROF("recurrent");
+  CK(launch_recurrent(a, s->dtype == GDN_BF16, s->Dk, s->B * s->H, st));
+  return GDN_OK;
+}
+
 int gdn_get_device_status(const gdn_shape *shape, const void *workspace, gdn_stream_t stream) {
   (void)shape;
   if (!workspace) return -1;

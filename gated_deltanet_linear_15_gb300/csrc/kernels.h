@@ -55,6 +55,17 @@ struct FixupArgs {
   int reverse;
 };
 
+struct RecArgs {
+  const void *q, *k, *v;  // [N, T, H, D] element type of the call
+  const float *g, *beta;  // [N, T, H]
+  const float *S_in;      // [N, H, D, D] or NULL (zeros)
+  void *o;                // [N, T, H, D]
+  float *S_out;           // [N, H, D, D], may equal S_in
+  int T, H;
+  float scale;
+  unsigned flags;
+};
+
 int launch_plan(const Plan &p, const int *cu, int N, int T, int Lseg, int S_max, int CH_max, int *status,
                 cudaStream_t st);
 int launch_gate_scan(const Plan &p, const float *g, int H, int CH_max, float *gsum, int *status, cudaStream_t st);
@@ -70,5 +81,7 @@ int launch_bwd_local(const BwdArgs &a, bool is_bf16, int D, int CH_max, cudaStre
 // tcgen05 local-gradient kernel (bf16, d = 128); maps: q, k, v, dO ([tokens, H, 128] bf16, box 64x1x64) and
 // the fp16 per-chunk states S0 and dS ([rows, 128] as a 3-D map, box 64x128x1)
 int launch_bwd_local_tc(const BwdArgs &a, const CUtensorMap *maps, int CH_max, cudaStream_t st);
+// token-by-token forward over NH = N * H (sequence, head) pairs
+int launch_recurrent(const RecArgs &a, bool is_bf16, int D, int NH, cudaStream_t st);
 
 }  // namespace gdn

@@ -141,6 +141,25 @@ int gdn_chunk_bwd(const gdn_shape *shape,
                   float *dS0,        /* required iff S0 != NULL */
                   void *workspace, size_t workspace_bytes, gdn_stream_t stream);
 
+/* Token-by-token (recurrent) forward for decoding a few tokens per sequence,
+ * e.g. after a chunked prefill: for every sequence n < B, head h and token
+ * t = 0 .. T-1 in order,
+ *     S <- exp(g_t) S;   S <- S + beta_t (v_t - S k_t) k_t^T;   o_t = S (scale q_t)
+ * with q_t, k_t L2-normalised first when GDN_L2NORM_QK is set.  This is the
+ * recurrence stated in the header above, evaluated without chunking (the
+ * tilnote.io note on FlashQLA, section on the workloads it wins, names
+ * agentic inference as a target use; the onedev.kr summary's background
+ * paragraph states the d x d state update).
+ *   q, k, v, o: [B, T, H, d] (dtype of the shape); g, beta: fp32 [B, T, H];
+ *   S_in: fp32 [B, H, d_v, d_k] or NULL (zero state); S_out: fp32 [B, H, d_v, d_k],
+ *   which may be the same buffer as S_in (updated in place).
+ * The shape must have cu_seqlens == NULL (GDN_ERR_UNSUPPORTED otherwise),
+ * d 64 or 128, bf16 or fp32 (fp32 also at d = 128); seg_chunks and the SP flags
+ * are ignored.  T == 0 copies S_in (or zeros) to S_out.  No workspace; state
+ * precision fp32 throughout; asynchronous on `stream`. */
+int gdn_recurrent_fwd(const gdn_shape *shape, const void *q, const void *k, const void *v, const float *g,
+                      const float *beta, const float *S_in, void *o, float *S_out, gdn_stream_t stream);
+
 /* Reads the device status word that the kernels of the last call on `stream`
  * set (synchronises the stream).  Every bit means the outputs of that call are
  * not reliable:

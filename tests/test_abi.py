@@ -121,3 +121,32 @@ def test_plan_query_sp_policy(lib):
     s = _shape(T=65536, H=8)           # long context, few heads: split
     lib.gdn_plan_query(ctypes.byref(s), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c))
     assert 1 < a.value < 1024 and b.value * 8 >= 100
+
+
+def _rec(lib, s, **ptrs):
+    p = dict(q=0x10000, k=0x10000, v=0x10000, g=0x10000, beta=0x10000, S_in=0, o=0x10000, S_out=0x10000)
+    p.update(ptrs)
+    return lib.gdn_recurrent_fwd(ctypes.byref(s), p["q"], p["k"], p["v"], p["g"], p["beta"], p["S_in"], p["o"],
+                                 p["S_out"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Dk=96, Dv=96), _lib.GDN_ERR_UNSUPPORTED),
+    (dict(Dk=128, Dv=64), _lib.GDN_ERR_UNSUPPORTED),
+    (dict(cu_seqlens=0x10000, num_seqs=1, B=1), _lib.GDN_ERR_UNSUPPORTED),  # B sequences of T tokens only
+    (dict(H=0), _lib.GDN_ERR_INVALID_ARG),
+    (dict(T=-1), _lib.GDN_ERR_INVALID_ARG),
+    (dict(dtype=7), _lib.GDN_ERR_INVALID_ARG),
+])
+def test_recurrent_bad_shapes_rejected(lib, kw, code):
+    assert _rec(lib, _shape(**kw)) == code
+    assert lib.gdn_last_error_string() != b""
+
+
+def test_recurrent_pointer_checks(lib):
+    s = _shape()
+    assert _rec(lib, s, S_out=0) == _lib.GDN_ERR_INVALID_ARG
+    assert b"S_out is NULL" in lib.gdn_last_error_string()
+    assert _rec(lib, s, k=0) == _lib.GDN_ERR_INVALID_ARG
+    assert _rec(lib, s, S_in=0x10004) == _lib.GDN_ERR_INVALID_ARG
+    assert b"aligned" in lib.gdn_last_error_string()
