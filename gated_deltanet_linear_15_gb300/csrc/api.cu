@@ -55,6 +55,7 @@ struct Layout {
   size_t off_E = 0, off_M = 0, off_S = 0;     // forward fix-up buffers
   size_t off_states = 0, off_dstates = 0;   // backward per-chunk states
   size_t off_F = 0, off_R = 0, off_dS = 0;  // reverse fix-up buffers
+  size_t off_wy = 0, wy_bytes = 0;          // backward WY tiles (bf16, d = 128)
   size_t fwd_total = 0, bwd_total = 0;
 };
 
@@ -148,6 +149,9 @@ int make_layout(const gdn_shape *s, Layout &L) {
   off += spbuf;
   L.off_dS = off;
   off += spbuf;
+  L.off_wy = off;
+  L.wy_bytes = (s->dtype == GDN_BF16 && L.D == 128) ? (size_t)L.CH_max * L.H * 3 * CH * CH * 2 : 0;
+  off = align256(off + L.wy_bytes);
   L.bwd_total = off;
   return GDN_OK;
 }
@@ -310,17 +314,33 @@ int state_map(CUtensorMap *m, const void *ptr, long rows) {
   return GDN_OK;
 }
 
+// WY tiles: fp16 [rows, 64] (three 64-row tiles per (chunk, head)), box = 64 x 64, 128-byte swizzle
+int wy_map(CUtensorMap *m, const void *ptr, long rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, 1};
+  cuuint64_t strides[2] = {64 * 2, (cuuint64_t)rows * 64 * 2};
+  cuuint32_t box[3] = {64, 64, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return GDN_OK;
+}
+
 // The chunk forward kernel for this problem: tcgen05 for bf16 with d = 128, the
 // mma.sync/CUDA-core kernel otherwise (d = 64, fp32 inputs, empty batches).
 int launch_forward_kernel(const Layout &L, const gdn_shape *s, const FwdArgs &fa, dim3 grid, cudaStream_t st) {
   const bool bf = s->dtype == GDN_BF16;
   if (bf && L.D == 128 && L.Ttot > 0) {
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, tw;
     int rc;
     if ((rc = qkv_map(&tk, fa.k, L.Ttot, L.H))) return rc;
     if ((rc = qkv_map(&tv, fa.v, L.Ttot, L.H))) return rc;
     if ((rc = qkv_map(&tq, fa.q ? fa.q : fa.k, L.Ttot, L.H))) return rc;
-    return launch_fwd_tc(fa, tq, tk, tv, grid, st);
+    if ((rc = wy_map(&tw, fa.wy ? fa.wy : fa.k, fa.wy ? (long)L.CH_max * L.H * 3 * CH : 64))) return rc;
+    return launch_fwd_tc(fa, tq, tk, tv, tw, grid, st);
   }
   return launch_fwd_chunk(fa, bf, L.D, grid, st);
 }
@@ -493,8 +513,25 @@ int gdn_chunk_bwd(const gdn_shape *s, const void *q, const void *k, const void *
   const bool bf = s->dtype == GDN_BF16;
   Plan pl;
   if ((rc = prologue(s, L, ws, g, st, pl))) return rc;
+  // 0. WY tiles of every chunk, shared by the three passes below (bf16, d = 128)
+  const void *wy = nullptr;
+  if (L.wy_bytes > 0 && L.Ttot > 0) {
+    WyArgs wa;
+    wa.k = k;
+    wa.g = g;
+    wa.beta = beta;
+    wa.plan = pl;
+    wa.wy = ws + L.off_wy;
+    wa.status = reinterpret_cast<int *>(ws + L.off_status);
+    wa.H = L.H;
+    wa.flags = s->flags;
+    PROF("bwd_wy");
+    CK(launch_wy(wa, L.CH_max, st));
+    wy = wa.wy;
+  }
   // 1. forward states at every chunk start
   FwdArgs fa = fwd_args(s, L, ws, pl);
+  fa.wy = wy;
   fa.q = q;
   fa.k = k;
   fa.v = v;
@@ -529,15 +566,17 @@ int gdn_chunk_bwd(const gdn_shape *s, const void *q, const void *k, const void *
   }
   ba.states = ws + L.off_states;
   ba.dstates = ws + L.off_dstates;
+  ba.wy = wy;
   ba.H = L.H;
   ba.Lseg = L.Lseg;
   ba.scale = s->scale;
   ba.flags = s->flags;
   // the reverse chain: tcgen05 for bf16 with d = 128, the mma.sync kernel otherwise
   const bool chain_tc = bf && L.D == 128 && L.Ttot > 0;
-  CUtensorMap cmaps[3];
+  CUtensorMap cmaps[4];
   if (chain_tc && ((rc = qkv_map(&cmaps[0], q, L.Ttot, L.H)) || (rc = qkv_map(&cmaps[1], k, L.Ttot, L.H)) ||
-                   (rc = qkv_map(&cmaps[2], dO, L.Ttot, L.H))))
+                   (rc = qkv_map(&cmaps[2], dO, L.Ttot, L.H)) ||
+                   (rc = wy_map(&cmaps[3], wy ? wy : k, wy ? (long)L.CH_max * L.H * 3 * CH : 64))))
     return rc;
   auto chain = [&](dim3 grid) {
     return chain_tc ? launch_bwd_chain_tc(ba, cmaps, grid, st) : launch_bwd_chain(ba, bf, L.D, grid, st);
@@ -571,11 +610,12 @@ int gdn_chunk_bwd(const gdn_shape *s, const void *q, const void *k, const void *
   {
     PROF("bwd_local");
     if (bf && L.D == 128 && L.Ttot > 0) {
-      CUtensorMap maps[6];
+      CUtensorMap maps[7];
       if ((rc = qkv_map(&maps[0], q, L.Ttot, L.H)) || (rc = qkv_map(&maps[1], k, L.Ttot, L.H)) ||
           (rc = qkv_map(&maps[2], v, L.Ttot, L.H)) || (rc = qkv_map(&maps[3], dO, L.Ttot, L.H)) ||
           (rc = state_map(&maps[4], ws + L.off_states, (long)L.CH_max * L.H * 128)) ||
-          (rc = state_map(&maps[5], ws + L.off_dstates, (long)L.CH_max * L.H * 128)))
+          (rc = state_map(&maps[5], ws + L.off_dstates, (long)L.CH_max * L.H * 128)) ||
+          (rc = wy_map(&maps[6], wy ? wy : k, wy ? (long)L.CH_max * L.H * 3 * CH : 64)))
         return rc;
       CK(launch_bwd_local_tc(ba, maps, L.CH_max, st));
     } else {

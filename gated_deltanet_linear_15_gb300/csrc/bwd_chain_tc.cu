@@ -37,6 +37,7 @@ struct __align__(1024) ChainTcSmem {
   Gates gt[2];
   float ys[1152];
   uint64_t bar_tma[2];
+  uint64_t bar_x;  // precomputed X1 tile of the current chunk (TMA)
   uint64_t bar_mma;
   uint32_t tmem_base;
 };
@@ -54,7 +55,7 @@ __device__ __forceinline__ void st_chunk_f16(uint8_t *dst, const float *v) {
 
 __global__ void __launch_bounds__(NTHREADS, 1)
     bwd_chain_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                        const __grid_constant__ CUtensorMap tmdo) {
+                        const __grid_constant__ CUtensorMap tmdo, const __grid_constant__ CUtensorMap tmw) {
   extern __shared__ unsigned char smraw[];
   ChainTcSmem &sm =
       *reinterpret_cast<ChainTcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
@@ -96,6 +97,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (tid == 0) {
     mbar_init(u32(&sm.bar_tma[0]), 1);
     mbar_init(u32(&sm.bar_tma[1]), 1);
+    mbar_init(u32(&sm.bar_x), 1);
     mbar_init(u32(&sm.bar_mma), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     tma_prefetch_desc(&tmk);
@@ -133,8 +135,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     load_scalars(sm.beta[stage], a.beta, H, h, tok0, nvalid, 64);
     cp_async_commit();
   };
+  // X1 = Ahat diag(beta) of chunk c, precomputed for the backward: loaded into sm.x1 once the
+  // previous chunk's MMA 2 has read it, waited for just before this chunk's MMA 2
+  const bool use_wy = a.wy != nullptr;
+  auto issue_x1 = [&](int c) {
+    const uint32_t bar = u32(&sm.bar_x);
+    mbar_expect_tx(bar, HT);
+    tma_load_3d(u32(sm.x1), &tmw, 0, ((chunk0 + c) * H + h) * 3 * CH, 0, bar);
+  };
   if (clast >= cbeg) {
     if (tid == 0) issue_tma(clast, 0);
+    if (tid == 0 && use_wy) issue_x1(clast);
     issue_gb(clast, 0, true);
   }
 
@@ -264,7 +275,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncthreads();
 
     // ---- MMA 1: [K; Q] K^T
-    if (tid == 0) {
+    const bool need_kq = !use_wy || with_do;  // with X1 given, only P (rows 64-127) is still needed
+    if (need_kq && tid == 0) {
       fence_after();
       const uint32_t idesc = idesc_f16(128, 64, false, false);
       const uint32_t base = u32(st);
@@ -276,11 +288,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mma_commit(u32(&sm.bar_mma));
     }
     __syncwarp();
-    if (__syncthreads_or(!mma_wait())) {
+    if (need_kq && __syncthreads_or(!mma_wait())) {
       failed = true;
       break;
     }
-    if (row < 64 || with_do) {
+    if ((row < 64 && !use_wy) || (row >= 64 && with_do)) {
       float v[32];
       const int c0 = wg * 32;
       tmem_ld32(tm + tl + TM_KQ + c0, v);
@@ -305,10 +317,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     fence_before();
     __syncthreads();
-    wy_inverse<false, false>(sm.nf, LN, gbeta, sm.ys, [&](int r, int cc, float a0, float a1) {
-      const float2 bb = *reinterpret_cast<const float2 *>(gbeta + cc);
-      *reinterpret_cast<__half2 *>(sm.x1 + sw128_offset(r, cc)) = __floats2half2_rn(a0 * bb.x, a1 * bb.y);
-    }, it == 0);
+    if (!use_wy) {
+      wy_inverse<false, false>(sm.nf, LN, gbeta, sm.ys, [&](int r, int cc, float a0, float a1) {
+        const float2 bb = *reinterpret_cast<const float2 *>(gbeta + cc);
+        *reinterpret_cast<__half2 *>(sm.x1 + sw128_offset(r, cc)) = __floats2half2_rn(a0 * bb.x, a1 * bb.y);
+      }, it == 0);
+    } else if (__syncthreads_or(!mbar_wait(u32(&sm.bar_x), it & 1, err, 8))) {
+      failed = true;
+      break;
+    }
 
     // ---- MMA 2: W^T = K^T X1^T;  meanwhile dS -> fp16 operand copy (+ workspace), gam_C dS back to TMEM
     if (tid == 0) {
@@ -348,6 +365,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       failed = true;
       break;
     }
+    if (use_wy && tid == 0 && c - 1 >= cbeg) issue_x1(c - 1);  // MMA 2 has consumed sm.x1
     {  // W^T read-out, columns scaled by gam
       const int c0 = wg * 32;
       float v[32];
@@ -462,7 +480,7 @@ int launch_bwd_chain_tc(const BwdArgs &a, const CUtensorMap *maps, dim3 grid, cu
   static_assert(sizeof(ChainTcSmem) + 1024 <= 232448, "shared memory budget");
   cudaError_t e = cudaFuncSetAttribute(bwd_chain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  bwd_chain_tc_kernel<<<grid, NTHREADS, smem, st>>>(a, maps[0], maps[1], maps[2]);
+  bwd_chain_tc_kernel<<<grid, NTHREADS, smem, st>>>(a, maps[0], maps[1], maps[2], maps[3]);
   return (int)cudaGetLastError();
 }
 

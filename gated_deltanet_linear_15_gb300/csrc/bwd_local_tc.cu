@@ -59,7 +59,7 @@ struct __align__(1024) LocalTcSmem {
   float part[20][CH];   // per-token partial sums (reused per round)
   float acc[12][CH];    // assembled per-token terms
   float red[LWARPS];
-  uint64_t bar_a, bar_b, bar_mma;  // TMA: {K, Q, V, S0, dS}, {dO}; tensor-core completion
+  uint64_t bar_a, bar_b, bar_w, bar_mma;  // TMA: {K, Q, V, S0, dS}, {dO}, {X1, X2, Ahat}; tensor-core completion
   uint32_t tmem_base;
 };
 
@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     bwd_local_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
                         const __grid_constant__ CUtensorMap tms0, const __grid_constant__ CUtensorMap tmds,
-                        int n_items) {
+                        const __grid_constant__ CUtensorMap tmw, int n_items) {
   extern __shared__ unsigned char smraw[];
   LocalTcSmem &sm =
       *reinterpret_cast<LocalTcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(LTHREADS, 1)
   if (tid == 0) {
     mbar_init(u32(&sm.bar_a), 1);
     mbar_init(u32(&sm.bar_b), 1);
+    mbar_init(u32(&sm.bar_w), 1);
     mbar_init(u32(&sm.bar_mma), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
@@ -182,12 +183,23 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     tma_load_3d(u32(sm.dob), &tmdo, 0, hh, t0, bar);
     tma_load_3d(u32(sm.dob + HT), &tmdo, 64, hh, t0, bar);
   };
+  // precomputed WY tiles (X1, X2, Ahat) of an item: their buffers are free once its dk is stored
+  const bool use_wy = a.wy != nullptr;
+  auto issue_wy = [&](int item) {
+    const uint32_t bar = u32(&sm.bar_w);
+    const int row = item * 3 * CH;  // item = chunk * H + head, three 64-row tiles each
+    mbar_expect_tx(bar, 3 * HT);
+    tma_load_3d(u32(sm.x1), &tmw, 0, row, 0, bar);
+    tma_load_3d(u32(sm.x2), &tmw, 0, row + CH, 0, bar);
+    tma_load_3d(u32(sm.ah), &tmw, 0, row + 2 * CH, 0, bar);
+  };
   int item = next_valid(blockIdx.x);
   if (tid == 0 && item < n_items) {
     issue_main(item);
     issue_do(item);
+    if (use_wy) issue_wy(item);
   }
-  bool pend_main = item < n_items, pend_do = pend_main, failed = false;
+  bool pend_main = item < n_items, pend_do = pend_main, pend_wy = pend_main && use_wy, failed = false;
   uint32_t it = 0;  // parity of the TMA barriers: one completion per item
   for (; item < n_items; ++it) {
   const int nitem = next_valid(item + gridDim.x);
@@ -290,15 +302,24 @@ __global__ void __launch_bounds__(LTHREADS, 1)
   }
   fence_before();
   __syncthreads();
-  wy_inverse<false, false>(sm.nf, LN, sm.beta, sm.ys, [&](int r, int c, float a0, float a1) {
-    const float b0 = sm.beta[c], b1 = sm.beta[c + 1], gr = sm.gt.gp[r];
-    const uint32_t off = sw128_offset(r, c);
-    *reinterpret_cast<__half2 *>(sm.x1 + off) = __floats2half2_rn(a0 * b0, a1 * b1);
-    *reinterpret_cast<__half2 *>(sm.x2 + off) =
-        __floats2half2_rn(c <= r ? a0 * b0 * (gr * sm.gt.rgp[c]) : 0.f,
-                          c + 1 <= r ? a1 * b1 * (gr * sm.gt.rgp[c + 1]) : 0.f);
-    *reinterpret_cast<__half2 *>(sm.ah + off) = __floats2half2_rn(a0, a1);
-  });
+  if (!use_wy) {
+    wy_inverse<false, false>(sm.nf, LN, sm.beta, sm.ys, [&](int r, int c, float a0, float a1) {
+      const float b0 = sm.beta[c], b1 = sm.beta[c + 1], gr = sm.gt.gp[r];
+      const uint32_t off = sw128_offset(r, c);
+      *reinterpret_cast<__half2 *>(sm.x1 + off) = __floats2half2_rn(a0 * b0, a1 * b1);
+      *reinterpret_cast<__half2 *>(sm.x2 + off) =
+          __floats2half2_rn(c <= r ? a0 * b0 * (gr * sm.gt.rgp[c]) : 0.f,
+                            c + 1 <= r ? a1 * b1 * (gr * sm.gt.rgp[c + 1]) : 0.f);
+      *reinterpret_cast<__half2 *>(sm.ah + off) = __floats2half2_rn(a0, a1);
+    });
+  } else {
+    const bool ok = mbar_wait(u32(&sm.bar_w), it & 1, err, 8);
+    pend_wy = false;
+    if (__syncthreads_or(!ok)) {
+      failed = true;
+      break;
+    }
+  }
 
   // ---- P2: W^T = K^T X1^T -> T1;  U^T = V^T X2^T -> T2
   if (tid == 0) {
@@ -882,11 +903,16 @@ float rg[8];
     }
   }
   __syncthreads();  // the next item rewrites the per-token scratch read above
+  if (use_wy && nitem < n_items) {  // X1, X2, Ahat of the next item (x2/ah held the dk staging until now)
+    if (tid == 0) issue_wy(nitem);
+    pend_wy = true;
+  }
   item = nitem;
   }
   if (failed) {  // let prefetches already in flight land before the CTA leaves (bounded waits)
     if (pend_main) mbar_wait(u32(&sm.bar_a), (it + 1) & 1, err, 8);
     if (pend_do) mbar_wait(u32(&sm.bar_b), (it + 1) & 1, err, 8);
+    if (pend_wy) mbar_wait(u32(&sm.bar_w), it & 1, err, 8);  // issued for the item of iteration it
   }
   fence_before();
   __syncthreads();
@@ -911,7 +937,7 @@ int launch_bwd_local_tc(const BwdArgs &a, const CUtensorMap *maps, int CH_max, c
   const int n_items = CH_max * a.H;
   const int grid = n_items < sms ? n_items : sms;  // persistent: one CTA per SM
   bwd_local_tc_kernel<<<grid, LTHREADS, smem, st>>>(a, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
-                                                    n_items);
+                                                    maps[6], n_items);
   return (int)cudaGetLastError();
 }
 

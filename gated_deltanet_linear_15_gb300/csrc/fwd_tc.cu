@@ -75,7 +75,7 @@ __device__ __forceinline__ uint32_t chunk_off(int r, int cb) { return r * 128 + 
 
 __global__ void __launch_bounds__(FT, 1)
     fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                  const __grid_constant__ CUtensorMap tmv) {
+                  const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmw) {
   extern __shared__ unsigned char smraw[];
   TcSmem &sm = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
 
@@ -106,6 +106,9 @@ __global__ void __launch_bounds__(FT, 1)
   const bool outputs = (a.pass == 1);
   const bool states = (a.pass == 2);
   const bool need_v = !transition;
+  // backward passes: the WY tiles X1, X2 were computed once per chunk; they arrive by TMA in the
+  // ring's Q slots (q is not needed without outputs) and replace the Gram product and the inverse
+  const bool use_wy = a.wy != nullptr && !outputs;
   const bool l2 = (a.flags & kFlagL2Norm) != 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wg = warp >> 2;                      // column group 0..3 within a lane quarter
@@ -124,6 +127,7 @@ __global__ void __launch_bounds__(FT, 1)
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
     tma_prefetch_desc(&tmq);
+    if (use_wy) tma_prefetch_desc(&tmw);
   }
   if (warp == 0) {
     tmem_alloc(u32(&sm.tmem_base), TM_COLS);
@@ -138,7 +142,7 @@ __global__ void __launch_bounds__(FT, 1)
   auto issue_tma = [&](int c, int stage) {
     const int tok0 = bos + c * CH;
     const bool wq = outputs && c >= cbeg;
-    const uint32_t bytes = (2 + (wq ? 2 : 0) + (need_v ? 2 : 0)) * HT;
+    const uint32_t bytes = (2 + (wq || use_wy ? 2 : 0) + (need_v ? 2 : 0)) * HT;
     const uint32_t bar = u32(&sm.bar_tma[stage]);
     uint8_t *st = sm.ring[stage];
     mbar_expect_tx(bar, bytes);
@@ -147,6 +151,10 @@ __global__ void __launch_bounds__(FT, 1)
     if (wq) {
       tma_load_3d(u32(st + 1 * HT), &tmq, 0, h, tok0, bar);
       tma_load_3d(u32(st + 3 * HT), &tmq, 64, h, tok0, bar);
+    } else if (use_wy) {
+      const int wrow = ((chunk0 + c) * H + h) * 3 * CH;
+      tma_load_3d(u32(st + 1 * HT), &tmw, 0, wrow, 0, bar);       // X1
+      tma_load_3d(u32(st + 3 * HT), &tmw, 0, wrow + CH, 0, bar);  // X2
     }
     if (need_v) {
       tma_load_3d(u32(st + 4 * HT), &tmv, 0, h, tok0, bar);
@@ -294,62 +302,65 @@ __global__ void __launch_bounds__(FT, 1)
     }
     __syncthreads();
 
-    // ---- MMA 1: [K; Q] K^T  (M = 128, N = 64, K = 128)
-    if (tid == 0) {
-      fence_after();
-      const uint32_t idesc = idesc_f16(128, 64, false, false);
-      const uint32_t base = u32(st);
+    if (!use_wy) {
+      // ---- MMA 1: [K; Q] K^T  (M = 128, N = 64, K = 128)
+      if (tid == 0) {
+        fence_after();
+        const uint32_t idesc = idesc_f16(128, 64, false, false);
+        const uint32_t base = u32(st);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t koff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
-        mma_f16(tm + TM_KQ, sdesc(base + koff, 16, 1024), sdesc(base + koff, 16, 1024), idesc, kk > 0);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t koff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
+          mma_f16(tm + TM_KQ, sdesc(base + koff, 16, 1024), sdesc(base + koff, 16, 1024), idesc, kk > 0);
+        }
+        mma_commit(u32(&sm.bar_mma));
       }
-      mma_commit(u32(&sm.bar_mma));
-    }
-    __syncwarp();
-    if (__syncthreads_or(!mma_wait())) {
-      failed = true;
-      break;
-    }
-
-    // ---- read-out: N (fp32, rows 0-63) and P (fp16, rows 64-127); each warp takes 16 columns
-    if (row < 64 || emit) {
-      const int c0 = wg * 16;
-      float v[16];
-      tmem_ld16(tm + tm_lane + TM_KQ + c0, v);
-      if (row < 64) {
-        float4 *dst = reinterpret_cast<float4 *>(&sm.nf[row * LN + c0]);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-      } else {
-        const int r = row - 64;
-        const float gr = G.gp[r];
-        float rg[16];
-        ld16f(G.rgp + c0, rg);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = c0 + i <= r ? v[i] * gr * rg[i] : 0.f;
-        st_chunk_f16(sm.p + chunk_off(r, c0), v);
-        st_chunk_f16(sm.p + chunk_off(r, c0 + 8), v + 8);
+      __syncwarp();
+      if (__syncthreads_or(!mma_wait())) {
+        failed = true;
+        break;
       }
-    }
-    fence_before();
-    __syncthreads();
 
-    // ---- Ahat (fp32 diagonal blocks, TF32 tensor-core merges) -> X1, X2 (fp16, K-major: rows = r)
-    wy_inverse<false, false>(sm.nf, LN, gbeta, sm.ys, [&](int r, int c, float a0, float a1) {
-      const float2 bb = *reinterpret_cast<const float2 *>(gbeta + c), rg = *reinterpret_cast<const float2 *>(G.rgp + c);
-      const float gr = G.gp[r], x0 = a0 * bb.x, x1 = a1 * bb.y;
-      const uint32_t off = sw128_offset(r, c);
-      *reinterpret_cast<__half2 *>(sm.x1 + off) = __floats2half2_rn(x0, x1);
-      *reinterpret_cast<__half2 *>(sm.x2 + off) =
-          __floats2half2_rn(c <= r ? x0 * (gr * rg.x) : 0.f, c + 1 <= r ? x1 * (gr * rg.y) : 0.f);
-    }, it == 0);
+      // ---- read-out: N (fp32, rows 0-63) and P (fp16, rows 64-127); each warp takes 16 columns
+      if (row < 64 || emit) {
+        const int c0 = wg * 16;
+        float v[16];
+        tmem_ld16(tm + tm_lane + TM_KQ + c0, v);
+        if (row < 64) {
+          float4 *dst = reinterpret_cast<float4 *>(&sm.nf[row * LN + c0]);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else {
+          const int r = row - 64;
+          const float gr = G.gp[r];
+          float rg[16];
+          ld16f(G.rgp + c0, rg);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = c0 + i <= r ? v[i] * gr * rg[i] : 0.f;
+          st_chunk_f16(sm.p + chunk_off(r, c0), v);
+          st_chunk_f16(sm.p + chunk_off(r, c0 + 8), v + 8);
+        }
+      }
+      fence_before();
+      __syncthreads();
+
+      // ---- Ahat (fp32 diagonal blocks, TF32 tensor-core merges) -> X1, X2 (fp16, K-major: rows = r)
+      wy_inverse<false, false>(sm.nf, LN, gbeta, sm.ys, [&](int r, int c, float a0, float a1) {
+        const float2 bb = *reinterpret_cast<const float2 *>(gbeta + c), rg = *reinterpret_cast<const float2 *>(G.rgp + c);
+        const float gr = G.gp[r], x0 = a0 * bb.x, x1 = a1 * bb.y;
+        const uint32_t off = sw128_offset(r, c);
+        *reinterpret_cast<__half2 *>(sm.x1 + off) = __floats2half2_rn(x0, x1);
+        *reinterpret_cast<__half2 *>(sm.x2 + off) =
+            __floats2half2_rn(c <= r ? x0 * (gr * rg.x) : 0.f, c + 1 <= r ? x1 * (gr * rg.y) : 0.f);
+      }, it == 0);
+    }
 
     // ---- MMA 2: W^T = K^T X1^T, U^T = V^T X2^T  (M = 128, N = 64, K = 64)
     if (tid == 0) {
       fence_after();
       const uint32_t idesc = idesc_f16(128, 64, true, false);
-      const uint32_t kb = u32(st), vb = u32(st + 4 * HT), x1b = u32(sm.x1), x2b = u32(sm.x2);
+      const uint32_t kb = u32(st), vb = u32(st + 4 * HT);
+      const uint32_t x1b = use_wy ? u32(st + HT) : u32(sm.x1), x2b = use_wy ? u32(st + 3 * HT) : u32(sm.x2);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         mma_f16(tm + TM_W, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(x1b + kk * 32, 16, 1024), idesc, kk > 0);
@@ -540,13 +551,13 @@ __global__ void __launch_bounds__(FT, 1)
 
 size_t fwd_tc_smem_bytes() { return sizeof(TcSmem) + 1024; }
 
-int launch_fwd_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, dim3 grid,
-                  cudaStream_t st) {
+int launch_fwd_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                  const CUtensorMap &tw, dim3 grid, cudaStream_t st) {
   const size_t smem = fwd_tc_smem_bytes();
   static_assert(sizeof(TcSmem) + 1024 <= 232448, "shared memory budget");
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  fwd_tc_kernel<<<grid, FT, smem, st>>>(a, tq, tk, tv);
+  fwd_tc_kernel<<<grid, FT, smem, st>>>(a, tq, tk, tv, tw);
   return (int)cudaGetLastError();
 }
 

@@ -26,6 +26,7 @@ struct FwdArgs {
   float scale;
   unsigned flags;
   int pass;  // 0: segment end states / transitions, 1: outputs, 2: per-chunk states
+  const void *wy;  // precomputed WY tiles (backward only) or NULL: X1/X2 come by TMA, no inverse
 };
 
 struct BwdArgs {
@@ -43,6 +44,7 @@ struct BwdArgs {
   float scale;
   unsigned flags;
   int pass;  // reverse chain: 0 segment starts / transitions, 1 per-chunk dS
+  const void *wy;  // precomputed WY tiles or NULL
 };
 
 struct FixupArgs {
@@ -53,6 +55,17 @@ struct FixupArgs {
   int H, D, Lseg;
   unsigned flags;
   int reverse;
+};
+
+// WY tiles of every (chunk, head): fp16 [CH_max, H, 3, 64, 64] = X1, X2, Ahat (row-major)
+struct WyArgs {
+  const void *k;
+  const float *g, *beta;
+  Plan plan;
+  void *wy;
+  int *status;
+  int H;
+  unsigned flags;
 };
 
 struct RecArgs {
@@ -71,15 +84,17 @@ int launch_plan(const Plan &p, const int *cu, int N, int T, int Lseg, int S_max,
 int launch_gate_scan(const Plan &p, const float *g, int H, int CH_max, float *gsum, int *status, cudaStream_t st);
 int launch_fixup(const FixupArgs &a, int N, cudaStream_t st);
 int launch_fwd_chunk(const FwdArgs &a, bool is_bf16, int D, dim3 grid, cudaStream_t st);
-// tcgen05 forward for bf16 inputs and d = 128; q, k, v tensor maps over [tokens, H, 128] with a 64 x 1 x 64 box
-int launch_fwd_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, dim3 grid,
-                  cudaStream_t st);
+// tcgen05 forward for bf16 inputs and d = 128; q, k, v tensor maps over [tokens, H, 128] with a 64 x 1 x 64 box;
+// tw: the WY tiles as [rows, 64] fp16 with a 64 x 64 box (used when a.wy != NULL)
+int launch_fwd_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                  const CUtensorMap &tw, dim3 grid, cudaStream_t st);
+int launch_wy(const WyArgs &a, int CH_max, cudaStream_t st);
 int launch_bwd_chain(const BwdArgs &a, bool is_bf16, int D, dim3 grid, cudaStream_t st);
-// tcgen05 reverse chain (bf16, d = 128); maps: q, k, dO ([tokens, H, 128] bf16, box 64x1x64)
+// tcgen05 reverse chain (bf16, d = 128); maps: q, k, dO ([tokens, H, 128] bf16, box 64x1x64) and the WY tiles
 int launch_bwd_chain_tc(const BwdArgs &a, const CUtensorMap *maps, dim3 grid, cudaStream_t st);
 int launch_bwd_local(const BwdArgs &a, bool is_bf16, int D, int CH_max, cudaStream_t st);
 // tcgen05 local-gradient kernel (bf16, d = 128); maps: q, k, v, dO ([tokens, H, 128] bf16, box 64x1x64) and
-// the fp16 per-chunk states S0 and dS ([rows, 128] as a 3-D map, box 64x128x1)
+// the fp16 per-chunk states S0 and dS ([rows, 128] as a 3-D map, box 64x128x1), and the WY tiles
 int launch_bwd_local_tc(const BwdArgs &a, const CUtensorMap *maps, int CH_max, cudaStream_t st);
 // token-by-token forward over NH = N * H (sequence, head) pairs
 int launch_recurrent(const RecArgs &a, bool is_bf16, int D, int NH, cudaStream_t st);
