@@ -83,6 +83,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else if (role != 0) {
     return;
   }
+  if (a.flags & kFlagDebugWaitTimeout) {  // test hook: an expiring bounded wait, then return
+    __shared__ uint64_t dbg_bar;
+    if (threadIdx.x == 0) debug_expire_wait(&dbg_bar, a.status, 4);
+    return;
+  }
   const bool store = (a.pass == 1);
   const bool l2 = (a.flags & kFlagL2Norm) != 0;
   const bool with_do = !transition;

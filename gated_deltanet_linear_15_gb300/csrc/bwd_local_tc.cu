@@ -118,6 +118,11 @@ __global__ void __launch_bounds__(LTHREADS, 1)
   extern __shared__ unsigned char smraw[];
   LocalTcSmem &sm =
       *reinterpret_cast<LocalTcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+  if (a.flags & kFlagDebugWaitTimeout) {  // test hook: an expiring bounded wait, then return
+    __shared__ uint64_t dbg_bar;
+    if (threadIdx.x == 0) debug_expire_wait(&dbg_bar, a.status, 4);
+    return;
+  }
   const int H = a.H;
   const bool l2 = (a.flags & kFlagL2Norm) != 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;

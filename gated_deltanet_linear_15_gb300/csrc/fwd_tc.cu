@@ -103,6 +103,11 @@ __global__ void __launch_bounds__(FT, 1)
   } else if (role != 0) {
     return;
   }
+  if (a.flags & kFlagDebugWaitTimeout) {  // test hook: an expiring bounded wait, then return
+    __shared__ uint64_t dbg_bar;
+    if (threadIdx.x == 0) debug_expire_wait(&dbg_bar, a.status, 4);
+    return;
+  }
   const bool outputs = (a.pass == 1);
   const bool states = (a.pass == 2);
   const bool need_v = !transition;

@@ -11,6 +11,7 @@ namespace gdn {
 constexpr unsigned kFlagL2Norm = 1u;
 constexpr unsigned kFlagSpOff = 2u;
 constexpr unsigned kFlagWindowOff = 4u;
+constexpr unsigned kFlagDebugWaitTimeout = 0x80000000u;  // test hook, see gdn.h
 
 struct FwdArgs {
   const void *q, *k, *v;

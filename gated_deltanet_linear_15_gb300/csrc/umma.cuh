@@ -186,6 +186,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, int *e
   return false;
 }
 
+// Test hook for the bounded waits: wait on a fresh barrier that nothing arrives at, with a short
+// bound, so the wait expires and records `code` in *err.  Called by thread 0 before the kernel has
+// allocated TMEM or issued any copy or product; the caller then returns.
+__device__ __forceinline__ void debug_expire_wait(uint64_t *bar, int *err, int code) {
+  mbar_init(smem_u32(bar), 1);
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  mbar_wait(smem_u32(bar), 0, err, code, 1024);
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_load_3d(uint32_t smem_dst, const CUtensorMap *map, int x, int y, int z,
                                             uint32_t mbar) {

@@ -56,7 +56,12 @@ enum {
 enum {
   GDN_L2NORM_QK = 1u,  /* normalise q and k per token in-kernel: x / sqrt(|x|^2 + 1e-6)   */
   GDN_SP_OFF = 2u,     /* no intra-card sequence parallelism: one segment per sequence    */
-  GDN_WINDOW_OFF = 4u  /* never skip the segment-start correction (always exact path)     */
+  GDN_WINDOW_OFF = 4u, /* never skip the segment-start correction (always exact path)     */
+  /* Test hook for the bounded device waits (bf16, d = 128 chunk kernels): each tensor-core
+   * kernel of the call first waits on a barrier that nothing arrives at, with a short bound;
+   * the wait expires, sets status value 4 (see gdn_get_device_status) and the kernel returns
+   * before any copy or product.  Outputs of such a call are not written. */
+  GDN_DEBUG_WAIT_TIMEOUT = 0x80000000u
 };
 
 /* Problem description shared by the forward, the backward and the size queries. */
