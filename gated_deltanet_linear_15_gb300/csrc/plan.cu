@@ -182,7 +182,7 @@ int launch_gate_scan(const Plan &p, const float *g, int H, int CH_max, float *gs
 constexpr int FIX_ROWS = 8;
 
 template <int D>
-__global__ void __launch_bounds__(256) fixup_kernel(FixupArgs a) {
+__global__ void __launch_bounds__(256, 4) fixup_kernel(FixupArgs a) {
   __shared__ float cur[FIX_ROWS][D];
   const int rb = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
   const int H = a.H;
@@ -218,10 +218,24 @@ __global__ void __launch_bounds__(256) fixup_kernel(FixupArgs a) {
     if (ms == START_FIXUP) {
       // cur holds the corrected state of segment js (computed in the previous step)
       const float *M = a.M + src;
+      // 8 rows of M in flight per step of the loop (the loads are independent; only the sums chain)
+#pragma unroll 8
       for (int k = 0; k < D; ++k) {
         const float x = cur[r][k];
+        float m[CPT];
+        if constexpr (CPT == 4) {
+          const float4 t4 = *reinterpret_cast<const float4 *>(M + (size_t)k * D + c0);
+          m[0] = t4.x;
+          m[1] = t4.y;
+          m[2] = t4.z;
+          m[3] = t4.w;
+        } else {
+          const float2 t2 = *reinterpret_cast<const float2 *>(M + (size_t)k * D + c0);
+          m[0] = t2.x;
+          m[1] = t2.y;
+        }
 #pragma unroll
-        for (int t = 0; t < CPT; ++t) acc[t] = fmaf(x, M[(size_t)k * D + c0 + t], acc[t]);
+        for (int t = 0; t < CPT; ++t) acc[t] = fmaf(x, m[t], acc[t]);
       }
     }
     __syncthreads();
