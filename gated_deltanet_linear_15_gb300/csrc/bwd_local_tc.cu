@@ -9,20 +9,20 @@
 // matrix multiplied with K once (onedev.kr FlashQLA talk summary, paragraph on
 // SFU load, last sentence).
 //
-// Rounds (MMA group -> read-out), TMEM regions T0..T7 of 64 columns:
-//   P1 [K;Q]K^T->T0          R1: N (fp32), P;  inverse; X1, X2, Ahat (fp16)
-//   P2 W^T->T1, U^T->T2      R2: W^T (gam-scaled columns)
-//   P3 Ut^T = U^T - S0 W^T   R3: Ut^T
-//   P4 Y = dS K^T->T3, Z = dO^T P->T4, Qa = S0^T dO^T->T5
-//                            R4: dUt^T = cdec*Y + Z; sums <Ut,Y>, <dUt,Ut>
-//   P5 dP = dO Ut^T->T0, dW'^T = -S0^T dUt^T->T1, dV^T = dUt^T X2->T6
+// Rounds (MMA group -> read-out), TMEM regions T0..T7 of 64 columns (X1, X2, Ahat arrive
+// precomputed by TMA; the inline inverse is kept for calls without them):
+//   P1 [K;Q]K^T->T0          R1: N (fp32), P
+//   P2 W^T->T1, U^T->T2, and (inputs only) Y = dS K^T->T3, Z = dO^T P->T4, Qa = S0^T dO^T->T5
+//                            R2: W^T (gam-scaled columns)
+//   P3 Ut^T = U^T - S0 W^T   R3/R4: Ut^T; dUt^T = cdec*Y + Z; sums <Ut,Y>, <dUt,Ut>
+//   P5 dP = dO Ut^T->T0, dW'^T = -S0^T dUt^T->T1, dV^T = dUt^T X2->T6, Kb = dS^T Ut^T->T2
 //                            R5: dPm (over P), dP*P sums; dW'^T tile; dv out, <dV,v>
 //   P6 Qb = K^T dPm^T->T7, M1 = dW' K^T->T3, M2 = dUt V^T->T4
 //                            R6: dq out (+ <dQ1,q>); dAhat tile, beta column sums
 //   P7 Y1 = Ahat^T dAhat->T0 R7: Y1 tile
 //   P8 dT = -Y1 Ahat^T->T1   R8: dN tile (strictly lower), beta row sums
-//   P9 Ka = Q^T dPm + dW'^T X1 + K^T (dN + dN^T)->T3, Kb = dS^T Ut^T->T4
-//                            R9: dk out;  dg (reverse cumsum), dbeta
+//   P9 Ka = Q^T dPm + dW'^T X1 + K^T (dN + dN^T)->T3
+//                            R9: dk out (Ka + cdec Kb);  dg (reverse cumsum), dbeta
 #include "chunk_common.cuh"
 #include "kernels.h"
 #include "umma.cuh"
@@ -305,6 +305,7 @@ __global__ void __launch_bounds__(LTHREADS, 1)
       st_chunk_f16(sm.p + chunk_off(r, cb), y);
     }
   }
+  fence_async_smem();  // P is an operand of the next round
   fence_before();
   __syncthreads();
   if (!use_wy) {
@@ -326,7 +327,8 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     }
   }
 
-  // ---- P2: W^T = K^T X1^T -> T1;  U^T = V^T X2^T -> T2
+  // ---- P2: W^T = K^T X1^T -> T1;  U^T = V^T X2^T -> T2;  and (needing only inputs and P)
+  //      P4: Y = dS K^T -> T3; Z = dO^T P -> T4; Qa = S0^T dO^T -> T5
   if (tid == 0) {
     fence_after();
     const uint32_t id = idesc_f16(128, 64, true, false);
@@ -336,6 +338,20 @@ __global__ void __launch_bounds__(LTHREADS, 1)
       mma_f16(tm + T1, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(x1b + kk * 32, 16, 1024), id, kk > 0);
       mma_f16(tm + T2, sdesc(vb + kk * 2048, HT, 1024), sdesc(x2b + kk * 32, 16, 1024), id, kk > 0);
     }
+    const uint32_t id_kk = idesc_f16(128, 64, false, false);
+    const uint32_t id_mm = idesc_f16(128, 64, true, true);
+    const uint32_t id_mk = idesc_f16(128, 64, true, false);
+    const uint32_t dsb = u32(sm.ds), dob = u32(sm.dob), pb = u32(sm.p), sb = u32(sm.s0);
+#pragma unroll 1
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
+      mma_f16(tm + T3, sdesc(dsb + aoff, 16, 1024), sdesc(kb + aoff, 16, 1024), id_kk, kk > 0);
+      mma_f16(tm + T5, sdesc(sb + kk * 2048, 2 * HT, 1024), sdesc(dob + (kk >> 2) * HT + (kk & 3) * 32, 16, 1024),
+              id_mk, kk > 0);
+    }
+#pragma unroll 1
+    for (int kk = 0; kk < 4; ++kk)
+      mma_f16(tm + T4, sdesc(dob + kk * 2048, HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id_mm, kk > 0);
     mma_commit(u32(&sm.bar_mma));
   }
   __syncwarp();
@@ -392,43 +408,7 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     failed = true;
     break;
   }
-  // R3: Ut^T -> ut
-#pragma unroll 1
-  for (int q4 = 0; q4 < 2; ++q4) {
-    const int cb = c0 + q4 * 8;
-    float v[8];
-    tmem_ld8(tm + tl + T2 + cb, v);
-    st_chunk_f16(sm.ut + chunk_off(row, cb), v);
-  }
-  fence_before();
-  fence_async_smem();
-  __syncthreads();
-
-  // ---- P4: Y = dS K^T -> T3; Z = dO^T P -> T4; Qa = S0^T dO^T -> T5
-  if (tid == 0) {
-    fence_after();
-    const uint32_t id_kk = idesc_f16(128, 64, false, false);
-    const uint32_t id_mm = idesc_f16(128, 64, true, true);
-    const uint32_t id_mk = idesc_f16(128, 64, true, false);
-    const uint32_t dsb = u32(sm.ds), kb = u32(sm.kq), dob = u32(sm.dob), pb = u32(sm.p), sb = u32(sm.s0);
-#pragma unroll 1
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
-      mma_f16(tm + T3, sdesc(dsb + aoff, 16, 1024), sdesc(kb + aoff, 16, 1024), id_kk, kk > 0);
-      mma_f16(tm + T5, sdesc(sb + kk * 2048, 2 * HT, 1024), sdesc(dob + (kk >> 2) * HT + (kk & 3) * 32, 16, 1024),
-              id_mk, kk > 0);
-    }
-#pragma unroll 1
-    for (int kk = 0; kk < 4; ++kk)
-      mma_f16(tm + T4, sdesc(dob + kk * 2048, HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id_mm, kk > 0);
-    mma_commit(u32(&sm.bar_mma));
-  }
-  __syncwarp();
-  if (__syncthreads_or(!mma_done())) {
-    failed = true;
-    break;
-  }
-  {  // R4: dUt^T = cdec*Y + Z -> wt (W^T is dead);  per-token sums <Ut, Y>, <dUt, Ut> over d_v
+  {  // R3+R4: Ut^T -> ut;  dUt^T = cdec*Y + Z -> wt (W^T is dead);  per-token sums <Ut, Y>, <dUt, Ut> over d_v
     float t1 = 0.f, t2 = 0.f;
 #pragma unroll 1
     for (int q4 = 0; q4 < 2; ++q4) {
@@ -437,6 +417,7 @@ __global__ void __launch_bounds__(LTHREADS, 1)
       tmem_ld8(tm + tl + T3 + cb, y);
       tmem_ld8(tm + tl + T4 + cb, z);
       tmem_ld8(tm + tl + T2 + cb, u);
+      st_chunk_f16(sm.ut + chunk_off(row, cb), u);
       float cd[8];
       ld8f(sm.gt.cdec + cb, cd);
 #pragma unroll
@@ -464,7 +445,7 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     sm.acc[1][tid] = sm.part[4][tid] + sm.part[5][tid] + sm.part[6][tid] + sm.part[7][tid];  // <dUt, Ut>
   }
 
-  // ---- P5: dP = dO Ut^T -> T0; dW'^T = -S0^T dUt^T -> T1; dV^T = dUt^T X2 -> T6
+  // ---- P5: dP = dO Ut^T -> T0; dW'^T = -S0^T dUt^T -> T1; dV^T = dUt^T X2 -> T6;  Kb = dS^T Ut^T -> T2
   if (tid == 0) {
     fence_after();
     const uint32_t id_kmn = idesc_f16(128, 64, false, true);
@@ -480,6 +461,10 @@ __global__ void __launch_bounds__(LTHREADS, 1)
 #pragma unroll 1
     for (int kk = 0; kk < 4; ++kk)
       mma_f16(tm + T6, sdesc(dub + kk * 32, 16, 1024), sdesc(x2b + kk * 2048, HT, 1024), id_kmn, kk > 0);
+    const uint32_t id_mm = idesc_f16(128, 64, true, true), dsb = u32(sm.ds);
+#pragma unroll 1
+    for (int kk = 0; kk < 8; ++kk)
+      mma_f16(tm + T2, sdesc(dsb + kk * 2048, 2 * HT, 1024), sdesc(ub + kk * 2048, 2 * HT, 1024), id_mm, kk > 0);
     mma_commit(u32(&sm.bar_mma));
   }
   __syncwarp();
@@ -780,14 +765,13 @@ float rg[8];
   fence_async_smem();
   __syncthreads();
 
-  // ---- P9: Ka = Q^T dPm + dW'^T X1 + K^T Sigma -> T3;  Kb = dS^T Ut^T -> T4
+  // ---- P9: Ka = Q^T dPm + dW'^T X1 + K^T Sigma -> T3  (Kb = dS^T Ut^T came with P5, in T2)
   if (tid == 0) {
     fence_after();
     const uint32_t id_mm = idesc_f16(128, 64, true, true);
     const uint32_t id_km = idesc_f16(128, 64, false, true);
     const uint32_t id_mk = idesc_f16(128, 64, true, false);
     const uint32_t kb = u32(sm.kq), pb = u32(sm.p), dwb = u32(sm.s0), x1b = u32(sm.x1), sgb = u32(sm.v + HT);
-    const uint32_t dsb = u32(sm.ds), ub = u32(sm.ut);
 #pragma unroll 1
     for (int kk = 0; kk < 4; ++kk) {
       mma_f16(tm + T3, sdesc(kb + HT + kk * 2048, 2 * HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id_mm, kk > 0);
@@ -796,9 +780,6 @@ float rg[8];
       mma_f16(tm + T3, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(sgb + kk * 2048, HT, 1024), id_mm, true);
       mma_f16(tm + T3, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(sgb + kk * 32, 16, 1024), id_mk, true);
     }
-#pragma unroll 1
-    for (int kk = 0; kk < 8; ++kk)
-      mma_f16(tm + T4, sdesc(dsb + kk * 2048, 2 * HT, 1024), sdesc(ub + kk * 2048, 2 * HT, 1024), id_mm, kk > 0);
     mma_commit(u32(&sm.bar_mma));
   }
   __syncwarp();
@@ -820,7 +801,7 @@ float rg[8];
         const int cb = c0 + q4 * 8;
         float ka[8], kbv[8];
         tmem_ld8(tm + tl + T3 + cb, ka);
-        tmem_ld8(tm + tl + T4 + cb, kbv);
+        tmem_ld8(tm + tl + T2 + cb, kbv);
         float cd[8];
         ld8f(sm.gt.cdec + cb, cd);
 #pragma unroll
@@ -840,7 +821,7 @@ float rg[8];
       const int cb = c0 + q4 * 8;
       float ka[8], kbv[8];
       tmem_ld8(tm + tl + T3 + cb, ka);
-      tmem_ld8(tm + tl + T4 + cb, kbv);
+      tmem_ld8(tm + tl + T2 + cb, kbv);
       float cd[8], dt[8], nkv[8];
       ld8f(sm.gt.cdec + cb, cd);
       if (l2) {
