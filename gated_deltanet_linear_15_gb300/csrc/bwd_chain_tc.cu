@@ -366,11 +366,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_st32(tm + tl + TM_S + c0, v);
       }
     }
+    fence_before();  // the rescaled dS in TMEM is accumulated into right below
     if (__syncthreads_or(!mma_wait())) {
       failed = true;
       break;
     }
     if (use_wy && tid == 0 && c - 1 >= cbeg) issue_x1(c - 1);  // MMA 2 has consumed sm.x1
+    // dS += dO^T Qg needs only inputs: issued now, it runs under the W^T read-out (MMA 3's commit
+    // covers it); MMA 4 then adds -dUt^T W
+    if (with_do && tid == 0) {
+      const uint32_t id_mm = idesc_f16(128, 128, true, true);
+      const uint32_t dob = u32(st + 4 * HT), qgb = u32(sm.qg);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_f16(tm + TM_S, sdesc(dob + kk * 2048, HT, 1024), sdesc(qgb + kk * 2048, HT, 1024), id_mm, true);
+    }
     {  // W^T read-out, columns scaled by gam
       const int c0 = wg * 32;
       float v[32];
@@ -426,17 +436,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     fence_async_smem();
     __syncthreads();
 
-    // ---- MMA 4: dS += dO^T Qg - dUt^T W   (M = 128, N = 128)
+    // ---- MMA 4: dS -= dUt^T W   (M = 128, N = 128; dO^T Qg was added after MMA 2)
     if (tid == 0) {
       fence_after();
-      const uint32_t id_mm = idesc_f16(128, 128, true, true);
       const uint32_t id_kk_neg = idesc_f16(128, 128, false, false, true);
-      const uint32_t dob = u32(st + 4 * HT), qgb = u32(sm.qg), dub = u32(sm.kc), wb = u32(sm.wt);
-      if (with_do) {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_f16(tm + TM_S, sdesc(dob + kk * 2048, HT, 1024), sdesc(qgb + kk * 2048, HT, 1024), id_mm, true);
-      }
+      const uint32_t dub = u32(sm.kc), wb = u32(sm.wt);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
         mma_f16(tm + TM_S, sdesc(dub + kk * 32, 16, 1024), sdesc(wb + kk * 32, 16, 1024), id_kk_neg, true);

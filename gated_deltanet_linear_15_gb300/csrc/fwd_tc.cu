@@ -400,9 +400,21 @@ __global__ void __launch_bounds__(FT, 1)
         tmem_st32(tm + tm_lane + TM_S + c0, v);
       }
     }
+    fence_async_smem();  // the fp16 state copy is read by the tensor core next
     if (__syncthreads_or(!mma_wait())) {
       failed = true;
       break;
+    }
+    // Oi^T = S0 Q^T needs only the state copy and Q: issued now, it runs under the W^T read-out
+    // (MMA 3's commit covers it)
+    if (emit && tid == 0) {
+      const uint32_t s0b = u32(sm.s0), qb = u32(st + HT);
+      const uint32_t id_o = idesc_f16(128, 64, false, false);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
+        mma_f16(tm + TM_O, sdesc(s0b + aoff, 16, 1024), sdesc(qb + aoff, 16, 1024), id_o, kk > 0);
+      }
     }
 
     // ---- W^T read-out: columns scaled by gam -> fp16 MN-major B (rows = d_k)
@@ -421,24 +433,16 @@ __global__ void __launch_bounds__(FT, 1)
     fence_async_smem();
     __syncthreads();
 
-    // ---- MMA 3: Ut^T = U^T - S0 W^T;  Oi^T = S0 Q^T   (M = 128, N = 64, K = 128)
+    // ---- MMA 3: Ut^T = U^T - S0 W^T   (M = 128, N = 64, K = 128)
     if (tid == 0) {
       fence_after();
-      const uint32_t s0b = u32(sm.s0), wb = u32(sm.wu), qb = u32(st + HT);
+      const uint32_t s0b = u32(sm.s0), wb = u32(sm.wu);
       const uint32_t id_u = idesc_f16(128, 64, false, true, /*neg_a=*/true);
-      const uint32_t id_o = idesc_f16(128, 64, false, false);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
         mma_f16(tm + TM_U, sdesc(s0b + aoff, 16, 1024), sdesc(wb + kk * 2048, 2 * HT, 1024), id_u,
                 need_v || kk > 0);
-      }
-      if (emit) {
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
-          mma_f16(tm + TM_O, sdesc(s0b + aoff, 16, 1024), sdesc(qb + aoff, 16, 1024), id_o, kk > 0);
-        }
       }
       mma_commit(u32(&sm.bar_mma));
     }
