@@ -396,45 +396,72 @@ def main():
     kernel_table = {k: {"launches": c, "total_ms": round(ms, 4), "share": round(ms / max(1e-9, sum(
         m for _, m in kern.values())), 4)} for k, (c, ms) in sorted(kern.items(), key=lambda kv: -kv[1][1])}
 
-    # ---- end-to-end through the public API with host buffers
+    # ---- end-to-end through the public API with host buffers.  Every step copies its inputs from
+    # pinned host memory and its outputs back.  Pipelined (the reported value): copies run on their own
+    # streams into double-buffered device tensors, so step i+1's upload and step i-1's download overlap
+    # step i's compute, as a data loader would; serial: everything on one stream (also reported).
     e2e = None
     if rank == 0:
-        host_in = {k: x[k].cpu().pin_memory() for k in ("q", "k", "v", "g", "beta", "dO")}
-        dev_in = {k: torch.empty_like(x[k]) for k in host_in}
-        host_out = {"o": torch.empty_like(o, device="cpu").pin_memory(),
-                    "dq": torch.empty_like(dq, device="cpu").pin_memory(),
-                    "dk": torch.empty_like(dk, device="cpu").pin_memory(),
-                    "dv": torch.empty_like(dv, device="cpu").pin_memory(),
-                    "dg": torch.empty_like(dg, device="cpu").pin_memory(),
-                    "dbeta": torch.empty_like(db, device="cpu").pin_memory()}
+        in_keys = ("q", "k", "v", "g", "beta", "dO")
+        host_in = {k: x[k].cpu().pin_memory() for k in in_keys}
+        outs = {"o": o, "dq": dq, "dk": dk, "dv": dv, "dg": dg, "dbeta": db}
+        host_out = {k: torch.empty_like(t, device="cpu").pin_memory() for k, t in outs.items()}
+        nbuf = 2
+        dev_in = [{k: torch.empty_like(x[k]) for k in in_keys} for _ in range(nbuf)]
+        dev_out = [{k: torch.empty_like(t) for k, t in outs.items()} for _ in range(nbuf)]
         h2d = sum(t.numel() * t.element_size() for t in host_in.values())
         d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+        s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
 
-        def e2e_step():
-            for k in host_in:
-                dev_in[k].copy_(host_in[k], non_blocking=True)
-            rc = g.gdn_chunk_fwd(shape, dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"],
-                                 x["S0"], o, ST, ws, ws_bytes, stream)
+        def compute(di, do):
+            rc = g.gdn_chunk_fwd(shape, di["q"], di["k"], di["v"], di["g"], di["beta"], x["S0"], do["o"], ST, ws,
+                                 ws_bytes, stream)
             assert rc == 0
-            rc = g.gdn_chunk_bwd(shape, dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"], x["S0"],
-                                 dev_in["dO"], x["dST"], dq, dk, dv, dg, db, dS0, ws, ws_bytes, stream)
+            rc = g.gdn_chunk_bwd(shape, di["q"], di["k"], di["v"], di["g"], di["beta"], x["S0"], di["dO"], x["dST"],
+                                 do["dq"], do["dk"], do["dv"], do["dg"], do["dbeta"], dS0, ws, ws_bytes, stream)
             assert rc == 0
-            for k, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv), ("dg", dg), ("dbeta", db)):
-                host_out[k].copy_(t, non_blocking=True)
 
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
+        def run(n, pipelined):
+            hs = s_h2d if pipelined else stream
+            ds = s_d2h if pipelined else stream
+            ev_in = [torch.cuda.Event() for _ in range(n)]
+            ev_comp = [torch.cuda.Event() for _ in range(n)]
+            ev_out = [torch.cuda.Event() for _ in range(n)]
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            hs.wait_event(t0)
+            for i in range(n):
+                b = i % nbuf
+                if pipelined and i >= nbuf:
+                    hs.wait_event(ev_comp[i - nbuf])  # compute i-2 has read this input buffer
+                with torch.cuda.stream(hs):
+                    for k in in_keys:
+                        dev_in[b][k].copy_(host_in[k], non_blocking=True)
+                ev_in[i].record(hs)
+                stream.wait_event(ev_in[i])
+                if pipelined and i >= nbuf:
+                    stream.wait_event(ev_out[i - nbuf])  # download i-2 has read this output buffer
+                compute(dev_in[b], dev_out[b])
+                ev_comp[i].record(stream)
+                ds.wait_event(ev_comp[i])
+                with torch.cuda.stream(ds):
+                    for k in host_out:
+                        host_out[k].copy_(dev_out[b][k], non_blocking=True)
+                ev_out[i].record(ds)
+            stream.wait_event(ev_out[n - 1])
+            t1.record(stream)
+            torch.cuda.synchronize()
+            return t0.elapsed_time(t1) / n
+
         n_e2e = max(3, min(args.steps, 10))
-        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        a1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = a0.elapsed_time(a1) / n_e2e
-        e2e = {"value": tokens_per_step / (e2e_ms / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
+        run(2, True)
+        pipe_ms = run(n_e2e, True)
+        run(2, False)
+        serial_ms = run(n_e2e, False)
+        e2e = {"value": tokens_per_step / (pipe_ms / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(pipe_ms, 4), "pipelined": True,
+               "serial_ms_per_step": round(serial_ms, 4),
+               "serial_value": tokens_per_step / (serial_ms / 1000.0)}
 
     if rank == 0:
         line = {
