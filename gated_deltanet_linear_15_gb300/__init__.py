@@ -6,10 +6,12 @@ workspace tensors from PyTorch's allocator).  If the library is not built the
 calls raise: there is no CPU or PyTorch fallback.
 
 Low-level (same names as the C entry points): ``gdn_chunk_fwd``,
-``gdn_chunk_bwd``, ``gdn_fwd_workspace_size``, ``gdn_bwd_workspace_size``,
-``gdn_plan_query``, ``gdn_get_device_status``.
-High-level: ``chunk_gated_delta_rule_fwd/_bwd`` (allocate outputs) and
-``chunk_gated_delta_rule`` (autograd).
+``gdn_chunk_fwd_static``, ``gdn_chunk_bwd``, ``gdn_recurrent_fwd``,
+``gdn_fwd_workspace_size``, ``gdn_bwd_workspace_size``, ``gdn_plan_query``,
+``gdn_get_device_status``.
+High-level: ``chunk_gated_delta_rule_fwd/_bwd`` (allocate outputs),
+``chunk_gated_delta_rule`` (autograd), ``recurrent_gated_delta_rule`` (decode);
+``cp`` splits sequences across ranks.
 """
 from __future__ import annotations
 
