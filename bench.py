@@ -78,10 +78,10 @@ def job_throughput(total_ms, world, tokens_per_rank_step, steps):
 # keyed by (profiler name, workload); valid only while the kernel's sources hash to the value
 # recorded with it (otherwise the roofline reports traffic null).  Summaries: profiles/*.md.
 NCU_TRAFFIC = {
-    ("bwd_local", "prefill_h32_t8192"): (819830272, "bwd_local_tc.cu", "9123a8c5b15af885"),
-    ("fwd_states", "prefill_h32_t8192"): (325293312, "fwd_tc.cu", "7e1e75e425ea8626"),
-    ("bwd_chain", "prefill_h32_t8192"): (363773184, "bwd_chain_tc.cu", "1d909baadeace169"),
-    ("bwd_wy", "prefill_h32_t8192"): (118617856, "wy.cu", "c079e64ca56b9892"),
+    ("bwd_local", "prefill_h32_t8192"): (819536896, "bwd_local_tc.cu", "6d84e77c48b48277"),
+    ("fwd_states", "prefill_h32_t8192"): (325058816, "fwd_tc.cu", "0a074519219164b2"),
+    ("bwd_chain", "prefill_h32_t8192"): (363377152, "bwd_chain_tc.cu", "07c13c77f2a474d8"),
+    ("bwd_wy", "prefill_h32_t8192"): (118649344, "wy.cu", "ef5bc4fe7faa6858"),
 }
 KERNEL_COMMON = ["chunk_common.cuh", "umma.cuh", "common.cuh", "kernels.h"]
 
