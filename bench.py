@@ -180,7 +180,7 @@ def cpu_oracle_sample(wname, heads=None, tokens=None):
     dt = time.perf_counter() - t0
     # the workload's tokens/s: T tokens of all H heads cost H/Hs times the sample
     tps = T * (Hs / w.H) / dt
-    return tps, min(cores, Hs), f"fwd+bwd of {Hs} of {w.H} heads x {T} tokens, {dt:.2f} s"
+    return tps, min(cores, Hs * x["N"]), f"fwd+bwd of {Hs} of {w.H} heads x {T} tokens, {dt:.2f} s"
 
 
 def run_reference(args):
