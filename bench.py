@@ -3,7 +3,10 @@
 
 One step = one forward (o, S_T) and one backward (dq, dk, dv, dg, dbeta) of the
 H=32, T=8192, d=128 bf16 prefill workload through the C ABI, inputs resident in
-HBM.  Prints ONE JSON line (rank 0).  See --help for the options.
+HBM.  By default the pair is gdn_chunk_fwd_save + gdn_chunk_bwd_saved (the
+forward keeps its per-chunk states and WY tiles for the backward); --recompute
+times gdn_chunk_fwd + gdn_chunk_bwd, and each run also reports the other pair.
+Prints ONE JSON line (rank 0).  See --help for the options.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gb300|reference]
 
@@ -278,6 +281,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-tokens", type=int, default=None, help="tokens per sequence in the reference sample")
     ap.add_argument("--seg-chunks", type=int, default=0)
+    ap.add_argument("--recompute", action="store_true",
+                    help="time the stateless pair (the backward recomputes the chunk states and WY tiles) "
+                         "instead of the saved-context pair")
     ap.add_argument("--decode", action="store_true",
                     help="time the token-by-token decode entry point instead (B sequences x T tokens)")
     ap.add_argument("--decode-batch", type=int, default=64)
@@ -319,6 +325,8 @@ def main():
     plan = g.gdn_plan_query(shape)
     ws_bytes = max(g.gdn_fwd_workspace_size(shape), g.gdn_bwd_workspace_size(shape))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    saved_bytes = g.gdn_saved_size(shape)
+    saved = torch.empty(max(saved_bytes, 256), dtype=torch.uint8, device=dev)
     o = torch.empty_like(x["v"])
     N, H, D = x["N"], x["H"], x["D"]
     ST = torch.empty(N, H, D, D, dtype=torch.float32, device=dev)
@@ -328,13 +336,27 @@ def main():
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def fwd():
-        rc = g.gdn_chunk_fwd(shape, x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], o, ST, ws, ws_bytes, stream)
+    # One training step of the layer: the forward (o, S_T) then the backward (all gradients), both from
+    # the inputs.  Saved-context pair (default): the forward also leaves its per-chunk states and WY
+    # tiles in `saved` and the backward reads them; --recompute: the backward rederives them.
+    def fwd_call(q, k, v, gg, beta, o_, recompute):
+        if recompute:
+            return g.gdn_chunk_fwd(shape, q, k, v, gg, beta, x["S0"], o_, ST, ws, ws_bytes, stream)
+        return g.gdn_chunk_fwd_save(shape, q, k, v, gg, beta, x["S0"], o_, ST, saved, ws, saved_bytes, ws_bytes,
+                                    stream)
+
+    def bwd_call(q, k, v, gg, beta, dO, outs, recompute):
+        a = (shape, q, k, v, gg, beta, x["S0"], dO, x["dST"], outs[0], outs[1], outs[2], outs[3], outs[4], dS0)
+        if recompute:
+            return g.gdn_chunk_bwd(*a, ws, ws_bytes, stream)
+        return g.gdn_chunk_bwd_saved(*a, saved, ws, saved_bytes, ws_bytes, stream)
+
+    def fwd(recompute=args.recompute):
+        rc = fwd_call(x["q"], x["k"], x["v"], x["g"], x["beta"], o, recompute)
         assert rc == 0, g._lib.last_error()
 
-    def bwd():
-        rc = g.gdn_chunk_bwd(shape, x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], x["dO"], x["dST"], dq, dk,
-                             dv, dg, db, dS0, ws, ws_bytes, stream)
+    def bwd(recompute=args.recompute):
+        rc = bwd_call(x["q"], x["k"], x["v"], x["g"], x["beta"], x["dO"], (dq, dk, dv, dg, db), recompute)
         assert rc == 0, g._lib.last_error()
 
     for _ in range(args.warmup):
@@ -396,6 +418,26 @@ def main():
     kernel_table = {k: {"launches": c, "total_ms": round(ms, 4), "share": round(ms / max(1e-9, sum(
         m for _, m in kern.values())), 4)} for k, (c, ms) in sorted(kern.items(), key=lambda kv: -kv[1][1])}
 
+    # ---- the other pair, for comparison (same inputs, same flush; after the timed region)
+    other = None
+    if world == 1:
+        alt = not args.recompute
+        for _ in range(3):
+            flush.zero_()
+            fwd(alt)
+            bwd(alt)
+        ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            ev2[i][0].record(stream)
+            fwd(alt)
+            bwd(alt)
+            ev2[i][1].record(stream)
+        torch.cuda.synchronize()
+        oms = statistics.mean(a.elapsed_time(b) for a, b in ev2)
+        other = {"pair": "recompute" if alt else "saved_context", "ms_per_step": round(oms, 4),
+                 "value": tokens_per_step / (oms / 1000.0)}
+
     # ---- end-to-end through the public API with host buffers.  Every step copies its inputs from
     # pinned host memory and its outputs back.  Pipelined (the reported value): copies run on their own
     # streams into double-buffered device tensors, so step i+1's upload and step i-1's download overlap
@@ -414,11 +456,10 @@ def main():
         s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
 
         def compute(di, do):
-            rc = g.gdn_chunk_fwd(shape, di["q"], di["k"], di["v"], di["g"], di["beta"], x["S0"], do["o"], ST, ws,
-                                 ws_bytes, stream)
+            rc = fwd_call(di["q"], di["k"], di["v"], di["g"], di["beta"], do["o"], args.recompute)
             assert rc == 0
-            rc = g.gdn_chunk_bwd(shape, di["q"], di["k"], di["v"], di["g"], di["beta"], x["S0"], di["dO"], x["dST"],
-                                 do["dq"], do["dk"], do["dv"], do["dg"], do["dbeta"], dS0, ws, ws_bytes, stream)
+            rc = bwd_call(di["q"], di["k"], di["v"], di["g"], di["beta"], di["dO"],
+                          (do["dq"], do["dk"], do["dv"], do["dg"], do["dbeta"]), args.recompute)
             assert rc == 0
 
         def run(n, pipelined):
@@ -472,7 +513,10 @@ def main():
             "config": {"workload": args.workload, "B": x["q"].shape[0], "T": x["q"].shape[1], "H": H, "d": D,
                        "chunk": 64, "l2norm_in_kernel": x["l2norm"], "initial_state": x["S0"] is not None,
                        "seg_chunks": plan["seg_chunks"], "l2": "256 MB flush before every step, outside the events",
+                       "pair": "recompute" if args.recompute else "saved_context",
+                       "saved_bytes": 0 if args.recompute else saved_bytes,
                        "parallelism": f"replica x{world}"},
+            "other_pair": other,
             "fwd_ms": round(1000 * fwd_s, 4), "bwd_ms": round(1000 * bwd_s, 4),
             "fwd_hbm_frac": round(fwd_b / fwd_s / 1e9 / hbm_peak, 4),
             "bwd_hbm_frac": round(bwd_b / bwd_s / 1e9 / hbm_peak, 4),

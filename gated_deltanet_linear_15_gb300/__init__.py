@@ -6,10 +6,12 @@ workspace tensors from PyTorch's allocator).  If the library is not built the
 calls raise: there is no CPU or PyTorch fallback.
 
 Low-level (same names as the C entry points): ``gdn_chunk_fwd``,
-``gdn_chunk_fwd_static``, ``gdn_chunk_bwd``, ``gdn_recurrent_fwd``,
-``gdn_fwd_workspace_size``, ``gdn_bwd_workspace_size``, ``gdn_plan_query``,
-``gdn_get_device_status``.
-High-level: ``chunk_gated_delta_rule_fwd/_bwd`` (allocate outputs),
+``gdn_chunk_fwd_static``, ``gdn_chunk_bwd``, ``gdn_chunk_fwd_save``,
+``gdn_chunk_bwd_saved``, ``gdn_recurrent_fwd``, ``gdn_fwd_workspace_size``,
+``gdn_bwd_workspace_size``, ``gdn_saved_size``, ``gdn_bwd_saved_workspace_size``,
+``gdn_plan_query``, ``gdn_get_device_status``.
+High-level: ``chunk_gated_delta_rule_fwd/_bwd`` (allocate outputs; optionally
+the forward keeps the per-chunk states and WY tiles for the backward),
 ``chunk_gated_delta_rule`` (autograd), ``recurrent_gated_delta_rule`` (decode);
 ``cp`` splits sequences across ranks.
 """
@@ -25,7 +27,8 @@ from . import _lib
 from ._lib import (GDN_BF16, GDN_FP32, GDN_L2NORM_QK, GDN_SP_OFF, GDN_WINDOW_OFF, GdnShape)
 
 __all__ = ["GdnShape", "make_shape", "gdn_chunk_fwd", "gdn_chunk_fwd_static", "gdn_chunk_bwd", "gdn_fwd_workspace_size",
-           "gdn_bwd_workspace_size", "gdn_plan_query", "gdn_get_device_status", "gdn_profile_enable",
+           "gdn_bwd_workspace_size", "gdn_saved_size", "gdn_bwd_saved_workspace_size", "gdn_chunk_fwd_save",
+           "gdn_chunk_bwd_saved", "gdn_plan_query", "gdn_get_device_status", "gdn_profile_enable",
            "gdn_profile_report",
            "chunk_gated_delta_rule_fwd", "chunk_gated_delta_rule_bwd", "chunk_gated_delta_rule",
            "GDN_L2NORM_QK", "GDN_SP_OFF", "GDN_WINDOW_OFF"]
@@ -111,6 +114,36 @@ def gdn_chunk_bwd(shape: GdnShape, q, k, v, g, beta, S0, dO, dS_T, dq, dk, dv, d
                                      _stream(stream))
 
 
+def gdn_saved_size(shape: GdnShape) -> int:
+    return int(_lib.load().gdn_saved_size(ctypes.byref(shape)))
+
+
+def gdn_bwd_saved_workspace_size(shape: GdnShape) -> int:
+    return int(_lib.load().gdn_bwd_saved_workspace_size(ctypes.byref(shape)))
+
+
+def _nbytes(t, given):
+    return int(given) if given is not None else t.numel() * t.element_size()
+
+
+def gdn_chunk_fwd_save(shape: GdnShape, q, k, v, g, beta, S0, o, S_T, saved, workspace, saved_bytes: int = None,
+                       workspace_bytes: int = None, stream=None) -> int:
+    """gdn_chunk_fwd that also leaves the per-chunk states and WY tiles in `saved`.  See gdn.h."""
+    return _lib.load().gdn_chunk_fwd_save(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                          _ptr(S0), _ptr(o), _ptr(S_T), _ptr(saved), _nbytes(saved, saved_bytes),
+                                          _ptr(workspace), _nbytes(workspace, workspace_bytes), _stream(stream))
+
+
+def gdn_chunk_bwd_saved(shape: GdnShape, q, k, v, g, beta, S0, dO, dS_T, dq, dk, dv, dg, dbeta, dS0, saved,
+                        workspace, saved_bytes: int = None, workspace_bytes: int = None, stream=None) -> int:
+    """gdn_chunk_bwd reading the forward's saved context instead of recomputing it.  See gdn.h."""
+    return _lib.load().gdn_chunk_bwd_saved(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                           _ptr(S0), _ptr(dO), _ptr(dS_T), _ptr(dq), _ptr(dk), _ptr(dv),
+                                           _ptr(dg), _ptr(dbeta), _ptr(dS0), _ptr(saved),
+                                           _nbytes(saved, saved_bytes), _ptr(workspace),
+                                           _nbytes(workspace, workspace_bytes), _stream(stream))
+
+
 def gdn_recurrent_fwd(shape: GdnShape, q, k, v, g, beta, S_in, o, S_out, stream=None) -> int:
     """Token-by-token forward (decoding); S_out may be S_in.  See gdn.h."""
     return _lib.load().gdn_recurrent_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
@@ -151,8 +184,9 @@ def _contig(*ts):
 
 def chunk_gated_delta_rule_fwd(q, k, v, g, beta, initial_state=None, output_final_state=True, cu_seqlens=None,
                                scale=None, use_qk_l2norm_in_kernel=False, sp=True, window=True, seg_chunks=0,
-                               workspace=None):
-    """o, S_T (S_T None unless output_final_state)."""
+                               workspace=None, save_context=False):
+    """o, S_T (S_T None unless output_final_state); with save_context=True also the saved
+    context (a uint8 tensor) to pass to chunk_gated_delta_rule_bwd(saved=...)."""
     _contig(q, k, v, g, beta, initial_state)
     shape = make_shape(q, v, cu_seqlens=cu_seqlens, scale=scale, l2norm=use_qk_l2norm_in_kernel, sp=sp,
                        window=window, seg_chunks=seg_chunks)
@@ -164,8 +198,12 @@ def chunk_gated_delta_rule_fwd(q, k, v, g, beta, initial_state=None, output_fina
     if need == 0:
         _check(_lib.GDN_ERR_INVALID_ARG, "gdn_fwd_workspace_size")
     ws = workspace if workspace is not None and workspace.numel() >= need else _workspace(need, q.device)
-    _check(gdn_chunk_fwd(shape, q, k, v, g, beta, initial_state, o, S_T, ws), "gdn_chunk_fwd")
-    return o, S_T
+    if not save_context:
+        _check(gdn_chunk_fwd(shape, q, k, v, g, beta, initial_state, o, S_T, ws), "gdn_chunk_fwd")
+        return o, S_T
+    saved = _workspace(gdn_saved_size(shape), q.device)
+    _check(gdn_chunk_fwd_save(shape, q, k, v, g, beta, initial_state, o, S_T, saved, ws), "gdn_chunk_fwd_save")
+    return o, S_T, saved
 
 
 def recurrent_gated_delta_rule(q, k, v, g, beta, initial_state=None, scale=None, use_qk_l2norm_in_kernel=False,
@@ -188,42 +226,55 @@ def recurrent_gated_delta_rule(q, k, v, g, beta, initial_state=None, scale=None,
 
 
 def chunk_gated_delta_rule_bwd(q, k, v, g, beta, dO, initial_state=None, dS_T=None, cu_seqlens=None, scale=None,
-                               use_qk_l2norm_in_kernel=False, sp=True, window=True, seg_chunks=0, workspace=None):
-    """dq, dk, dv, dg, dbeta, dS0 (dS0 None without an initial state)."""
+                               use_qk_l2norm_in_kernel=False, sp=True, window=True, seg_chunks=0, workspace=None,
+                               saved=None):
+    """dq, dk, dv, dg, dbeta, dS0 (dS0 None without an initial state).  `saved`: the context
+    that chunk_gated_delta_rule_fwd(save_context=True) returned for these same inputs."""
     _contig(q, k, v, g, beta, dO, initial_state, dS_T)
     shape = make_shape(q, v, cu_seqlens=cu_seqlens, scale=scale, l2norm=use_qk_l2norm_in_kernel, sp=sp,
                        window=window, seg_chunks=seg_chunks)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dg, db = torch.empty_like(g), torch.empty_like(beta)
     dS0 = torch.empty_like(initial_state) if initial_state is not None else None
-    need = gdn_bwd_workspace_size(shape)
+    need = gdn_bwd_workspace_size(shape) if saved is None else gdn_bwd_saved_workspace_size(shape)
     if need == 0:
         _check(_lib.GDN_ERR_INVALID_ARG, "gdn_bwd_workspace_size")
     ws = workspace if workspace is not None and workspace.numel() >= need else _workspace(need, q.device)
-    _check(gdn_chunk_bwd(shape, q, k, v, g, beta, initial_state, dO, dS_T, dq, dk, dv, dg, db, dS0, ws),
-           "gdn_chunk_bwd")
+    if saved is None:
+        _check(gdn_chunk_bwd(shape, q, k, v, g, beta, initial_state, dO, dS_T, dq, dk, dv, dg, db, dS0, ws),
+               "gdn_chunk_bwd")
+    else:
+        _check(gdn_chunk_bwd_saved(shape, q, k, v, g, beta, initial_state, dO, dS_T, dq, dk, dv, dg, db, dS0,
+                                   saved, ws), "gdn_chunk_bwd_saved")
     return dq, dk, dv, dg, db, dS0
 
 
 class ChunkGatedDeltaRuleFunction(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, g, beta, initial_state, cu_seqlens, scale, l2norm):
-        o, S_T = chunk_gated_delta_rule_fwd(q, k, v, g, beta, initial_state, True, cu_seqlens, scale, l2norm)
-        ctx.save_for_backward(q, k, v, g, beta, initial_state, cu_seqlens)
+    def forward(ctx, q, k, v, g, beta, initial_state, cu_seqlens, scale, l2norm, save_context):
+        if save_context:
+            o, S_T, saved = chunk_gated_delta_rule_fwd(q, k, v, g, beta, initial_state, True, cu_seqlens, scale,
+                                                       l2norm, save_context=True)
+        else:
+            (o, S_T), saved = chunk_gated_delta_rule_fwd(q, k, v, g, beta, initial_state, True, cu_seqlens, scale,
+                                                         l2norm), None
+        ctx.save_for_backward(q, k, v, g, beta, initial_state, cu_seqlens, saved)
         ctx.scale, ctx.l2norm = scale, l2norm
         return o, S_T
 
     @staticmethod
     def backward(ctx, dO, dS_T):
-        q, k, v, g, beta, S0, cu = ctx.saved_tensors
+        q, k, v, g, beta, S0, cu, saved = ctx.saved_tensors
         dq, dk, dv, dg, db, dS0 = chunk_gated_delta_rule_bwd(
             q, k, v, g, beta, dO.contiguous(), S0, None if dS_T is None else dS_T.contiguous(), cu, ctx.scale,
-            ctx.l2norm)
-        return dq, dk, dv, dg, db, dS0, None, None, None
+            ctx.l2norm, saved=saved)
+        return dq, dk, dv, dg, db, dS0, None, None, None, None
 
 
 def chunk_gated_delta_rule(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=None,
-                           use_qk_l2norm_in_kernel=False):
-    """Autograd entry: returns (o, final_state)."""
+                           use_qk_l2norm_in_kernel=False, save_context=True):
+    """Autograd entry: returns (o, final_state).  save_context=True keeps the per-chunk states
+    and WY tiles from the forward until the backward (gdn_saved_size bytes: 56 KB per chunk
+    and head at d = 128, bf16) instead of recomputing them there."""
     return ChunkGatedDeltaRuleFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, scale,
-                                             use_qk_l2norm_in_kernel)
+                                             use_qk_l2norm_in_kernel, save_context)

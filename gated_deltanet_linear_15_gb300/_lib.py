@@ -15,7 +15,8 @@ GDN_STATIC_SCRATCH_BYTES = 16 << 20
 
 # every symbol include/gdn.h declares
 EXPORTS = ("gdn_fwd_workspace_size", "gdn_bwd_workspace_size", "gdn_chunk_fwd", "gdn_chunk_fwd_static",
-           "gdn_chunk_bwd", "gdn_recurrent_fwd",
+           "gdn_chunk_bwd", "gdn_saved_size", "gdn_bwd_saved_workspace_size", "gdn_chunk_fwd_save",
+           "gdn_chunk_bwd_saved", "gdn_recurrent_fwd",
            "gdn_get_device_status", "gdn_plan_query", "gdn_profile_enable", "gdn_profile_report",
            "gdn_status_string", "gdn_last_error_string")
 
@@ -58,6 +59,15 @@ def load():
         lib.gdn_chunk_fwd_static.restype = ctypes.c_int
         lib.gdn_chunk_bwd.argtypes = [S, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
         lib.gdn_chunk_bwd.restype = ctypes.c_int
+        lib.gdn_saved_size.argtypes = [S]
+        lib.gdn_saved_size.restype = ctypes.c_size_t
+        lib.gdn_bwd_saved_workspace_size.argtypes = [S]
+        lib.gdn_bwd_saved_workspace_size.restype = ctypes.c_size_t
+        lib.gdn_chunk_fwd_save.argtypes = [S, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, ctypes.c_size_t, P]
+        lib.gdn_chunk_fwd_save.restype = ctypes.c_int
+        lib.gdn_chunk_bwd_saved.argtypes = [S, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P,
+                                            ctypes.c_size_t, P]
+        lib.gdn_chunk_bwd_saved.restype = ctypes.c_int
         lib.gdn_recurrent_fwd.argtypes = [S, P, P, P, P, P, P, P, P, P]
         lib.gdn_recurrent_fwd.restype = ctypes.c_int
         lib.gdn_get_device_status.argtypes = [S, P, P]

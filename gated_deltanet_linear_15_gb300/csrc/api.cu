@@ -56,6 +56,9 @@ struct Layout {
   size_t off_states = 0, off_dstates = 0;   // backward per-chunk states
   size_t off_F = 0, off_R = 0, off_dS = 0;  // reverse fix-up buffers
   size_t off_wy = 0, wy_bytes = 0;          // backward WY tiles (bf16, d = 128)
+  size_t states_bytes = 0;                  // per-chunk start states
+  size_t bwd_saved_total = 0;               // backward workspace when the forward saved its context
+  size_t saved_off_wy = 0, saved_total = 0; // saved context: [states][WY tiles]
   size_t fwd_total = 0, bwd_total = 0;
 };
 
@@ -139,20 +142,27 @@ int make_layout(const gdn_shape *s, Layout &L) {
   L.off_S = off;
   off += spbuf;
   L.fwd_total = off;
-  L.off_states = off;
-  off = align256(off + (size_t)L.CH_max * L.H * DD * L.esize);
+  // backward: the reverse-chain buffers first, then the per-chunk states and WY tiles that the
+  // backward recomputes unless the forward saved them (a saved-context backward needs only the
+  // prefix up to bwd_saved_total)
+  L.states_bytes = align256((size_t)L.CH_max * L.H * DD * L.esize);
   L.off_dstates = off;
-  off = align256(off + (size_t)L.CH_max * L.H * DD * L.esize);
+  off += L.states_bytes;
   L.off_F = off;
   off += spbuf;
   L.off_R = off;
   off += spbuf;
   L.off_dS = off;
   off += spbuf;
+  L.bwd_saved_total = off;
+  L.off_states = off;
+  off += L.states_bytes;
   L.off_wy = off;
   L.wy_bytes = (s->dtype == GDN_BF16 && L.D == 128) ? (size_t)L.CH_max * L.H * 3 * CH * CH * 2 : 0;
   off = align256(off + L.wy_bytes);
   L.bwd_total = off;
+  L.saved_off_wy = L.states_bytes;
+  L.saved_total = align256(L.states_bytes + L.wy_bytes);
   return GDN_OK;
 }
 
@@ -334,13 +344,18 @@ int wy_map(CUtensorMap *m, const void *ptr, long rows) {
 int launch_forward_kernel(const Layout &L, const gdn_shape *s, const FwdArgs &fa, dim3 grid, cudaStream_t st) {
   const bool bf = s->dtype == GDN_BF16;
   if (bf && L.D == 128 && L.Ttot > 0) {
-    CUtensorMap tq, tk, tv, tw;
+    CUtensorMap tq, tk, tv, tw, ts;
     int rc;
     if ((rc = qkv_map(&tk, fa.k, L.Ttot, L.H))) return rc;
     if ((rc = qkv_map(&tv, fa.v, L.Ttot, L.H))) return rc;
     if ((rc = qkv_map(&tq, fa.q ? fa.q : fa.k, L.Ttot, L.H))) return rc;
-    if ((rc = wy_map(&tw, fa.wy ? fa.wy : fa.k, fa.wy ? (long)L.CH_max * L.H * 3 * CH : 64))) return rc;
-    return launch_fwd_tc(fa, tq, tk, tv, tw, grid, st);
+    // WY tiles: read by the backward's state pass, or written by a saved-context forward
+    const void *wyp = fa.wy ? fa.wy : fa.wy_save;
+    if ((rc = wy_map(&tw, wyp ? wyp : fa.k, wyp ? (long)L.CH_max * L.H * 3 * CH : 64))) return rc;
+    // chunk-start states written by the state pass or a saved-context forward (unused otherwise)
+    if ((rc = state_map(&ts, fa.states ? fa.states : fa.k, fa.states ? (long)L.CH_max * L.H * 128 : 128)))
+      return rc;
+    return launch_fwd_tc(fa, tq, tk, tv, tw, ts, grid, st);
   }
   return launch_fwd_chunk(fa, bf, L.D, grid, st);
 }
@@ -392,6 +407,194 @@ FwdArgs fwd_args(const gdn_shape *s, const Layout &L, char *ws, const Plan &pl) 
   return fa;
 }
 
+int fwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g, const float *beta,
+             const float *S0, void *o, float *S_T, void *workspace, size_t workspace_bytes, void *saved,
+             size_t saved_bytes, gdn_stream_t stream) {
+  g_last_error.clear();
+  Layout L;
+  int rc = make_layout(s, L);
+  if (rc) return rc;
+  if (L.Ttot > 0 || S_T) {
+    rc = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {g, "g"}, {beta, "beta"}, {o, "o"}},
+                    {{S0, "S0"}, {S_T, "S_T"}, {s->cu_seqlens, "cu_seqlens"}});
+    if (rc) return rc;
+  }
+  if (!workspace || workspace_bytes < L.fwd_total)
+    return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", L.fwd_total,
+                workspace ? workspace_bytes : (size_t)0);
+  if (!aligned16(workspace)) return fail(GDN_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+  if (saved) {
+    if (saved_bytes < L.saved_total)
+      return fail(GDN_ERR_WORKSPACE, "saved context of %zu bytes needed, %zu given", L.saved_total, saved_bytes);
+    if (!aligned16(saved)) return fail(GDN_ERR_INVALID_ARG, "saved is not 16-byte aligned");
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(workspace);
+  Plan pl;
+  if ((rc = prologue(s, L, ws, g, st, pl))) return rc;
+  FwdArgs fa = fwd_args(s, L, ws, pl);
+  fa.q = q;
+  fa.k = k;
+  fa.v = v;
+  fa.g = g;
+  fa.beta = beta;
+  fa.S0 = S0;
+  fa.o = o;
+  fa.ST = S_T;
+  if (saved && L.Ttot > 0) {  // the outputs pass also leaves the chunk-start states and WY tiles
+    fa.states = saved;
+    if (L.wy_bytes > 0) fa.wy_save = static_cast<char *>(saved) + L.saved_off_wy;
+  }
+  return forward_passes(s, L, ws, fa, 1, st);
+}
+
+int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g, const float *beta,
+             const float *S0, const void *dO, const float *dS_T, void *dq, void *dk, void *dv, float *dg,
+             float *dbeta, float *dS0, const void *saved, size_t saved_bytes, void *workspace,
+             size_t workspace_bytes, gdn_stream_t stream) {
+  g_last_error.clear();
+  Layout L;
+  int rc = make_layout(s, L);
+  if (rc) return rc;
+  if (S0 && !dS0) return fail(GDN_ERR_INVALID_ARG, "dS0 is required when S0 is given");
+  rc = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {g, "g"}, {beta, "beta"}, {dO, "dO"}, {dq, "dq"}, {dk, "dk"},
+                   {dv, "dv"}, {dg, "dg"}, {dbeta, "dbeta"}},
+                  {{S0, "S0"}, {dS_T, "dS_T"}, {dS0, "dS0"}, {s->cu_seqlens, "cu_seqlens"}});
+  if (rc) return rc;
+  const size_t need = saved ? L.bwd_saved_total : L.bwd_total;
+  if (!workspace || workspace_bytes < need)
+    return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                workspace ? workspace_bytes : (size_t)0);
+  if (!aligned16(workspace)) return fail(GDN_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+  if (saved) {
+    if (saved_bytes < L.saved_total)
+      return fail(GDN_ERR_WORKSPACE, "saved context of %zu bytes needed, %zu given", L.saved_total, saved_bytes);
+    if (!aligned16(saved)) return fail(GDN_ERR_INVALID_ARG, "saved is not 16-byte aligned");
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(workspace);
+  const bool bf = s->dtype == GDN_BF16;
+  Plan pl;
+  if ((rc = prologue(s, L, ws, g, st, pl))) return rc;
+  const void *wy = nullptr;
+  const void *states = ws + L.off_states;
+  if (saved) {
+    // the forward left the chunk-start states and the WY tiles: nothing to recompute
+    states = saved;
+    if (L.wy_bytes > 0 && L.Ttot > 0) wy = static_cast<const char *>(saved) + L.saved_off_wy;
+  } else {
+    // 0. WY tiles of every chunk, shared by the three passes below (bf16, d = 128)
+    if (L.wy_bytes > 0 && L.Ttot > 0) {
+      WyArgs wa;
+      wa.k = k;
+      wa.g = g;
+      wa.beta = beta;
+      wa.plan = pl;
+      wa.wy = ws + L.off_wy;
+      wa.status = reinterpret_cast<int *>(ws + L.off_status);
+      wa.H = L.H;
+      wa.flags = s->flags;
+      PROF("bwd_wy");
+      CK(launch_wy(wa, L.CH_max, st));
+      wy = wa.wy;
+    }
+    // 1. forward states at every chunk start
+    FwdArgs fa = fwd_args(s, L, ws, pl);
+    fa.wy = wy;
+    fa.q = q;
+    fa.k = k;
+    fa.v = v;
+    fa.g = g;
+    fa.beta = beta;
+    fa.S0 = S0;
+    fa.states = ws + L.off_states;
+    if ((rc = forward_passes(s, L, ws, fa, 2, st))) return rc;
+  }
+  // 2. reverse chain: dS at every chunk end (and dS0)
+  BwdArgs ba;
+  std::memset(&ba, 0, sizeof ba);
+  ba.q = q;
+  ba.k = k;
+  ba.v = v;
+  ba.dO = dO;
+  ba.g = g;
+  ba.beta = beta;
+  ba.dST = dS_T;
+  ba.dq = dq;
+  ba.dk = dk;
+  ba.dv = dv;
+  ba.dg = dg;
+  ba.dbeta = dbeta;
+  ba.dS0 = dS0;
+  ba.plan = pl;
+  ba.gsum = reinterpret_cast<const float *>(ws + L.off_gsum);
+  ba.status = reinterpret_cast<int *>(ws + L.off_status);
+  if (L.sp) {
+    ba.Fbuf = reinterpret_cast<float *>(ws + L.off_F);
+    ba.Rbuf = reinterpret_cast<float *>(ws + L.off_R);
+    ba.dSend = reinterpret_cast<float *>(ws + L.off_dS);
+  }
+  ba.states = states;
+  ba.dstates = ws + L.off_dstates;
+  ba.wy = wy;
+  ba.H = L.H;
+  ba.Lseg = L.Lseg;
+  ba.scale = s->scale;
+  ba.flags = s->flags;
+  // the reverse chain: tcgen05 for bf16 with d = 128, the mma.sync kernel otherwise
+  const bool chain_tc = bf && L.D == 128 && L.Ttot > 0;
+  CUtensorMap cmaps[4];
+  if (chain_tc && ((rc = qkv_map(&cmaps[0], q, L.Ttot, L.H)) || (rc = qkv_map(&cmaps[1], k, L.Ttot, L.H)) ||
+                   (rc = qkv_map(&cmaps[2], dO, L.Ttot, L.H)) ||
+                   (rc = wy_map(&cmaps[3], wy ? wy : k, wy ? (long)L.CH_max * L.H * 3 * CH : 64))))
+    return rc;
+  auto chain = [&](dim3 grid) {
+    return chain_tc ? launch_bwd_chain_tc(ba, cmaps, grid, st) : launch_bwd_chain(ba, bf, L.D, grid, st);
+  };
+  if (L.sp) {
+    ba.pass = 0;
+    {
+      PROF("bwd_chain_pass_a");
+      CK(chain(dim3(L.S_max, L.H, 2)));
+    }
+    FixupArgs fx;
+    fx.plan = pl;
+    fx.gsum = ba.gsum;
+    fx.E = ba.Fbuf;
+    fx.M = ba.Rbuf;
+    fx.out = ba.dSend;
+    fx.H = L.H;
+    fx.D = L.D;
+    fx.Lseg = L.Lseg;
+    fx.flags = s->flags;
+    fx.reverse = 1;
+    PROF("fixup_bwd");
+    CK(launch_fixup(fx, L.N, st));
+  }
+  ba.pass = 1;
+  {
+    PROF("bwd_chain");
+    CK(chain(dim3(L.S_max, L.H, 1)));
+  }
+  // 3. local gradients, every (chunk, head) in parallel
+  {
+    PROF("bwd_local");
+    if (bf && L.D == 128 && L.Ttot > 0) {
+      CUtensorMap maps[7];
+      if ((rc = qkv_map(&maps[0], q, L.Ttot, L.H)) || (rc = qkv_map(&maps[1], k, L.Ttot, L.H)) ||
+          (rc = qkv_map(&maps[2], v, L.Ttot, L.H)) || (rc = qkv_map(&maps[3], dO, L.Ttot, L.H)) ||
+          (rc = state_map(&maps[4], states, (long)L.CH_max * L.H * 128)) ||
+          (rc = state_map(&maps[5], ws + L.off_dstates, (long)L.CH_max * L.H * 128)) ||
+          (rc = wy_map(&maps[6], wy ? wy : k, wy ? (long)L.CH_max * L.H * 3 * CH : 64)))
+        return rc;
+      CK(launch_bwd_local_tc(ba, maps, L.CH_max, st));
+    } else {
+      CK(launch_bwd_local(ba, bf, L.D, L.CH_max, st));
+    }
+  }
+  return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -408,36 +611,32 @@ size_t gdn_bwd_workspace_size(const gdn_shape *shape) {
   return L.bwd_total;
 }
 
+size_t gdn_saved_size(const gdn_shape *shape) {
+  Layout L;
+  if (make_layout(shape, L) != GDN_OK) return 0;
+  return L.saved_total;
+}
+
+size_t gdn_bwd_saved_workspace_size(const gdn_shape *shape) {
+  Layout L;
+  if (make_layout(shape, L) != GDN_OK) return 0;
+  return L.bwd_saved_total;
+}
+
 int gdn_chunk_fwd(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g, const float *beta,
                   const float *S0, void *o, float *S_T, void *workspace, size_t workspace_bytes,
                   gdn_stream_t stream) {
-  g_last_error.clear();
-  Layout L;
-  int rc = make_layout(s, L);
-  if (rc) return rc;
-  if (L.Ttot > 0 || S_T) {
-    rc = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {g, "g"}, {beta, "beta"}, {o, "o"}},
-                    {{S0, "S0"}, {S_T, "S_T"}, {s->cu_seqlens, "cu_seqlens"}});
-    if (rc) return rc;
+  return fwd_impl(s, q, k, v, g, beta, S0, o, S_T, workspace, workspace_bytes, nullptr, 0, stream);
+}
+
+int gdn_chunk_fwd_save(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,
+                       const float *beta, const float *S0, void *o, float *S_T, void *saved, size_t saved_bytes,
+                       void *workspace, size_t workspace_bytes, gdn_stream_t stream) {
+  if (!saved) {
+    g_last_error.clear();
+    return fail(GDN_ERR_INVALID_ARG, "saved is NULL (use gdn_chunk_fwd to save nothing)");
   }
-  if (!workspace || workspace_bytes < L.fwd_total)
-    return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", L.fwd_total,
-                workspace ? workspace_bytes : (size_t)0);
-  if (!aligned16(workspace)) return fail(GDN_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  char *ws = static_cast<char *>(workspace);
-  Plan pl;
-  if ((rc = prologue(s, L, ws, g, st, pl))) return rc;
-  FwdArgs fa = fwd_args(s, L, ws, pl);
-  fa.q = q;
-  fa.k = k;
-  fa.v = v;
-  fa.g = g;
-  fa.beta = beta;
-  fa.S0 = S0;
-  fa.o = o;
-  fa.ST = S_T;
-  return forward_passes(s, L, ws, fa, 1, st);
+  return fwd_impl(s, q, k, v, g, beta, S0, o, S_T, workspace, workspace_bytes, saved, saved_bytes, stream);
 }
 
 }  // extern "C"
@@ -495,136 +694,21 @@ int gdn_chunk_fwd_static(const gdn_shape *s, const void *q, const void *k, const
 int gdn_chunk_bwd(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g, const float *beta,
                   const float *S0, const void *dO, const float *dS_T, void *dq, void *dk, void *dv, float *dg,
                   float *dbeta, float *dS0, void *workspace, size_t workspace_bytes, gdn_stream_t stream) {
-  g_last_error.clear();
-  Layout L;
-  int rc = make_layout(s, L);
-  if (rc) return rc;
-  if (S0 && !dS0) return fail(GDN_ERR_INVALID_ARG, "dS0 is required when S0 is given");
-  rc = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {g, "g"}, {beta, "beta"}, {dO, "dO"}, {dq, "dq"}, {dk, "dk"},
-                   {dv, "dv"}, {dg, "dg"}, {dbeta, "dbeta"}},
-                  {{S0, "S0"}, {dS_T, "dS_T"}, {dS0, "dS0"}, {s->cu_seqlens, "cu_seqlens"}});
-  if (rc) return rc;
-  if (!workspace || workspace_bytes < L.bwd_total)
-    return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", L.bwd_total,
-                workspace ? workspace_bytes : (size_t)0);
-  if (!aligned16(workspace)) return fail(GDN_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  char *ws = static_cast<char *>(workspace);
-  const bool bf = s->dtype == GDN_BF16;
-  Plan pl;
-  if ((rc = prologue(s, L, ws, g, st, pl))) return rc;
-  // 0. WY tiles of every chunk, shared by the three passes below (bf16, d = 128)
-  const void *wy = nullptr;
-  if (L.wy_bytes > 0 && L.Ttot > 0) {
-    WyArgs wa;
-    wa.k = k;
-    wa.g = g;
-    wa.beta = beta;
-    wa.plan = pl;
-    wa.wy = ws + L.off_wy;
-    wa.status = reinterpret_cast<int *>(ws + L.off_status);
-    wa.H = L.H;
-    wa.flags = s->flags;
-    PROF("bwd_wy");
-    CK(launch_wy(wa, L.CH_max, st));
-    wy = wa.wy;
-  }
-  // 1. forward states at every chunk start
-  FwdArgs fa = fwd_args(s, L, ws, pl);
-  fa.wy = wy;
-  fa.q = q;
-  fa.k = k;
-  fa.v = v;
-  fa.g = g;
-  fa.beta = beta;
-  fa.S0 = S0;
-  fa.states = ws + L.off_states;
-  if ((rc = forward_passes(s, L, ws, fa, 2, st))) return rc;
-  // 2. reverse chain: dS at every chunk end (and dS0)
-  BwdArgs ba;
-  std::memset(&ba, 0, sizeof ba);
-  ba.q = q;
-  ba.k = k;
-  ba.v = v;
-  ba.dO = dO;
-  ba.g = g;
-  ba.beta = beta;
-  ba.dST = dS_T;
-  ba.dq = dq;
-  ba.dk = dk;
-  ba.dv = dv;
-  ba.dg = dg;
-  ba.dbeta = dbeta;
-  ba.dS0 = dS0;
-  ba.plan = pl;
-  ba.gsum = reinterpret_cast<const float *>(ws + L.off_gsum);
-  ba.status = reinterpret_cast<int *>(ws + L.off_status);
-  if (L.sp) {
-    ba.Fbuf = reinterpret_cast<float *>(ws + L.off_F);
-    ba.Rbuf = reinterpret_cast<float *>(ws + L.off_R);
-    ba.dSend = reinterpret_cast<float *>(ws + L.off_dS);
-  }
-  ba.states = ws + L.off_states;
-  ba.dstates = ws + L.off_dstates;
-  ba.wy = wy;
-  ba.H = L.H;
-  ba.Lseg = L.Lseg;
-  ba.scale = s->scale;
-  ba.flags = s->flags;
-  // the reverse chain: tcgen05 for bf16 with d = 128, the mma.sync kernel otherwise
-  const bool chain_tc = bf && L.D == 128 && L.Ttot > 0;
-  CUtensorMap cmaps[4];
-  if (chain_tc && ((rc = qkv_map(&cmaps[0], q, L.Ttot, L.H)) || (rc = qkv_map(&cmaps[1], k, L.Ttot, L.H)) ||
-                   (rc = qkv_map(&cmaps[2], dO, L.Ttot, L.H)) ||
-                   (rc = wy_map(&cmaps[3], wy ? wy : k, wy ? (long)L.CH_max * L.H * 3 * CH : 64))))
-    return rc;
-  auto chain = [&](dim3 grid) {
-    return chain_tc ? launch_bwd_chain_tc(ba, cmaps, grid, st) : launch_bwd_chain(ba, bf, L.D, grid, st);
-  };
-  if (L.sp) {
-    ba.pass = 0;
-    {
-      PROF("bwd_chain_pass_a");
-      CK(chain(dim3(L.S_max, L.H, 2)));
-    }
-    FixupArgs fx;
-    fx.plan = pl;
-    fx.gsum = ba.gsum;
-    fx.E = ba.Fbuf;
-    fx.M = ba.Rbuf;
-    fx.out = ba.dSend;
-    fx.H = L.H;
-    fx.D = L.D;
-    fx.Lseg = L.Lseg;
-    fx.flags = s->flags;
-    fx.reverse = 1;
-    PROF("fixup_bwd");
-    CK(launch_fixup(fx, L.N, st));
-  }
-  ba.pass = 1;
-  {
-    PROF("bwd_chain");
-    CK(chain(dim3(L.S_max, L.H, 1)));
-  }
-  // 3. local gradients, every (chunk, head) in parallel
-  {
-    PROF("bwd_local");
-    if (bf && L.D == 128 && L.Ttot > 0) {
-      CUtensorMap maps[7];
-      if ((rc = qkv_map(&maps[0], q, L.Ttot, L.H)) || (rc = qkv_map(&maps[1], k, L.Ttot, L.H)) ||
-          (rc = qkv_map(&maps[2], v, L.Ttot, L.H)) || (rc = qkv_map(&maps[3], dO, L.Ttot, L.H)) ||
-          (rc = state_map(&maps[4], ws + L.off_states, (long)L.CH_max * L.H * 128)) ||
-          (rc = state_map(&maps[5], ws + L.off_dstates, (long)L.CH_max * L.H * 128)) ||
-          (rc = wy_map(&maps[6], wy ? wy : k, wy ? (long)L.CH_max * L.H * 3 * CH : 64)))
-        return rc;
-      CK(launch_bwd_local_tc(ba, maps, L.CH_max, st));
-    } else {
-      CK(launch_bwd_local(ba, bf, L.D, L.CH_max, st));
-    }
-  }
-  return GDN_OK;
+  return bwd_impl(s, q, k, v, g, beta, S0, dO, dS_T, dq, dk, dv, dg, dbeta, dS0, nullptr, 0, workspace,
+                  workspace_bytes, stream);
 }
 
+int gdn_chunk_bwd_saved(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,
+                        const float *beta, const float *S0, const void *dO, const float *dS_T, void *dq, void *dk,
+                        void *dv, float *dg, float *dbeta, float *dS0, const void *saved, size_t saved_bytes,
+                        void *workspace, size_t workspace_bytes, gdn_stream_t stream) {
+  if (!saved) {
+    g_last_error.clear();
+    return fail(GDN_ERR_INVALID_ARG, "saved is NULL (use gdn_chunk_bwd to recompute the forward)");
+  }
+  return bwd_impl(s, q, k, v, g, beta, S0, dO, dS_T, dq, dk, dv, dg, dbeta, dS0, saved, saved_bytes, workspace,
+                  workspace_bytes, stream);
+}
 int gdn_recurrent_fwd(const gdn_shape *s, const void *q, const void *k, const void *v, const float *g,
                       const float *beta, const float *S_in, void *o, float *S_out, gdn_stream_t stream) {
   g_last_error.clear();

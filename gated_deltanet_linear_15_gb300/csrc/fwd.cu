@@ -74,7 +74,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_chunk_kernel(FwdArgs a) {
     return;
   }
   const bool outputs = (a.pass == 1);
-  const bool states = (a.pass == 2);
   const bool need_v = !transition;
   const bool l2 = (a.flags & kFlagL2Norm) != 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -139,7 +138,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_chunk_kernel(FwdArgs a) {
     cp_async_wait_all();
     __syncthreads();  // tiles of chunk c landed; state copy of S0 complete
 
-    if (states && c >= cbeg) {
+    if (a.pass != 0 && a.states && c >= cbeg) {
       // bf16/fp32 copy of the state at the chunk start, for the backward
       E *dst = static_cast<E *>(a.states) + ((size_t)(chunk0 + c) * H + h) * DD;
       constexpr int EPV = 16 / sizeof(E);

@@ -47,6 +47,7 @@ struct __align__(1024) TcSmem {
   uint8_t x1[HT], x2[HT], p[HT];
   uint8_t wu[2 * HT];   // W^T (MN-major B, rows = d_k), later Ut^T (K-major A, rows = d_v), then O staging
   uint8_t s0[4 * HT];   // S0 fp16 (K-major A: rows = d_v, two k-blocks of 128 rows)
+  uint8_t ah[HT];       // Ahat fp16 (row-major, swizzled), staged for the saved-context store
   float nf[CH * (CH + 4)];
   float g[2][CH], beta[2][CH];  // per ring stage
   Gates gt[2];  // per ring stage; the next chunk's gates are computed during this chunk
@@ -75,7 +76,8 @@ __device__ __forceinline__ uint32_t chunk_off(int r, int cb) { return r * 128 + 
 
 __global__ void __launch_bounds__(FT, 1)
     fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                  const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmw) {
+                  const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmw,
+                  const __grid_constant__ CUtensorMap tms) {
   extern __shared__ unsigned char smraw[];
   TcSmem &sm = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
 
@@ -109,11 +111,14 @@ __global__ void __launch_bounds__(FT, 1)
     return;
   }
   const bool outputs = (a.pass == 1);
-  const bool states = (a.pass == 2);
   const bool need_v = !transition;
   // backward passes: the WY tiles X1, X2 were computed once per chunk; they arrive by TMA in the
   // ring's Q slots (q is not needed without outputs) and replace the Gram product and the inverse
   const bool use_wy = a.wy != nullptr && !outputs;
+  // chunk-start states (state pass, or outputs pass of a saved-context forward) and WY tiles (saved-
+  // context forward) leave shared memory by TMA stores issued by thread 0
+  const bool save_states = a.pass != 0 && a.states != nullptr;
+  const bool save_wy = outputs && a.wy_save != nullptr;
   const bool l2 = (a.flags & kFlagL2Norm) != 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wg = warp >> 2;                      // column group 0..3 within a lane quarter
@@ -132,7 +137,8 @@ __global__ void __launch_bounds__(FT, 1)
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
     tma_prefetch_desc(&tmq);
-    if (use_wy) tma_prefetch_desc(&tmw);
+    if (use_wy || save_wy) tma_prefetch_desc(&tmw);
+    if (save_states) tma_prefetch_desc(&tms);
   }
   if (warp == 0) {
     tmem_alloc(u32(&sm.tmem_base), TM_COLS);
@@ -291,6 +297,8 @@ __global__ void __launch_bounds__(FT, 1)
     // prefetch the next chunk into the other stage (its previous contents were consumed)
     if (tid == 0 && c + 1 < cend) issue_tma(c + 1, stage ^ 1);
     if (c + 1 < cend) issue_gb(c + 1, stage ^ 1, false);
+    // the previous chunk's tile stores have read s0 / x1 / x2 / ah (overwritten below)
+    if (tid == 0 && (save_states || save_wy)) tma_store_wait_read();
     // chunk cfirst: wait for its tiles and normalise them here; later chunks were normalised one
     // iteration ahead, while MMA 3 and MMA 4 of the previous chunk ran
     const bool tma_ok = it > 0 || mbar_wait(u32(&sm.bar_tma[stage]), 0, err, 8);
@@ -349,7 +357,8 @@ __global__ void __launch_bounds__(FT, 1)
       fence_before();
       __syncthreads();
 
-      // ---- Ahat (fp32 diagonal blocks, TF32 tensor-core merges) -> X1, X2 (fp16, K-major: rows = r)
+      // ---- Ahat (fp32 diagonal blocks, TF32 tensor-core merges) -> X1, X2 (fp16, K-major: rows = r);
+      // a saved-context forward also stages Ahat, and stores the three tiles below
       wy_inverse<false, false>(sm.nf, LN, gbeta, sm.ys, [&](int r, int c, float a0, float a1) {
         const float2 bb = *reinterpret_cast<const float2 *>(gbeta + c), rg = *reinterpret_cast<const float2 *>(G.rgp + c);
         const float gr = G.gp[r], x0 = a0 * bb.x, x1 = a1 * bb.y;
@@ -357,12 +366,20 @@ __global__ void __launch_bounds__(FT, 1)
         *reinterpret_cast<__half2 *>(sm.x1 + off) = __floats2half2_rn(x0, x1);
         *reinterpret_cast<__half2 *>(sm.x2 + off) =
             __floats2half2_rn(c <= r ? x0 * (gr * rg.x) : 0.f, c + 1 <= r ? x1 * (gr * rg.y) : 0.f);
+        if (save_wy) *reinterpret_cast<__half2 *>(sm.ah + off) = __floats2half2_rn(a0, a1);
       }, it == 0);
     }
 
     // ---- MMA 2: W^T = K^T X1^T, U^T = V^T X2^T  (M = 128, N = 64, K = 64)
     if (tid == 0) {
       fence_after();
+      if (save_wy && emit) {  // X1, X2, Ahat rows of this (chunk, head) in the saved context
+        const int wrow = ((chunk0 + c) * H + h) * 3 * CH;
+        tma_store_3d(&tmw, 0, wrow, 0, u32(sm.x1));
+        tma_store_3d(&tmw, 0, wrow + CH, 0, u32(sm.x2));
+        tma_store_3d(&tmw, 0, wrow + 2 * CH, 0, u32(sm.ah));
+        tma_store_commit();
+      }
       const uint32_t idesc = idesc_f16(128, 64, true, false);
       const uint32_t kb = u32(st), vb = u32(st + 4 * HT);
       const uint32_t x1b = use_wy ? u32(st + HT) : u32(sm.x1), x2b = use_wy ? u32(st + 3 * HT) : u32(sm.x2);
@@ -378,23 +395,17 @@ __global__ void __launch_bounds__(FT, 1)
       mma_commit(u32(&sm.bar_mma));
     }
     __syncwarp();
-    // meanwhile: S0 -> fp16 operand copy, gam_C * S0 back into TMEM (state copy for the backward)
+    // meanwhile: S0 -> fp16 operand copy, gam_C * S0 back into TMEM (the copy is also the chunk-start
+    // state that the backward reads)
     {
       const float gC = G.gamC;
-      f16 *stg = states && c >= cbeg
-                     ? static_cast<f16 *>(a.states) + ((size_t)(chunk0 + c) * H + h) * DD + (size_t)row * D
-                     : nullptr;
       {
         const int c0 = wg * 32;
         float v[32];
         tmem_ld32(tm + tm_lane + TM_S + c0, v);
         const int kb = c0 >> 6;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint8_t *dst = sm.s0 + kb * 2 * HT + chunk_off(row, c0 + q4 * 8);
-          st_chunk_f16(dst, v + q4 * 8);
-          if (stg) *reinterpret_cast<uint4 *>(stg + c0 + q4 * 8) = *reinterpret_cast<const uint4 *>(dst);
-        }
+        for (int q4 = 0; q4 < 4; ++q4) st_chunk_f16(sm.s0 + kb * 2 * HT + chunk_off(row, c0 + q4 * 8), v + q4 * 8);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] *= gC;
         tmem_st32(tm + tm_lane + TM_S + c0, v);
@@ -404,6 +415,12 @@ __global__ void __launch_bounds__(FT, 1)
     if (__syncthreads_or(!mma_wait())) {
       failed = true;
       break;
+    }
+    if (tid == 0 && save_states && c >= cbeg) {  // the fp16 chunk-start state, two 64-column blocks
+      const int srow = ((chunk0 + c) * H + h) * D;
+      tma_store_3d(&tms, 0, srow, 0, u32(sm.s0));
+      tma_store_3d(&tms, 64, srow, 0, u32(sm.s0 + 2 * HT));
+      tma_store_commit();
     }
     // Oi^T = S0 Q^T needs only the state copy and Q: issued now, it runs under the W^T read-out
     // (MMA 3's commit covers it)
@@ -552,6 +569,7 @@ __global__ void __launch_bounds__(FT, 1)
       }
     }
   }
+  if (tid == 0 && (save_states || save_wy)) tma_store_wait_all();
   fence_before();
   __syncthreads();
   fence_after();
@@ -561,12 +579,12 @@ __global__ void __launch_bounds__(FT, 1)
 size_t fwd_tc_smem_bytes() { return sizeof(TcSmem) + 1024; }
 
 int launch_fwd_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                  const CUtensorMap &tw, dim3 grid, cudaStream_t st) {
+                  const CUtensorMap &tw, const CUtensorMap &ts, dim3 grid, cudaStream_t st) {
   const size_t smem = fwd_tc_smem_bytes();
   static_assert(sizeof(TcSmem) + 1024 <= 232448, "shared memory budget");
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  fwd_tc_kernel<<<grid, FT, smem, st>>>(a, tq, tk, tv, tw);
+  fwd_tc_kernel<<<grid, FT, smem, st>>>(a, tq, tk, tv, tw, ts);
   return (int)cudaGetLastError();
 }
 

@@ -22,12 +22,13 @@ struct FwdArgs {
   const float *gsum;  // [CH_max, H] per-chunk sum of g
   int *status;
   float *Ebuf, *Mbuf, *Sstart;  // [S_max, H, D, D]
-  void *states;                 // [CH_max, H, D, D] element type of q
+  void *states;                 // [CH_max, H, D, D] state at every chunk start (fp16 / fp32), or NULL
   int H, Lseg;
   float scale;
   unsigned flags;
-  int pass;  // 0: segment end states / transitions, 1: outputs, 2: per-chunk states
+  int pass;  // 0: segment end states / transitions, 1: outputs (+ states if set), 2: states only
   const void *wy;  // precomputed WY tiles (backward only) or NULL: X1/X2 come by TMA, no inverse
+  void *wy_save;   // outputs pass (bf16, d = 128): also write the inline X1, X2, Ahat tiles here, or NULL
 };
 
 struct BwdArgs {
@@ -88,7 +89,7 @@ int launch_fwd_chunk(const FwdArgs &a, bool is_bf16, int D, dim3 grid, cudaStrea
 // tcgen05 forward for bf16 inputs and d = 128; q, k, v tensor maps over [tokens, H, 128] with a 64 x 1 x 64 box;
 // tw: the WY tiles as [rows, 64] fp16 with a 64 x 64 box (used when a.wy != NULL)
 int launch_fwd_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                  const CUtensorMap &tw, dim3 grid, cudaStream_t st);
+                  const CUtensorMap &tw, const CUtensorMap &ts, dim3 grid, cudaStream_t st);
 int launch_wy(const WyArgs &a, int CH_max, cudaStream_t st);
 int launch_bwd_chain(const BwdArgs &a, bool is_bf16, int D, dim3 grid, cudaStream_t st);
 // tcgen05 reverse chain (bf16, d = 128); maps: q, k, dO ([tokens, H, 128] bf16, box 64x1x64) and the WY tiles

@@ -146,6 +146,54 @@ int gdn_chunk_bwd(const gdn_shape *shape,
                   float *dS0,        /* required iff S0 != NULL */
                   void *workspace, size_t workspace_bytes, gdn_stream_t stream);
 
+/*
+ * Saved-context training pair: the forward also leaves, in a caller-owned
+ * buffer `saved`, what the backward would otherwise recompute -- the state at
+ * every chunk start (fp16 for bf16 inputs, fp32 for fp32 inputs; [chunks, H,
+ * d_v, d_k]) and, for bf16 with d = 128, the WY tiles X1 = Ahat diag(beta),
+ * X2 = lower(diag(gamma) Ahat diag(beta / gamma)) and Ahat = (I + diag(beta) N)^{-1}
+ * of every chunk, with N the strict lower triangle of K K^T (normalised keys)
+ * and gamma_r = exp(in-chunk prefix sum of g) (fp16 64 x 64 row-major tiles,
+ * [chunks, H, 3, 64, 64], after the states; onedev.kr FlashQLA talk summary,
+ * paragraph on the WY representation, which names these intra-chunk
+ * quantities).  The backward then starts at the reverse chain.  This trades
+ * memory for time (d = 128, bf16: 56 KB per chunk and head, 234 MB for 32
+ * heads x 8192 tokens); the pages recompute instead, and gdn_chunk_bwd keeps
+ * that form.
+ *  - gdn_saved_size: bytes of `saved` for this shape (0 on error).
+ *  - gdn_bwd_saved_workspace_size: workspace bytes of gdn_chunk_bwd_saved
+ *    (smaller than gdn_bwd_workspace_size by the recomputed regions).
+ *  - gdn_chunk_fwd_save: exactly gdn_chunk_fwd (same o and S_T) plus the
+ *    writes to `saved` (non-NULL, 16-byte aligned, >= gdn_saved_size bytes,
+ *    else GDN_ERR_INVALID_ARG / GDN_ERR_WORKSPACE before any launch).
+ *  - gdn_chunk_bwd_saved: exactly gdn_chunk_bwd, reading `saved` instead of
+ *    recomputing.  The shape (including cu_seqlens contents, flags and
+ *    scale), q, k, v, g, beta and S0 must be those of the forward that wrote
+ *    `saved`, and `saved` must not have been modified since; the library
+ *    cannot check this, and other inputs give gradients of another problem.
+ *    The segment plan (seg_chunks, GDN_SP_OFF) may differ between the two
+ *    calls: `saved` is indexed by chunk, not by segment.
+ */
+size_t gdn_saved_size(const gdn_shape *shape);
+size_t gdn_bwd_saved_workspace_size(const gdn_shape *shape);
+int gdn_chunk_fwd_save(const gdn_shape *shape,
+                       const void *q, const void *k, const void *v,
+                       const float *g, const float *beta,
+                       const float *S0, /* nullable */
+                       void *o, float *S_T, /* S_T nullable */
+                       void *saved, size_t saved_bytes,
+                       void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+int gdn_chunk_bwd_saved(const gdn_shape *shape,
+                        const void *q, const void *k, const void *v,
+                        const float *g, const float *beta,
+                        const float *S0,   /* nullable */
+                        const void *dO,
+                        const float *dS_T, /* nullable */
+                        void *dq, void *dk, void *dv, float *dg, float *dbeta,
+                        float *dS0,        /* required iff S0 != NULL */
+                        const void *saved, size_t saved_bytes,
+                        void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+
 /* Token-by-token (recurrent) forward for decoding a few tokens per sequence,
  * e.g. after a chunked prefill: for every sequence n < B, head h and token
  * t = 0 .. T-1 in order,

@@ -26,15 +26,22 @@ def rel_err(x, ref):
     return float(np.max(dev)) / rms
 
 
-def run_gpu(x, *, bwd=True, sp=True, window=True, seg_chunks=0, with_final=True):
-    o, ST = g.chunk_gated_delta_rule_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], with_final,
-                                         x["cu_seqlens"], x["scale"], x["l2norm"], sp=sp, window=window,
-                                         seg_chunks=seg_chunks)
+def run_gpu(x, *, bwd=True, sp=True, window=True, seg_chunks=0, with_final=True, saved=False, bwd_plan=None):
+    """Forward (+ backward) through the library.  saved=True: the forward keeps its per-chunk states
+    and WY tiles and the backward reads them; bwd_plan = dict(sp=, window=, seg_chunks=) gives the
+    backward another segment plan than the forward."""
+    res = g.chunk_gated_delta_rule_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], with_final,
+                                       x["cu_seqlens"], x["scale"], x["l2norm"], sp=sp, window=window,
+                                       seg_chunks=seg_chunks, save_context=saved)
+    o, ST = res[0], res[1]
+    ctx = res[2] if saved else None
     out = dict(o=o, S_T=ST)
     if bwd:
+        plan = dict(sp=sp, window=window, seg_chunks=seg_chunks)
+        plan.update(bwd_plan or {})
         dq, dk, dv, dg, db, dS0 = g.chunk_gated_delta_rule_bwd(
             x["q"], x["k"], x["v"], x["g"], x["beta"], x["dO"], x["S0"], x["dST"], x["cu_seqlens"], x["scale"],
-            x["l2norm"], sp=sp, window=window, seg_chunks=seg_chunks)
+            x["l2norm"], saved=ctx, **plan)
         out.update(dq=dq, dk=dk, dv=dv, dg=dg, dbeta=db, dS0=dS0)
     torch.cuda.synchronize()
     return out

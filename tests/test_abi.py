@@ -92,6 +92,46 @@ def test_workspace_checks(lib):
     assert lib.gdn_bwd_workspace_size(ctypes.byref(s)) > need   # per-chunk states for the backward
 
 
+def test_saved_context_sizes(lib):
+    """Saved context = fp16 chunk-start states + three fp16 64 x 64 WY tiles per (chunk, head) at
+    bf16, d = 128; the saved-context backward needs the recompute workspace minus exactly that."""
+    s = _shape(T=1000, H=3)
+    chunks = (1000 + 63) // 64
+    states = chunks * 3 * 128 * 128 * 2
+    tiles = chunks * 3 * 3 * 64 * 64 * 2
+    assert lib.gdn_saved_size(ctypes.byref(s)) == states + tiles
+    full = lib.gdn_bwd_workspace_size(ctypes.byref(s))
+    assert lib.gdn_bwd_saved_workspace_size(ctypes.byref(s)) == full - states - tiles
+    # fp32, d = 64: fp32 states, no WY tiles
+    s = _shape(T=1000, H=3, Dk=64, Dv=64, dtype=_lib.GDN_FP32)
+    assert lib.gdn_saved_size(ctypes.byref(s)) == chunks * 3 * 64 * 64 * 4
+    assert lib.gdn_saved_size(ctypes.byref(_shape(Dk=96, Dv=96))) == 0
+
+
+def test_saved_context_checks(lib):
+    s = _shape()
+    p, big = 0x10000, 1 << 40
+    need = lib.gdn_saved_size(ctypes.byref(s))
+
+    def fwd(saved, nbytes):
+        return lib.gdn_chunk_fwd_save(ctypes.byref(s), p, p, p, p, p, None, p, None, saved, nbytes, p, big, None)
+
+    def bwd(saved, nbytes, ws_bytes=big):
+        return lib.gdn_chunk_bwd_saved(ctypes.byref(s), p, p, p, p, p, None, p, None, p, p, p, p, p, None, saved,
+                                       nbytes, p, ws_bytes, None)
+
+    assert fwd(None, need) == _lib.GDN_ERR_INVALID_ARG
+    assert b"saved" in lib.gdn_last_error_string()
+    assert fwd(p, need - 1) == _lib.GDN_ERR_WORKSPACE
+    assert fwd(p + 8, need) == _lib.GDN_ERR_INVALID_ARG
+    assert bwd(None, need) == _lib.GDN_ERR_INVALID_ARG
+    assert bwd(p, need - 1) == _lib.GDN_ERR_WORKSPACE
+    assert bwd(p + 4, need) == _lib.GDN_ERR_INVALID_ARG
+    ws = lib.gdn_bwd_saved_workspace_size(ctypes.byref(s))
+    assert bwd(p, need, ws - 1) == _lib.GDN_ERR_WORKSPACE
+    assert b"workspace" in lib.gdn_last_error_string()
+
+
 def test_cu_seqlens_requires_B1(lib):
     s = _shape(B=2, cu_seqlens=0x10000, num_seqs=2)
     assert _fwd(lib, s) == _lib.GDN_ERR_INVALID_ARG

@@ -40,7 +40,7 @@ def _slice(x, n, h):
 @pytest.mark.parametrize("name,pairs", CASES, ids=[c[0] for c in CASES])
 def test_full_size_sampled(name, pairs):
     x = make_inputs(name, DEV)
-    got = run_gpu(x)
+    runs = {"recompute": run_gpu(x), "saved": run_gpu(x, saved=True)}
     if pairs is None:
         lens = np.array(x["seqlens"])
         pairs = [(int(lens.argmin()), 3), (int(lens.argmax()), 20)]
@@ -51,13 +51,14 @@ def test_full_size_sampled(name, pairs):
                             l2norm=x["l2norm"])
         rg = oracle.bwd(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["g"]), sl(x["beta"]), sl(x["dO"]), S0, None,
                         scale=x["scale"], l2norm=x["l2norm"])
-        errs = {"o": rel_err(sl(got["o"]), ro), "S_T": rel_err(got["S_T"][n:n + 1, h:h + 1], rS)}
-        for key in ("dq", "dk", "dv", "dg", "dbeta"):
-            errs[key] = rel_err(sl(got[key]), rg[key])
-        if S0 is not None:
-            errs["dS0"] = rel_err(got["dS0"][n:n + 1, h:h + 1], rg["dS0"])
-        bad = {k: v for k, v in errs.items() if not v <= TOL["bf16"]}
-        assert not bad, f"{name} seq {n} head {h}: {bad} (all {errs})"
+        for mode, got in runs.items():
+            errs = {"o": rel_err(sl(got["o"]), ro), "S_T": rel_err(got["S_T"][n:n + 1, h:h + 1], rS)}
+            for key in ("dq", "dk", "dv", "dg", "dbeta"):
+                errs[key] = rel_err(sl(got[key]), rg[key])
+            if S0 is not None:
+                errs["dS0"] = rel_err(got["dS0"][n:n + 1, h:h + 1], rg["dS0"])
+            bad = {k: v for k, v in errs.items() if not v <= TOL["bf16"]}
+            assert not bad, f"{name} ({mode}) seq {n} head {h}: {bad} (all {errs})"
 
 
 def test_homogeneity_full_prefill():
