@@ -28,7 +28,7 @@ from ._lib import (GDN_BF16, GDN_FP32, GDN_L2NORM_QK, GDN_SP_OFF, GDN_WINDOW_OFF
 
 __all__ = ["GdnShape", "make_shape", "gdn_chunk_fwd", "gdn_chunk_fwd_static", "gdn_chunk_bwd", "gdn_fwd_workspace_size",
            "gdn_bwd_workspace_size", "gdn_saved_size", "gdn_bwd_saved_workspace_size", "gdn_chunk_fwd_save",
-           "gdn_chunk_bwd_saved", "gdn_plan_query", "gdn_get_device_status", "gdn_profile_enable",
+           "gdn_chunk_bwd_saved", "gdn_plan_query", "gdn_get_device_status", "gdn_profile_enable", "gdn_profile_only",
            "gdn_profile_report",
            "chunk_gated_delta_rule_fwd", "chunk_gated_delta_rule_bwd", "chunk_gated_delta_rule",
            "GDN_L2NORM_QK", "GDN_SP_OFF", "GDN_WINDOW_OFF"]
@@ -152,6 +152,11 @@ def gdn_recurrent_fwd(shape: GdnShape, q, k, v, g, beta, S_in, o, S_out, stream=
 
 def gdn_profile_enable(on: bool) -> None:
     _check(_lib.load().gdn_profile_enable(int(bool(on))), "gdn_profile_enable")
+
+
+def gdn_profile_only(name: Optional[str]) -> None:
+    """Bracket only launches of kernel `name` (None: every launch) while profiling is on."""
+    _check(_lib.load().gdn_profile_only(name.encode() if name else None), "gdn_profile_only")
 
 
 def gdn_profile_report(reset: bool = True) -> dict:

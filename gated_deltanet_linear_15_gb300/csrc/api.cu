@@ -210,6 +210,7 @@ struct Profiler {
   std::vector<std::string> names;
   std::vector<double> total_ms;
   std::vector<long> count;
+  std::string only;  // bracket only launches of this name ("" = every launch)
 };
 Profiler g_prof;
 
@@ -220,6 +221,7 @@ struct ProfScope {
   ProfScope(const char *n, cudaStream_t s) : st(s), name(n) {
     std::lock_guard<std::mutex> lk(g_prof.mu);
     if (!g_prof.on || g_prof.used + 2 > (int)g_prof.pool.size()) return;
+    if (!g_prof.only.empty() && g_prof.only != n) return;
     idx = g_prof.used;
     g_prof.used += 2;
     cudaEventRecord(g_prof.pool[idx], st);
@@ -263,15 +265,15 @@ void prof_drain_locked() {
 // plan + gate scan, shared by both directions
 int prologue(const gdn_shape *s, const Layout &L, char *ws, const float *g, cudaStream_t st, Plan &pl) {
   pl = plan_of(L, ws);
-  int *status = reinterpret_cast<int *>(ws + L.off_status);
-  CK((int)cudaMemsetAsync(status, 0, 4, st));
+  int *status = reinterpret_cast<int *>(ws + L.off_status);  // [0] status word, [1]/[2] fix-up flags
   {
     PROF("plan");
     CK(launch_plan(pl, s->cu_seqlens, L.N, s->cu_seqlens ? s->T : L.Tseq, L.Lseg, L.S_max, L.CH_max, status, st));
   }
   {
     PROF("gate_scan");
-    CK(launch_gate_scan(pl, g, L.H, L.CH_max, reinterpret_cast<float *>(ws + L.off_gsum), status, st));
+    CK(launch_gate_scan(pl, g, L.H, L.CH_max, reinterpret_cast<float *>(ws + L.off_gsum), status, L.sp ? 1 : 0,
+                        L.Lseg, L.S_max, s->flags, st));
   }
   return GDN_OK;
 }
@@ -380,6 +382,7 @@ int forward_passes(const gdn_shape *s, const Layout &L, char *ws, FwdArgs fa, in
     fx.Lseg = L.Lseg;
     fx.flags = fa.flags;
     fx.reverse = 0;
+    fx.fixflag = fa.status + 1;
     PROF("fixup_fwd");
     CK(launch_fixup(fx, L.N, st));
   }
@@ -568,6 +571,7 @@ int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
     fx.Lseg = L.Lseg;
     fx.flags = s->flags;
     fx.reverse = 1;
+    fx.fixflag = ba.status + 2;
     PROF("fixup_bwd");
     CK(launch_fixup(fx, L.N, st));
   }
@@ -580,12 +584,14 @@ int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
   {
     PROF("bwd_local");
     if (bf && L.D == 128 && L.Ttot > 0) {
-      CUtensorMap maps[7];
+      CUtensorMap maps[10];
       if ((rc = qkv_map(&maps[0], q, L.Ttot, L.H)) || (rc = qkv_map(&maps[1], k, L.Ttot, L.H)) ||
           (rc = qkv_map(&maps[2], v, L.Ttot, L.H)) || (rc = qkv_map(&maps[3], dO, L.Ttot, L.H)) ||
           (rc = state_map(&maps[4], states, (long)L.CH_max * L.H * 128)) ||
           (rc = state_map(&maps[5], ws + L.off_dstates, (long)L.CH_max * L.H * 128)) ||
-          (rc = wy_map(&maps[6], wy ? wy : k, wy ? (long)L.CH_max * L.H * 3 * CH : 64)))
+          (rc = wy_map(&maps[6], wy ? wy : k, wy ? (long)L.CH_max * L.H * 3 * CH : 64)) ||
+          (rc = qkv_map(&maps[7], dq, L.Ttot, L.H)) || (rc = qkv_map(&maps[8], dk, L.Ttot, L.H)) ||
+          (rc = qkv_map(&maps[9], dv, L.Ttot, L.H)))
         return rc;
       CK(launch_bwd_local_tc(ba, maps, L.CH_max, st));
     } else {
@@ -774,6 +780,12 @@ int gdn_profile_enable(int on) {
   }
   if (!on) prof_drain_locked();
   g_prof.on = on != 0;
+  return GDN_OK;
+}
+
+int gdn_profile_only(const char *name) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  g_prof.only = name ? name : "";
   return GDN_OK;
 }
 

@@ -60,6 +60,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   ChainTcSmem &sm =
       *reinterpret_cast<ChainTcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
   const int s = blockIdx.x, h = blockIdx.y, role = blockIdx.z;
+  // pass A of a call in which no segment needs the exact fix-up (status[2], set after the gate scan)
+  if (a.pass == 0 && a.status && a.status[2] == 0) return;
   const int H = a.H;
   const int n = a.plan.seg_seq[s];
   if (n < 0) return;
@@ -486,7 +488,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 int launch_bwd_chain_tc(const BwdArgs &a, const CUtensorMap *maps, dim3 grid, cudaStream_t st) {
   const size_t smem = sizeof(ChainTcSmem) + 1024;
-  static_assert(sizeof(ChainTcSmem) + 1024 <= 232448, "shared memory budget");
+  static_assert(sizeof(ChainTcSmem) + 1024 <= 232448 - 256, "shared memory budget (the rest: static shared memory)");
   cudaError_t e = cudaFuncSetAttribute(bwd_chain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
   bwd_chain_tc_kernel<<<grid, NTHREADS, smem, st>>>(a, maps[0], maps[1], maps[2], maps[3]);

@@ -53,13 +53,14 @@ struct __align__(1024) LocalTcSmem {
   uint8_t wt[2 * HT];   // W^T [d_k][token], later dUt^T [d_v][token]
   uint8_t ut[2 * HT];   // Ut^T [d_v][token]
   float nf[CH * LN];
-  float g[CH], beta[CH], nq[CH], nk[CH];  // nq, nk hold reciprocal norms
-  Gates gt;
+  float g[2][CH], beta[2][CH];  // per item parity: the next item's gates are prepared during this one
+  float nq[CH], nk[CH];         // reciprocal norms
+  Gates gt[2];
   float ys[1152];
   float part[20][CH];   // per-token partial sums (reused per round)
-  float acc[12][CH];    // assembled per-token terms
+  float acc[7][CH];     // assembled per-token terms
   float red[LWARPS];
-  uint64_t bar_a, bar_b, bar_w, bar_mma;  // TMA: {K, Q, V, S0, dS}, {dO}, {X1, X2, Ahat}; tensor-core completion
+  uint64_t bar_a, bar_b, bar_w, bar_mma, bar_mma2;  // TMA: {K, Q, V, S0, dS}, {dO}, {X1, X2, Ahat}; tensor cores
   uint32_t tmem_base;
 };
 
@@ -114,7 +115,9 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     bwd_local_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
                         const __grid_constant__ CUtensorMap tms0, const __grid_constant__ CUtensorMap tmds,
-                        const __grid_constant__ CUtensorMap tmw, int n_items) {
+                        const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmdq,
+                        const __grid_constant__ CUtensorMap tmdk, const __grid_constant__ CUtensorMap tmdv,
+                        int n_items) {
   extern __shared__ unsigned char smraw[];
   LocalTcSmem &sm =
       *reinterpret_cast<LocalTcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
@@ -136,6 +139,7 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     mbar_init(u32(&sm.bar_b), 1);
     mbar_init(u32(&sm.bar_w), 1);
     mbar_init(u32(&sm.bar_mma), 1);
+    mbar_init(u32(&sm.bar_mma2), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == 0) {
@@ -147,12 +151,42 @@ __global__ void __launch_bounds__(LTHREADS, 1)
   fence_after();
   const uint32_t tm = sm.tmem_base;
   const uint32_t tl = (uint32_t)(wq * 32) << 16;
-  uint32_t phase = 0;
+  uint32_t phase = 0, phase2 = 0;
   auto mma_done = [&]() {
     const bool r = mbar_wait(u32(&sm.bar_mma), phase, err, 4);
     phase ^= 1;
     fence_after();
     return r;
+  };
+  auto mma2_done = [&]() {  // the input-only products issued with P1 (one commit per item)
+    const bool r = mbar_wait(u32(&sm.bar_mma2), phase2, err, 4);
+    phase2 ^= 1;
+    fence_after();
+    return r;
+  };
+  // A staged bf16 output tile (two swizzled [64 token][64 feature] halves at `stg`) to rows tok0.. of
+  // head h: one TMA store per half for a full chunk (thread 0), else coalesced 16-byte stores of the
+  // valid rows (all threads).  The caller fenced the staging writes for the async proxy and synced.
+  auto store_tile = [&](const CUtensorMap *map, void *gptr, const uint8_t *stg, int hh, int t0, int nv) {
+    if (nv == CH) {
+      if (tid == 0) {
+        tma_store_3d(map, 0, hh, t0, u32(stg));
+        tma_store_3d(map, 64, hh, t0, u32(stg + HT));
+        tma_store_commit();
+      }
+      return;
+    }
+    bf16 *gp = static_cast<bf16 *>(gptr);
+    for (int e = tid; e < CH * (D / 8); e += LTHREADS) {
+      const int r = e >> 4, cc = e & 15;
+      if (r < nv)
+        *reinterpret_cast<uint4 *>(gp + ((size_t)(t0 + r) * H + hh) * D + cc * 8) =
+            *reinterpret_cast<const uint4 *>(stg + (cc >> 3) * HT + r * 128 + (((cc & 7) ^ (r & 7)) << 4));
+    }
+  };
+  // bf16 element (token, feature) of such a staging tile
+  auto stg_at = [&](uint8_t *stg, int tkn, int f) {
+    return reinterpret_cast<bf16 *>(stg + (f >> 6) * HT + sw128_offset(tkn, f & 63));
   };
 
   // Work items (chunk gc, head h) = (item / H, item % H), strided over the persistent CTAs; chunks past
@@ -214,8 +248,21 @@ __global__ void __launch_bounds__(LTHREADS, 1)
   const int len = a.plan.seq_len[n];
   const int tok0 = a.plan.seq_bos[n] + lc * CH;
   const int nvalid = min(CH, len - lc * CH);
-  if (tid < 64) sm.g[tid] = tid < nvalid ? a.g[(size_t)(tok0 + tid) * H + h] : 0.f;
-  else if (tid < 128) sm.beta[tid - 64] = (tid - 64) < nvalid ? a.beta[(size_t)(tok0 + tid - 64) * H + h] : 0.f;
+  const int gbuf = it & 1;
+  Gates &G = sm.gt[gbuf];
+  float *const gbeta = sm.beta[gbuf];
+  if (it == 0) {  // later items had g, beta and their gates prepared during the previous item
+    if (tid < 64) sm.g[0][tid] = tid < nvalid ? a.g[(size_t)(tok0 + tid) * H + h] : 0.f;
+    else if (tid < 128) sm.beta[0][tid - 64] = (tid - 64) < nvalid ? a.beta[(size_t)(tok0 + tid - 64) * H + h] : 0.f;
+  }
+  float gb_next = 0.f;  // g (tid < 64) or beta (64 <= tid < 128) of the next item, stored mid-item
+  if (nitem < n_items && tid < 128) {
+    const int ngc = nitem / H, nh = nitem % H, nn = a.plan.chunk_seq[ngc];
+    const int nlc = ngc - a.plan.seq_chunk0[nn];
+    const int ntok0 = a.plan.seq_bos[nn] + nlc * CH, nnv = min(CH, a.plan.seq_len[nn] - nlc * CH);
+    const int r = tid & 63;
+    if (r < nnv) gb_next = tid < 64 ? a.g[(size_t)(ntok0 + r) * H + nh] : a.beta[(size_t)(ntok0 + r) * H + nh];
+  }
   {
     const bool ok = mbar_wait(u32(&sm.bar_a), it & 1, err, 8) && mbar_wait(u32(&sm.bar_b), it & 1, err, 8);
     pend_main = pend_do = false;
@@ -224,7 +271,7 @@ __global__ void __launch_bounds__(LTHREADS, 1)
       break;
     }
   }
-  if (warp == 0) gate_prefix(sm.g, sm.gt);
+  if (it == 0 && warp == 0) gate_prefix(sm.g[0], sm.gt[0]);
   // ---- prep: bf16 -> fp16 in place; q, k normalised (norms kept for the Jacobians); rows >= nvalid zero
 #pragma unroll 1
   for (int task = tid; task < 4 * 2 * CH; task += LTHREADS) {
@@ -269,7 +316,30 @@ __global__ void __launch_bounds__(LTHREADS, 1)
   fence_async_smem();
   __syncthreads();
 
-  // ---- P1: [K; Q] K^T -> T0
+  // Input-only products of the second round: W^T = K^T X1^T -> T1; U^T = V^T X2^T -> T2;
+  // Y = dS K^T -> T3; Qa = S0^T dO^T -> T5 (thread 0; committed to bar_mma2 by the caller)
+  auto issue_p2a = [&]() {
+    const uint32_t id = idesc_f16(128, 64, true, false);
+    const uint32_t kb = u32(sm.kq), vb = u32(sm.v), x1b = u32(sm.x1), x2b = u32(sm.x2);
+#pragma unroll 1
+    for (int kk = 0; kk < 4; ++kk) {
+      mma_f16(tm + T1, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(x1b + kk * 32, 16, 1024), id, kk > 0);
+      mma_f16(tm + T2, sdesc(vb + kk * 2048, HT, 1024), sdesc(x2b + kk * 32, 16, 1024), id, kk > 0);
+    }
+    const uint32_t id_kk = idesc_f16(128, 64, false, false);
+    const uint32_t id_mk = idesc_f16(128, 64, true, false);
+    const uint32_t dsb = u32(sm.ds), dob = u32(sm.dob), sb = u32(sm.s0);
+#pragma unroll 1
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
+      mma_f16(tm + T3, sdesc(dsb + aoff, 16, 1024), sdesc(kb + aoff, 16, 1024), id_kk, kk > 0);
+      mma_f16(tm + T5, sdesc(sb + kk * 2048, 2 * HT, 1024), sdesc(dob + (kk >> 2) * HT + (kk & 3) * 32, 16, 1024),
+              id_mk, kk > 0);
+    }
+  };
+
+  // ---- P1: [K; Q] K^T -> T0 (bar_mma); with the WY tiles at hand the input-only products follow at
+  //      once (bar_mma2) and run while R1 reads N and P out
   if (tid == 0) {
     fence_after();
     const uint32_t id = idesc_f16(128, 64, false, false), kb = u32(sm.kq);
@@ -279,6 +349,10 @@ __global__ void __launch_bounds__(LTHREADS, 1)
       mma_f16(tm + T0, sdesc(kb + off, 16, 1024), sdesc(kb + off, 16, 1024), id, kk > 0);
     }
     mma_commit(u32(&sm.bar_mma));
+    if (use_wy) {
+      if (mbar_wait(u32(&sm.bar_w), it & 1, err, 8)) issue_p2a();  // on failure every thread's wait below fails too
+      mma_commit(u32(&sm.bar_mma2));
+    }
   }
   __syncwarp();
   if (__syncthreads_or(!mma_done())) {
@@ -297,9 +371,9 @@ __global__ void __launch_bounds__(LTHREADS, 1)
       dst[1] = make_float4(v[4], v[5], v[6], v[7]);
     } else {
       const int r = row - 64;
-      const float gr = sm.gt.gp[r];
+      const float gr = G.gp[r];
       float y[8], rg[8];
-      ld8f(sm.gt.rgp + cb, rg);
+      ld8f(G.rgp + cb, rg);
 #pragma unroll
       for (int i = 0; i < 8; ++i) y[i] = cb + i <= r ? v[i] * gr * rg[i] : 0.f;
       st_chunk_f16(sm.p + chunk_off(r, cb), y);
@@ -309,15 +383,21 @@ __global__ void __launch_bounds__(LTHREADS, 1)
   fence_before();
   __syncthreads();
   if (!use_wy) {
-    wy_inverse<false, false>(sm.nf, LN, sm.beta, sm.ys, [&](int r, int c, float a0, float a1) {
-      const float b0 = sm.beta[c], b1 = sm.beta[c + 1], gr = sm.gt.gp[r];
+    wy_inverse<false, false>(sm.nf, LN, gbeta, sm.ys, [&](int r, int c, float a0, float a1) {
+      const float b0 = gbeta[c], b1 = gbeta[c + 1], gr = G.gp[r];
       const uint32_t off = sw128_offset(r, c);
       *reinterpret_cast<__half2 *>(sm.x1 + off) = __floats2half2_rn(a0 * b0, a1 * b1);
       *reinterpret_cast<__half2 *>(sm.x2 + off) =
-          __floats2half2_rn(c <= r ? a0 * b0 * (gr * sm.gt.rgp[c]) : 0.f,
-                            c + 1 <= r ? a1 * b1 * (gr * sm.gt.rgp[c + 1]) : 0.f);
+          __floats2half2_rn(c <= r ? a0 * b0 * (gr * G.rgp[c]) : 0.f,
+                            c + 1 <= r ? a1 * b1 * (gr * G.rgp[c + 1]) : 0.f);
       *reinterpret_cast<__half2 *>(sm.ah + off) = __floats2half2_rn(a0, a1);
     });
+    if (tid == 0) {
+      fence_after();
+      issue_p2a();
+      mma_commit(u32(&sm.bar_mma2));
+    }
+    __syncwarp();
   } else {
     const bool ok = mbar_wait(u32(&sm.bar_w), it & 1, err, 8);
     pend_wy = false;
@@ -326,36 +406,7 @@ __global__ void __launch_bounds__(LTHREADS, 1)
       break;
     }
   }
-
-  // ---- P2: W^T = K^T X1^T -> T1;  U^T = V^T X2^T -> T2;  and (needing only inputs and P)
-  //      P4: Y = dS K^T -> T3; Z = dO^T P -> T4; Qa = S0^T dO^T -> T5
-  if (tid == 0) {
-    fence_after();
-    const uint32_t id = idesc_f16(128, 64, true, false);
-    const uint32_t kb = u32(sm.kq), vb = u32(sm.v), x1b = u32(sm.x1), x2b = u32(sm.x2);
-#pragma unroll 1
-    for (int kk = 0; kk < 4; ++kk) {
-      mma_f16(tm + T1, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(x1b + kk * 32, 16, 1024), id, kk > 0);
-      mma_f16(tm + T2, sdesc(vb + kk * 2048, HT, 1024), sdesc(x2b + kk * 32, 16, 1024), id, kk > 0);
-    }
-    const uint32_t id_kk = idesc_f16(128, 64, false, false);
-    const uint32_t id_mm = idesc_f16(128, 64, true, true);
-    const uint32_t id_mk = idesc_f16(128, 64, true, false);
-    const uint32_t dsb = u32(sm.ds), dob = u32(sm.dob), pb = u32(sm.p), sb = u32(sm.s0);
-#pragma unroll 1
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
-      mma_f16(tm + T3, sdesc(dsb + aoff, 16, 1024), sdesc(kb + aoff, 16, 1024), id_kk, kk > 0);
-      mma_f16(tm + T5, sdesc(sb + kk * 2048, 2 * HT, 1024), sdesc(dob + (kk >> 2) * HT + (kk & 3) * 32, 16, 1024),
-              id_mk, kk > 0);
-    }
-#pragma unroll 1
-    for (int kk = 0; kk < 4; ++kk)
-      mma_f16(tm + T4, sdesc(dob + kk * 2048, HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id_mm, kk > 0);
-    mma_commit(u32(&sm.bar_mma));
-  }
-  __syncwarp();
-  if (__syncthreads_or(!mma_done())) {
+  if (__syncthreads_or(!mma2_done())) {
     failed = true;
     break;
   }
@@ -366,7 +417,7 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     float v[8];
     tmem_ld8(tm + tl + T1 + cb, v);
     float gm[8];
-    ld8f(sm.gt.gam + cb, gm);
+    ld8f(G.gam + cb, gm);
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] *= gm[i];
     st_chunk_f16(sm.wt + chunk_off(row, cb), v);
@@ -375,7 +426,24 @@ __global__ void __launch_bounds__(LTHREADS, 1)
   fence_async_smem();
   __syncthreads();
 
-  {  // <dS, S0> over the whole state (both tiles share one layout, so compare byte positions)
+  // ---- Z = dO^T P -> T4 and P3: Ut^T = U^T - S0 W^T (T2), one commit
+  if (tid == 0) {
+    fence_after();
+    const uint32_t id_mm = idesc_f16(128, 64, true, true);
+    const uint32_t dob = u32(sm.dob), pb = u32(sm.p);
+#pragma unroll 1
+    for (int kk = 0; kk < 4; ++kk)
+      mma_f16(tm + T4, sdesc(dob + kk * 2048, HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id_mm, kk > 0);
+    const uint32_t id = idesc_f16(128, 64, false, true, true);
+    const uint32_t sb = u32(sm.s0), wb = u32(sm.wt);
+#pragma unroll 1
+    for (int kk = 0; kk < 8; ++kk)
+      mma_f16(tm + T2, sdesc(sb + (kk >> 2) * 2 * HT + (kk & 3) * 32, 16, 1024), sdesc(wb + kk * 2048, 2 * HT, 1024),
+              id, true);
+    mma_commit(u32(&sm.bar_mma));
+  }
+  __syncwarp();
+  {  // meanwhile: <dS, S0> over the whole state (both tiles share one layout, so compare byte positions)
     float acc = 0.f;
     const uint4 *A4 = reinterpret_cast<const uint4 *>(sm.s0), *B4 = reinterpret_cast<const uint4 *>(sm.ds);
 #pragma unroll 2
@@ -391,19 +459,6 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     acc = warp_sum(acc);
     if (lane == 0) sm.red[warp] = acc;
   }
-
-  // ---- P3: Ut^T = U^T - S0 W^T  (T2)
-  if (tid == 0) {
-    fence_after();
-    const uint32_t id = idesc_f16(128, 64, false, true, true);
-    const uint32_t sb = u32(sm.s0), wb = u32(sm.wt);
-#pragma unroll 1
-    for (int kk = 0; kk < 8; ++kk)
-      mma_f16(tm + T2, sdesc(sb + (kk >> 2) * 2 * HT + (kk & 3) * 32, 16, 1024), sdesc(wb + kk * 2048, 2 * HT, 1024),
-              id, true);
-    mma_commit(u32(&sm.bar_mma));
-  }
-  __syncwarp();
   if (__syncthreads_or(!mma_done())) {
     failed = true;
     break;
@@ -419,7 +474,7 @@ __global__ void __launch_bounds__(LTHREADS, 1)
       tmem_ld8(tm + tl + T2 + cb, u);
       st_chunk_f16(sm.ut + chunk_off(row, cb), u);
       float cd[8];
-      ld8f(sm.gt.cdec + cb, cd);
+      ld8f(G.cdec + cb, cd);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float du = cd[i] * y[i] + z[i];
@@ -476,7 +531,7 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     // dP rows (lanes 0-63): Z = dP * P row sums (thread-local) and column sums; dPm over P
     if (row < 64) {
       const int r = row;
-      const float gr = sm.gt.gp[r];
+      const float gr = G.gp[r];
       float rs = 0.f, cs = 0.f;
 #pragma unroll 1
       for (int q4 = 0; q4 < 2; ++q4) {
@@ -487,7 +542,7 @@ __global__ void __launch_bounds__(LTHREADS, 1)
         const uint4 raw = *reinterpret_cast<const uint4 *>(pp);
         const __half *ph = reinterpret_cast<const __half *>(&raw);
 float rg[8];
-        ld8f(sm.gt.rgp + cb, rg);
+        ld8f(G.rgp + cb, rg);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float dpv = v[i];
@@ -510,14 +565,13 @@ float rg[8];
       float v[8];
       tmem_ld8(tm + tl + T1 + cb, v);
       float gm[8];
-      ld8f(sm.gt.gam + cb, gm);
+      ld8f(G.gam + cb, gm);
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[i] *= gm[i];
       st_chunk_f16(sm.s0 + chunk_off(row, cb), v);
     }
     // dV^T (lanes d_v, columns token): stage bf16 dv[token][d_v] in dob (dO is dead); <dV, v>
     {
-      bf16 *stg = reinterpret_cast<bf16 *>(sm.dob);
       float t = 0.f;
 #pragma unroll 1
       for (int q4 = 0; q4 < 2; ++q4) {
@@ -527,7 +581,7 @@ float rg[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int tkn = cb + i;
-          stg[tkn * D + row] = __float2bfloat16_rn(v[i]);
+          *stg_at(sm.dob, tkn, row) = __float2bfloat16_rn(v[i]);
           sv[i] = v[i] * ld_f16(sm.v, tkn, row, HT);
         }
         const float a = colsum8(sv);
@@ -540,12 +594,7 @@ float rg[8];
   fence_async_smem();
   __syncthreads();
   {
-    bf16 *dvg = static_cast<bf16 *>(a.dv);
-    const uint4 *stg = reinterpret_cast<const uint4 *>(sm.dob);
-    for (int e = tid; e < CH * (D / 8); e += LTHREADS) {
-      const int r = e >> 4, cc = e & 15;
-      if (r < nvalid) *reinterpret_cast<uint4 *>(dvg + ((size_t)(tok0 + r) * H + h) * D + cc * 8) = stg[e];
-    }
+    store_tile(&tmdv, a.dv, sm.dob, h, tok0, nvalid);
     if (tid < 64) {
       sm.acc[2][tid] = sm.part[16][tid] + sm.part[17][tid] + sm.part[18][tid] + sm.part[19][tid];  // row sums of dP * P
       sm.acc[3][tid] = sm.part[10][tid] + sm.part[11][tid];  // column sums of dP * P
@@ -556,6 +605,7 @@ float rg[8];
 
   // ---- P6: Qb = K^T dPm^T -> T7;  M1 = dW' K^T -> T3;  M2 = dUt V^T -> T4
   if (tid == 0) {
+    tma_store_wait_read();  // the dv tile store has read dob (the dq staging below rewrites it)
     fence_after();
     const uint32_t id_mk = idesc_f16(128, 64, true, false);
     const uint32_t kb = u32(sm.kq), pb = u32(sm.p), dwb = u32(sm.s0), dub = u32(sm.wt), vb = u32(sm.v);
@@ -592,7 +642,7 @@ float rg[8];
         tmem_ld8(tm + tl + T5 + cb, qa);
         tmem_ld8(tm + tl + T7 + cb, qb);
         float gm[8];
-        ld8f(sm.gt.gam + cb, gm);
+        ld8f(G.gam + cb, gm);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int tkn = cb + i;
@@ -613,7 +663,7 @@ float rg[8];
     // M1, M2 (lanes 0-63 = r): dAhat = beta_i (M1 + Gamma M2); beta column sums colsum_i(Ahat (M1 + Gamma M2))
     if (row < 64) {
       const int r = row;
-      const float gr = sm.gt.gp[r];
+      const float gr = G.gp[r];
       float cs = 0.f;
 #pragma unroll 1
       for (int q4 = 0; q4 < 2; ++q4) {
@@ -624,8 +674,8 @@ float rg[8];
         const uint4 raw = *reinterpret_cast<const uint4 *>(sm.ah + chunk_off(r, cb));
         const __half *hh = reinterpret_cast<const __half *>(&raw);
         float rg[8], bt[8];
-        ld8f(sm.gt.rgp + cb, rg);
-        ld8f(sm.beta + cb, bt);
+        ld8f(G.rgp + cb, rg);
+        ld8f(gbeta + cb, bt);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int col = cb + i;
@@ -641,7 +691,6 @@ float rg[8];
     }
     __syncthreads();
     // dq raw = (scale dq^ - q^ (q^ . dq^) / scale) / |q|   (or scale dq^ without normalisation)
-    bf16 *stg = reinterpret_cast<bf16 *>(sm.dob);
     const float rscale = 1.f / a.scale;
 #pragma unroll 1
     for (int q4 = 0; q4 < 2; ++q4) {
@@ -650,7 +699,7 @@ float rg[8];
       tmem_ld8(tm + tl + T5 + cb, qa);
       tmem_ld8(tm + tl + T7 + cb, qb);
       float gm[8], dt[8], nqv[8];
-      ld8f(sm.gt.gam + cb, gm);
+      ld8f(G.gam + cb, gm);
       if (l2) {
         float p0[8], p1[8], p2[8], p3[8];
         ld8f(sm.part[4] + cb, p0);
@@ -672,7 +721,7 @@ float rg[8];
         } else {
           o = a.scale * dq;
         }
-        stg[tkn * D + row] = __float2bfloat16_rn(o);
+        *stg_at(sm.dob, tkn, row) = __float2bfloat16_rn(o);
       }
     }
   }
@@ -680,21 +729,20 @@ float rg[8];
   fence_async_smem();
   __syncthreads();
   {
-    bf16 *dqg = static_cast<bf16 *>(a.dq);
-    const uint4 *stg = reinterpret_cast<const uint4 *>(sm.dob);
-    for (int e = tid; e < CH * (D / 8); e += LTHREADS) {
-      const int r = e >> 4, cc = e & 15;
-      if (r < nvalid) *reinterpret_cast<uint4 *>(dqg + ((size_t)(tok0 + r) * H + h) * D + cc * 8) = stg[e];
-    }
+    store_tile(&tmdq, a.dq, sm.dob, h, tok0, nvalid);
     if (tid < 64) {
       sm.acc[5][tid] = sm.part[0][tid] + sm.part[1][tid] + sm.part[2][tid] + sm.part[3][tid];  // gam <dO S0, q>
       sm.acc[6][tid] = sm.part[8][tid] + sm.part[9][tid];                                      // beta col terms
     }
+    if (tid < 128) (tid < 64 ? sm.g[gbuf ^ 1] : sm.beta[gbuf ^ 1])[tid & 63] = gb_next;  // next item's g, beta
   }
   fence_async_smem();
   __syncthreads();
   if (nitem < n_items) {  // dO of the next item into its (now free) buffer
-    if (tid == 0) issue_do(nitem);
+    if (tid == 0) {
+      tma_store_wait_read();  // the dq tile store has read dob
+      issue_do(nitem);
+    }
     pend_do = true;
   }
 
@@ -709,6 +757,7 @@ float rg[8];
     mma_commit(u32(&sm.bar_mma));
   }
   __syncwarp();
+  if (warp == 1 && nitem < n_items) gate_prefix(sm.g[gbuf ^ 1], sm.gt[gbuf ^ 1]);  // next item's gates, under P7
   if (__syncthreads_or(!mma_done())) {
     failed = true;
     break;
@@ -742,7 +791,7 @@ float rg[8];
   }
   if (row < 64) {  // R8: dN[r][i] = beta_r dT_ri (i < r), zero elsewhere; beta row sums of dT * N
     const int r = row;
-    const float br = sm.beta[r];
+    const float br = gbeta[r];
     uint8_t *sg = sm.v + HT;
     float rb = 0.f;
 #pragma unroll 1
@@ -803,7 +852,7 @@ float rg[8];
         tmem_ld8(tm + tl + T3 + cb, ka);
         tmem_ld8(tm + tl + T2 + cb, kbv);
         float cd[8];
-        ld8f(sm.gt.cdec + cb, cd);
+        ld8f(G.cdec + cb, cd);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int tkn = cb + i;
@@ -815,7 +864,7 @@ float rg[8];
       if (lane < 16) sm.part[wq][c0 + lane] = t2;
     }
     __syncthreads();
-    bf16 *stg = reinterpret_cast<bf16 *>(sm.x2);  // x2 + ah (16 KB, both dead after P8)
+    uint8_t *const stg = sm.x2;  // x2 + ah (16 KB, both dead after P8)
 #pragma unroll 1
     for (int q4 = 0; q4 < 2; ++q4) {
       const int cb = c0 + q4 * 8;
@@ -823,7 +872,7 @@ float rg[8];
       tmem_ld8(tm + tl + T3 + cb, ka);
       tmem_ld8(tm + tl + T2 + cb, kbv);
       float cd[8], dt[8], nkv[8];
-      ld8f(sm.gt.cdec + cb, cd);
+      ld8f(G.cdec + cb, cd);
       if (l2) {
         float p0[8], p1[8], p2[8], p3[8];
         ld8f(sm.part[0] + cb, p0);
@@ -839,20 +888,14 @@ float rg[8];
         const int tkn = cb + i;
         float o = ka[i] + cd[i] * kbv[i];
         if (l2) o = (o - ld_f16(sm.wt, tkn, row, HT) * dt[i]) * nkv[i];
-        stg[tkn * D + row] = __float2bfloat16_rn(o);
+        *stg_at(stg, tkn, row) = __float2bfloat16_rn(o);
       }
     }
   }
   fence_before();
+  fence_async_smem();
   __syncthreads();
-  {
-    bf16 *dkg = static_cast<bf16 *>(a.dk);
-    const uint4 *stg = reinterpret_cast<const uint4 *>(sm.x2);
-    for (int e = tid; e < CH * (D / 8); e += LTHREADS) {
-      const int r = e >> 4, cc = e & 15;
-      if (r < nvalid) *reinterpret_cast<uint4 *>(dkg + ((size_t)(tok0 + r) * H + h) * D + cc * 8) = stg[e];
-    }
-  }
+  store_tile(&tmdk, a.dk, sm.x2, h, tok0, nvalid);
   // ---- gate and beta gradients
   if (warp == 0) {
     float dGv[2];
@@ -860,14 +903,14 @@ float rg[8];
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const int r = lane + 32 * t;
-      const float y = sm.gt.cdec[r] * sm.acc[0][r];
+      const float y = G.cdec[r] * sm.acc[0][r];
       sumy += y;
       dGv[t] = sm.acc[1][r] + sm.acc[2][r] - sm.acc[3][r] + sm.acc[5][r] - sm.acc[4][r] - y;
     }
     sumy = warp_sum(sumy);
     float red = 0.f;
     for (int i = 0; i < LWARPS; ++i) red += sm.red[i];
-    if (lane == 31) dGv[1] += sumy + sm.gt.gamC * red;
+    if (lane == 31) dGv[1] += sumy + G.gamC * red;
     float hi = dGv[1], lo = dGv[0];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -889,6 +932,7 @@ float rg[8];
     }
   }
   __syncthreads();  // the next item rewrites the per-token scratch read above
+  if (tid == 0) tma_store_wait_read();  // the dk tile store has read x2 / ah (rewritten by the next item)
   if (use_wy && nitem < n_items) {  // X1, X2, Ahat of the next item (x2/ah held the dk staging until now)
     if (tid == 0) issue_wy(nitem);
     pend_wy = true;
@@ -900,6 +944,7 @@ float rg[8];
     if (pend_do) mbar_wait(u32(&sm.bar_b), (it + 1) & 1, err, 8);
     if (pend_wy) mbar_wait(u32(&sm.bar_w), it & 1, err, 8);  // issued for the item of iteration it
   }
+  if (tid == 0) tma_store_wait_all();  // output tiles written before the CTA leaves
   fence_before();
   __syncthreads();
   fence_after();
@@ -911,7 +956,7 @@ size_t bwd_local_tc_smem_bytes() { return sizeof(LocalTcSmem) + 1024; }
 int launch_bwd_local_tc(const BwdArgs &a, const CUtensorMap *maps, int CH_max, cudaStream_t st) {
   if (CH_max == 0) return 0;
   const size_t smem = bwd_local_tc_smem_bytes();
-  static_assert(sizeof(LocalTcSmem) + 1024 <= 232448, "shared memory budget");
+  static_assert(sizeof(LocalTcSmem) + 1024 <= 232448 - 256, "shared memory budget (the rest: static shared memory)");
   cudaError_t e = cudaFuncSetAttribute(bwd_local_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
   static int sms = 0;
@@ -923,7 +968,7 @@ int launch_bwd_local_tc(const BwdArgs &a, const CUtensorMap *maps, int CH_max, c
   const int n_items = CH_max * a.H;
   const int grid = n_items < sms ? n_items : sms;  // persistent: one CTA per SM
   bwd_local_tc_kernel<<<grid, LTHREADS, smem, st>>>(a, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
-                                                    maps[6], n_items);
+                                                    maps[6], maps[7], maps[8], maps[9], n_items);
   return (int)cudaGetLastError();
 }
 

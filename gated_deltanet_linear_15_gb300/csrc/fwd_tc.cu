@@ -82,6 +82,8 @@ __global__ void __launch_bounds__(FT, 1)
   TcSmem &sm = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
 
   const int s = blockIdx.x, h = blockIdx.y, role = blockIdx.z;
+  // pass A of a call in which no segment needs the exact fix-up (status[1], set after the gate scan)
+  if (a.pass == 0 && a.status && a.status[1] == 0) return;
   const int H = a.H;
   const int n = a.plan.seg_seq[s];
   if (n < 0) return;
@@ -581,7 +583,7 @@ size_t fwd_tc_smem_bytes() { return sizeof(TcSmem) + 1024; }
 int launch_fwd_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                   const CUtensorMap &tw, const CUtensorMap &ts, dim3 grid, cudaStream_t st) {
   const size_t smem = fwd_tc_smem_bytes();
-  static_assert(sizeof(TcSmem) + 1024 <= 232448, "shared memory budget");
+  static_assert(sizeof(TcSmem) + 1024 <= 232448 - 256, "shared memory budget (the rest: static shared memory)");
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
   fwd_tc_kernel<<<grid, FT, smem, st>>>(a, tq, tk, tv, tw, ts);

@@ -57,6 +57,7 @@ struct FixupArgs {
   int H, D, Lseg;
   unsigned flags;
   int reverse;
+  const int *fixflag;  // nonzero iff some segment of this direction needs the fix-up (NULL: always run)
 };
 
 // WY tiles of every (chunk, head): fp16 [CH_max, H, 3, 64, 64] = X1, X2, Ahat (row-major)
@@ -83,8 +84,10 @@ struct RecArgs {
 
 int launch_plan(const Plan &p, const int *cu, int N, int T, int Lseg, int S_max, int CH_max, int *status,
                 cudaStream_t st);
-int launch_gate_scan(const Plan &p, const float *g, int H, int CH_max, float *gsum, int *status, cudaStream_t st);
+int launch_gate_scan(const Plan &p, const float *g, int H, int CH_max, float *gsum, int *status, int modes, int Lseg,
+                     int S_max, unsigned flags, cudaStream_t st);
 int launch_fixup(const FixupArgs &a, int N, cudaStream_t st);
+
 int launch_fwd_chunk(const FwdArgs &a, bool is_bf16, int D, dim3 grid, cudaStream_t st);
 // tcgen05 forward for bf16 inputs and d = 128; q, k, v tensor maps over [tokens, H, 128] with a 64 x 1 x 64 box;
 // tw: the WY tiles as [rows, 64] fp16 with a 64 x 64 box (used when a.wy != NULL)

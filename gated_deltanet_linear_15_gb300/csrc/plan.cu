@@ -24,6 +24,8 @@ __global__ void plan_kernel(Plan p, const int *cu, int N, int T, int Lseg, int S
   __shared__ int carry_c, carry_s, bad;
   __shared__ int wsum_c[32], wsum_s[32];
   const int tid = threadIdx.x, nt = blockDim.x;
+  if (tid < 4 && status) status[tid] = 0;  // status word and the fix-up flags of this call
+  __syncthreads();
   if (tid == 0) {
     carry_c = 0;
     carry_s = 0;
@@ -136,46 +138,114 @@ int launch_plan(const Plan &p, const int *cu, int N, int T, int Lseg, int S_max,
   return (int)cudaGetLastError();
 }
 
-// One block per global chunk, one warp per head (looping): gsum[c, h] = sum of g
-// over the chunk's tokens; status bit 0 if the centred in-chunk prefix leaves
-// the range of the gamma factoring.
-__global__ void gate_scan_kernel(Plan p, const float *g, int H, float *gsum, int *status) {
+// One block per global chunk: the chunk's log-gates of 32 heads at a time are
+// staged in shared memory with coalesced row loads (tokens are rows of H gates),
+// then one warp per head scans its 64 values: gsum[c, h] = sum of g over the
+// chunk's tokens; status bit 0 if the centred in-chunk prefix leaves the range
+// of the gamma factoring.
+__device__ void fixup_modes(const Plan &p, const float *gsum, int H, int Lseg, int S_max, unsigned flags, int *status,
+                            int i0, int stride);
+
+// With modes != 0 (a call with segments) the last block to finish also runs the fix-up mode scan
+// over every (segment, head) (status[3] counts finished blocks; the plan kernel zeroed it).
+__global__ void __launch_bounds__(256) gate_scan_kernel(Plan p, const float *g, int H, float *gsum, int *status,
+                                                        int modes, int Lseg, int S_max, unsigned flags) {
+  __shared__ float tile[CH][33];
+  __shared__ int last;
   const int c = blockIdx.x;
   const int n = p.chunk_seq[c];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (n < 0) {
     for (int h = threadIdx.x; h < H; h += blockDim.x) gsum[(size_t)c * H + h] = 0.f;
-    return;
-  }
+  } else {
   const int lc = c - p.seq_chunk0[n];
   const long tok0 = (long)p.seq_bos[n] + (long)lc * CH;
   const int nvalid = min(CH, p.seq_len[n] - lc * CH);
-  for (int h = warp; h < H; h += blockDim.x / 32) {
-    float a = lane < nvalid ? g[(size_t)(tok0 + lane) * H + h] : 0.f;
-    float b = lane + 32 < nvalid ? g[(size_t)(tok0 + lane + 32) * H + h] : 0.f;
-    for (int o = 1; o < 32; o <<= 1) {
-      const float ya = __shfl_up_sync(0xffffffffu, a, o), yb = __shfl_up_sync(0xffffffffu, b, o);
-      if (lane >= o) {
-        a += ya;
-        b += yb;
+  for (int h0 = 0; h0 < H; h0 += 32) {
+    const int hh = h0 + lane;
+    for (int r = warp; r < CH; r += 8) tile[r][lane] = (r < nvalid && hh < H) ? g[(size_t)(tok0 + r) * H + hh] : 0.f;
+    __syncthreads();
+    for (int hl = warp; hl < 32 && h0 + hl < H; hl += 8) {
+      float a = tile[lane][hl], b = tile[lane + 32][hl];
+      for (int o = 1; o < 32; o <<= 1) {
+        const float ya = __shfl_up_sync(0xffffffffu, a, o), yb = __shfl_up_sync(0xffffffffu, b, o);
+        if (lane >= o) {
+          a += ya;
+          b += yb;
+        }
+      }
+      const float Gmid = __shfl_sync(0xffffffffu, a, 31);
+      b += Gmid;
+      const float Glast = __shfl_sync(0xffffffffu, b, 31);
+      float rng = fmaxf(fabsf(a - Gmid), fabsf(b - Gmid));
+      for (int o = 16; o > 0; o >>= 1) rng = fmaxf(rng, __shfl_xor_sync(0xffffffffu, rng, o));
+      if (lane == 0) {
+        gsum[(size_t)c * H + h0 + hl] = Glast;
+        if (rng > FACTOR_RANGE && status) atomicOr(status, 1);
       }
     }
-    const float Gmid = __shfl_sync(0xffffffffu, a, 31);
-    b += Gmid;
-    const float Glast = __shfl_sync(0xffffffffu, b, 31);
-    float rng = fmaxf(fabsf(a - Gmid), fabsf(b - Gmid));
-    for (int o = 16; o > 0; o >>= 1) rng = fmaxf(rng, __shfl_xor_sync(0xffffffffu, rng, o));
-    if (lane == 0) {
-      gsum[(size_t)c * H + h] = Glast;
-      if (rng > FACTOR_RANGE && status) atomicOr(status, 1);
-    }
+    __syncthreads();
   }
+  }
+  if (!modes) return;
+  // last block: every block's gsum writes are visible once it has fenced and counted itself
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(status + 3, 1) == (int)gridDim.x - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  fixup_modes(p, gsum, H, Lseg, S_max, flags, status, threadIdx.x, blockDim.x);
 }
 
-int launch_gate_scan(const Plan &p, const float *g, int H, int CH_max, float *gsum, int *status, cudaStream_t st) {
+int launch_gate_scan(const Plan &p, const float *g, int H, int CH_max, float *gsum, int *status, int modes, int Lseg,
+                     int S_max, unsigned flags, cudaStream_t st) {
   if (CH_max == 0) return 0;
-  gate_scan_kernel<<<CH_max, 256, 0, st>>>(p, g, H, gsum, status);
+  gate_scan_kernel<<<CH_max, 256, 0, st>>>(p, g, H, gsum, status, modes, Lseg, S_max, flags);
   return (int)cudaGetLastError();
+}
+
+// Does any segment start (forward) or end (reverse) need the exact fix-up?  status[1] / status[2]
+// become nonzero if so; the pass-A launches and the fix-ups of a direction without any such segment
+// return at once.  (segment, head) pairs i0, i0 + stride, ...; gsum read through L2 (other blocks
+// wrote it in this launch).
+__device__ void fixup_modes(const Plan &p, const float *gsum, int H, int Lseg, int S_max, unsigned flags, int *status,
+                            int i0, int stride) {
+  const bool window = !(flags & kFlagWindowOff);
+  bool fwd_fix = false, bwd_fix = false;
+  for (int i = i0; i < S_max * H; i += stride) {
+    const int s = i / H, h = i % H;
+    const int n = __ldcg(p.seg_seq + s);
+    if (n < 0) continue;
+    const int j = s - __ldcg(p.seq_seg0 + n), nseg = __ldcg(p.seq_nseg + n), chunk0 = __ldcg(p.seq_chunk0 + n);
+    const int nchunks = (__ldcg(p.seq_len + n) + CH - 1) / CH;
+    const int cbeg = j * Lseg, cend = min((j + 1) * Lseg, nchunks);
+    // the start-mode rules of the chunk kernels, on L2-coherent loads of gsum
+    if (j > 0) {
+      bool warm = false;
+      if (window) {
+        float acc = 0.f;
+        for (int ww = 1; ww <= WMAX && ww <= cbeg && !warm; ++ww) {
+          acc += __ldcg(gsum + (size_t)(chunk0 + cbeg - ww) * H + h);
+          warm = acc <= LN_EPS_WINDOW;
+        }
+      }
+      fwd_fix |= !warm;
+    }
+    if (j < nseg - 1) {
+      bool warm = false;
+      if (window) {
+        float acc = 0.f;
+        for (int ww = 1; ww <= WMAX && cend + ww <= nchunks && !warm; ++ww) {
+          acc += __ldcg(gsum + (size_t)(chunk0 + cend + ww - 1) * H + h);
+          warm = acc <= LN_EPS_WINDOW;
+        }
+      }
+      bwd_fix |= !warm;
+    }
+  }
+  if (fwd_fix) atomicOr(status + 1, 1);
+  if (bwd_fix) atomicOr(status + 2, 1);
 }
 
 // grid (D / FIX_ROWS, H, N); FIX_ROWS rows of the state per CTA, 256 threads.
@@ -186,6 +256,7 @@ __global__ void __launch_bounds__(256, 4) fixup_kernel(FixupArgs a) {
   __shared__ float cur[FIX_ROWS][D];
   const int rb = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
   const int H = a.H;
+  if (a.fixflag && *a.fixflag == 0) return;  // no segment of this direction needs the exact fix-up
   const int nseg = a.plan.seq_nseg[n];
   if (nseg <= 1) return;
   const int seg0 = a.plan.seq_seg0[n], chunk0 = a.plan.seq_chunk0[n];

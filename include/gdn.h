@@ -238,6 +238,10 @@ int gdn_plan_query(const gdn_shape *shape, int *seg_chunks, int *max_segments, i
  * returning the full report length; reset != 0 clears the totals. */
 int gdn_profile_enable(int on);
 int gdn_profile_report(char *buf, size_t len, int reset);
+/* Restrict the bracketing to launches of one kernel name as it appears in the
+ * report (NULL or "" = every launch), so that a timed loop carries the events of
+ * the kernel it measures and no others. */
+int gdn_profile_only(const char *name);
 
 const char *gdn_status_string(int status);
 const char *gdn_last_error_string(void); /* thread-local, "" if none */
