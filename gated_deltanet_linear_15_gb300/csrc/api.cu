@@ -55,10 +55,11 @@ struct Layout {
   size_t off_E = 0, off_M = 0, off_S = 0;     // forward fix-up buffers
   size_t off_states = 0, off_dstates = 0;   // backward per-chunk states
   size_t off_F = 0, off_R = 0, off_dS = 0;  // reverse fix-up buffers
-  size_t off_wy = 0, wy_bytes = 0;          // backward WY tiles (bf16, d = 128)
+  size_t off_t64 = 0, off_t128 = 0;        // recomputed chunk context tiles (bf16, d = 128)
+  size_t t64_bytes = 0, t128_bytes = 0;
   size_t states_bytes = 0;                  // per-chunk start states
   size_t bwd_saved_total = 0;               // backward workspace when the forward saved its context
-  size_t saved_off_wy = 0, saved_total = 0; // saved context: [states][WY tiles]
+  size_t saved_off_t64 = 0, saved_off_t128 = 0, saved_total = 0;  // saved context: [states][t64][t128]
   size_t fwd_total = 0, bwd_total = 0;
 };
 
@@ -157,12 +158,17 @@ int make_layout(const gdn_shape *s, Layout &L) {
   L.bwd_saved_total = off;
   L.off_states = off;
   off += L.states_bytes;
-  L.off_wy = off;
-  L.wy_bytes = (s->dtype == GDN_BF16 && L.D == 128) ? (size_t)L.CH_max * L.H * 3 * CH * CH * 2 : 0;
-  off = align256(off + L.wy_bytes);
+  const bool tiles = s->dtype == GDN_BF16 && L.D == 128;
+  L.t64_bytes = tiles ? align256((size_t)L.CH_max * L.H * T64_TILES * CH * CH * 2) : 0;
+  L.t128_bytes = tiles ? align256((size_t)L.CH_max * L.H * T128_TILES * 128 * CH * 2) : 0;
+  L.off_t64 = off;
+  off += L.t64_bytes;
+  L.off_t128 = off;
+  off += L.t128_bytes;
   L.bwd_total = off;
-  L.saved_off_wy = L.states_bytes;
-  L.saved_total = align256(L.states_bytes + L.wy_bytes);
+  L.saved_off_t64 = L.states_bytes;
+  L.saved_off_t128 = L.states_bytes + L.t64_bytes;
+  L.saved_total = L.states_bytes + L.t64_bytes + L.t128_bytes;
   return GDN_OK;
 }
 
@@ -326,13 +332,14 @@ int state_map(CUtensorMap *m, const void *ptr, long rows) {
   return GDN_OK;
 }
 
-// WY tiles: fp16 [rows, 64] (three 64-row tiles per (chunk, head)), box = 64 x 64, 128-byte swizzle
-int wy_map(CUtensorMap *m, const void *ptr, long rows) {
+// 64-column fp16 tiles [rows, 64], box = 64 columns x `box_rows` rows, 128-byte swizzle (the t64 tiles with
+// 64-row boxes, the t128 tiles with 128-row boxes)
+int tile_map(CUtensorMap *m, const void *ptr, long rows, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   cuuint64_t dims[3] = {64, (cuuint64_t)rows, 1};
   cuuint64_t strides[2] = {64 * 2, (cuuint64_t)rows * 64 * 2};
-  cuuint32_t box[3] = {64, 64, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -340,24 +347,32 @@ int wy_map(CUtensorMap *m, const void *ptr, long rows) {
   if (r != CUDA_SUCCESS) return fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return GDN_OK;
 }
+int t64_map(CUtensorMap *m, const Layout &L, const void *ptr) {
+  return tile_map(m, ptr, (long)L.CH_max * L.H * T64_TILES * CH, 64);
+}
+int t128_map(CUtensorMap *m, const Layout &L, const void *ptr) {
+  return tile_map(m, ptr, (long)L.CH_max * L.H * T128_TILES * 128, 128);
+}
 
 // The chunk forward kernel for this problem: tcgen05 for bf16 with d = 128, the
 // mma.sync/CUDA-core kernel otherwise (d = 64, fp32 inputs, empty batches).
 int launch_forward_kernel(const Layout &L, const gdn_shape *s, const FwdArgs &fa, dim3 grid, cudaStream_t st) {
   const bool bf = s->dtype == GDN_BF16;
   if (bf && L.D == 128 && L.Ttot > 0) {
-    CUtensorMap tq, tk, tv, tw, ts;
+    CUtensorMap tq, tk, tv, tw, ts, tt;
     int rc;
     if ((rc = qkv_map(&tk, fa.k, L.Ttot, L.H))) return rc;
     if ((rc = qkv_map(&tv, fa.v, L.Ttot, L.H))) return rc;
     if ((rc = qkv_map(&tq, fa.q ? fa.q : fa.k, L.Ttot, L.H))) return rc;
-    // WY tiles: read by the backward's state pass, or written by a saved-context forward
-    const void *wyp = fa.wy ? fa.wy : fa.wy_save;
-    if ((rc = wy_map(&tw, wyp ? wyp : fa.k, wyp ? (long)L.CH_max * L.H * 3 * CH : 64))) return rc;
-    // chunk-start states written by the state pass or a saved-context forward (unused otherwise)
+    // context tiles and chunk-start states written for the backward (maps unused when not saving)
+    if (fa.t64) {
+      if ((rc = t64_map(&tw, L, fa.t64)) || (rc = t128_map(&tt, L, fa.t128))) return rc;
+    } else if ((rc = tile_map(&tw, fa.k, 64, 64)) || (rc = tile_map(&tt, fa.k, 128, 128))) {
+      return rc;
+    }
     if ((rc = state_map(&ts, fa.states ? fa.states : fa.k, fa.states ? (long)L.CH_max * L.H * 128 : 128)))
       return rc;
-    return launch_fwd_tc(fa, tq, tk, tv, tw, ts, grid, st);
+    return launch_fwd_tc(fa, tq, tk, tv, tw, ts, tt, grid, st);
   }
   return launch_fwd_chunk(fa, bf, L.D, grid, st);
 }
@@ -444,9 +459,12 @@ int fwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
   fa.S0 = S0;
   fa.o = o;
   fa.ST = S_T;
-  if (saved && L.Ttot > 0) {  // the outputs pass also leaves the chunk-start states and WY tiles
+  if (saved && L.Ttot > 0) {  // the outputs pass also leaves the chunk-start states and context tiles
     fa.states = saved;
-    if (L.wy_bytes > 0) fa.wy_save = static_cast<char *>(saved) + L.saved_off_wy;
+    if (L.t64_bytes > 0) {
+      fa.t64 = static_cast<char *>(saved) + L.saved_off_t64;
+      fa.t128 = static_cast<char *>(saved) + L.saved_off_t128;
+    }
   }
   return forward_passes(s, L, ws, fa, 1, st);
 }
@@ -479,31 +497,15 @@ int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
   const bool bf = s->dtype == GDN_BF16;
   Plan pl;
   if ((rc = prologue(s, L, ws, g, st, pl))) return rc;
-  const void *wy = nullptr;
-  const void *states = ws + L.off_states;
-  if (saved) {
-    // the forward left the chunk-start states and the WY tiles: nothing to recompute
-    states = saved;
-    if (L.wy_bytes > 0 && L.Ttot > 0) wy = static_cast<const char *>(saved) + L.saved_off_wy;
+  const char *states = ws + L.off_states, *t64 = ws + L.off_t64, *t128 = ws + L.off_t128;
+  if (saved) {  // the forward left the chunk-start states and context tiles: nothing to recompute
+    states = static_cast<const char *>(saved);
+    t64 = states + L.saved_off_t64;
+    t128 = states + L.saved_off_t128;
   } else {
-    // 0. WY tiles of every chunk, shared by the three passes below (bf16, d = 128)
-    if (L.wy_bytes > 0 && L.Ttot > 0) {
-      WyArgs wa;
-      wa.k = k;
-      wa.g = g;
-      wa.beta = beta;
-      wa.plan = pl;
-      wa.wy = ws + L.off_wy;
-      wa.status = reinterpret_cast<int *>(ws + L.off_status);
-      wa.H = L.H;
-      wa.flags = s->flags;
-      PROF("bwd_wy");
-      CK(launch_wy(wa, L.CH_max, st));
-      wy = wa.wy;
-    }
-    // 1. forward states at every chunk start
+    // 1. forward states at every chunk start (and, bf16 with d = 128, the context tiles: a forward
+    //    pass that writes no output)
     FwdArgs fa = fwd_args(s, L, ws, pl);
-    fa.wy = wy;
     fa.q = q;
     fa.k = k;
     fa.v = v;
@@ -511,7 +513,12 @@ int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
     fa.beta = beta;
     fa.S0 = S0;
     fa.states = ws + L.off_states;
-    if ((rc = forward_passes(s, L, ws, fa, 2, st))) return rc;
+    const bool tiles = L.t64_bytes > 0 && L.Ttot > 0;
+    if (tiles) {
+      fa.t64 = ws + L.off_t64;
+      fa.t128 = ws + L.off_t128;
+    }
+    if ((rc = forward_passes(s, L, ws, fa, tiles ? 1 : 2, st))) return rc;
   }
   // 2. reverse chain: dS at every chunk end (and dS0)
   BwdArgs ba;
@@ -539,17 +546,17 @@ int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
   }
   ba.states = states;
   ba.dstates = ws + L.off_dstates;
-  ba.wy = wy;
   ba.H = L.H;
   ba.Lseg = L.Lseg;
   ba.scale = s->scale;
   ba.flags = s->flags;
   // the reverse chain: tcgen05 for bf16 with d = 128, the mma.sync kernel otherwise
   const bool chain_tc = bf && L.D == 128 && L.Ttot > 0;
-  CUtensorMap cmaps[4];
+  CUtensorMap cmaps[6];
   if (chain_tc && ((rc = qkv_map(&cmaps[0], q, L.Ttot, L.H)) || (rc = qkv_map(&cmaps[1], k, L.Ttot, L.H)) ||
-                   (rc = qkv_map(&cmaps[2], dO, L.Ttot, L.H)) ||
-                   (rc = wy_map(&cmaps[3], wy ? wy : k, wy ? (long)L.CH_max * L.H * 3 * CH : 64))))
+                   (rc = qkv_map(&cmaps[2], dO, L.Ttot, L.H)) || (rc = t64_map(&cmaps[3], L, t64)) ||
+                   (rc = t128_map(&cmaps[4], L, t128)) ||
+                   (rc = state_map(&cmaps[5], ba.dstates, (long)L.CH_max * L.H * 128))))
     return rc;
   auto chain = [&](dim3 grid) {
     return chain_tc ? launch_bwd_chain_tc(ba, cmaps, grid, st) : launch_bwd_chain(ba, bf, L.D, grid, st);
@@ -584,14 +591,14 @@ int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
   {
     PROF("bwd_local");
     if (bf && L.D == 128 && L.Ttot > 0) {
-      CUtensorMap maps[10];
+      CUtensorMap maps[11];
       if ((rc = qkv_map(&maps[0], q, L.Ttot, L.H)) || (rc = qkv_map(&maps[1], k, L.Ttot, L.H)) ||
           (rc = qkv_map(&maps[2], v, L.Ttot, L.H)) || (rc = qkv_map(&maps[3], dO, L.Ttot, L.H)) ||
           (rc = state_map(&maps[4], states, (long)L.CH_max * L.H * 128)) ||
           (rc = state_map(&maps[5], ws + L.off_dstates, (long)L.CH_max * L.H * 128)) ||
-          (rc = wy_map(&maps[6], wy ? wy : k, wy ? (long)L.CH_max * L.H * 3 * CH : 64)) ||
-          (rc = qkv_map(&maps[7], dq, L.Ttot, L.H)) || (rc = qkv_map(&maps[8], dk, L.Ttot, L.H)) ||
-          (rc = qkv_map(&maps[9], dv, L.Ttot, L.H)))
+          (rc = t64_map(&maps[6], L, t64)) || (rc = qkv_map(&maps[7], dq, L.Ttot, L.H)) ||
+          (rc = qkv_map(&maps[8], dk, L.Ttot, L.H)) || (rc = qkv_map(&maps[9], dv, L.Ttot, L.H)) ||
+          (rc = t128_map(&maps[10], L, t128)))
         return rc;
       CK(launch_bwd_local_tc(ba, maps, L.CH_max, st));
     } else {

@@ -1,11 +1,12 @@
 // Blackwell-native reverse state chain of the chunked backward (bf16 inputs,
 // d = 128): one CTA per (segment, head), chunks in reverse order, dS (the
-// gradient w.r.t. a chunk's end state) resident in fp32 TMEM.  Per chunk:
-//   [K; Q] K^T            -> N (inverse -> X1 = Ahat diag(beta)), P
-//   W^T = K^T X1^T        (columns scaled by gam at read-out)
-//   dUt^T = dS Kc^T + dO^T P               Kc = diag(cdec) K
-//   dS <- gam_C dS + dO^T Qg - dUt^T W     Qg = diag(gam) Q
-// and the fp16 dS at every chunk end goes to the workspace for the
+// gradient w.r.t. a chunk's end state) resident in fp32 TMEM.  The forward's
+// chunk context supplies P = diag(gp) tril(Q K^T) diag(rgp) and the
+// gam-scaled W^T of every chunk (TMA, with the inputs), so a chunk is two
+// tensor-core rounds:
+//   dUt^T = dS Kc^T + dO^T P,  dS += dO^T Qg     Kc = diag(cdec) K, Qg = diag(gam) Q
+//   dS <- dS - dUt^T W                          (after gam_C dS and the fp16 copy)
+// and the fp16 dS at every chunk end goes to the workspace (TMA store) for the
 // local-gradient kernel.  Pass 0 (reverse sequence parallelism) runs a
 // segment from zero (role 0) or the transition from I with dO = 0 (role 1);
 // pass 1 runs it from its exact end gradient and stores the per-chunk dS
@@ -23,21 +24,18 @@ namespace {
 constexpr int D = 128;
 constexpr int HT = 8192;
 constexpr int LN = CH + 4;
-constexpr uint32_t TM_S = 0, TM_KQ = 128, TM_W = 192, TM_DU = 256, TM_COLS = 512;
+constexpr uint32_t TM_S = 0, TM_DU = 256, TM_COLS = 512;
 
 struct __align__(1024) ChainTcSmem {
-  uint8_t ring[2][6 * HT];  // [K0 | Q0 | K1 | Q1 | dO0 | dO1]
+  // input ring, 2 stages: [K0 | Q0 | K1 | Q1 | dO0 | dO1 | P | W0 W1] half-tiles (0/1 = feature block;
+  // W = the gam-scaled W^T tile [d_k][token], K-major B of dUt^T W)
+  uint8_t ring[2][9 * HT];
   uint8_t kc[2 * HT];       // diag(cdec) K (K-major B, rows = token); later dUt^T (K-major A, rows = d_v)
   uint8_t qg[2 * HT];       // diag(gam) Q (MN-major B, rows = token)
-  uint8_t x1[HT], p[HT];
-  uint8_t wt[2 * HT];       // W^T [d_k][token]: MN-major view for nothing, K-major B view for dUt^T W
   uint8_t ds16[4 * HT];     // dS fp16 (K-major A: rows = d_v, two k-blocks of 128 rows)
-  float nf[CH * LN];
-  float g[2][CH], beta[2][CH];
+  float g[2][CH];
   Gates gt[2];
-  float ys[1152];
   uint64_t bar_tma[2];
-  uint64_t bar_x;  // precomputed X1 tile of the current chunk (TMA)
   uint64_t bar_mma;
   uint32_t tmem_base;
 };
@@ -55,7 +53,8 @@ __device__ __forceinline__ void st_chunk_f16(uint8_t *dst, const float *v) {
 
 __global__ void __launch_bounds__(NTHREADS, 1)
     bwd_chain_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                        const __grid_constant__ CUtensorMap tmdo, const __grid_constant__ CUtensorMap tmw) {
+                        const __grid_constant__ CUtensorMap tmdo, const __grid_constant__ CUtensorMap tmp,
+                        const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmds) {
   extern __shared__ unsigned char smraw[];
   ChainTcSmem &sm =
       *reinterpret_cast<ChainTcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
@@ -104,12 +103,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (tid == 0) {
     mbar_init(u32(&sm.bar_tma[0]), 1);
     mbar_init(u32(&sm.bar_tma[1]), 1);
-    mbar_init(u32(&sm.bar_x), 1);
     mbar_init(u32(&sm.bar_mma), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmq);
     tma_prefetch_desc(&tmdo);
+    tma_prefetch_desc(&tmp);
+    tma_prefetch_desc(&tmw);
+    if (store) tma_prefetch_desc(&tmds);
   }
   if (warp == 0) {
     tmem_alloc(u32(&sm.tmem_base), TM_COLS);
@@ -123,37 +124,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   auto issue_tma = [&](int c, int stage) {
     const int tok0 = bos + c * CH;
+    const int crow = (chunk0 + c) * H + h;  // (chunk, head) index of the context tiles
     const uint32_t bar = u32(&sm.bar_tma[stage]);
     uint8_t *st = sm.ring[stage];
-    mbar_expect_tx(bar, (2 + (with_do ? 4 : 0)) * HT);
+    mbar_expect_tx(bar, (4 + (with_do ? 5 : 0)) * HT);
     tma_load_3d(u32(st + 0 * HT), &tmk, 0, h, tok0, bar);
     tma_load_3d(u32(st + 2 * HT), &tmk, 64, h, tok0, bar);
+    tma_load_3d(u32(st + 7 * HT), &tmw, 0, (crow * T128_TILES + T128_W) * D, 0, bar);
     if (with_do) {
       tma_load_3d(u32(st + 1 * HT), &tmq, 0, h, tok0, bar);
       tma_load_3d(u32(st + 3 * HT), &tmq, 64, h, tok0, bar);
       tma_load_3d(u32(st + 4 * HT), &tmdo, 0, h, tok0, bar);
       tma_load_3d(u32(st + 5 * HT), &tmdo, 64, h, tok0, bar);
+      tma_load_3d(u32(st + 6 * HT), &tmp, 0, (crow * T64_TILES + T64_P) * CH, 0, bar);
     }
-  };
-  auto issue_gb = [&](int c, int stage, bool with_g) {
-    const int tok0 = bos + c * CH;
-    const int nvalid = min(CH, len - c * CH);
-    if (with_g) load_scalars(sm.g[stage], a.g, H, h, tok0, nvalid, 0);
-    load_scalars(sm.beta[stage], a.beta, H, h, tok0, nvalid, 64);
-    cp_async_commit();
-  };
-  // X1 = Ahat diag(beta) of chunk c, precomputed for the backward: loaded into sm.x1 once the
-  // previous chunk's MMA 2 has read it, waited for just before this chunk's MMA 2
-  const bool use_wy = a.wy != nullptr;
-  auto issue_x1 = [&](int c) {
-    const uint32_t bar = u32(&sm.bar_x);
-    mbar_expect_tx(bar, HT);
-    tma_load_3d(u32(sm.x1), &tmw, 0, ((chunk0 + c) * H + h) * 3 * CH, 0, bar);
   };
   if (clast >= cbeg) {
     if (tid == 0) issue_tma(clast, 0);
-    if (tid == 0 && use_wy) issue_x1(clast);
-    issue_gb(clast, 0, true);
+    load_scalars(sm.g[0], a.g, H, h, bos + clast * CH, min(CH, len - clast * CH), 0);
+    cp_async_commit();
   }
 
   // initial dS -> TMEM
@@ -194,7 +183,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int stage = it & 1;
     const int nvalid = min(CH, len - c * CH);
     uint8_t *st = sm.ring[stage];
-    float *gbeta = sm.beta[stage];
     float gnext0 = 0.f, gnext1 = 0.f;  // log-gates of the next (previous in time) chunk
     if (warp == 0 && c - 1 >= cbeg) {
       const int tokn = bos + (c - 1) * CH;
@@ -203,7 +191,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     cp_async_wait_all();
     if (tid == 0 && c - 1 >= cbeg) issue_tma(c - 1, stage ^ 1);
-    if (c - 1 >= cbeg) issue_gb(c - 1, stage ^ 1, false);
+    if (tid == 0 && store) tma_store_wait_read();  // the previous chunk's dS store has read ds16
     const bool tma_ok = mbar_wait(u32(&sm.bar_tma[stage]), (it >> 1) & 1, err, 8);
     if (__syncthreads_or(!tma_ok)) {
       failed = true;
@@ -213,12 +201,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (it == 0 && warp == 0) gate_prefix(sm.g[stage], G);
     __syncthreads();
 
-    // ---- prep: K^, Q^ (normalised, fp16) with Kc = cdec K^, Qg = gam Q^;  dO -> fp16; rows >= nvalid zero
+    // ---- prep: Kc = cdec K^, Qg = gam Q^ (normalised, fp16);  dO -> fp16 in place; rows >= nvalid zero
     {
       const bool isq = tid >= 128;
       if (!isq || with_do) {
         const int r = (tid >> 1) & 63, hb = tid & 1;
-        uint8_t *rowp = st + (isq ? HT : 0) + hb * 2 * HT + r * 128;
+        const uint8_t *rowp = st + (isq ? HT : 0) + hb * 2 * HT + r * 128;
         uint32_t raw[32];
 #pragma unroll
         for (int chk = 0; chk < 8; ++chk) {
@@ -244,19 +232,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         uint8_t *row2 = (isq ? sm.qg : sm.kc) + hb * HT + r * 128;
 #pragma unroll
         for (int chk = 0; chk < 8; ++chk) {
-          uint32_t y[4], z[4];
+          uint32_t z[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const uint32_t wv = raw[4 * chk + i];
-            const float lo = __uint_as_float(wv << 16), hi = __uint_as_float(wv & 0xffff0000u);
-            const __half2 a2 = __floats2half2_rn(lo * mul, hi * mul);
-            const __half2 b2 = __floats2half2_rn(lo * m2, hi * m2);
-            y[i] = *reinterpret_cast<const uint32_t *>(&a2);
+            const __half2 b2 = __floats2half2_rn(__uint_as_float(wv << 16) * m2, __uint_as_float(wv & 0xffff0000u) * m2);
             z[i] = *reinterpret_cast<const uint32_t *>(&b2);
           }
-          const int off = (chk ^ (r & 7)) * 16;
-          *reinterpret_cast<uint4 *>(rowp + off) = make_uint4(y[0], y[1], y[2], y[3]);
-          *reinterpret_cast<uint4 *>(row2 + off) = make_uint4(z[0], z[1], z[2], z[3]);
+          *reinterpret_cast<uint4 *>(row2 + (chk ^ (r & 7)) * 16) = make_uint4(z[0], z[1], z[2], z[3]);
         }
       }
       if (with_do) {
@@ -278,78 +261,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
     }
-    fence_async_smem();
-    __syncthreads();
-
-    // ---- MMA 1: [K; Q] K^T
-    const bool need_kq = !use_wy || with_do;  // with X1 given, only P (rows 64-127) is still needed
-    if (need_kq && tid == 0) {
-      fence_after();
-      const uint32_t idesc = idesc_f16(128, 64, false, false);
-      const uint32_t base = u32(st);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t koff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
-        mma_f16(tm + TM_KQ, sdesc(base + koff, 16, 1024), sdesc(base + koff, 16, 1024), idesc, kk > 0);
-      }
-      mma_commit(u32(&sm.bar_mma));
-    }
-    __syncwarp();
-    if (need_kq && __syncthreads_or(!mma_wait())) {
-      failed = true;
-      break;
-    }
-    if ((row < 64 && !use_wy) || (row >= 64 && with_do)) {
-      float v[32];
-      const int c0 = wg * 32;
-      tmem_ld32(tm + tl + TM_KQ + c0, v);
-      if (row < 64) {
-        float4 *dst = reinterpret_cast<float4 *>(&sm.nf[row * LN + c0]);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-      } else {
-        const int r = row - 64;
-        const float gr = G.gp[r];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const float4 ga = reinterpret_cast<const float4 *>(G.rgp + c0 + q4 * 8)[0];
-          const float4 gb = reinterpret_cast<const float4 *>(G.rgp + c0 + q4 * 8)[1];
-          const float rg[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-          float y[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) y[i] = c0 + q4 * 8 + i <= r ? v[q4 * 8 + i] * gr * rg[i] : 0.f;
-          st_chunk_f16(sm.p + r * 128 + ((((c0 >> 3) + q4) ^ (r & 7)) * 16), y);
-        }
-      }
-    }
-    fence_before();
-    __syncthreads();
-    if (!use_wy) {
-      wy_inverse<false, false>(sm.nf, LN, gbeta, sm.ys, [&](int r, int cc, float a0, float a1) {
-        const float2 bb = *reinterpret_cast<const float2 *>(gbeta + cc);
-        *reinterpret_cast<__half2 *>(sm.x1 + sw128_offset(r, cc)) = __floats2half2_rn(a0 * bb.x, a1 * bb.y);
-      }, it == 0);
-    } else if (__syncthreads_or(!mbar_wait(u32(&sm.bar_x), it & 1, err, 8))) {
-      failed = true;
-      break;
-    }
-
-    // ---- MMA 2: W^T = K^T X1^T;  meanwhile dS -> fp16 operand copy (+ workspace), gam_C dS back to TMEM
-    if (tid == 0) {
-      fence_after();
-      const uint32_t idesc = idesc_f16(128, 64, true, false);
-      const uint32_t kb = u32(st), x1b = u32(sm.x1);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_f16(tm + TM_W, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(x1b + kk * 32, 16, 1024), idesc, kk > 0);
-      mma_commit(u32(&sm.bar_mma));
-    }
-    __syncwarp();
+    // ---- dS (end of chunk c) -> fp16 operand copy, gam_C dS back into TMEM
     {
       const float gC = G.gamC;
-      f16 *stg = store && c < cend
-                     ? static_cast<f16 *>(a.dstates) + ((size_t)(chunk0 + c) * H + h) * DD + (size_t)row * D
-                     : nullptr;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int c0 = wg * 64 + half * 32;
@@ -359,55 +273,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const int chk = ((c0 & 63) >> 3) + q4;
-          uint8_t *dst = sm.ds16 + kb * 2 * HT + row * 128 + ((chk ^ (row & 7)) * 16);
-          st_chunk_f16(dst, v + q4 * 8);
-          if (stg) *reinterpret_cast<uint4 *>(stg + c0 + q4 * 8) = *reinterpret_cast<const uint4 *>(dst);
+          st_chunk_f16(sm.ds16 + kb * 2 * HT + row * 128 + ((chk ^ (row & 7)) * 16), v + q4 * 8);
         }
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] *= gC;
         tmem_st32(tm + tl + TM_S + c0, v);
       }
     }
-    fence_before();  // the rescaled dS in TMEM is accumulated into right below
-    if (__syncthreads_or(!mma_wait())) {
-      failed = true;
-      break;
-    }
-    if (use_wy && tid == 0 && c - 1 >= cbeg) issue_x1(c - 1);  // MMA 2 has consumed sm.x1
-    // dS += dO^T Qg needs only inputs: issued now, it runs under the W^T read-out (MMA 3's commit
-    // covers it); MMA 4 then adds -dUt^T W
-    if (with_do && tid == 0) {
-      const uint32_t id_mm = idesc_f16(128, 128, true, true);
-      const uint32_t dob = u32(st + 4 * HT), qgb = u32(sm.qg);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_f16(tm + TM_S, sdesc(dob + kk * 2048, HT, 1024), sdesc(qgb + kk * 2048, HT, 1024), id_mm, true);
-    }
-    {  // W^T read-out, columns scaled by gam
-      const int c0 = wg * 32;
-      float v[32];
-      tmem_ld32(tm + tl + TM_W + c0, v);
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const float4 ga = reinterpret_cast<const float4 *>(G.gam + c0 + q4 * 8)[0];
-        const float4 gb = reinterpret_cast<const float4 *>(G.gam + c0 + q4 * 8)[1];
-        const float gm[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-        float y[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) y[i] = v[q4 * 8 + i] * gm[i];
-        st_chunk_f16(sm.wt + row * 128 + ((((c0 >> 3) + q4) ^ (row & 7)) * 16), y);
-      }
-    }
-    fence_before();
     fence_async_smem();
+    fence_before();
     __syncthreads();
 
-    // ---- MMA 3: dUt^T = dS Kc^T + dO^T P   (M = 128, N = 64)
+    // ---- dUt^T = dS Kc^T + dO^T P -> TM_DU (M = 128, N = 64);  dS += dO^T Qg (N = 128)
     if (tid == 0) {
       fence_after();
+      if (store && c < cend) {  // the fp16 dS at the end of chunk c, for the local-gradient kernel
+        const int srow = ((chunk0 + c) * H + h) * D;
+        tma_store_3d(&tmds, 0, srow, 0, u32(sm.ds16));
+        tma_store_3d(&tmds, 64, srow, 0, u32(sm.ds16 + 2 * HT));
+        tma_store_commit();
+      }
       const uint32_t id_kk = idesc_f16(128, 64, false, false);
       const uint32_t id_mm = idesc_f16(128, 64, true, true);
-      const uint32_t dsb = u32(sm.ds16), kcb = u32(sm.kc), dob = u32(st + 4 * HT), pb = u32(sm.p);
+      const uint32_t dsb = u32(sm.ds16), kcb = u32(sm.kc), dob = u32(st + 4 * HT), pb = u32(st + 6 * HT);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
@@ -418,6 +306,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           mma_f16(tm + TM_DU, sdesc(dob + kk * 2048, HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id_mm, true);
+        const uint32_t id_s = idesc_f16(128, 128, true, true), qgb = u32(sm.qg);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f16(tm + TM_S, sdesc(dob + kk * 2048, HT, 1024), sdesc(qgb + kk * 2048, HT, 1024), id_s, true);
       }
       mma_commit(u32(&sm.bar_mma));
     }
@@ -438,18 +330,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     fence_async_smem();
     __syncthreads();
 
-    // ---- MMA 4: dS -= dUt^T W   (M = 128, N = 128; dO^T Qg was added after MMA 2)
+    // ---- dS -= dUt^T W   (M = 128, N = 128)
     if (tid == 0) {
       fence_after();
       const uint32_t id_kk_neg = idesc_f16(128, 128, false, false, true);
-      const uint32_t dub = u32(sm.kc), wb = u32(sm.wt);
+      const uint32_t dub = u32(sm.kc), wb = u32(st + 7 * HT);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
         mma_f16(tm + TM_S, sdesc(dub + kk * 32, 16, 1024), sdesc(wb + kk * 32, 16, 1024), id_kk_neg, true);
       mma_commit(u32(&sm.bar_mma));
     }
     __syncwarp();
-    if (warp == 0 && c - 1 >= cbeg) {  // gates of the next chunk, overlapping MMA 4
+    if (warp == 0 && c - 1 >= cbeg) {  // gates of the next chunk, overlapping the last product
       float *gn = sm.g[stage ^ 1];
       const int nvn = min(CH, len - (c - 1) * CH);
       gn[lane] = lane < nvn ? gnext0 : 0.f;
@@ -480,6 +372,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
   }
+  if (tid == 0 && store) tma_store_wait_all();
   fence_before();
   __syncthreads();
   fence_after();
@@ -491,7 +384,7 @@ int launch_bwd_chain_tc(const BwdArgs &a, const CUtensorMap *maps, dim3 grid, cu
   static_assert(sizeof(ChainTcSmem) + 1024 <= 232448 - 256, "shared memory budget (the rest: static shared memory)");
   cudaError_t e = cudaFuncSetAttribute(bwd_chain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  bwd_chain_tc_kernel<<<grid, NTHREADS, smem, st>>>(a, maps[0], maps[1], maps[2], maps[3]);
+  bwd_chain_tc_kernel<<<grid, NTHREADS, smem, st>>>(a, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5]);
   return (int)cudaGetLastError();
 }
 

@@ -9,18 +9,17 @@
 // matrix multiplied with K once (onedev.kr FlashQLA talk summary, paragraph on
 // SFU load, last sentence).
 //
-// Rounds (MMA group -> read-out), TMEM regions T0..T7 of 64 columns (X1, X2, Ahat arrive
-// precomputed by TMA; the inline inverse is kept for calls without them):
-//   P1 [K;Q]K^T->T0          R1: N (fp32), P
-//   P2 W^T->T1, U^T->T2, and (inputs only) Y = dS K^T->T3, Z = dO^T P->T4, Qa = S0^T dO^T->T5
-//                            R2: W^T (gam-scaled columns)
-//   P3 Ut^T = U^T - S0 W^T   R3/R4: Ut^T; dUt^T = cdec*Y + Z; sums <Ut,Y>, <dUt,Ut>
+// Rounds (MMA group -> read-out), TMEM regions T0..T7 of 64 columns.  The forward's chunk context
+// supplies X1, X2, Ahat, P, N and Ut^T by TMA with the inputs, so nothing of the forward chunk is
+// recomputed here:
+//   P2 Y = dS K^T->T3, Qa = S0^T dO^T->T5, Z = dO^T P->T4
+//                            R2: dUt^T = cdec*Y + Z; sums <Ut,Y>, <dUt,Ut>
 //   P5 dP = dO Ut^T->T0, dW'^T = -S0^T dUt^T->T1, dV^T = dUt^T X2->T6, Kb = dS^T Ut^T->T2
 //                            R5: dPm (over P), dP*P sums; dW'^T tile; dv out, <dV,v>
 //   P6 Qb = K^T dPm^T->T7, M1 = dW' K^T->T3, M2 = dUt V^T->T4
 //                            R6: dq out (+ <dQ1,q>); dAhat tile, beta column sums
 //   P7 Y1 = Ahat^T dAhat->T0 R7: Y1 tile
-//   P8 dT = -Y1 Ahat^T->T1   R8: dN tile (strictly lower), beta row sums
+//   P8 dT = -Y1 Ahat^T->T1   R8: dN tile (strictly lower), beta row sums (with N)
 //   P9 Ka = Q^T dPm + dW'^T X1 + K^T (dN + dN^T)->T3
 //                            R9: dk out (Ka + cdec Kb);  dg (reverse cumsum), dbeta
 #include "chunk_common.cuh"
@@ -35,7 +34,6 @@ namespace {
 
 constexpr int D = 128;
 constexpr int HT = 8192;
-constexpr int LN = CH + 4;
 constexpr int LTHREADS = 512;  // 16 warps: four per TMEM lane quarter, 16 columns each per read-out
 constexpr int LWARPS = LTHREADS / 32;
 constexpr uint32_t T0 = 0, T1 = 64, T2 = 128, T3 = 192, T4 = 256, T5 = 320, T6 = 384, T7 = 448;
@@ -51,16 +49,15 @@ struct __align__(1024) LocalTcSmem {
   uint8_t x2[HT];       // X2, later dAhat
   uint8_t ah[HT];       // Ahat (fp16)
   uint8_t wt[2 * HT];   // W^T [d_k][token], later dUt^T [d_v][token]
-  uint8_t ut[2 * HT];   // Ut^T [d_v][token]
-  float nf[CH * LN];
+  uint8_t ut[2 * HT];   // Ut^T [d_v][token] (context tile)
+  uint8_t n16[HT];      // N = K K^T (fp16, [r][i], context tile)
   float g[2][CH], beta[2][CH];  // per item parity: the next item's gates are prepared during this one
   float nq[CH], nk[CH];         // reciprocal norms
   Gates gt[2];
-  float ys[1152];
   float part[20][CH];   // per-token partial sums (reused per round)
   float acc[7][CH];     // assembled per-token terms
   float red[LWARPS];
-  uint64_t bar_a, bar_b, bar_w, bar_mma, bar_mma2;  // TMA: {K, Q, V, S0, dS}, {dO}, {X1, X2, Ahat}; tensor cores
+  uint64_t bar_a, bar_b, bar_w, bar_mma;  // TMA: {K, Q, V, S0, dS, Ut^T, P, N}, {dO}, {X1, X2, Ahat}; tensor cores
   uint32_t tmem_base;
 };
 
@@ -117,7 +114,7 @@ __global__ void __launch_bounds__(LTHREADS, 1)
                         const __grid_constant__ CUtensorMap tms0, const __grid_constant__ CUtensorMap tmds,
                         const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmdq,
                         const __grid_constant__ CUtensorMap tmdk, const __grid_constant__ CUtensorMap tmdv,
-                        int n_items) {
+                        const __grid_constant__ CUtensorMap tmu, int n_items) {
   extern __shared__ unsigned char smraw[];
   LocalTcSmem &sm =
       *reinterpret_cast<LocalTcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
@@ -139,7 +136,6 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     mbar_init(u32(&sm.bar_b), 1);
     mbar_init(u32(&sm.bar_w), 1);
     mbar_init(u32(&sm.bar_mma), 1);
-    mbar_init(u32(&sm.bar_mma2), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == 0) {
@@ -151,16 +147,10 @@ __global__ void __launch_bounds__(LTHREADS, 1)
   fence_after();
   const uint32_t tm = sm.tmem_base;
   const uint32_t tl = (uint32_t)(wq * 32) << 16;
-  uint32_t phase = 0, phase2 = 0;
+  uint32_t phase = 0;
   auto mma_done = [&]() {
     const bool r = mbar_wait(u32(&sm.bar_mma), phase, err, 4);
     phase ^= 1;
-    fence_after();
-    return r;
-  };
-  auto mma2_done = [&]() {  // the input-only products issued with P1 (one commit per item)
-    const bool r = mbar_wait(u32(&sm.bar_mma2), phase2, err, 4);
-    phase2 ^= 1;
     fence_after();
     return r;
   };
@@ -200,10 +190,13 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     const int gc = item / H, n = a.plan.chunk_seq[gc];
     return a.plan.seq_bos[n] + (gc - a.plan.seq_chunk0[n]) * CH;
   };
-  auto issue_main = [&](int item) {  // K, Q, V, S0, dS
+  auto issue_main = [&](int item) {  // K, Q, V, S0, dS and the context tiles Ut^T, P, N
     const int hh = item % H, t0 = item_tok0(item), srow = item * D;  // state rows of (chunk, head)
     const uint32_t bar = u32(&sm.bar_a);
-    mbar_expect_tx(bar, 14 * HT);
+    mbar_expect_tx(bar, 18 * HT);
+    tma_load_3d(u32(sm.ut), &tmu, 0, (item * T128_TILES + T128_U) * D, 0, bar);
+    tma_load_3d(u32(sm.p), &tmw, 0, (item * T64_TILES + T64_P) * CH, 0, bar);
+    tma_load_3d(u32(sm.n16), &tmw, 0, (item * T64_TILES + T64_N) * CH, 0, bar);
     tma_load_3d(u32(sm.kq + 0 * HT), &tmk, 0, hh, t0, bar);
     tma_load_3d(u32(sm.kq + 2 * HT), &tmk, 64, hh, t0, bar);
     tma_load_3d(u32(sm.kq + 1 * HT), &tmq, 0, hh, t0, bar);
@@ -222,23 +215,23 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     tma_load_3d(u32(sm.dob), &tmdo, 0, hh, t0, bar);
     tma_load_3d(u32(sm.dob + HT), &tmdo, 64, hh, t0, bar);
   };
-  // precomputed WY tiles (X1, X2, Ahat) of an item: their buffers are free once its dk is stored
-  const bool use_wy = a.wy != nullptr;
+  // the WY tiles X1, X2, Ahat of an item (item = chunk * H + head): their buffers are free once the
+  // previous item's dk is stored
   auto issue_wy = [&](int item) {
     const uint32_t bar = u32(&sm.bar_w);
-    const int row = item * 3 * CH;  // item = chunk * H + head, three 64-row tiles each
+    const int row = item * T64_TILES * CH;
     mbar_expect_tx(bar, 3 * HT);
-    tma_load_3d(u32(sm.x1), &tmw, 0, row, 0, bar);
-    tma_load_3d(u32(sm.x2), &tmw, 0, row + CH, 0, bar);
-    tma_load_3d(u32(sm.ah), &tmw, 0, row + 2 * CH, 0, bar);
+    tma_load_3d(u32(sm.x1), &tmw, 0, row + T64_X1 * CH, 0, bar);
+    tma_load_3d(u32(sm.x2), &tmw, 0, row + T64_X2 * CH, 0, bar);
+    tma_load_3d(u32(sm.ah), &tmw, 0, row + T64_AH * CH, 0, bar);
   };
   int item = next_valid(blockIdx.x);
   if (tid == 0 && item < n_items) {
     issue_main(item);
     issue_do(item);
-    if (use_wy) issue_wy(item);
+    issue_wy(item);
   }
-  bool pend_main = item < n_items, pend_do = pend_main, pend_wy = pend_main && use_wy, failed = false;
+  bool pend_main = item < n_items, pend_do = pend_main, pend_wy = pend_main, failed = false;
   uint32_t it = 0;  // parity of the TMA barriers: one completion per item
   for (; item < n_items; ++it) {
   const int nitem = next_valid(item + gridDim.x);
@@ -316,19 +309,13 @@ __global__ void __launch_bounds__(LTHREADS, 1)
   fence_async_smem();
   __syncthreads();
 
-  // Input-only products of the second round: W^T = K^T X1^T -> T1; U^T = V^T X2^T -> T2;
-  // Y = dS K^T -> T3; Qa = S0^T dO^T -> T5 (thread 0; committed to bar_mma2 by the caller)
-  auto issue_p2a = [&]() {
-    const uint32_t id = idesc_f16(128, 64, true, false);
-    const uint32_t kb = u32(sm.kq), vb = u32(sm.v), x1b = u32(sm.x1), x2b = u32(sm.x2);
-#pragma unroll 1
-    for (int kk = 0; kk < 4; ++kk) {
-      mma_f16(tm + T1, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(x1b + kk * 32, 16, 1024), id, kk > 0);
-      mma_f16(tm + T2, sdesc(vb + kk * 2048, HT, 1024), sdesc(x2b + kk * 32, 16, 1024), id, kk > 0);
-    }
+  // ---- P2: Y = dS K^T -> T3;  Qa = S0^T dO^T -> T5;  Z = dO^T P -> T4  (inputs and context only)
+  if (tid == 0) {
+    fence_after();
     const uint32_t id_kk = idesc_f16(128, 64, false, false);
     const uint32_t id_mk = idesc_f16(128, 64, true, false);
-    const uint32_t dsb = u32(sm.ds), dob = u32(sm.dob), sb = u32(sm.s0);
+    const uint32_t id_mm = idesc_f16(128, 64, true, true);
+    const uint32_t kb = u32(sm.kq), dsb = u32(sm.ds), dob = u32(sm.dob), sb = u32(sm.s0), pb = u32(sm.p);
 #pragma unroll 1
     for (int kk = 0; kk < 8; ++kk) {
       const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
@@ -336,110 +323,9 @@ __global__ void __launch_bounds__(LTHREADS, 1)
       mma_f16(tm + T5, sdesc(sb + kk * 2048, 2 * HT, 1024), sdesc(dob + (kk >> 2) * HT + (kk & 3) * 32, 16, 1024),
               id_mk, kk > 0);
     }
-  };
-
-  // ---- P1: [K; Q] K^T -> T0 (bar_mma); with the WY tiles at hand the input-only products follow at
-  //      once (bar_mma2) and run while R1 reads N and P out
-  if (tid == 0) {
-    fence_after();
-    const uint32_t id = idesc_f16(128, 64, false, false), kb = u32(sm.kq);
-#pragma unroll 1
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t off = (kk >> 2) * 2 * HT + (kk & 3) * 32;
-      mma_f16(tm + T0, sdesc(kb + off, 16, 1024), sdesc(kb + off, 16, 1024), id, kk > 0);
-    }
-    mma_commit(u32(&sm.bar_mma));
-    if (use_wy) {
-      if (mbar_wait(u32(&sm.bar_w), it & 1, err, 8)) issue_p2a();  // on failure every thread's wait below fails too
-      mma_commit(u32(&sm.bar_mma2));
-    }
-  }
-  __syncwarp();
-  if (__syncthreads_or(!mma_done())) {
-    failed = true;
-    break;
-  }
-  // R1: rows 0-63 -> N (fp32), rows 64-127 -> P (fp16, [r][i])
-#pragma unroll 1
-  for (int q4 = 0; q4 < 2; ++q4) {
-    const int cb = c0 + q4 * 8;
-    float v[8];
-    tmem_ld8(tm + tl + T0 + cb, v);
-    if (row < 64) {
-      float4 *dst = reinterpret_cast<float4 *>(&sm.nf[row * LN + cb]);
-      dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-      dst[1] = make_float4(v[4], v[5], v[6], v[7]);
-    } else {
-      const int r = row - 64;
-      const float gr = G.gp[r];
-      float y[8], rg[8];
-      ld8f(G.rgp + cb, rg);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) y[i] = cb + i <= r ? v[i] * gr * rg[i] : 0.f;
-      st_chunk_f16(sm.p + chunk_off(r, cb), y);
-    }
-  }
-  fence_async_smem();  // P is an operand of the next round
-  fence_before();
-  __syncthreads();
-  if (!use_wy) {
-    wy_inverse<false, false>(sm.nf, LN, gbeta, sm.ys, [&](int r, int c, float a0, float a1) {
-      const float b0 = gbeta[c], b1 = gbeta[c + 1], gr = G.gp[r];
-      const uint32_t off = sw128_offset(r, c);
-      *reinterpret_cast<__half2 *>(sm.x1 + off) = __floats2half2_rn(a0 * b0, a1 * b1);
-      *reinterpret_cast<__half2 *>(sm.x2 + off) =
-          __floats2half2_rn(c <= r ? a0 * b0 * (gr * G.rgp[c]) : 0.f,
-                            c + 1 <= r ? a1 * b1 * (gr * G.rgp[c + 1]) : 0.f);
-      *reinterpret_cast<__half2 *>(sm.ah + off) = __floats2half2_rn(a0, a1);
-    });
-    if (tid == 0) {
-      fence_after();
-      issue_p2a();
-      mma_commit(u32(&sm.bar_mma2));
-    }
-    __syncwarp();
-  } else {
-    const bool ok = mbar_wait(u32(&sm.bar_w), it & 1, err, 8);
-    pend_wy = false;
-    if (__syncthreads_or(!ok)) {
-      failed = true;
-      break;
-    }
-  }
-  if (__syncthreads_or(!mma2_done())) {
-    failed = true;
-    break;
-  }
-  // R2: W^T (lanes d_k, columns token) * gam -> wt
-#pragma unroll 1
-  for (int q4 = 0; q4 < 2; ++q4) {
-    const int cb = c0 + q4 * 8;
-    float v[8];
-    tmem_ld8(tm + tl + T1 + cb, v);
-    float gm[8];
-    ld8f(G.gam + cb, gm);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] *= gm[i];
-    st_chunk_f16(sm.wt + chunk_off(row, cb), v);
-  }
-  fence_before();
-  fence_async_smem();
-  __syncthreads();
-
-  // ---- Z = dO^T P -> T4 and P3: Ut^T = U^T - S0 W^T (T2), one commit
-  if (tid == 0) {
-    fence_after();
-    const uint32_t id_mm = idesc_f16(128, 64, true, true);
-    const uint32_t dob = u32(sm.dob), pb = u32(sm.p);
 #pragma unroll 1
     for (int kk = 0; kk < 4; ++kk)
       mma_f16(tm + T4, sdesc(dob + kk * 2048, HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id_mm, kk > 0);
-    const uint32_t id = idesc_f16(128, 64, false, true, true);
-    const uint32_t sb = u32(sm.s0), wb = u32(sm.wt);
-#pragma unroll 1
-    for (int kk = 0; kk < 8; ++kk)
-      mma_f16(tm + T2, sdesc(sb + (kk >> 2) * 2 * HT + (kk & 3) * 32, 16, 1024), sdesc(wb + kk * 2048, 2 * HT, 1024),
-              id, true);
     mma_commit(u32(&sm.bar_mma));
   }
   __syncwarp();
@@ -463,7 +349,7 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     failed = true;
     break;
   }
-  {  // R3+R4: Ut^T -> ut;  dUt^T = cdec*Y + Z -> wt (W^T is dead);  per-token sums <Ut, Y>, <dUt, Ut> over d_v
+  {  // R2: dUt^T = cdec*Y + Z -> wt;  per-token sums <Ut, Y>, <dUt, Ut> over d_v (Ut^T from its tile)
     float t1 = 0.f, t2 = 0.f;
 #pragma unroll 1
     for (int q4 = 0; q4 < 2; ++q4) {
@@ -471,8 +357,16 @@ __global__ void __launch_bounds__(LTHREADS, 1)
       float y[8], z[8], u[8], s1[8], s2[8];
       tmem_ld8(tm + tl + T3 + cb, y);
       tmem_ld8(tm + tl + T4 + cb, z);
-      tmem_ld8(tm + tl + T2 + cb, u);
-      st_chunk_f16(sm.ut + chunk_off(row, cb), u);
+      {
+        const uint4 raw = *reinterpret_cast<const uint4 *>(sm.ut + chunk_off(row, cb));
+        const __half2 *uh = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __half22float2(uh[i]);
+          u[2 * i] = f.x;
+          u[2 * i + 1] = f.y;
+        }
+      }
       float cd[8];
       ld8f(G.cdec + cb, cd);
 #pragma unroll
@@ -500,6 +394,14 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     sm.acc[1][tid] = sm.part[4][tid] + sm.part[5][tid] + sm.part[6][tid] + sm.part[7][tid];  // <dUt, Ut>
   }
 
+  {  // X1, X2, Ahat of this item (loaded at the end of the previous one)
+    const bool ok = mbar_wait(u32(&sm.bar_w), it & 1, err, 8);
+    pend_wy = false;
+    if (__syncthreads_or(!ok)) {
+      failed = true;
+      break;
+    }
+  }
   // ---- P5: dP = dO Ut^T -> T0; dW'^T = -S0^T dUt^T -> T1; dV^T = dUt^T X2 -> T6;  Kb = dS^T Ut^T -> T2
   if (tid == 0) {
     fence_after();
@@ -799,11 +701,13 @@ float rg[8];
       const int cb = c0 + q4 * 8;
       float v[8], y[8];
       tmem_ld8(tm + tl + T1 + cb, v);
+      const uint4 nraw = *reinterpret_cast<const uint4 *>(sm.n16 + chunk_off(r, cb));
+      const __half *nh = reinterpret_cast<const __half *>(&nraw);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int col = cb + i;
         const bool lo = col < r;
-        rb += lo ? v[i] * sm.nf[r * LN + col] : 0.f;
+        rb += lo ? v[i] * __half2float(nh[i]) : 0.f;
         y[i] = lo ? br * v[i] : 0.f;
       }
       st_chunk_f16(sg + chunk_off(r, cb), y);
@@ -933,7 +837,7 @@ float rg[8];
   }
   __syncthreads();  // the next item rewrites the per-token scratch read above
   if (tid == 0) tma_store_wait_read();  // the dk tile store has read x2 / ah (rewritten by the next item)
-  if (use_wy && nitem < n_items) {  // X1, X2, Ahat of the next item (x2/ah held the dk staging until now)
+  if (nitem < n_items) {  // X1, X2, Ahat of the next item (x2/ah held the dk staging until now)
     if (tid == 0) issue_wy(nitem);
     pend_wy = true;
   }
@@ -968,7 +872,7 @@ int launch_bwd_local_tc(const BwdArgs &a, const CUtensorMap *maps, int CH_max, c
   const int n_items = CH_max * a.H;
   const int grid = n_items < sms ? n_items : sms;  // persistent: one CTA per SM
   bwd_local_tc_kernel<<<grid, LTHREADS, smem, st>>>(a, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
-                                                    maps[6], maps[7], maps[8], maps[9], n_items);
+                                                    maps[6], maps[7], maps[8], maps[9], maps[10], n_items);
   return (int)cudaGetLastError();
 }
 

@@ -77,7 +77,7 @@ __device__ __forceinline__ uint32_t chunk_off(int r, int cb) { return r * 128 + 
 __global__ void __launch_bounds__(FT, 1)
     fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmw,
-                  const __grid_constant__ CUtensorMap tms) {
+                  const __grid_constant__ CUtensorMap tms, const __grid_constant__ CUtensorMap tmt) {
   extern __shared__ unsigned char smraw[];
   TcSmem &sm = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
 
@@ -114,13 +114,12 @@ __global__ void __launch_bounds__(FT, 1)
   }
   const bool outputs = (a.pass == 1);
   const bool need_v = !transition;
-  // backward passes: the WY tiles X1, X2 were computed once per chunk; they arrive by TMA in the
-  // ring's Q slots (q is not needed without outputs) and replace the Gram product and the inverse
-  const bool use_wy = a.wy != nullptr && !outputs;
-  // chunk-start states (state pass, or outputs pass of a saved-context forward) and WY tiles (saved-
-  // context forward) leave shared memory by TMA stores issued by thread 0
+  // chunk-start states and the chunk context tiles (X1, X2, Ahat, P, N, scaled W^T, Ut^T) leave shared
+  // memory by TMA stores issued by thread 0 (N from registers); a pass with o == NULL computes P but
+  // no output
   const bool save_states = a.pass != 0 && a.states != nullptr;
-  const bool save_wy = outputs && a.wy_save != nullptr;
+  const bool save_wy = outputs && a.t64 != nullptr;
+  const bool want_o = outputs && a.o != nullptr;
   const bool l2 = (a.flags & kFlagL2Norm) != 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wg = warp >> 2;                      // column group 0..3 within a lane quarter
@@ -139,7 +138,10 @@ __global__ void __launch_bounds__(FT, 1)
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
     tma_prefetch_desc(&tmq);
-    if (use_wy || save_wy) tma_prefetch_desc(&tmw);
+    if (save_wy) {
+      tma_prefetch_desc(&tmw);
+      tma_prefetch_desc(&tmt);
+    }
     if (save_states) tma_prefetch_desc(&tms);
   }
   if (warp == 0) {
@@ -155,7 +157,7 @@ __global__ void __launch_bounds__(FT, 1)
   auto issue_tma = [&](int c, int stage) {
     const int tok0 = bos + c * CH;
     const bool wq = outputs && c >= cbeg;
-    const uint32_t bytes = (2 + (wq || use_wy ? 2 : 0) + (need_v ? 2 : 0)) * HT;
+    const uint32_t bytes = (2 + (wq ? 2 : 0) + (need_v ? 2 : 0)) * HT;
     const uint32_t bar = u32(&sm.bar_tma[stage]);
     uint8_t *st = sm.ring[stage];
     mbar_expect_tx(bar, bytes);
@@ -164,10 +166,6 @@ __global__ void __launch_bounds__(FT, 1)
     if (wq) {
       tma_load_3d(u32(st + 1 * HT), &tmq, 0, h, tok0, bar);
       tma_load_3d(u32(st + 3 * HT), &tmq, 64, h, tok0, bar);
-    } else if (use_wy) {
-      const int wrow = ((chunk0 + c) * H + h) * 3 * CH;
-      tma_load_3d(u32(st + 1 * HT), &tmw, 0, wrow, 0, bar);       // X1
-      tma_load_3d(u32(st + 3 * HT), &tmw, 0, wrow + CH, 0, bar);  // X2
     }
     if (need_v) {
       tma_load_3d(u32(st + 4 * HT), &tmv, 0, h, tok0, bar);
@@ -282,7 +280,11 @@ __global__ void __launch_bounds__(FT, 1)
   for (int c = cfirst; c < cend && !failed; ++c) {
     const int it = c - cfirst;
     const int stage = it & 1;
-    const bool emit = outputs && c >= cbeg;
+    const bool emit = outputs && c >= cbeg;  // Q, P (and the output if wanted)
+    const bool emit_o = emit && want_o;
+    const bool save_c = save_wy && emit;      // this chunk's context tiles
+    const int t64row = ((chunk0 + c) * H + h) * T64_TILES * CH;
+    const int t128row = ((chunk0 + c) * H + h) * T128_TILES * D;
     const int tok0 = bos + c * CH;
     const int nvalid = min(CH, len - c * CH);
     uint8_t *st = sm.ring[stage];
@@ -317,7 +319,7 @@ __global__ void __launch_bounds__(FT, 1)
     }
     __syncthreads();
 
-    if (!use_wy) {
+    {
       // ---- MMA 1: [K; Q] K^T  (M = 128, N = 64, K = 128)
       if (tid == 0) {
         fence_after();
@@ -345,6 +347,15 @@ __global__ void __launch_bounds__(FT, 1)
           float4 *dst = reinterpret_cast<float4 *>(&sm.nf[row * LN + c0]);
 #pragma unroll
           for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          if (save_c) {  // N (fp16, row-major) straight from registers: 32 contiguous bytes per thread
+            uint8_t *nt = reinterpret_cast<uint8_t *>(static_cast<f16 *>(a.t64) +
+                                                      ((size_t)t64row + T64_N * CH + row) * CH + c0);
+            __half2 hv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) hv[i] = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+            reinterpret_cast<uint4 *>(nt)[0] = *reinterpret_cast<const uint4 *>(hv);
+            reinterpret_cast<uint4 *>(nt)[1] = *reinterpret_cast<const uint4 *>(hv + 4);
+          }
         } else {
           const int r = row - 64;
           const float gr = G.gp[r];
@@ -375,16 +386,16 @@ __global__ void __launch_bounds__(FT, 1)
     // ---- MMA 2: W^T = K^T X1^T, U^T = V^T X2^T  (M = 128, N = 64, K = 64)
     if (tid == 0) {
       fence_after();
-      if (save_wy && emit) {  // X1, X2, Ahat rows of this (chunk, head) in the saved context
-        const int wrow = ((chunk0 + c) * H + h) * 3 * CH;
-        tma_store_3d(&tmw, 0, wrow, 0, u32(sm.x1));
-        tma_store_3d(&tmw, 0, wrow + CH, 0, u32(sm.x2));
-        tma_store_3d(&tmw, 0, wrow + 2 * CH, 0, u32(sm.ah));
+      if (save_c) {  // X1, X2, Ahat and P of this (chunk, head)
+        tma_store_3d(&tmw, 0, t64row + T64_X1 * CH, 0, u32(sm.x1));
+        tma_store_3d(&tmw, 0, t64row + T64_X2 * CH, 0, u32(sm.x2));
+        tma_store_3d(&tmw, 0, t64row + T64_AH * CH, 0, u32(sm.ah));
+        tma_store_3d(&tmw, 0, t64row + T64_P * CH, 0, u32(sm.p));
         tma_store_commit();
       }
       const uint32_t idesc = idesc_f16(128, 64, true, false);
       const uint32_t kb = u32(st), vb = u32(st + 4 * HT);
-      const uint32_t x1b = use_wy ? u32(st + HT) : u32(sm.x1), x2b = use_wy ? u32(st + 3 * HT) : u32(sm.x2);
+      const uint32_t x1b = u32(sm.x1), x2b = u32(sm.x2);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         mma_f16(tm + TM_W, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(x1b + kk * 32, 16, 1024), idesc, kk > 0);
@@ -426,7 +437,7 @@ __global__ void __launch_bounds__(FT, 1)
     }
     // Oi^T = S0 Q^T needs only the state copy and Q: issued now, it runs under the W^T read-out
     // (MMA 3's commit covers it)
-    if (emit && tid == 0) {
+    if (emit_o && tid == 0) {
       const uint32_t s0b = u32(sm.s0), qb = u32(st + HT);
       const uint32_t id_o = idesc_f16(128, 64, false, false);
 #pragma unroll
@@ -455,6 +466,10 @@ __global__ void __launch_bounds__(FT, 1)
     // ---- MMA 3: Ut^T = U^T - S0 W^T   (M = 128, N = 64, K = 128)
     if (tid == 0) {
       fence_after();
+      if (save_c) {  // the gam-scaled W^T tile
+        tma_store_3d(&tmt, 0, t128row + T128_W * D, 0, u32(sm.wu));
+        tma_store_commit();
+      }
       const uint32_t s0b = u32(sm.s0), wb = u32(sm.wu);
       const uint32_t id_u = idesc_f16(128, 64, false, true, /*neg_a=*/true);
 #pragma unroll
@@ -475,6 +490,7 @@ __global__ void __launch_bounds__(FT, 1)
       if (next_ok) prep_kq(stn, nvn, outputs && c + 1 >= cbeg);
     }
     {
+      if (tid == 0 && save_c) tma_store_wait_read();  // the W^T store has read wu (Ut^T is written next)
       const bool mok = mma_wait();
       if (__syncthreads_or(!mok || !next_ok)) {
         failed = true;
@@ -503,13 +519,17 @@ __global__ void __launch_bounds__(FT, 1)
     // ---- MMA 4: S += (Ut^T diag(cdec)) K (N = 128, K = 64);  Oa^T = Ut^T P^T (N = 64, K = 64)
     if (tid == 0) {
       fence_after();
+      if (save_c) {  // the Ut^T tile
+        tma_store_3d(&tmt, 0, t128row + T128_U * D, 0, u32(sm.wu));
+        tma_store_commit();
+      }
       const uint32_t ucb = u32(sm.uc), ub = u32(sm.wu), kb = u32(st), pb = u32(sm.p);
       const uint32_t id_s = idesc_f16(128, 128, false, true);
       const uint32_t id_o = idesc_f16(128, 64, false, false);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
         mma_f16(tm + TM_S, sdesc(ucb + kk * 32, 16, 1024), sdesc(kb + kk * 2048, 2 * HT, 1024), id_s, true);
-      if (emit) {
+      if (emit_o) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           mma_f16(tm + TM_OA, sdesc(ub + kk * 32, 16, 1024), sdesc(pb + kk * 32, 16, 1024), id_o, kk > 0);
@@ -526,13 +546,14 @@ __global__ void __launch_bounds__(FT, 1)
       __syncwarp();
       if (gate_prefix(gn, sm.gt[stage ^ 1]) && lane == 0 && err) atomicOr(err, 1);
     }
+    if (tid == 0 && save_c && emit_o) tma_store_wait_read();  // the Ut^T store has read wu (O staging)
     if (__syncthreads_or(!mma_wait())) {
       failed = true;
       break;
     }
 
     // ---- O^T = Oi^T diag(gam) + Oa^T -> bf16 [token][d_v] staging in wu (free now) -> coalesced rows of o
-    if (emit) {
+    if (emit_o) {
       bf16 *stg = reinterpret_cast<bf16 *>(sm.wu);
       const int c0 = wg * 16;
       float v[16], va[16];
@@ -544,7 +565,7 @@ __global__ void __launch_bounds__(FT, 1)
     }
     fence_before();
     __syncthreads();
-    if (emit) {
+    if (emit_o) {
       const uint4 *stg = reinterpret_cast<const uint4 *>(sm.wu);
       bf16 *og = static_cast<bf16 *>(a.o);
       for (int e = tid; e < CH * (D / 8); e += FT) {
@@ -581,12 +602,12 @@ __global__ void __launch_bounds__(FT, 1)
 size_t fwd_tc_smem_bytes() { return sizeof(TcSmem) + 1024; }
 
 int launch_fwd_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                  const CUtensorMap &tw, const CUtensorMap &ts, dim3 grid, cudaStream_t st) {
+                  const CUtensorMap &tw, const CUtensorMap &ts, const CUtensorMap &tt, dim3 grid, cudaStream_t st) {
   const size_t smem = fwd_tc_smem_bytes();
   static_assert(sizeof(TcSmem) + 1024 <= 232448 - 256, "shared memory budget (the rest: static shared memory)");
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  fwd_tc_kernel<<<grid, FT, smem, st>>>(a, tq, tk, tv, tw, ts);
+  fwd_tc_kernel<<<grid, FT, smem, st>>>(a, tq, tk, tv, tw, ts, tt);
   return (int)cudaGetLastError();
 }
 

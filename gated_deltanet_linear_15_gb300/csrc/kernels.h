@@ -26,10 +26,18 @@ struct FwdArgs {
   int H, Lseg;
   float scale;
   unsigned flags;
-  int pass;  // 0: segment end states / transitions, 1: outputs (+ states if set), 2: states only
-  const void *wy;  // precomputed WY tiles (backward only) or NULL: X1/X2 come by TMA, no inverse
-  void *wy_save;   // outputs pass (bf16, d = 128): also write the inline X1, X2, Ahat tiles here, or NULL
+  int pass;  // 0: segment end states / transitions, 1: outputs (+ saves if set), 2: states only
+  // pass 1, bf16 with d = 128: the chunk context tiles for the backward (both set, or both NULL), see
+  // T64_* and T128_*; with o == NULL the pass writes no output and only produces states and tiles
+  void *t64, *t128;
 };
+
+// Chunk context tiles of every (chunk, head), fp16 row-major, written by the forward:
+//   t64  [CH_max, H, 5, 64, 64]:  X1 = Ahat diag(beta), X2 = lower(diag(gp) Ahat diag(beta rgp)), Ahat,
+//                                 P = diag(gp) tril(Q K^T) diag(rgp), N = K K^T (normalised keys)
+//   t128 [CH_max, H, 2, 128, 64]: W^T with its token columns scaled by gam (rows d_k), Ut^T (rows d_v)
+constexpr int T64_X1 = 0, T64_X2 = 1, T64_AH = 2, T64_P = 3, T64_N = 4, T64_TILES = 5;
+constexpr int T128_W = 0, T128_U = 1, T128_TILES = 2;
 
 struct BwdArgs {
   const void *q, *k, *v, *dO;
@@ -46,7 +54,6 @@ struct BwdArgs {
   float scale;
   unsigned flags;
   int pass;  // reverse chain: 0 segment starts / transitions, 1 per-chunk dS
-  const void *wy;  // precomputed WY tiles or NULL
 };
 
 struct FixupArgs {
@@ -58,17 +65,6 @@ struct FixupArgs {
   unsigned flags;
   int reverse;
   const int *fixflag;  // nonzero iff some segment of this direction needs the fix-up (NULL: always run)
-};
-
-// WY tiles of every (chunk, head): fp16 [CH_max, H, 3, 64, 64] = X1, X2, Ahat (row-major)
-struct WyArgs {
-  const void *k;
-  const float *g, *beta;
-  Plan plan;
-  void *wy;
-  int *status;
-  int H;
-  unsigned flags;
 };
 
 struct RecArgs {
@@ -90,16 +86,18 @@ int launch_fixup(const FixupArgs &a, int N, cudaStream_t st);
 
 int launch_fwd_chunk(const FwdArgs &a, bool is_bf16, int D, dim3 grid, cudaStream_t st);
 // tcgen05 forward for bf16 inputs and d = 128; q, k, v tensor maps over [tokens, H, 128] with a 64 x 1 x 64 box;
-// tw: the WY tiles as [rows, 64] fp16 with a 64 x 64 box (used when a.wy != NULL)
+// stores: t64 tiles ([rows, 64] fp16, box 64 x 64), chunk-start states ([rows, 128] fp16, box 64 x 128), t128
+// tiles ([rows, 64] fp16, box 64 x 128)
 int launch_fwd_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                  const CUtensorMap &tw, const CUtensorMap &ts, dim3 grid, cudaStream_t st);
-int launch_wy(const WyArgs &a, int CH_max, cudaStream_t st);
+                  const CUtensorMap &t64, const CUtensorMap &ts, const CUtensorMap &t128, dim3 grid, cudaStream_t st);
 int launch_bwd_chain(const BwdArgs &a, bool is_bf16, int D, dim3 grid, cudaStream_t st);
-// tcgen05 reverse chain (bf16, d = 128); maps: q, k, dO ([tokens, H, 128] bf16, box 64x1x64) and the WY tiles
+// tcgen05 reverse chain (bf16, d = 128); maps: q, k, dO ([tokens, H, 128] bf16, box 64x1x64), the t64 and
+// t128 context tiles, and the per-chunk dS store ([rows, 128] fp16, box 64x128x1)
 int launch_bwd_chain_tc(const BwdArgs &a, const CUtensorMap *maps, dim3 grid, cudaStream_t st);
 int launch_bwd_local(const BwdArgs &a, bool is_bf16, int D, int CH_max, cudaStream_t st);
-// tcgen05 local-gradient kernel (bf16, d = 128); maps: q, k, v, dO ([tokens, H, 128] bf16, box 64x1x64) and
-// the fp16 per-chunk states S0 and dS ([rows, 128] as a 3-D map, box 64x128x1), and the WY tiles
+// tcgen05 local-gradient kernel (bf16, d = 128); maps: q, k, v, dO ([tokens, H, 128] bf16, box 64x1x64), the
+// fp16 per-chunk states S0 and dS ([rows, 128] as a 3-D map, box 64x128x1), the t64 and t128 context tiles,
+// and dq, dk, dv (as q)
 int launch_bwd_local_tc(const BwdArgs &a, const CUtensorMap *maps, int CH_max, cudaStream_t st);
 // token-by-token forward over NH = N * H (sequence, head) pairs
 int launch_recurrent(const RecArgs &a, bool is_bf16, int D, int NH, cudaStream_t st);
