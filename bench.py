@@ -81,10 +81,9 @@ def job_throughput(total_ms, world, tokens_per_rank_step, steps):
 # keyed by (profiler name, workload); valid only while the kernel's sources hash to the value
 # recorded with it (otherwise the roofline reports traffic null).  Summaries: profiles/*.md.
 NCU_TRAFFIC = {
-    ("bwd_local", "prefill_h32_t8192"): (819536896, "bwd_local_tc.cu", "6d84e77c48b48277"),
-    ("fwd_states", "prefill_h32_t8192"): (325058816, "fwd_tc.cu", "0a074519219164b2"),
-    ("bwd_chain", "prefill_h32_t8192"): (363377152, "bwd_chain_tc.cu", "07c13c77f2a474d8"),
-    ("bwd_wy", "prefill_h32_t8192"): (118649344, "wy.cu", "ef5bc4fe7faa6858"),
+    ("bwd_local", "prefill_h32_t8192"): (958345728, "bwd_local_tc.cu", "18a593aeba9b828e"),
+    ("fwd_chunk", "prefill_h32_t8192"): (670688768, "fwd_tc.cu", "ee68a43e255105ab"),
+    ("bwd_chain", "prefill_h32_t8192"): (445985792, "bwd_chain_tc.cu", "105040e468d43810"),
 }
 KERNEL_COMMON = ["chunk_common.cuh", "umma.cuh", "common.cuh", "kernels.h"]
 

@@ -186,12 +186,21 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     while (item < n_items && a.plan.chunk_seq[item / H] < 0) item += gridDim.x;
     return item;
   };
-  auto item_tok0 = [&](int item) {
-    const int gc = item / H, n = a.plan.chunk_seq[gc];
-    return a.plan.seq_bos[n] + (gc - a.plan.seq_chunk0[n]) * CH;
+  // first token and valid rows of a work item (plan lookups, done one item ahead)
+  struct ItemInfo {
+    int item, tok0, nvalid;
   };
-  auto issue_main = [&](int item) {  // K, Q, V, S0, dS and the context tiles Ut^T, P, N
-    const int hh = item % H, t0 = item_tok0(item), srow = item * D;  // state rows of (chunk, head)
+  auto info_of = [&](int item) {
+    ItemInfo r{item, 0, 0};
+    if (item < n_items) {
+      const int gc = item / H, n = a.plan.chunk_seq[gc], lc = gc - a.plan.seq_chunk0[n];
+      r.tok0 = a.plan.seq_bos[n] + lc * CH;
+      r.nvalid = min(CH, a.plan.seq_len[n] - lc * CH);
+    }
+    return r;
+  };
+  auto issue_main = [&](int item, int t0) {  // K, Q, V, S0, dS and the context tiles Ut^T, P, N
+    const int hh = item % H, srow = item * D;  // state rows of (chunk, head)
     const uint32_t bar = u32(&sm.bar_a);
     mbar_expect_tx(bar, 18 * HT);
     tma_load_3d(u32(sm.ut), &tmu, 0, (item * T128_TILES + T128_U) * D, 0, bar);
@@ -208,8 +217,8 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     tma_load_3d(u32(sm.ds), &tmds, 0, srow, 0, bar);
     tma_load_3d(u32(sm.ds + 2 * HT), &tmds, 64, srow, 0, bar);
   };
-  auto issue_do = [&](int item) {
-    const int hh = item % H, t0 = item_tok0(item);
+  auto issue_do = [&](int item, int t0) {
+    const int hh = item % H;
     const uint32_t bar = u32(&sm.bar_b);
     mbar_expect_tx(bar, 2 * HT);
     tma_load_3d(u32(sm.dob), &tmdo, 0, hh, t0, bar);
@@ -225,22 +234,18 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     tma_load_3d(u32(sm.x2), &tmw, 0, row + T64_X2 * CH, 0, bar);
     tma_load_3d(u32(sm.ah), &tmw, 0, row + T64_AH * CH, 0, bar);
   };
-  int item = next_valid(blockIdx.x);
-  if (tid == 0 && item < n_items) {
-    issue_main(item);
-    issue_do(item);
-    issue_wy(item);
+  ItemInfo cur = info_of(next_valid(blockIdx.x));
+  if (tid == 0 && cur.item < n_items) {
+    issue_main(cur.item, cur.tok0);
+    issue_do(cur.item, cur.tok0);
+    issue_wy(cur.item);
   }
-  bool pend_main = item < n_items, pend_do = pend_main, pend_wy = pend_main, failed = false;
+  bool pend_main = cur.item < n_items, pend_do = pend_main, pend_wy = pend_main, failed = false;
   uint32_t it = 0;  // parity of the TMA barriers: one completion per item
-  for (; item < n_items; ++it) {
-  const int nitem = next_valid(item + gridDim.x);
-  const int gc = item / H, h = item % H;
-  const int n = a.plan.chunk_seq[gc];
-  const int lc = gc - a.plan.seq_chunk0[n];
-  const int len = a.plan.seq_len[n];
-  const int tok0 = a.plan.seq_bos[n] + lc * CH;
-  const int nvalid = min(CH, len - lc * CH);
+  for (; cur.item < n_items; ++it) {
+  const ItemInfo nxt = info_of(next_valid(cur.item + gridDim.x));  // consumed late in this item
+  const int nitem = nxt.item;
+  const int item = cur.item, h = item % H, tok0 = cur.tok0, nvalid = cur.nvalid;
   const int gbuf = it & 1;
   Gates &G = sm.gt[gbuf];
   float *const gbeta = sm.beta[gbuf];
@@ -248,14 +253,7 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     if (tid < 64) sm.g[0][tid] = tid < nvalid ? a.g[(size_t)(tok0 + tid) * H + h] : 0.f;
     else if (tid < 128) sm.beta[0][tid - 64] = (tid - 64) < nvalid ? a.beta[(size_t)(tok0 + tid - 64) * H + h] : 0.f;
   }
-  float gb_next = 0.f;  // g (tid < 64) or beta (64 <= tid < 128) of the next item, stored mid-item
-  if (nitem < n_items && tid < 128) {
-    const int ngc = nitem / H, nh = nitem % H, nn = a.plan.chunk_seq[ngc];
-    const int nlc = ngc - a.plan.seq_chunk0[nn];
-    const int ntok0 = a.plan.seq_bos[nn] + nlc * CH, nnv = min(CH, a.plan.seq_len[nn] - nlc * CH);
-    const int r = tid & 63;
-    if (r < nnv) gb_next = tid < 64 ? a.g[(size_t)(ntok0 + r) * H + nh] : a.beta[(size_t)(ntok0 + r) * H + nh];
-  }
+  float gb_next = 0.f;  // g (tid < 64) or beta (64 <= tid < 128) of the next item, loaded under P2
   {
     const bool ok = mbar_wait(u32(&sm.bar_a), it & 1, err, 8) && mbar_wait(u32(&sm.bar_b), it & 1, err, 8);
     pend_main = pend_do = false;
@@ -329,6 +327,11 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     mma_commit(u32(&sm.bar_mma));
   }
   __syncwarp();
+  if (nitem < n_items && tid < 128) {  // the next item's g or beta, stored mid-item
+    const int r = tid & 63, nh = nitem % H;
+    if (r < nxt.nvalid)
+      gb_next = tid < 64 ? a.g[(size_t)(nxt.tok0 + r) * H + nh] : a.beta[(size_t)(nxt.tok0 + r) * H + nh];
+  }
   {  // meanwhile: <dS, S0> over the whole state (both tiles share one layout, so compare byte positions)
     float acc = 0.f;
     const uint4 *A4 = reinterpret_cast<const uint4 *>(sm.s0), *B4 = reinterpret_cast<const uint4 *>(sm.ds);
@@ -643,7 +646,7 @@ float rg[8];
   if (nitem < n_items) {  // dO of the next item into its (now free) buffer
     if (tid == 0) {
       tma_store_wait_read();  // the dq tile store has read dob
-      issue_do(nitem);
+      issue_do(nitem, nxt.tok0);
     }
     pend_do = true;
   }
@@ -743,7 +746,7 @@ float rg[8];
   fence_async_smem();
   __syncthreads();
   if (nitem < n_items) {  // K, Q, V, S0, dS of the next item: their buffers are free after P9
-    if (tid == 0) issue_main(nitem);
+    if (tid == 0) issue_main(nitem, nxt.tok0);
     pend_main = true;
   }
   {  // R9: dk^T = Ka + cdec * Kb (lanes d_k); Jacobian; dk out
@@ -841,7 +844,7 @@ float rg[8];
     if (tid == 0) issue_wy(nitem);
     pend_wy = true;
   }
-  item = nitem;
+  cur = nxt;
   }
   if (failed) {  // let prefetches already in flight land before the CTA leaves (bounded waits)
     if (pend_main) mbar_wait(u32(&sm.bar_a), (it + 1) & 1, err, 8);

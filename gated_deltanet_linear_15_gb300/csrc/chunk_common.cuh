@@ -169,10 +169,16 @@ __device__ __forceinline__ void umma_fence_proxy() { asm volatile("fence.proxy.a
 // (c even), the zero upper blocks only when with_zeros; with NF_T the strict
 // lower part is also stored transposed into
 // the strict upper triangle of nf.  Uses warps 0-7 (any further warps only join
-// the barriers); ends with a proxy fence and __syncthreads().
-template <bool PRECISE, bool NF_T, class Out>
+// the barriers, or, with WARPS8, do not take part at all); ends with a proxy
+// fence and a barrier.
+template <bool PRECISE, bool NF_T, bool WARPS8 = false, class Out>
 __device__ __forceinline__ void wy_inverse(float *nf, int ldn, const float *beta, float *dinv, Out out,
                                            bool with_zeros = true) {
+  // WARPS8: called by warps 0-7 only, which synchronise among themselves (named barrier 1)
+  auto bar = [] {
+    if (WARPS8) asm volatile("bar.sync 1, 256;\n" ::: "memory");
+    else __syncthreads();
+  };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int DL = 17;  // dinv row stride
   if (warp < 4 && lane < 16) {  // column jj of block warp; rows of N read as 16-byte vectors (broadcast)
@@ -203,7 +209,7 @@ __device__ __forceinline__ void wy_inverse(float *nf, int ldn, const float *beta
 #pragma unroll
     for (int r = 0; r < 16; ++r) dinv[(b + r) * DL + jj] = x[r];
   }
-  __syncthreads();
+  bar();
   auto mma = [&](float(&c)[4], const float(&av)[4], const float(&bv)[2]) {
     if (PRECISE) {
       mma_3xtf32(c, av, bv);
@@ -257,7 +263,7 @@ __device__ __forceinline__ void wy_inverse(float *nf, int ldn, const float *beta
       nf[(16 * J + c) * ldn + 16 * I + r] = x1v[e];
     }
   }
-  __syncthreads();
+  bar();
   // level 2: Y = T_LL E0 (32 x 32, stored transposed in the upper-right quadrant), then X_LL = -E1 Y;
   // warp (mt, nt) owns the m16n8 tile at rows 16 mt, columns 8 nt.  Block relations are warp-uniform.
   const int mt = (warp >> 2) & 1, nt = warp & 3;
@@ -287,7 +293,7 @@ __device__ __forceinline__ void wy_inverse(float *nf, int ldn, const float *beta
       nf[j * ldn + 32 + i] = y[e];
     }
   }
-  __syncthreads();
+  bar();
   float xl[4] = {0.f, 0.f, 0.f, 0.f};
   if (warp < 8) {
     const int a0 = 32 + 16 * mt;
@@ -311,7 +317,7 @@ __device__ __forceinline__ void wy_inverse(float *nf, int ldn, const float *beta
       mma(xl, av, bv);
     }
   }
-  __syncthreads();  // Y is read; its slots may now take the transposed lower-left block
+  bar();  // Y is read; its slots may now take the transposed lower-left block
   if (warp < 8) {
     auto give = [&](int r, int c, float a0, float a1) {
       out(r, c, a0, a1);
@@ -350,7 +356,7 @@ __device__ __forceinline__ void wy_inverse(float *nf, int ldn, const float *beta
     }
   }
   umma_fence_proxy();  // shared-memory operands written above are read by the tensor-core async proxy
-  __syncthreads();
+  bar();
 }
 
 }  // namespace gdn

@@ -54,6 +54,7 @@ struct __align__(1024) TcSmem {
   float ys[1152];
   uint64_t bar_tma[2];
   uint64_t bar_mma;
+  uint64_t bar_kq;  // MMA 1 ([K; Q] K^T) of a chunk, issued right after the previous chunk's MMA 4
   uint32_t tmem_base;
 };
 
@@ -134,6 +135,7 @@ __global__ void __launch_bounds__(FT, 1)
     mbar_init(u32(&sm.bar_tma[0]), 1);
     mbar_init(u32(&sm.bar_tma[1]), 1);
     mbar_init(u32(&sm.bar_mma), 1);
+    mbar_init(u32(&sm.bar_kq), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
@@ -205,13 +207,24 @@ __global__ void __launch_bounds__(FT, 1)
   fence_after();
 
   int *err = a.status;
-  uint32_t mma_phase = 0;
+  uint32_t mma_phase = 0, kq_phase = 0;
   bool failed = false;
   auto mma_wait = [&]() {
     const bool ok = mbar_wait(u32(&sm.bar_mma), mma_phase, err, 4);
     mma_phase ^= 1;
     fence_after();
     return ok;
+  };
+  // MMA 1: [K; Q] K^T of the chunk in ring stage `stg` -> TM_KQ (M = 128, N = 64, K = 128); thread 0
+  auto issue_mma1 = [&](const uint8_t *stg) {
+    const uint32_t idesc = idesc_f16(128, 64, false, false);
+    const uint32_t base = u32(stg);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint32_t koff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
+      mma_f16(tm + TM_KQ, sdesc(base + koff, 16, 1024), sdesc(base + koff, 16, 1024), idesc, kk > 0);
+    }
+    mma_commit(u32(&sm.bar_kq));
   };
 
   // In-place operand preparation of one ring stage: bf16 -> fp16, L2 norm of the q/k rows (q also
@@ -320,22 +333,20 @@ __global__ void __launch_bounds__(FT, 1)
     __syncthreads();
 
     {
-      // ---- MMA 1: [K; Q] K^T  (M = 128, N = 64, K = 128)
-      if (tid == 0) {
+      // ---- MMA 1: [K; Q] K^T (the first chunk here; later chunks had it issued after the previous MMA 4)
+      if (it == 0 && tid == 0) {
         fence_after();
-        const uint32_t idesc = idesc_f16(128, 64, false, false);
-        const uint32_t base = u32(st);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t koff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
-          mma_f16(tm + TM_KQ, sdesc(base + koff, 16, 1024), sdesc(base + koff, 16, 1024), idesc, kk > 0);
-        }
-        mma_commit(u32(&sm.bar_mma));
+        issue_mma1(st);
       }
       __syncwarp();
-      if (__syncthreads_or(!mma_wait())) {
-        failed = true;
-        break;
+      {
+        const bool ok = mbar_wait(u32(&sm.bar_kq), kq_phase, err, 4);
+        kq_phase ^= 1;
+        fence_after();
+        if (__syncthreads_or(!ok)) {
+          failed = true;
+          break;
+        }
       }
 
       // ---- read-out: N (fp32, rows 0-63) and P (fp16, rows 64-127); each warp takes 16 columns
@@ -372,7 +383,10 @@ __global__ void __launch_bounds__(FT, 1)
 
       // ---- Ahat (fp32 diagonal blocks, TF32 tensor-core merges) -> X1, X2 (fp16, K-major: rows = r);
       // a saved-context forward also stages Ahat, and stores the three tiles below
-      wy_inverse<false, false>(sm.nf, LN, gbeta, sm.ys, [&](int r, int c, float a0, float a1) {
+      // (warps 0-7); meanwhile warps 8-15 copy S0 to its fp16 operand form and put gam_C * S0 back into
+      // TMEM (the copy is also the chunk-start state that the backward reads)
+      if (warp < 8) {
+      wy_inverse<false, false, true>(sm.nf, LN, gbeta, sm.ys, [&](int r, int c, float a0, float a1) {
         const float2 bb = *reinterpret_cast<const float2 *>(gbeta + c), rg = *reinterpret_cast<const float2 *>(G.rgp + c);
         const float gr = G.gp[r], x0 = a0 * bb.x, x1 = a1 * bb.y;
         const uint32_t off = sw128_offset(r, c);
@@ -381,6 +395,25 @@ __global__ void __launch_bounds__(FT, 1)
             __floats2half2_rn(c <= r ? x0 * (gr * rg.x) : 0.f, c + 1 <= r ? x1 * (gr * rg.y) : 0.f);
         if (save_wy) *reinterpret_cast<__half2 *>(sm.ah + off) = __floats2half2_rn(a0, a1);
       }, it == 0);
+      } else {
+        const float gC = G.gamC;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          const int c0 = (wg - 2) * 64 + half * 32;
+          float v[32];
+          tmem_ld32(tm + tm_lane + TM_S + c0, v);
+          const int kb = c0 >> 6;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) st_chunk_f16(sm.s0 + kb * 2 * HT + chunk_off(row, c0 + q4 * 8), v + q4 * 8);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= gC;
+          tmem_st32(tm + tm_lane + TM_S + c0, v);
+        }
+        fence_async_smem();  // the fp16 state copy is an operand of MMA 3 and of Oi
+      }
+      fence_before();
+      __syncthreads();
+      fence_after();
     }
 
     // ---- MMA 2: W^T = K^T X1^T, U^T = V^T X2^T  (M = 128, N = 64, K = 64)
@@ -408,23 +441,6 @@ __global__ void __launch_bounds__(FT, 1)
       mma_commit(u32(&sm.bar_mma));
     }
     __syncwarp();
-    // meanwhile: S0 -> fp16 operand copy, gam_C * S0 back into TMEM (the copy is also the chunk-start
-    // state that the backward reads)
-    {
-      const float gC = G.gamC;
-      {
-        const int c0 = wg * 32;
-        float v[32];
-        tmem_ld32(tm + tm_lane + TM_S + c0, v);
-        const int kb = c0 >> 6;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) st_chunk_f16(sm.s0 + kb * 2 * HT + chunk_off(row, c0 + q4 * 8), v + q4 * 8);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= gC;
-        tmem_st32(tm + tm_lane + TM_S + c0, v);
-      }
-    }
-    fence_async_smem();  // the fp16 state copy is read by the tensor core next
     if (__syncthreads_or(!mma_wait())) {
       failed = true;
       break;
@@ -535,6 +551,9 @@ __global__ void __launch_bounds__(FT, 1)
           mma_f16(tm + TM_OA, sdesc(ub + kk * 32, 16, 1024), sdesc(pb + kk * 32, 16, 1024), id_o, kk > 0);
       }
       mma_commit(u32(&sm.bar_mma));
+      // the next chunk's Gram product: its K, Q were normalised while MMA 3 ran; it runs during this
+      // chunk's O read-out
+      if (more) issue_mma1(stn);
     }
     __syncwarp();
     if (more && need_v) prep_v(stn, nvn);  // the next chunk's V, while MMA 4 runs
