@@ -58,6 +58,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   extern __shared__ unsigned char smraw[];
   ChainTcSmem &sm =
       *reinterpret_cast<ChainTcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+  pdl_trigger();
+  pdl_wait();
   const int s = blockIdx.x, h = blockIdx.y, role = blockIdx.z;
   // pass A of a call in which no segment needs the exact fix-up (status[2], set after the gate scan)
   if (a.pass == 0 && a.status && a.status[2] == 0) return;
@@ -384,8 +386,8 @@ int launch_bwd_chain_tc(const BwdArgs &a, const CUtensorMap *maps, dim3 grid, cu
   static_assert(sizeof(ChainTcSmem) + 1024 <= 232448 - 256, "shared memory budget (the rest: static shared memory)");
   cudaError_t e = cudaFuncSetAttribute(bwd_chain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  bwd_chain_tc_kernel<<<grid, NTHREADS, smem, st>>>(a, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5]);
-  return (int)cudaGetLastError();
+  return (int)launch_pdl(bwd_chain_tc_kernel, grid, dim3(NTHREADS), smem, st, a, maps[0], maps[1], maps[2], maps[3],
+                         maps[4], maps[5]);
 }
 
 }  // namespace gdn

@@ -118,6 +118,8 @@ __global__ void __launch_bounds__(LTHREADS, 1)
   extern __shared__ unsigned char smraw[];
   LocalTcSmem &sm =
       *reinterpret_cast<LocalTcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+  pdl_trigger();
+  pdl_wait();
   if (a.flags & kFlagDebugWaitTimeout) {  // test hook: an expiring bounded wait, then return
     __shared__ uint64_t dbg_bar;
     if (threadIdx.x == 0) debug_expire_wait(&dbg_bar, a.status, 4);
@@ -874,9 +876,8 @@ int launch_bwd_local_tc(const BwdArgs &a, const CUtensorMap *maps, int CH_max, c
   }
   const int n_items = CH_max * a.H;
   const int grid = n_items < sms ? n_items : sms;  // persistent: one CTA per SM
-  bwd_local_tc_kernel<<<grid, LTHREADS, smem, st>>>(a, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
-                                                    maps[6], maps[7], maps[8], maps[9], maps[10], n_items);
-  return (int)cudaGetLastError();
+  return (int)launch_pdl(bwd_local_tc_kernel, dim3(grid), dim3(LTHREADS), smem, st, a, maps[0], maps[1], maps[2],
+                         maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], maps[9], maps[10], n_items);
 }
 
 }  // namespace gdn

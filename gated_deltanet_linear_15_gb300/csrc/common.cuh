@@ -269,4 +269,27 @@ __device__ __forceinline__ int bwd_start_mode(const float *gsum, int H, int h, i
   return START_FIXUP;
 }
 
+// Programmatic dependent launch.  A kernel started with launch_pdl may be scheduled while the
+// previous kernel on its stream is still finishing: it calls pdl_trigger() (its own dependents may
+// then be scheduled) and pdl_wait() (returns once the previous grid has completed and its memory
+// is visible) before it touches global memory.  Launched without the attribute, both are no-ops.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace gdn

@@ -81,6 +81,8 @@ __global__ void __launch_bounds__(FT, 1)
                   const __grid_constant__ CUtensorMap tms, const __grid_constant__ CUtensorMap tmt) {
   extern __shared__ unsigned char smraw[];
   TcSmem &sm = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+  pdl_trigger();
+  pdl_wait();
 
   const int s = blockIdx.x, h = blockIdx.y, role = blockIdx.z;
   // pass A of a call in which no segment needs the exact fix-up (status[1], set after the gate scan)
@@ -626,8 +628,7 @@ int launch_fwd_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk
   static_assert(sizeof(TcSmem) + 1024 <= 232448 - 256, "shared memory budget (the rest: static shared memory)");
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  fwd_tc_kernel<<<grid, FT, smem, st>>>(a, tq, tk, tv, tw, ts, tt);
-  return (int)cudaGetLastError();
+  return (int)launch_pdl(fwd_tc_kernel, grid, dim3(FT), smem, st, a, tq, tk, tv, tw, ts, tt);
 }
 
 }  // namespace gdn

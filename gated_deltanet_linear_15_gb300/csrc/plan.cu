@@ -21,6 +21,8 @@ namespace gdn {
 // cu_seqlens (not starting at 0, decreasing, or not ending at T) sets status
 // bit 1 and leaves every sequence empty, so the chunk kernels do nothing.
 __global__ void plan_kernel(Plan p, const int *cu, int N, int T, int Lseg, int S_max, int CH_max, int *status) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int carry_c, carry_s, bad;
   __shared__ int wsum_c[32], wsum_s[32];
   const int tid = threadIdx.x, nt = blockDim.x;
@@ -134,8 +136,7 @@ __global__ void plan_kernel(Plan p, const int *cu, int N, int T, int Lseg, int S
 
 int launch_plan(const Plan &p, const int *cu, int N, int T, int Lseg, int S_max, int CH_max, int *status,
                 cudaStream_t st) {
-  plan_kernel<<<1, 1024, 0, st>>>(p, cu, N, T, Lseg, S_max, CH_max, status);
-  return (int)cudaGetLastError();
+  return (int)launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, st, p, cu, N, T, Lseg, S_max, CH_max, status);
 }
 
 // One block per global chunk: the chunk's log-gates of 32 heads at a time are
@@ -150,6 +151,8 @@ __device__ void fixup_modes(const Plan &p, const float *gsum, int H, int Lseg, i
 // over every (segment, head) (status[3] counts finished blocks; the plan kernel zeroed it).
 __global__ void __launch_bounds__(256) gate_scan_kernel(Plan p, const float *g, int H, float *gsum, int *status,
                                                         int modes, int Lseg, int S_max, unsigned flags) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float tile[CH][33];
   __shared__ int last;
   const int c = blockIdx.x;
@@ -201,8 +204,8 @@ __global__ void __launch_bounds__(256) gate_scan_kernel(Plan p, const float *g, 
 int launch_gate_scan(const Plan &p, const float *g, int H, int CH_max, float *gsum, int *status, int modes, int Lseg,
                      int S_max, unsigned flags, cudaStream_t st) {
   if (CH_max == 0) return 0;
-  gate_scan_kernel<<<CH_max, 256, 0, st>>>(p, g, H, gsum, status, modes, Lseg, S_max, flags);
-  return (int)cudaGetLastError();
+  return (int)launch_pdl(gate_scan_kernel, dim3(CH_max), dim3(256), 0, st, p, g, H, gsum, status, modes, Lseg, S_max,
+                         flags);
 }
 
 // Does any segment start (forward) or end (reverse) need the exact fix-up?  status[1] / status[2]
@@ -220,25 +223,35 @@ __device__ void fixup_modes(const Plan &p, const float *gsum, int H, int Lseg, i
     const int j = s - __ldcg(p.seq_seg0 + n), nseg = __ldcg(p.seq_nseg + n), chunk0 = __ldcg(p.seq_chunk0 + n);
     const int nchunks = (__ldcg(p.seq_len + n) + CH - 1) / CH;
     const int cbeg = j * Lseg, cend = min((j + 1) * Lseg, nchunks);
-    // the start-mode rules of the chunk kernels, on L2-coherent loads of gsum
+    // the start-mode rules of the chunk kernels, on L2-coherent loads of gsum: all WMAX sums of
+    // each window are loaded at once (no dependent load chain), then scanned
     if (j > 0) {
+      float gs[WMAX];
+#pragma unroll
+      for (int ww = 1; ww <= WMAX; ++ww) gs[ww - 1] = ww <= cbeg ? __ldcg(gsum + (size_t)(chunk0 + cbeg - ww) * H + h) : 0.f;
       bool warm = false;
       if (window) {
         float acc = 0.f;
-        for (int ww = 1; ww <= WMAX && ww <= cbeg && !warm; ++ww) {
-          acc += __ldcg(gsum + (size_t)(chunk0 + cbeg - ww) * H + h);
-          warm = acc <= LN_EPS_WINDOW;
+#pragma unroll
+        for (int ww = 1; ww <= WMAX; ++ww) {
+          acc += gs[ww - 1];
+          warm |= ww <= cbeg && acc <= LN_EPS_WINDOW;
         }
       }
       fwd_fix |= !warm;
     }
     if (j < nseg - 1) {
+      float gs[WMAX];
+#pragma unroll
+      for (int ww = 1; ww <= WMAX; ++ww)
+        gs[ww - 1] = cend + ww <= nchunks ? __ldcg(gsum + (size_t)(chunk0 + cend + ww - 1) * H + h) : 0.f;
       bool warm = false;
       if (window) {
         float acc = 0.f;
-        for (int ww = 1; ww <= WMAX && cend + ww <= nchunks && !warm; ++ww) {
-          acc += __ldcg(gsum + (size_t)(chunk0 + cend + ww - 1) * H + h);
-          warm = acc <= LN_EPS_WINDOW;
+#pragma unroll
+        for (int ww = 1; ww <= WMAX; ++ww) {
+          acc += gs[ww - 1];
+          warm |= cend + ww <= nchunks && acc <= LN_EPS_WINDOW;
         }
       }
       bwd_fix |= !warm;
@@ -253,6 +266,8 @@ constexpr int FIX_ROWS = 8;
 
 template <int D>
 __global__ void __launch_bounds__(256, 4) fixup_kernel(FixupArgs a) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float cur[FIX_ROWS][D];
   const int rb = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
   const int H = a.H;
@@ -323,10 +338,9 @@ __global__ void __launch_bounds__(256, 4) fixup_kernel(FixupArgs a) {
 int launch_fixup(const FixupArgs &a, int N, cudaStream_t st) {
   if (N == 0) return 0;
   dim3 grid(a.D / FIX_ROWS, a.H, N);
-  if (a.D == 128) fixup_kernel<128><<<grid, 256, 0, st>>>(a);
-  else if (a.D == 64) fixup_kernel<64><<<grid, 256, 0, st>>>(a);
-  else return -1;
-  return (int)cudaGetLastError();
+  if (a.D == 128) return (int)launch_pdl(fixup_kernel<128>, grid, dim3(256), 0, st, a);
+  if (a.D == 64) return (int)launch_pdl(fixup_kernel<64>, grid, dim3(256), 0, st, a);
+  return -1;
 }
 
 }  // namespace gdn
