@@ -57,9 +57,11 @@ struct Layout {
   size_t off_F = 0, off_R = 0, off_dS = 0;  // reverse fix-up buffers
   size_t off_t64 = 0, off_t128 = 0;        // recomputed chunk context tiles (bf16, d = 128)
   size_t t64_bytes = 0, t128_bytes = 0;
+  size_t off_tqkv = 0, off_nrm = 0, tqkv_bytes = 0, nrm_bytes = 0;
   size_t states_bytes = 0;                  // per-chunk start states
   size_t bwd_saved_total = 0;               // backward workspace when the forward saved its context
-  size_t saved_off_t64 = 0, saved_off_t128 = 0, saved_total = 0;  // saved context: [states][t64][t128]
+  size_t saved_off_t64 = 0, saved_off_t128 = 0, saved_off_tqkv = 0, saved_off_nrm = 0;
+  size_t saved_total = 0;  // saved context: [states][t64][t128][tqkv][nrm]
   size_t fwd_total = 0, bwd_total = 0;
 };
 
@@ -165,10 +167,18 @@ int make_layout(const gdn_shape *s, Layout &L) {
   off += L.t64_bytes;
   L.off_t128 = off;
   off += L.t128_bytes;
+  L.tqkv_bytes = tiles ? align256((size_t)L.CH_max * L.H * TQ_TILES * CH * 128 * 2) : 0;
+  L.nrm_bytes = tiles ? align256((size_t)L.CH_max * L.H * 2 * CH * 4) : 0;
+  L.off_tqkv = off;
+  off += L.tqkv_bytes;
+  L.off_nrm = off;
+  off += L.nrm_bytes;
   L.bwd_total = off;
   L.saved_off_t64 = L.states_bytes;
   L.saved_off_t128 = L.states_bytes + L.t64_bytes;
-  L.saved_total = L.states_bytes + L.t64_bytes + L.t128_bytes;
+  L.saved_off_tqkv = L.saved_off_t128 + L.t128_bytes;
+  L.saved_off_nrm = L.saved_off_tqkv + L.tqkv_bytes;
+  L.saved_total = L.saved_off_nrm + L.nrm_bytes;
   return GDN_OK;
 }
 
@@ -332,13 +342,13 @@ int state_map(CUtensorMap *m, const void *ptr, long rows) {
   return GDN_OK;
 }
 
-// 64-column fp16 tiles [rows, 64], box = 64 columns x `box_rows` rows, 128-byte swizzle (the t64 tiles with
-// 64-row boxes, the t128 tiles with 128-row boxes)
-int tile_map(CUtensorMap *m, const void *ptr, long rows, int box_rows) {
+// fp16 tiles [rows, cols], box = 64 columns x `box_rows` rows, 128-byte swizzle (the t64 tiles with
+// 64-row boxes, the t128 tiles with 128-row boxes, the 128-column tqkv tiles with 64-row boxes)
+int tile_map(CUtensorMap *m, const void *ptr, long rows, int box_rows, int cols = 64) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  cuuint64_t dims[3] = {64, (cuuint64_t)rows, 1};
-  cuuint64_t strides[2] = {64 * 2, (cuuint64_t)rows * 64 * 2};
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, 1};
+  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)rows * cols * 2};
   cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
@@ -353,26 +363,31 @@ int t64_map(CUtensorMap *m, const Layout &L, const void *ptr) {
 int t128_map(CUtensorMap *m, const Layout &L, const void *ptr) {
   return tile_map(m, ptr, (long)L.CH_max * L.H * T128_TILES * 128, 128);
 }
+int tqkv_map(CUtensorMap *m, const Layout &L, const void *ptr) {
+  return tile_map(m, ptr, (long)L.CH_max * L.H * TQ_TILES * CH, 64, 128);
+}
 
 // The chunk forward kernel for this problem: tcgen05 for bf16 with d = 128, the
 // mma.sync/CUDA-core kernel otherwise (d = 64, fp32 inputs, empty batches).
 int launch_forward_kernel(const Layout &L, const gdn_shape *s, const FwdArgs &fa, dim3 grid, cudaStream_t st) {
   const bool bf = s->dtype == GDN_BF16;
   if (bf && L.D == 128 && L.Ttot > 0) {
-    CUtensorMap tq, tk, tv, tw, ts, tt;
+    CUtensorMap tq, tk, tv, tw, ts, tt, t3;
     int rc;
     if ((rc = qkv_map(&tk, fa.k, L.Ttot, L.H))) return rc;
     if ((rc = qkv_map(&tv, fa.v, L.Ttot, L.H))) return rc;
     if ((rc = qkv_map(&tq, fa.q ? fa.q : fa.k, L.Ttot, L.H))) return rc;
     // context tiles and chunk-start states written for the backward (maps unused when not saving)
     if (fa.t64) {
-      if ((rc = t64_map(&tw, L, fa.t64)) || (rc = t128_map(&tt, L, fa.t128))) return rc;
-    } else if ((rc = tile_map(&tw, fa.k, 64, 64)) || (rc = tile_map(&tt, fa.k, 128, 128))) {
+      if ((rc = t64_map(&tw, L, fa.t64)) || (rc = t128_map(&tt, L, fa.t128)) || (rc = tqkv_map(&t3, L, fa.tqkv)))
+        return rc;
+    } else if ((rc = tile_map(&tw, fa.k, 64, 64)) || (rc = tile_map(&tt, fa.k, 128, 128)) ||
+               (rc = tile_map(&t3, fa.k, 64, 64, 128))) {
       return rc;
     }
     if ((rc = state_map(&ts, fa.states ? fa.states : fa.k, fa.states ? (long)L.CH_max * L.H * 128 : 128)))
       return rc;
-    return launch_fwd_tc(fa, tq, tk, tv, tw, ts, tt, grid, st);
+    return launch_fwd_tc(fa, tq, tk, tv, tw, ts, tt, t3, grid, st);
   }
   return launch_fwd_chunk(fa, bf, L.D, grid, st);
 }
@@ -464,6 +479,8 @@ int fwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
     if (L.t64_bytes > 0) {
       fa.t64 = static_cast<char *>(saved) + L.saved_off_t64;
       fa.t128 = static_cast<char *>(saved) + L.saved_off_t128;
+      fa.tqkv = static_cast<char *>(saved) + L.saved_off_tqkv;
+      fa.nrm = reinterpret_cast<float *>(static_cast<char *>(saved) + L.saved_off_nrm);
     }
   }
   return forward_passes(s, L, ws, fa, 1, st);
@@ -498,10 +515,13 @@ int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
   Plan pl;
   if ((rc = prologue(s, L, ws, g, st, pl))) return rc;
   const char *states = ws + L.off_states, *t64 = ws + L.off_t64, *t128 = ws + L.off_t128;
+  const char *tqkv = ws + L.off_tqkv, *nrm = ws + L.off_nrm;
   if (saved) {  // the forward left the chunk-start states and context tiles: nothing to recompute
     states = static_cast<const char *>(saved);
     t64 = states + L.saved_off_t64;
     t128 = states + L.saved_off_t128;
+    tqkv = states + L.saved_off_tqkv;
+    nrm = states + L.saved_off_nrm;
   } else {
     // 1. forward states at every chunk start (and, bf16 with d = 128, the context tiles: a forward
     //    pass that writes no output)
@@ -517,6 +537,8 @@ int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
     if (tiles) {
       fa.t64 = ws + L.off_t64;
       fa.t128 = ws + L.off_t128;
+      fa.tqkv = ws + L.off_tqkv;
+      fa.nrm = reinterpret_cast<float *>(ws + L.off_nrm);
     }
     if ((rc = forward_passes(s, L, ws, fa, tiles ? 1 : 2, st))) return rc;
   }
@@ -545,6 +567,7 @@ int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
     ba.dSend = reinterpret_cast<float *>(ws + L.off_dS);
   }
   ba.states = states;
+  ba.nrm = reinterpret_cast<const float *>(nrm);
   ba.dstates = ws + L.off_dstates;
   ba.H = L.H;
   ba.Lseg = L.Lseg;
@@ -552,11 +575,10 @@ int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
   ba.flags = s->flags;
   // the reverse chain: tcgen05 for bf16 with d = 128, the mma.sync kernel otherwise
   const bool chain_tc = bf && L.D == 128 && L.Ttot > 0;
-  CUtensorMap cmaps[6];
-  if (chain_tc && ((rc = qkv_map(&cmaps[0], q, L.Ttot, L.H)) || (rc = qkv_map(&cmaps[1], k, L.Ttot, L.H)) ||
-                   (rc = qkv_map(&cmaps[2], dO, L.Ttot, L.H)) || (rc = t64_map(&cmaps[3], L, t64)) ||
-                   (rc = t128_map(&cmaps[4], L, t128)) ||
-                   (rc = state_map(&cmaps[5], ba.dstates, (long)L.CH_max * L.H * 128))))
+  CUtensorMap cmaps[5];
+  if (chain_tc && ((rc = tqkv_map(&cmaps[0], L, tqkv)) || (rc = qkv_map(&cmaps[1], dO, L.Ttot, L.H)) ||
+                   (rc = t64_map(&cmaps[2], L, t64)) || (rc = t128_map(&cmaps[3], L, t128)) ||
+                   (rc = state_map(&cmaps[4], ba.dstates, (long)L.CH_max * L.H * 128))))
     return rc;
   auto chain = [&](dim3 grid) {
     return chain_tc ? launch_bwd_chain_tc(ba, cmaps, grid, st) : launch_bwd_chain(ba, bf, L.D, grid, st);
@@ -591,14 +613,13 @@ int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
   {
     PROF("bwd_local");
     if (bf && L.D == 128 && L.Ttot > 0) {
-      CUtensorMap maps[11];
-      if ((rc = qkv_map(&maps[0], q, L.Ttot, L.H)) || (rc = qkv_map(&maps[1], k, L.Ttot, L.H)) ||
-          (rc = qkv_map(&maps[2], v, L.Ttot, L.H)) || (rc = qkv_map(&maps[3], dO, L.Ttot, L.H)) ||
-          (rc = state_map(&maps[4], states, (long)L.CH_max * L.H * 128)) ||
-          (rc = state_map(&maps[5], ws + L.off_dstates, (long)L.CH_max * L.H * 128)) ||
-          (rc = t64_map(&maps[6], L, t64)) || (rc = qkv_map(&maps[7], dq, L.Ttot, L.H)) ||
-          (rc = qkv_map(&maps[8], dk, L.Ttot, L.H)) || (rc = qkv_map(&maps[9], dv, L.Ttot, L.H)) ||
-          (rc = t128_map(&maps[10], L, t128)))
+      CUtensorMap maps[9];
+      if ((rc = tqkv_map(&maps[0], L, tqkv)) || (rc = qkv_map(&maps[1], dO, L.Ttot, L.H)) ||
+          (rc = state_map(&maps[2], states, (long)L.CH_max * L.H * 128)) ||
+          (rc = state_map(&maps[3], ws + L.off_dstates, (long)L.CH_max * L.H * 128)) ||
+          (rc = t64_map(&maps[4], L, t64)) || (rc = qkv_map(&maps[5], dq, L.Ttot, L.H)) ||
+          (rc = qkv_map(&maps[6], dk, L.Ttot, L.H)) || (rc = qkv_map(&maps[7], dv, L.Ttot, L.H)) ||
+          (rc = t128_map(&maps[8], L, t128)))
         return rc;
       CK(launch_bwd_local_tc(ba, maps, L.CH_max, st));
     } else {

@@ -1,11 +1,11 @@
 // Blackwell-native reverse state chain of the chunked backward (bf16 inputs,
 // d = 128): one CTA per (segment, head), chunks in reverse order, dS (the
 // gradient w.r.t. a chunk's end state) resident in fp32 TMEM.  The forward's
-// chunk context supplies P = diag(gp) tril(Q K^T) diag(rgp) and the
-// gam-scaled W^T of every chunk (TMA, with the inputs), so a chunk is two
-// tensor-core rounds:
-//   dUt^T = dS Kc^T + dO^T P,  dS += dO^T Qg     Kc = diag(cdec) K, Qg = diag(gam) Q
-//   dS <- dS - dUt^T W                          (after gam_C dS and the fp16 copy)
+// chunk context supplies the operand forms of K and Q (normalised, fp16),
+// P = diag(gp) tril(Q K^T) diag(rgp) and the gam-scaled W^T of every chunk
+// (TMA, with dO), so a chunk is dO's conversion and two tensor-core rounds:
+//   Y = dS K^T, Z = dO^T P, dS += (diag(gam) dO)^T Q;   dUt^T = Y diag(cdec) + Z (read-out)
+//   dS <- dS - dUt^T W                                    (after gam_C dS and the fp16 copy)
 // and the fp16 dS at every chunk end goes to the workspace (TMA store) for the
 // local-gradient kernel.  Pass 0 (reverse sequence parallelism) runs a
 // segment from zero (role 0) or the transition from I with dO = 0 (role 1);
@@ -24,14 +24,14 @@ namespace {
 constexpr int D = 128;
 constexpr int HT = 8192;
 constexpr int LN = CH + 4;
-constexpr uint32_t TM_S = 0, TM_DU = 256, TM_COLS = 512;
+constexpr uint32_t TM_S = 0, TM_DU = 256, TM_Y = 320, TM_COLS = 512;
 
 struct __align__(1024) ChainTcSmem {
   // input ring, 2 stages: [K0 | Q0 | K1 | Q1 | dO0 | dO1 | P | W0 W1] half-tiles (0/1 = feature block;
-  // W = the gam-scaled W^T tile [d_k][token], K-major B of dUt^T W)
+  // K, Q the fp16 operand tiles of the context; W = the gam-scaled W^T tile [d_k][token])
   uint8_t ring[2][9 * HT];
-  uint8_t kc[2 * HT];       // diag(cdec) K (K-major B, rows = token); later dUt^T (K-major A, rows = d_v)
-  uint8_t qg[2 * HT];       // diag(gam) Q (MN-major B, rows = token)
+  uint8_t kc[2 * HT];       // dUt^T (K-major A, rows = d_v)
+  uint8_t dog[2 * HT];      // diag(gam) dO (MN-major A, rows = token)
   uint8_t ds16[4 * HT];     // dS fp16 (K-major A: rows = d_v, two k-blocks of 128 rows)
   float g[2][CH];
   Gates gt[2];
@@ -52,9 +52,9 @@ __device__ __forceinline__ void st_chunk_f16(uint8_t *dst, const float *v) {
 }  // namespace
 
 __global__ void __launch_bounds__(NTHREADS, 1)
-    bwd_chain_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                        const __grid_constant__ CUtensorMap tmdo, const __grid_constant__ CUtensorMap tmp,
-                        const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmds) {
+    bwd_chain_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tm3, const __grid_constant__ CUtensorMap tmdo,
+                        const __grid_constant__ CUtensorMap tmp, const __grid_constant__ CUtensorMap tmw,
+                        const __grid_constant__ CUtensorMap tmds) {
   extern __shared__ unsigned char smraw[];
   ChainTcSmem &sm =
       *reinterpret_cast<ChainTcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
@@ -92,7 +92,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     return;
   }
   const bool store = (a.pass == 1);
-  const bool l2 = (a.flags & kFlagL2Norm) != 0;
   const bool with_do = !transition;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wg = warp >> 2;
@@ -107,8 +106,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(u32(&sm.bar_tma[1]), 1);
     mbar_init(u32(&sm.bar_mma), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    tma_prefetch_desc(&tmk);
-    tma_prefetch_desc(&tmq);
+    tma_prefetch_desc(&tm3);
     tma_prefetch_desc(&tmdo);
     tma_prefetch_desc(&tmp);
     tma_prefetch_desc(&tmw);
@@ -129,13 +127,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int crow = (chunk0 + c) * H + h;  // (chunk, head) index of the context tiles
     const uint32_t bar = u32(&sm.bar_tma[stage]);
     uint8_t *st = sm.ring[stage];
+    const int qrow = crow * TQ_TILES * CH;
     mbar_expect_tx(bar, (4 + (with_do ? 5 : 0)) * HT);
-    tma_load_3d(u32(st + 0 * HT), &tmk, 0, h, tok0, bar);
-    tma_load_3d(u32(st + 2 * HT), &tmk, 64, h, tok0, bar);
+    tma_load_3d(u32(st + 0 * HT), &tm3, 0, qrow + TQ_K * CH, 0, bar);
+    tma_load_3d(u32(st + 2 * HT), &tm3, 64, qrow + TQ_K * CH, 0, bar);
     tma_load_3d(u32(st + 7 * HT), &tmw, 0, (crow * T128_TILES + T128_W) * D, 0, bar);
     if (with_do) {
-      tma_load_3d(u32(st + 1 * HT), &tmq, 0, h, tok0, bar);
-      tma_load_3d(u32(st + 3 * HT), &tmq, 64, h, tok0, bar);
+      tma_load_3d(u32(st + 1 * HT), &tm3, 0, qrow + TQ_Q * CH, 0, bar);
+      tma_load_3d(u32(st + 3 * HT), &tm3, 64, qrow + TQ_Q * CH, 0, bar);
       tma_load_3d(u32(st + 4 * HT), &tmdo, 0, h, tok0, bar);
       tma_load_3d(u32(st + 5 * HT), &tmdo, 64, h, tok0, bar);
       tma_load_3d(u32(st + 6 * HT), &tmp, 0, (crow * T64_TILES + T64_P) * CH, 0, bar);
@@ -203,64 +202,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (it == 0 && warp == 0) gate_prefix(sm.g[stage], G);
     __syncthreads();
 
-    // ---- prep: Kc = cdec K^, Qg = gam Q^ (normalised, fp16);  dO -> fp16 in place; rows >= nvalid zero
-    {
-      const bool isq = tid >= 128;
-      if (!isq || with_do) {
-        const int r = (tid >> 1) & 63, hb = tid & 1;
-        const uint8_t *rowp = st + (isq ? HT : 0) + hb * 2 * HT + r * 128;
-        uint32_t raw[32];
+    // ---- prep: dO -> fp16 in place and diag(gam) dO (rows >= nvalid zero); K, Q come as operand tiles
+    if (with_do) {
+      const int r = tid >> 2, qr = tid & 3;
+      uint8_t *rowp = st + 4 * HT + (qr >> 1) * HT + r * 128;
+      uint8_t *rowg = sm.dog + (qr >> 1) * HT + r * 128;
+      const float mul = r < nvalid ? 1.f : 0.f, mg = mul * G.gam[r];
 #pragma unroll
-        for (int chk = 0; chk < 8; ++chk) {
-          const uint4 q4 = *reinterpret_cast<const uint4 *>(rowp + ((chk ^ (r & 7)) * 16));
-          raw[4 * chk] = q4.x;
-          raw[4 * chk + 1] = q4.y;
-          raw[4 * chk + 2] = q4.z;
-          raw[4 * chk + 3] = q4.w;
+      for (int cc = 0; cc < 4; ++cc) {
+        const int off = (((qr & 1) * 4 + cc) ^ (r & 7)) * 16;
+        uint4 q4 = *reinterpret_cast<const uint4 *>(rowp + off);
+        uint4 g4;
+        uint32_t *wv = reinterpret_cast<uint32_t *>(&q4), *gv = reinterpret_cast<uint32_t *>(&g4);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float lo = __uint_as_float(wv[i] << 16), hi = __uint_as_float(wv[i] & 0xffff0000u);
+          const __half2 a2 = __floats2half2_rn(lo * mul, hi * mul), b2 = __floats2half2_rn(lo * mg, hi * mg);
+          wv[i] = *reinterpret_cast<const uint32_t *>(&a2);
+          gv[i] = *reinterpret_cast<const uint32_t *>(&b2);
         }
-        float mul = isq ? a.scale : 1.f;
-        if (l2) {
-          float ss = 0.f;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float lo = __uint_as_float(raw[i] << 16), hi = __uint_as_float(raw[i] & 0xffff0000u);
-            ss = fmaf(lo, lo, fmaf(hi, hi, ss));
-          }
-          ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-          mul *= rsqrtf(ss + 1e-6f);
-        }
-        if (r >= nvalid) mul = 0.f;
-        const float m2 = mul * (isq ? G.gam[r] : G.cdec[r]);
-        uint8_t *row2 = (isq ? sm.qg : sm.kc) + hb * HT + r * 128;
-#pragma unroll
-        for (int chk = 0; chk < 8; ++chk) {
-          uint32_t z[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t wv = raw[4 * chk + i];
-            const __half2 b2 = __floats2half2_rn(__uint_as_float(wv << 16) * m2, __uint_as_float(wv & 0xffff0000u) * m2);
-            z[i] = *reinterpret_cast<const uint32_t *>(&b2);
-          }
-          *reinterpret_cast<uint4 *>(row2 + (chk ^ (r & 7)) * 16) = make_uint4(z[0], z[1], z[2], z[3]);
-        }
-      }
-      if (with_do) {
-        const int r = tid >> 2, qr = tid & 3;
-        uint8_t *rowp = st + 4 * HT + (qr >> 1) * HT + r * 128;
-        const float mul = r < nvalid ? 1.f : 0.f;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const int chk = (qr & 1) * 4 + cc;
-          uint4 q4 = *reinterpret_cast<const uint4 *>(rowp + ((chk ^ (r & 7)) * 16));
-          uint32_t *wv = reinterpret_cast<uint32_t *>(&q4);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const __half2 a2 = __floats2half2_rn(__uint_as_float(wv[i] << 16) * mul,
-                                                 __uint_as_float(wv[i] & 0xffff0000u) * mul);
-            wv[i] = *reinterpret_cast<const uint32_t *>(&a2);
-          }
-          *reinterpret_cast<uint4 *>(rowp + ((chk ^ (r & 7)) * 16)) = q4;
-        }
+        *reinterpret_cast<uint4 *>(rowp + off) = q4;
+        *reinterpret_cast<uint4 *>(rowg + off) = g4;
       }
     }
     // ---- dS (end of chunk c) -> fp16 operand copy, gam_C dS back into TMEM
@@ -286,7 +248,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     fence_before();
     __syncthreads();
 
-    // ---- dUt^T = dS Kc^T + dO^T P -> TM_DU (M = 128, N = 64);  dS += dO^T Qg (N = 128)
+    // ---- Y = dS K^T -> TM_Y, Z = dO^T P -> TM_DU (M = 128, N = 64);  dS += (diag(gam) dO)^T Q (N = 128)
     if (tid == 0) {
       fence_after();
       if (store && c < cend) {  // the fp16 dS at the end of chunk c, for the local-gradient kernel
@@ -297,21 +259,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       const uint32_t id_kk = idesc_f16(128, 64, false, false);
       const uint32_t id_mm = idesc_f16(128, 64, true, true);
-      const uint32_t dsb = u32(sm.ds16), kcb = u32(sm.kc), dob = u32(st + 4 * HT), pb = u32(st + 6 * HT);
+      const uint32_t dsb = u32(sm.ds16), kb = u32(st), dob = u32(st + 4 * HT), pb = u32(st + 6 * HT);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
-        const uint32_t boff = (kk >> 2) * HT + (kk & 3) * 32;
-        mma_f16(tm + TM_DU, sdesc(dsb + aoff, 16, 1024), sdesc(kcb + boff, 16, 1024), id_kk, kk > 0);
+        const uint32_t off = (kk >> 2) * 2 * HT + (kk & 3) * 32;
+        mma_f16(tm + TM_Y, sdesc(dsb + off, 16, 1024), sdesc(kb + off, 16, 1024), id_kk, kk > 0);
       }
       if (with_do) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_f16(tm + TM_DU, sdesc(dob + kk * 2048, HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id_mm, true);
-        const uint32_t id_s = idesc_f16(128, 128, true, true), qgb = u32(sm.qg);
+          mma_f16(tm + TM_DU, sdesc(dob + kk * 2048, HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id_mm, kk > 0);
+        const uint32_t id_s = idesc_f16(128, 128, true, true), dgb = u32(sm.dog), qb = u32(st + HT);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_f16(tm + TM_S, sdesc(dob + kk * 2048, HT, 1024), sdesc(qgb + kk * 2048, HT, 1024), id_s, true);
+          mma_f16(tm + TM_S, sdesc(dgb + kk * 2048, HT, 1024), sdesc(qb + kk * 2048, 2 * HT, 1024), id_s, true);
       }
       mma_commit(u32(&sm.bar_mma));
     }
@@ -320,13 +281,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       failed = true;
       break;
     }
-    {  // dUt^T -> fp16 K-major A (rows = d_v, k = token) in the Kc space (Kc is dead)
+    {  // dUt^T = Y diag(cdec) + Z -> fp16 K-major A (rows = d_v, k = token)
       const int c0 = wg * 32;
-      float v[32];
-      tmem_ld32(tm + tl + TM_DU + c0, v);
+      float y[32], v[32];
+      tmem_ld32(tm + tl + TM_Y + c0, y);
+      if (with_do) {
+        tmem_ld32(tm + tl + TM_DU + c0, v);
+      } else {
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4)
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+      }
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const float4 ca = reinterpret_cast<const float4 *>(G.cdec + c0 + q4 * 8)[0];
+        const float4 cb = reinterpret_cast<const float4 *>(G.cdec + c0 + q4 * 8)[1];
+        const float cd[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[q4 * 8 + i] = fmaf(cd[i], y[q4 * 8 + i], v[q4 * 8 + i]);
         st_chunk_f16(sm.kc + row * 128 + ((((c0 >> 3) + q4) ^ (row & 7)) * 16), v + q4 * 8);
+      }
     }
     fence_before();
     fence_async_smem();
@@ -387,7 +360,7 @@ int launch_bwd_chain_tc(const BwdArgs &a, const CUtensorMap *maps, dim3 grid, cu
   cudaError_t e = cudaFuncSetAttribute(bwd_chain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
   return (int)launch_pdl(bwd_chain_tc_kernel, grid, dim3(NTHREADS), smem, st, a, maps[0], maps[1], maps[2], maps[3],
-                         maps[4], maps[5]);
+                         maps[4]);
 }
 
 }  // namespace gdn

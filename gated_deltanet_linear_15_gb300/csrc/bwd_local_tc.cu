@@ -22,6 +22,8 @@
 //   P8 dT = -Y1 Ahat^T->T1   R8: dN tile (strictly lower), beta row sums (with N)
 //   P9 Ka = Q^T dPm + dW'^T X1 + K^T (dN + dN^T)->T3
 //                            R9: dk out (Ka + cdec Kb);  dg (reverse cumsum), dbeta
+#include <cstddef>
+
 #include "chunk_common.cuh"
 #include "kernels.h"
 #include "umma.cuh"
@@ -52,7 +54,7 @@ struct __align__(1024) LocalTcSmem {
   uint8_t ut[2 * HT];   // Ut^T [d_v][token] (context tile)
   uint8_t n16[HT];      // N = K K^T (fp16, [r][i], context tile)
   float g[2][CH], beta[2][CH];  // per item parity: the next item's gates are prepared during this one
-  float nq[CH], nk[CH];         // reciprocal norms
+  float nk[CH], nq[CH];         // reciprocal norms 1/|k|, 1/|q| (context, one bulk copy)
   Gates gt[2];
   float part[20][CH];   // per-token partial sums (reused per round)
   float acc[7][CH];     // assembled per-token terms
@@ -109,8 +111,7 @@ __device__ __forceinline__ uint32_t chunk_off(int r, int cb) { return r * 128 + 
 }  // namespace
 
 __global__ void __launch_bounds__(LTHREADS, 1)
-    bwd_local_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                        const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
+    bwd_local_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tm3, const __grid_constant__ CUtensorMap tmdo,
                         const __grid_constant__ CUtensorMap tms0, const __grid_constant__ CUtensorMap tmds,
                         const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmdq,
                         const __grid_constant__ CUtensorMap tmdk, const __grid_constant__ CUtensorMap tmdv,
@@ -201,19 +202,19 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     }
     return r;
   };
-  auto issue_main = [&](int item, int t0) {  // K, Q, V, S0, dS and the context tiles Ut^T, P, N
-    const int hh = item % H, srow = item * D;  // state rows of (chunk, head)
+  auto issue_main = [&](int item) {  // K, Q, V operand tiles, S0, dS, Ut^T, P, N
+    const int srow = item * D, qrow = item * TQ_TILES * CH;  // state / operand-tile rows of (chunk, head)
     const uint32_t bar = u32(&sm.bar_a);
     mbar_expect_tx(bar, 18 * HT);
     tma_load_3d(u32(sm.ut), &tmu, 0, (item * T128_TILES + T128_U) * D, 0, bar);
     tma_load_3d(u32(sm.p), &tmw, 0, (item * T64_TILES + T64_P) * CH, 0, bar);
     tma_load_3d(u32(sm.n16), &tmw, 0, (item * T64_TILES + T64_N) * CH, 0, bar);
-    tma_load_3d(u32(sm.kq + 0 * HT), &tmk, 0, hh, t0, bar);
-    tma_load_3d(u32(sm.kq + 2 * HT), &tmk, 64, hh, t0, bar);
-    tma_load_3d(u32(sm.kq + 1 * HT), &tmq, 0, hh, t0, bar);
-    tma_load_3d(u32(sm.kq + 3 * HT), &tmq, 64, hh, t0, bar);
-    tma_load_3d(u32(sm.v), &tmv, 0, hh, t0, bar);
-    tma_load_3d(u32(sm.v + HT), &tmv, 64, hh, t0, bar);
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) {
+      tma_load_3d(u32(sm.kq + 2 * hb * HT), &tm3, 64 * hb, qrow + TQ_K * CH, 0, bar);
+      tma_load_3d(u32(sm.kq + (2 * hb + 1) * HT), &tm3, 64 * hb, qrow + TQ_Q * CH, 0, bar);
+      tma_load_3d(u32(sm.v + hb * HT), &tm3, 64 * hb, qrow + TQ_V * CH, 0, bar);
+    }
     tma_load_3d(u32(sm.s0), &tms0, 0, srow, 0, bar);
     tma_load_3d(u32(sm.s0 + 2 * HT), &tms0, 64, srow, 0, bar);
     tma_load_3d(u32(sm.ds), &tmds, 0, srow, 0, bar);
@@ -231,14 +232,16 @@ __global__ void __launch_bounds__(LTHREADS, 1)
   auto issue_wy = [&](int item) {
     const uint32_t bar = u32(&sm.bar_w);
     const int row = item * T64_TILES * CH;
-    mbar_expect_tx(bar, 3 * HT);
+    mbar_expect_tx(bar, 3 * HT + 2 * CH * 4);
+    // the reciprocal norms too: the previous item's dk read them until its dk was staged
+    bulk_load(u32(sm.nk), a.nrm + (size_t)item * 2 * CH, 2 * CH * 4, bar);
     tma_load_3d(u32(sm.x1), &tmw, 0, row + T64_X1 * CH, 0, bar);
     tma_load_3d(u32(sm.x2), &tmw, 0, row + T64_X2 * CH, 0, bar);
     tma_load_3d(u32(sm.ah), &tmw, 0, row + T64_AH * CH, 0, bar);
   };
   ItemInfo cur = info_of(next_valid(blockIdx.x));
   if (tid == 0 && cur.item < n_items) {
-    issue_main(cur.item, cur.tok0);
+    issue_main(cur.item);
     issue_do(cur.item, cur.tok0);
     issue_wy(cur.item);
   }
@@ -265,45 +268,24 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     }
   }
   if (it == 0 && warp == 0) gate_prefix(sm.g[0], sm.gt[0]);
-  // ---- prep: bf16 -> fp16 in place; q, k normalised (norms kept for the Jacobians); rows >= nvalid zero
-#pragma unroll 1
-  for (int task = tid; task < 4 * 2 * CH; task += LTHREADS) {
-    const int t = task >> 7;  // 0 K, 1 Q, 2 V, 3 dO
-    const int r = (task >> 1) & 63, hb = task & 1;
-    uint8_t *rowp = (t == 0 ? sm.kq : t == 1 ? sm.kq + HT : t == 2 ? sm.v : sm.dob) +
-                    hb * (t < 2 ? 2 * HT : HT) + r * 128;
-    float mul = (t == 1) ? a.scale : 1.f;
-    if (l2 && t < 2) {
-      float ss = 0.f;
-#pragma unroll 1
-      for (int chk = 0; chk < 8; ++chk) {
-        const uint4 raw = *reinterpret_cast<const uint4 *>(rowp + ((chk ^ (r & 7)) * 16));
-        const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+  // ---- prep: dO bf16 -> fp16 in place, rows >= nvalid zero (K, Q, V arrive as operand tiles, with
+  //      their norms, from the forward's context); thread t takes 2 of the 16 chunks of dO row t / 8
+  {
+    const int r = tid >> 3, part = tid & 7;
+    uint8_t *rowp = sm.dob + (part >> 2) * HT + r * 128;
+    const float mul = r < nvalid ? 1.f : 0.f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __bfloat1622float2(b2[i]);
-          ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
-        }
-      }
-      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-      const float rn = 1.f / sqrtf(ss + 1e-6f);
-      mul = mul * rn;
-      if (hb == 0) (t == 0 ? sm.nk : sm.nq)[r] = rn;
-    }
-    if (r >= nvalid) mul = 0.f;
-#pragma unroll 1
-    for (int chk = 0; chk < 8; ++chk) {
-      uint8_t *cp = rowp + ((chk ^ (r & 7)) * 16);
-      const uint4 raw = *reinterpret_cast<const uint4 *>(cp);
-      const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
-      float y[8];
+    for (int cc = 0; cc < 2; ++cc) {
+      const int off = (((part & 3) * 2 + cc) ^ (r & 7)) * 16;
+      uint4 q4 = *reinterpret_cast<const uint4 *>(rowp + off);
+      uint32_t *w = reinterpret_cast<uint32_t *>(&q4);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(b2[i]);
-        y[2 * i] = f.x * mul;
-        y[2 * i + 1] = f.y * mul;
+        const __half2 a2 =
+            __floats2half2_rn(__uint_as_float(w[i] << 16) * mul, __uint_as_float(w[i] & 0xffff0000u) * mul);
+        w[i] = *reinterpret_cast<const uint32_t *>(&a2);
       }
-      st_chunk_f16(cp, y);
+      *reinterpret_cast<uint4 *>(rowp + off) = q4;
     }
   }
   fence_async_smem();
@@ -748,7 +730,7 @@ float rg[8];
   fence_async_smem();
   __syncthreads();
   if (nitem < n_items) {  // K, Q, V, S0, dS of the next item: their buffers are free after P9
-    if (tid == 0) issue_main(nitem, nxt.tok0);
+    if (tid == 0) issue_main(nitem);
     pend_main = true;
   }
   {  // R9: dk^T = Ka + cdec * Kb (lanes d_k); Jacobian; dk out
@@ -860,6 +842,9 @@ float rg[8];
   if (warp == 0) tmem_dealloc(tm, 512);
 }
 
+static_assert(offsetof(LocalTcSmem, nk) % 16 == 0 && offsetof(LocalTcSmem, nq) == offsetof(LocalTcSmem, nk) + CH * 4,
+              "the reciprocal norms arrive by one 16-byte-aligned bulk copy");
+
 size_t bwd_local_tc_smem_bytes() { return sizeof(LocalTcSmem) + 1024; }
 
 int launch_bwd_local_tc(const BwdArgs &a, const CUtensorMap *maps, int CH_max, cudaStream_t st) {
@@ -877,7 +862,7 @@ int launch_bwd_local_tc(const BwdArgs &a, const CUtensorMap *maps, int CH_max, c
   const int n_items = CH_max * a.H;
   const int grid = n_items < sms ? n_items : sms;  // persistent: one CTA per SM
   return (int)launch_pdl(bwd_local_tc_kernel, dim3(grid), dim3(LTHREADS), smem, st, a, maps[0], maps[1], maps[2],
-                         maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], maps[9], maps[10], n_items);
+                         maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], n_items);
 }
 
 }  // namespace gdn

@@ -78,7 +78,8 @@ __device__ __forceinline__ uint32_t chunk_off(int r, int cb) { return r * 128 + 
 __global__ void __launch_bounds__(FT, 1)
     fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmw,
-                  const __grid_constant__ CUtensorMap tms, const __grid_constant__ CUtensorMap tmt) {
+                  const __grid_constant__ CUtensorMap tms, const __grid_constant__ CUtensorMap tmt,
+                  const __grid_constant__ CUtensorMap tm3) {
   extern __shared__ unsigned char smraw[];
   TcSmem &sm = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
   pdl_trigger();
@@ -145,6 +146,7 @@ __global__ void __launch_bounds__(FT, 1)
     if (save_wy) {
       tma_prefetch_desc(&tmw);
       tma_prefetch_desc(&tmt);
+      tma_prefetch_desc(&tm3);
     }
     if (save_states) tma_prefetch_desc(&tms);
   }
@@ -233,7 +235,7 @@ __global__ void __launch_bounds__(FT, 1)
   // scaled), rows >= nvalid zeroed.  prep_kq: thread t takes quarter-row t % 256 of K (t < 256) or
   // of Q: 32 features = four 16-byte chunks of one 128-byte swizzled row; the four quarters of a row
   // sit in adjacent lanes (two shuffles for the squared norm).  prep_v: eighth-row t of V.
-  auto prep_kq = [&](uint8_t *st, int nvalid, bool with_q) {
+  auto prep_kq = [&](uint8_t *st, int nvalid, bool with_q, float *nrm_out) {
     const bool isq = tid >= 256;
     if (isq && !with_q) return;
     const int r = (tid >> 2) & 63, qq = tid & 3;
@@ -258,7 +260,11 @@ __global__ void __launch_bounds__(FT, 1)
       }
       ss += __shfl_xor_sync(0xffffffffu, ss, 1);
       ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-      mul *= rsqrtf(ss + 1e-6f);
+      const float rn = rsqrtf(ss + 1e-6f);
+      mul *= rn;
+      if (nrm_out && qq == 0) nrm_out[(isq ? CH : 0) + r] = rn;  // context: 1/|k|, 1/|q| per token
+    } else if (nrm_out && qq == 0) {
+      nrm_out[(isq ? CH : 0) + r] = 1.f;
     }
     if (r >= nvalid) mul = 0.f;
 #pragma unroll
@@ -313,11 +319,11 @@ __global__ void __launch_bounds__(FT, 1)
     }
     // g, beta of this chunk (issued one chunk ahead) must have landed before the next prefetch reuses cp.async
     cp_async_wait_all();
+    // the previous chunk's tile stores have read s0 / x1 / x2 / ah / its ring stage (overwritten below)
+    if (tid == 0 && (save_states || save_wy)) tma_store_wait_read();
     // prefetch the next chunk into the other stage (its previous contents were consumed)
     if (tid == 0 && c + 1 < cend) issue_tma(c + 1, stage ^ 1);
     if (c + 1 < cend) issue_gb(c + 1, stage ^ 1, false);
-    // the previous chunk's tile stores have read s0 / x1 / x2 / ah (overwritten below)
-    if (tid == 0 && (save_states || save_wy)) tma_store_wait_read();
     // chunk cfirst: wait for its tiles and normalise them here; later chunks were normalised one
     // iteration ahead, while MMA 3 and MMA 4 of the previous chunk ran
     const bool tma_ok = it > 0 || mbar_wait(u32(&sm.bar_tma[stage]), 0, err, 8);
@@ -328,7 +334,7 @@ __global__ void __launch_bounds__(FT, 1)
     Gates &G = sm.gt[stage];
     if (it == 0) {
       if (warp == 0 && gate_prefix(sm.g[stage], G) && lane == 0 && err) atomicOr(err, 1);
-      prep_kq(st, nvalid, emit);
+      prep_kq(st, nvalid, emit, save_c ? a.nrm + ((size_t)(chunk0 + c) * H + h) * 2 * CH : nullptr);
       if (need_v) prep_v(st, nvalid);
       fence_async_smem();
     }
@@ -421,11 +427,18 @@ __global__ void __launch_bounds__(FT, 1)
     // ---- MMA 2: W^T = K^T X1^T, U^T = V^T X2^T  (M = 128, N = 64, K = 64)
     if (tid == 0) {
       fence_after();
-      if (save_c) {  // X1, X2, Ahat and P of this (chunk, head)
+      if (save_c) {  // X1, X2, Ahat and P of this (chunk, head), and its K, Q, V operand tiles
         tma_store_3d(&tmw, 0, t64row + T64_X1 * CH, 0, u32(sm.x1));
         tma_store_3d(&tmw, 0, t64row + T64_X2 * CH, 0, u32(sm.x2));
         tma_store_3d(&tmw, 0, t64row + T64_AH * CH, 0, u32(sm.ah));
         tma_store_3d(&tmw, 0, t64row + T64_P * CH, 0, u32(sm.p));
+        const int qrow = ((chunk0 + c) * H + h) * TQ_TILES * CH;
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+          tma_store_3d(&tm3, 64 * hb, qrow + TQ_K * CH, 0, u32(st + 2 * hb * HT));
+          tma_store_3d(&tm3, 64 * hb, qrow + TQ_Q * CH, 0, u32(st + (2 * hb + 1) * HT));
+          tma_store_3d(&tm3, 64 * hb, qrow + TQ_V * CH, 0, u32(st + (4 + hb) * HT));
+        }
         tma_store_commit();
       }
       const uint32_t idesc = idesc_f16(128, 64, true, false);
@@ -505,7 +518,9 @@ __global__ void __launch_bounds__(FT, 1)
     bool next_ok = true;
     if (more) {  // the next chunk's tiles (issued at the top of this iteration), normalised while MMA 3 runs
       next_ok = mbar_wait(u32(&sm.bar_tma[stage ^ 1]), ((it + 1) >> 1) & 1, err, 8);
-      if (next_ok) prep_kq(stn, nvn, outputs && c + 1 >= cbeg);
+      if (next_ok)
+        prep_kq(stn, nvn, outputs && c + 1 >= cbeg,
+                save_wy && outputs && c + 1 >= cbeg ? a.nrm + ((size_t)(chunk0 + c + 1) * H + h) * 2 * CH : nullptr);
     }
     {
       if (tid == 0 && save_c) tma_store_wait_read();  // the W^T store has read wu (Ut^T is written next)
@@ -623,12 +638,13 @@ __global__ void __launch_bounds__(FT, 1)
 size_t fwd_tc_smem_bytes() { return sizeof(TcSmem) + 1024; }
 
 int launch_fwd_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                  const CUtensorMap &tw, const CUtensorMap &ts, const CUtensorMap &tt, dim3 grid, cudaStream_t st) {
+                  const CUtensorMap &tw, const CUtensorMap &ts, const CUtensorMap &tt, const CUtensorMap &t3,
+                  dim3 grid, cudaStream_t st) {
   const size_t smem = fwd_tc_smem_bytes();
   static_assert(sizeof(TcSmem) + 1024 <= 232448 - 256, "shared memory budget (the rest: static shared memory)");
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  return (int)launch_pdl(fwd_tc_kernel, grid, dim3(FT), smem, st, a, tq, tk, tv, tw, ts, tt);
+  return (int)launch_pdl(fwd_tc_kernel, grid, dim3(FT), smem, st, a, tq, tk, tv, tw, ts, tt, t3);
 }
 
 }  // namespace gdn

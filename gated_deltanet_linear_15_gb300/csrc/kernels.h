@@ -27,17 +27,22 @@ struct FwdArgs {
   float scale;
   unsigned flags;
   int pass;  // 0: segment end states / transitions, 1: outputs (+ saves if set), 2: states only
-  // pass 1, bf16 with d = 128: the chunk context tiles for the backward (both set, or both NULL), see
-  // T64_* and T128_*; with o == NULL the pass writes no output and only produces states and tiles
-  void *t64, *t128;
+  // pass 1, bf16 with d = 128: the chunk context for the backward (all set, or all NULL), see T64_*,
+  // T128_*, TQ_*; with o == NULL the pass writes no output and only produces states and context
+  void *t64, *t128, *tqkv;
+  float *nrm;
 };
 
 // Chunk context tiles of every (chunk, head), fp16 row-major, written by the forward:
 //   t64  [CH_max, H, 5, 64, 64]:  X1 = Ahat diag(beta), X2 = lower(diag(gp) Ahat diag(beta rgp)), Ahat,
 //                                 P = diag(gp) tril(Q K^T) diag(rgp), N = K K^T (normalised keys)
 //   t128 [CH_max, H, 2, 128, 64]: W^T with its token columns scaled by gam (rows d_k), Ut^T (rows d_v)
+//   tqkv [CH_max, H, 3, 64, 128]: the operand forms of K, Q, V (normalised, q scaled, fp16; rows = tokens,
+//                                 zero past the sequence end)
+//   nrm  [CH_max, H, 2, 64] fp32: reciprocal norms 1/|k|, 1/|q| per token (1 without normalisation)
 constexpr int T64_X1 = 0, T64_X2 = 1, T64_AH = 2, T64_P = 3, T64_N = 4, T64_TILES = 5;
 constexpr int T128_W = 0, T128_U = 1, T128_TILES = 2;
+constexpr int TQ_K = 0, TQ_Q = 1, TQ_V = 2, TQ_TILES = 3;
 
 struct BwdArgs {
   const void *q, *k, *v, *dO;
@@ -54,6 +59,7 @@ struct BwdArgs {
   float scale;
   unsigned flags;
   int pass;  // reverse chain: 0 segment starts / transitions, 1 per-chunk dS
+  const float *nrm;  // context reciprocal norms (bf16, d = 128), see FwdArgs
 };
 
 struct FixupArgs {
@@ -89,15 +95,17 @@ int launch_fwd_chunk(const FwdArgs &a, bool is_bf16, int D, dim3 grid, cudaStrea
 // stores: t64 tiles ([rows, 64] fp16, box 64 x 64), chunk-start states ([rows, 128] fp16, box 64 x 128), t128
 // tiles ([rows, 64] fp16, box 64 x 128)
 int launch_fwd_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                  const CUtensorMap &t64, const CUtensorMap &ts, const CUtensorMap &t128, dim3 grid, cudaStream_t st);
+                  const CUtensorMap &t64, const CUtensorMap &ts, const CUtensorMap &t128, const CUtensorMap &tqkv,
+                  dim3 grid, cudaStream_t st);
 int launch_bwd_chain(const BwdArgs &a, bool is_bf16, int D, dim3 grid, cudaStream_t st);
-// tcgen05 reverse chain (bf16, d = 128); maps: q, k, dO ([tokens, H, 128] bf16, box 64x1x64), the t64 and
-// t128 context tiles, and the per-chunk dS store ([rows, 128] fp16, box 64x128x1)
+// tcgen05 reverse chain (bf16, d = 128); maps: the tqkv context ([rows, 128] fp16, box 64x64), dO
+// ([tokens, H, 128] bf16, box 64x1x64), the t64 and t128 context tiles, and the per-chunk dS store
+// ([rows, 128] fp16, box 64x128x1)
 int launch_bwd_chain_tc(const BwdArgs &a, const CUtensorMap *maps, dim3 grid, cudaStream_t st);
 int launch_bwd_local(const BwdArgs &a, bool is_bf16, int D, int CH_max, cudaStream_t st);
-// tcgen05 local-gradient kernel (bf16, d = 128); maps: q, k, v, dO ([tokens, H, 128] bf16, box 64x1x64), the
-// fp16 per-chunk states S0 and dS ([rows, 128] as a 3-D map, box 64x128x1), the t64 and t128 context tiles,
-// and dq, dk, dv (as q)
+// tcgen05 local-gradient kernel (bf16, d = 128); maps: the tqkv context, dO ([tokens, H, 128] bf16, box
+// 64x1x64), the fp16 per-chunk states S0 and dS ([rows, 128] as a 3-D map, box 64x128x1), the t64 and t128
+// context tiles, and dq, dk, dv (as dO)
 int launch_bwd_local_tc(const BwdArgs &a, const CUtensorMap *maps, int CH_max, cudaStream_t st);
 // token-by-token forward over NH = N * H (sequence, head) pairs
 int launch_recurrent(const RecArgs &a, bool is_bf16, int D, int NH, cudaStream_t st);

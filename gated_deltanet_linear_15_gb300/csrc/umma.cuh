@@ -204,6 +204,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t smem_dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(mbar)
       : "memory");
 }
+// contiguous global -> shared copy of `bytes` (multiple of 16, both addresses 16-byte aligned),
+// completing on an mbarrier's transaction count
+__device__ __forceinline__ void bulk_load(uint32_t smem_dst, const void *gsrc, uint32_t bytes, uint32_t mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                   smem_dst),
+               "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(mbar)
+               : "memory");
+}
 // shared -> global tile store (bulk-group completion); the source must have been written before a
 // fence.proxy.async.shared::cta and a barrier, and stays untouched until tma_store_wait_read()
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int x, int y, int z, uint32_t smem_src) {

@@ -94,12 +94,13 @@ def test_workspace_checks(lib):
 
 def test_saved_context_sizes(lib):
     """Saved context = fp16 chunk-start states + five fp16 64 x 64 tiles (X1, X2, Ahat, P, N) + two
-    fp16 128 x 64 tiles (scaled W^T, Ut^T) per (chunk, head) at bf16, d = 128; the saved-context
-    backward needs the recompute workspace minus exactly that."""
+    fp16 128 x 64 tiles (scaled W^T, Ut^T) + three fp16 64 x 128 operand tiles (K, Q, V) + 2 x 64 fp32
+    reciprocal norms per (chunk, head) at bf16, d = 128; the saved-context backward needs the
+    recompute workspace minus exactly that."""
     s = _shape(T=1000, H=3)
     chunks = (1000 + 63) // 64
     states = chunks * 3 * 128 * 128 * 2
-    tiles = chunks * 3 * (5 * 64 * 64 + 2 * 128 * 64) * 2
+    tiles = chunks * 3 * ((5 * 64 * 64 + 2 * 128 * 64 + 3 * 64 * 128) * 2 + 2 * 64 * 4)
     assert lib.gdn_saved_size(ctypes.byref(s)) == states + tiles
     full = lib.gdn_bwd_workspace_size(ctypes.byref(s))
     assert lib.gdn_bwd_saved_workspace_size(ctypes.byref(s)) == full - states - tiles
