@@ -311,11 +311,6 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     mma_commit(u32(&sm.bar_mma));
   }
   __syncwarp();
-  if (nitem < n_items && tid < 128) {  // the next item's g or beta, stored mid-item
-    const int r = tid & 63, nh = nitem % H;
-    if (r < nxt.nvalid)
-      gb_next = tid < 64 ? a.g[(size_t)(nxt.tok0 + r) * H + nh] : a.beta[(size_t)(nxt.tok0 + r) * H + nh];
-  }
   {  // meanwhile: <dS, S0> over the whole state (both tiles share one layout, so compare byte positions)
     float acc = 0.f;
     const uint4 *A4 = reinterpret_cast<const uint4 *>(sm.s0), *B4 = reinterpret_cast<const uint4 *>(sm.ds);
@@ -412,6 +407,11 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     mma_commit(u32(&sm.bar_mma));
   }
   __syncwarp();
+  if (nitem < n_items && tid < 128) {  // the next item's g or beta, stored after dq (its plan lookups have landed by now)
+    const int r = tid & 63, nh = nitem % H;
+    if (r < nxt.nvalid)
+      gb_next = tid < 64 ? a.g[(size_t)(nxt.tok0 + r) * H + nh] : a.beta[(size_t)(nxt.tok0 + r) * H + nh];
+  }
   if (__syncthreads_or(!mma_done())) {
     failed = true;
     break;
