@@ -57,7 +57,7 @@ struct __align__(1024) LocalTcSmem {
   float nk[CH], nq[CH];         // reciprocal norms 1/|k|, 1/|q| (context, one bulk copy)
   Gates gt[2];
   float part[20][CH];   // per-token partial sums (reused per round)
-  float acc[7][CH];     // assembled per-token terms
+  float acc[9][CH];     // assembled per-token terms
   float red[LWARPS];
   uint64_t bar_a, bar_b, bar_w, bar_mma;  // TMA: {K, Q, V, S0, dS, Ut^T, P, N}, {dO}, {X1, X2, Ahat}; tensor cores
   uint32_t tmem_base;
@@ -331,12 +331,22 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     failed = true;
     break;
   }
-  {  // R2: dUt^T = cdec*Y + Z -> wt;  per-token sums <Ut, Y>, <dUt, Ut> over d_v (Ut^T from its tile)
-    float t1 = 0.f, t2 = 0.f;
+  {  // R2: dUt^T = cdec*Y + Z -> wt;  per-token sums <Ut, Y>, <dUt, Ut> over d_v (Ut^T from its tile),
+     // and gam <Qa, q^> over d_k (Qa = S0^T dO^T: the dO S0 part of dq^ dotted with q^)
+    float t1 = 0.f, t2 = 0.f, t3 = 0.f;
 #pragma unroll 1
     for (int q4 = 0; q4 < 2; ++q4) {
       const int cb = c0 + q4 * 8;
       float y[8], z[8], u[8], s1[8], s2[8];
+      {
+        float qa[8], gm[8];
+        tmem_ld8(tm + tl + T5 + cb, qa);
+        ld8f(G.gam + cb, gm);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) qa[i] *= gm[i] * ld_f16(sm.kq + HT, cb + i, row, 2 * HT);
+        const float a3 = colsum8(qa);
+        if ((lane >> 3) == q4) t3 = a3;
+      }
       tmem_ld8(tm + tl + T3 + cb, y);
       tmem_ld8(tm + tl + T4 + cb, z);
       {
@@ -367,13 +377,15 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     }
     if (lane < 16) sm.part[wq][c0 + lane] = t1;
     if (lane < 16) sm.part[4 + wq][c0 + lane] = t2;
+    if (lane < 16) sm.part[8 + wq][c0 + lane] = t3;
   }
   fence_before();
   fence_async_smem();
   __syncthreads();
   if (tid < 64) {
-    sm.acc[0][tid] = sm.part[0][tid] + sm.part[1][tid] + sm.part[2][tid] + sm.part[3][tid];  // <Ut, Y>
-    sm.acc[1][tid] = sm.part[4][tid] + sm.part[5][tid] + sm.part[6][tid] + sm.part[7][tid];  // <dUt, Ut>
+    sm.acc[0][tid] = sm.part[0][tid] + sm.part[1][tid] + sm.part[2][tid] + sm.part[3][tid];    // <Ut, Y>
+    sm.acc[1][tid] = sm.part[4][tid] + sm.part[5][tid] + sm.part[6][tid] + sm.part[7][tid];    // <dUt, Ut>
+    sm.acc[5][tid] = sm.part[8][tid] + sm.part[9][tid] + sm.part[10][tid] + sm.part[11][tid];  // gam <dO S0, q>
   }
 
   {  // X1, X2, Ahat of this item (loaded at the end of the previous one)
@@ -521,39 +533,12 @@ float rg[8];
     for (int e = tid; e < 2 * HT / 16; e += LTHREADS) dst[e] = src[(e >= HT / 16 ? 2 * HT / 16 : 0) + (e % (HT / 16))];
   }
   {
-    // dq^T = gam*Qa + Qb (lanes d_k): <dQ1, q^> and Jacobian dots over d_k; stage dq^ (fp32 kept in regs)
-    {
-      float t1 = 0.f, t2 = 0.f;
-#pragma unroll 1
-      for (int q4 = 0; q4 < 2; ++q4) {
-        const int cb = c0 + q4 * 8;
-        float qa[8], qb[8], s1[8], s2[8];
-        tmem_ld8(tm + tl + T5 + cb, qa);
-        tmem_ld8(tm + tl + T7 + cb, qb);
-        float gm[8];
-        ld8f(G.gam + cb, gm);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int tkn = cb + i;
-          const float qv = ld_f16(sm.kq + HT, tkn, row, 2 * HT);
-          const float a1 = gm[i] * qa[i];
-          s1[i] = a1 * qv;
-          s2[i] = (qb[i] + a1) * qv;  // dq^ (w.r.t. the normalised, scaled q) times q^
-        }
-        const float a1 = colsum8(s1), a2 = colsum8(s2);
-        if ((lane >> 3) == q4) {
-          t1 = a1;
-          t2 = a2;
-        }
-      }
-      if (lane < 16) sm.part[wq][c0 + lane] = t1;
-      if (lane < 16) sm.part[4 + wq][c0 + lane] = t2;
-    }
-    // M1, M2 (lanes 0-63 = r): dAhat = beta_i (M1 + Gamma M2); beta column sums colsum_i(Ahat (M1 + Gamma M2))
+    // M1, M2 (lanes 0-63 = r): dAhat = beta_i (M1 + Gamma M2); beta column sums colsum_i(Ahat (M1 + Gamma M2));
+    // and colsum_i(Ahat M1) (the dW'^T X1 part of dk^ dotted with k^)
     if (row < 64) {
       const int r = row;
       const float gr = G.gp[r];
-      float cs = 0.f;
+      float cs = 0.f, ca = 0.f;
 #pragma unroll 1
       for (int q4 = 0; q4 < 2; ++q4) {
         const int cb = c0 + q4 * 8;
@@ -565,20 +550,26 @@ float rg[8];
         float rg[8], bt[8];
         ld8f(G.rgp + cb, rg);
         ld8f(gbeta + cb, bt);
+        float am[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int col = cb + i;
+          const float hv = __half2float(hh[i]);
           const float x = m1[i] + (col <= r ? m2[i] * gr * rg[i] : 0.f);
-          m2[i] = __half2float(hh[i]) * x;
+          am[i] = hv * m1[i];
+          m2[i] = hv * x;
           m1[i] = bt[i] * x;
         }
         st_chunk_f16(sm.x2 + chunk_off(r, cb), m1);
-        const float a = colsum8(m2);
-        if ((lane >> 3) == q4) cs = a;
+        const float a = colsum8(m2), b = colsum8(am);
+        if ((lane >> 3) == q4) {
+          cs = a;
+          ca = b;
+        }
       }
       if (lane < 16) sm.part[8 + wq][c0 + lane] = cs;
+      if (lane < 16) sm.part[10 + wq][c0 + lane] = ca;
     }
-    __syncthreads();
     // dq raw = (scale dq^ - q^ (q^ . dq^) / scale) / |q|   (or scale dq^ without normalisation)
     const float rscale = 1.f / a.scale;
 #pragma unroll 1
@@ -589,15 +580,13 @@ float rg[8];
       tmem_ld8(tm + tl + T7 + cb, qb);
       float gm[8], dt[8], nqv[8];
       ld8f(G.gam + cb, gm);
-      if (l2) {
-        float p0[8], p1[8], p2[8], p3[8];
-        ld8f(sm.part[4] + cb, p0);
-        ld8f(sm.part[5] + cb, p1);
-        ld8f(sm.part[6] + cb, p2);
-        ld8f(sm.part[7] + cb, p3);
+      if (l2) {  // q^ . dq^ = gam <Qa, q^> + sum_s dP * P (the Qb part: row sums of dP * P)
+        float p0[8], p1[8];
+        ld8f(sm.acc[5] + cb, p0);
+        ld8f(sm.acc[2] + cb, p1);
         ld8f(sm.nq + cb, nqv);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) dt[i] = (p0[i] + p1[i]) + (p2[i] + p3[i]);
+        for (int i = 0; i < 8; ++i) dt[i] = p0[i] + p1[i];
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -620,8 +609,8 @@ float rg[8];
   {
     store_tile(&tmdq, a.dq, sm.dob, h, tok0, nvalid);
     if (tid < 64) {
-      sm.acc[5][tid] = sm.part[0][tid] + sm.part[1][tid] + sm.part[2][tid] + sm.part[3][tid];  // gam <dO S0, q>
-      sm.acc[6][tid] = sm.part[8][tid] + sm.part[9][tid];                                      // beta col terms
+      sm.acc[6][tid] = sm.part[8][tid] + sm.part[9][tid];    // beta col terms
+      sm.acc[7][tid] = sm.part[10][tid] + sm.part[11][tid];  // colsum(Ahat M1)
     }
     if (tid < 128) (tid < 64 ? sm.g[gbuf ^ 1] : sm.beta[gbuf ^ 1])[tid & 63] = gb_next;  // next item's g, beta
   }
@@ -682,11 +671,11 @@ float rg[8];
     const int r = row;
     const float br = gbeta[r];
     uint8_t *sg = sm.v + HT;
-    float rb = 0.f;
+    float rb = 0.f, cn = 0.f;  // row sums of dT * N; column sums of dN * N
 #pragma unroll 1
     for (int q4 = 0; q4 < 2; ++q4) {
       const int cb = c0 + q4 * 8;
-      float v[8], y[8];
+      float v[8], y[8], dn[8];
       tmem_ld8(tm + tl + T1 + cb, v);
       const uint4 nraw = *reinterpret_cast<const uint4 *>(sm.n16 + chunk_off(r, cb));
       const __half *nh = reinterpret_cast<const __half *>(&nraw);
@@ -694,12 +683,17 @@ float rg[8];
       for (int i = 0; i < 8; ++i) {
         const int col = cb + i;
         const bool lo = col < r;
-        rb += lo ? v[i] * __half2float(nh[i]) : 0.f;
+        const float nv = __half2float(nh[i]);
+        rb += lo ? v[i] * nv : 0.f;
         y[i] = lo ? br * v[i] : 0.f;
+        dn[i] = y[i] * nv;
       }
       st_chunk_f16(sg + chunk_off(r, cb), y);
+      const float a = colsum8(dn);
+      if ((lane >> 3) == q4) cn = a;
     }
     sm.part[16 + wg][r] = rb;
+    if (lane < 16) sm.part[12 + wq][c0 + lane] = cn;
   }
   fence_before();
   fence_async_smem();
@@ -727,6 +721,12 @@ float rg[8];
     failed = true;
     break;
   }
+  if (tid < 64) {  // k^ . dk^ per token: Q^T dPm, dW'^T X1, K^T (dN + dN^T) and cdec Kb parts, from sums above
+    const int t = tid;
+    const float rbs = sm.part[16][t] + sm.part[17][t] + sm.part[18][t] + sm.part[19][t];
+    sm.acc[8][t] = sm.acc[3][t] + gbeta[t] * (sm.acc[7][t] + rbs) + (sm.part[12][t] + sm.part[13][t]) +
+                   G.cdec[t] * sm.acc[0][t];
+  }
   fence_async_smem();
   __syncthreads();
   if (nitem < n_items) {  // K, Q, V, S0, dS of the next item: their buffers are free after P9
@@ -734,27 +734,6 @@ float rg[8];
     pend_main = true;
   }
   {  // R9: dk^T = Ka + cdec * Kb (lanes d_k); Jacobian; dk out
-    if (l2) {
-      float t2 = 0.f;
-#pragma unroll 1
-      for (int q4 = 0; q4 < 2; ++q4) {
-        const int cb = c0 + q4 * 8;
-        float ka[8], kbv[8];
-        tmem_ld8(tm + tl + T3 + cb, ka);
-        tmem_ld8(tm + tl + T2 + cb, kbv);
-        float cd[8];
-        ld8f(G.cdec + cb, cd);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int tkn = cb + i;
-          ka[i] = (ka[i] + cd[i] * kbv[i]) * ld_f16(sm.wt, tkn, row, HT);
-        }
-        const float a2 = colsum8(ka);
-        if ((lane >> 3) == q4) t2 = a2;
-      }
-      if (lane < 16) sm.part[wq][c0 + lane] = t2;
-    }
-    __syncthreads();
     uint8_t *const stg = sm.x2;  // x2 + ah (16 KB, both dead after P8)
 #pragma unroll 1
     for (int q4 = 0; q4 < 2; ++q4) {
@@ -765,14 +744,8 @@ float rg[8];
       float cd[8], dt[8], nkv[8];
       ld8f(G.cdec + cb, cd);
       if (l2) {
-        float p0[8], p1[8], p2[8], p3[8];
-        ld8f(sm.part[0] + cb, p0);
-        ld8f(sm.part[1] + cb, p1);
-        ld8f(sm.part[2] + cb, p2);
-        ld8f(sm.part[3] + cb, p3);
+        ld8f(sm.acc[8] + cb, dt);
         ld8f(sm.nk + cb, nkv);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) dt[i] = (p0[i] + p1[i]) + (p2[i] + p3[i]);
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
