@@ -140,6 +140,7 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     mbar_init(u32(&sm.bar_w), 1);
     mbar_init(u32(&sm.bar_mma), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    for (const CUtensorMap *m : {&tm3, &tmdo, &tms0, &tmds, &tmw, &tmdq, &tmdk, &tmdv, &tmu}) tma_prefetch_desc(m);
   }
   if (warp == 0) {
     tmem_alloc(u32(&sm.tmem_base), 512);
