@@ -472,24 +472,15 @@ float rg[8];
       for (int i = 0; i < 8; ++i) v[i] *= gm[i];
       st_chunk_f16(sm.s0 + chunk_off(row, cb), v);
     }
-    // dV^T (lanes d_v, columns token): stage bf16 dv[token][d_v] in dob (dO is dead); <dV, v>
-    {
-      float t = 0.f;
+    // dV^T (lanes d_v, columns token): stage bf16 dv[token][d_v] in dob (dO is dead); <dV, v> comes
+    // with R6 as colsum(X2 M2)
 #pragma unroll 1
-      for (int q4 = 0; q4 < 2; ++q4) {
-        const int cb = c0 + q4 * 8;
-        float v[8], sv[8];
-        tmem_ld8(tm + tl + T6 + cb, v);
+    for (int q4 = 0; q4 < 2; ++q4) {
+      const int cb = c0 + q4 * 8;
+      float v[8];
+      tmem_ld8(tm + tl + T6 + cb, v);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int tkn = cb + i;
-          *stg_at(sm.dob, tkn, row) = __float2bfloat16_rn(v[i]);
-          sv[i] = v[i] * ld_f16(sm.v, tkn, row, HT);
-        }
-        const float a = colsum8(sv);
-        if ((lane >> 3) == q4) t = a;
-      }
-      if (lane < 16) sm.part[12 + wq][c0 + lane] = t;
+      for (int i = 0; i < 8; ++i) *stg_at(sm.dob, cb + i, row) = __float2bfloat16_rn(v[i]);
     }
   }
   fence_before();
@@ -500,7 +491,6 @@ float rg[8];
     if (tid < 64) {
       sm.acc[2][tid] = sm.part[16][tid] + sm.part[17][tid] + sm.part[18][tid] + sm.part[19][tid];  // row sums of dP * P
       sm.acc[3][tid] = sm.part[10][tid] + sm.part[11][tid];  // column sums of dP * P
-      sm.acc[4][tid] = sm.part[12][tid] + sm.part[13][tid] + sm.part[14][tid] + sm.part[15][tid];  // <dV, v>
     }
   }
   __syncthreads();
@@ -535,11 +525,12 @@ float rg[8];
   }
   {
     // M1, M2 (lanes 0-63 = r): dAhat = beta_i (M1 + Gamma M2); beta column sums colsum_i(Ahat (M1 + Gamma M2));
-    // and colsum_i(Ahat M1) (the dW'^T X1 part of dk^ dotted with k^)
+    // colsum_i(Ahat M1) (the dW'^T X1 part of dk^ dotted with k^); colsum_i(X2 M2) = <dV, v> (dV = X2^T dUt,
+    // M2 = dUt V^T); X2 is read before dAhat replaces it
     if (row < 64) {
       const int r = row;
       const float gr = G.gp[r];
-      float cs = 0.f, ca = 0.f;
+      float cs = 0.f, ca = 0.f, cv = 0.f;
 #pragma unroll 1
       for (int q4 = 0; q4 < 2; ++q4) {
         const int cb = c0 + q4 * 8;
@@ -548,28 +539,33 @@ float rg[8];
         tmem_ld8(tm + tl + T4 + cb, m2);
         const uint4 raw = *reinterpret_cast<const uint4 *>(sm.ah + chunk_off(r, cb));
         const __half *hh = reinterpret_cast<const __half *>(&raw);
+        const uint4 xraw = *reinterpret_cast<const uint4 *>(sm.x2 + chunk_off(r, cb));
+        const __half *xh = reinterpret_cast<const __half *>(&xraw);
         float rg[8], bt[8];
         ld8f(G.rgp + cb, rg);
         ld8f(gbeta + cb, bt);
-        float am[8];
+        float am[8], xm[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int col = cb + i;
           const float hv = __half2float(hh[i]);
           const float x = m1[i] + (col <= r ? m2[i] * gr * rg[i] : 0.f);
           am[i] = hv * m1[i];
+          xm[i] = __half2float(xh[i]) * m2[i];
           m2[i] = hv * x;
           m1[i] = bt[i] * x;
         }
         st_chunk_f16(sm.x2 + chunk_off(r, cb), m1);
-        const float a = colsum8(m2), b = colsum8(am);
+        const float a = colsum8(m2), b = colsum8(am), e = colsum8(xm);
         if ((lane >> 3) == q4) {
           cs = a;
           ca = b;
+          cv = e;
         }
       }
       if (lane < 16) sm.part[8 + wq][c0 + lane] = cs;
       if (lane < 16) sm.part[10 + wq][c0 + lane] = ca;
+      if (lane < 16) sm.part[14 + wq][c0 + lane] = cv;
     }
     // dq raw = (scale dq^ - q^ (q^ . dq^) / scale) / |q|   (or scale dq^ without normalisation)
     const float rscale = 1.f / a.scale;
@@ -612,6 +608,7 @@ float rg[8];
     if (tid < 64) {
       sm.acc[6][tid] = sm.part[8][tid] + sm.part[9][tid];    // beta col terms
       sm.acc[7][tid] = sm.part[10][tid] + sm.part[11][tid];  // colsum(Ahat M1)
+      sm.acc[4][tid] = sm.part[14][tid] + sm.part[15][tid];  // <dV, v>
     }
     if (tid < 128) (tid < 64 ? sm.g[gbuf ^ 1] : sm.beta[gbuf ^ 1])[tid & 63] = gb_next;  // next item's g, beta
   }
