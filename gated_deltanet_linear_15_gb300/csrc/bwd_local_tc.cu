@@ -11,16 +11,19 @@
 //
 // Rounds (MMA group -> read-out), TMEM regions T0..T7 of 64 columns.  The forward's chunk context
 // supplies X1, X2, Ahat, P, N and Ut^T by TMA with the inputs, so nothing of the forward chunk is
-// recomputed here:
-//   P2 Y = dS K^T->T3, Qa = S0^T dO^T->T5, Z = dO^T P->T4
-//                            R2: dUt^T = cdec*Y + Z; sums <Ut,Y>, <dUt,Ut>
-//   P5 dP = dO Ut^T->T0, dW'^T = -S0^T dUt^T->T1, dV^T = dUt^T X2->T6, Kb = dS^T Ut^T->T2
-//                            R5: dPm (over P), dP*P sums; dW'^T tile; dv out, <dV,v>
-//   P6 Qb = K^T dPm^T->T7, M1 = dW' K^T->T3, M2 = dUt V^T->T4
-//                            R6: dq out (+ <dQ1,q>); dAhat tile, beta column sums
-//   P7 Y1 = Ahat^T dAhat->T0 R7: Y1 tile
-//   P8 dT = -Y1 Ahat^T->T1   R8: dN tile (strictly lower), beta row sums (with N)
-//   P9 Ka = Q^T dPm + dW'^T X1 + K^T (dN + dN^T)->T3
+// recomputed here.  Each round commits once the products its read-out needs are issued; the products
+// read later (in brackets) are issued after that commit and covered by the next one, and the CUDA-core
+// work no following product needs runs while the next round computes:
+//   P2 Y = dS K^T->T3, Z = dO^T P->T4 [Qa = S0^T dO^T->T5]
+//                            R2: dUt^T = cdec*Y + Z
+//   P5 dP = dO Ut^T->T0, dW'^T = -S0^T dUt^T->T1, dV^T = dUt^T X2->T6 [Kb = dS^T Ut^T->T2]
+//                            under P5: sums <Ut,Y>, <dUt,Ut>;  R5: dPm (over P), dP*P sums; dW'^T tile
+//   P6 M1 = dW' K^T->T3, M2 = dUt V^T->T4 [Qb = K^T dPm^T->T7]
+//                            under P6: dv out, gam <Qa,q>;  R6: dAhat tile, beta column sums, <dV,v>
+//   P7 Y1 = Ahat^T dAhat->T0 [Ka = Q^T dPm + dW'^T X1->T3]
+//                            under P7: K^ copy, next item's gates;  R7: Y1 tile
+//   P8 dT = -Y1 Ahat^T->T1   under P8: dq out;  R8: dN tile (strictly lower), beta row sums (with N)
+//   P9 Ka += K^T (dN + dN^T)->T3
 //                            R9: dk out (Ka + cdec Kb);  dg (reverse cumsum), dbeta
 #include <cstddef>
 
@@ -36,8 +39,10 @@ namespace {
 
 constexpr int D = 128;
 constexpr int HT = 8192;
-constexpr int LTHREADS = 512;  // 16 warps: four per TMEM lane quarter, 16 columns each per read-out
+constexpr int LTHREADS = 512;  // 16 worker warps: four per TMEM lane quarter, 16 columns each per read-out
 constexpr int LWARPS = LTHREADS / 32;
+constexpr int PRODUCER = LTHREADS;       // lane 0 of warp 16 issues every product, TMA load and TMA store
+constexpr int LNTHREADS = LTHREADS + 32;
 constexpr uint32_t T0 = 0, T1 = 64, T2 = 128, T3 = 192, T4 = 256, T5 = 320, T6 = 384, T7 = 448;
 
 struct __align__(1024) LocalTcSmem {
@@ -105,12 +110,28 @@ __device__ __forceinline__ void ld8f(const float *p, float (&v)[8]) {
   v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
+// Barrier 1 over the 16 worker warps only (the producer warp does not take part), OR-reducing pred.
+__device__ __forceinline__ bool wbar_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n"
+      ".reg .pred p, q;\n"
+      "setp.ne.u32 p, %1, 0;\n"
+      "bar.red.or.pred q, 1, %2, p;\n"
+      "selp.u32 %0, 1, 0, q;\n"
+      "}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "n"(LTHREADS)
+      : "memory");
+  return r != 0;
+}
+
 // byte offset of the 16-byte chunk holding columns [cb, cb + 8) of row r in a swizzled tile
 __device__ __forceinline__ uint32_t chunk_off(int r, int cb) { return r * 128 + ((((cb & 63) >> 3) ^ (r & 7)) << 4); }
 
 }  // namespace
 
-__global__ void __launch_bounds__(LTHREADS, 1)
+__global__ void __launch_bounds__(LNTHREADS, 1)
     bwd_local_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tm3, const __grid_constant__ CUtensorMap tmdo,
                         const __grid_constant__ CUtensorMap tms0, const __grid_constant__ CUtensorMap tmds,
                         const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmdq,
@@ -158,18 +179,15 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     fence_after();
     return r;
   };
-  // A staged bf16 output tile (two swizzled [64 token][64 feature] halves at `stg`) to rows tok0.. of
-  // head h: one TMA store per half for a full chunk (thread 0), else coalesced 16-byte stores of the
-  // valid rows (all threads).  The caller fenced the staging writes for the async proxy and synced.
-  auto store_tile = [&](const CUtensorMap *map, void *gptr, const uint8_t *stg, int hh, int t0, int nv) {
-    if (nv == CH) {
-      if (tid == 0) {
-        tma_store_3d(map, 0, hh, t0, u32(stg));
-        tma_store_3d(map, 64, hh, t0, u32(stg + HT));
-        tma_store_commit();
-      }
-      return;
-    }
+  // A staged bf16 output tile (two swizzled [64 token][64 feature] halves at `stg`) to rows t0.. of head hh:
+  // a full chunk by two TMA stores (the producer; the workers fenced the staging for the async proxy and
+  // met it at a barrier), a partial one by coalesced 16-byte stores of the valid rows (the workers)
+  auto store_tma = [&](const CUtensorMap *map, const uint8_t *stg, int hh, int t0) {
+    tma_store_3d(map, 0, hh, t0, u32(stg));
+    tma_store_3d(map, 64, hh, t0, u32(stg + HT));
+    tma_store_commit();
+  };
+  auto store_rows = [&](void *gptr, const uint8_t *stg, int hh, int t0, int nv) {
     bf16 *gp = static_cast<bf16 *>(gptr);
     for (int e = tid; e < CH * (D / 8); e += LTHREADS) {
       const int r = e >> 4, cc = e & 15;
@@ -241,13 +259,15 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     tma_load_3d(u32(sm.ah), &tmw, 0, row + T64_AH * CH, 0, bar);
   };
   ItemInfo cur = info_of(next_valid(blockIdx.x));
-  if (tid == 0 && cur.item < n_items) {
+  if (tid == PRODUCER && cur.item < n_items) {
     issue_main(cur.item);
     issue_do(cur.item, cur.tok0);
     issue_wy(cur.item);
   }
-  bool pend_main = cur.item < n_items, pend_do = pend_main, pend_wy = pend_main, failed = false;
+  // ---------------- worker warps 0-15: read-outs and the CUDA-core parts of every round
+  bool failed = false, release = false;  // release: the producer still waits at a CTA-wide barrier
   uint32_t it = 0;  // parity of the TMA barriers: one completion per item
+  if (warp < LWARPS) {
   for (; cur.item < n_items; ++it) {
   const ItemInfo nxt = info_of(next_valid(cur.item + gridDim.x));  // consumed late in this item
   const int nitem = nxt.item;
@@ -259,12 +279,11 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     if (tid < 64) sm.g[0][tid] = tid < nvalid ? a.g[(size_t)(tok0 + tid) * H + h] : 0.f;
     else if (tid < 128) sm.beta[0][tid - 64] = (tid - 64) < nvalid ? a.beta[(size_t)(tok0 + tid - 64) * H + h] : 0.f;
   }
-  float gb_next = 0.f;  // g (tid < 64) or beta (64 <= tid < 128) of the next item, loaded under P2
+  float gb_next = 0.f;  // g (tid < 64) or beta (64 <= tid < 128) of the next item, loaded under P5
   {
     const bool ok = mbar_wait(u32(&sm.bar_a), it & 1, err, 8) && mbar_wait(u32(&sm.bar_b), it & 1, err, 8);
-    pend_main = pend_do = false;
-    if (__syncthreads_or(!ok)) {
-      failed = true;
+    if (wbar_or(!ok)) {
+      failed = release = true;
       break;
     }
   }
@@ -290,28 +309,10 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     }
   }
   fence_async_smem();
-  __syncthreads();
-
-  // ---- P2: Y = dS K^T -> T3;  Qa = S0^T dO^T -> T5;  Z = dO^T P -> T4  (inputs and context only)
-  if (tid == 0) {
-    fence_after();
-    const uint32_t id_kk = idesc_f16(128, 64, false, false);
-    const uint32_t id_mk = idesc_f16(128, 64, true, false);
-    const uint32_t id_mm = idesc_f16(128, 64, true, true);
-    const uint32_t kb = u32(sm.kq), dsb = u32(sm.ds), dob = u32(sm.dob), sb = u32(sm.s0), pb = u32(sm.p);
-#pragma unroll 1
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
-      mma_f16(tm + T3, sdesc(dsb + aoff, 16, 1024), sdesc(kb + aoff, 16, 1024), id_kk, kk > 0);
-      mma_f16(tm + T5, sdesc(sb + kk * 2048, 2 * HT, 1024), sdesc(dob + (kk >> 2) * HT + (kk & 3) * 32, 16, 1024),
-              id_mk, kk > 0);
-    }
-#pragma unroll 1
-    for (int kk = 0; kk < 4; ++kk)
-      mma_f16(tm + T4, sdesc(dob + kk * 2048, HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id_mm, kk > 0);
-    mma_commit(u32(&sm.bar_mma));
+  if (__syncthreads_or(false)) {  // B2: the producer issues P2
+    failed = true;
+    break;
   }
-  __syncwarp();
   {  // meanwhile: <dS, S0> over the whole state (both tiles share one layout, so compare byte positions)
     float acc = 0.f;
     const uint4 *A4 = reinterpret_cast<const uint4 *>(sm.s0), *B4 = reinterpret_cast<const uint4 *>(sm.ds);
@@ -328,28 +329,43 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     acc = warp_sum(acc);
     if (lane == 0) sm.red[warp] = acc;
   }
-  if (__syncthreads_or(!mma_done())) {
-    failed = true;
+  if (wbar_or(!mma_done())) {  // P2
+    failed = release = true;
     break;
   }
-  {  // R2: dUt^T = cdec*Y + Z -> wt;  per-token sums <Ut, Y>, <dUt, Ut> over d_v (Ut^T from its tile),
-     // and gam <Qa, q^> over d_k (Qa = S0^T dO^T: the dO S0 part of dq^ dotted with q^)
-    float t1 = 0.f, t2 = 0.f, t3 = 0.f;
+  {  // R2: dUt^T = cdec*Y + Z -> wt (the per-token sums over Y and Z follow under P5)
 #pragma unroll 1
     for (int q4 = 0; q4 < 2; ++q4) {
       const int cb = c0 + q4 * 8;
-      float y[8], z[8], u[8], s1[8], s2[8];
-      {
-        float qa[8], gm[8];
-        tmem_ld8(tm + tl + T5 + cb, qa);
-        ld8f(G.gam + cb, gm);
+      float y[8], z[8], cd[8];
+      tmem_ld8x2(tm + tl + T3 + cb, y, tm + tl + T4 + cb, z);
+      ld8f(G.cdec + cb, cd);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) qa[i] *= gm[i] * ld_f16(sm.kq + HT, cb + i, row, 2 * HT);
-        const float a3 = colsum8(qa);
-        if ((lane >> 3) == q4) t3 = a3;
-      }
-      tmem_ld8(tm + tl + T3 + cb, y);
-      tmem_ld8(tm + tl + T4 + cb, z);
+      for (int i = 0; i < 8; ++i) z[i] = cd[i] * y[i] + z[i];
+      st_chunk_f16(sm.wt + chunk_off(row, cb), z);
+    }
+  }
+  fence_before();
+  fence_async_smem();
+  {  // X1, X2, Ahat of this item (loaded at the end of the previous one)
+    const bool ok = mbar_wait(u32(&sm.bar_w), it & 1, err, 8);
+    if (__syncthreads_or(!ok)) {  // B3: the producer issues P5
+      failed = true;
+      break;
+    }
+  }
+  if (nitem < n_items && tid < 128) {  // the next item's g or beta, stored under P7 (its plan lookups have landed by now)
+    const int r = tid & 63, nh = nitem % H;
+    if (r < nxt.nvalid)
+      gb_next = tid < 64 ? a.g[(size_t)(nxt.tok0 + r) * H + nh] : a.beta[(size_t)(nxt.tok0 + r) * H + nh];
+  }
+  {  // under P5: per-token sums <Ut, Y>, <dUt, Ut> over d_v (Y and Z stay in T3, T4 until P6; Ut^T from its tile)
+    float t1 = 0.f, t2 = 0.f;
+#pragma unroll 1
+    for (int q4 = 0; q4 < 2; ++q4) {
+      const int cb = c0 + q4 * 8;
+      float y[8], z[8], u[8], cd[8];
+      tmem_ld8x2(tm + tl + T3 + cb, y, tm + tl + T4 + cb, z);
       {
         const uint4 raw = *reinterpret_cast<const uint4 *>(sm.ut + chunk_off(row, cb));
         const __half2 *uh = reinterpret_cast<const __half2 *>(&raw);
@@ -360,17 +376,14 @@ __global__ void __launch_bounds__(LTHREADS, 1)
           u[2 * i + 1] = f.y;
         }
       }
-      float cd[8];
       ld8f(G.cdec + cb, cd);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float du = cd[i] * y[i] + z[i];
-        s1[i] = u[i] * y[i];
-        s2[i] = du * u[i];
-        z[i] = du;
+        y[i] *= u[i];
+        z[i] = du * u[i];
       }
-      st_chunk_f16(sm.wt + chunk_off(row, cb), z);
-      const float a1 = colsum8(s1), a2 = colsum8(s2);
+      const float a1 = colsum8(y), a2 = colsum8(z);
       if ((lane >> 3) == q4) {
         t1 = a1;
         t2 = a2;
@@ -378,55 +391,9 @@ __global__ void __launch_bounds__(LTHREADS, 1)
     }
     if (lane < 16) sm.part[wq][c0 + lane] = t1;
     if (lane < 16) sm.part[4 + wq][c0 + lane] = t2;
-    if (lane < 16) sm.part[8 + wq][c0 + lane] = t3;
   }
-  fence_before();
-  fence_async_smem();
-  __syncthreads();
-  if (tid < 64) {
-    sm.acc[0][tid] = sm.part[0][tid] + sm.part[1][tid] + sm.part[2][tid] + sm.part[3][tid];    // <Ut, Y>
-    sm.acc[1][tid] = sm.part[4][tid] + sm.part[5][tid] + sm.part[6][tid] + sm.part[7][tid];    // <dUt, Ut>
-    sm.acc[5][tid] = sm.part[8][tid] + sm.part[9][tid] + sm.part[10][tid] + sm.part[11][tid];  // gam <dO S0, q>
-  }
-
-  {  // X1, X2, Ahat of this item (loaded at the end of the previous one)
-    const bool ok = mbar_wait(u32(&sm.bar_w), it & 1, err, 8);
-    pend_wy = false;
-    if (__syncthreads_or(!ok)) {
-      failed = true;
-      break;
-    }
-  }
-  // ---- P5: dP = dO Ut^T -> T0; dW'^T = -S0^T dUt^T -> T1; dV^T = dUt^T X2 -> T6;  Kb = dS^T Ut^T -> T2
-  if (tid == 0) {
-    fence_after();
-    const uint32_t id_kmn = idesc_f16(128, 64, false, true);
-    const uint32_t id_mmn_neg = idesc_f16(128, 64, true, true, true);
-    const uint32_t dob = u32(sm.dob), ub = u32(sm.ut), sb = u32(sm.s0), dub = u32(sm.wt), x2b = u32(sm.x2);
-#pragma unroll 1
-    for (int kk = 0; kk < 8; ++kk) {
-      mma_f16(tm + T0, sdesc(dob + (kk >> 2) * HT + (kk & 3) * 32, 16, 1024), sdesc(ub + kk * 2048, 2 * HT, 1024),
-              id_kmn, kk > 0);
-      mma_f16(tm + T1, sdesc(sb + kk * 2048, 2 * HT, 1024), sdesc(dub + kk * 2048, 2 * HT, 1024), id_mmn_neg,
-              kk > 0);
-    }
-#pragma unroll 1
-    for (int kk = 0; kk < 4; ++kk)
-      mma_f16(tm + T6, sdesc(dub + kk * 32, 16, 1024), sdesc(x2b + kk * 2048, HT, 1024), id_kmn, kk > 0);
-    const uint32_t id_mm = idesc_f16(128, 64, true, true), dsb = u32(sm.ds);
-#pragma unroll 1
-    for (int kk = 0; kk < 8; ++kk)
-      mma_f16(tm + T2, sdesc(dsb + kk * 2048, 2 * HT, 1024), sdesc(ub + kk * 2048, 2 * HT, 1024), id_mm, kk > 0);
-    mma_commit(u32(&sm.bar_mma));
-  }
-  __syncwarp();
-  if (nitem < n_items && tid < 128) {  // the next item's g or beta, stored after dq (its plan lookups have landed by now)
-    const int r = tid & 63, nh = nitem % H;
-    if (r < nxt.nvalid)
-      gb_next = tid < 64 ? a.g[(size_t)(nxt.tok0 + r) * H + nh] : a.beta[(size_t)(nxt.tok0 + r) * H + nh];
-  }
-  if (__syncthreads_or(!mma_done())) {
-    failed = true;
+  if (wbar_or(!mma_done())) {  // P5
+    failed = release = true;
     break;
   }
   {
@@ -472,56 +439,49 @@ float rg[8];
       for (int i = 0; i < 8; ++i) v[i] *= gm[i];
       st_chunk_f16(sm.s0 + chunk_off(row, cb), v);
     }
-    // dV^T (lanes d_v, columns token): stage bf16 dv[token][d_v] in dob (dO is dead); <dV, v> comes
-    // with R6 as colsum(X2 M2)
-#pragma unroll 1
-    for (int q4 = 0; q4 < 2; ++q4) {
-      const int cb = c0 + q4 * 8;
-      float v[8];
-      tmem_ld8(tm + tl + T6 + cb, v);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) *stg_at(sm.dob, cb + i, row) = __float2bfloat16_rn(v[i]);
-    }
   }
   fence_before();
   fence_async_smem();
-  __syncthreads();
-  {
-    store_tile(&tmdv, a.dv, sm.dob, h, tok0, nvalid);
-    if (tid < 64) {
-      sm.acc[2][tid] = sm.part[16][tid] + sm.part[17][tid] + sm.part[18][tid] + sm.part[19][tid];  // row sums of dP * P
-      sm.acc[3][tid] = sm.part[10][tid] + sm.part[11][tid];  // column sums of dP * P
-    }
-  }
-  __syncthreads();
-
-  // ---- P6: Qb = K^T dPm^T -> T7;  M1 = dW' K^T -> T3;  M2 = dUt V^T -> T4
-  if (tid == 0) {
-    tma_store_wait_read();  // the dv tile store has read dob (the dq staging below rewrites it)
-    fence_after();
-    const uint32_t id_mk = idesc_f16(128, 64, true, false);
-    const uint32_t kb = u32(sm.kq), pb = u32(sm.p), dwb = u32(sm.s0), dub = u32(sm.wt), vb = u32(sm.v);
-#pragma unroll 1
-    for (int kk = 0; kk < 4; ++kk)
-      mma_f16(tm + T7, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(pb + kk * 32, 16, 1024), id_mk, kk > 0);
-#pragma unroll 1
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t boff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
-      mma_f16(tm + T3, sdesc(dwb + kk * 2048, 2 * HT, 1024), sdesc(kb + boff, 16, 1024), id_mk, kk > 0);
-      mma_f16(tm + T4, sdesc(dub + kk * 2048, 2 * HT, 1024), sdesc(vb + (kk >> 2) * HT + (kk & 3) * 32, 16, 1024),
-              id_mk, kk > 0);
-    }
-    mma_commit(u32(&sm.bar_mma));
-  }
-  __syncwarp();
-  if (__syncthreads_or(!mma_done())) {
+  if (__syncthreads_or(false)) {  // B4: the producer issues P6
     failed = true;
     break;
   }
-  {  // K^ -> wt (dUt^T is dead): R9 reads k^ there, so the K/Q buffer is free once P9 is done
-    const uint4 *src = reinterpret_cast<const uint4 *>(sm.kq);
-    uint4 *dst = reinterpret_cast<uint4 *>(sm.wt);
-    for (int e = tid; e < 2 * HT / 16; e += LTHREADS) dst[e] = src[(e >= HT / 16 ? 2 * HT / 16 : 0) + (e % (HT / 16))];
+  if (tid < 64) {
+    sm.acc[0][tid] = sm.part[0][tid] + sm.part[1][tid] + sm.part[2][tid] + sm.part[3][tid];      // <Ut, Y>
+    sm.acc[1][tid] = sm.part[4][tid] + sm.part[5][tid] + sm.part[6][tid] + sm.part[7][tid];      // <dUt, Ut>
+    sm.acc[2][tid] = sm.part[16][tid] + sm.part[17][tid] + sm.part[18][tid] + sm.part[19][tid];  // row sums of dP * P
+    sm.acc[3][tid] = sm.part[10][tid] + sm.part[11][tid];  // column sums of dP * P
+  }
+  {  // under P6: dV^T (lanes d_v, columns token) staged as bf16 dv[token][d_v] in dob (dO is dead; <dV, v>
+     // comes with R6 as colsum(X2 M2)); gam <Qa, q^> per token over d_k (Qa = S0^T dO^T: the dO S0 part
+     // of dq^ dotted with q^)
+    float t3 = 0.f;
+#pragma unroll 1
+    for (int q4 = 0; q4 < 2; ++q4) {
+      const int cb = c0 + q4 * 8;
+      float v[8], w[8], gm[8];
+      tmem_ld8x2(tm + tl + T6 + cb, w, tm + tl + T5 + cb, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) *stg_at(sm.dob, cb + i, row) = __float2bfloat16_rn(w[i]);
+      ld8f(G.gam + cb, gm);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] *= gm[i] * ld_f16(sm.kq + HT, cb + i, row, 2 * HT);
+      const float a3 = colsum8(v);
+      if ((lane >> 3) == q4) t3 = a3;
+    }
+    if (lane < 16) sm.part[12 + wq][c0 + lane] = t3;
+  }
+  fence_before();
+  fence_async_smem();
+  if (__syncthreads_or(false)) {  // B5: the producer stores a full dv tile
+    failed = true;
+    break;
+  }
+  if (nvalid < CH) store_rows(a.dv, sm.dob, h, tok0, nvalid);
+  if (tid < 64) sm.acc[5][tid] = sm.part[12][tid] + sm.part[13][tid] + sm.part[14][tid] + sm.part[15][tid];
+  if (wbar_or(!mma_done())) {  // P6
+    failed = release = true;
+    break;
   }
   {
     // M1, M2 (lanes 0-63 = r): dAhat = beta_i (M1 + Gamma M2); beta column sums colsum_i(Ahat (M1 + Gamma M2));
@@ -535,8 +495,7 @@ float rg[8];
       for (int q4 = 0; q4 < 2; ++q4) {
         const int cb = c0 + q4 * 8;
         float m1[8], m2[8];
-        tmem_ld8(tm + tl + T3 + cb, m1);
-        tmem_ld8(tm + tl + T4 + cb, m2);
+        tmem_ld8x2(tm + tl + T3 + cb, m1, tm + tl + T4 + cb, m2);
         const uint4 raw = *reinterpret_cast<const uint4 *>(sm.ah + chunk_off(r, cb));
         const __half *hh = reinterpret_cast<const __half *>(&raw);
         const uint4 xraw = *reinterpret_cast<const uint4 *>(sm.x2 + chunk_off(r, cb));
@@ -567,14 +526,53 @@ float rg[8];
       if (lane < 16) sm.part[10 + wq][c0 + lane] = ca;
       if (lane < 16) sm.part[14 + wq][c0 + lane] = cv;
     }
-    // dq raw = (scale dq^ - q^ (q^ . dq^) / scale) / |q|   (or scale dq^ without normalisation)
+  }
+  if (tid < 128) (tid < 64 ? sm.g[gbuf ^ 1] : sm.beta[gbuf ^ 1])[tid & 63] = gb_next;  // next item's g, beta
+  if (tid < 128) (tid < 64 ? sm.g[gbuf ^ 1] : sm.beta[gbuf ^ 1])[tid & 63] = gb_next;  // next item's g, beta
+  fence_before();
+  fence_async_smem();
+  if (__syncthreads_or(false)) {  // B6: the producer issues P7 and the next item's dO
+    failed = true;
+    break;
+  }
+  if (tid < 64) {
+    sm.acc[6][tid] = sm.part[8][tid] + sm.part[9][tid];    // beta col terms
+    sm.acc[7][tid] = sm.part[10][tid] + sm.part[11][tid];  // colsum(Ahat M1)
+    sm.acc[4][tid] = sm.part[14][tid] + sm.part[15][tid];  // <dV, v>
+  }
+  {  // K^ -> wt (dUt^T is dead): R9 reads k^ there, so the K/Q buffer is free once P9 is done
+    const uint4 *src = reinterpret_cast<const uint4 *>(sm.kq);
+    uint4 *dst = reinterpret_cast<uint4 *>(sm.wt);
+    for (int e = tid; e < 2 * HT / 16; e += LTHREADS) dst[e] = src[(e >= HT / 16 ? 2 * HT / 16 : 0) + (e % (HT / 16))];
+  }
+  if (warp == 1 && nitem < n_items) gate_prefix(sm.g[gbuf ^ 1], sm.gt[gbuf ^ 1]);  // next item's gates, under P7
+  if (wbar_or(!mma_done())) {  // P7
+    failed = release = true;
+    break;
+  }
+  if (row < 64) {  // R7: Y1 -> v (first half; V is dead)
+#pragma unroll 1
+    for (int q4 = 0; q4 < 2; ++q4) {
+      const int cb = c0 + q4 * 8;
+      float v[8];
+      tmem_ld8(tm + tl + T0 + cb, v);
+      st_chunk_f16(sm.v + chunk_off(row, cb), v);
+    }
+  }
+  fence_before();
+  fence_async_smem();
+  if (__syncthreads_or(false)) {  // B7: the producer issues P8
+    failed = true;
+    break;
+  }
+  {  // under P8: dq raw = (scale dq^ - q^ (q^ . dq^) / scale) / |q|   (or scale dq^ without normalisation),
+     // staged in ds (dS is dead: its last reader, Kb, completed under P6)
     const float rscale = 1.f / a.scale;
 #pragma unroll 1
     for (int q4 = 0; q4 < 2; ++q4) {
       const int cb = c0 + q4 * 8;
       float qa[8], qb[8];
-      tmem_ld8(tm + tl + T5 + cb, qa);
-      tmem_ld8(tm + tl + T7 + cb, qb);
+      tmem_ld8x2(tm + tl + T5 + cb, qa, tm + tl + T7 + cb, qb);
       float gm[8], dt[8], nqv[8];
       ld8f(G.gam + cb, gm);
       if (l2) {  // q^ . dq^ = gam <Qa, q^> + sum_s dP * P (the Qb part: row sums of dP * P)
@@ -596,73 +594,19 @@ float rg[8];
         } else {
           o = a.scale * dq;
         }
-        *stg_at(sm.dob, tkn, row) = __float2bfloat16_rn(o);
+        *stg_at(sm.ds, tkn, row) = __float2bfloat16_rn(o);
       }
     }
   }
   fence_before();
   fence_async_smem();
-  __syncthreads();
-  {
-    store_tile(&tmdq, a.dq, sm.dob, h, tok0, nvalid);
-    if (tid < 64) {
-      sm.acc[6][tid] = sm.part[8][tid] + sm.part[9][tid];    // beta col terms
-      sm.acc[7][tid] = sm.part[10][tid] + sm.part[11][tid];  // colsum(Ahat M1)
-      sm.acc[4][tid] = sm.part[14][tid] + sm.part[15][tid];  // <dV, v>
-    }
-    if (tid < 128) (tid < 64 ? sm.g[gbuf ^ 1] : sm.beta[gbuf ^ 1])[tid & 63] = gb_next;  // next item's g, beta
-  }
-  fence_async_smem();
-  __syncthreads();
-  if (nitem < n_items) {  // dO of the next item into its (now free) buffer
-    if (tid == 0) {
-      tma_store_wait_read();  // the dq tile store has read dob
-      issue_do(nitem, nxt.tok0);
-    }
-    pend_do = true;
-  }
-
-  // ---- P7: Y1 = Ahat^T dAhat -> T0
-  if (tid == 0) {
-    fence_after();
-    const uint32_t id = idesc_f16(128, 64, true, true);
-    const uint32_t ab = u32(sm.ah), dab = u32(sm.x2);
-#pragma unroll 1
-    for (int kk = 0; kk < 4; ++kk)
-      mma_f16(tm + T0, sdesc(ab + kk * 2048, HT, 1024), sdesc(dab + kk * 2048, HT, 1024), id, kk > 0);
-    mma_commit(u32(&sm.bar_mma));
-  }
-  __syncwarp();
-  if (warp == 1 && nitem < n_items) gate_prefix(sm.g[gbuf ^ 1], sm.gt[gbuf ^ 1]);  // next item's gates, under P7
-  if (__syncthreads_or(!mma_done())) {
+  if (__syncthreads_or(false)) {  // B8: the producer stores a full dq tile
     failed = true;
     break;
   }
-  if (row < 64) {  // R7: Y1 -> v (first half; V is dead)
-#pragma unroll 1
-    for (int q4 = 0; q4 < 2; ++q4) {
-      const int cb = c0 + q4 * 8;
-      float v[8];
-      tmem_ld8(tm + tl + T0 + cb, v);
-      st_chunk_f16(sm.v + chunk_off(row, cb), v);
-    }
-  }
-  fence_before();
-  fence_async_smem();
-  __syncthreads();
-
-  // ---- P8: dT = -Y1 Ahat^T -> T1
-  if (tid == 0) {
-    fence_after();
-    const uint32_t id = idesc_f16(128, 64, false, false, true);
-    const uint32_t yb = u32(sm.v), ab = u32(sm.ah);
-#pragma unroll 1
-    for (int kk = 0; kk < 4; ++kk) mma_f16(tm + T1, sdesc(yb + kk * 32, 16, 1024), sdesc(ab + kk * 32, 16, 1024), id, kk > 0);
-    mma_commit(u32(&sm.bar_mma));
-  }
-  __syncwarp();
-  if (__syncthreads_or(!mma_done())) {
-    failed = true;
+  if (nvalid < CH) store_rows(a.dq, sm.ds, h, tok0, nvalid);
+  if (wbar_or(!mma_done())) {  // P8
+    failed = release = true;
     break;
   }
   if (row < 64) {  // R8: dN[r][i] = beta_r dT_ri (i < r), zero elsewhere; beta row sums of dT * N
@@ -695,27 +639,7 @@ float rg[8];
   }
   fence_before();
   fence_async_smem();
-  __syncthreads();
-
-  // ---- P9: Ka = Q^T dPm + dW'^T X1 + K^T Sigma -> T3  (Kb = dS^T Ut^T came with P5, in T2)
-  if (tid == 0) {
-    fence_after();
-    const uint32_t id_mm = idesc_f16(128, 64, true, true);
-    const uint32_t id_km = idesc_f16(128, 64, false, true);
-    const uint32_t id_mk = idesc_f16(128, 64, true, false);
-    const uint32_t kb = u32(sm.kq), pb = u32(sm.p), dwb = u32(sm.s0), x1b = u32(sm.x1), sgb = u32(sm.v + HT);
-#pragma unroll 1
-    for (int kk = 0; kk < 4; ++kk) {
-      mma_f16(tm + T3, sdesc(kb + HT + kk * 2048, 2 * HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id_mm, kk > 0);
-      mma_f16(tm + T3, sdesc(dwb + kk * 32, 16, 1024), sdesc(x1b + kk * 2048, HT, 1024), id_km, true);
-      // K^T (dN + dN^T): the dN tile read once as MN-major (dN) and once as K-major (dN^T)
-      mma_f16(tm + T3, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(sgb + kk * 2048, HT, 1024), id_mm, true);
-      mma_f16(tm + T3, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(sgb + kk * 32, 16, 1024), id_mk, true);
-    }
-    mma_commit(u32(&sm.bar_mma));
-  }
-  __syncwarp();
-  if (__syncthreads_or(!mma_done())) {
+  if (__syncthreads_or(false)) {  // B9: the producer issues P9, then the next item's main tiles once P9 is done
     failed = true;
     break;
   }
@@ -725,41 +649,8 @@ float rg[8];
     sm.acc[8][t] = sm.acc[3][t] + gbeta[t] * (sm.acc[7][t] + rbs) + (sm.part[12][t] + sm.part[13][t]) +
                    G.cdec[t] * sm.acc[0][t];
   }
-  fence_async_smem();
-  __syncthreads();
-  if (nitem < n_items) {  // K, Q, V, S0, dS of the next item: their buffers are free after P9
-    if (tid == 0) issue_main(nitem);
-    pend_main = true;
-  }
-  {  // R9: dk^T = Ka + cdec * Kb (lanes d_k); Jacobian; dk out
-    uint8_t *const stg = sm.x2;  // x2 + ah (16 KB, both dead after P8)
-#pragma unroll 1
-    for (int q4 = 0; q4 < 2; ++q4) {
-      const int cb = c0 + q4 * 8;
-      float ka[8], kbv[8];
-      tmem_ld8(tm + tl + T3 + cb, ka);
-      tmem_ld8(tm + tl + T2 + cb, kbv);
-      float cd[8], dt[8], nkv[8];
-      ld8f(G.cdec + cb, cd);
-      if (l2) {
-        ld8f(sm.acc[8] + cb, dt);
-        ld8f(sm.nk + cb, nkv);
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int tkn = cb + i;
-        float o = ka[i] + cd[i] * kbv[i];
-        if (l2) o = (o - ld_f16(sm.wt, tkn, row, HT) * dt[i]) * nkv[i];
-        *stg_at(stg, tkn, row) = __float2bfloat16_rn(o);
-      }
-    }
-  }
-  fence_before();
-  fence_async_smem();
-  __syncthreads();
-  store_tile(&tmdk, a.dk, sm.x2, h, tok0, nvalid);
   // ---- gate and beta gradients
-  if (warp == 0) {
+  if (warp == LWARPS - 1) {  // under P9 (the other warps' shadow work is the k^ . dk^ sum)
     float dGv[2];
     float sumy = 0.f;
 #pragma unroll
@@ -793,20 +684,218 @@ float rg[8];
       }
     }
   }
-  __syncthreads();  // the next item rewrites the per-token scratch read above
-  if (tid == 0) tma_store_wait_read();  // the dk tile store has read x2 / ah (rewritten by the next item)
-  if (nitem < n_items) {  // X1, X2, Ahat of the next item (x2/ah held the dk staging until now)
-    if (tid == 0) issue_wy(nitem);
-    pend_wy = true;
+  if (wbar_or(!mma_done())) {  // P9
+    failed = release = true;
+    break;
+  }
+  {  // R9: dk^T = Ka + cdec * Kb (lanes d_k); Jacobian; dk out
+    uint8_t *const stg = sm.x2;  // x2 + ah (16 KB, both dead after P8)
+#pragma unroll 1
+    for (int q4 = 0; q4 < 2; ++q4) {
+      const int cb = c0 + q4 * 8;
+      float ka[8], kbv[8];
+      tmem_ld8x2(tm + tl + T3 + cb, ka, tm + tl + T2 + cb, kbv);
+      float cd[8], dt[8], nkv[8];
+      ld8f(G.cdec + cb, cd);
+      if (l2) {
+        ld8f(sm.acc[8] + cb, dt);
+        ld8f(sm.nk + cb, nkv);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int tkn = cb + i;
+        float o = ka[i] + cd[i] * kbv[i];
+        if (l2) o = (o - ld_f16(sm.wt, tkn, row, HT) * dt[i]) * nkv[i];
+        *stg_at(stg, tkn, row) = __float2bfloat16_rn(o);
+      }
+    }
+  }
+  fence_before();
+  fence_async_smem();
+  if (__syncthreads_or(false)) {  // B10: the producer stores a full dk tile
+    failed = true;
+    break;
+  }
+  if (nvalid < CH) {
+    store_rows(a.dk, sm.x2, h, tok0, nvalid);
+    if (__syncthreads_or(false)) {  // B11: x2 / ah read, the producer may load the next WY tiles
+      failed = true;
+      break;
+    }
   }
   cur = nxt;
   }
-  if (failed) {  // let prefetches already in flight land before the CTA leaves (bounded waits)
-    if (pend_main) mbar_wait(u32(&sm.bar_a), (it + 1) & 1, err, 8);
-    if (pend_do) mbar_wait(u32(&sm.bar_b), (it + 1) & 1, err, 8);
-    if (pend_wy) mbar_wait(u32(&sm.bar_w), it & 1, err, 8);  // issued for the item of iteration it
+  if (release) __syncthreads_or(true);  // meet the producer at its pending CTA-wide barrier: it stops there
+  } else {
+  // ---------------- producer warp 16 (lane 0): every tensor-core product, TMA load and TMA store
+  bool pend_main = cur.item < n_items, pend_do = pend_main, pend_wy = pend_main;  // loads in flight
+  for (; cur.item < n_items; ++it) {
+    const ItemInfo nxt = info_of(next_valid(cur.item + gridDim.x));
+    const int nitem = nxt.item;
+    const int item = cur.item, h = item % H, tok0 = cur.tok0, nvalid = cur.nvalid;
+    {
+      const bool f = __syncthreads_or(false);  // B2
+      pend_main = pend_do = false;  // the workers waited for both (a failed wait is not repeated)
+      if (f) break;
+    }
+    // ---- P2: Y = dS K^T -> T3;  Qa = S0^T dO^T -> T5;  Z = dO^T P -> T4  (inputs and context only)
+    if (lane == 0) {
+      fence_after();
+      const uint32_t id_kk = idesc_f16(128, 64, false, false);
+      const uint32_t id_mk = idesc_f16(128, 64, true, false);
+      const uint32_t id_mm = idesc_f16(128, 64, true, true);
+      const uint32_t kb = u32(sm.kq), dsb = u32(sm.ds), dob = u32(sm.dob), sb = u32(sm.s0), pb = u32(sm.p);
+#pragma unroll 1
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
+        mma_f16(tm + T3, sdesc(dsb + aoff, 16, 1024), sdesc(kb + aoff, 16, 1024), id_kk, kk > 0);
+      }
+#pragma unroll 1
+      for (int kk = 0; kk < 4; ++kk)
+        mma_f16(tm + T4, sdesc(dob + kk * 2048, HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id_mm, kk > 0);
+      mma_commit(u32(&sm.bar_mma));
+      // Qa is first read under P6: the P5 commit covers it (the tensor cores run in issue order)
+#pragma unroll 1
+      for (int kk = 0; kk < 8; ++kk)
+        mma_f16(tm + T5, sdesc(sb + kk * 2048, 2 * HT, 1024), sdesc(dob + (kk >> 2) * HT + (kk & 3) * 32, 16, 1024),
+                id_mk, kk > 0);
+    }
+    __syncwarp();
+    {
+      const bool f = __syncthreads_or(false);  // B3
+      pend_wy = false;
+      if (f) break;
+    }
+    // ---- P5: dP = dO Ut^T -> T0; dW'^T = -S0^T dUt^T -> T1; dV^T = dUt^T X2 -> T6;  Kb = dS^T Ut^T -> T2
+    if (lane == 0) {
+      fence_after();
+      const uint32_t id_kmn = idesc_f16(128, 64, false, true);
+      const uint32_t id_mmn_neg = idesc_f16(128, 64, true, true, true);
+      const uint32_t dob = u32(sm.dob), ub = u32(sm.ut), sb = u32(sm.s0), dub = u32(sm.wt), x2b = u32(sm.x2);
+#pragma unroll 1
+      for (int kk = 0; kk < 8; ++kk) {
+        mma_f16(tm + T0, sdesc(dob + (kk >> 2) * HT + (kk & 3) * 32, 16, 1024), sdesc(ub + kk * 2048, 2 * HT, 1024),
+                id_kmn, kk > 0);
+        mma_f16(tm + T1, sdesc(sb + kk * 2048, 2 * HT, 1024), sdesc(dub + kk * 2048, 2 * HT, 1024), id_mmn_neg,
+                kk > 0);
+      }
+#pragma unroll 1
+      for (int kk = 0; kk < 4; ++kk)
+        mma_f16(tm + T6, sdesc(dub + kk * 32, 16, 1024), sdesc(x2b + kk * 2048, HT, 1024), id_kmn, kk > 0);
+      mma_commit(u32(&sm.bar_mma));
+      // Kb is first read in R9: the P6 commit covers it
+      const uint32_t id_mm = idesc_f16(128, 64, true, true), dsb = u32(sm.ds);
+#pragma unroll 1
+      for (int kk = 0; kk < 8; ++kk)
+        mma_f16(tm + T2, sdesc(dsb + kk * 2048, 2 * HT, 1024), sdesc(ub + kk * 2048, 2 * HT, 1024), id_mm, kk > 0);
+    }
+    __syncwarp();
+    if (__syncthreads_or(false)) break;  // B4
+    // ---- P6: M1 = dW' K^T -> T3;  M2 = dUt V^T -> T4;  then Qb = K^T dPm^T -> T7 (first read under P8: the
+    //      P7 commit covers it)
+    if (lane == 0) {
+      fence_after();
+      const uint32_t id_mk = idesc_f16(128, 64, true, false);
+      const uint32_t kb = u32(sm.kq), pb = u32(sm.p), dwb = u32(sm.s0), dub = u32(sm.wt), vb = u32(sm.v);
+#pragma unroll 1
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t boff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
+        mma_f16(tm + T3, sdesc(dwb + kk * 2048, 2 * HT, 1024), sdesc(kb + boff, 16, 1024), id_mk, kk > 0);
+        mma_f16(tm + T4, sdesc(dub + kk * 2048, 2 * HT, 1024), sdesc(vb + (kk >> 2) * HT + (kk & 3) * 32, 16, 1024),
+                id_mk, kk > 0);
+      }
+      mma_commit(u32(&sm.bar_mma));
+#pragma unroll 1
+      for (int kk = 0; kk < 4; ++kk)
+        mma_f16(tm + T7, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(pb + kk * 32, 16, 1024), id_mk, kk > 0);
+    }
+    __syncwarp();
+    if (__syncthreads_or(false)) break;  // B5
+    if (lane == 0 && nvalid == CH) store_tma(&tmdv, sm.dob, h, tok0);
+    if (__syncthreads_or(false)) break;  // B6
+    // ---- P7: Y1 = Ahat^T dAhat -> T0;  then Ka's context-only part Q^T dPm + dW'^T X1 -> T3 (first read in
+    //      R9: the P8 commit covers it; M1 in T3 was read above)
+    if (lane == 0) {
+      fence_after();
+      const uint32_t id = idesc_f16(128, 64, true, true);
+      const uint32_t id_km = idesc_f16(128, 64, false, true);
+      const uint32_t ab = u32(sm.ah), dab = u32(sm.x2);
+      const uint32_t kb = u32(sm.kq), pb = u32(sm.p), dwb = u32(sm.s0), x1b = u32(sm.x1);
+#pragma unroll 1
+      for (int kk = 0; kk < 4; ++kk)
+        mma_f16(tm + T0, sdesc(ab + kk * 2048, HT, 1024), sdesc(dab + kk * 2048, HT, 1024), id, kk > 0);
+      mma_commit(u32(&sm.bar_mma));
+#pragma unroll 1
+      for (int kk = 0; kk < 4; ++kk) {
+        mma_f16(tm + T3, sdesc(kb + HT + kk * 2048, 2 * HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id, kk > 0);
+        mma_f16(tm + T3, sdesc(dwb + kk * 32, 16, 1024), sdesc(x1b + kk * 2048, HT, 1024), id_km, true);
+      }
+      if (nitem < n_items) {  // dO of the next item into its buffer, once the dv tile store has read it
+        tma_store_wait_read();
+        issue_do(nitem, nxt.tok0);
+      }
+    }
+    __syncwarp();
+    if (nitem < n_items) pend_do = true;
+    if (__syncthreads_or(false)) break;  // B7
+    // ---- P8: dT = -Y1 Ahat^T -> T1
+    if (lane == 0) {
+      fence_after();
+      const uint32_t id = idesc_f16(128, 64, false, false, true);
+      const uint32_t yb = u32(sm.v), ab = u32(sm.ah);
+#pragma unroll 1
+      for (int kk = 0; kk < 4; ++kk) mma_f16(tm + T1, sdesc(yb + kk * 32, 16, 1024), sdesc(ab + kk * 32, 16, 1024), id, kk > 0);
+      mma_commit(u32(&sm.bar_mma));
+    }
+    __syncwarp();
+    if (__syncthreads_or(false)) break;  // B8
+    if (lane == 0 && nvalid == CH) store_tma(&tmdq, sm.ds, h, tok0);
+    if (__syncthreads_or(false)) break;  // B9
+    // ---- P9: Ka += K^T (dN + dN^T) -> T3  (Ka's context-only part came with P7; Kb = dS^T Ut^T with P5, in T2)
+    if (lane == 0) {
+      fence_after();
+      const uint32_t id_mm = idesc_f16(128, 64, true, true);
+      const uint32_t id_mk = idesc_f16(128, 64, true, false);
+      const uint32_t kb = u32(sm.kq), sgb = u32(sm.v + HT);
+#pragma unroll 1
+      for (int kk = 0; kk < 4; ++kk) {
+        // the dN tile read once as MN-major (dN) and once as K-major (dN^T)
+        mma_f16(tm + T3, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(sgb + kk * 2048, HT, 1024), id_mm, true);
+        mma_f16(tm + T3, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(sgb + kk * 32, 16, 1024), id_mk, true);
+      }
+      mma_commit(u32(&sm.bar_mma));
+    }
+    __syncwarp();
+    // K, Q, V, S0, dS, Ut^T, P, N of the next item once P9 is done (ds also once the dq store has read it);
+    // P9 is the sixth of six commits per item: its completion has parity 1
+    if (lane == 0 && nitem < n_items && mbar_wait(u32(&sm.bar_mma), 1, err, 4)) {
+      tma_store_wait_read();
+      issue_main(nitem);
+      pend_main = true;  // the flags are read by lane 0 only
+    }
+    __syncwarp();
+    if (__syncthreads_or(false)) break;  // B10
+    if (lane == 0 && nvalid == CH) store_tma(&tmdk, sm.x2, h, tok0);
+    if (nvalid < CH && __syncthreads_or(false)) break;  // B11
+    if (lane == 0 && nitem < n_items) {  // X1, X2, Ahat of the next item once the dk staging is read
+      tma_store_wait_read();
+      issue_wy(nitem);
+    }
+    __syncwarp();
+    if (nitem < n_items) pend_wy = true;
+    cur = nxt;
   }
-  if (tid == 0) tma_store_wait_all();  // output tiles written before the CTA leaves
+  failed = cur.item < n_items;
+  if (lane == 0) {
+    if (failed) {  // let loads already in flight land before the CTA leaves (bounded waits)
+      if (pend_main) mbar_wait(u32(&sm.bar_a), (it + 1) & 1, err, 8);
+      if (pend_do) mbar_wait(u32(&sm.bar_b), (it + 1) & 1, err, 8);
+      if (pend_wy) mbar_wait(u32(&sm.bar_w), it & 1, err, 8);  // issued for the item of iteration it
+    }
+    tma_store_wait_all();  // output tiles written before the CTA leaves
+  }
+  __syncwarp();
+  }
   fence_before();
   __syncthreads();
   fence_after();
@@ -832,7 +921,7 @@ int launch_bwd_local_tc(const BwdArgs &a, const CUtensorMap *maps, int CH_max, c
   }
   const int n_items = CH_max * a.H;
   const int grid = n_items < sms ? n_items : sms;  // persistent: one CTA per SM
-  return (int)launch_pdl(bwd_local_tc_kernel, dim3(grid), dim3(LTHREADS), smem, st, a, maps[0], maps[1], maps[2],
+  return (int)launch_pdl(bwd_local_tc_kernel, dim3(grid), dim3(LNTHREADS), smem, st, a, maps[0], maps[1], maps[2],
                          maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], n_items);
 }
 
