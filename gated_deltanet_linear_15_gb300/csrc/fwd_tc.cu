@@ -35,7 +35,8 @@ namespace {
 
 constexpr int D = 128;
 constexpr int HT = 8192;  // one 64 x 64 fp16 half-tile, 128B-swizzled
-constexpr int FT = 512;   // threads per CTA
+constexpr int FT = 512;   // worker threads (16 warps); warp 16 is the producer
+constexpr int FWARPS = FT / 32;
 
 // TMEM columns
 constexpr uint32_t TM_S = 0, TM_KQ = 128, TM_W = 192, TM_U = 256, TM_O = 320, TM_OA = 384, TM_COLS = 512;
@@ -75,7 +76,7 @@ __device__ __forceinline__ void st_chunk_f16(uint8_t *dst, const float *v) {
 // byte offset of the 16-byte chunk holding columns [cb, cb + 8) of row r in a swizzled [rows][64] tile
 __device__ __forceinline__ uint32_t chunk_off(int r, int cb) { return r * 128 + ((((cb & 63) >> 3) ^ (r & 7)) << 4); }
 
-__global__ void __launch_bounds__(FT, 1)
+__global__ void __launch_bounds__(FT + 32, 1)
     fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmw,
                   const __grid_constant__ CUtensorMap tms, const __grid_constant__ CUtensorMap tmt,
@@ -185,7 +186,7 @@ __global__ void __launch_bounds__(FT, 1)
     load_scalars(sm.beta[stage], a.beta, H, h, tok0, nvalid, 64);
     cp_async_commit();
   };
-  if (tid == 0 && cfirst < cend) issue_tma(cfirst, 0);
+  if (tid == FT && cfirst < cend) issue_tma(cfirst, 0);
   if (cfirst < cend) issue_gb(cfirst, 0, true);
 
   // ---------------------------------------------------------------- initial state -> TMEM
@@ -195,7 +196,7 @@ __global__ void __launch_bounds__(FT, 1)
       if (mode == START_INIT) src = a.S0 ? a.S0 + ((size_t)n * H + h) * DD : nullptr;
       else if (mode == START_FIXUP && a.pass != 0) src = a.Sstart + sh_idx * DD;
     }
-    {
+    if (warp < FWARPS) {
       const int c0 = wg * 32;
       float v[32];
 #pragma unroll
@@ -298,7 +299,13 @@ __global__ void __launch_bounds__(FT, 1)
     }
   };
 
-  for (int c = cfirst; c < cend && !failed; ++c) {
+  // Worker warps 0-15 do the read-outs and the CUDA-core work; lane 0 of warp 16 (the producer) issues
+  // every TMA copy and tensor-core product, so no worker waits on a blocking MMA issue.  The two sides
+  // meet at CTA-wide OR-barriers (A1, A3, A4, A5; A2 on a segment's first chunk) that also carry a
+  // failed wait; the workers sync among themselves on barrier 2, and the producer tells them that a
+  // context store has read wu (barrier 3, arrive / sync).
+  const bool producer = warp == FWARPS;
+  for (int c = cfirst; c < cend; ++c) {
     const int it = c - cfirst;
     const int stage = it & 1;
     const bool emit = outputs && c >= cbeg;  // Q, P (and the output if wanted)
@@ -309,91 +316,209 @@ __global__ void __launch_bounds__(FT, 1)
     const int tok0 = bos + c * CH;
     const int nvalid = min(CH, len - c * CH);
     uint8_t *st = sm.ring[stage];
-
+    const bool more = c + 1 < cend;
+    const int nvn = more ? min(CH, len - (c + 1) * CH) : 0;
+    uint8_t *stn = sm.ring[stage ^ 1];
     float *gbeta = sm.beta[stage];
+    Gates &G = sm.gt[stage];
+
+    if (producer) {
+      // ================================================================ producer
+      // the previous chunk's tile stores have read s0 / x1 / x2 / ah / p / its ring stage (rewritten next)
+      if (lane == 0 && (save_states || save_wy)) tma_store_wait_read();
+      __syncwarp();
+      if (__syncthreads_or(false)) {  // A1
+        failed = true;
+        break;
+      }
+      // the next chunk into the other stage: its last reader, the previous chunk's MMA 4, completed
+      if (lane == 0 && more) issue_tma(c + 1, stage ^ 1);
+      if (it == 0) {
+        __syncthreads_or(false);  // A2: the first chunk normalised
+        if (lane == 0) {
+          fence_after();
+          issue_mma1(st);
+        }
+      }
+      __syncwarp();
+      if (__syncthreads_or(false)) {  // A3: Ahat, X1, X2, P and the fp16 state copy are in shared memory
+        failed = true;
+        break;
+      }
+      if (lane == 0) {
+        fence_after();
+        if (save_c) {  // X1, X2, Ahat and P of this (chunk, head), and its K, Q, V operand tiles
+          tma_store_3d(&tmw, 0, t64row + T64_X1 * CH, 0, u32(sm.x1));
+          tma_store_3d(&tmw, 0, t64row + T64_X2 * CH, 0, u32(sm.x2));
+          tma_store_3d(&tmw, 0, t64row + T64_AH * CH, 0, u32(sm.ah));
+          tma_store_3d(&tmw, 0, t64row + T64_P * CH, 0, u32(sm.p));
+          const int qrow = ((chunk0 + c) * H + h) * TQ_TILES * CH;
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
+            tma_store_3d(&tm3, 64 * hb, qrow + TQ_K * CH, 0, u32(st + 2 * hb * HT));
+            tma_store_3d(&tm3, 64 * hb, qrow + TQ_Q * CH, 0, u32(st + (2 * hb + 1) * HT));
+            tma_store_3d(&tm3, 64 * hb, qrow + TQ_V * CH, 0, u32(st + (4 + hb) * HT));
+          }
+        }
+        if (save_states && c >= cbeg) {  // the fp16 chunk-start state, two 64-column blocks
+          const int srow = ((chunk0 + c) * H + h) * D;
+          tma_store_3d(&tms, 0, srow, 0, u32(sm.s0));
+          tma_store_3d(&tms, 64, srow, 0, u32(sm.s0 + 2 * HT));
+        }
+        if (save_c || (save_states && c >= cbeg)) tma_store_commit();
+        // ---- MMA 2: W^T = K^T X1^T, U^T = V^T X2^T  (M = 128, N = 64, K = 64)
+        const uint32_t idesc = idesc_f16(128, 64, true, false);
+        const uint32_t kb = u32(st), vb = u32(st + 4 * HT);
+        const uint32_t x1b = u32(sm.x1), x2b = u32(sm.x2);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f16(tm + TM_W, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(x1b + kk * 32, 16, 1024), idesc, kk > 0);
+        if (need_v) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f16(tm + TM_U, sdesc(vb + kk * 2048, HT, 1024), sdesc(x2b + kk * 32, 16, 1024), idesc, kk > 0);
+        }
+        mma_commit(u32(&sm.bar_mma));
+        // Oi^T = S0 Q^T needs only the state copy and Q: it runs under the W^T read-out (MMA 3's commit
+        // covers it)
+        if (emit_o) {
+          const uint32_t s0b = u32(sm.s0), qb = u32(st + HT);
+          const uint32_t id_o = idesc_f16(128, 64, false, false);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
+            mma_f16(tm + TM_O, sdesc(s0b + aoff, 16, 1024), sdesc(qb + aoff, 16, 1024), id_o, kk > 0);
+          }
+        }
+      }
+      __syncwarp();
+      if (__syncthreads_or(false)) {  // A4: the gam-scaled W^T is in wu
+        failed = true;
+        break;
+      }
+      if (lane == 0) {
+        fence_after();
+        if (save_c) {  // the gam-scaled W^T tile
+          tma_store_3d(&tmt, 0, t128row + T128_W * D, 0, u32(sm.wu));
+          tma_store_commit();
+        }
+        // ---- MMA 3: Ut^T = U^T - S0 W^T   (M = 128, N = 64, K = 128)
+        const uint32_t s0b = u32(sm.s0), wb = u32(sm.wu);
+        const uint32_t id_u = idesc_f16(128, 64, false, true, /*neg_a=*/true);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
+          mma_f16(tm + TM_U, sdesc(s0b + aoff, 16, 1024), sdesc(wb + kk * 2048, 2 * HT, 1024), id_u,
+                  need_v || kk > 0);
+        }
+        mma_commit(u32(&sm.bar_mma));
+        if (save_c) tma_store_wait_read();  // the W^T store has read wu (Ut^T is written next)
+      }
+      __syncwarp();
+      named_bar_arrive<3, FT + 32>();
+      if (__syncthreads_or(false)) {  // A5: Ut^T, Ut^T diag(cdec) and the next chunk's K, Q are ready
+        failed = true;
+        break;
+      }
+      if (lane == 0) {
+        fence_after();
+        if (save_c) {  // the Ut^T tile
+          tma_store_3d(&tmt, 0, t128row + T128_U * D, 0, u32(sm.wu));
+          tma_store_commit();
+        }
+        // ---- MMA 4: S += (Ut^T diag(cdec)) K (N = 128, K = 64);  Oa^T = Ut^T P^T (N = 64, K = 64)
+        const uint32_t ucb = u32(sm.uc), ub = u32(sm.wu), kb = u32(st), pb = u32(sm.p);
+        const uint32_t id_s = idesc_f16(128, 128, false, true);
+        const uint32_t id_o = idesc_f16(128, 64, false, false);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f16(tm + TM_S, sdesc(ucb + kk * 32, 16, 1024), sdesc(kb + kk * 2048, 2 * HT, 1024), id_s, true);
+        if (emit_o) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f16(tm + TM_OA, sdesc(ub + kk * 32, 16, 1024), sdesc(pb + kk * 32, 16, 1024), id_o, kk > 0);
+        }
+        mma_commit(u32(&sm.bar_mma));
+        if (save_c && emit_o) tma_store_wait_read();  // the Ut^T store has read wu (the O staging)
+      }
+      __syncwarp();
+      named_bar_arrive<3, FT + 32>();
+      // the next chunk's Gram product: its K, Q were normalised while MMA 3 ran; it runs during this
+      // chunk's O read-out
+      if (lane == 0 && more) issue_mma1(stn);
+      __syncwarp();
+      continue;
+    }
+
+    // ================================================================ workers
     float gnext0 = 0.f, gnext1 = 0.f;  // next chunk's log-gates (warp 0), consumed while MMA 4 runs
-    if (warp == 0 && c + 1 < cend) {
-      const int tokn = bos + (c + 1) * CH, nvn = min(CH, len - (c + 1) * CH);
+    if (warp == 0 && more) {
+      const int tokn = bos + (c + 1) * CH;
       if (lane < nvn) gnext0 = a.g[(size_t)(tokn + lane) * H + h];
       if (lane + 32 < nvn) gnext1 = a.g[(size_t)(tokn + lane + 32) * H + h];
     }
     // g, beta of this chunk (issued one chunk ahead) must have landed before the next prefetch reuses cp.async
     cp_async_wait_all();
-    // the previous chunk's tile stores have read s0 / x1 / x2 / ah / its ring stage (overwritten below)
-    if (tid == 0 && (save_states || save_wy)) tma_store_wait_read();
-    // prefetch the next chunk into the other stage (its previous contents were consumed)
-    if (tid == 0 && c + 1 < cend) issue_tma(c + 1, stage ^ 1);
-    if (c + 1 < cend) issue_gb(c + 1, stage ^ 1, false);
+    if (more) issue_gb(c + 1, stage ^ 1, false);
     // chunk cfirst: wait for its tiles and normalise them here; later chunks were normalised one
     // iteration ahead, while MMA 3 and MMA 4 of the previous chunk ran
     const bool tma_ok = it > 0 || mbar_wait(u32(&sm.bar_tma[stage]), 0, err, 8);
-    if (__syncthreads_or(!tma_ok)) {
+    if (__syncthreads_or(!tma_ok || failed)) {  // A1
       failed = true;
       break;
     }
-    Gates &G = sm.gt[stage];
     if (it == 0) {
       if (warp == 0 && gate_prefix(sm.g[stage], G) && lane == 0 && err) atomicOr(err, 1);
       prep_kq(st, nvalid, emit, save_c ? a.nrm + ((size_t)(chunk0 + c) * H + h) * 2 * CH : nullptr);
       if (need_v) prep_v(st, nvalid);
       fence_async_smem();
+      __syncthreads_or(false);  // A2: the producer issues MMA 1
     }
-    __syncthreads();
+    {  // MMA 1: [K; Q] K^T (the first chunk here; later chunks had it issued after the previous MMA 4)
+      const bool ok = mbar_wait(u32(&sm.bar_kq), kq_phase, err, 4);
+      kq_phase ^= 1;
+      fence_after();
+      failed |= !ok;
+    }
 
-    {
-      // ---- MMA 1: [K; Q] K^T (the first chunk here; later chunks had it issued after the previous MMA 4)
-      if (it == 0 && tid == 0) {
-        fence_after();
-        issue_mma1(st);
-      }
-      __syncwarp();
-      {
-        const bool ok = mbar_wait(u32(&sm.bar_kq), kq_phase, err, 4);
-        kq_phase ^= 1;
-        fence_after();
-        if (__syncthreads_or(!ok)) {
-          failed = true;
-          break;
+    // ---- read-out: N (fp32, rows 0-63) and P (fp16, rows 64-127); each warp takes 16 columns
+    if (row < 64 || emit) {
+      const int c0 = wg * 16;
+      float v[16];
+      tmem_ld16(tm + tm_lane + TM_KQ + c0, v);
+      if (row < 64) {
+        float4 *dst = reinterpret_cast<float4 *>(&sm.nf[row * LN + c0]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        if (save_c) {  // N (fp16, row-major) straight from registers: 32 contiguous bytes per thread
+          uint8_t *nt = reinterpret_cast<uint8_t *>(static_cast<f16 *>(a.t64) +
+                                                    ((size_t)t64row + T64_N * CH + row) * CH + c0);
+          __half2 hv[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) hv[i] = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+          reinterpret_cast<uint4 *>(nt)[0] = *reinterpret_cast<const uint4 *>(hv);
+          reinterpret_cast<uint4 *>(nt)[1] = *reinterpret_cast<const uint4 *>(hv + 4);
         }
+      } else {
+        const int r = row - 64;
+        const float gr = G.gp[r];
+        float rg[16];
+        ld16f(G.rgp + c0, rg);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = c0 + i <= r ? v[i] * gr * rg[i] : 0.f;
+        st_chunk_f16(sm.p + chunk_off(r, c0), v);
+        st_chunk_f16(sm.p + chunk_off(r, c0 + 8), v + 8);
       }
+    }
+    fence_before();
+    fence_async_smem();  // P is an operand of MMA 4 and a context tile
+    named_bar_sync<2, FT>();
 
-      // ---- read-out: N (fp32, rows 0-63) and P (fp16, rows 64-127); each warp takes 16 columns
-      if (row < 64 || emit) {
-        const int c0 = wg * 16;
-        float v[16];
-        tmem_ld16(tm + tm_lane + TM_KQ + c0, v);
-        if (row < 64) {
-          float4 *dst = reinterpret_cast<float4 *>(&sm.nf[row * LN + c0]);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-          if (save_c) {  // N (fp16, row-major) straight from registers: 32 contiguous bytes per thread
-            uint8_t *nt = reinterpret_cast<uint8_t *>(static_cast<f16 *>(a.t64) +
-                                                      ((size_t)t64row + T64_N * CH + row) * CH + c0);
-            __half2 hv[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) hv[i] = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
-            reinterpret_cast<uint4 *>(nt)[0] = *reinterpret_cast<const uint4 *>(hv);
-            reinterpret_cast<uint4 *>(nt)[1] = *reinterpret_cast<const uint4 *>(hv + 4);
-          }
-        } else {
-          const int r = row - 64;
-          const float gr = G.gp[r];
-          float rg[16];
-          ld16f(G.rgp + c0, rg);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = c0 + i <= r ? v[i] * gr * rg[i] : 0.f;
-          st_chunk_f16(sm.p + chunk_off(r, c0), v);
-          st_chunk_f16(sm.p + chunk_off(r, c0 + 8), v + 8);
-        }
-      }
-      fence_before();
-      __syncthreads();
-
-      // ---- Ahat (fp32 diagonal blocks, TF32 tensor-core merges) -> X1, X2 (fp16, K-major: rows = r);
-      // a saved-context forward also stages Ahat, and stores the three tiles below
-      // (warps 0-7); meanwhile warps 8-15 copy S0 to its fp16 operand form and put gam_C * S0 back into
-      // TMEM (the copy is also the chunk-start state that the backward reads)
-      if (warp < 8) {
+    // ---- Ahat (fp32 diagonal blocks, TF32 tensor-core merges) -> X1, X2 (fp16, K-major: rows = r);
+    // a saved-context forward also stages Ahat for its store (warps 0-7); meanwhile warps 8-15 copy S0
+    // to its fp16 operand form and put gam_C * S0 back into TMEM (the copy is also the chunk-start state
+    // that the backward reads)
+    if (warp < 8) {
       wy_inverse<false, false, true>(sm.nf, LN, gbeta, sm.ys, [&](int r, int c, float a0, float a1) {
         const float2 bb = *reinterpret_cast<const float2 *>(gbeta + c), rg = *reinterpret_cast<const float2 *>(G.rgp + c);
         const float gr = G.gp[r], x0 = a0 * bb.x, x1 = a1 * bb.y;
@@ -403,80 +528,28 @@ __global__ void __launch_bounds__(FT, 1)
             __floats2half2_rn(c <= r ? x0 * (gr * rg.x) : 0.f, c + 1 <= r ? x1 * (gr * rg.y) : 0.f);
         if (save_wy) *reinterpret_cast<__half2 *>(sm.ah + off) = __floats2half2_rn(a0, a1);
       }, it == 0);
-      } else {
-        const float gC = G.gamC;
+    } else {
+      const float gC = G.gamC;
 #pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          const int c0 = (wg - 2) * 64 + half * 32;
-          float v[32];
-          tmem_ld32(tm + tm_lane + TM_S + c0, v);
-          const int kb = c0 >> 6;
+      for (int half = 0; half < 2; ++half) {
+        const int c0 = (wg - 2) * 64 + half * 32;
+        float v[32];
+        tmem_ld32(tm + tm_lane + TM_S + c0, v);
+        const int kb = c0 >> 6;
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) st_chunk_f16(sm.s0 + kb * 2 * HT + chunk_off(row, c0 + q4 * 8), v + q4 * 8);
+        for (int q4 = 0; q4 < 4; ++q4) st_chunk_f16(sm.s0 + kb * 2 * HT + chunk_off(row, c0 + q4 * 8), v + q4 * 8);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= gC;
-          tmem_st32(tm + tm_lane + TM_S + c0, v);
-        }
-        fence_async_smem();  // the fp16 state copy is an operand of MMA 3 and of Oi
+        for (int i = 0; i < 32; ++i) v[i] *= gC;
+        tmem_st32(tm + tm_lane + TM_S + c0, v);
       }
-      fence_before();
-      __syncthreads();
-      fence_after();
+      fence_async_smem();  // the fp16 state copy is an operand of MMA 3 and of Oi
     }
-
-    // ---- MMA 2: W^T = K^T X1^T, U^T = V^T X2^T  (M = 128, N = 64, K = 64)
-    if (tid == 0) {
-      fence_after();
-      if (save_c) {  // X1, X2, Ahat and P of this (chunk, head), and its K, Q, V operand tiles
-        tma_store_3d(&tmw, 0, t64row + T64_X1 * CH, 0, u32(sm.x1));
-        tma_store_3d(&tmw, 0, t64row + T64_X2 * CH, 0, u32(sm.x2));
-        tma_store_3d(&tmw, 0, t64row + T64_AH * CH, 0, u32(sm.ah));
-        tma_store_3d(&tmw, 0, t64row + T64_P * CH, 0, u32(sm.p));
-        const int qrow = ((chunk0 + c) * H + h) * TQ_TILES * CH;
-#pragma unroll
-        for (int hb = 0; hb < 2; ++hb) {
-          tma_store_3d(&tm3, 64 * hb, qrow + TQ_K * CH, 0, u32(st + 2 * hb * HT));
-          tma_store_3d(&tm3, 64 * hb, qrow + TQ_Q * CH, 0, u32(st + (2 * hb + 1) * HT));
-          tma_store_3d(&tm3, 64 * hb, qrow + TQ_V * CH, 0, u32(st + (4 + hb) * HT));
-        }
-        tma_store_commit();
-      }
-      const uint32_t idesc = idesc_f16(128, 64, true, false);
-      const uint32_t kb = u32(st), vb = u32(st + 4 * HT);
-      const uint32_t x1b = u32(sm.x1), x2b = u32(sm.x2);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        mma_f16(tm + TM_W, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(x1b + kk * 32, 16, 1024), idesc, kk > 0);
-      }
-      if (need_v) {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_f16(tm + TM_U, sdesc(vb + kk * 2048, HT, 1024), sdesc(x2b + kk * 32, 16, 1024), idesc, kk > 0);
-      }
-      mma_commit(u32(&sm.bar_mma));
-    }
-    __syncwarp();
-    if (__syncthreads_or(!mma_wait())) {
+    fence_before();
+    if (__syncthreads_or(failed)) {  // A3: the producer stores the context tiles, issues MMA 2 and Oi
       failed = true;
       break;
     }
-    if (tid == 0 && save_states && c >= cbeg) {  // the fp16 chunk-start state, two 64-column blocks
-      const int srow = ((chunk0 + c) * H + h) * D;
-      tma_store_3d(&tms, 0, srow, 0, u32(sm.s0));
-      tma_store_3d(&tms, 64, srow, 0, u32(sm.s0 + 2 * HT));
-      tma_store_commit();
-    }
-    // Oi^T = S0 Q^T needs only the state copy and Q: issued now, it runs under the W^T read-out
-    // (MMA 3's commit covers it)
-    if (emit_o && tid == 0) {
-      const uint32_t s0b = u32(sm.s0), qb = u32(st + HT);
-      const uint32_t id_o = idesc_f16(128, 64, false, false);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
-        mma_f16(tm + TM_O, sdesc(s0b + aoff, 16, 1024), sdesc(qb + aoff, 16, 1024), id_o, kk > 0);
-      }
-    }
+    failed |= !mma_wait();
 
     // ---- W^T read-out: columns scaled by gam -> fp16 MN-major B (rows = d_k)
     {
@@ -492,29 +565,10 @@ __global__ void __launch_bounds__(FT, 1)
     }
     fence_before();
     fence_async_smem();
-    __syncthreads();
-
-    // ---- MMA 3: Ut^T = U^T - S0 W^T   (M = 128, N = 64, K = 128)
-    if (tid == 0) {
-      fence_after();
-      if (save_c) {  // the gam-scaled W^T tile
-        tma_store_3d(&tmt, 0, t128row + T128_W * D, 0, u32(sm.wu));
-        tma_store_commit();
-      }
-      const uint32_t s0b = u32(sm.s0), wb = u32(sm.wu);
-      const uint32_t id_u = idesc_f16(128, 64, false, true, /*neg_a=*/true);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
-        mma_f16(tm + TM_U, sdesc(s0b + aoff, 16, 1024), sdesc(wb + kk * 2048, 2 * HT, 1024), id_u,
-                need_v || kk > 0);
-      }
-      mma_commit(u32(&sm.bar_mma));
+    if (__syncthreads_or(failed)) {  // A4: the producer stores W^T and issues MMA 3
+      failed = true;
+      break;
     }
-    __syncwarp();
-    const bool more = c + 1 < cend;
-    const int nvn = more ? min(CH, len - (c + 1) * CH) : 0;
-    uint8_t *stn = sm.ring[stage ^ 1];
     bool next_ok = true;
     if (more) {  // the next chunk's tiles (issued at the top of this iteration), normalised while MMA 3 runs
       next_ok = mbar_wait(u32(&sm.bar_tma[stage ^ 1]), ((it + 1) >> 1) & 1, err, 8);
@@ -522,14 +576,8 @@ __global__ void __launch_bounds__(FT, 1)
         prep_kq(stn, nvn, outputs && c + 1 >= cbeg,
                 save_wy && outputs && c + 1 >= cbeg ? a.nrm + ((size_t)(chunk0 + c + 1) * H + h) * 2 * CH : nullptr);
     }
-    {
-      if (tid == 0 && save_c) tma_store_wait_read();  // the W^T store has read wu (Ut^T is written next)
-      const bool mok = mma_wait();
-      if (__syncthreads_or(!mok || !next_ok)) {
-        failed = true;
-        break;
-      }
-    }
+    failed |= !mma_wait();
+    named_bar_sync<3, FT + 32>();  // the W^T store has read wu
 
     // ---- Ut^T read-out -> fp16 K-major A (rows = d_v, k = token), and Ut^T diag(cdec)
     {
@@ -547,46 +595,21 @@ __global__ void __launch_bounds__(FT, 1)
     }
     fence_before();
     fence_async_smem();
-    __syncthreads();
-
-    // ---- MMA 4: S += (Ut^T diag(cdec)) K (N = 128, K = 64);  Oa^T = Ut^T P^T (N = 64, K = 64)
-    if (tid == 0) {
-      fence_after();
-      if (save_c) {  // the Ut^T tile
-        tma_store_3d(&tmt, 0, t128row + T128_U * D, 0, u32(sm.wu));
-        tma_store_commit();
-      }
-      const uint32_t ucb = u32(sm.uc), ub = u32(sm.wu), kb = u32(st), pb = u32(sm.p);
-      const uint32_t id_s = idesc_f16(128, 128, false, true);
-      const uint32_t id_o = idesc_f16(128, 64, false, false);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_f16(tm + TM_S, sdesc(ucb + kk * 32, 16, 1024), sdesc(kb + kk * 2048, 2 * HT, 1024), id_s, true);
-      if (emit_o) {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_f16(tm + TM_OA, sdesc(ub + kk * 32, 16, 1024), sdesc(pb + kk * 32, 16, 1024), id_o, kk > 0);
-      }
-      mma_commit(u32(&sm.bar_mma));
-      // the next chunk's Gram product: its K, Q were normalised while MMA 3 ran; it runs during this
-      // chunk's O read-out
-      if (more) issue_mma1(stn);
+    if (__syncthreads_or(failed || !next_ok)) {  // A5: the producer stores Ut^T, issues MMA 4 and the next MMA 1
+      failed = true;
+      break;
     }
-    __syncwarp();
     if (more && need_v) prep_v(stn, nvn);  // the next chunk's V, while MMA 4 runs
     fence_async_smem();
-    if (warp == 0 && c + 1 < cend) {  // gates of the next chunk, overlapping MMA 4
+    if (warp == 0 && more) {  // gates of the next chunk, overlapping MMA 4
       float *gn = sm.g[stage ^ 1];
       gn[lane] = gnext0;
       gn[lane + 32] = gnext1;
       __syncwarp();
       if (gate_prefix(gn, sm.gt[stage ^ 1]) && lane == 0 && err) atomicOr(err, 1);
     }
-    if (tid == 0 && save_c && emit_o) tma_store_wait_read();  // the Ut^T store has read wu (O staging)
-    if (__syncthreads_or(!mma_wait())) {
-      failed = true;
-      break;
-    }
+    failed |= !mma_wait();
+    named_bar_sync<3, FT + 32>();  // the Ut^T store has read wu
 
     // ---- O^T = Oi^T diag(gam) + Oa^T -> bf16 [token][d_v] staging in wu (free now) -> coalesced rows of o
     if (emit_o) {
@@ -600,7 +623,7 @@ __global__ void __launch_bounds__(FT, 1)
       for (int i = 0; i < 16; ++i) stg[(c0 + i) * D + row] = __float2bfloat16_rn(fmaf(v[i], gm[i], va[i]));
     }
     fence_before();
-    __syncthreads();
+    named_bar_sync<2, FT>();
     if (emit_o) {
       const uint4 *stg = reinterpret_cast<const uint4 *>(sm.wu);
       bf16 *og = static_cast<bf16 *>(a.o);
@@ -612,7 +635,7 @@ __global__ void __launch_bounds__(FT, 1)
   }
 
   // ---------------------------------------------------------------- end-of-segment state
-  if (!failed) {
+  if (!failed && warp < FWARPS) {
     float *dst = nullptr;
     if (a.pass == 0) dst = (transition ? a.Mbuf : a.Ebuf) + sh_idx * DD;
     else if (j == nseg - 1 && a.ST) dst = a.ST + ((size_t)n * H + h) * DD;
@@ -628,7 +651,7 @@ __global__ void __launch_bounds__(FT, 1)
       }
     }
   }
-  if (tid == 0 && (save_states || save_wy)) tma_store_wait_all();
+  if (tid == FT && (save_states || save_wy)) tma_store_wait_all();
   fence_before();
   __syncthreads();
   fence_after();
@@ -644,7 +667,7 @@ int launch_fwd_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk
   static_assert(sizeof(TcSmem) + 1024 <= 232448 - 256, "shared memory budget (the rest: static shared memory)");
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  return (int)launch_pdl(fwd_tc_kernel, grid, dim3(FT), smem, st, a, tq, tk, tv, tw, ts, tt, t3);
+  return (int)launch_pdl(fwd_tc_kernel, grid, dim3(FT + 32), smem, st, a, tq, tk, tv, tw, ts, tt, t3);
 }
 
 }  // namespace gdn

@@ -181,6 +181,16 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(mbar) : "memory");
 }
+// Named barriers over part of a CTA (ID and thread count are compile-time: a multiple of 32).  sync
+// waits for `N` arrivals; arrive counts the calling warp without waiting.
+template <int ID, int N>
+__device__ __forceinline__ void named_bar_sync() {
+  asm volatile("bar.sync %0, %1;\n" ::"n"(ID), "n"(N) : "memory");
+}
+template <int ID, int N>
+__device__ __forceinline__ void named_bar_arrive() {
+  asm volatile("bar.arrive %0, %1;\n" ::"n"(ID), "n"(N) : "memory");
+}
 // Wait for the phase with the given parity to complete.  Bounded: after
 // `limit` polls it records `code` in *err and returns false (never hangs).
 __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, int *err, int code,
