@@ -81,9 +81,9 @@ def job_throughput(total_ms, world, tokens_per_rank_step, steps):
 # keyed by (profiler name, workload); valid only while the kernel's sources hash to the value
 # recorded with it (otherwise the roofline reports traffic null).  Summaries: profiles/*.md.
 NCU_TRAFFIC = {
-    ("bwd_local", "prefill_h32_t8192"): (960643072, "bwd_local_tc.cu", "6f77f7ee6a7a214a"),
-    ("fwd_chunk", "prefill_h32_t8192"): (873353728, "fwd_tc.cu", "213089fbec043ad7"),
-    ("bwd_chain", "prefill_h32_t8192"): (445828864, "bwd_chain_tc.cu", "0ce3c5c70a712b8a"),
+    ("bwd_local", "prefill_h32_t8192"): (959723520, "bwd_local_tc.cu", "669bdc4b65a59ee3"),
+    ("fwd_chunk", "prefill_h32_t8192"): (877718272, "fwd_tc.cu", "c237066f7b067b4a"),
+    ("bwd_chain", "prefill_h32_t8192"): (444913664, "bwd_chain_tc.cu", "6f1080fba9ae1a58"),
 }
 KERNEL_COMMON = ["chunk_common.cuh", "umma.cuh", "common.cuh", "kernels.h"]
 
