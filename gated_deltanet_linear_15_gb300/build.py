@@ -15,7 +15,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libgdn.so")
-SOURCES = ["api.cu", "plan.cu", "fwd.cu", "fwd_tc.cu", "bwd.cu", "bwd_chain_tc.cu", "bwd_local_tc.cu", "recurrent.cu"]
+SOURCES = ["api.cu", "plan.cu", "fwd.cu", "fwd_prep_tc.cu", "fwd_tc.cu", "bwd.cu", "bwd_chain_tc.cu", "bwd_local_tc.cu",
+           "recurrent.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
 

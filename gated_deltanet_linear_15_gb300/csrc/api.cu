@@ -62,7 +62,8 @@ struct Layout {
   size_t bwd_saved_total = 0;               // backward workspace when the forward saved its context
   size_t saved_off_t64 = 0, saved_off_t128 = 0, saved_off_tqkv = 0, saved_off_nrm = 0;
   size_t saved_total = 0;  // saved context: [states][t64][t128][tqkv][nrm]
-  size_t fwd_total = 0, bwd_total = 0;
+  size_t off_fctx_t64 = 0, off_fctx_tqkv = 0;  // the plain forward's chunk context (bf16, d = 128)
+  size_t fwd_core = 0, fwd_total = 0, bwd_total = 0;
 };
 
 // Chunks per segment.  One CTA per (segment, head) runs a serial chain over its
@@ -144,10 +145,22 @@ int make_layout(const gdn_shape *s, Layout &L) {
   off += spbuf;
   L.off_S = off;
   off += spbuf;
+  L.fwd_core = off;
+  const bool tiles = s->dtype == GDN_BF16 && L.D == 128;
+  L.t64_bytes = tiles ? align256((size_t)L.CH_max * L.H * T64_TILES * CH * CH * 2) : 0;
+  L.t128_bytes = tiles ? align256((size_t)L.CH_max * L.H * T128_TILES * 128 * CH * 2) : 0;
+  L.tqkv_bytes = tiles ? align256((size_t)L.CH_max * L.H * TQ_TILES * CH * 128 * 2) : 0;
+  L.nrm_bytes = tiles ? align256((size_t)L.CH_max * L.H * 2 * CH * 4) : 0;
+  // a forward that saves no context still passes the chunk-local half's tiles to the recurrent half
+  L.off_fctx_t64 = off;
+  off += L.t64_bytes;
+  L.off_fctx_tqkv = off;
+  off += L.tqkv_bytes;
   L.fwd_total = off;
-  // backward: the reverse-chain buffers first, then the per-chunk states and WY tiles that the
-  // backward recomputes unless the forward saved them (a saved-context backward needs only the
-  // prefix up to bwd_saved_total)
+  // backward (its own call: it reuses the forward-only context region): the reverse-chain buffers
+  // first, then the per-chunk states and context tiles that the backward recomputes unless the
+  // forward saved them (a saved-context backward needs only the prefix up to bwd_saved_total)
+  off = L.fwd_core;
   L.states_bytes = align256((size_t)L.CH_max * L.H * DD * L.esize);
   L.off_dstates = off;
   off += L.states_bytes;
@@ -160,15 +173,10 @@ int make_layout(const gdn_shape *s, Layout &L) {
   L.bwd_saved_total = off;
   L.off_states = off;
   off += L.states_bytes;
-  const bool tiles = s->dtype == GDN_BF16 && L.D == 128;
-  L.t64_bytes = tiles ? align256((size_t)L.CH_max * L.H * T64_TILES * CH * CH * 2) : 0;
-  L.t128_bytes = tiles ? align256((size_t)L.CH_max * L.H * T128_TILES * 128 * CH * 2) : 0;
   L.off_t64 = off;
   off += L.t64_bytes;
   L.off_t128 = off;
   off += L.t128_bytes;
-  L.tqkv_bytes = tiles ? align256((size_t)L.CH_max * L.H * TQ_TILES * CH * 128 * 2) : 0;
-  L.nrm_bytes = tiles ? align256((size_t)L.CH_max * L.H * 2 * CH * 4) : 0;
   L.off_tqkv = off;
   off += L.tqkv_bytes;
   L.off_nrm = off;
@@ -367,34 +375,42 @@ int tqkv_map(CUtensorMap *m, const Layout &L, const void *ptr) {
   return tile_map(m, ptr, (long)L.CH_max * L.H * TQ_TILES * CH, 64, 128);
 }
 
-// The chunk forward kernel for this problem: tcgen05 for bf16 with d = 128, the
-// mma.sync/CUDA-core kernel otherwise (d = 64, fp32 inputs, empty batches).
+// The chunk forward kernel for this problem: tcgen05 for bf16 with d = 128 (its recurrent half, on the
+// context that the chunk-local half stored), the mma.sync/CUDA-core kernel otherwise (d = 64, fp32
+// inputs, empty batches).
+bool tc_forward(const Layout &L, const gdn_shape *s) { return s->dtype == GDN_BF16 && L.D == 128 && L.Ttot > 0; }
+
 int launch_forward_kernel(const Layout &L, const gdn_shape *s, const FwdArgs &fa, dim3 grid, cudaStream_t st) {
-  const bool bf = s->dtype == GDN_BF16;
-  if (bf && L.D == 128 && L.Ttot > 0) {
-    CUtensorMap tq, tk, tv, tw, ts, tt, t3;
+  if (tc_forward(L, s)) {
+    CUtensorMap t3, tw, ts, tt;
     int rc;
-    if ((rc = qkv_map(&tk, fa.k, L.Ttot, L.H))) return rc;
-    if ((rc = qkv_map(&tv, fa.v, L.Ttot, L.H))) return rc;
-    if ((rc = qkv_map(&tq, fa.q ? fa.q : fa.k, L.Ttot, L.H))) return rc;
-    // context tiles and chunk-start states written for the backward (maps unused when not saving)
-    if (fa.t64) {
-      if ((rc = t64_map(&tw, L, fa.t64)) || (rc = t128_map(&tt, L, fa.t128)) || (rc = tqkv_map(&t3, L, fa.tqkv)))
-        return rc;
-    } else if ((rc = tile_map(&tw, fa.k, 64, 64)) || (rc = tile_map(&tt, fa.k, 128, 128)) ||
-               (rc = tile_map(&t3, fa.k, 64, 64, 128))) {
-      return rc;
-    }
+    if ((rc = tqkv_map(&t3, L, fa.tqkv)) || (rc = t64_map(&tw, L, fa.t64))) return rc;
+    // the chunk-start states and W^T, Ut^T tiles written for the backward (maps unused when not saving)
+    if ((rc = t128_map(&tt, L, fa.t128 ? fa.t128 : fa.t64))) return rc;
     if ((rc = state_map(&ts, fa.states ? fa.states : fa.k, fa.states ? (long)L.CH_max * L.H * 128 : 128)))
       return rc;
-    return launch_fwd_tc(fa, tq, tk, tv, tw, ts, tt, t3, grid, st);
+    return launch_fwd_tc(fa, t3, tw, ts, tt, grid, st);
   }
-  return launch_fwd_chunk(fa, bf, L.D, grid, st);
+  return launch_fwd_chunk(fa, s->dtype == GDN_BF16, L.D, grid, st);
+}
+
+// The chunk-local half of the tcgen05 forward: operand tiles, N, P, X1, X2 (and, when the context is
+// kept, Ahat and the norms) of every (chunk, head).
+int launch_forward_prep(const Layout &L, const FwdArgs &fa, cudaStream_t st) {
+  CUtensorMap tq, tk, tv, tw, t3;
+  int rc;
+  if ((rc = qkv_map(&tk, fa.k, L.Ttot, L.H)) || (rc = qkv_map(&tv, fa.v, L.Ttot, L.H)) ||
+      (rc = qkv_map(&tq, fa.q, L.Ttot, L.H)) || (rc = t64_map(&tw, L, fa.t64)) || (rc = tqkv_map(&t3, L, fa.tqkv)))
+    return rc;
+  return launch_fwd_prep_tc(fa, tq, tk, tv, tw, t3, L.CH_max, st);
 }
 
 // Forward state pass: pass A + fix-up when segments exist, then `pass` (1: outputs, 2: states).
 int forward_passes(const gdn_shape *s, const Layout &L, char *ws, FwdArgs fa, int pass, cudaStream_t st) {
-  const bool bf = s->dtype == GDN_BF16;
+  if (tc_forward(L, s)) {
+    PROF("fwd_prep");
+    CK(launch_forward_prep(L, fa, st));
+  }
   if (L.sp) {
     fa.pass = 0;
     {
@@ -482,6 +498,9 @@ int fwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
       fa.tqkv = static_cast<char *>(saved) + L.saved_off_tqkv;
       fa.nrm = reinterpret_cast<float *>(static_cast<char *>(saved) + L.saved_off_nrm);
     }
+  } else if (L.t64_bytes > 0) {  // the two halves of the tcgen05 forward meet in the workspace
+    fa.t64 = ws + L.off_fctx_t64;
+    fa.tqkv = ws + L.off_fctx_tqkv;
   }
   return forward_passes(s, L, ws, fa, 1, st);
 }

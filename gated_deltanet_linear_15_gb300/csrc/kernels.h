@@ -27,8 +27,10 @@ struct FwdArgs {
   float scale;
   unsigned flags;
   int pass;  // 0: segment end states / transitions, 1: outputs (+ saves if set), 2: states only
-  // pass 1, bf16 with d = 128: the chunk context for the backward (all set, or all NULL), see T64_*,
-  // T128_*, TQ_*; with o == NULL the pass writes no output and only produces states and context
+  // bf16 with d = 128: the chunk context, see T64_*, T128_*, TQ_*.  t64 and tqkv are always set: the
+  // chunk-local half writes them and the recurrent half reads them.  t128 and nrm are set when the
+  // context is kept for the backward (then the chunk-local half also writes Ahat, N and the norms, and
+  // pass 1 the W^T, Ut^T tiles); with o == NULL pass 1 writes no output and only states and context
   void *t64, *t128, *tqkv;
   float *nrm;
 };
@@ -91,12 +93,15 @@ int launch_gate_scan(const Plan &p, const float *g, int H, int CH_max, float *gs
 int launch_fixup(const FixupArgs &a, int N, cudaStream_t st);
 
 int launch_fwd_chunk(const FwdArgs &a, bool is_bf16, int D, dim3 grid, cudaStream_t st);
-// tcgen05 forward for bf16 inputs and d = 128; q, k, v tensor maps over [tokens, H, 128] with a 64 x 1 x 64 box;
-// stores: t64 tiles ([rows, 64] fp16, box 64 x 64), chunk-start states ([rows, 128] fp16, box 64 x 128), t128
-// tiles ([rows, 64] fp16, box 64 x 128)
-int launch_fwd_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                  const CUtensorMap &t64, const CUtensorMap &ts, const CUtensorMap &t128, const CUtensorMap &tqkv,
-                  dim3 grid, cudaStream_t st);
+// tcgen05 forward for bf16 inputs and d = 128, chunk-local half: one CTA per (chunk, head) over CH_max x H;
+// maps: q, k, v over [tokens, H, 128] bf16 (box 64 x 1 x 64), the t64 tiles ([rows, 64] fp16, box 64 x 64)
+// and the tqkv tiles ([rows, 128] fp16, box 64 x 64)
+int launch_fwd_prep_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const CUtensorMap &t64, const CUtensorMap &tqkv, int CH_max, cudaStream_t st);
+// tcgen05 forward, recurrent half: one CTA per (segment, head); reads the tqkv and t64 tiles, stores the
+// chunk-start states ([rows, 128] fp16, box 64 x 128) and the t128 tiles ([rows, 64] fp16, box 64 x 128)
+int launch_fwd_tc(const FwdArgs &a, const CUtensorMap &tqkv, const CUtensorMap &t64, const CUtensorMap &ts,
+                  const CUtensorMap &t128, dim3 grid, cudaStream_t st);
 int launch_bwd_chain(const BwdArgs &a, bool is_bf16, int D, dim3 grid, cudaStream_t st);
 // tcgen05 reverse chain (bf16, d = 128); maps: the tqkv context ([rows, 128] fp16, box 64x64), dO
 // ([tokens, H, 128] bf16, box 64x1x64), the t64 and t128 context tiles, and the per-chunk dS store
