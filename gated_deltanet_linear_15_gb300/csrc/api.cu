@@ -382,14 +382,15 @@ bool tc_forward(const Layout &L, const gdn_shape *s) { return s->dtype == GDN_BF
 
 int launch_forward_kernel(const Layout &L, const gdn_shape *s, const FwdArgs &fa, dim3 grid, cudaStream_t st) {
   if (tc_forward(L, s)) {
-    CUtensorMap t3, tw, ts, tt;
+    CUtensorMap t3, tw, ts, tt, to;
     int rc;
     if ((rc = tqkv_map(&t3, L, fa.tqkv)) || (rc = t64_map(&tw, L, fa.t64))) return rc;
+    if ((rc = qkv_map(&to, fa.o ? fa.o : fa.k, L.Ttot, L.H))) return rc;  // unused without an output
     // the chunk-start states and W^T, Ut^T tiles written for the backward (maps unused when not saving)
     if ((rc = t128_map(&tt, L, fa.t128 ? fa.t128 : fa.t64))) return rc;
     if ((rc = state_map(&ts, fa.states ? fa.states : fa.k, fa.states ? (long)L.CH_max * L.H * 128 : 128)))
       return rc;
-    return launch_fwd_tc(fa, t3, tw, ts, tt, grid, st);
+    return launch_fwd_tc(fa, t3, tw, ts, tt, to, grid, st);
   }
   return launch_fwd_chunk(fa, s->dtype == GDN_BF16, L.D, grid, st);
 }

@@ -51,7 +51,10 @@ struct __align__(1024) TcSmem {
   float g[2][CH];      // per ring stage
   Gates gt[2];         // per ring stage; the next chunk's gates are computed during this chunk
   uint64_t bar_tma[2];
-  uint64_t bar_mma;
+  // tensor-core commits: MMA 3 and MMA 4 on bar_mma, MMA 2 on its own barrier (it is issued for the next
+  // chunk right after MMA 4, so both could complete before the workers wait: a parity wait on one
+  // barrier cannot tell two completed phases from none)
+  uint64_t bar_mma, bar_mma2;
   uint32_t tmem_base;
 };
 
@@ -72,7 +75,8 @@ __device__ __forceinline__ uint32_t chunk_off(int r, int cb) { return r * 128 + 
 
 __global__ void __launch_bounds__(FT + 32, 1)
     fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tm3, const __grid_constant__ CUtensorMap tmw,
-                  const __grid_constant__ CUtensorMap tms, const __grid_constant__ CUtensorMap tmt) {
+                  const __grid_constant__ CUtensorMap tms, const __grid_constant__ CUtensorMap tmt,
+                  const __grid_constant__ CUtensorMap tmo) {
   extern __shared__ unsigned char smraw[];
   TcSmem &sm = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
   pdl_trigger();
@@ -129,11 +133,13 @@ __global__ void __launch_bounds__(FT + 32, 1)
     mbar_init(u32(&sm.bar_tma[0]), 1);
     mbar_init(u32(&sm.bar_tma[1]), 1);
     mbar_init(u32(&sm.bar_mma), 1);
+    mbar_init(u32(&sm.bar_mma2), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     tma_prefetch_desc(&tm3);
     tma_prefetch_desc(&tmw);
     if (save_wy) tma_prefetch_desc(&tmt);
     if (save_states) tma_prefetch_desc(&tms);
+    if (want_o) tma_prefetch_desc(&tmo);
   }
   if (warp == 0) {
     tmem_alloc(u32(&sm.tmem_base), TM_COLS);
@@ -168,6 +174,22 @@ __global__ void __launch_bounds__(FT + 32, 1)
       tma_load_3d(u32(st + R_X2 * HT), &tmw, 0, t64row + T64_X2 * CH, 0, bar);
     }
   };
+  // MMA 2: W^T = K^T X1^T, U^T = V^T X2^T  (M = 128, N = 64, K = 64) of the chunk in ring stage `st`: needs
+  // no state, so it is issued as soon as the tiles are in and the previous chunk has read TM_W, TM_U
+  auto issue_mma2 = [&](const uint8_t *st) {
+    const uint32_t idesc = idesc_f16(128, 64, true, false);
+    const uint32_t kb = u32(st + R_K * HT), vb = u32(st + R_V * HT);
+    const uint32_t x1b = u32(st + R_X1 * HT), x2b = u32(st + R_X2 * HT);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_f16(tm + TM_W, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(x1b + kk * 32, 16, 1024), idesc, kk > 0);
+    if (need_v) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_f16(tm + TM_U, sdesc(vb + kk * 2048, HT, 1024), sdesc(x2b + kk * 32, 16, 1024), idesc, kk > 0);
+    }
+    mma_commit(u32(&sm.bar_mma2));
+  };
   auto issue_g = [&](int c, int stage) {  // cp.async of the log-gates of chunk c
     const int tok0 = bos + c * CH;
     const int nvalid = min(CH, len - c * CH);
@@ -200,7 +222,7 @@ __global__ void __launch_bounds__(FT + 32, 1)
   fence_after();
 
   int *err = a.status;
-  uint32_t mma_phase = 0;
+  uint32_t mma_phase = 0, mma2_phase = 0;
   bool failed = false;
   auto mma_wait = [&]() {
     const bool ok = mbar_wait(u32(&sm.bar_mma), mma_phase, err, 4);
@@ -209,7 +231,7 @@ __global__ void __launch_bounds__(FT + 32, 1)
     return ok;
   };
 
-  // Workers and producer meet at CTA-wide OR-barriers (A1, A3, A4) that also carry a failed wait; the
+  // Workers and producer meet at CTA-wide OR-barriers (A1, A3, A4, A5) that also carry a failed wait; the
   // workers sync among themselves on barrier 2, and the producer tells them that a context store has
   // read wu (barrier 3, arrive / sync).
   const bool producer = warp == FWARPS;
@@ -230,28 +252,16 @@ __global__ void __launch_bounds__(FT + 32, 1)
     if (producer) {
       // ================================================================ producer
       // the previous chunk's stores have read s0 / wu (rewritten below)
-      if (lane == 0 && (save_states || save_wy)) tma_store_wait_read();
+      if (lane == 0 && (save_states || save_wy || want_o)) tma_store_wait_read();
       __syncwarp();
       if (__syncthreads_or(false)) {  // A1: this chunk's tiles have landed; the previous chunk is done
         failed = true;
         break;
       }
       if (lane == 0) {
-        if (more) issue_tma(c + 1, stage ^ 1);  // its stage's last readers (the previous MMA 4) are done
         fence_after();
-        // ---- MMA 2: W^T = K^T X1^T, U^T = V^T X2^T  (M = 128, N = 64, K = 64): needs no state
-        const uint32_t idesc = idesc_f16(128, 64, true, false);
-        const uint32_t kb = u32(st + R_K * HT), vb = u32(st + R_V * HT);
-        const uint32_t x1b = u32(st + R_X1 * HT), x2b = u32(st + R_X2 * HT);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_f16(tm + TM_W, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(x1b + kk * 32, 16, 1024), idesc, kk > 0);
-        if (need_v) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f16(tm + TM_U, sdesc(vb + kk * 2048, HT, 1024), sdesc(x2b + kk * 32, 16, 1024), idesc, kk > 0);
-        }
-        mma_commit(u32(&sm.bar_mma));
+        if (it == 0) issue_mma2(st);  // later chunks: issued at the previous chunk's A4
+        if (more) issue_tma(c + 1, stage ^ 1);  // its stage's last readers (the previous MMA 4) are done
       }
       __syncwarp();
       if (__syncthreads_or(false)) {  // A3: the fp16 state copy and the gam-scaled W^T are in shared memory
@@ -260,13 +270,10 @@ __global__ void __launch_bounds__(FT + 32, 1)
       }
       if (lane == 0) {
         fence_after();
-        if (save_states && c >= cbeg) {  // the fp16 chunk-start state, two 64-column blocks
-          const int srow = ((chunk0 + c) * H + h) * D;
-          tma_store_3d(&tms, 0, srow, 0, u32(sm.s0));
-          tma_store_3d(&tms, 64, srow, 0, u32(sm.s0 + 2 * HT));
+        if (save_c) {  // the gam-scaled W^T
+          tma_store_3d(&tmt, 0, t128row + T128_W * D, 0, u32(sm.wu));
+          tma_store_commit();
         }
-        if (save_c) tma_store_3d(&tmt, 0, t128row + T128_W * D, 0, u32(sm.wu));  // the gam-scaled W^T
-        if ((save_states && c >= cbeg) || save_c) tma_store_commit();
         // ---- MMA 3: Ut^T = U^T - S0 W^T   (M = 128, N = 64, K = 128)
         const uint32_t s0b = u32(sm.s0), wb = u32(sm.wu);
         const uint32_t id_u = idesc_f16(128, 64, false, true, /*neg_a=*/true);
@@ -277,9 +284,20 @@ __global__ void __launch_bounds__(FT + 32, 1)
                   need_v || kk > 0);
         }
         mma_commit(u32(&sm.bar_mma));
+        if (save_c) tma_store_wait_read();  // the W^T store has read wu (Ut^T is written next)
+      }
+      __syncwarp();
+      named_bar_arrive<3, FT + 32>();
+      if (lane == 0) {
+        if (save_states && c >= cbeg) {  // the fp16 chunk-start state, two 64-column blocks
+          const int srow = ((chunk0 + c) * H + h) * D;
+          tma_store_3d(&tms, 0, srow, 0, u32(sm.s0));
+          tma_store_3d(&tms, 64, srow, 0, u32(sm.s0 + 2 * HT));
+          tma_store_commit();
+        }
         // Oi^T = S0 Q^T: read at the O read-out, after MMA 4's commit
         if (emit_o) {
-          const uint32_t qb = u32(st + R_Q * HT);
+          const uint32_t s0b = u32(sm.s0), qb = u32(st + R_Q * HT);
           const uint32_t id_o = idesc_f16(128, 64, false, false);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
@@ -287,10 +305,8 @@ __global__ void __launch_bounds__(FT + 32, 1)
             mma_f16(tm + TM_O, sdesc(s0b + aoff, 16, 1024), sdesc(qb + aoff, 16, 1024), id_o, kk > 0);
           }
         }
-        if (save_c) tma_store_wait_read();  // the W^T store has read wu (Ut^T is written next)
       }
       __syncwarp();
-      named_bar_arrive<3, FT + 32>();
       if (__syncthreads_or(false)) {  // A4: Ut^T and Ut^T diag(cdec) are in shared memory
         failed = true;
         break;
@@ -318,6 +334,22 @@ __global__ void __launch_bounds__(FT + 32, 1)
       }
       __syncwarp();
       named_bar_arrive<3, FT + 32>();
+      // MMA 2 of the next chunk once its tiles are in: TM_W and TM_U were read before A3 and A4
+      if (lane == 0 && more && mbar_wait(u32(&sm.bar_tma[stage ^ 1]), ((it + 1) >> 1) & 1, err, 8)) {
+        fence_after();
+        issue_mma2(sm.ring[stage ^ 1]);
+      }
+      __syncwarp();
+      if (__syncthreads_or(false)) {  // A5: the O tile is staged
+        failed = true;
+        break;
+      }
+      if (lane == 0 && emit_o && nvalid == CH) {  // a full chunk of o by two TMA stores
+        tma_store_3d(&tmo, 0, h, tok0, u32(sm.wu));
+        tma_store_3d(&tmo, 64, h, tok0, u32(sm.wu + HT));
+        tma_store_commit();
+      }
+      __syncwarp();
       continue;
     }
 
@@ -352,7 +384,11 @@ __global__ void __launch_bounds__(FT + 32, 1)
       for (int i = 0; i < 32; ++i) v[i] *= gC;
       tmem_st32(tm + tm_lane + TM_S + c0, v);
     }
-    failed |= !mma_wait();  // MMA 2
+    {  // MMA 2 (its own barrier, one completion per chunk)
+      failed |= !mbar_wait(u32(&sm.bar_mma2), mma2_phase, err, 4);
+      mma2_phase ^= 1;
+      fence_after();
+    }
 
     // ---- W^T read-out: columns scaled by gam -> fp16 MN-major B (rows = d_k)
     {
@@ -405,25 +441,32 @@ __global__ void __launch_bounds__(FT + 32, 1)
     failed |= !mma_wait();  // MMA 4
     named_bar_sync<3, FT + 32>();  // the Ut^T store has read wu
 
-    // ---- O^T = Oi^T diag(gam) + Oa^T -> bf16 [token][d_v] staging in wu -> coalesced rows of o
+    // ---- O^T = Oi^T diag(gam) + Oa^T -> bf16 staging in wu (two swizzled [64 token][64 feature] halves) ->
+    // o by TMA (a full chunk, the producer) or coalesced rows (a partial one)
     if (emit_o) {
-      bf16 *stg = reinterpret_cast<bf16 *>(sm.wu);
       const int c0 = wg * 16;
       float v[16], va[16];
       tmem_ld16x2(tm + tm_lane + TM_O + c0, v, tm + tm_lane + TM_OA + c0, va);
       float gm[16];
       ld16f(G.gam + c0, gm);
+      uint8_t *stg = sm.wu + (row >> 6) * HT;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) stg[(c0 + i) * D + row] = __float2bfloat16_rn(fmaf(v[i], gm[i], va[i]));
+      for (int i = 0; i < 16; ++i)
+        *reinterpret_cast<bf16 *>(stg + sw128_offset(c0 + i, row & 63)) = __float2bfloat16_rn(fmaf(v[i], gm[i], va[i]));
     }
     fence_before();
-    named_bar_sync<2, FT>();
-    if (emit_o) {
-      const uint4 *stg = reinterpret_cast<const uint4 *>(sm.wu);
+    fence_async_smem();
+    if (__syncthreads_or(failed)) {  // A5: the producer stores a full chunk of o
+      failed = true;
+      break;
+    }
+    if (emit_o && nvalid < CH) {
       bf16 *og = static_cast<bf16 *>(a.o);
       for (int e = tid; e < CH * (D / 8); e += FT) {
         const int r = e >> 4, cc = e & 15;
-        if (r < nvalid) *reinterpret_cast<uint4 *>(og + ((size_t)(tok0 + r) * H + h) * D + cc * 8) = stg[e];
+        if (r < nvalid)
+          *reinterpret_cast<uint4 *>(og + ((size_t)(tok0 + r) * H + h) * D + cc * 8) =
+              *reinterpret_cast<const uint4 *>(sm.wu + (cc >> 3) * HT + r * 128 + (((cc & 7) ^ (r & 7)) << 4));
       }
     }
   }
@@ -445,7 +488,7 @@ __global__ void __launch_bounds__(FT + 32, 1)
       }
     }
   }
-  if (tid == FT && (save_states || save_wy)) tma_store_wait_all();
+  if (tid == FT && (save_states || save_wy || want_o)) tma_store_wait_all();
   fence_before();
   __syncthreads();
   fence_after();
@@ -455,12 +498,12 @@ __global__ void __launch_bounds__(FT + 32, 1)
 size_t fwd_tc_smem_bytes() { return sizeof(TcSmem) + 1024; }
 
 int launch_fwd_tc(const FwdArgs &a, const CUtensorMap &t3, const CUtensorMap &tw, const CUtensorMap &ts,
-                  const CUtensorMap &tt, dim3 grid, cudaStream_t st) {
+                  const CUtensorMap &tt, const CUtensorMap &to, dim3 grid, cudaStream_t st) {
   const size_t smem = fwd_tc_smem_bytes();
   static_assert(sizeof(TcSmem) + 1024 <= 232448 - 256, "shared memory budget (the rest: static shared memory)");
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  return (int)launch_pdl(fwd_tc_kernel, grid, dim3(FT + 32), smem, st, a, t3, tw, ts, tt);
+  return (int)launch_pdl(fwd_tc_kernel, grid, dim3(FT + 32), smem, st, a, t3, tw, ts, tt, to);
 }
 
 }  // namespace gdn

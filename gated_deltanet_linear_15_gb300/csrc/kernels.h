@@ -99,9 +99,10 @@ int launch_fwd_chunk(const FwdArgs &a, bool is_bf16, int D, dim3 grid, cudaStrea
 int launch_fwd_prep_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &t64, const CUtensorMap &tqkv, int CH_max, cudaStream_t st);
 // tcgen05 forward, recurrent half: one CTA per (segment, head); reads the tqkv and t64 tiles, stores the
-// chunk-start states ([rows, 128] fp16, box 64 x 128) and the t128 tiles ([rows, 64] fp16, box 64 x 128)
+// chunk-start states ([rows, 128] fp16, box 64 x 128), the t128 tiles ([rows, 64] fp16, box 64 x 128) and
+// full chunks of o (map over [tokens, H, 128] bf16, box 64 x 1 x 64)
 int launch_fwd_tc(const FwdArgs &a, const CUtensorMap &tqkv, const CUtensorMap &t64, const CUtensorMap &ts,
-                  const CUtensorMap &t128, dim3 grid, cudaStream_t st);
+                  const CUtensorMap &t128, const CUtensorMap &to, dim3 grid, cudaStream_t st);
 int launch_bwd_chain(const BwdArgs &a, bool is_bf16, int D, dim3 grid, cudaStream_t st);
 // tcgen05 reverse chain (bf16, d = 128); maps: the tqkv context ([rows, 128] fp16, box 64x64), dO
 // ([tokens, H, 128] bf16, box 64x1x64), the t64 and t128 context tiles, and the per-chunk dS store
