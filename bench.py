@@ -81,9 +81,10 @@ def job_throughput(total_ms, world, tokens_per_rank_step, steps):
 # keyed by (profiler name, workload); valid only while the kernel's sources hash to the value
 # recorded with it (otherwise the roofline reports traffic null).  Summaries: profiles/*.md.
 NCU_TRAFFIC = {
-    ("bwd_local", "prefill_h32_t8192"): (959723520, "bwd_local_tc.cu", "669bdc4b65a59ee3"),
-    ("fwd_chunk", "prefill_h32_t8192"): (877718272, "fwd_tc.cu", "c237066f7b067b4a"),
-    ("bwd_chain", "prefill_h32_t8192"): (444913664, "bwd_chain_tc.cu", "6f1080fba9ae1a58"),
+    ("bwd_local", "prefill_h32_t8192"): (959556864, "bwd_local_tc.cu", "c9d8c043af0ae028"),
+    ("fwd_chunk", "prefill_h32_t8192"): (615529472, "fwd_tc.cu", "aa2f978c51b5690f"),
+    ("fwd_prep", "prefill_h32_t8192"): (514273536, "fwd_prep_tc.cu", "52f69028525893cc"),
+    ("bwd_chain", "prefill_h32_t8192"): (445611008, "bwd_chain_tc.cu", "49f98b5741a6441f"),
 }
 KERNEL_COMMON = ["chunk_common.cuh", "umma.cuh", "common.cuh", "kernels.h"]
 
