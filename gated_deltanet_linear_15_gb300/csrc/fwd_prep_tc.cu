@@ -8,8 +8,8 @@
 //   X1 = Ahat diag(beta), X2 = lower(diag(gp) Ahat diag(beta rgp)).
 // The recurrent kernel (fwd_tc.cu) then reads K, Q, V, X1, X2 and P by TMA and
 // runs only the state-dependent products per chunk.  Splitting the chunk-local
-// WY work out of the serial chain follows the pages' four-step chunked
-// algorithm (onedev.kr FlashQLA talk summary, paragraph on the WY
+// WY work out of the serial chain follows the four-step chunked algorithm
+// (onedev.kr FlashQLA talk summary, paragraph on the WY
 // representation: the intra-chunk inverse needs no state); the diagonal gamma
 // scaling is pulled out of the inverse as there (paragraph on SFU load).
 // Persistent CTAs, two per SM (one CTA's latency-bound phases overlap the other's),

@@ -150,16 +150,20 @@ int gdn_chunk_bwd(const gdn_shape *shape,
  * Saved-context training pair: the forward also leaves, in a caller-owned
  * buffer `saved`, what the backward would otherwise recompute -- the state at
  * every chunk start (fp16 for bf16 inputs, fp32 for fp32 inputs; [chunks, H,
- * d_v, d_k]) and, for bf16 with d = 128, the WY tiles X1 = Ahat diag(beta),
- * X2 = lower(diag(gamma) Ahat diag(beta / gamma)) and Ahat = (I + diag(beta) N)^{-1}
- * of every chunk, with N the strict lower triangle of K K^T (normalised keys)
- * and gamma_r = exp(in-chunk prefix sum of g) (fp16 64 x 64 row-major tiles,
- * [chunks, H, 3, 64, 64], after the states; onedev.kr FlashQLA talk summary,
- * paragraph on the WY representation, which names these intra-chunk
- * quantities).  The backward then starts at the reverse chain.  This trades
- * memory for time (d = 128, bf16: 56 KB per chunk and head, 234 MB for 32
- * heads x 8192 tokens); the pages recompute instead, and gdn_chunk_bwd keeps
- * that form.
+ * d_v, d_k]) and, for bf16 with d = 128, the chunk context after it, in this
+ * order: fp16 64 x 64 tiles [chunks, H, 5, 64, 64] X1 = Ahat diag(beta),
+ * X2 = lower(diag(gamma) Ahat diag(beta / gamma)), Ahat = (I + diag(beta) N)^{-1},
+ * P = diag(gamma) tril(Q K^T) diag(1 / gamma) and N (the strict lower
+ * triangle of K K^T, normalised keys), with gamma_r = exp(in-chunk prefix sum
+ * of g); fp16 128 x 64 tiles [chunks, H, 2, 128, 64] W^T (columns scaled by
+ * gamma) and Ut^T = U^T - S0 W^T; the fp16 operand tiles [chunks, H, 3, 64,
+ * 128] of K, Q (normalised, Q scaled) and V; fp32 [chunks, H, 2, 64]
+ * reciprocal norms 1/|k|, 1/|q| (onedev.kr FlashQLA talk summary, paragraph
+ * on the WY representation, which names these intra-chunk quantities).  The
+ * backward then starts at the reverse chain.  This trades memory for time
+ * (d = 128, bf16: 152.5 KB per chunk and head, 640 MB for 32 heads x 8192
+ * tokens); the chunked algorithm as published recomputes these in the
+ * backward instead, and gdn_chunk_bwd keeps that form.
  *  - gdn_saved_size: bytes of `saved` for this shape (0 on error).
  *  - gdn_bwd_saved_workspace_size: workspace bytes of gdn_chunk_bwd_saved
  *    (smaller than gdn_bwd_workspace_size by the recomputed regions).
