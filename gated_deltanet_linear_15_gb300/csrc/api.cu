@@ -125,6 +125,11 @@ int make_layout(const gdn_shape *s, Layout &L) {
     maxc = (s->T + CH - 1) / CH;
     L.CH_max = L.N * maxc;
   }
+  // the context tiles of the tcgen05 path are addressed by 32-bit TMA row coordinates (the largest map,
+  // the five 64-row tiles per (chunk, head), has CH_max * H * 320 rows)
+  if (s->dtype == GDN_BF16 && L.D == 128 && (long)L.CH_max * L.H * T64_TILES * CH > (long)INT32_MAX)
+    return fail(GDN_ERR_UNSUPPORTED, "too many (chunk, head) pairs for the context tiles (%ld, at most %ld)",
+                (long)L.CH_max * L.H, (long)INT32_MAX / (T64_TILES * CH));
   L.Lseg = std::max(1, choose_lseg(*s, L.N, maxc, L.CH_max));
   if (s->cu_seqlens) L.S_max = L.CH_max / L.Lseg + 2 * L.N + 1;
   else L.S_max = L.N * std::max(1, (maxc + L.Lseg - 1) / L.Lseg);

@@ -128,6 +128,18 @@ def test_forward_context_region(lib):
     assert fwd - lib.gdn_bwd_saved_workspace_size(ctypes.byref(s)) == -chunks * H * 64 * 64 * 4
 
 
+def test_context_tile_coordinates_bound(lib):
+    """The context tiles are addressed by 32-bit TMA row coordinates (320 rows per (chunk, head) in
+    the largest map): a bf16, d = 128 shape beyond that is refused before any launch; fp32, d = 64
+    (no context tiles) is not limited by it."""
+    s = _shape(T=(1 << 30) // 2 - 64, H=64)   # 8.4 M chunks x 64 heads
+    assert lib.gdn_fwd_workspace_size(ctypes.byref(s)) == 0
+    assert _fwd(lib, s) == _lib.GDN_ERR_UNSUPPORTED
+    assert b"context tiles" in lib.gdn_last_error_string()
+    s = _shape(T=1 << 16, H=64)               # 1024 chunks x 64 heads: fine
+    assert lib.gdn_fwd_workspace_size(ctypes.byref(s)) > 0
+
+
 def test_saved_context_checks(lib):
     s = _shape()
     p, big = 0x10000, 1 << 40
