@@ -51,7 +51,7 @@ __device__ __forceinline__ void st_chunk_f16(uint8_t *dst, const float *v) {
 
 }  // namespace
 
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(NTHREADS + 32, 1)
     bwd_chain_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tm3, const __grid_constant__ CUtensorMap tmdo,
                         const __grid_constant__ CUtensorMap tmp, const __grid_constant__ CUtensorMap tmw,
                         const __grid_constant__ CUtensorMap tmds) {
@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   };
   if (clast >= cbeg) {
-    if (tid == 0) issue_tma(clast, 0);
+    if (tid == NTHREADS) issue_tma(clast, 0);
     load_scalars(sm.g[0], a.g, H, h, bos + clast * CH, min(CH, len - clast * CH), 0);
     cp_async_commit();
   }
@@ -155,6 +155,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
+      if (warp >= NWARPS) break;  // the producer warp holds no state
       const int c0 = wg * 64 + half * 32;
       float v[32];
 #pragma unroll
@@ -179,28 +180,107 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     return ok;
   };
 
-  for (int c = clast; c >= cbeg && !failed; --c) {
+  // Lane 0 of warp NWARPS (the producer) issues every TMA copy and tensor-core product (an MMA issue
+  // blocks its thread while the tensor pipe's queue is full; the nine tile loads of a chunk cost its
+  // thread ~1.5 k cycles); the 8 worker warps convert dO, copy dS and read TMEM.  The two sides meet at
+  // CTA-wide OR-barriers B2 (dO and the dS copy ready: round 1) and B3 (dUt^T ready: round 2), which
+  // carry a failed wait; the workers sync among themselves on barrier 1, and the producer tells them
+  // that the previous chunk's dS store has read ds16 (barrier 2, arrive / sync).  A worker that gives up
+  // at barrier 1 releases the producer with one CTA-wide OR-barrier.
+  const bool producer = warp == NWARPS;
+  bool release = false;
+  for (int c = clast; c >= cbeg; --c) {
     const int it = clast - c;
     const int stage = it & 1;
     const int nvalid = min(CH, len - c * CH);
     uint8_t *st = sm.ring[stage];
+    if (producer) {
+      // ================================================================ producer
+      if (lane == 0) {
+        // round 2 of the previous chunk (the second of two commits per chunk: parity 1) has read its
+        // ring stage, which takes the tiles of chunk c - 1 below
+        if (it > 0) mbar_wait(u32(&sm.bar_mma), 1, err, 4);
+        if (store) tma_store_wait_read();  // the previous chunk's dS store has read ds16
+      }
+      __syncwarp();
+      named_bar_arrive<2, NTHREADS + 32>();
+      if (lane == 0 && c - 1 >= cbeg) issue_tma(c - 1, stage ^ 1);
+      __syncwarp();
+      if (__syncthreads_or(false)) {  // B2: dO and the fp16 dS copy are ready
+        failed = true;
+        break;
+      }
+      if (lane == 0) {
+        fence_after();
+        if (store && c < cend) {  // the fp16 dS at the end of chunk c, for the local-gradient kernel
+          const int srow = ((chunk0 + c) * H + h) * D;
+          tma_store_3d(&tmds, 0, srow, 0, u32(sm.ds16));
+          tma_store_3d(&tmds, 64, srow, 0, u32(sm.ds16 + 2 * HT));
+          tma_store_commit();
+        }
+        const uint32_t id_kk = idesc_f16(128, 64, false, false);
+        const uint32_t id_mm = idesc_f16(128, 64, true, true);
+        const uint32_t dsb = u32(sm.ds16), kb = u32(st), dob = u32(st + 4 * HT), pb = u32(st + 6 * HT);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * 2 * HT + (kk & 3) * 32;
+          mma_f16(tm + TM_Y, sdesc(dsb + off, 16, 1024), sdesc(kb + off, 16, 1024), id_kk, kk > 0);
+        }
+        if (with_do) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f16(tm + TM_DU, sdesc(dob + kk * 2048, HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id_mm, kk > 0);
+          const uint32_t id_s = idesc_f16(128, 128, true, true), dgb = u32(sm.dog), qb = u32(st + HT);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f16(tm + TM_S, sdesc(dgb + kk * 2048, HT, 1024), sdesc(qb + kk * 2048, 2 * HT, 1024), id_s, true);
+        }
+        mma_commit(u32(&sm.bar_mma));
+      }
+      __syncwarp();
+      if (__syncthreads_or(false)) {  // B3: dUt^T is ready
+        failed = true;
+        break;
+      }
+      if (lane == 0) {
+        fence_after();
+        const uint32_t id_kk_neg = idesc_f16(128, 128, false, false, true);
+        const uint32_t dub = u32(sm.kc), wb = u32(st + 7 * HT);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f16(tm + TM_S, sdesc(dub + kk * 32, 16, 1024), sdesc(wb + kk * 32, 16, 1024), id_kk_neg, true);
+        mma_commit(u32(&sm.bar_mma));
+      }
+      __syncwarp();
+      continue;
+    }
+
+    // ================================================================ workers
     float gnext0 = 0.f, gnext1 = 0.f;  // log-gates of the next (previous in time) chunk
     if (warp == 0 && c - 1 >= cbeg) {
       const int tokn = bos + (c - 1) * CH;
       gnext0 = a.g[(size_t)(tokn + lane) * H + h];
       gnext1 = a.g[(size_t)(tokn + lane + 32) * H + h];
     }
-    cp_async_wait_all();
-    if (tid == 0 && c - 1 >= cbeg) issue_tma(c - 1, stage ^ 1);
-    if (tid == 0 && store) tma_store_wait_read();  // the previous chunk's dS store has read ds16
-    const bool tma_ok = mbar_wait(u32(&sm.bar_tma[stage]), (it >> 1) & 1, err, 8);
-    if (__syncthreads_or(!tma_ok)) {
-      failed = true;
-      break;
+    if (it == 0) cp_async_wait_all();  // the first chunk's gates; later ones come from gnext
+    {
+      const bool tma_ok = mbar_wait(u32(&sm.bar_tma[stage]), (it >> 1) & 1, err, 8);
+      uint32_t any;
+      asm volatile(
+          "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+          : "=r"(any)
+          : "r"((uint32_t)(!tma_ok || failed)), "n"(NTHREADS)
+          : "memory");
+      if (any) {
+        failed = release = true;
+        break;
+      }
     }
     Gates &G = sm.gt[stage];
-    if (it == 0 && warp == 0) gate_prefix(sm.g[stage], G);
-    __syncthreads();
+    if (it == 0) {
+      if (warp == 0) gate_prefix(sm.g[stage], G);
+      named_bar_sync<1, NTHREADS>();
+    }
 
     // ---- prep: dO -> fp16 in place and diag(gam) dO (rows >= nvalid zero); K, Q come as operand tiles
     if (with_do) {
@@ -225,6 +305,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         *reinterpret_cast<uint4 *>(rowg + off) = g4;
       }
     }
+    named_bar_sync<2, NTHREADS + 32>();  // the previous chunk's dS store has read ds16
     // ---- dS (end of chunk c) -> fp16 operand copy, gam_C dS back into TMEM
     {
       const float gC = G.gamC;
@@ -246,41 +327,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     fence_async_smem();
     fence_before();
-    __syncthreads();
-
-    // ---- Y = dS K^T -> TM_Y, Z = dO^T P -> TM_DU (M = 128, N = 64);  dS += (diag(gam) dO)^T Q (N = 128)
-    if (tid == 0) {
-      fence_after();
-      if (store && c < cend) {  // the fp16 dS at the end of chunk c, for the local-gradient kernel
-        const int srow = ((chunk0 + c) * H + h) * D;
-        tma_store_3d(&tmds, 0, srow, 0, u32(sm.ds16));
-        tma_store_3d(&tmds, 64, srow, 0, u32(sm.ds16 + 2 * HT));
-        tma_store_commit();
-      }
-      const uint32_t id_kk = idesc_f16(128, 64, false, false);
-      const uint32_t id_mm = idesc_f16(128, 64, true, true);
-      const uint32_t dsb = u32(sm.ds16), kb = u32(st), dob = u32(st + 4 * HT), pb = u32(st + 6 * HT);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t off = (kk >> 2) * 2 * HT + (kk & 3) * 32;
-        mma_f16(tm + TM_Y, sdesc(dsb + off, 16, 1024), sdesc(kb + off, 16, 1024), id_kk, kk > 0);
-      }
-      if (with_do) {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_f16(tm + TM_DU, sdesc(dob + kk * 2048, HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id_mm, kk > 0);
-        const uint32_t id_s = idesc_f16(128, 128, true, true), dgb = u32(sm.dog), qb = u32(st + HT);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_f16(tm + TM_S, sdesc(dgb + kk * 2048, HT, 1024), sdesc(qb + kk * 2048, 2 * HT, 1024), id_s, true);
-      }
-      mma_commit(u32(&sm.bar_mma));
-    }
-    __syncwarp();
-    if (__syncthreads_or(!mma_wait())) {
+    if (__syncthreads_or(false)) {  // B2: the producer stores dS and issues round 1
       failed = true;
       break;
     }
+    failed |= !mma_wait();  // round 1
     {  // dUt^T = Y diag(cdec) + Z -> fp16 K-major A (rows = d_v, k = token)
       const int c0 = wg * 32;
       float y[32], v[32];
@@ -303,19 +354,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     fence_before();
     fence_async_smem();
-    __syncthreads();
-
-    // ---- dS -= dUt^T W   (M = 128, N = 128)
-    if (tid == 0) {
-      fence_after();
-      const uint32_t id_kk_neg = idesc_f16(128, 128, false, false, true);
-      const uint32_t dub = u32(sm.kc), wb = u32(st + 7 * HT);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_f16(tm + TM_S, sdesc(dub + kk * 32, 16, 1024), sdesc(wb + kk * 32, 16, 1024), id_kk_neg, true);
-      mma_commit(u32(&sm.bar_mma));
+    if (__syncthreads_or(failed)) {  // B3: the producer issues round 2
+      failed = true;
+      break;
     }
-    __syncwarp();
     if (warp == 0 && c - 1 >= cbeg) {  // gates of the next chunk, overlapping the last product
       float *gn = sm.g[stage ^ 1];
       const int nvn = min(CH, len - (c - 1) * CH);
@@ -324,13 +366,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       __syncwarp();
       gate_prefix(gn, sm.gt[stage ^ 1]);
     }
-    if (__syncthreads_or(!mma_wait())) {
-      failed = true;
-      break;
-    }
+    failed |= !mma_wait();  // round 2
   }
+  if (release) __syncthreads_or(true);  // meet the producer at its pending CTA-wide barrier: it stops there
 
-  if (!failed) {
+  if (!failed && warp < NWARPS) {
     float *dst = nullptr;
     if (a.pass == 0) dst = (transition ? a.Rbuf : a.Fbuf) + sh_idx * DD;
     else if (j == 0 && a.dS0) dst = a.dS0 + ((size_t)n * H + h) * DD;
@@ -347,7 +387,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
   }
-  if (tid == 0 && store) tma_store_wait_all();
+  if (tid == NTHREADS && store) tma_store_wait_all();
   fence_before();
   __syncthreads();
   fence_after();
@@ -359,7 +399,7 @@ int launch_bwd_chain_tc(const BwdArgs &a, const CUtensorMap *maps, dim3 grid, cu
   static_assert(sizeof(ChainTcSmem) + 1024 <= 232448 - 256, "shared memory budget (the rest: static shared memory)");
   cudaError_t e = cudaFuncSetAttribute(bwd_chain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  return (int)launch_pdl(bwd_chain_tc_kernel, grid, dim3(NTHREADS), smem, st, a, maps[0], maps[1], maps[2], maps[3],
+  return (int)launch_pdl(bwd_chain_tc_kernel, grid, dim3(NTHREADS + 32), smem, st, a, maps[0], maps[1], maps[2], maps[3],
                          maps[4]);
 }
 

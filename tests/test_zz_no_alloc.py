@@ -55,7 +55,7 @@ def test_static_scratch_rejects_oversized_shape():
     from gated_deltanet_linear_15_gb300 import _lib
     lib = _lib.load()
     s = g.GdnShape()
-    s.B, s.T, s.H, s.Dk, s.Dv = 1, 1 << 20, 1024, 128, 128   # per-chunk gate sums alone exceed the array
+    s.B, s.T, s.H, s.Dk, s.Dv = 1, 1 << 20, 64, 128, 128   # the forward's chunk-context region alone exceeds the array
     s.dtype, s.scale = _lib.GDN_BF16, 0.1
     p = 1 << 20
     rc = lib.gdn_chunk_fwd_static(ctypes.byref(s), p, p, p, p, p, None, p, None, None)
