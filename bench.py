@@ -83,8 +83,8 @@ def job_throughput(total_ms, world, tokens_per_rank_step, steps):
 NCU_TRAFFIC = {
     ("bwd_local", "prefill_h32_t8192"): (959556864, "bwd_local_tc.cu", "c9d8c043af0ae028"),
     ("fwd_chunk", "prefill_h32_t8192"): (615529472, "fwd_tc.cu", "aa2f978c51b5690f"),
-    ("fwd_prep", "prefill_h32_t8192"): (514273536, "fwd_prep_tc.cu", "5b5c1d7b19e85a1c"),
-    ("bwd_chain", "prefill_h32_t8192"): (444592640, "bwd_chain_tc.cu", "c06123d83eb6e887"),
+    ("fwd_prep", "prefill_h32_t8192"): (514273536, "fwd_prep_tc.cu", "d7ad282d62ba273c"),
+    ("bwd_chain", "prefill_h32_t8192"): (444592640, "bwd_chain_tc.cu", "85a6b5f1c290cd45"),
 }
 KERNEL_COMMON = ["chunk_common.cuh", "umma.cuh", "common.cuh", "kernels.h"]
 

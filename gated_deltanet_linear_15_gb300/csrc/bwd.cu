@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_chain_kernel(BwdArgs a) {
   }
   const bool store = (a.pass == 1);
   const bool l2 = (a.flags & kFlagL2Norm) != 0;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   const int wr = warp >> 1, wc = warp & 1;
   const I *qg = static_cast<const I *>(a.q);
   const I *kg = static_cast<const I *>(a.k);

@@ -23,7 +23,6 @@ namespace {
 
 constexpr int D = 128;
 constexpr int HT = 8192;
-constexpr int LN = CH + 4;
 constexpr uint32_t TM_S = 0, TM_DU = 256, TM_Y = 320, TM_COLS = 512;
 
 struct __align__(1024) ChainTcSmem {

@@ -24,8 +24,7 @@ using namespace umma;
 
 namespace {
 
-constexpr int D = 128;
-constexpr int HT = 8192;  // one 64 x 64 fp16 half-tile, 128B-swizzled
+constexpr int HT = 8192;  // one 64 x 64 fp16 half-tile, 128B-swizzled (d = 128: two per 64-row tile)
 constexpr int PT = 256;   // threads per CTA (warps 0-7: the inverse's warp count)
 constexpr int LN = CH + 4;
 
