@@ -183,7 +183,7 @@ def cpu_oracle_sample(wname, heads=None, tokens=None):
     dt = time.perf_counter() - t0
     # the workload's tokens/s: T tokens of all H heads cost H/Hs times the sample
     tps = T * (Hs / w.H) / dt
-    return tps, min(cores, Hs * x["N"]), f"fwd+bwd of {Hs} of {w.H} heads x {T} tokens, {dt:.2f} s"
+    return tps, min(cores, Hs * x["N"]), f"fwd+bwd of {Hs} of {w.H} heads x {T} tokens, {dt:.2f} s", dt, Hs / w.H
 
 
 def run_reference(args):
@@ -191,19 +191,25 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    times, tps_all = [], []
-    desc, cores = "", 1
+    tps_all, dts = [], []
+    desc, cores, frac = "", 1, 1.0
     from gdn_inputs import WORKLOADS
     w = WORKLOADS[args.workload]
     for i in range(args.warmup + args.steps):
-        tps, cores, desc = cpu_oracle_sample(args.workload, tokens=args.ref_tokens)
+        tps, cores, desc, dt, frac = cpu_oracle_sample(args.workload, tokens=args.ref_tokens)
         if i >= args.warmup:
             tps_all.append(tps)
+            dts.append(dt)
     value = statistics.median(tps_all)
     tokens_per_step = (w.B * w.T) if w.T else 135168
+    # Each step is a bounded sample of the workload (a fraction of its heads); ms_per_step is the
+    # sample's measured wall time, value the workload-equivalent throughput (sample tokens x head
+    # fraction / time), and the whole-workload time per step it implies is given beside it.
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": 1000.0 * tokens_per_step / value, "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": 1000.0 * statistics.median(dts), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "sampled": True, "sample_head_fraction": round(frac, 4), "timed_seconds": round(sum(dts), 3),
+            "workload_ms_per_step_equivalent": 1000.0 * tokens_per_step / value,
             "config": {"workload": args.workload, "B": w.B, "T": w.T, "H": w.H, "d": w.D},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -310,7 +316,7 @@ def main():
     # CPU baseline first (before heavy GPU work), rank 0 at N=1 only
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tps, cores, desc = cpu_oracle_sample(args.workload)
+        tps, cores, desc, _, _ = cpu_oracle_sample(args.workload)
         cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
 
     import __graft_entry__
@@ -339,14 +345,16 @@ def main():
     # One training step of the layer: the forward (o, S_T) then the backward (all gradients), both from
     # the inputs.  Saved-context pair (default): the forward also leaves its per-chunk states and WY
     # tiles in `saved` and the backward reads them; --recompute: the backward rederives them.
-    def fwd_call(q, k, v, gg, beta, o_, recompute):
+    def fwd_call(q, k, v, gg, beta, o_, recompute, st_=None):
+        st_ = ST if st_ is None else st_
         if recompute:
-            return g.gdn_chunk_fwd(shape, q, k, v, gg, beta, x["S0"], o_, ST, ws, ws_bytes, stream)
-        return g.gdn_chunk_fwd_save(shape, q, k, v, gg, beta, x["S0"], o_, ST, saved, ws, saved_bytes, ws_bytes,
+            return g.gdn_chunk_fwd(shape, q, k, v, gg, beta, x["S0"], o_, st_, ws, ws_bytes, stream)
+        return g.gdn_chunk_fwd_save(shape, q, k, v, gg, beta, x["S0"], o_, st_, saved, ws, saved_bytes, ws_bytes,
                                     stream)
 
     def bwd_call(q, k, v, gg, beta, dO, outs, recompute):
-        a = (shape, q, k, v, gg, beta, x["S0"], dO, x["dST"], outs[0], outs[1], outs[2], outs[3], outs[4], dS0)
+        ds0 = outs[5] if len(outs) > 5 else dS0
+        a = (shape, q, k, v, gg, beta, x["S0"], dO, x["dST"], outs[0], outs[1], outs[2], outs[3], outs[4], ds0)
         if recompute:
             return g.gdn_chunk_bwd(*a, ws, ws_bytes, stream)
         return g.gdn_chunk_bwd_saved(*a, saved, ws, saved_bytes, ws_bytes, stream)
@@ -459,7 +467,9 @@ def main():
     if rank == 0:
         in_keys = ("q", "k", "v", "g", "beta", "dO")
         host_in = {k: x[k].cpu().pin_memory() for k in in_keys}
-        outs = {"o": o, "dq": dq, "dk": dk, "dv": dv, "dg": dg, "dbeta": db}
+        outs = {"o": o, "S_T": ST, "dq": dq, "dk": dk, "dv": dv, "dg": dg, "dbeta": db}
+        if dS0 is not None:
+            outs["dS0"] = dS0
         host_out = {k: torch.empty_like(t, device="cpu").pin_memory() for k, t in outs.items()}
         nbuf = 2
         dev_in = [{k: torch.empty_like(x[k]) for k in in_keys} for _ in range(nbuf)]
@@ -469,10 +479,10 @@ def main():
         s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
 
         def compute(di, do):
-            rc = fwd_call(di["q"], di["k"], di["v"], di["g"], di["beta"], do["o"], args.recompute)
+            rc = fwd_call(di["q"], di["k"], di["v"], di["g"], di["beta"], do["o"], args.recompute, do["S_T"])
             assert rc == 0
             rc = bwd_call(di["q"], di["k"], di["v"], di["g"], di["beta"], di["dO"],
-                          (do["dq"], do["dk"], do["dv"], do["dg"], do["dbeta"]), args.recompute)
+                          (do["dq"], do["dk"], do["dv"], do["dg"], do["dbeta"], do.get("dS0")), args.recompute)
             assert rc == 0
 
         def run(n, pipelined):

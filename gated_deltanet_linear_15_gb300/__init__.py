@@ -28,8 +28,8 @@ from ._lib import (GDN_BF16, GDN_FP32, GDN_L2NORM_QK, GDN_SP_OFF, GDN_WINDOW_OFF
 
 __all__ = ["GdnShape", "make_shape", "gdn_chunk_fwd", "gdn_chunk_fwd_static", "gdn_chunk_bwd", "gdn_fwd_workspace_size",
            "gdn_bwd_workspace_size", "gdn_saved_size", "gdn_bwd_saved_workspace_size", "gdn_chunk_fwd_save",
-           "gdn_chunk_bwd_saved", "gdn_plan_query", "gdn_get_device_status", "gdn_profile_enable", "gdn_profile_only",
-           "gdn_profile_report",
+           "gdn_chunk_bwd_saved", "gdn_plan_query", "gdn_get_device_status", "gdn_device_status_code",
+           "gdn_profile_enable", "gdn_profile_only", "gdn_profile_report",
            "chunk_gated_delta_rule_fwd", "chunk_gated_delta_rule_bwd", "chunk_gated_delta_rule",
            "GDN_L2NORM_QK", "GDN_SP_OFF", "GDN_WINDOW_OFF"]
 
@@ -173,7 +173,12 @@ def gdn_profile_report(reset: bool = True) -> dict:
 
 
 def gdn_get_device_status(shape: GdnShape, workspace, stream=None) -> int:
+    """The device status word of the last call (workspace None: of gdn_chunk_fwd_static)."""
     return int(_lib.load().gdn_get_device_status(ctypes.byref(shape), _ptr(workspace), _stream(stream)))
+
+
+def gdn_device_status_code(word: int) -> int:
+    return int(_lib.load().gdn_device_status_code(int(word)))
 
 
 # ------------------------------------------------------------------ allocation helpers

@@ -9,6 +9,7 @@ from . import build as _build
 
 GDN_BF16, GDN_FP32 = 0, 1
 GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE, GDN_ERR_CUDA = 0, 1, 2, 3, 4
+GDN_ERR_TIMEOUT, GDN_ERR_NUMERIC = 5, 6
 GDN_L2NORM_QK, GDN_SP_OFF, GDN_WINDOW_OFF = 1, 2, 4
 GDN_DEBUG_WAIT_TIMEOUT = 0x80000000
 GDN_STATIC_SCRATCH_BYTES = 16 << 20
@@ -17,7 +18,7 @@ GDN_STATIC_SCRATCH_BYTES = 16 << 20
 EXPORTS = ("gdn_fwd_workspace_size", "gdn_bwd_workspace_size", "gdn_chunk_fwd", "gdn_chunk_fwd_static",
            "gdn_chunk_bwd", "gdn_saved_size", "gdn_bwd_saved_workspace_size", "gdn_chunk_fwd_save",
            "gdn_chunk_bwd_saved", "gdn_recurrent_fwd",
-           "gdn_get_device_status", "gdn_plan_query", "gdn_profile_enable", "gdn_profile_report", "gdn_profile_only",
+           "gdn_get_device_status", "gdn_device_status_code", "gdn_plan_query", "gdn_profile_enable", "gdn_profile_report", "gdn_profile_only",
            "gdn_status_string", "gdn_last_error_string")
 
 
@@ -72,6 +73,8 @@ def load():
         lib.gdn_recurrent_fwd.restype = ctypes.c_int
         lib.gdn_get_device_status.argtypes = [S, P, P]
         lib.gdn_get_device_status.restype = ctypes.c_int
+        lib.gdn_device_status_code.argtypes = [ctypes.c_int]
+        lib.gdn_device_status_code.restype = ctypes.c_int
         lib.gdn_plan_query.argtypes = [S, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
                                        ctypes.POINTER(ctypes.c_int)]
         lib.gdn_plan_query.restype = ctypes.c_int

@@ -739,6 +739,14 @@ int gdn_chunk_fwd_static(const gdn_shape *s, const void *q, const void *k, const
   {
     std::lock_guard<std::mutex> lk(g_static_mu);
     if (!g_static_ptr[dev]) {
+      // the address lookup may not run inside a stream capture: refuse that case with a clear message
+      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+      if (cudaStreamIsCapturing(reinterpret_cast<cudaStream_t>(stream), &cs) != cudaSuccess)
+        return fail(GDN_ERR_CUDA, "gdn_chunk_fwd_static: cudaStreamIsCapturing failed");
+      if (cs != cudaStreamCaptureStatusNone)
+        return fail(GDN_ERR_INVALID_ARG,
+                    "gdn_chunk_fwd_static: the first call on device %d must come before any stream capture "
+                    "(it looks up the static scratch's device address)", dev);
       void *p = nullptr;
       const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
       if (e != cudaSuccess || !p)
@@ -806,12 +814,23 @@ int gdn_recurrent_fwd(const gdn_shape *s, const void *q, const void *k, const vo
 
 int gdn_get_device_status(const gdn_shape *shape, const void *workspace, gdn_stream_t stream) {
   (void)shape;
-  if (!workspace) return -1;
   int v = 0;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(&v, workspace, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess) return -1;
+  // workspace NULL: the status word of gdn_chunk_fwd_static, word 0 of the static scratch on the
+  // current device (read through the symbol, so no cached address is involved)
+  const cudaError_t e = workspace ? cudaMemcpyAsync(&v, workspace, 4, cudaMemcpyDeviceToHost, st)
+                                  : cudaMemcpyFromSymbolAsync(&v, g_static_scratch, 4, 0, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return -1;
   if (cudaStreamSynchronize(st) != cudaSuccess) return -1;
   return v;
+}
+
+int gdn_device_status_code(int word) {
+  if (word < 0) return GDN_ERR_CUDA;
+  if (word & 2) return GDN_ERR_INVALID_ARG;
+  if (word & (4 | 8)) return GDN_ERR_TIMEOUT;
+  if (word & 1) return GDN_ERR_NUMERIC;
+  return GDN_OK;
 }
 
 int gdn_plan_query(const gdn_shape *shape, int *seg_chunks, int *max_segments, int *max_chunks) {
@@ -871,6 +890,8 @@ const char *gdn_status_string(int status) {
     case GDN_ERR_UNSUPPORTED: return "unsupported configuration";
     case GDN_ERR_WORKSPACE: return "workspace missing or too small";
     case GDN_ERR_CUDA: return "CUDA error";
+    case GDN_ERR_TIMEOUT: return "a bounded device wait expired";
+    case GDN_ERR_NUMERIC: return "an fp16 tensor-core operand overflowed or was not finite";
     default: return "unknown status";
   }
 }

@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_chain_kernel(BwdArgs a) {
   issue_loads(clast);
 
   Acc<SWM, SWN> dS;
+  bool nbad = false;  // numeric guard: an fp16 operand out of range
   {
     const float *src = nullptr;
     if (!transition) {
@@ -138,10 +139,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_chain_kernel(BwdArgs a) {
         *reinterpret_cast<uint4 *>(dst + (size_t)r * D + cc) = *reinterpret_cast<const uint4 *>(&sm.ds[r * LD + cc]);
       }
     }
-    prep_rows<I, E, D>(sm.k, LD, 1.f, l2, nullptr);
+    nbad |= prep_rows<I, E, D>(sm.k, LD, 1.f, l2, nullptr);
     if (!transition) {
-      prep_rows<I, E, D>(sm.q, LD, a.scale, l2, nullptr);
-      prep_rows<I, E, D>(sm.dob, LD, 1.f, false, nullptr);
+      nbad |= prep_rows<I, E, D>(sm.q, LD, a.scale, l2, nullptr);
+      nbad |= prep_rows<I, E, D>(sm.dob, LD, 1.f, false, nullptr);
     }
     if (warp == 0) gate_prefix(sm.g, sm.gt);
     __syncthreads();
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_chain_kernel(BwdArgs a) {
       } else {
         acc.each([&](int r, int cc, float &v) {
           const int row = m0 + r, col = n0 + cc;
-          sm.p[row * LC + col] = fromf<E>(col <= row ? v * sm.gt.gp[row] * sm.gt.rgp[col] : 0.f);
+          sm.p[row * LC + col] = fromf<E>(col <= row ? v * gratio(sm.gt, row, col) : 0.f);
         });
       }
     }
@@ -210,8 +211,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_chain_kernel(BwdArgs a) {
     }
     __syncthreads();
     if (c - 1 >= cbeg) issue_loads(c - 1);  // K, Q, dO, g, beta tiles are free now
-    dS.pairs([&](int r, int cc, float &v0, float &v1) { st2(&sm.ds[(wr * SWM + r) * LD + wc * SWN + cc], v0, v1); });
+    dS.pairs([&](int r, int cc, float &v0, float &v1) {
+      if (std::is_same<E, f16>::value) nbad |= f16_out(v0) | f16_out(v1);
+      st2(&sm.ds[(wr * SWM + r) * LD + wc * SWN + cc], v0, v1);
+    });
   }
+  if (nbad && a.status) atomicOr(a.status, 1);
 
   float *dst = nullptr;
   if (a.pass == 0) dst = (transition ? a.Rbuf : a.Fbuf) + sh_idx * DD;
@@ -238,7 +243,7 @@ template <typename E, int D> struct LocalSmem {
   float g[CH], beta[CH], nq[CH], nk[CH];
   Gates gt;
   float ys[1152];
-  float part[14][CH];   // gate-gradient partials (see the final sum)
+  float part[18][CH];   // gate-gradient partials (see the final sum)
   float bpart[6][CH];   // beta-gradient partials
   float rdot[2][CH];    // row dots for the normalisation Jacobians
   float red[NWARPS];
@@ -308,17 +313,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_local_kernel(BwdArgs a) {
     } else {
       acc.each([&](int r, int cc, float &v) {
         const int row = m0 + r, col = n0 + cc;
-        sm.p[row * LC + col] = fromf<E>(col <= row ? v * sm.gt.gp[row] * sm.gt.rgp[col] : 0.f);
+        sm.p[row * LC + col] = fromf<E>(col <= row ? v * gratio(sm.gt, row, col) : 0.f);
       });
     }
   }
   __syncthreads();
   wy_inverse<std::is_same<E, float>::value, true>(sm.nf, LN, sm.beta, sm.ys,
                                                     [&](int r, int c, float a0, float a1) {
-    const float b0 = sm.beta[c], b1 = sm.beta[c + 1], gr = sm.gt.gp[r];
+    const float b0 = sm.beta[c], b1 = sm.beta[c + 1];
     st2(&sm.x1[r * LC + c], a0 * b0, a1 * b1);
-    st2(&sm.x2[r * LC + c], c <= r ? a0 * b0 * (gr * sm.gt.rgp[c]) : 0.f,
-        c + 1 <= r ? a1 * b1 * (gr * sm.gt.rgp[c + 1]) : 0.f);
+    st2(&sm.x2[r * LC + c], c <= r ? a0 * b0 * gratio(sm.gt, r, c) : 0.f,
+        c + 1 <= r ? a1 * b1 * gratio(sm.gt, r, c + 1) : 0.f);
   });
 
   const int m0 = wr * 16, n0 = wc * WN;  // 64 x D outputs: 4 x 2 warps of 16 x D/2
@@ -342,7 +347,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_local_kernel(BwdArgs a) {
   }
   __syncthreads();
 
-  // ---- Y = K dS^T: y-terms; dUt = diag(cdec) Y + P^T dO; <dUt, Ut>
+  // ---- Y = K dS^T: y-terms <Ut, Y>; dUt = diag(cdec) Y + P^T dO
   Acc<16, WN> dU;
   {
     dU.zero();
@@ -351,19 +356,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_local_kernel(BwdArgs a) {
     dU.each([&](int r, int cc, float &v) { ry[r >> 3] += v * tof(sm.ut[(m0 + r) * LD + n0 + cc]); });
     dU.each([&](int r, int cc, float &v) { v *= sm.gt.cdec[m0 + r]; });
     warp_mma<16, WN, true, true>(dU, sm.p, LC, sm.dob, LD, m0, n0, CH);
-    float ru[2] = {0.f, 0.f};
-    dU.each([&](int r, int cc, float &v) { ru[r >> 3] += v * tof(sm.ut[(m0 + r) * LD + n0 + cc]); });
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
-      ry[t] = quad_sum(ry[t]);
-      ru[t] = quad_sum(ru[t]);
-    }
+    for (int t = 0; t < 2; ++t) ry[t] = quad_sum(ry[t]);
     if ((lane & 3) == 0) {
       const int r = m0 + (lane >> 2);
       sm.part[0 + wc][r] = ry[0];
       sm.part[0 + wc][r + 8] = ry[1];
-      sm.part[2 + wc][r] = ru[0];
-      sm.part[2 + wc][r + 8] = ru[1];
     }
   }
   // dK accumulator (kept in registers): diag(cdec) Ut dS
@@ -402,7 +400,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_local_kernel(BwdArgs a) {
       const float z = v * pv;
       rs[r >> 3] += z;
       cs[cc >> 3][cc & 1] += z;
-      dpm[row * LC + col] = fromf<E>(col <= row ? v * sm.gt.gp[row] * sm.gt.rgp[col] : 0.f);
+      dpm[row * LC + col] = fromf<E>(col <= row ? v * gratio(sm.gt, row, col) : 0.f);
     });
 #pragma unroll
     for (int t = 0; t < 2; ++t) rs[t] = quad_sum(rs[t]);
@@ -487,19 +485,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_local_kernel(BwdArgs a) {
     Acc<16, WN> acc;
     acc.zero();
     warp_mma<16, WN, true, true>(acc, sm.x2, LC, du, LD, m0, n0, CH);
-    float rv[2] = {0.f, 0.f};
     I *dvg = static_cast<I *>(a.dv);
     acc.pairs([&](int r, int cc, float &v0, float &v1) {
       const int row = m0 + r;
-      rv[r >> 3] += v0 * tof(sm.v[row * LD + n0 + cc]) + v1 * tof(sm.v[row * LD + n0 + cc + 1]);
       if (row < nvalid) st2(dvg + ((size_t)(tok0 + row) * H + h) * D + n0 + cc, v0, v1);
     });
-#pragma unroll
-    for (int t = 0; t < 2; ++t) rv[t] = quad_sum(rv[t]);
-    if ((lane & 3) == 0) {
-      sm.part[12 + wc][m0 + (lane >> 2)] = rv[0];
-      sm.part[12 + wc][m0 + (lane >> 2) + 8] = rv[1];
-    }
   }
   // ---- dAhat = (dW' K^T + Gamma * (dUt V^T)) diag(beta); beta column terms
   {
@@ -509,12 +499,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_local_kernel(BwdArgs a) {
     const int pm0 = wr * 16, pn0 = wc * 32;
     warp_mma<16, 32, false, false>(a1, dw, LD, sm.k, LD, pm0, pn0, D);
     warp_mma<16, 32, false, false>(a2, du, LD, sm.v, LD, pm0, pn0, D);
-    float cs[4][2];
+    float cs[4][2], xc[4][2], rwx[2] = {0.f, 0.f};
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) cs[jj][0] = cs[jj][1] = 0.f;
+    for (int jj = 0; jj < 4; ++jj) cs[jj][0] = cs[jj][1] = xc[jj][0] = xc[jj][1] = 0.f;
     // element (r, i): a1 = <dW'_r, k_i>, a2 = <dUt_r, v_i>; the V term carries
-    // Gamma_ri = gp_r rgp_i <= 1 for i <= r (entries above the diagonal do not
-    // reach the strictly lower part of dT and are dropped)
+    // Gamma_ri = gamma_r / gamma_i <= 1 for i <= r (entries above the diagonal do not
+    // reach the strictly lower part of dT and are dropped).  Gate terms: <dW_r, W_r> =
+    // rowsum_r(beta Ahat a1) and the row / column sums of X2 * a2 = beta Ahat Gamma a2 over the
+    // strictly lower triangle (a diagonal ratio does not depend on the gates; leaving it out of both
+    // sums avoids a difference of two large, differently rounded numbers under strong decay)
     {
       const int lr = lane >> 2, lcc = 2 * (lane & 3);
 #pragma unroll
@@ -524,11 +517,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_local_kernel(BwdArgs a) {
           const int row = pm0 + lr + 8 * (e >> 1), col = pn0 + 8 * jj + lcc + (e & 1);
           const float ah = ahat_at(sm.nf, LN, row, col);
           const float x1 = a1.c[0][jj][e];
-          const float x2 = col <= row ? a2.c[0][jj][e] * (sm.gt.gp[row] * sm.gt.rgp[col]) : 0.f;
+          const float x2 = col <= row ? a2.c[0][jj][e] * gratio(sm.gt, row, col) : 0.f;
+          const float xo = col < row ? sm.beta[col] * ah * x2 : 0.f;
+          rwx[e >> 1] += sm.beta[col] * ah * x1 + xo;
+          xc[jj][e & 1] += xo;
           cs[jj][e & 1] += ah * (x1 + x2);
           a1.c[0][jj][e] = sm.beta[col] * (x1 + x2);
         }
     }
+#pragma unroll
+    for (int t = 0; t < 2; ++t) rwx[t] = quad_sum(rwx[t]);
+    if ((lane & 3) == 0) {
+      sm.part[2 + wc][pm0 + (lane >> 2)] = rwx[0];
+      sm.part[2 + wc][pm0 + (lane >> 2) + 8] = rwx[1];
+    }
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        float x = xc[jj][t];
+        x += __shfl_xor_sync(0xffffffffu, x, 4);
+        x += __shfl_xor_sync(0xffffffffu, x, 8);
+        x += __shfl_xor_sync(0xffffffffu, x, 16);
+        if (lane < 4) sm.part[14 + wr][pn0 + 8 * jj + 2 * lane + t] = x;
+      }
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
@@ -618,39 +630,41 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_local_kernel(BwdArgs a) {
   }
   // ---- gate and beta gradients
   if (warp == 0) {
-    float extra = 0.f;  // added to dG of the last row
-    float sumy = 0.f;
-    float dGv[2];
+    // dg_t = sum_{r >= t} dG_r + gam_C <dS, S0> + sum_{r < t} y_r (the state terms y_r = cdec_r <Ut_r, Y_r>
+    // depend on g_t only for r < t): a reverse inclusive scan of dG and a forward exclusive scan of y
+    float dGv[2], yv[2];
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const int r = lane + 32 * t;
-      const float y = sm.gt.cdec[r] * (sm.part[0][r] + sm.part[1][r]);
-      sumy += y;
-      float d = sm.part[2][r] + sm.part[3][r];                                     // <dUt, Ut>
+      yv[t] = sm.gt.cdec[r] * (sm.part[0][r] + sm.part[1][r]);
+      float d = sm.part[2][r] + sm.part[3][r];                                     // <dW, W> + X2 * M2 rows
       d += sm.part[4][r] + sm.part[5][r];                                          // row sums of dP * P
       d -= sm.part[6][r] + sm.part[7][r] + sm.part[8][r] + sm.part[9][r];          // column sums
       d += sm.part[10][r] + sm.part[11][r];                                        // gam <dO, S0 q>
-      d -= sm.part[12][r] + sm.part[13][r];                                        // -<dV, v>
-      d -= y;
+      d -= sm.part[14][r] + sm.part[15][r] + sm.part[16][r] + sm.part[17][r];      // X2 * M2 columns
       dGv[t] = d;
     }
-    sumy = warp_sum(sumy);
     float red = 0.f;
     for (int i = 0; i < NWARPS; ++i) red += sm.red[i];
-    extra = sumy + sm.gt.gamC * red;
-    if (lane == 31) dGv[1] += extra;
-    // dg_i = sum_{r >= i} dG_r : reverse inclusive scan over 64 values
-    float hi = dGv[1], lo = dGv[0];
+    float hi = dGv[1], lo = dGv[0], ylo = yv[0], yhi = yv[1];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const float yh = __shfl_down_sync(0xffffffffu, hi, o), yl = __shfl_down_sync(0xffffffffu, lo, o);
+      const float fl = __shfl_up_sync(0xffffffffu, ylo, o), fh = __shfl_up_sync(0xffffffffu, yhi, o);
       if (lane + o < 32) {
         hi += yh;
         lo += yl;
       }
+      if (lane >= o) {
+        ylo += fl;
+        yhi += fh;
+      }
     }
-    const float tot_hi = __shfl_sync(0xffffffffu, hi, 0);
-    lo += tot_hi;
+    lo += __shfl_sync(0xffffffffu, hi, 0);
+    yhi += __shfl_sync(0xffffffffu, ylo, 31);
+    const float base = sm.gt.gamC * red;
+    lo += base + (ylo - yv[0]);
+    hi += base + (yhi - yv[1]);
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const int r = lane + 32 * t;
@@ -694,7 +708,9 @@ int launch_bwd_chain(const BwdArgs &a, bool is_bf16, int D, dim3 grid, cudaStrea
 }
 int launch_bwd_local(const BwdArgs &a, bool is_bf16, int D, int CH_max, cudaStream_t st) {
   if (CH_max == 0) return 0;
-  if (is_bf16 && D == 128) return launch_local<bf16, 128>(a, CH_max, st);
+  // bf16 with d = 128 reaches this kernel only for a call without tokens (its local gradients run on the
+  // tensor cores otherwise), where there is no chunk to differentiate
+  if (is_bf16 && D == 128) return 0;
   if (is_bf16 && D == 64) return launch_local<bf16, 64>(a, CH_max, st);
   if (!is_bf16 && D == 64) return launch_local<float, 64>(a, CH_max, st);
   return -1;

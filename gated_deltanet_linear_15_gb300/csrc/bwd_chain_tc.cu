@@ -172,6 +172,7 @@ __global__ void __launch_bounds__(NTHREADS + 32, 1)
   int *err = a.status;
   uint32_t mma_phase = 0;
   bool failed = false;
+  bool nbad = false;  // numeric guard: an fp16 operand out of range
   auto mma_wait = [&]() {
     const bool ok = mbar_wait(u32(&sm.bar_mma), mma_phase, err, 4);
     mma_phase ^= 1;
@@ -296,6 +297,7 @@ __global__ void __launch_bounds__(NTHREADS + 32, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const float lo = __uint_as_float(wv[i] << 16), hi = __uint_as_float(wv[i] & 0xffff0000u);
+          nbad |= f16_out(lo * mul) | f16_out(hi * mul);
           const __half2 a2 = __floats2half2_rn(lo * mul, hi * mul), b2 = __floats2half2_rn(lo * mg, hi * mg);
           wv[i] = *reinterpret_cast<const uint32_t *>(&a2);
           gv[i] = *reinterpret_cast<const uint32_t *>(&b2);
@@ -320,7 +322,10 @@ __global__ void __launch_bounds__(NTHREADS + 32, 1)
           st_chunk_f16(sm.ds16 + kb * 2 * HT + row * 128 + ((chk ^ (row & 7)) * 16), v + q4 * 8);
         }
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= gC;
+        for (int i = 0; i < 32; ++i) {
+          nbad |= f16_out(v[i]);
+          v[i] *= gC;
+        }
         tmem_st32(tm + tl + TM_S + c0, v);
       }
     }
@@ -347,7 +352,10 @@ __global__ void __launch_bounds__(NTHREADS + 32, 1)
         const float4 cb = reinterpret_cast<const float4 *>(G.cdec + c0 + q4 * 8)[1];
         const float cd[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[q4 * 8 + i] = fmaf(cd[i], y[q4 * 8 + i], v[q4 * 8 + i]);
+        for (int i = 0; i < 8; ++i) {
+          v[q4 * 8 + i] = fmaf(cd[i], y[q4 * 8 + i], v[q4 * 8 + i]);
+          nbad |= f16_out(v[q4 * 8 + i]);
+        }
         st_chunk_f16(sm.kc + row * 128 + ((((c0 >> 3) + q4) ^ (row & 7)) * 16), v + q4 * 8);
       }
     }
@@ -386,6 +394,7 @@ __global__ void __launch_bounds__(NTHREADS + 32, 1)
       }
     }
   }
+  if (nbad && err) atomicOr(err, 1);
   if (tid == NTHREADS && store) tma_store_wait_all();
   fence_before();
   __syncthreads();

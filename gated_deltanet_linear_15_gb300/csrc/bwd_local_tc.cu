@@ -359,13 +359,13 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     if (r < nxt.nvalid)
       gb_next = tid < 64 ? a.g[(size_t)(nxt.tok0 + r) * H + nh] : a.beta[(size_t)(nxt.tok0 + r) * H + nh];
   }
-  {  // under P5: per-token sums <Ut, Y>, <dUt, Ut> over d_v (Y and Z stay in T3, T4 until P6; Ut^T from its tile)
-    float t1 = 0.f, t2 = 0.f;
+  {  // under P5: per-token sums <Ut, Y> over d_v (Y stays in T3 until P6; Ut^T from its tile)
+    float t1 = 0.f;
 #pragma unroll 1
     for (int q4 = 0; q4 < 2; ++q4) {
       const int cb = c0 + q4 * 8;
-      float y[8], z[8], u[8], cd[8];
-      tmem_ld8x2(tm + tl + T3 + cb, y, tm + tl + T4 + cb, z);
+      float y[8], u[8];
+      tmem_ld8(tm + tl + T3 + cb, y);
       {
         const uint4 raw = *reinterpret_cast<const uint4 *>(sm.ut + chunk_off(row, cb));
         const __half2 *uh = reinterpret_cast<const __half2 *>(&raw);
@@ -376,21 +376,12 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
           u[2 * i + 1] = f.y;
         }
       }
-      ld8f(G.cdec + cb, cd);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float du = cd[i] * y[i] + z[i];
-        y[i] *= u[i];
-        z[i] = du * u[i];
-      }
-      const float a1 = colsum8(y), a2 = colsum8(z);
-      if ((lane >> 3) == q4) {
-        t1 = a1;
-        t2 = a2;
-      }
+      for (int i = 0; i < 8; ++i) y[i] *= u[i];
+      const float a1 = colsum8(y);
+      if ((lane >> 3) == q4) t1 = a1;
     }
     if (lane < 16) sm.part[wq][c0 + lane] = t1;
-    if (lane < 16) sm.part[4 + wq][c0 + lane] = t2;
   }
   if (wbar_or(!mma_done())) {  // P5
     failed = release = true;
@@ -400,7 +391,6 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     // dP rows (lanes 0-63): Z = dP * P row sums (thread-local) and column sums; dPm over P
     if (row < 64) {
       const int r = row;
-      const float gr = G.gp[r];
       float rs = 0.f, cs = 0.f;
 #pragma unroll 1
       for (int q4 = 0; q4 < 2; ++q4) {
@@ -410,15 +400,15 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
         uint8_t *pp = sm.p + chunk_off(r, cb);
         const uint4 raw = *reinterpret_cast<const uint4 *>(pp);
         const __half *ph = reinterpret_cast<const __half *>(&raw);
-float rg[8];
-        ld8f(G.rgp + cb, rg);
+        float rt[8];
+        gratio8(G, r, cb, rt);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float dpv = v[i];
           const float zz = dpv * __half2float(ph[i]);
           rs += zz;
           zc[i] = zz;
-          y[i] = cb + i <= r ? dpv * gr * rg[i] : 0.f;
+          y[i] = cb + i <= r ? dpv * rt[i] : 0.f;
         }
         st_chunk_f16(pp, y);
         const float a = colsum8(zc);
@@ -448,7 +438,6 @@ float rg[8];
   }
   if (tid < 64) {
     sm.acc[0][tid] = sm.part[0][tid] + sm.part[1][tid] + sm.part[2][tid] + sm.part[3][tid];      // <Ut, Y>
-    sm.acc[1][tid] = sm.part[4][tid] + sm.part[5][tid] + sm.part[6][tid] + sm.part[7][tid];      // <dUt, Ut>
     sm.acc[2][tid] = sm.part[16][tid] + sm.part[17][tid] + sm.part[18][tid] + sm.part[19][tid];  // row sums of dP * P
     sm.acc[3][tid] = sm.part[10][tid] + sm.part[11][tid];  // column sums of dP * P
   }
@@ -485,12 +474,15 @@ float rg[8];
   }
   {
     // M1, M2 (lanes 0-63 = r): dAhat = beta_i (M1 + Gamma M2); beta column sums colsum_i(Ahat (M1 + Gamma M2));
-    // colsum_i(Ahat M1) (the dW'^T X1 part of dk^ dotted with k^); colsum_i(X2 M2) = <dV, v> (dV = X2^T dUt,
-    // M2 = dUt V^T); X2 is read before dAhat replaces it
+    // colsum_i(Ahat M1) (the dW'^T X1 part of dk^ dotted with k^).  Gate terms: <dW_r, W_r> =
+    // rowsum_r(beta Ahat M1) and the row and column sums of X2 * M2 (X2 = Gamma Ahat diag(beta), M2 =
+    // dUt V^T) over the strictly lower triangle only: a diagonal ratio gamma_r / gamma_r does not depend
+    // on the gates, and leaving it out of both sums keeps the small gate gradient of a strongly decaying
+    // chunk from being the difference of two large, differently rounded numbers.  X2 is read before dAhat
+    // replaces it
     if (row < 64) {
       const int r = row;
-      const float gr = G.gp[r];
-      float cs = 0.f, ca = 0.f, cv = 0.f;
+      float cs = 0.f, ca = 0.f, cv = 0.f, rwx = 0.f;
 #pragma unroll 1
       for (int q4 = 0; q4 < 2; ++q4) {
         const int cb = c0 + q4 * 8;
@@ -500,17 +492,18 @@ float rg[8];
         const __half *hh = reinterpret_cast<const __half *>(&raw);
         const uint4 xraw = *reinterpret_cast<const uint4 *>(sm.x2 + chunk_off(r, cb));
         const __half *xh = reinterpret_cast<const __half *>(&xraw);
-        float rg[8], bt[8];
-        ld8f(G.rgp + cb, rg);
+        float rt[8], bt[8];
+        gratio8(G, r, cb, rt);
         ld8f(gbeta + cb, bt);
         float am[8], xm[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int col = cb + i;
           const float hv = __half2float(hh[i]);
-          const float x = m1[i] + (col <= r ? m2[i] * gr * rg[i] : 0.f);
+          const float x = m1[i] + (col <= r ? m2[i] * rt[i] : 0.f);
           am[i] = hv * m1[i];
-          xm[i] = __half2float(xh[i]) * m2[i];
+          xm[i] = col < r ? __half2float(xh[i]) * m2[i] : 0.f;
+          rwx += bt[i] * am[i] + xm[i];
           m2[i] = hv * x;
           m1[i] = bt[i] * x;
         }
@@ -525,9 +518,9 @@ float rg[8];
       if (lane < 16) sm.part[8 + wq][c0 + lane] = cs;
       if (lane < 16) sm.part[10 + wq][c0 + lane] = ca;
       if (lane < 16) sm.part[14 + wq][c0 + lane] = cv;
+      sm.part[4 + wg][r] = rwx;  // row terms, per 16-column block
     }
   }
-  if (tid < 128) (tid < 64 ? sm.g[gbuf ^ 1] : sm.beta[gbuf ^ 1])[tid & 63] = gb_next;  // next item's g, beta
   if (tid < 128) (tid < 64 ? sm.g[gbuf ^ 1] : sm.beta[gbuf ^ 1])[tid & 63] = gb_next;  // next item's g, beta
   fence_before();
   fence_async_smem();
@@ -538,7 +531,8 @@ float rg[8];
   if (tid < 64) {
     sm.acc[6][tid] = sm.part[8][tid] + sm.part[9][tid];    // beta col terms
     sm.acc[7][tid] = sm.part[10][tid] + sm.part[11][tid];  // colsum(Ahat M1)
-    sm.acc[4][tid] = sm.part[14][tid] + sm.part[15][tid];  // <dV, v>
+    sm.acc[4][tid] = sm.part[14][tid] + sm.part[15][tid];  // strictly lower column sums of X2 * M2
+    sm.acc[1][tid] = sm.part[4][tid] + sm.part[5][tid] + sm.part[6][tid] + sm.part[7][tid];  // <dW, W> + rows of X2 * M2
   }
   {  // K^ -> wt (dUt^T is dead): R9 reads k^ there, so the K/Q buffer is free once P9 is done
     const uint4 *src = reinterpret_cast<const uint4 *>(sm.kq);
@@ -651,29 +645,38 @@ float rg[8];
   }
   // ---- gate and beta gradients
   if (warp == LWARPS - 1) {  // under P9 (the other warps' shadow work is the k^ . dk^ sum)
-    float dGv[2];
-    float sumy = 0.f;
+    // dg_t = sum_{r >= t} dG_r + gam_C <dS, S0> + sum_{r < t} y_r: dG_r holds the terms whose decay factor
+    // starts or ends at r (gamma_r of the inter-chunk output and of W; the ratios of P and X2, diagonal
+    // excluded); the state terms y_r = cdec_r <Ut_r, Y_r> depend on g_t only for r < t (through cdec_r),
+    // so they enter by a forward exclusive scan (not as a total minus a reverse partial sum)
+    float dGv[2], yv[2];
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const int r = lane + 32 * t;
-      const float y = G.cdec[r] * sm.acc[0][r];
-      sumy += y;
-      dGv[t] = sm.acc[1][r] + sm.acc[2][r] - sm.acc[3][r] + sm.acc[5][r] - sm.acc[4][r] - y;
+      yv[t] = G.cdec[r] * sm.acc[0][r];
+      dGv[t] = sm.acc[1][r] + sm.acc[2][r] - sm.acc[3][r] + sm.acc[5][r] - sm.acc[4][r];
     }
-    sumy = warp_sum(sumy);
     float red = 0.f;
     for (int i = 0; i < LWARPS; ++i) red += sm.red[i];
-    if (lane == 31) dGv[1] += sumy + G.gamC * red;
-    float hi = dGv[1], lo = dGv[0];
+    float hi = dGv[1], lo = dGv[0], ylo = yv[0], yhi = yv[1];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const float yh = __shfl_down_sync(0xffffffffu, hi, o), yl = __shfl_down_sync(0xffffffffu, lo, o);
+      const float fl = __shfl_up_sync(0xffffffffu, ylo, o), fh = __shfl_up_sync(0xffffffffu, yhi, o);
       if (lane + o < 32) {
         hi += yh;
         lo += yl;
       }
+      if (lane >= o) {
+        ylo += fl;
+        yhi += fh;
+      }
     }
     lo += __shfl_sync(0xffffffffu, hi, 0);
+    yhi += __shfl_sync(0xffffffffu, ylo, 31);
+    const float base = G.gamC * red;
+    lo += base + (ylo - yv[0]);
+    hi += base + (yhi - yv[1]);
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const int r = lane + 32 * t;

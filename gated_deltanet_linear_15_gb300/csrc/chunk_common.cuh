@@ -38,12 +38,14 @@ __device__ __forceinline__ void load_scalars(float *dst, const float *base, int 
 // In place, one warp per row: raw input values x (type I) become operand values
 // (type E)  x * mul / sqrt(sum x^2 + 1e-6)  when `l2`, else  x * mul.  The
 // normalisation's row reduction uses warp shuffles; `norm_out` (optional)
-// receives the norm of each row.
+// receives the norm of each row.  Returns true when one of this thread's values
+// does not fit an fp16 operand (numeric guard; always false for fp32 operands).
 template <typename I, typename E, int D>
-__device__ __forceinline__ void prep_rows(E *t, int ld, float mul, bool l2, float *norm_out) {
+__device__ __forceinline__ bool prep_rows(E *t, int ld, float mul, bool l2, float *norm_out) {
   static_assert(sizeof(I) == sizeof(E), "in-place conversion needs equal element sizes");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const I *src = reinterpret_cast<const I *>(t);
+  bool bad = false;
   for (int r = warp; r < CH; r += NWARPS) {
     float x[D / 32];
     float ss = 0.f;
@@ -61,8 +63,12 @@ __device__ __forceinline__ void prep_rows(E *t, int ld, float mul, bool l2, floa
     }
     __syncwarp();
 #pragma unroll
-    for (int i = 0; i < D / 32; ++i) t[r * ld + lane + 32 * i] = fromf<E>(x[i] * f);
+    for (int i = 0; i < D / 32; ++i) {
+      if (std::is_same<E, f16>::value) bad |= f16_out(x[i] * f);
+      t[r * ld + lane + 32 * i] = fromf<E>(x[i] * f);
+    }
   }
+  return bad;
 }
 
 // Gate quantities of one chunk from the raw log-gates g[0..CH) (one warp).
@@ -72,11 +78,29 @@ __device__ __forceinline__ void prep_rows(E *t, int ld, float mul, bool l2, floa
 //   cdec_r = exp(G_last - G_r)             (decay from token r to the chunk end)
 // Each exponential is taken once per token (onedev.kr FlashQLA talk summary,
 // paragraph on SFU load: the diagonal scaling is pulled out of the inverse).
-// Returns true in lane 0 if |G_r - G_mid| exceeds the factoring range.
+// The decay ratio gamma_r / gamma_c (c <= r) is then gp_r * rgp_c.  The pages
+// put no lower bound on alpha in (0, 1) (same page, paragraph on the effective
+// sliding window), so a chunk can decay by more than fp32 can factor: when
+// |G_r - G_mid| exceeds FACTOR_RANGE for some r, gp or rgp would overflow and
+// the chunk is marked `pw`; its ratios are then taken pairwise as
+// exp(G_r - G_c) (C^2 / 2 exponentials, for that chunk only).  Log-gates below
+// GATE_FLOOR are raised to it: exp(GATE_FLOOR) and every ratio across such a
+// token are zero in fp32 either way, and the prefix sums keep their precision.
+// The prefix sums are taken in fp64 and each exponent argument (a difference
+// of two prefix sums) is formed in fp64 before its fp32 exponential: a chunk
+// can hold a large decay (|G| ~ 100) followed by slow decay, and there fp32
+// prefix sums would lose the small differences that the ratios need.
 struct __align__(16) Gates {
-  float G[CH], gam[CH], gp[CH], rgp[CH], cdec[CH];
+  double G[CH];
+  float gam[CH], gp[CH], rgp[CH], cdec[CH];
   float gamC;  // exp(G_last)
+  int pw;      // nonzero: take decay ratios pairwise (the span leaves the factoring range)
 };
+
+// gamma_r / gamma_c for c <= r (callers mask c > r themselves)
+__device__ __forceinline__ float gratio(const Gates &gt, int r, int c) {
+  return gt.pw ? expf((float)(gt.G[r] - gt.G[c])) : gt.gp[r] * gt.rgp[c];
+}
 
 // 16 consecutive floats from 16-byte aligned shared memory (four vector loads)
 __device__ __forceinline__ void ld16f(const float *p, float (&v)[16]) {
@@ -92,34 +116,50 @@ __device__ __forceinline__ void ld16f(const float *p, float (&v)[16]) {
 
 __device__ __forceinline__ bool gate_prefix(const float *g, Gates &gt) {
   const int lane = threadIdx.x & 31;
-  float a = g[lane], b = g[lane + 32];
+  double a = fmaxf(g[lane], GATE_FLOOR), b = fmaxf(g[lane + 32], GATE_FLOOR);
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const float ya = __shfl_up_sync(0xffffffffu, a, o);
-    const float yb = __shfl_up_sync(0xffffffffu, b, o);
+    const double ya = __shfl_up_sync(0xffffffffu, a, o);
+    const double yb = __shfl_up_sync(0xffffffffu, b, o);
     if (lane >= o) {
       a += ya;
       b += yb;
     }
   }
-  const float Gmid = __shfl_sync(0xffffffffu, a, 31);
+  const double Gmid = __shfl_sync(0xffffffffu, a, 31);
   b += Gmid;
-  const float Glast = __shfl_sync(0xffffffffu, b, 31);
+  const double Glast = __shfl_sync(0xffffffffu, b, 31);
   gt.G[lane] = a;
   gt.G[lane + 32] = b;
-  gt.gam[lane] = expf(a);
-  gt.gam[lane + 32] = expf(b);
-  gt.gp[lane] = expf(a - Gmid);
-  gt.gp[lane + 32] = expf(b - Gmid);
-  gt.rgp[lane] = expf(Gmid - a);
-  gt.rgp[lane + 32] = expf(Gmid - b);
-  gt.cdec[lane] = expf(Glast - a);
-  gt.cdec[lane + 32] = expf(Glast - b);
-  if (lane == 0) gt.gamC = expf(Glast);
-  float rng = fmaxf(fabsf(a - Gmid), fabsf(b - Gmid));
+  gt.gam[lane] = expf((float)a);
+  gt.gam[lane + 32] = expf((float)b);
+  gt.gp[lane] = expf((float)(a - Gmid));
+  gt.gp[lane + 32] = expf((float)(b - Gmid));
+  gt.rgp[lane] = expf((float)(Gmid - a));
+  gt.rgp[lane + 32] = expf((float)(Gmid - b));
+  gt.cdec[lane] = expf((float)(Glast - a));
+  gt.cdec[lane + 32] = expf((float)(Glast - b));
+  if (lane == 0) gt.gamC = expf((float)Glast);
+  float rng = fmaxf(fabsf((float)(a - Gmid)), fabsf((float)(b - Gmid)));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) rng = fmaxf(rng, __shfl_xor_sync(0xffffffffu, rng, o));
-  return rng > FACTOR_RANGE;
+  const bool pw = rng > FACTOR_RANGE;
+  if (lane == 0) gt.pw = pw;
+  return pw;
+}
+
+// o[i] = gamma_r / gamma_{cb + i} for cb + i <= r, 0 above the diagonal (eight columns from cb, a multiple of 8)
+__device__ __forceinline__ void gratio8(const Gates &gt, int r, int cb, float (&o)[8]) {
+  if (!gt.pw) {
+    const float4 a = reinterpret_cast<const float4 *>(gt.rgp + cb)[0], b = reinterpret_cast<const float4 *>(gt.rgp + cb)[1];
+    const float gr = gt.gp[r];
+    o[0] = gr * a.x; o[1] = gr * a.y; o[2] = gr * a.z; o[3] = gr * a.w;
+    o[4] = gr * b.x; o[5] = gr * b.y; o[6] = gr * b.z; o[7] = gr * b.w;
+  } else {
+    const double Gr = gt.G[r];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = cb + i <= r ? expf((float)(Gr - gt.G[cb + i])) : 0.f;
+  }
 }
 
 // Ahat entry (a, b) from the transposed upper-triangle storage written by wy_inverse<., true>.

@@ -230,6 +230,13 @@ struct Plan {
 constexpr float LN_EPS_WINDOW = -16.635532f;  // ln(2^-24)
 constexpr int WMAX = 8;                        // longest warm-up, in chunks
 constexpr float FACTOR_RANGE = 80.f;           // |G_r - G_mid| limit of the gamma factoring
+constexpr float GATE_FLOOR = -128.f;           // log-gates below this decay to zero in fp32 anyway
+constexpr float F16_MAX = 65504.f;             // largest finite fp16 value
+
+// Numeric guard of the fp16 operands: true when x is not finite or would not fit fp16.  The kernels
+// test the values that become operands (widened inputs, chunk-start states, dS, Ut, dUt) and set
+// status bit 0 when one fails.
+__device__ __forceinline__ bool f16_out(float x) { return !(fabsf(x) <= F16_MAX); }
 
 enum StartMode { START_INIT = 0, START_WARMUP = 1, START_FIXUP = 2 };
 

@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_chunk_kernel(FwdArgs a) {
 
   // ---- initial state into registers (fp32) and its E copy
   Acc<SWM, SWN> Sacc;
+  bool nbad = false;  // numeric guard: an fp16 operand out of range
   {
     const float *src = nullptr;
     if (transition) {
@@ -149,12 +150,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_chunk_kernel(FwdArgs a) {
         *reinterpret_cast<uint4 *>(dst + (size_t)r * D + cc) = *reinterpret_cast<const uint4 *>(&sm.s[r * LD + cc]);
       }
     }
-    prep_rows<I, E, D>(sm.k, LD, 1.f, l2, nullptr);
-    if (emit) prep_rows<I, E, D>(sm.q, LD, a.scale, l2, nullptr);
-    if (need_v) prep_rows<I, E, D>(sm.v, LD, 1.f, false, nullptr);
-    if (warp == 0) {
-      if (gate_prefix(sm.g, sm.gt) && lane == 0 && a.status) atomicOr(a.status, 1);
-    }
+    nbad |= prep_rows<I, E, D>(sm.k, LD, 1.f, l2, nullptr);
+    if (emit) nbad |= prep_rows<I, E, D>(sm.q, LD, a.scale, l2, nullptr);
+    if (need_v) nbad |= prep_rows<I, E, D>(sm.v, LD, 1.f, false, nullptr);
+    if (warp == 0) gate_prefix(sm.g, sm.gt);
     __syncthreads();
 
     // ---- K~ = diag(cdec) K, and [K; Q] K^T  ->  N (fp32) and P (E)
@@ -176,7 +175,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_chunk_kernel(FwdArgs a) {
       } else {
         acc.each([&](int r, int cc, float &v) {
           const int row = m0 + r, col = n0 + cc;
-          sm.p[row * LC + col] = fromf<E>(col <= row ? v * sm.gt.gp[row] * sm.gt.rgp[col] : 0.f);
+          sm.p[row * LC + col] = fromf<E>(col <= row ? v * gratio(sm.gt, row, col) : 0.f);
         });
       }
     }
@@ -184,10 +183,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_chunk_kernel(FwdArgs a) {
 
     wy_inverse<std::is_same<E, float>::value, false>(sm.nf, LN, sm.beta, sm.ys,
                                                      [&](int r, int c, float a0, float a1) {
-      const float b0 = sm.beta[c], b1 = sm.beta[c + 1], gr = sm.gt.gp[r];
+      const float b0 = sm.beta[c], b1 = sm.beta[c + 1];
       st2(&sm.x1[r * LC + c], a0 * b0, a1 * b1);
-      st2(&sm.x2[r * LC + c], c <= r ? a0 * b0 * (gr * sm.gt.rgp[c]) : 0.f,
-          c + 1 <= r ? a1 * b1 * (gr * sm.gt.rgp[c + 1]) : 0.f);
+      st2(&sm.x2[r * LC + c], c <= r ? a0 * b0 * gratio(sm.gt, r, c) : 0.f,
+          c + 1 <= r ? a1 * b1 * gratio(sm.gt, r, c + 1) : 0.f);
     });
 
     // ---- U (warps 0-3, registers) and -W (warps 4-7, shared)
@@ -247,7 +246,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_chunk_kernel(FwdArgs a) {
     __syncthreads();
 
     // ---- state copy for the next chunk, output rows to HBM
-    Sacc.pairs([&](int r, int cc, float &v0, float &v1) { st2(&sm.s[(wr * SWM + r) * LD + wc * SWN + cc], v0, v1); });
+    Sacc.pairs([&](int r, int cc, float &v0, float &v1) {
+      if (std::is_same<E, f16>::value) nbad |= f16_out(v0) | f16_out(v1);
+      st2(&sm.s[(wr * SWM + r) * LD + wc * SWN + cc], v0, v1);
+    });
     if (emit) {
       I *og = static_cast<I *>(a.o);
       const I *ostage = reinterpret_cast<const I *>(sm.w);
@@ -262,6 +264,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_chunk_kernel(FwdArgs a) {
     }
   }
 
+  if (nbad && a.status) atomicOr(a.status, 1);
   // ---- end-of-segment state
   float *dst = nullptr;
   if (a.pass == 0) {

@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(PT, 2)
   fence_after();
   const uint32_t tm = sm.tmem_base;
   bool pend = item < n_items;  // a q, k, v load in flight
+  bool nbad = false;           // numeric guard: a widened operand out of fp16 range
   uint32_t it = 0;             // parity of both barriers: one completion each per item
 
   for (; item < n_items; ++it) {
@@ -129,7 +130,7 @@ __global__ void __launch_bounds__(PT, 2)
     // the previous item's X1, X2, Ahat, P stores have read their staging (rewritten below)
     if (tid == 0) tma_store_wait_read();
     __syncthreads();
-    if (warp == 0 && gate_prefix(sm.g, sm.gt) && lane == 0 && err) atomicOr(err, 1);
+    if (warp == 0) gate_prefix(sm.g, sm.gt);
     const bool tma_ok = mbar_wait(u32(&sm.bar_tma), it & 1, err, 8);
     pend = false;
     if (__syncthreads_or(!tma_ok)) break;
@@ -174,8 +175,9 @@ __global__ void __launch_bounds__(PT, 2)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const uint32_t w = raw[4 * cc + i];
-          const __half2 a2 =
-              __floats2half2_rn(__uint_as_float(w << 16) * mul, __uint_as_float(w & 0xffff0000u) * mul);
+          const float lo = __uint_as_float(w << 16) * mul, hi = __uint_as_float(w & 0xffff0000u) * mul;
+          nbad |= f16_out(lo) | f16_out(hi);
+          const __half2 a2 = __floats2half2_rn(lo, hi);
           y[i] = *reinterpret_cast<const uint32_t *>(&a2);
         }
         *reinterpret_cast<uint4 *>(rowp + (((ch0 + cc) ^ (r & 7)) * 16)) = make_uint4(y[0], y[1], y[2], y[3]);
@@ -194,8 +196,9 @@ __global__ void __launch_bounds__(PT, 2)
         uint32_t *w = reinterpret_cast<uint32_t *>(&q4);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const __half2 a2 =
-              __floats2half2_rn(__uint_as_float(w[i] << 16) * mul, __uint_as_float(w[i] & 0xffff0000u) * mul);
+          const float lo = __uint_as_float(w[i] << 16) * mul, hi = __uint_as_float(w[i] & 0xffff0000u) * mul;
+          nbad |= f16_out(lo) | f16_out(hi);
+          const __half2 a2 = __floats2half2_rn(lo, hi);
           w[i] = *reinterpret_cast<const uint32_t *>(&a2);
         }
         *reinterpret_cast<uint4 *>(rowp + ((chk ^ (r & 7)) * 16)) = q4;
@@ -256,14 +259,14 @@ __global__ void __launch_bounds__(PT, 2)
         }
       } else {
         const int r = row - 64;
-        const float gr = sm.gt.gp[r];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          float w8[8];
+          float w8[8], rt[8];
+          gratio8(sm.gt, r, c0 + 8 * q, rt);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int c = c0 + 8 * q + i;
-            w8[i] = c <= r ? v[8 * q + i] * gr * sm.gt.rgp[c] : 0.f;
+            w8[i] = c <= r ? v[8 * q + i] * rt[i] : 0.f;
           }
           st_chunk_f16(sm.p + chunk_off(r, c0 + 8 * q), w8);
         }
@@ -276,12 +279,12 @@ __global__ void __launch_bounds__(PT, 2)
     const float *beta = sm.beta;
     const Gates &G = sm.gt;
     wy_inverse<false, false>(sm.nf, LN, beta, sm.ys, [&](int r, int c, float a0, float a1) {
-      const float2 bb = *reinterpret_cast<const float2 *>(beta + c), rg = *reinterpret_cast<const float2 *>(G.rgp + c);
-      const float gr = G.gp[r], x0 = a0 * bb.x, x1 = a1 * bb.y;
+      const float2 bb = *reinterpret_cast<const float2 *>(beta + c);
+      const float x0 = a0 * bb.x, x1 = a1 * bb.y;
       const uint32_t off = sw128_offset(r, c);
       *reinterpret_cast<__half2 *>(sm.x1 + off) = __floats2half2_rn(x0, x1);
       *reinterpret_cast<__half2 *>(sm.x2 + off) =
-          __floats2half2_rn(c <= r ? x0 * (gr * rg.x) : 0.f, c + 1 <= r ? x1 * (gr * rg.y) : 0.f);
+          __floats2half2_rn(c <= r ? x0 * gratio(G, r, c) : 0.f, c + 1 <= r ? x1 * gratio(G, r, c + 1) : 0.f);
       *reinterpret_cast<__half2 *>(sm.ah + off) = __floats2half2_rn(a0, a1);
     }, it == 0);  // ends with a proxy fence and a barrier; the zero upper blocks persist across items
 
@@ -294,6 +297,7 @@ __global__ void __launch_bounds__(PT, 2)
     }
     item = nitem;
   }
+  if (nbad && err) atomicOr(err, 1);
   if (tid == 0) {
     if (pend) mbar_wait(u32(&sm.bar_tma), it & 1, err, 8);  // a load in flight lands before the CTA leaves
     tma_store_wait_all();  // the stores have read shared memory before the CTA leaves

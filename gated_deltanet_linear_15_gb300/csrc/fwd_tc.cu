@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(FT + 32, 1)
       break;
     }
     if (it == 0) {  // later chunks had their gates prepared during the previous chunk
-      if (warp == 0 && gate_prefix(sm.g[stage], G) && lane == 0 && err) atomicOr(err, 1);
+      if (warp == 0) gate_prefix(sm.g[stage], G);
       named_bar_sync<2, FT>();
     }
     // ---- S0 -> its fp16 operand form (rows = d_v), gam_C * S0 back into TMEM; warp w takes lane quarter
@@ -380,8 +380,13 @@ __global__ void __launch_bounds__(FT + 32, 1)
       const int kb = c0 >> 6;
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) st_chunk_f16(sm.s0 + kb * 2 * HT + chunk_off(row, c0 + q4 * 8), v + q4 * 8);
+      bool bad = false;  // numeric guard: the fp16 state copy out of range
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] *= gC;
+      for (int i = 0; i < 32; ++i) {
+        bad |= f16_out(v[i]);
+        v[i] *= gC;
+      }
+      if (bad && err) atomicOr(err, 1);
       tmem_st32(tm + tm_lane + TM_S + c0, v);
     }
     {  // MMA 2 (its own barrier, one completion per chunk)
@@ -416,6 +421,10 @@ __global__ void __launch_bounds__(FT + 32, 1)
       const int c0 = wg * 16;
       float v[16];
       tmem_ld16(tm + tm_lane + TM_U + c0, v);
+      bool bad = false;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) bad |= f16_out(v[i]);
+      if (bad && err) atomicOr(err, 1);
       st_chunk_f16(sm.wu + chunk_off(row, c0), v);
       st_chunk_f16(sm.wu + chunk_off(row, c0 + 8), v + 8);
       float cd[16];
@@ -436,7 +445,7 @@ __global__ void __launch_bounds__(FT + 32, 1)
       gn[lane] = gnext0;
       gn[lane + 32] = gnext1;
       __syncwarp();
-      if (gate_prefix(gn, sm.gt[stage ^ 1]) && lane == 0 && err) atomicOr(err, 1);
+      gate_prefix(gn, sm.gt[stage ^ 1]);
     }
     failed |= !mma_wait();  // MMA 4
     named_bar_sync<3, FT + 32>();  // the Ut^T store has read wu

@@ -142,8 +142,7 @@ int launch_plan(const Plan &p, const int *cu, int N, int T, int Lseg, int S_max,
 // One block per global chunk: the chunk's log-gates of 32 heads at a time are
 // staged in shared memory with coalesced row loads (tokens are rows of H gates),
 // then one warp per head scans its 64 values: gsum[c, h] = sum of g over the
-// chunk's tokens; status bit 0 if the centred in-chunk prefix leaves the range
-// of the gamma factoring.
+// chunk's tokens (each g raised to GATE_FLOOR first, as in the chunk kernels).
 __device__ void fixup_modes(const Plan &p, const float *gsum, int H, int Lseg, int S_max, unsigned flags, int *status,
                             int i0, int stride);
 
@@ -169,7 +168,7 @@ __global__ void __launch_bounds__(256) gate_scan_kernel(Plan p, const float *g, 
     for (int r = warp; r < CH; r += 8) tile[r][lane] = (r < nvalid && hh < H) ? g[(size_t)(tok0 + r) * H + hh] : 0.f;
     __syncthreads();
     for (int hl = warp; hl < 32 && h0 + hl < H; hl += 8) {
-      float a = tile[lane][hl], b = tile[lane + 32][hl];
+      float a = fmaxf(tile[lane][hl], GATE_FLOOR), b = fmaxf(tile[lane + 32][hl], GATE_FLOOR);
       for (int o = 1; o < 32; o <<= 1) {
         const float ya = __shfl_up_sync(0xffffffffu, a, o), yb = __shfl_up_sync(0xffffffffu, b, o);
         if (lane >= o) {
@@ -180,12 +179,7 @@ __global__ void __launch_bounds__(256) gate_scan_kernel(Plan p, const float *g, 
       const float Gmid = __shfl_sync(0xffffffffu, a, 31);
       b += Gmid;
       const float Glast = __shfl_sync(0xffffffffu, b, 31);
-      float rng = fmaxf(fabsf(a - Gmid), fabsf(b - Gmid));
-      for (int o = 16; o > 0; o >>= 1) rng = fmaxf(rng, __shfl_xor_sync(0xffffffffu, rng, o));
-      if (lane == 0) {
-        gsum[(size_t)c * H + h0 + hl] = Glast;
-        if (rng > FACTOR_RANGE && status) atomicOr(status, 1);
-      }
+      if (lane == 0) gsum[(size_t)c * H + h0 + hl] = Glast;
     }
     __syncthreads();
   }

@@ -16,7 +16,15 @@ so GPU runs generate on the GPU and CPU tests on the CPU):
   unit sphere (a Gaussian divided by its norm), for runs with normalisation
   off.
 * v ~ N(0, 1); beta = sigmoid(N(0, 1)); dO ~ N(0, 1).
-* log-gate g: per-workload law (uniform, or -softplus(N(0,1) - 2)).
+* log-gate g: per-workload law (uniform, or -softplus(N(0,1) - 2)).  Extra laws
+  for strong decay, which the pages allow (alpha in (0, 1) with no lower bound):
+  ``uniform_8_2`` g ~ U[-8, -2]; ``alpha0_heads`` g = -1e4 (alpha = 0 in any
+  float format) in even heads and -softplus(N(0,1) - 2) in odd ones;
+  ``runs_0_6`` per head, runs of 17 tokens with g ~ U[-1e-3, 0] (alpha ~ 1)
+  alternating with runs of 17 tokens at g = -6, the phase shifted per head.
+* ``beta_one=True`` sets beta = 1; ``repeat_keys=m`` makes token t's key (and
+  query) the one drawn for token t mod m of the same sequence and head, so
+  the same key recurs (the overwrite case of the delta rule).
 * S0 ~ N(0, 0.02^2) where a workload carries an initial state.
 * varlen lengths: integers uniform on [512, 16384], inclusive.
 
@@ -88,6 +96,19 @@ def _gate(law: str, shape, H: int, gen: torch.Generator, device) -> torch.Tensor
         return torch.where(head < 6, fast, slow)
     if law == "zero":
         return torch.zeros(shape, device=device, dtype=torch.float32)
+    if law == "uniform_8_2":
+        u = torch.rand(shape, generator=gen, device=device, dtype=torch.float32)
+        return -8.0 + 6.0 * u
+    if law == "alpha0_heads":
+        z = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+        head = torch.arange(H, device=device).view(*([1] * (len(shape) - 1)), H)
+        return torch.where(head % 2 == 0, torch.full_like(z, -1e4), -torch.nn.functional.softplus(z - 2.0))
+    if law == "runs_0_6":
+        u = torch.rand(shape, generator=gen, device=device, dtype=torch.float32)
+        t = torch.arange(shape[-2], device=device).view(*([1] * (len(shape) - 2)), shape[-2], 1)
+        head = torch.arange(H, device=device).view(*([1] * (len(shape) - 1)), H)
+        fast = ((t + 7 * head) // 17) % 2 == 1
+        return torch.where(fast, torch.full_like(u, -6.0), -1e-3 * u)
     raise ValueError(f"unknown gate law {law}")
 
 
@@ -98,7 +119,8 @@ def _unit(x: torch.Tensor) -> torch.Tensor:
 def make_inputs(w: Workload | str, device="cpu", *, T: Optional[int] = None, H: Optional[int] = None,
                 B: Optional[int] = None, seqlens: Optional[list[int]] = None, seed: Optional[int] = None,
                 unit_keys: bool = False, with_dST: bool = False, gate: Optional[str] = None,
-                dtype: Optional[str] = None, D: Optional[int] = None, with_S0: Optional[bool] = None):
+                dtype: Optional[str] = None, D: Optional[int] = None, with_S0: Optional[bool] = None,
+                beta_one: bool = False, repeat_keys: int = 0):
     """Return a dict of tensors for workload ``w`` (optionally with overridden sizes).
 
     Keys: q, k, v [B, T, H, D] (or [1, sum(L), H, D] for varlen), g, beta
@@ -140,10 +162,18 @@ def make_inputs(w: Workload | str, device="cpu", *, T: Optional[int] = None, H: 
 
     q = randn(shp)
     k = randn(shp)
+    if repeat_keys:
+        idx = torch.arange(Tdim, device=device) % repeat_keys
+        if cu is not None:   # within each packed sequence
+            starts = torch.repeat_interleave(cu[:-1].long(), torch.tensor(seqlens, device=device))
+            idx = starts + (torch.arange(Tdim, device=device) - starts) % repeat_keys
+        q, k = q[:, idx], k[:, idx]
     if unit_keys:
         q, k = _unit(q), _unit(k)
     v = randn(shp)
     beta = torch.sigmoid(randn((B, Tdim, H)))
+    if beta_one:
+        beta = torch.ones_like(beta)
     g = _gate(law, (B, Tdim, H), H, gen, device)
     S0 = 0.02 * randn((N, H, D, D)) if has_S0 else None
     if has_S0 and w.name == "tiny_fp32" and T is None:

@@ -30,6 +30,13 @@
  *    launch returns GDN_ERR_CUDA.  gdn_last_error_string() (thread-local)
  *    gives a one-line reason.
  *  - Results are deterministic (no floating-point atomics).
+ *  - Log-gates: g = log(alpha) with alpha in (0, 1) per (token, head), any
+ *    depth of decay (onedev.kr talk summary, paragraph on the effective sliding
+ *    window, puts no lower bound on alpha).  Values below -128 act as -128: the
+ *    decay across such a token is zero in fp32 either way.  A chunk whose
+ *    in-chunk decay span is too wide for the factored form of the decay
+ *    ratios takes them pairwise (see the forward below); results are the same
+ *    up to rounding.
  */
 #ifndef GDN_H_
 #define GDN_H_
@@ -50,7 +57,9 @@ enum {
   GDN_ERR_INVALID_ARG = 1, /* bad pointer, shape, stride or alignment                 */
   GDN_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. d not in {64, 128})      */
   GDN_ERR_WORKSPACE = 3,   /* workspace NULL or smaller than the size query          */
-  GDN_ERR_CUDA = 4         /* a CUDA call or kernel launch failed                     */
+  GDN_ERR_CUDA = 4,        /* a CUDA call or kernel launch failed                     */
+  GDN_ERR_TIMEOUT = 5,     /* device side: a bounded wait expired (status bits 2, 3)  */
+  GDN_ERR_NUMERIC = 6      /* device side: an fp16 operand overflowed (status bit 0)  */
 };
 
 enum {
@@ -93,6 +102,11 @@ size_t gdn_bwd_workspace_size(const gdn_shape *shape);
  * corrected (state from zero plus the composed d_k x d_k transition --
  * paragraph on parallelism); the sequential start-state fix-up; pass B, the
  * fused WY + state pass + output over every segment.
+ * Decay ratios gamma_r / gamma_i inside a chunk are factored as
+ * exp(G_r - G_mid) exp(G_mid - G_i) (G = in-chunk prefix of g, G_mid its
+ * value at the chunk middle), one exponential per token (same page, paragraph
+ * on SFU load); a chunk with |G_r - G_mid| > 80 for some r, where a factor
+ * would leave fp32, takes exp(G_r - G_i) pairwise instead.
  */
 int gdn_chunk_fwd(const gdn_shape *shape,
                   const void *q, const void *k, const void *v,
@@ -119,6 +133,13 @@ int gdn_chunk_fwd(const gdn_shape *shape,
  *  - All calls share the one array: calls that overlap on the GPU (other
  *    streams, other threads) race and must be serialised by the caller.
  *  - No cudaMalloc, cudaFree or allocating library routine is called.
+ *  - A first call on a device made while `stream` is being captured returns
+ *    GDN_ERR_INVALID_ARG and launches nothing.
+ *  - The looked-up address is kept for the life of the process: after
+ *    cudaDeviceReset (or any loss of the device's primary context) it is stale,
+ *    and the library must not be called on that device again.
+ *  - The device status word of the last call is read with
+ *    gdn_get_device_status(shape, NULL, stream).
  */
 #define GDN_STATIC_SCRATCH_BYTES (16u << 20)
 int gdn_chunk_fwd_static(const gdn_shape *shape,
@@ -220,16 +241,25 @@ int gdn_recurrent_fwd(const gdn_shape *shape, const void *q, const void *k, cons
 /* Reads the device status word that the kernels of the last call on `stream`
  * set (synchronises the stream).  Every bit means the outputs of that call are
  * not reliable:
- *   bit 0 (1): a chunk's in-chunk log-decay span exceeded the range of the
- *              gamma factoring (|G_r - G_mid| > 80);
+ *   bit 0 (1): numeric guard -- a value that becomes an fp16 tensor-core
+ *              operand (q, k, v or dO widened from bf16, a chunk-start state,
+ *              dS, Ut or dUt) was not finite or beyond +-65504;
  *   bit 1 (2): cu_seqlens is not non-decreasing, or describes more chunks or
  *              segments than the workspace was sized for;
  *   bit 2 (4): a tensor-core completion wait ran past its iteration limit (the
  *              kernel stopped that work item and returned);
  *   bit 3 (8): a TMA tile-load wait ran past its iteration limit (likewise).
  * Returns the word (0 = clean), or -1 on a CUDA error.  `workspace` is the one
- * passed to that call. */
+ * passed to that call, or NULL for a call of gdn_chunk_fwd_static (then the
+ * word is read from the static scratch on the current device).  The status
+ * lives in the caller's workspace because the library allocates nothing, which
+ * is why this takes the workspace and not the stream alone. */
 int gdn_get_device_status(const gdn_shape *shape, const void *workspace, gdn_stream_t stream);
+
+/* Maps a status word of gdn_get_device_status to one status code: GDN_OK (0),
+ * GDN_ERR_INVALID_ARG (bit 1), GDN_ERR_TIMEOUT (bits 2, 3), GDN_ERR_NUMERIC
+ * (bit 0), in that order of precedence; GDN_ERR_CUDA for -1. */
+int gdn_device_status_code(int word);
 
 /* The segment plan for this shape on the current device: chunks per segment,
  * an upper bound on the number of segments, and on the number of chunks. */

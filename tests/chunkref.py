@@ -89,30 +89,38 @@ def chunk_bwd(Q, K, V, g, beta, S0, dO, dS1):
     Y = K @ dS1.T                                  # C x dv
     dUt = P.T @ dO + c[:, None] * Y
     dS0 = gam[-1] * dS1 + dO.T @ (gam[:, None] * Q) - dUt.T @ W
-    # output / state local terms
+    # Gate gradient.  dG_r collects the terms whose decay factor starts or ends at token r: the
+    # derivative of gamma_r (decay from the chunk start) and of each ratio gamma_r / gamma_i
+    # (i < r: + at r, - at i; the diagonal ratio is 1 and contributes nothing, so it is left out
+    # of every row and column sum).  dg_t = sum_{r >= t} dG_r, plus the state terms, which depend
+    # on g_t through gamma_C (every t) and through c_r = gamma_C / gamma_r for r < t only.
+    lo = np.tril(np.ones((Cn, Cn)), -1)
     dQ = gam[:, None] * (dO @ S0)
     dG = (dQ * Q).sum(1)                          # gamma_r <dO_r, S0 q_r>
     dP = dO @ Ut.T
-    Z = dP * P
+    Z = dP * P * lo
     dG += Z.sum(1) - Z.sum(0)
     dPm = Gam * dP
     dQ += dPm @ K
     dK = dPm.T @ Q + c[:, None] * (Ut @ dS1)
-    y = c * (Ut * Y).sum(1)
-    dG[-1] += gam[-1] * (dS1 * S0).sum() + y.sum()
-    dG -= y
-    # through Ut = U - W S0^T  (W and U rows both carry gamma_r on the left)
+    y = c * (Ut * Y).sum(1)                       # c_r <dS_C, ut_r k_r^T>
+    # through Ut = U - W S0^T, with W = diag(gamma) Ahat diag(beta) K and U = X2 V,
+    # X2 = Gamma * Ahat diag(beta)
     dW = -dUt @ S0
     dU = dUt
-    dG += (dUt * Ut).sum(1)                       # = <dW_r, W_r> + <dU_r, U_r>
     dWp = gam[:, None] * dW
+    M1 = dWp @ K.T                                # gamma_r <dW_r, k_i>
+    M2 = dU @ V.T                                 # <dU_r, v_i>
+    X2 = Gam * Ahat * beta[None, :]
+    dG += (Ahat * M1 * beta[None, :]).sum(1)      # <dW_r, W_r>
+    XM = X2 * M2 * lo
+    dG += XM.sum(1) - XM.sum(0)
     dUp = gam[:, None] * dU
     AdW = Ahat.T @ dWp
     AdU = Ahat.T @ dUp
     dK += beta[:, None] * AdW
     dV = (beta / gam)[:, None] * AdU
     dbeta = (K * AdW).sum(1) + (V * AdU).sum(1) / gam
-    dG -= (dV * V).sum(1)
     dAhat = dWp @ (beta[:, None] * K).T + dUp @ ((beta / gam)[:, None] * V).T
     dT = -Ahat.T @ dAhat @ Ahat.T
     N = np.tril(K @ K.T, -1)
@@ -120,7 +128,7 @@ def chunk_bwd(Q, K, V, g, beta, S0, dO, dS1):
     dbeta += (dTl * N).sum(1)
     dN = beta[:, None] * dTl
     dK += (dN + dN.T) @ K                          # dA and dA^T batched into one product with K
-    dg = np.cumsum(dG[::-1])[::-1]
+    dg = np.cumsum(dG[::-1])[::-1] + gam[-1] * (dS1 * S0).sum() + (np.cumsum(y) - y)
     return dQ, dK, dV, dg, dbeta, dS0
 
 

@@ -51,6 +51,17 @@ def _fwd(lib, s, ptr=0x10000, ws_bytes=1 << 40, q=None):
 def test_status_strings(lib):
     assert lib.gdn_status_string(0) == b"ok"
     assert lib.gdn_status_string(2) == b"unsupported configuration"
+    assert b"wait" in lib.gdn_status_string(_lib.GDN_ERR_TIMEOUT)
+    assert b"fp16" in lib.gdn_status_string(_lib.GDN_ERR_NUMERIC)
+
+
+@pytest.mark.parametrize("word,code", [
+    (0, _lib.GDN_OK), (1, _lib.GDN_ERR_NUMERIC), (2, _lib.GDN_ERR_INVALID_ARG), (3, _lib.GDN_ERR_INVALID_ARG),
+    (4, _lib.GDN_ERR_TIMEOUT), (8, _lib.GDN_ERR_TIMEOUT), (5, _lib.GDN_ERR_TIMEOUT), (-1, _lib.GDN_ERR_CUDA),
+])
+def test_device_status_code(lib, word, code):
+    """Status words map to one code: malformed cu_seqlens first, then an expired wait, then the numeric guard."""
+    assert lib.gdn_device_status_code(word) == code
 
 
 @pytest.mark.parametrize("kw,code", [

@@ -1,23 +1,25 @@
 """Full-size workloads in the launch configuration the bench times (automatic
-segment plan), checked against the oracle on sampled (sequence, head) pairs,
-plus the Euler-homogeneity identities of the backward over every element."""
-import numpy as np
+segment plan), both training pairs, compared with the oracle element by element
+over every (sequence, head) of the prefill, training and long-context
+workloads, and over every sequence of four heads of the packed varlen batch
+(whose fp64 copies of all 32 heads would take tens of GB of host memory); plus
+the Euler-homogeneity identities of the backward over every element.  The raw
+and adjusted margins of each output are printed at the end of the session."""
 import pytest
 import torch
 
-import oracle
 from gdn_inputs import make_inputs
-from tests.gpu_util import TOL, rel_err, run_gpu
+from tests.gpu_util import TOL, compare, run_gpu, run_oracle
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
-# (workload, sampled (sequence, head) pairs)
+# (workload, heads compared; None = all)
 CASES = [
-    ("prefill_h32_t8192", [(0, 0), (0, 31)]),
-    ("train_b4_h16_t4096", [(0, 0), (3, 15)]),
-    ("long_h8_t65536", [(0, 2), (0, 7)]),        # a decaying head and an alpha ~ 1 head
-    ("varlen_n16_h32", None),                      # shortest and longest sequence
+    ("prefill_h32_t8192", None),
+    ("train_b4_h16_t4096", None),
+    ("long_h8_t65536", None),
+    ("varlen_n16_h32", [0, 7, 20, 31]),
 ]
 
 
@@ -27,38 +29,26 @@ def _built():
     __graft_entry__.build()
 
 
-def _slice(x, n, h):
-    cu = x["cu_seqlens"]
-    if cu is None:
-        sl = lambda t: t[n:n + 1, :, h:h + 1]
-    else:
-        a, b = int(cu[n]), int(cu[n + 1])
-        sl = lambda t: t[:, a:b, h:h + 1]
-    return sl
+def _heads(t, heads, state=False):
+    """Select heads of a [B, T, H, ...] tensor (or a [N, H, D, D] state) on the CPU."""
+    if t is None:
+        return None
+    t = t.detach().cpu()
+    return t[:, heads].contiguous() if state else t[:, :, heads].contiguous()
 
 
-@pytest.mark.parametrize("name,pairs", CASES, ids=[c[0] for c in CASES])
-def test_full_size_sampled(name, pairs):
+@pytest.mark.parametrize("name,heads", CASES, ids=[c[0] for c in CASES])
+def test_full_size_every_sequence_and_head(name, heads):
     x = make_inputs(name, DEV)
     runs = {"recompute": run_gpu(x), "saved": run_gpu(x, saved=True)}
-    if pairs is None:
-        lens = np.array(x["seqlens"])
-        pairs = [(int(lens.argmin()), 3), (int(lens.argmax()), 20)]
-    for n, h in pairs:
-        sl = _slice(x, n, h)
-        S0 = None if x["S0"] is None else x["S0"][n:n + 1, h:h + 1]
-        ro, rS = oracle.fwd(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["g"]), sl(x["beta"]), S0, scale=x["scale"],
-                            l2norm=x["l2norm"])
-        rg = oracle.bwd(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["g"]), sl(x["beta"]), sl(x["dO"]), S0, None,
-                        scale=x["scale"], l2norm=x["l2norm"])
-        for mode, got in runs.items():
-            errs = {"o": rel_err(sl(got["o"]), ro), "S_T": rel_err(got["S_T"][n:n + 1, h:h + 1], rS)}
-            for key in ("dq", "dk", "dv", "dg", "dbeta"):
-                errs[key] = rel_err(sl(got[key]), rg[key])
-            if S0 is not None:
-                errs["dS0"] = rel_err(got["dS0"][n:n + 1, h:h + 1], rg["dS0"])
-            bad = {k: v for k, v in errs.items() if not v <= TOL["bf16"]}
-            assert not bad, f"{name} ({mode}) seq {n} head {h}: {bad} (all {errs})"
+    heads = list(range(x["H"])) if heads is None else heads
+    xs = {k: _heads(x[k], heads) for k in ("q", "k", "v", "g", "beta", "dO")}
+    xs.update(S0=_heads(x["S0"], heads, True), dST=None, cu_seqlens=x["cu_seqlens"], scale=x["scale"],
+              l2norm=x["l2norm"])
+    ref = run_oracle(xs)
+    for mode, got in runs.items():
+        sel = {k: _heads(got[k], heads, k in ("S_T", "dS0")) for k in got if got[k] is not None}
+        compare(sel, ref, TOL["bf16"], label=f"full {name} ({mode})")
 
 
 def test_homogeneity_full_prefill():

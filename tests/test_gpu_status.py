@@ -50,3 +50,29 @@ def test_forced_wait_expiry_sets_status_and_returns():
     torch.cuda.synchronize()  # the kernels returned: no hang
     assert g.gdn_get_device_status(shape, ws) & 4
     _clean_call_is_correct(x)
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_numeric_guard_forward(D):
+    """A value beyond fp16's range in v (|v| ~ 1e5, fine in bf16) cannot become an fp16 tensor-core
+    operand: the forward sets status bit 0 (GDN_ERR_NUMERIC) instead of returning silent infinities."""
+    x = make_inputs("prefill_h32_t8192", "cuda", T=130, H=2, D=D, seed=23)
+    x["v"][0, 70, 1, 5] = 1e5
+    shape = g.make_shape(x["q"], x["v"], scale=x["scale"], l2norm=x["l2norm"])
+    rc, _, _, ws = _fwd(x, shape)
+    assert rc == 0
+    word = g.gdn_get_device_status(shape, ws)
+    assert word & 1
+    assert g.gdn_device_status_code(word) == _lib.GDN_ERR_NUMERIC
+    _clean_call_is_correct(make_inputs("prefill_h32_t8192", "cuda", T=130, H=2, D=D, seed=23))
+
+
+def test_numeric_guard_backward():
+    """The same guard on dO in the backward (widened where the reverse chain converts it)."""
+    x = make_inputs("train_b4_h16_t4096", "cuda", B=1, T=130, H=2, seed=24)
+    x["dO"][0, 100, 0, 3] = -1e5
+    shape = g.make_shape(x["q"], x["v"], scale=x["scale"], l2norm=x["l2norm"])
+    ws = torch.empty(g.gdn_bwd_workspace_size(shape), dtype=torch.uint8, device="cuda")
+    g.chunk_gated_delta_rule_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["dO"], x["S0"], None, None,
+                                 x["scale"], x["l2norm"], workspace=ws)
+    assert g.gdn_get_device_status(shape, ws) & 1
