@@ -217,6 +217,78 @@ def run_reference(args):
     return 0
 
 
+# ----------------------------------------------------------------------------- segment-length sweep
+def run_sweep(args, g, x, dev):
+    """Saved-context fwd + bwd timed per segment length (CUDA events around each call, 256 MB L2 flush
+    before every step, outside the events), with the per-kernel table of one profiled pass and the
+    library's own estimate for the plan (gdn_plan_estimate).  One JSON line per length."""
+    import torch
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    N, H, D = x["N"], x["H"], x["D"]
+    o = torch.empty_like(x["v"])
+    ST = torch.empty(N, H, D, D, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"])
+    dg, db = torch.empty_like(x["g"]), torch.empty_like(x["beta"])
+    dS0 = torch.empty_like(x["S0"]) if x["S0"] is not None else None
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    time.sleep(0.3)
+    for L in [int(v) for v in args.sweep_seg_chunks.split(",")]:
+        shape = g.make_shape(x["q"], x["v"], cu_seqlens=x["cu_seqlens"], scale=x["scale"], l2norm=x["l2norm"],
+                             seg_chunks=L)
+        plan = g.gdn_plan_query(shape)
+        est = g.gdn_plan_estimate(shape)
+        ws_bytes = max(g.gdn_fwd_workspace_size(shape), g.gdn_bwd_saved_workspace_size(shape))
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        saved_bytes = g.gdn_saved_size(shape)
+        saved = torch.empty(max(saved_bytes, 256), dtype=torch.uint8, device=dev)
+
+        def fwd():
+            rc = g.gdn_chunk_fwd_save(shape, x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], o, ST, saved, ws,
+                                      saved_bytes, ws_bytes, stream)
+            assert rc == 0, g._lib.last_error()
+
+        def bwd():
+            rc = g.gdn_chunk_bwd_saved(shape, x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], x["dO"], x["dST"],
+                                       dq, dk, dv, dg, db, dS0, saved, ws, saved_bytes, ws_bytes, stream)
+            assert rc == 0, g._lib.last_error()
+
+        for _ in range(args.warmup):
+            flush.zero_()
+            fwd()
+            bwd()
+        g.gdn_profile_report(reset=True)
+        g.gdn_profile_only(None)
+        g.gdn_profile_enable(True)
+        flush.zero_()
+        fwd()
+        bwd()
+        torch.cuda.synchronize()
+        g.gdn_profile_enable(False)
+        kern = g.gdn_profile_report(reset=True)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for e in evs:
+            flush.zero_()
+            e[0].record(stream)
+            fwd()
+            e[1].record(stream)
+            bwd()
+            e[2].record(stream)
+        torch.cuda.synchronize()
+        fwd_ms = statistics.median(a.elapsed_time(b) for a, b, c in evs)
+        bwd_ms = statistics.median(b.elapsed_time(c) for a, b, c in evs)
+        print(json.dumps({"sweep": args.workload, "seg_chunks_requested": L, "seg_chunks": plan["seg_chunks"],
+                          "max_segments": plan["max_segments"], "fwd_ms": round(fwd_ms, 4),
+                          "bwd_ms": round(bwd_ms, 4), "step_ms": round(fwd_ms + bwd_ms, 4),
+                          "estimate_us": est,
+                          "kernels_ms": {k: round(ms / c, 4) for k, (c, ms) in kern.items()}}), flush=True)
+        del ws, saved
+    print(json.dumps({"sweep_clocks": clocks.stop()}), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------------------- decode arm
 def run_decode(args):
     """gdn_recurrent_fwd on B sequences x T tokens (H=32, d=128, bf16, fp32 state updated in place).
@@ -287,6 +359,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-tokens", type=int, default=None, help="tokens per sequence in the reference sample")
     ap.add_argument("--seg-chunks", type=int, default=0)
+    ap.add_argument("--sweep-seg-chunks", default="",
+                    help="comma-separated segment lengths (0 = the automatic plan): time the saved-context pair "
+                         "for each and print one JSON line per length instead of the bench line")
     ap.add_argument("--recompute", action="store_true",
                     help="time the stateless pair (the backward recomputes the chunk states and WY tiles) "
                          "instead of the saved-context pair")
@@ -326,6 +401,8 @@ def main():
 
     w = WORKLOADS[args.workload]
     x = make_inputs(w, dev, seed=replica_seed(w.seed, rank))
+    if args.sweep_seg_chunks:
+        return run_sweep(args, g, x, dev)
     shape = g.make_shape(x["q"], x["v"], cu_seqlens=x["cu_seqlens"], scale=x["scale"], l2norm=x["l2norm"],
                          seg_chunks=args.seg_chunks)
     plan = g.gdn_plan_query(shape)

@@ -28,7 +28,7 @@ from ._lib import (GDN_BF16, GDN_FP32, GDN_L2NORM_QK, GDN_SP_OFF, GDN_WINDOW_OFF
 
 __all__ = ["GdnShape", "make_shape", "gdn_chunk_fwd", "gdn_chunk_fwd_static", "gdn_chunk_bwd", "gdn_fwd_workspace_size",
            "gdn_bwd_workspace_size", "gdn_saved_size", "gdn_bwd_saved_workspace_size", "gdn_chunk_fwd_save",
-           "gdn_chunk_bwd_saved", "gdn_plan_query", "gdn_get_device_status", "gdn_device_status_code",
+           "gdn_chunk_bwd_saved", "gdn_plan_query", "gdn_plan_estimate", "gdn_get_device_status", "gdn_device_status_code",
            "gdn_profile_enable", "gdn_profile_only", "gdn_profile_report",
            "chunk_gated_delta_rule_fwd", "chunk_gated_delta_rule_bwd", "chunk_gated_delta_rule",
            "GDN_L2NORM_QK", "GDN_SP_OFF", "GDN_WINDOW_OFF"]
@@ -86,6 +86,13 @@ def gdn_plan_query(shape: GdnShape):
     _check(_lib.load().gdn_plan_query(ctypes.byref(shape), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)),
            "gdn_plan_query")
     return dict(seg_chunks=a.value, max_segments=b.value, max_chunks=c.value)
+
+
+def gdn_plan_estimate(shape: GdnShape):
+    """The library's modelled time (µs) of the forward state pass and the backward reverse chain."""
+    f, b = ctypes.c_double(), ctypes.c_double()
+    _check(_lib.load().gdn_plan_estimate(ctypes.byref(shape), ctypes.byref(f), ctypes.byref(b)), "gdn_plan_estimate")
+    return dict(fwd_us=round(f.value, 2), bwd_us=round(b.value, 2))
 
 
 def gdn_chunk_fwd(shape: GdnShape, q, k, v, g, beta, S0, o, S_T, workspace, workspace_bytes: int = None,

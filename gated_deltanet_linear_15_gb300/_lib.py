@@ -18,7 +18,7 @@ GDN_STATIC_SCRATCH_BYTES = 16 << 20
 EXPORTS = ("gdn_fwd_workspace_size", "gdn_bwd_workspace_size", "gdn_chunk_fwd", "gdn_chunk_fwd_static",
            "gdn_chunk_bwd", "gdn_saved_size", "gdn_bwd_saved_workspace_size", "gdn_chunk_fwd_save",
            "gdn_chunk_bwd_saved", "gdn_recurrent_fwd",
-           "gdn_get_device_status", "gdn_device_status_code", "gdn_plan_query", "gdn_profile_enable", "gdn_profile_report", "gdn_profile_only",
+           "gdn_get_device_status", "gdn_device_status_code", "gdn_plan_query", "gdn_plan_estimate", "gdn_profile_enable", "gdn_profile_report", "gdn_profile_only",
            "gdn_status_string", "gdn_last_error_string")
 
 
@@ -78,6 +78,8 @@ def load():
         lib.gdn_plan_query.argtypes = [S, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
                                        ctypes.POINTER(ctypes.c_int)]
         lib.gdn_plan_query.restype = ctypes.c_int
+        lib.gdn_plan_estimate.argtypes = [S, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
+        lib.gdn_plan_estimate.restype = ctypes.c_int
         lib.gdn_profile_enable.argtypes = [ctypes.c_int]
         lib.gdn_profile_enable.restype = ctypes.c_int
         lib.gdn_profile_report.argtypes = [ctypes.c_char_p, ctypes.c_size_t, ctypes.c_int]

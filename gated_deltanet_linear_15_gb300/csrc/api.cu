@@ -1,7 +1,9 @@
 // C ABI of the library: argument validation, workspace layout, segment-length
 // choice and the launch sequence of the forward and backward passes.
 #include <algorithm>
+#include <array>
 #include <cmath>
+#include <functional>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -66,30 +68,100 @@ struct Layout {
   size_t fwd_core = 0, fwd_total = 0, bwd_total = 0;
 };
 
-// Chunks per segment.  One CTA per (segment, head) runs a serial chain over its
-// chunks, so with few (sequence, head) pairs the sequences are split until the
-// work items fill the SMs (onedev.kr FlashQLA talk summary, paragraph on
-// parallelism: one head per SM leaves most of a >100-SM card idle).  Estimated
-// time ~ waves(items) * (chunks per segment + ~2 warm-up chunks).
+// Modelled time of the two recurrent passes (the forward's state pass and the backward's reverse
+// chain) for L chunks per segment.  One CTA per (segment, head) walks its chunks serially and holds a
+// whole SM, and the hardware starts the CTAs in launch order (segments of a head, heads in turn) on
+// whichever SM frees first, so the pass takes the makespan of that list on the SMs.  An item costs a
+// fixed part plus its chunks, plus kWarmChunks warm-up chunks for a segment that does not start its
+// sequence (the window case of the gate scan; the exact case adds a pass A that the host cannot
+// foresee, since it depends on the gates).  The constants are a least-squares fit to GB300 timings of
+// the tcgen05 kernels over 23 segment lengths of the H = 32, T = 8192 prefill (bench.py
+// --sweep-seg-chunks: within 4 % of every measured length); the d = 64 and fp32 kernels are costed the
+// same way.  Packed batches, whose lengths the host does not see, are costed in whole waves of an
+// average item.
+struct PassCost {
+  double item_us, chunk_us, warm_us;
+};
+constexpr PassCost kFwdPass = {3.0, 4.95, 5.0}, kChainPass = {11.0, 4.0, 0.5};
+constexpr int kWarmChunks = 2;
+
+void plan_cost_us(const gdn_shape &s, int N, int maxc, int CH_max, int L, double *fwd_us, double *bwd_us) {
+  const int slots = num_sms();
+  L = std::max(1, std::min(L, maxc));
+  const int S = (maxc + L - 1) / L;
+  const long items = s.cu_seqlens ? (long)std::ceil(s.H * ((double)CH_max / L + 0.5 * N)) : (long)N * s.H * S;
+  if (s.cu_seqlens || items > 16L * slots) {
+    const double waves = std::ceil((double)items / slots);
+    const double warm = L < maxc ? kWarmChunks : 0.0;
+    *fwd_us = waves * (kFwdPass.item_us + L * kFwdPass.chunk_us + warm * kFwdPass.warm_us);
+    *bwd_us = waves * (kChainPass.item_us + L * kChainPass.chunk_us + warm * kChainPass.warm_us);
+    return;
+  }
+  double out[2];
+  for (int pass = 0; pass < 2; ++pass) {
+    const PassCost &pc = pass ? kChainPass : kFwdPass;
+    std::vector<double> sm(std::min<long>(slots, items), 0.0);  // a min-heap of the SMs' free times
+    for (long i = 0; i < items; ++i) {
+      const int j = (int)(i % S);  // launch order: the segments of one (sequence, head), then the next
+      const int len = std::min(L, maxc - j * L), warm = j ? std::min(kWarmChunks, j * L) : 0;
+      const double d = pc.item_us + len * pc.chunk_us + warm * pc.warm_us;
+      if ((long)i < (long)sm.size()) {
+        sm[i] = d;
+        std::push_heap(sm.begin(), sm.begin() + i + 1, std::greater<double>());
+      } else {
+        std::pop_heap(sm.begin(), sm.end(), std::greater<double>());
+        sm.back() += d;
+        std::push_heap(sm.begin(), sm.end(), std::greater<double>());
+      }
+    }
+    out[pass] = *std::max_element(sm.begin(), sm.end());
+  }
+  *fwd_us = out[0];
+  *bwd_us = out[1];
+}
+
+// Chunks per segment.  With few (sequence, head) pairs the sequences are split until the work items
+// fill the SMs (onedev.kr FlashQLA talk summary, paragraph on parallelism: one head per SM leaves most
+// of a >100-SM card idle); the length minimises the modelled time of the two recurrent passes over the
+// lengths that give each segment count its shortest longest segment, up to 16 waves of items.  Results
+// are cached per shape class (the plan is chosen on every call).
 int choose_lseg(const gdn_shape &s, int N, int maxc, int CH_max) {
   if (maxc <= 0) return 1;
   if (s.flags & GDN_SP_OFF) return maxc;
   if (s.seg_chunks > 0) return s.seg_chunks;
   const int slots = num_sms();
   if ((long)N * s.H >= slots) return maxc;
+  static std::mutex mu;
+  static std::vector<std::array<long, 6>> cache;  // {N, H, maxc, CH_max, packed, SMs}
+  static std::vector<int> cached;
+  const std::array<long, 6> key = {N, s.H, maxc, CH_max, s.cu_seqlens != nullptr, slots};
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (size_t i = 0; i < cache.size(); ++i)
+      if (cache[i] == key) return cached[i];
+  }
   int best = maxc;
   double best_cost = 1e300;
-  for (int L = 1; L <= maxc; ++L) {
-    double items;
-    if (s.cu_seqlens) items = (double)s.H * ((double)CH_max / L + 0.5 * N);
-    else items = (double)N * s.H * ((maxc + L - 1) / L);
-    const double waves = std::ceil(items / slots);
-    const double cost = waves * (L + (L < maxc ? 2.0 : 0.0));
-    if (cost < best_cost - 1e-9) {
-      best_cost = cost;
+  int prevL = 0;
+  for (int S = 1; S <= maxc; ++S) {
+    const int L = (maxc + S - 1) / S;
+    if (L == prevL) continue;
+    prevL = L;
+    if ((long)N * s.H * S > 16L * slots) break;
+    double f, b;
+    plan_cost_us(s, N, maxc, CH_max, L, &f, &b);
+    if (f + b < best_cost - 1e-9) {
+      best_cost = f + b;
       best = L;
     }
   }
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache.size() > 256) {
+    cache.clear();
+    cached.clear();
+  }
+  cache.push_back(key);
+  cached.push_back(best);
   return best;
 }
 
@@ -830,6 +902,18 @@ int gdn_device_status_code(int word) {
   if (word & 2) return GDN_ERR_INVALID_ARG;
   if (word & (4 | 8)) return GDN_ERR_TIMEOUT;
   if (word & 1) return GDN_ERR_NUMERIC;
+  return GDN_OK;
+}
+
+int gdn_plan_estimate(const gdn_shape *shape, double *fwd_us, double *bwd_us) {
+  Layout L;
+  int rc = make_layout(shape, L);
+  if (rc) return rc;
+  const int maxc = shape->cu_seqlens ? (int)((L.Ttot + CH - 1) / CH) : (shape->T + CH - 1) / CH;
+  double f = 0.0, b = 0.0;
+  if (maxc > 0) plan_cost_us(*shape, L.N, maxc, L.CH_max, std::min(L.Lseg, maxc), &f, &b);
+  if (fwd_us) *fwd_us = f;
+  if (bwd_us) *bwd_us = b;
   return GDN_OK;
 }
 

@@ -255,14 +255,27 @@ __device__ void fixup_modes(const Plan &p, const float *gsum, int H, int Lseg, i
   if (bwd_fix) atomicOr(status + 2, 1);
 }
 
-// grid (D / FIX_ROWS, H, N); FIX_ROWS rows of the state per CTA, 256 threads.
+// Start-state fix-up (forward: S_start[j+1] = S_start[j] M_j + E_j over the segments of one (sequence,
+// head); the reverse chain mirrors it), the sequential composition of the segment summaries
+// (onedev.kr talk summary, paragraph on parallelism).  grid (D / FIX_ROWS, H, N): FIX_ROWS rows of the
+// state per CTA, 256 threads.  The composition is serial over segments, but every step's inputs (M_j
+// and E_j's rows) are independent of the chain, so they stream through a two-stage shared-memory ring
+// by cp.async: step i computes while step i + 1's 64 KB transition lands.  The segment start modes
+// (which segments take the fix-up at all) are decided up front, one segment per thread.
 constexpr int FIX_ROWS = 8;
+constexpr int FIX_MODES = 2048;  // segments per sequence whose modes are kept in shared memory
+
+template <int D> constexpr size_t fixup_smem_bytes() { return 2 * ((size_t)D * D + FIX_ROWS * D) * sizeof(float); }
 
 template <int D>
-__global__ void __launch_bounds__(256, 4) fixup_kernel(FixupArgs a) {
+__global__ void __launch_bounds__(256, 1) fixup_kernel(FixupArgs a) {
   pdl_trigger();
   pdl_wait();
+  extern __shared__ __align__(16) float fx_sm[];  // 2 stages of [M (D x D) | E rows (FIX_ROWS x D)]
   __shared__ float cur[FIX_ROWS][D];
+  __shared__ signed char fix_mode[FIX_MODES];  // per segment: 0 no fix-up, 1 fix-up from E alone, 2 from E and M
+  __shared__ int nwork;
+  __shared__ short work[FIX_MODES];            // target segment of each working step, in chain order
   const int rb = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
   const int H = a.H;
   if (a.fixflag && *a.fixflag == 0) return;  // no segment of this direction needs the exact fix-up
@@ -273,67 +286,122 @@ __global__ void __launch_bounds__(256, 4) fixup_kernel(FixupArgs a) {
   const bool window = !(a.flags & kFlagWindowOff);
   const size_t DD = (size_t)D * D;
   constexpr int CPT = D / 32;  // columns per thread
-  const int r = threadIdx.x >> 5;
-  const int c0 = (threadIdx.x & 31) * CPT;
+  const int tid = threadIdx.x;
+  const int r = tid >> 5;
+  const int c0 = (tid & 31) * CPT;
   const int row = rb * FIX_ROWS + r;
-  for (int step = 0; step < nseg - 1; ++step) {
-    int jt, js, mt, ms, w;
-    if (!a.reverse) {
-      jt = step + 1;
-      js = jt - 1;
-      mt = fwd_start_mode(a.gsum, H, h, chunk0, jt * a.Lseg, jt, window, &w);
-      if (mt != START_FIXUP) continue;
-      ms = fwd_start_mode(a.gsum, H, h, chunk0, js * a.Lseg, js, window, &w);
-    } else {
-      jt = nseg - 2 - step;
-      js = jt + 1;
-      mt = bwd_start_mode(a.gsum, H, h, chunk0, min((jt + 1) * a.Lseg, nchunks), nchunks, jt, nseg, window, &w);
-      if (mt != START_FIXUP) continue;
-      ms = bwd_start_mode(a.gsum, H, h, chunk0, min((js + 1) * a.Lseg, nchunks), nchunks, js, nseg, window, &w);
-    }
-    const size_t src = ((size_t)(seg0 + js) * H + h) * DD;
-    float acc[CPT];
-#pragma unroll
-    for (int t = 0; t < CPT; ++t) acc[t] = a.E[src + (size_t)row * D + c0 + t];
-    if (ms == START_FIXUP) {
-      // cur holds the corrected state of segment js (computed in the previous step)
-      const float *M = a.M + src;
-      // 8 rows of M in flight per step of the loop (the loads are independent; only the sums chain)
-#pragma unroll 8
-      for (int k = 0; k < D; ++k) {
-        const float x = cur[r][k];
-        float m[CPT];
-        if constexpr (CPT == 4) {
-          const float4 t4 = *reinterpret_cast<const float4 *>(M + (size_t)k * D + c0);
-          m[0] = t4.x;
-          m[1] = t4.y;
-          m[2] = t4.z;
-          m[3] = t4.w;
-        } else {
-          const float2 t2 = *reinterpret_cast<const float2 *>(M + (size_t)k * D + c0);
-          m[0] = t2.x;
-          m[1] = t2.y;
-        }
-#pragma unroll
-        for (int t = 0; t < CPT; ++t) acc[t] = fmaf(x, m[t], acc[t]);
-      }
-    }
+  // mode of segment j as the target of a fix-up step: is its start (end, reversed) corrected, and is the
+  // segment it is composed from itself corrected (then its transition M takes part)
+  auto start_mode = [&](int j) {
+    int w;
+    if (!a.reverse) return fwd_start_mode(a.gsum, H, h, chunk0, j * a.Lseg, j, window, &w);
+    return bwd_start_mode(a.gsum, H, h, chunk0, min((j + 1) * a.Lseg, nchunks), nchunks, j, nseg, window, &w);
+  };
+  const bool small = nseg <= FIX_MODES;
+  if (small) {
+    for (int j = tid; j < nseg; j += blockDim.x) fix_mode[j] = start_mode(j) == START_FIXUP;
     __syncthreads();
-    float *out = a.out + ((size_t)(seg0 + jt) * H + h) * DD + (size_t)row * D;
-#pragma unroll
-    for (int t = 0; t < CPT; ++t) {
-      cur[r][c0 + t] = acc[t];
-      out[c0 + t] = acc[t];
+    if (tid == 0) {  // working steps in chain order: target jt, composed from js (forward js = jt - 1)
+      int nw = 0;
+      for (int step = 0; step < nseg - 1; ++step) {
+        const int jt = a.reverse ? nseg - 2 - step : step + 1, js = a.reverse ? jt + 1 : jt - 1;
+        if (fix_mode[jt]) work[nw++] = (short)(fix_mode[js] ? jt | 0x4000 : jt);
+      }
+      nwork = nw;
     }
     __syncthreads();
   }
+  const int nw = small ? nwork : nseg - 1;
+  // step i -> (target jt, uses M); for very long plans the modes are evaluated on the fly
+  auto step_of = [&](int i, int &jt, bool &withM) {
+    if (small) {
+      const int v = work[i];
+      jt = v & 0x3fff;
+      withM = (v & 0x4000) != 0;
+      return true;
+    }
+    jt = a.reverse ? nseg - 2 - i : i + 1;
+    if (start_mode(jt) != START_FIXUP) return false;
+    withM = start_mode(a.reverse ? jt + 1 : jt - 1) == START_FIXUP;
+    return true;
+  };
+  auto issue = [&](int i) {  // cp.async of step i's M (if used) and E rows into stage i & 1
+    int jt;
+    bool withM;
+    if (i < nw && step_of(i, jt, withM)) {
+      const int js = a.reverse ? jt + 1 : jt - 1;
+      const size_t src = ((size_t)(seg0 + js) * H + h) * DD;
+      float *st = fx_sm + (size_t)(i & 1) * (DD + FIX_ROWS * D);
+      if (withM)
+        for (int e = tid; e < (int)(DD / 4); e += blockDim.x) cp_async16(st + 4 * e, a.M + src + 4 * e, true);
+      for (int e = tid; e < FIX_ROWS * D / 4; e += blockDim.x)
+        cp_async16(st + DD + 4 * e, a.E + src + (size_t)rb * FIX_ROWS * D + 4 * e, true);
+    }
+    cp_async_commit();  // one group per step, empty or not
+  };
+  issue(0);
+  issue(1);
+  for (int i = 0; i < nw; ++i) {
+    int jt;
+    bool withM;
+    const bool active = step_of(i, jt, withM);
+    asm volatile("cp.async.wait_group 1;\n" ::: "memory");  // step i's group has landed (i + 1's may be in flight)
+    __syncthreads();
+    if (active) {
+      const float *st = fx_sm + (size_t)(i & 1) * (DD + FIX_ROWS * D);
+      float acc[CPT];
+#pragma unroll
+      for (int t = 0; t < CPT; ++t) acc[t] = st[DD + r * D + c0 + t];
+      if (withM) {  // cur holds the corrected state of the source segment (the previous working step)
+#pragma unroll 8
+        for (int k = 0; k < D; ++k) {
+          const float x = cur[r][k];
+          float m[CPT];
+          if constexpr (CPT == 4) {
+            const float4 t4 = *reinterpret_cast<const float4 *>(st + (size_t)k * D + c0);
+            m[0] = t4.x;
+            m[1] = t4.y;
+            m[2] = t4.z;
+            m[3] = t4.w;
+          } else {
+            const float2 t2 = *reinterpret_cast<const float2 *>(st + (size_t)k * D + c0);
+            m[0] = t2.x;
+            m[1] = t2.y;
+          }
+#pragma unroll
+          for (int t = 0; t < CPT; ++t) acc[t] = fmaf(x, m[t], acc[t]);
+        }
+      }
+      __syncthreads();  // every thread has read cur and this stage
+      float *out = a.out + ((size_t)(seg0 + jt) * H + h) * DD + (size_t)row * D;
+#pragma unroll
+      for (int t = 0; t < CPT; ++t) {
+        cur[r][c0 + t] = acc[t];
+        out[c0 + t] = acc[t];
+      }
+    } else {
+      __syncthreads();
+    }
+    issue(i + 2);  // into the stage just read
+  }
+  asm volatile("cp.async.wait_all;\n" ::: "memory");
 }
 
 int launch_fixup(const FixupArgs &a, int N, cudaStream_t st) {
   if (N == 0) return 0;
   dim3 grid(a.D / FIX_ROWS, a.H, N);
-  if (a.D == 128) return (int)launch_pdl(fixup_kernel<128>, grid, dim3(256), 0, st, a);
-  if (a.D == 64) return (int)launch_pdl(fixup_kernel<64>, grid, dim3(256), 0, st, a);
+  if (a.D == 128) {
+    const size_t smem = fixup_smem_bytes<128>();
+    cudaError_t e = cudaFuncSetAttribute(fixup_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return (int)e;
+    return (int)launch_pdl(fixup_kernel<128>, grid, dim3(256), smem, st, a);
+  }
+  if (a.D == 64) {
+    const size_t smem = fixup_smem_bytes<64>();
+    cudaError_t e = cudaFuncSetAttribute(fixup_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return (int)e;
+    return (int)launch_pdl(fixup_kernel<64>, grid, dim3(256), smem, st, a);
+  }
   return -1;
 }
 

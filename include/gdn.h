@@ -265,6 +265,13 @@ int gdn_device_status_code(int word);
  * an upper bound on the number of segments, and on the number of chunks. */
 int gdn_plan_query(const gdn_shape *shape, int *seg_chunks, int *max_segments, int *max_chunks);
 
+/* The library's cost model of that plan: the modelled time in microseconds of the forward's state
+ * pass and of the backward's reverse chain on the current device (the passes whose length the
+ * segment plan sets; the chunk-parallel kernels do not depend on it).  The automatic plan is the
+ * segment length that minimises their sum.  The model's constants are GB300 measurements; the
+ * paragraph on parallelism of the onedev.kr talk summary calls the pages' own split model coarse. */
+int gdn_plan_estimate(const gdn_shape *shape, double *fwd_us, double *bwd_us);
+
 /* Diagnostics for benchmarks: when enabled, every kernel launch of the library
  * is bracketed by CUDA events (from a pool created on the first enable) on its
  * stream.  gdn_profile_report() waits for the recorded events and writes one
