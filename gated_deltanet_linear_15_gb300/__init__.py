@@ -58,7 +58,7 @@ def _check(rc: int, what: str):
 
 def make_shape(q: torch.Tensor, v: torch.Tensor, *, cu_seqlens: Optional[torch.Tensor] = None,
                scale: Optional[float] = None, l2norm: bool = False, sp: bool = True, window: bool = True,
-               seg_chunks: int = 0) -> GdnShape:
+               seg_chunks: int = 0, single_launch: bool = False) -> GdnShape:
     B, T, H, Dk = q.shape
     s = GdnShape()
     s.B, s.T, s.H, s.Dk, s.Dv = B, T, H, Dk, v.shape[-1]
@@ -67,7 +67,8 @@ def make_shape(q: torch.Tensor, v: torch.Tensor, *, cu_seqlens: Optional[torch.T
         s.num_seqs = cu_seqlens.numel() - 1
     s.dtype = GDN_BF16 if q.dtype == torch.bfloat16 else GDN_FP32
     s.scale = 1.0 / math.sqrt(Dk) if scale is None else float(scale)
-    s.flags = (GDN_L2NORM_QK if l2norm else 0) | (0 if sp else GDN_SP_OFF) | (0 if window else GDN_WINDOW_OFF)
+    s.flags = (GDN_L2NORM_QK if l2norm else 0) | (0 if sp else GDN_SP_OFF) | (0 if window else GDN_WINDOW_OFF) | \
+        (_lib.GDN_SP_SINGLE_LAUNCH if single_launch else 0)
     s.seg_chunks = int(seg_chunks)
     return s
 
@@ -201,12 +202,12 @@ def _contig(*ts):
 
 def chunk_gated_delta_rule_fwd(q, k, v, g, beta, initial_state=None, output_final_state=True, cu_seqlens=None,
                                scale=None, use_qk_l2norm_in_kernel=False, sp=True, window=True, seg_chunks=0,
-                               workspace=None, save_context=False):
+                               workspace=None, save_context=False, single_launch=False):
     """o, S_T (S_T None unless output_final_state); with save_context=True also the saved
     context (a uint8 tensor) to pass to chunk_gated_delta_rule_bwd(saved=...)."""
     _contig(q, k, v, g, beta, initial_state)
     shape = make_shape(q, v, cu_seqlens=cu_seqlens, scale=scale, l2norm=use_qk_l2norm_in_kernel, sp=sp,
-                       window=window, seg_chunks=seg_chunks)
+                       window=window, seg_chunks=seg_chunks, single_launch=single_launch)
     N = shape.num_seqs if cu_seqlens is not None else q.shape[0]
     o = torch.empty_like(v)
     S_T = torch.empty(N, q.shape[2], v.shape[-1], q.shape[-1], dtype=torch.float32, device=q.device) \
@@ -244,12 +245,12 @@ def recurrent_gated_delta_rule(q, k, v, g, beta, initial_state=None, scale=None,
 
 def chunk_gated_delta_rule_bwd(q, k, v, g, beta, dO, initial_state=None, dS_T=None, cu_seqlens=None, scale=None,
                                use_qk_l2norm_in_kernel=False, sp=True, window=True, seg_chunks=0, workspace=None,
-                               saved=None):
+                               saved=None, single_launch=False):
     """dq, dk, dv, dg, dbeta, dS0 (dS0 None without an initial state).  `saved`: the context
     that chunk_gated_delta_rule_fwd(save_context=True) returned for these same inputs."""
     _contig(q, k, v, g, beta, dO, initial_state, dS_T)
     shape = make_shape(q, v, cu_seqlens=cu_seqlens, scale=scale, l2norm=use_qk_l2norm_in_kernel, sp=sp,
-                       window=window, seg_chunks=seg_chunks)
+                       window=window, seg_chunks=seg_chunks, single_launch=single_launch)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dg, db = torch.empty_like(g), torch.empty_like(beta)
     dS0 = torch.empty_like(initial_state) if initial_state is not None else None

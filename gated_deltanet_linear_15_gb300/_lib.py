@@ -10,8 +10,9 @@ from . import build as _build
 GDN_BF16, GDN_FP32 = 0, 1
 GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE, GDN_ERR_CUDA = 0, 1, 2, 3, 4
 GDN_ERR_TIMEOUT, GDN_ERR_NUMERIC = 5, 6
-GDN_L2NORM_QK, GDN_SP_OFF, GDN_WINDOW_OFF = 1, 2, 4
+GDN_L2NORM_QK, GDN_SP_OFF, GDN_WINDOW_OFF, GDN_SP_SINGLE_LAUNCH = 1, 2, 4, 8
 GDN_DEBUG_WAIT_TIMEOUT = 0x80000000
+GDN_DEBUG_PEER_TIMEOUT = 0x40000000
 GDN_STATIC_SCRATCH_BYTES = 16 << 20
 
 # every symbol include/gdn.h declares

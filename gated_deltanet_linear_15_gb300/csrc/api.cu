@@ -54,6 +54,8 @@ struct Layout {
   bool sp = false;  // more than one segment possible for some sequence
   size_t esize = 2;
   size_t off_status = 0, off_plan = 0, off_gsum = 0;
+  size_t off_sched = 0, off_lists = 0;  // single-launch sequence parallelism: zeroed counters, work lists
+  int sched_zero = 0;                   // ints of the zeroed counter region
   size_t off_E = 0, off_M = 0, off_S = 0;     // forward fix-up buffers
   size_t off_states = 0, off_dstates = 0;   // backward per-chunk states
   size_t off_F = 0, off_R = 0, off_dS = 0;  // reverse fix-up buffers
@@ -215,6 +217,13 @@ int make_layout(const gdn_shape *s, Layout &L) {
   off = align256(off + nplan * 4);
   L.off_gsum = off;
   off = align256(off + (size_t)L.CH_max * L.H * 4);
+  // the two directions' schedules: [hdr fwd | hdr bwd | needA, doneA, doneF fwd | the same bwd] (zeroed by the
+  // plan kernel), then per direction listA [2 S_max H], listBn, listBf [S_max H], listF [N H]
+  L.off_sched = off;
+  L.sched_zero = L.sp ? 2 * SCHED_HDR + 6 * L.N * L.H : 0;
+  off = align256(off + (size_t)L.sched_zero * 4);
+  L.off_lists = off;
+  if (L.sp) off = align256(off + (size_t)2 * (4 * (size_t)L.S_max * L.H + (size_t)L.N * L.H) * 4);
   const size_t spbuf = L.sp ? align256((size_t)L.S_max * L.H * DD * 4) : 0;
   L.off_E = off;
   off += spbuf;
@@ -265,6 +274,33 @@ int make_layout(const gdn_shape *s, Layout &L) {
   L.saved_off_nrm = L.saved_off_tqkv + L.tqkv_bytes;
   L.saved_total = L.saved_off_nrm + L.nrm_bytes;
   return GDN_OK;
+}
+
+// The work lists of one direction (0 forward, 1 reverse) of the single-launch sequence parallelism.
+Sched sched_of(const Layout &L, char *ws, int dir) {
+  int *z = reinterpret_cast<int *>(ws + L.off_sched);
+  int *lists = reinterpret_cast<int *>(ws + L.off_lists);
+  const size_t NH = (size_t)L.N * L.H, SH = (size_t)L.S_max * L.H;
+  Sched sc;
+  sc.hdr = z + dir * SCHED_HDR;
+  sc.needA = z + 2 * SCHED_HDR + dir * 3 * NH;
+  sc.doneA = sc.needA + NH;
+  sc.doneF = sc.doneA + NH;
+  sc.listA = lists + dir * (4 * SH + NH);
+  sc.listBn = sc.listA + 2 * SH;
+  sc.listBf = sc.listBn + SH;
+  sc.listF = sc.listBf + SH;
+  return sc;
+}
+
+// Is sequence parallelism run as one launch per direction?  On request (GDN_SP_SINGLE_LAUNCH), for the tcgen05
+// path (bf16, d = 128) with segments.
+bool single_launch_sp(const Layout &L, const gdn_shape *s) {
+  return (s->flags & GDN_SP_SINGLE_LAUNCH) && L.sp && s->dtype == GDN_BF16 && L.D == 128 && L.Ttot > 0;
+}
+// CTAs of such a launch: one per possible work item (pass A two roles, pass B, fix-up row blocks)
+unsigned sched_grid(const Layout &L) {
+  return (unsigned)(3 * L.S_max * L.H + (L.D / FIX_ROWS) * L.N * L.H);
 }
 
 Plan plan_of(const Layout &L, char *ws) {
@@ -367,14 +403,17 @@ void prof_drain_locked() {
 int prologue(const gdn_shape *s, const Layout &L, char *ws, const float *g, cudaStream_t st, Plan &pl) {
   pl = plan_of(L, ws);
   int *status = reinterpret_cast<int *>(ws + L.off_status);  // [0] status word, [1]/[2] fix-up flags
+  const bool single = single_launch_sp(L, s);
   {
     PROF("plan");
-    CK(launch_plan(pl, s->cu_seqlens, L.N, s->cu_seqlens ? s->T : L.Tseq, L.Lseg, L.S_max, L.CH_max, status, st));
+    CK(launch_plan(pl, s->cu_seqlens, L.N, s->cu_seqlens ? s->T : L.Tseq, L.Lseg, L.S_max, L.CH_max, status,
+                   single ? reinterpret_cast<int *>(ws + L.off_sched) : nullptr, L.sched_zero, st));
   }
   {
     PROF("gate_scan");
+    const Sched sc[2] = {sched_of(L, ws, 0), sched_of(L, ws, 1)};
     CK(launch_gate_scan(pl, g, L.H, L.CH_max, reinterpret_cast<float *>(ws + L.off_gsum), status, L.sp ? 1 : 0,
-                        L.Lseg, L.S_max, s->flags, st));
+                        L.Lseg, L.S_max, s->flags, single ? sc : nullptr, L.N * L.H, st));
   }
   return GDN_OK;
 }
@@ -488,6 +527,14 @@ int forward_passes(const gdn_shape *s, const Layout &L, char *ws, FwdArgs fa, in
   if (tc_forward(L, s)) {
     PROF("fwd_prep");
     CK(launch_forward_prep(L, fa, st));
+  }
+  if (single_launch_sp(L, s)) {  // pass A, the fix-up and pass B in one launch
+    fa.pass = pass;
+    fa.sched = sched_of(L, ws, 0);
+    fa.sched_on = 1;
+    PROF(pass == 1 ? "fwd_chunk" : "fwd_states");
+    CK(launch_forward_kernel(L, s, fa, dim3(sched_grid(L)), st));
+    return GDN_OK;
   }
   if (L.sp) {
     fa.pass = 0;
@@ -680,6 +727,13 @@ int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
   auto chain = [&](dim3 grid) {
     return chain_tc ? launch_bwd_chain_tc(ba, cmaps, grid, st) : launch_bwd_chain(ba, bf, L.D, grid, st);
   };
+  if (single_launch_sp(L, s) && chain_tc) {  // pass A, the fix-up and the chain in one launch
+    ba.pass = 1;
+    ba.sched = sched_of(L, ws, 1);
+    ba.sched_on = 1;
+    PROF("bwd_chain");
+    CK(chain(dim3(sched_grid(L))));
+  } else {
   if (L.sp) {
     ba.pass = 0;
     {
@@ -705,6 +759,7 @@ int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
   {
     PROF("bwd_chain");
     CK(chain(dim3(L.S_max, L.H, 1)));
+  }
   }
   // 3. local gradients, every (chunk, head) in parallel
   {
@@ -900,7 +955,7 @@ int gdn_get_device_status(const gdn_shape *shape, const void *workspace, gdn_str
 int gdn_device_status_code(int word) {
   if (word < 0) return GDN_ERR_CUDA;
   if (word & 2) return GDN_ERR_INVALID_ARG;
-  if (word & (4 | 8)) return GDN_ERR_TIMEOUT;
+  if (word & (4 | 8 | 16)) return GDN_ERR_TIMEOUT;
   if (word & 1) return GDN_ERR_NUMERIC;
   return GDN_OK;
 }

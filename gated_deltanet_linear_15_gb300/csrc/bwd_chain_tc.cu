@@ -12,6 +12,7 @@
 // pass 1 runs it from its exact end gradient and stores the per-chunk dS
 // (and dS0 for the first segment).  Layouts and primitives as in fwd_tc.cu.
 #include "chunk_common.cuh"
+#include "fixup.cuh"
 #include "kernels.h"
 #include "umma.cuh"
 
@@ -50,18 +51,16 @@ __device__ __forceinline__ void st_chunk_f16(uint8_t *dst, const float *v) {
 
 }  // namespace
 
-__global__ void __launch_bounds__(NTHREADS + 32, 1)
-    bwd_chain_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tm3, const __grid_constant__ CUtensorMap tmdo,
-                        const __grid_constant__ CUtensorMap tmp, const __grid_constant__ CUtensorMap tmw,
-                        const __grid_constant__ CUtensorMap tmds) {
+// One work item: segment s of head h in pass `pass` (0: pass A, role 0 the start gradient from zero or its
+// warm-up, role 1 the reverse transition; 1: the per-chunk dS).
+__device__ __forceinline__ void chain_tc_item(const BwdArgs &a, const CUtensorMap &tm3, const CUtensorMap &tmdo,
+                                              const CUtensorMap &tmp, const CUtensorMap &tmw, const CUtensorMap &tmds,
+                                              int s, int h, int role, int pass) {
   extern __shared__ unsigned char smraw[];
   ChainTcSmem &sm =
       *reinterpret_cast<ChainTcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
-  pdl_trigger();
-  pdl_wait();
-  const int s = blockIdx.x, h = blockIdx.y, role = blockIdx.z;
   // pass A of a call in which no segment needs the exact fix-up (status[2], set after the gate scan)
-  if (a.pass == 0 && a.status && a.status[2] == 0) return;
+  if (pass == 0 && a.status && a.status[2] == 0) return;
   const int H = a.H;
   const int n = a.plan.seg_seq[s];
   if (n < 0) return;
@@ -74,7 +73,7 @@ __global__ void __launch_bounds__(NTHREADS + 32, 1)
   int w = 0;
   const int mode = bwd_start_mode(a.gsum, H, h, chunk0, cend, nchunks, j, nseg, window, &w);
   bool transition = false;
-  if (a.pass == 0) {
+  if (pass == 0) {
     if (j == 0) return;
     int w2;
     if (bwd_start_mode(a.gsum, H, h, chunk0, cbeg, nchunks, j - 1, nseg, window, &w2) != START_FIXUP) return;
@@ -90,7 +89,7 @@ __global__ void __launch_bounds__(NTHREADS + 32, 1)
     if (threadIdx.x == 0) debug_expire_wait(&dbg_bar, a.status, 4);
     return;
   }
-  const bool store = (a.pass == 1);
+  const bool store = (pass == 1);
   const bool with_do = !transition;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wg = warp >> 2;
@@ -150,7 +149,7 @@ __global__ void __launch_bounds__(NTHREADS + 32, 1)
     const float *src = nullptr;
     if (!transition) {
       if (mode == START_INIT) src = a.dST ? a.dST + ((size_t)n * H + h) * DD : nullptr;
-      else if (mode == START_FIXUP && a.pass != 0) src = a.dSend + sh_idx * DD;
+      else if (mode == START_FIXUP && pass != 0) src = a.dSend + sh_idx * DD;
     }
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
@@ -160,7 +159,7 @@ __global__ void __launch_bounds__(NTHREADS + 32, 1)
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const int col = c0 + i;
-        v[i] = src ? src[(size_t)row * D + col] : (transition && col == row ? 1.f : 0.f);
+        v[i] = src ? __ldcg(src + (size_t)row * D + col) : (transition && col == row ? 1.f : 0.f);
       }
       tmem_st32(tm + tl + TM_S + c0, v);
     }
@@ -379,7 +378,7 @@ __global__ void __launch_bounds__(NTHREADS + 32, 1)
 
   if (!failed && warp < NWARPS) {
     float *dst = nullptr;
-    if (a.pass == 0) dst = (transition ? a.Rbuf : a.Fbuf) + sh_idx * DD;
+    if (pass == 0) dst = (transition ? a.Rbuf : a.Fbuf) + sh_idx * DD;
     else if (j == 0 && a.dS0) dst = a.dS0 + ((size_t)n * H + h) * DD;
     if (dst) {
 #pragma unroll
@@ -402,13 +401,98 @@ __global__ void __launch_bounds__(NTHREADS + 32, 1)
   if (warp == 0) tmem_dealloc(tm, TM_COLS);
 }
 
+template <bool SCHED>
+__global__ void __launch_bounds__(NTHREADS + 32, 1)
+    bwd_chain_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tm3, const __grid_constant__ CUtensorMap tmdo,
+                        const __grid_constant__ CUtensorMap tmp, const __grid_constant__ CUtensorMap tmw,
+                        const __grid_constant__ CUtensorMap tmds) {
+  pdl_trigger();
+  pdl_wait();
+  int s = blockIdx.x, h = blockIdx.y, role = blockIdx.z, pass = a.pass;
+  int *doneA = nullptr;  // a pass-A item reports its completion here
+  if (SCHED) {
+    // single-launch sequence parallelism: this CTA runs the ticket-th item of the work lists (see Sched)
+    __shared__ int tk, ok;
+    const Sched &sc = a.sched;
+    const int tid = threadIdx.x;
+    if (tid == 0) tk = atomicAdd(sc.hdr, 1);
+    __syncthreads();
+    constexpr int NRB = D / FIX_ROWS;
+    const int nA = __ldcg(sc.hdr + 1), nBn = __ldcg(sc.hdr + 2), nF = __ldcg(sc.hdr + 3), nBf = __ldcg(sc.hdr + 4);
+    int t = tk;
+    if (t < nA) {  // pass A
+      const int e = sc.listA[t];
+      s = (e >> 1) / a.H;
+      h = (e >> 1) % a.H;
+      role = e & 1;
+      pass = 0;
+      doneA = sc.doneA + a.plan.seg_seq[s] * a.H + h;
+    } else if ((t -= nA) < nBn) {  // the chain from an end that needs no fix-up
+      s = sc.listBn[t] / a.H;
+      h = sc.listBn[t] % a.H;
+      role = 0;
+    } else if ((t -= nBn) < nF * NRB) {  // a fix-up row block, once its (sequence, head)'s pass A is done
+      if (tid >= 256) return;
+      const int pair = sc.listF[t / NRB];
+      if (tid == 0) ok = wait_count_geq(sc.doneA + pair, sc.needA[pair], PEER_WAIT_LIMIT);
+      fix_bar();
+      if (!ok) {
+        if (tid == 0 && a.status) atomicOr(a.status, 16);
+        return;
+      }
+      __threadfence();
+      FixupArgs fx;
+      fx.plan = a.plan;
+      fx.gsum = a.gsum;
+      fx.E = a.Fbuf;
+      fx.M = a.Rbuf;
+      fx.out = a.dSend;
+      fx.H = a.H;
+      fx.D = D;
+      fx.Lseg = a.Lseg;
+      fx.flags = a.flags;
+      fx.reverse = 1;
+      fx.fixflag = nullptr;
+      extern __shared__ unsigned char smraw[];
+      fixup_rows<D>(fx, t % NRB, pair % a.H, pair / a.H,
+                    reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023));
+      __threadfence();
+      fix_bar();
+      if (tid == 0) atomicAdd(sc.doneF + pair, 1);
+      return;
+    } else if ((t -= nF * NRB) < nBf) {  // the chain from a fixed-up end, once its fix-up blocks are done
+      s = sc.listBf[t] / a.H;
+      h = sc.listBf[t] % a.H;
+      role = 0;
+      const int pair = a.plan.seg_seq[s] * a.H + h;
+      if (tid == 0) {
+        const bool hook = (a.flags & kFlagDebugPeerTimeout) != 0;  // test hook: a wait that cannot succeed
+        ok = wait_count_geq(sc.doneF + pair, hook ? NRB + 1 : NRB, hook ? 1024 : PEER_WAIT_LIMIT);
+        if (!ok && a.status) atomicOr(a.status, 16);
+      }
+      __syncthreads();
+      if (!ok) return;
+      __threadfence();
+    } else {
+      return;  // a ticket past the lists: no work
+    }
+  }
+  chain_tc_item(a, tm3, tmdo, tmp, tmw, tmds, s, h, role, pass);
+  if (doneA) {  // the start-gradient / transition stores of every thread are visible before the count
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) atomicAdd(doneA, 1);
+  }
+}
+
 int launch_bwd_chain_tc(const BwdArgs &a, const CUtensorMap *maps, dim3 grid, cudaStream_t st) {
   const size_t smem = sizeof(ChainTcSmem) + 1024;
   static_assert(sizeof(ChainTcSmem) + 1024 <= 232448 - 256, "shared memory budget (the rest: static shared memory)");
-  cudaError_t e = cudaFuncSetAttribute(bwd_chain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static_assert(fixup_smem_bytes<D>() <= sizeof(ChainTcSmem), "a fix-up row block fits the kernel's shared memory");
+  auto kern = a.sched_on ? bwd_chain_tc_kernel<true> : bwd_chain_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  return (int)launch_pdl(bwd_chain_tc_kernel, grid, dim3(NTHREADS + 32), smem, st, a, maps[0], maps[1], maps[2], maps[3],
-                         maps[4]);
+  return (int)launch_pdl(kern, grid, dim3(NTHREADS + 32), smem, st, a, maps[0], maps[1], maps[2], maps[3], maps[4]);
 }
 
 }  // namespace gdn

@@ -86,20 +86,39 @@ __device__ __forceinline__ bool prep_rows(E *t, int ld, float mul, bool l2, floa
 // exp(G_r - G_c) (C^2 / 2 exponentials, for that chunk only).  Log-gates below
 // GATE_FLOOR are raised to it: exp(GATE_FLOOR) and every ratio across such a
 // token are zero in fp32 either way, and the prefix sums keep their precision.
-// The prefix sums are taken in fp64 and each exponent argument (a difference
-// of two prefix sums) is formed in fp64 before its fp32 exponential: a chunk
-// can hold a large decay (|G| ~ 100) followed by slow decay, and there fp32
-// prefix sums would lose the small differences that the ratios need.
+// A chunk whose prefix sums stay within |G| <= 16 takes them in plain fp32
+// (their differences then carry an absolute error of a few 1e-6).  A chunk
+// that decays further can hold a large decay (|G| ~ 100) followed by slow
+// decay, where plain fp32 prefix sums lose the small differences that the
+// ratios need; it carries the sums as unevaluated pairs hi + lo of fp32 values
+// (each addition error-free by Knuth's TwoSum) and forms each exponent argument
+// (a difference of two prefix sums) from both parts.  (fp64 would do the same,
+// but it is slow on this part.)
 struct __align__(16) Gates {
-  double G[CH];
+  float Ghi[CH], Glo[CH];
   float gam[CH], gp[CH], rgp[CH], cdec[CH];
   float gamC;  // exp(G_last)
   int pw;      // nonzero: take decay ratios pairwise (the span leaves the factoring range)
 };
 
-// gamma_r / gamma_c for c <= r (callers mask c > r themselves)
+// (hi, lo) += (bh, bl), hi + lo exact up to lo's rounding (Knuth's TwoSum, then a renormalisation)
+__device__ __forceinline__ void two_add(float &hi, float &lo, float bh, float bl) {
+  const float s = hi + bh, v = s - hi;
+  const float e = (hi - (s - v)) + (bh - v);
+  const float l = lo + bl + e;
+  hi = s + l;
+  lo = l - (hi - s);
+}
+// (ah + al) - (bh + bl) as one fp32 value
+__device__ __forceinline__ float two_diff(float ah, float al, float bh, float bl) { return (ah - bh) + (al - bl); }
+
+// gamma_r / gamma_c for c <= r (callers mask c > r themselves); the pairwise form out of line, so that
+// the factored one stays small in the kernels' read-out loops
+static __device__ __noinline__ float gratio_pw(const Gates &gt, int r, int c) {
+  return expf(two_diff(gt.Ghi[r], gt.Glo[r], gt.Ghi[c], gt.Glo[c]));
+}
 __device__ __forceinline__ float gratio(const Gates &gt, int r, int c) {
-  return gt.pw ? expf((float)(gt.G[r] - gt.G[c])) : gt.gp[r] * gt.rgp[c];
+  return gt.pw ? gratio_pw(gt, r, c) : gt.gp[r] * gt.rgp[c];
 }
 
 // 16 consecutive floats from 16-byte aligned shared memory (four vector loads)
@@ -116,31 +135,51 @@ __device__ __forceinline__ void ld16f(const float *p, float (&v)[16]) {
 
 __device__ __forceinline__ bool gate_prefix(const float *g, Gates &gt) {
   const int lane = threadIdx.x & 31;
-  double a = fmaxf(g[lane], GATE_FLOOR), b = fmaxf(g[lane + 32], GATE_FLOOR);
+  const float ga = fmaxf(g[lane], GATE_FLOOR), gb = fmaxf(g[lane + 32], GATE_FLOOR);
+  float a = ga, b = gb, al = 0.f, bl = 0.f;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double ya = __shfl_up_sync(0xffffffffu, a, o);
-    const double yb = __shfl_up_sync(0xffffffffu, b, o);
+    const float ya = __shfl_up_sync(0xffffffffu, a, o), yb = __shfl_up_sync(0xffffffffu, b, o);
     if (lane >= o) {
       a += ya;
       b += yb;
     }
   }
-  const double Gmid = __shfl_sync(0xffffffffu, a, 31);
-  b += Gmid;
-  const double Glast = __shfl_sync(0xffffffffu, b, 31);
-  gt.G[lane] = a;
-  gt.G[lane + 32] = b;
-  gt.gam[lane] = expf((float)a);
-  gt.gam[lane + 32] = expf((float)b);
-  gt.gp[lane] = expf((float)(a - Gmid));
-  gt.gp[lane + 32] = expf((float)(b - Gmid));
-  gt.rgp[lane] = expf((float)(Gmid - a));
-  gt.rgp[lane + 32] = expf((float)(Gmid - b));
-  gt.cdec[lane] = expf((float)(Glast - a));
-  gt.cdec[lane + 32] = expf((float)(Glast - b));
-  if (lane == 0) gt.gamC = expf((float)Glast);
-  float rng = fmaxf(fabsf((float)(a - Gmid)), fabsf((float)(b - Gmid)));
+  float Gm = __shfl_sync(0xffffffffu, a, 31), Gml = 0.f;
+  b += Gm;
+  // |G| over the chunk: beyond 16, redo the sums as hi + lo pairs (a warp-uniform branch)
+  if (__any_sync(0xffffffffu, fmaxf(fabsf(a), fabsf(b)) > 16.f)) {
+    a = ga;
+    b = gb;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float ya = __shfl_up_sync(0xffffffffu, a, o), yal = __shfl_up_sync(0xffffffffu, al, o);
+      const float yb = __shfl_up_sync(0xffffffffu, b, o), ybl = __shfl_up_sync(0xffffffffu, bl, o);
+      if (lane >= o) {
+        two_add(a, al, ya, yal);
+        two_add(b, bl, yb, ybl);
+      }
+    }
+    Gm = __shfl_sync(0xffffffffu, a, 31);
+    Gml = __shfl_sync(0xffffffffu, al, 31);
+    two_add(b, bl, Gm, Gml);
+  }
+  const float Gl = __shfl_sync(0xffffffffu, b, 31), Gll = __shfl_sync(0xffffffffu, bl, 31);
+  gt.Ghi[lane] = a;
+  gt.Glo[lane] = al;
+  gt.Ghi[lane + 32] = b;
+  gt.Glo[lane + 32] = bl;
+  gt.gam[lane] = expf(a + al);
+  gt.gam[lane + 32] = expf(b + bl);
+  const float da = two_diff(a, al, Gm, Gml), db = two_diff(b, bl, Gm, Gml);
+  gt.gp[lane] = expf(da);
+  gt.gp[lane + 32] = expf(db);
+  gt.rgp[lane] = expf(-da);
+  gt.rgp[lane + 32] = expf(-db);
+  gt.cdec[lane] = expf(two_diff(Gl, Gll, a, al));
+  gt.cdec[lane + 32] = expf(two_diff(Gl, Gll, b, bl));
+  if (lane == 0) gt.gamC = expf(Gl + Gll);
+  float rng = fmaxf(fabsf(da), fabsf(db));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) rng = fmaxf(rng, __shfl_xor_sync(0xffffffffu, rng, o));
   const bool pw = rng > FACTOR_RANGE;
@@ -156,9 +195,9 @@ __device__ __forceinline__ void gratio8(const Gates &gt, int r, int cb, float (&
     o[0] = gr * a.x; o[1] = gr * a.y; o[2] = gr * a.z; o[3] = gr * a.w;
     o[4] = gr * b.x; o[5] = gr * b.y; o[6] = gr * b.z; o[7] = gr * b.w;
   } else {
-    const double Gr = gt.G[r];
+    const float Gr = gt.Ghi[r], Grl = gt.Glo[r];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) o[i] = cb + i <= r ? expf((float)(Gr - gt.G[cb + i])) : 0.f;
+    for (int i = 0; i < 8; ++i) o[i] = cb + i <= r ? expf(two_diff(Gr, Grl, gt.Ghi[cb + i], gt.Glo[cb + i])) : 0.f;
   }
 }
 

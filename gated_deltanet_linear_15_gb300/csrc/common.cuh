@@ -276,6 +276,20 @@ __device__ __forceinline__ int bwd_start_mode(const float *gsum, int H, int h, i
   return START_FIXUP;
 }
 
+// Bounded wait of one thread until *p >= target (acquire at GPU scope), polling with a short sleep;
+// false when it gives up after `limit` polls (~1 s at the default).  The single-launch sequence
+// parallelism waits this way for work items of other CTAs that started before it.
+constexpr int PEER_WAIT_LIMIT = 1 << 22;
+__device__ __forceinline__ bool wait_count_geq(const int *p, int target, int limit) {
+  for (int i = 0; i < limit; ++i) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+    if (v >= target) return true;
+    __nanosleep(256);
+  }
+  return false;
+}
+
 // Programmatic dependent launch.  A kernel started with launch_pdl may be scheduled while the
 // previous kernel on its stream is still finishing: it calls pdl_trigger() (its own dependents may
 // then be scheduled) and pdl_wait() (returns once the previous grid has completed and its memory

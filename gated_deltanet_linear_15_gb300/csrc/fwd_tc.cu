@@ -23,6 +23,7 @@
 // reaches lanes 32 (w % 4)..; the four warps of a lane quarter split the columns)
 // and do the CUDA-core work.  The tiles of chunk c+1 are loaded while chunk c runs.
 #include "chunk_common.cuh"
+#include "fixup.cuh"
 #include "kernels.h"
 #include "umma.cuh"
 
@@ -73,18 +74,15 @@ __device__ __forceinline__ uint32_t chunk_off(int r, int cb) { return r * 128 + 
 
 }  // namespace
 
-__global__ void __launch_bounds__(FT + 32, 1)
-    fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tm3, const __grid_constant__ CUtensorMap tmw,
-                  const __grid_constant__ CUtensorMap tms, const __grid_constant__ CUtensorMap tmt,
-                  const __grid_constant__ CUtensorMap tmo) {
+// One work item: segment s of head h in pass `pass` (0: pass A, role 0 the end state from zero or its
+// warm-up, role 1 the transition; 1: outputs; 2: states only).
+__device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap &tm3, const CUtensorMap &tmw,
+                                            const CUtensorMap &tms, const CUtensorMap &tmt, const CUtensorMap &tmo,
+                                            int s, int h, int role, int pass) {
   extern __shared__ unsigned char smraw[];
   TcSmem &sm = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
-  pdl_trigger();
-  pdl_wait();
-
-  const int s = blockIdx.x, h = blockIdx.y, role = blockIdx.z;
   // pass A of a call in which no segment needs the exact fix-up (status[1], set after the gate scan)
-  if (a.pass == 0 && a.status && a.status[1] == 0) return;
+  if (pass == 0 && a.status && a.status[1] == 0) return;
   const int H = a.H;
   const int n = a.plan.seg_seq[s];
   if (n < 0) return;
@@ -97,7 +95,7 @@ __global__ void __launch_bounds__(FT + 32, 1)
   int w = 0;
   const int mode = fwd_start_mode(a.gsum, H, h, chunk0, cbeg, j, window, &w);
   bool transition = false;
-  if (a.pass == 0) {
+  if (pass == 0) {
     if (j >= nseg - 1) return;
     int w2;
     if (fwd_start_mode(a.gsum, H, h, chunk0, cend, j + 1, window, &w2) != START_FIXUP) return;
@@ -113,11 +111,11 @@ __global__ void __launch_bounds__(FT + 32, 1)
     if (threadIdx.x == 0) debug_expire_wait(&dbg_bar, a.status, 4);
     return;
   }
-  const bool outputs = (a.pass == 1);
+  const bool outputs = (pass == 1);
   const bool need_v = !transition;
   // chunk-start states and the W^T, Ut^T context tiles leave shared memory by TMA stores (a pass
   // with o == NULL writes states and context but no output)
-  const bool save_states = a.pass != 0 && a.states != nullptr;
+  const bool save_states = pass != 0 && a.states != nullptr;
   const bool save_wy = outputs && a.t128 != nullptr;
   const bool want_o = outputs && a.o != nullptr;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -204,7 +202,7 @@ __global__ void __launch_bounds__(FT + 32, 1)
     const float *src = nullptr;
     if (!transition) {
       if (mode == START_INIT) src = a.S0 ? a.S0 + ((size_t)n * H + h) * DD : nullptr;
-      else if (mode == START_FIXUP && a.pass != 0) src = a.Sstart + sh_idx * DD;
+      else if (mode == START_FIXUP && pass != 0) src = a.Sstart + sh_idx * DD;
     }
     if (warp < FWARPS) {
       const int c0 = wg * 32;
@@ -212,7 +210,7 @@ __global__ void __launch_bounds__(FT + 32, 1)
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const int col = c0 + i;
-        v[i] = src ? src[(size_t)row * D + col] : (transition && col == row ? 1.f : 0.f);
+        v[i] = src ? __ldcg(src + (size_t)row * D + col) : (transition && col == row ? 1.f : 0.f);
       }
       tmem_st32(tm + tm_lane + TM_S + c0, v);
     }
@@ -483,7 +481,7 @@ __global__ void __launch_bounds__(FT + 32, 1)
   // ---------------------------------------------------------------- end-of-segment state
   if (!failed && warp < FWARPS) {
     float *dst = nullptr;
-    if (a.pass == 0) dst = (transition ? a.Mbuf : a.Ebuf) + sh_idx * DD;
+    if (pass == 0) dst = (transition ? a.Mbuf : a.Ebuf) + sh_idx * DD;
     else if (j == nseg - 1 && a.ST) dst = a.ST + ((size_t)n * H + h) * DD;
     if (dst) {
       {
@@ -504,15 +502,101 @@ __global__ void __launch_bounds__(FT + 32, 1)
   if (warp == 0) tmem_dealloc(tm, TM_COLS);
 }
 
+template <bool SCHED>
+__global__ void __launch_bounds__(FT + 32, 1)
+    fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tm3, const __grid_constant__ CUtensorMap tmw,
+                  const __grid_constant__ CUtensorMap tms, const __grid_constant__ CUtensorMap tmt,
+                  const __grid_constant__ CUtensorMap tmo) {
+  pdl_trigger();
+  pdl_wait();
+  int s = blockIdx.x, h = blockIdx.y, role = blockIdx.z, pass = a.pass;
+  int *doneA = nullptr;  // a pass-A item reports its completion here
+  if (SCHED) {
+    // single-launch sequence parallelism: this CTA runs the ticket-th item of the work lists (see Sched)
+    __shared__ int tk, ok;
+    const Sched &sc = a.sched;
+    const int tid = threadIdx.x;
+    if (tid == 0) tk = atomicAdd(sc.hdr, 1);
+    __syncthreads();
+    constexpr int NRB = D / FIX_ROWS;
+    const int nA = __ldcg(sc.hdr + 1), nBn = __ldcg(sc.hdr + 2), nF = __ldcg(sc.hdr + 3), nBf = __ldcg(sc.hdr + 4);
+    int t = tk;
+    if (t < nA) {  // pass A
+      const int e = sc.listA[t];
+      s = (e >> 1) / a.H;
+      h = (e >> 1) % a.H;
+      role = e & 1;
+      pass = 0;
+      doneA = sc.doneA + a.plan.seg_seq[s] * a.H + h;
+    } else if ((t -= nA) < nBn) {  // pass B from a start that needs no fix-up
+      s = sc.listBn[t] / a.H;
+      h = sc.listBn[t] % a.H;
+      role = 0;
+    } else if ((t -= nBn) < nF * NRB) {  // a fix-up row block, once its (sequence, head)'s pass A is done
+      if (tid >= 256) return;
+      const int pair = sc.listF[t / NRB];
+      if (tid == 0) ok = wait_count_geq(sc.doneA + pair, sc.needA[pair], PEER_WAIT_LIMIT);
+      fix_bar();
+      if (!ok) {
+        if (tid == 0 && a.status) atomicOr(a.status, 16);
+        return;
+      }
+      __threadfence();
+      FixupArgs fx;
+      fx.plan = a.plan;
+      fx.gsum = a.gsum;
+      fx.E = a.Ebuf;
+      fx.M = a.Mbuf;
+      fx.out = a.Sstart;
+      fx.H = a.H;
+      fx.D = D;
+      fx.Lseg = a.Lseg;
+      fx.flags = a.flags;
+      fx.reverse = 0;
+      fx.fixflag = nullptr;
+      extern __shared__ unsigned char smraw[];
+      fixup_rows<D>(fx, t % NRB, pair % a.H, pair / a.H,
+                    reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023));
+      __threadfence();
+      fix_bar();
+      if (tid == 0) atomicAdd(sc.doneF + pair, 1);
+      return;
+    } else if ((t -= nF * NRB) < nBf) {  // pass B from a fixed-up start, once its fix-up blocks are done
+      s = sc.listBf[t] / a.H;
+      h = sc.listBf[t] % a.H;
+      role = 0;
+      const int pair = a.plan.seg_seq[s] * a.H + h;
+      if (tid == 0) {
+        const bool hook = (a.flags & kFlagDebugPeerTimeout) != 0;  // test hook: a wait that cannot succeed
+        ok = wait_count_geq(sc.doneF + pair, hook ? NRB + 1 : NRB, hook ? 1024 : PEER_WAIT_LIMIT);
+        if (!ok && a.status) atomicOr(a.status, 16);
+      }
+      __syncthreads();
+      if (!ok) return;
+      __threadfence();
+    } else {
+      return;  // a ticket past the lists: no work
+    }
+  }
+  fwd_tc_item(a, tm3, tmw, tms, tmt, tmo, s, h, role, pass);
+  if (doneA) {  // the end state / transition stores of every thread are visible before the count
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) atomicAdd(doneA, 1);
+  }
+}
+
 size_t fwd_tc_smem_bytes() { return sizeof(TcSmem) + 1024; }
 
 int launch_fwd_tc(const FwdArgs &a, const CUtensorMap &t3, const CUtensorMap &tw, const CUtensorMap &ts,
                   const CUtensorMap &tt, const CUtensorMap &to, dim3 grid, cudaStream_t st) {
   const size_t smem = fwd_tc_smem_bytes();
   static_assert(sizeof(TcSmem) + 1024 <= 232448 - 256, "shared memory budget (the rest: static shared memory)");
-  cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static_assert(fixup_smem_bytes<D>() <= sizeof(TcSmem), "a fix-up row block fits the kernel's shared memory");
+  auto kern = a.sched_on ? fwd_tc_kernel<true> : fwd_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  return (int)launch_pdl(fwd_tc_kernel, grid, dim3(FT + 32), smem, st, a, t3, tw, ts, tt, to);
+  return (int)launch_pdl(kern, grid, dim3(FT + 32), smem, st, a, t3, tw, ts, tt, to);
 }
 
 }  // namespace gdn

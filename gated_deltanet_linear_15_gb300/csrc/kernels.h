@@ -12,6 +12,23 @@ constexpr unsigned kFlagL2Norm = 1u;
 constexpr unsigned kFlagSpOff = 2u;
 constexpr unsigned kFlagWindowOff = 4u;
 constexpr unsigned kFlagDebugWaitTimeout = 0x80000000u;  // test hook, see gdn.h
+constexpr unsigned kFlagDebugPeerTimeout = 0x40000000u;  // test hook, see gdn.h
+
+// Single-launch sequence parallelism (bf16, d = 128): one launch of a recurrent kernel runs pass A, the
+// start-state fix-up and pass B.  Each CTA takes a ticket (an atomic counter) when it starts and runs the
+// ticket-th item of the work lists that the gate scan built on the device, in this order: the pass-A items
+// that some fix-up needs, the pass-B items whose start needs no fix-up, the fix-up row blocks, the pass-B
+// items whose start is fixed up.  An item waits (bounded) only for items of lower tickets, which belong to
+// CTAs that started earlier: fix-up blocks for their (sequence, head)'s pass-A items, fixed-up pass-B items
+// for their fix-up blocks.  One schedule per direction.
+struct Sched {
+  int *hdr;                               // [0] ticket counter, [1] pass-A items, [2] pass-B items without
+                                          // fix-up, [3] (sequence, head) pairs with a fix-up, [4] fixed-up pass-B items
+  int *listA, *listBn, *listF, *listBf;   // (segment * H + head) * 2 + role; segment * H + head; n * H + head; as listBn
+  int *needA, *doneA, *doneF;             // per (sequence, head): pass-A items, pass-A items done, fix-up blocks done
+};
+constexpr int SCHED_HDR = 8;              // ints of each header
+constexpr int FIX_ROWS = 8;               // state rows per fix-up block
 
 struct FwdArgs {
   const void *q, *k, *v;
@@ -33,6 +50,8 @@ struct FwdArgs {
   // pass 1 the W^T, Ut^T tiles); with o == NULL pass 1 writes no output and only states and context
   void *t64, *t128, *tqkv;
   float *nrm;
+  Sched sched;  // single-launch sequence parallelism when sched_on (pass then names the pass-B kind, 1 or 2)
+  int sched_on;
 };
 
 // Chunk context tiles of every (chunk, head), fp16 row-major, written by the forward:
@@ -62,6 +81,8 @@ struct BwdArgs {
   unsigned flags;
   int pass;  // reverse chain: 0 segment starts / transitions, 1 per-chunk dS
   const float *nrm;  // context reciprocal norms (bf16, d = 128), see FwdArgs
+  Sched sched;       // single-launch sequence parallelism when sched_on, see FwdArgs
+  int sched_on;
 };
 
 struct FixupArgs {
@@ -86,10 +107,12 @@ struct RecArgs {
   unsigned flags;
 };
 
-int launch_plan(const Plan &p, const int *cu, int N, int T, int Lseg, int S_max, int CH_max, int *status,
-                cudaStream_t st);
+// zero: `nzero` ints cleared with the status words (the schedules' counters), or NULL
+int launch_plan(const Plan &p, const int *cu, int N, int T, int Lseg, int S_max, int CH_max, int *status, int *zero,
+                int nzero, cudaStream_t st);
+// sched[0] / sched[1]: forward / reverse schedules to build (hdr NULL: none)
 int launch_gate_scan(const Plan &p, const float *g, int H, int CH_max, float *gsum, int *status, int modes, int Lseg,
-                     int S_max, unsigned flags, cudaStream_t st);
+                     int S_max, unsigned flags, const Sched *sched, int NH, cudaStream_t st);
 int launch_fixup(const FixupArgs &a, int N, cudaStream_t st);
 
 int launch_fwd_chunk(const FwdArgs &a, bool is_bf16, int D, dim3 grid, cudaStream_t st);

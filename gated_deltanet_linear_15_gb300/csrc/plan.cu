@@ -13,6 +13,7 @@
 // from the composition S_start(j+1) = S_start(j) M_j + E_j over the segments of
 // the sequence (onedev.kr talk summary, paragraph on parallelism).  Rows of the
 // state are independent in this composition, so CTAs split the rows.
+#include "fixup.cuh"
 #include "kernels.h"
 
 namespace gdn {
@@ -20,13 +21,15 @@ namespace gdn {
 // One block.  Builds the per-sequence and per-segment tables; a malformed
 // cu_seqlens (not starting at 0, decreasing, or not ending at T) sets status
 // bit 1 and leaves every sequence empty, so the chunk kernels do nothing.
-__global__ void plan_kernel(Plan p, const int *cu, int N, int T, int Lseg, int S_max, int CH_max, int *status) {
+__global__ void plan_kernel(Plan p, const int *cu, int N, int T, int Lseg, int S_max, int CH_max, int *status,
+                            int *zero, int nzero) {
   pdl_trigger();
   pdl_wait();
   __shared__ int carry_c, carry_s, bad;
   __shared__ int wsum_c[32], wsum_s[32];
   const int tid = threadIdx.x, nt = blockDim.x;
   if (tid < 4 && status) status[tid] = 0;  // status word and the fix-up flags of this call
+  for (int i = tid; i < nzero; i += nt) zero[i] = 0;  // the schedules' counters
   __syncthreads();
   if (tid == 0) {
     carry_c = 0;
@@ -134,9 +137,10 @@ __global__ void plan_kernel(Plan p, const int *cu, int N, int T, int Lseg, int S
   }
 }
 
-int launch_plan(const Plan &p, const int *cu, int N, int T, int Lseg, int S_max, int CH_max, int *status,
-                cudaStream_t st) {
-  return (int)launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, st, p, cu, N, T, Lseg, S_max, CH_max, status);
+int launch_plan(const Plan &p, const int *cu, int N, int T, int Lseg, int S_max, int CH_max, int *status, int *zero,
+                int nzero, cudaStream_t st) {
+  return (int)launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, st, p, cu, N, T, Lseg, S_max, CH_max, status, zero,
+                         zero ? nzero : 0);
 }
 
 // One block per global chunk: the chunk's log-gates of 32 heads at a time are
@@ -144,12 +148,13 @@ int launch_plan(const Plan &p, const int *cu, int N, int T, int Lseg, int S_max,
 // then one warp per head scans its 64 values: gsum[c, h] = sum of g over the
 // chunk's tokens (each g raised to GATE_FLOOR first, as in the chunk kernels).
 __device__ void fixup_modes(const Plan &p, const float *gsum, int H, int Lseg, int S_max, unsigned flags, int *status,
-                            int i0, int stride);
+                            int i0, int stride, Sched fs, Sched bs, int NH);
 
 // With modes != 0 (a call with segments) the last block to finish also runs the fix-up mode scan
 // over every (segment, head) (status[3] counts finished blocks; the plan kernel zeroed it).
 __global__ void __launch_bounds__(256) gate_scan_kernel(Plan p, const float *g, int H, float *gsum, int *status,
-                                                        int modes, int Lseg, int S_max, unsigned flags) {
+                                                        int modes, int Lseg, int S_max, unsigned flags, Sched fs,
+                                                        Sched bs, int NH) {
   pdl_trigger();
   pdl_wait();
   __shared__ float tile[CH][33];
@@ -192,199 +197,106 @@ __global__ void __launch_bounds__(256) gate_scan_kernel(Plan p, const float *g, 
   __syncthreads();
   if (!last) return;
   __threadfence();
-  fixup_modes(p, gsum, H, Lseg, S_max, flags, status, threadIdx.x, blockDim.x);
+  fixup_modes(p, gsum, H, Lseg, S_max, flags, status, threadIdx.x, blockDim.x, fs, bs, NH);
 }
 
 int launch_gate_scan(const Plan &p, const float *g, int H, int CH_max, float *gsum, int *status, int modes, int Lseg,
-                     int S_max, unsigned flags, cudaStream_t st) {
+                     int S_max, unsigned flags, const Sched *sched, int NH, cudaStream_t st) {
   if (CH_max == 0) return 0;
+  Sched none;
+  memset(&none, 0, sizeof none);
   return (int)launch_pdl(gate_scan_kernel, dim3(CH_max), dim3(256), 0, st, p, g, H, gsum, status, modes, Lseg, S_max,
-                         flags);
+                         flags, sched ? sched[0] : none, sched ? sched[1] : none, NH);
 }
 
 // Does any segment start (forward) or end (reverse) need the exact fix-up?  status[1] / status[2]
 // become nonzero if so; the pass-A launches and the fix-ups of a direction without any such segment
-// return at once.  (segment, head) pairs i0, i0 + stride, ...; gsum read through L2 (other blocks
-// wrote it in this launch).
+// return at once.  With schedules (fs.hdr / bs.hdr set) it also builds each direction's work lists of
+// the single-launch sequence parallelism (see Sched): pass A of segment j is needed when the start of
+// segment j + 1 (forward; the end of segment j - 1 reversed) takes the fix-up, with the transition role
+// too when segment j's own start (end) does.  (segment, head) pairs i0, i0 + stride, ...; gsum read
+// through L2 (other blocks wrote it in this launch).  Called by one block, which synchronises itself.
+__device__ __forceinline__ bool window_ok(const float *gsum, int H, int h, int chunk0, int first, int count) {
+  // the start-mode rule of the chunk kernels (fwd_start_mode / bwd_start_mode) on L2-coherent loads:
+  // some w <= min(WMAX, count) with sum_{chunks first - w + 1 .. first} (forward) <= ln eps; the caller
+  // passes the chunks in scan order through `first` and the direction through the sign of count
+  float gs[WMAX];
+  const int n = count < 0 ? -count : count;
+#pragma unroll
+  for (int ww = 1; ww <= WMAX; ++ww) {
+    const int c = count < 0 ? first + ww - 1 : first - ww;
+    gs[ww - 1] = ww <= n ? __ldcg(gsum + (size_t)(chunk0 + c) * H + h) : 0.f;
+  }
+  float acc = 0.f;
+  bool warm = false;
+#pragma unroll
+  for (int ww = 1; ww <= WMAX; ++ww) {
+    acc += gs[ww - 1];
+    warm |= ww <= n && acc <= LN_EPS_WINDOW;
+  }
+  return warm;
+}
+
 __device__ void fixup_modes(const Plan &p, const float *gsum, int H, int Lseg, int S_max, unsigned flags, int *status,
-                            int i0, int stride) {
+                            int i0, int stride, Sched fs, Sched bs, int NH) {
   const bool window = !(flags & kFlagWindowOff);
   bool fwd_fix = false, bwd_fix = false;
+  // forward start of segment j needs the fix-up (j > 0 and no certified warm-up)
+  auto ffix = [&](int j, int chunk0, int h) { return j > 0 && !(window && window_ok(gsum, H, h, chunk0, j * Lseg, j * Lseg)); };
+  // reverse end of segment j needs the fix-up (j < nseg - 1 and no certified warm-up after it)
+  auto bfix = [&](int j, int nseg, int nchunks, int chunk0, int h) {
+    const int cend = min((j + 1) * Lseg, nchunks);
+    return j < nseg - 1 && !(window && window_ok(gsum, H, h, chunk0, cend, -(nchunks - cend)));
+  };
+  auto push = [](Sched &sc, int k, int v) {
+    int *list = k == 0 ? sc.listA : (k == 1 ? sc.listBn : sc.listBf);
+    list[atomicAdd(sc.hdr + 1 + (k == 0 ? 0 : (k == 1 ? 1 : 3)), 1)] = v;
+  };
   for (int i = i0; i < S_max * H; i += stride) {
     const int s = i / H, h = i % H;
     const int n = __ldcg(p.seg_seq + s);
     if (n < 0) continue;
     const int j = s - __ldcg(p.seq_seg0 + n), nseg = __ldcg(p.seq_nseg + n), chunk0 = __ldcg(p.seq_chunk0 + n);
     const int nchunks = (__ldcg(p.seq_len + n) + CH - 1) / CH;
-    const int cbeg = j * Lseg, cend = min((j + 1) * Lseg, nchunks);
-    // the start-mode rules of the chunk kernels, on L2-coherent loads of gsum: all WMAX sums of
-    // each window are loaded at once (no dependent load chain), then scanned
-    if (j > 0) {
-      float gs[WMAX];
-#pragma unroll
-      for (int ww = 1; ww <= WMAX; ++ww) gs[ww - 1] = ww <= cbeg ? __ldcg(gsum + (size_t)(chunk0 + cbeg - ww) * H + h) : 0.f;
-      bool warm = false;
-      if (window) {
-        float acc = 0.f;
-#pragma unroll
-        for (int ww = 1; ww <= WMAX; ++ww) {
-          acc += gs[ww - 1];
-          warm |= ww <= cbeg && acc <= LN_EPS_WINDOW;
-        }
+    const bool fj = ffix(j, chunk0, h), bj = bfix(j, nseg, nchunks, chunk0, h);
+    fwd_fix |= fj;
+    bwd_fix |= bj;
+    const int pair = n * H + h, sh = s * H + h;
+    if (fs.hdr) {
+      if (j < nseg - 1 && ffix(j + 1, chunk0, h)) {
+        push(fs, 0, sh * 2);
+        if (fj) push(fs, 0, sh * 2 + 1);
+        atomicAdd(fs.needA + pair, fj ? 2 : 1);
       }
-      fwd_fix |= !warm;
+      push(fs, fj ? 2 : 1, sh);
     }
-    if (j < nseg - 1) {
-      float gs[WMAX];
-#pragma unroll
-      for (int ww = 1; ww <= WMAX; ++ww)
-        gs[ww - 1] = cend + ww <= nchunks ? __ldcg(gsum + (size_t)(chunk0 + cend + ww - 1) * H + h) : 0.f;
-      bool warm = false;
-      if (window) {
-        float acc = 0.f;
-#pragma unroll
-        for (int ww = 1; ww <= WMAX; ++ww) {
-          acc += gs[ww - 1];
-          warm |= cend + ww <= nchunks && acc <= LN_EPS_WINDOW;
-        }
+    if (bs.hdr) {
+      if (j > 0 && bfix(j - 1, nseg, nchunks, chunk0, h)) {
+        push(bs, 0, sh * 2);
+        if (bj) push(bs, 0, sh * 2 + 1);
+        atomicAdd(bs.needA + pair, bj ? 2 : 1);
       }
-      bwd_fix |= !warm;
+      push(bs, bj ? 2 : 1, sh);
     }
   }
   if (fwd_fix) atomicOr(status + 1, 1);
   if (bwd_fix) atomicOr(status + 2, 1);
+  if (!fs.hdr && !bs.hdr) return;
+  __syncthreads();
+  // fix-up row blocks: every (sequence, head) with a pass-A item
+  for (int pair = i0; pair < NH; pair += stride) {
+    if (fs.hdr && __ldcg(fs.needA + pair) > 0) fs.listF[atomicAdd(fs.hdr + 3, 1)] = pair;
+    if (bs.hdr && __ldcg(bs.needA + pair) > 0) bs.listF[atomicAdd(bs.hdr + 3, 1)] = pair;
+  }
 }
 
-// Start-state fix-up (forward: S_start[j+1] = S_start[j] M_j + E_j over the segments of one (sequence,
-// head); the reverse chain mirrors it), the sequential composition of the segment summaries
-// (onedev.kr talk summary, paragraph on parallelism).  grid (D / FIX_ROWS, H, N): FIX_ROWS rows of the
-// state per CTA, 256 threads.  The composition is serial over segments, but every step's inputs (M_j
-// and E_j's rows) are independent of the chain, so they stream through a two-stage shared-memory ring
-// by cp.async: step i computes while step i + 1's 64 KB transition lands.  The segment start modes
-// (which segments take the fix-up at all) are decided up front, one segment per thread.
-constexpr int FIX_ROWS = 8;
-constexpr int FIX_MODES = 2048;  // segments per sequence whose modes are kept in shared memory
-
-template <int D> constexpr size_t fixup_smem_bytes() { return 2 * ((size_t)D * D + FIX_ROWS * D) * sizeof(float); }
-
+// grid (D / FIX_ROWS, H, N), 256 threads: one fix-up row block per CTA (see fixup_rows)
 template <int D>
 __global__ void __launch_bounds__(256, 1) fixup_kernel(FixupArgs a) {
   pdl_trigger();
   pdl_wait();
-  extern __shared__ __align__(16) float fx_sm[];  // 2 stages of [M (D x D) | E rows (FIX_ROWS x D)]
-  __shared__ float cur[FIX_ROWS][D];
-  __shared__ signed char fix_mode[FIX_MODES];  // per segment: 0 no fix-up, 1 fix-up from E alone, 2 from E and M
-  __shared__ int nwork;
-  __shared__ short work[FIX_MODES];            // target segment of each working step, in chain order
-  const int rb = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
-  const int H = a.H;
-  if (a.fixflag && *a.fixflag == 0) return;  // no segment of this direction needs the exact fix-up
-  const int nseg = a.plan.seq_nseg[n];
-  if (nseg <= 1) return;
-  const int seg0 = a.plan.seq_seg0[n], chunk0 = a.plan.seq_chunk0[n];
-  const int nchunks = (a.plan.seq_len[n] + CH - 1) / CH;
-  const bool window = !(a.flags & kFlagWindowOff);
-  const size_t DD = (size_t)D * D;
-  constexpr int CPT = D / 32;  // columns per thread
-  const int tid = threadIdx.x;
-  const int r = tid >> 5;
-  const int c0 = (tid & 31) * CPT;
-  const int row = rb * FIX_ROWS + r;
-  // mode of segment j as the target of a fix-up step: is its start (end, reversed) corrected, and is the
-  // segment it is composed from itself corrected (then its transition M takes part)
-  auto start_mode = [&](int j) {
-    int w;
-    if (!a.reverse) return fwd_start_mode(a.gsum, H, h, chunk0, j * a.Lseg, j, window, &w);
-    return bwd_start_mode(a.gsum, H, h, chunk0, min((j + 1) * a.Lseg, nchunks), nchunks, j, nseg, window, &w);
-  };
-  const bool small = nseg <= FIX_MODES;
-  if (small) {
-    for (int j = tid; j < nseg; j += blockDim.x) fix_mode[j] = start_mode(j) == START_FIXUP;
-    __syncthreads();
-    if (tid == 0) {  // working steps in chain order: target jt, composed from js (forward js = jt - 1)
-      int nw = 0;
-      for (int step = 0; step < nseg - 1; ++step) {
-        const int jt = a.reverse ? nseg - 2 - step : step + 1, js = a.reverse ? jt + 1 : jt - 1;
-        if (fix_mode[jt]) work[nw++] = (short)(fix_mode[js] ? jt | 0x4000 : jt);
-      }
-      nwork = nw;
-    }
-    __syncthreads();
-  }
-  const int nw = small ? nwork : nseg - 1;
-  // step i -> (target jt, uses M); for very long plans the modes are evaluated on the fly
-  auto step_of = [&](int i, int &jt, bool &withM) {
-    if (small) {
-      const int v = work[i];
-      jt = v & 0x3fff;
-      withM = (v & 0x4000) != 0;
-      return true;
-    }
-    jt = a.reverse ? nseg - 2 - i : i + 1;
-    if (start_mode(jt) != START_FIXUP) return false;
-    withM = start_mode(a.reverse ? jt + 1 : jt - 1) == START_FIXUP;
-    return true;
-  };
-  auto issue = [&](int i) {  // cp.async of step i's M (if used) and E rows into stage i & 1
-    int jt;
-    bool withM;
-    if (i < nw && step_of(i, jt, withM)) {
-      const int js = a.reverse ? jt + 1 : jt - 1;
-      const size_t src = ((size_t)(seg0 + js) * H + h) * DD;
-      float *st = fx_sm + (size_t)(i & 1) * (DD + FIX_ROWS * D);
-      if (withM)
-        for (int e = tid; e < (int)(DD / 4); e += blockDim.x) cp_async16(st + 4 * e, a.M + src + 4 * e, true);
-      for (int e = tid; e < FIX_ROWS * D / 4; e += blockDim.x)
-        cp_async16(st + DD + 4 * e, a.E + src + (size_t)rb * FIX_ROWS * D + 4 * e, true);
-    }
-    cp_async_commit();  // one group per step, empty or not
-  };
-  issue(0);
-  issue(1);
-  for (int i = 0; i < nw; ++i) {
-    int jt;
-    bool withM;
-    const bool active = step_of(i, jt, withM);
-    asm volatile("cp.async.wait_group 1;\n" ::: "memory");  // step i's group has landed (i + 1's may be in flight)
-    __syncthreads();
-    if (active) {
-      const float *st = fx_sm + (size_t)(i & 1) * (DD + FIX_ROWS * D);
-      float acc[CPT];
-#pragma unroll
-      for (int t = 0; t < CPT; ++t) acc[t] = st[DD + r * D + c0 + t];
-      if (withM) {  // cur holds the corrected state of the source segment (the previous working step)
-#pragma unroll 8
-        for (int k = 0; k < D; ++k) {
-          const float x = cur[r][k];
-          float m[CPT];
-          if constexpr (CPT == 4) {
-            const float4 t4 = *reinterpret_cast<const float4 *>(st + (size_t)k * D + c0);
-            m[0] = t4.x;
-            m[1] = t4.y;
-            m[2] = t4.z;
-            m[3] = t4.w;
-          } else {
-            const float2 t2 = *reinterpret_cast<const float2 *>(st + (size_t)k * D + c0);
-            m[0] = t2.x;
-            m[1] = t2.y;
-          }
-#pragma unroll
-          for (int t = 0; t < CPT; ++t) acc[t] = fmaf(x, m[t], acc[t]);
-        }
-      }
-      __syncthreads();  // every thread has read cur and this stage
-      float *out = a.out + ((size_t)(seg0 + jt) * H + h) * DD + (size_t)row * D;
-#pragma unroll
-      for (int t = 0; t < CPT; ++t) {
-        cur[r][c0 + t] = acc[t];
-        out[c0 + t] = acc[t];
-      }
-    } else {
-      __syncthreads();
-    }
-    issue(i + 2);  // into the stage just read
-  }
-  asm volatile("cp.async.wait_all;\n" ::: "memory");
+  extern __shared__ __align__(16) unsigned char fx_smem[];
+  fixup_rows<D>(a, blockIdx.x, blockIdx.y, blockIdx.z, fx_smem);
 }
 
 int launch_fixup(const FixupArgs &a, int N, cudaStream_t st) {

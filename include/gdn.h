@@ -66,11 +66,22 @@ enum {
   GDN_L2NORM_QK = 1u,  /* normalise q and k per token in-kernel: x / sqrt(|x|^2 + 1e-6)   */
   GDN_SP_OFF = 2u,     /* no intra-card sequence parallelism: one segment per sequence    */
   GDN_WINDOW_OFF = 4u, /* never skip the segment-start correction (always exact path)     */
+  /* bf16, d = 128: run pass A, the start-state fix-up and pass B of each direction as one
+   * launch (CTAs take work items in start order and wait, bounded, for the items they need)
+   * instead of three.  Results are identical; measured on GB300 it is not faster (the
+   * segments that need the fix-up keep the serial pass A -> fix-up -> pass B path, and the
+   * launches it removes overlap their neighbours), so it is off by default. */
+  GDN_SP_SINGLE_LAUNCH = 8u,
   /* Test hook for the bounded device waits (bf16, d = 128 chunk kernels): each tensor-core
    * kernel of the call first waits on a barrier that nothing arrives at, with a short bound;
    * the wait expires, sets status value 4 (see gdn_get_device_status) and the kernel returns
    * before any copy or product.  Outputs of such a call are not written. */
-  GDN_DEBUG_WAIT_TIMEOUT = 0x80000000u
+  GDN_DEBUG_WAIT_TIMEOUT = 0x80000000u,
+  /* Test hook for the bounded waits between CTAs of the single-launch sequence parallelism
+   * (GDN_SP_SINGLE_LAUNCH, with segments that take the exact fix-up): every segment whose start (end, reversed) is
+   * fixed up waits for one more fix-up block than exists, with a short bound; the wait expires, sets
+   * status value 16 and that segment's CTA returns without writing its outputs. */
+  GDN_DEBUG_PEER_TIMEOUT = 0x40000000u
 };
 
 /* Problem description shared by the forward, the backward and the size queries. */
@@ -81,7 +92,7 @@ typedef struct {
   int num_seqs;               /* number of sequences when cu_seqlens != NULL             */
   gdn_dtype dtype;            /* dtype of q, k, v, o, dO, dq, dk, dv                     */
   float scale;                /* o_t = S_t (scale * q_t), applied after normalisation    */
-  unsigned flags;             /* GDN_L2NORM_QK | GDN_SP_OFF | GDN_WINDOW_OFF             */
+  unsigned flags;             /* GDN_L2NORM_QK | GDN_SP_OFF | GDN_WINDOW_OFF | GDN_SP_SINGLE_LAUNCH */
   int seg_chunks;             /* chunks per segment for sequence parallelism; 0 = auto   */
   int reserved[3];            /* must be 0                                               */
 } gdn_shape;
@@ -101,7 +112,11 @@ size_t gdn_bwd_workspace_size(const gdn_shape *shape);
  * effective sliding window); pass A over segments whose start must be
  * corrected (state from zero plus the composed d_k x d_k transition --
  * paragraph on parallelism); the sequential start-state fix-up; pass B, the
- * fused WY + state pass + output over every segment.
+ * fused WY + state pass + output over every segment.  With bf16, d = 128 and
+ * GDN_SP_SINGLE_LAUNCH, pass A, the fix-up and pass B are one launch: its CTAs
+ * take work items in start order from lists the gate scan builds, and an item
+ * that needs others' results (a fix-up, a fixed-up segment) waits for them
+ * with a bound; the segments that need no fix-up run alongside pass A.
  * Decay ratios gamma_r / gamma_i inside a chunk are factored as
  * exp(G_r - G_mid) exp(G_mid - G_i) (G = in-chunk prefix of g, G_mid its
  * value at the chunk middle), one exponential per token (same page, paragraph
@@ -248,7 +263,10 @@ int gdn_recurrent_fwd(const gdn_shape *shape, const void *q, const void *k, cons
  *              segments than the workspace was sized for;
  *   bit 2 (4): a tensor-core completion wait ran past its iteration limit (the
  *              kernel stopped that work item and returned);
- *   bit 3 (8): a TMA tile-load wait ran past its iteration limit (likewise).
+ *   bit 3 (8): a TMA tile-load wait ran past its iteration limit (likewise);
+ *   bit 4 (16): a wait for another CTA's work item of the single-launch
+ *              sequence parallelism ran past its limit (the waiting item
+ *              returned without output).
  * Returns the word (0 = clean), or -1 on a CUDA error.  `workspace` is the one
  * passed to that call, or NULL for a call of gdn_chunk_fwd_static (then the
  * word is read from the static scratch on the current device).  The status
@@ -257,7 +275,7 @@ int gdn_recurrent_fwd(const gdn_shape *shape, const void *q, const void *k, cons
 int gdn_get_device_status(const gdn_shape *shape, const void *workspace, gdn_stream_t stream);
 
 /* Maps a status word of gdn_get_device_status to one status code: GDN_OK (0),
- * GDN_ERR_INVALID_ARG (bit 1), GDN_ERR_TIMEOUT (bits 2, 3), GDN_ERR_NUMERIC
+ * GDN_ERR_INVALID_ARG (bit 1), GDN_ERR_TIMEOUT (bits 2, 3, 4), GDN_ERR_NUMERIC
  * (bit 0), in that order of precedence; GDN_ERR_CUDA for -1. */
 int gdn_device_status_code(int word);
 

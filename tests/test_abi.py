@@ -57,7 +57,8 @@ def test_status_strings(lib):
 
 @pytest.mark.parametrize("word,code", [
     (0, _lib.GDN_OK), (1, _lib.GDN_ERR_NUMERIC), (2, _lib.GDN_ERR_INVALID_ARG), (3, _lib.GDN_ERR_INVALID_ARG),
-    (4, _lib.GDN_ERR_TIMEOUT), (8, _lib.GDN_ERR_TIMEOUT), (5, _lib.GDN_ERR_TIMEOUT), (-1, _lib.GDN_ERR_CUDA),
+    (4, _lib.GDN_ERR_TIMEOUT), (8, _lib.GDN_ERR_TIMEOUT), (16, _lib.GDN_ERR_TIMEOUT), (5, _lib.GDN_ERR_TIMEOUT),
+    (-1, _lib.GDN_ERR_CUDA),
 ])
 def test_device_status_code(lib, word, code):
     """Status words map to one code: malformed cu_seqlens first, then an expired wait, then the numeric guard."""

@@ -44,13 +44,17 @@ def test_no_initial_state_no_norm():
     compare(run_gpu(x), run_oracle(x), TOL["bf16"])
 
 
+@pytest.mark.parametrize("single_launch", [False, True], ids=["three_launches", "single_launch"])
 @pytest.mark.parametrize("seg_chunks", [1, 2, 3])
 @pytest.mark.parametrize("window", [True, False])
-def test_sequence_parallel_exact_and_window(seg_chunks, window):
+def test_sequence_parallel_exact_and_window(seg_chunks, window, single_launch):
     """Forced segmentation: slow decay (alpha ~ 1) exercises pass A + fix-up; with the
-    window on, fast-decay heads take the warm-up path instead."""
+    window on, fast-decay heads take the warm-up path instead.  Both the three-launch form and
+    the single launch whose CTAs wait for each other's work items (GDN_SP_SINGLE_LAUNCH)."""
     x = make_inputs("long_h8_t65536", DEV, T=64 * 7 + 9, H=8, with_S0=True, with_dST=True)
-    compare(run_gpu(x, seg_chunks=seg_chunks, window=window), run_oracle(x), TOL["bf16"])
+    for saved in (False, True):
+        compare(run_gpu(x, seg_chunks=seg_chunks, window=window, single_launch=single_launch, saved=saved),
+                run_oracle(x), TOL["bf16"])
 
 
 def test_sp_on_off_agree():

@@ -76,3 +76,28 @@ def test_numeric_guard_backward():
     g.chunk_gated_delta_rule_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["dO"], x["S0"], None, None,
                                  x["scale"], x["l2norm"], workspace=ws)
     assert g.gdn_get_device_status(shape, ws) & 1
+
+
+@pytest.mark.parametrize("direction", ["forward", "backward"])
+def test_forced_peer_wait_expiry_sets_status_and_returns(direction):
+    """The single-launch sequence parallelism's (GDN_SP_SINGLE_LAUNCH) bounded wait between CTAs: with the
+    GDN_DEBUG_PEER_TIMEOUT hook every fixed-up segment waits for a fix-up block that never
+    comes; the wait expires, the kernel records status value 16 and the call ends (no hang).
+    A clean call afterwards is correct."""
+    x = make_inputs("long_h8_t65536", "cuda", T=64 * 7 + 9, H=8, seed=25, with_S0=True)
+    shape = g.make_shape(x["q"], x["v"], scale=x["scale"], l2norm=x["l2norm"], seg_chunks=1, window=False,
+                         single_launch=True)
+    shape.flags |= _lib.GDN_DEBUG_PEER_TIMEOUT
+    if direction == "forward":
+        rc, _, _, ws = _fwd(x, shape)
+        assert rc == 0
+    else:
+        ws = torch.empty(g.gdn_bwd_workspace_size(shape), dtype=torch.uint8, device="cuda")
+        grads = [torch.empty_like(x[k]) for k in ("q", "k", "v", "g", "beta", "S0")]
+        rc = g.gdn_chunk_bwd(shape, x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], x["dO"], None, *grads, ws)
+        assert rc == 0
+    torch.cuda.synchronize()  # the kernels returned: no hang
+    word = g.gdn_get_device_status(shape, ws)
+    assert word & 16
+    assert g.gdn_device_status_code(word) == _lib.GDN_ERR_TIMEOUT
+    _clean_call_is_correct(x)
