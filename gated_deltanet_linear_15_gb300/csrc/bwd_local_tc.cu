@@ -26,6 +26,7 @@
 //   P9 Ka += K^T (dN + dN^T)->T3
 //                            R9: dk out (Ka + cdec Kb);  dg (reverse cumsum), dbeta
 #include <cstddef>
+#include <type_traits>
 
 #include "chunk_common.cuh"
 #include "kernels.h"
@@ -392,6 +393,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     if (row < 64) {
       const int r = row;
       float rs = 0.f, cs = 0.f;
+      auto r5 = [&](auto pw) {
 #pragma unroll 1
       for (int q4 = 0; q4 < 2; ++q4) {
         const int cb = c0 + q4 * 8;
@@ -401,7 +403,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
         const uint4 raw = *reinterpret_cast<const uint4 *>(pp);
         const __half *ph = reinterpret_cast<const __half *>(&raw);
         float rt[8];
-        gratio8(G, r, cb, rt);
+        ratio8<decltype(pw)::value>(G, r, cb, rt);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float dpv = v[i];
@@ -414,6 +416,9 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
         const float a = colsum8(zc);
         if ((lane >> 3) == q4) cs = a;
       }
+      };
+      if (G.pw) r5(std::true_type{});
+      else r5(std::false_type{});
       sm.part[16 + wg][r] = rs;          // row sums of Z, per 16-column block
       if (lane < 16) sm.part[10 + wq][c0 + lane] = cs;  // column sums of Z, per row quarter (wq 0/1)
     }
@@ -483,6 +488,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     if (row < 64) {
       const int r = row;
       float cs = 0.f, ca = 0.f, cv = 0.f, rwx = 0.f;
+      auto r6 = [&](auto pw) {
 #pragma unroll 1
       for (int q4 = 0; q4 < 2; ++q4) {
         const int cb = c0 + q4 * 8;
@@ -493,7 +499,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
         const uint4 xraw = *reinterpret_cast<const uint4 *>(sm.x2 + chunk_off(r, cb));
         const __half *xh = reinterpret_cast<const __half *>(&xraw);
         float rt[8], bt[8];
-        gratio8(G, r, cb, rt);
+        ratio8<decltype(pw)::value>(G, r, cb, rt);
         ld8f(gbeta + cb, bt);
         float am[8], xm[8];
 #pragma unroll
@@ -515,6 +521,9 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
           cv = e;
         }
       }
+      };
+      if (G.pw) r6(std::true_type{});
+      else r6(std::false_type{});
       if (lane < 16) sm.part[8 + wq][c0 + lane] = cs;
       if (lane < 16) sm.part[10 + wq][c0 + lane] = ca;
       if (lane < 16) sm.part[14 + wq][c0 + lane] = cv;

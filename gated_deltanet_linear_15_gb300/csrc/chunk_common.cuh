@@ -120,6 +120,15 @@ static __device__ __noinline__ float gratio_pw(const Gates &gt, int r, int c) {
 __device__ __forceinline__ float gratio(const Gates &gt, int r, int c) {
   return gt.pw ? gratio_pw(gt, r, c) : gt.gp[r] * gt.rgp[c];
 }
+// the ratios for columns c, c + 1 (c even) of row r, one check for both
+__device__ __forceinline__ float2 gratio2(const Gates &gt, int r, int c) {
+  if (!gt.pw) {
+    const float2 rg = *reinterpret_cast<const float2 *>(gt.rgp + c);
+    const float gr = gt.gp[r];
+    return make_float2(gr * rg.x, gr * rg.y);
+  }
+  return make_float2(gratio_pw(gt, r, c), gratio_pw(gt, r, c + 1));
+}
 
 // 16 consecutive floats from 16-byte aligned shared memory (four vector loads)
 __device__ __forceinline__ void ld16f(const float *p, float (&v)[16]) {
@@ -187,9 +196,11 @@ __device__ __forceinline__ bool gate_prefix(const float *g, Gates &gt) {
   return pw;
 }
 
-// o[i] = gamma_r / gamma_{cb + i} for cb + i <= r, 0 above the diagonal (eight columns from cb, a multiple of 8)
-__device__ __forceinline__ void gratio8(const Gates &gt, int r, int cb, float (&o)[8]) {
-  if (!gt.pw) {
+// o[i] = gamma_r / gamma_{cb + i} for cb + i <= r, 0 above the diagonal (eight columns from cb, a multiple of 8),
+// with the form chosen at compile time: read-out loops are instantiated once per form and pick one by Gates::pw,
+// so the factored loop carries none of the pairwise code
+template <bool PW> __device__ __forceinline__ void ratio8(const Gates &gt, int r, int cb, float (&o)[8]) {
+  if constexpr (!PW) {
     const float4 a = reinterpret_cast<const float4 *>(gt.rgp + cb)[0], b = reinterpret_cast<const float4 *>(gt.rgp + cb)[1];
     const float gr = gt.gp[r];
     o[0] = gr * a.x; o[1] = gr * a.y; o[2] = gr * a.z; o[3] = gr * a.w;
@@ -198,6 +209,18 @@ __device__ __forceinline__ void gratio8(const Gates &gt, int r, int cb, float (&
     const float Gr = gt.Ghi[r], Grl = gt.Glo[r];
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[i] = cb + i <= r ? expf(two_diff(Gr, Grl, gt.Ghi[cb + i], gt.Glo[cb + i])) : 0.f;
+  }
+}
+// the same with the form chosen at run time (the pairwise form element by element out of line)
+__device__ __forceinline__ void gratio8(const Gates &gt, int r, int cb, float (&o)[8]) {
+  if (!gt.pw) {
+    const float4 a = reinterpret_cast<const float4 *>(gt.rgp + cb)[0], b = reinterpret_cast<const float4 *>(gt.rgp + cb)[1];
+    const float gr = gt.gp[r];
+    o[0] = gr * a.x; o[1] = gr * a.y; o[2] = gr * a.z; o[3] = gr * a.w;
+    o[4] = gr * b.x; o[5] = gr * b.y; o[6] = gr * b.z; o[7] = gr * b.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = cb + i <= r ? gratio_pw(gt, r, cb + i) : 0.f;
   }
 }
 

@@ -259,17 +259,21 @@ __global__ void __launch_bounds__(PT, 2)
         }
       } else {
         const int r = row - 64;
+        auto pread = [&](auto pw) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float w8[8], rt[8];
-          gratio8(sm.gt, r, c0 + 8 * q, rt);
+          for (int q = 0; q < 4; ++q) {
+            float w8[8], rt[8];
+            ratio8<decltype(pw)::value>(sm.gt, r, c0 + 8 * q, rt);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int c = c0 + 8 * q + i;
-            w8[i] = c <= r ? v[8 * q + i] * rt[i] : 0.f;
+            for (int i = 0; i < 8; ++i) {
+              const int c = c0 + 8 * q + i;
+              w8[i] = c <= r ? v[8 * q + i] * rt[i] : 0.f;
+            }
+            st_chunk_f16(sm.p + chunk_off(r, c0 + 8 * q), w8);
           }
-          st_chunk_f16(sm.p + chunk_off(r, c0 + 8 * q), w8);
-        }
+        };
+        if (sm.gt.pw) pread(std::true_type{});
+        else pread(std::false_type{});
       }
     }
     fence_before();
@@ -281,10 +285,11 @@ __global__ void __launch_bounds__(PT, 2)
     wy_inverse<false, false>(sm.nf, LN, beta, sm.ys, [&](int r, int c, float a0, float a1) {
       const float2 bb = *reinterpret_cast<const float2 *>(beta + c);
       const float x0 = a0 * bb.x, x1 = a1 * bb.y;
+      const float2 rt = gratio2(G, r, c);
       const uint32_t off = sw128_offset(r, c);
       *reinterpret_cast<__half2 *>(sm.x1 + off) = __floats2half2_rn(x0, x1);
       *reinterpret_cast<__half2 *>(sm.x2 + off) =
-          __floats2half2_rn(c <= r ? x0 * gratio(G, r, c) : 0.f, c + 1 <= r ? x1 * gratio(G, r, c + 1) : 0.f);
+          __floats2half2_rn(c <= r ? x0 * rt.x : 0.f, c + 1 <= r ? x1 * rt.y : 0.f);
       *reinterpret_cast<__half2 *>(sm.ah + off) = __floats2half2_rn(a0, a1);
     }, it == 0);  // ends with a proxy fence and a barrier; the zero upper blocks persist across items
 
