@@ -81,12 +81,11 @@ def job_throughput(total_ms, world, tokens_per_rank_step, steps):
 # keyed by (profiler name, workload); valid only while the kernel's sources hash to the value
 # recorded with it (otherwise the roofline reports traffic null).  Summaries: profiles/*.md.
 NCU_TRAFFIC = {
-    ("bwd_local", "prefill_h32_t8192"): (959556864, "bwd_local_tc.cu", "c9d8c043af0ae028"),
-    ("fwd_chunk", "prefill_h32_t8192"): (615529472, "fwd_tc.cu", "aa2f978c51b5690f"),
-    ("fwd_prep", "prefill_h32_t8192"): (514273536, "fwd_prep_tc.cu", "d7ad282d62ba273c"),
-    ("bwd_chain", "prefill_h32_t8192"): (444592640, "bwd_chain_tc.cu", "85a6b5f1c290cd45"),
+    ("bwd_local", "prefill_h32_t8192"): (960259584, "bwd_local_tc.cu", "47a3d9e8f898bf14"),
+    ("fwd_prep", "prefill_h32_t8192"): (514429952, "fwd_prep_tc.cu", "6353d3e852b92fb8"),
+    ("bwd_chain", "prefill_h32_t8192"): (422545408, "bwd_chain_tc.cu", "a89b9bca45ef57e9"),
 }
-KERNEL_COMMON = ["chunk_common.cuh", "umma.cuh", "common.cuh", "kernels.h"]
+KERNEL_COMMON = ["chunk_common.cuh", "umma.cuh", "common.cuh", "kernels.h", "fixup.cuh"]
 
 
 def measured_traffic(kernel, workload):
