@@ -77,13 +77,6 @@ __device__ __forceinline__ void st_chunk_f16(uint8_t *dst, const float *v) {
   for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
   *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<uint4 *>(h);
 }
-// fp16 element (row, col) of a [rows][64]-per-half-tile swizzled operand whose
-// feature blocks sit `blk` bytes apart
-__device__ __forceinline__ float ld_f16(const uint8_t *t, int row, int col, int blk) {
-  const uint8_t *p = t + (col >> 6) * blk + sw128_offset(row, col & 63);
-  return __half2float(*reinterpret_cast<const __half *>(p));
-}
-
 
 // v[8] per lane -> lane l holds the sum over the warp's lanes of v[l % 8]
 __device__ __forceinline__ float colsum8(float (&v)[8]) {
@@ -129,6 +122,29 @@ __device__ __forceinline__ bool wbar_or(bool pred) {
 
 // byte offset of the 16-byte chunk holding columns [cb, cb + 8) of row r in a swizzled tile
 __device__ __forceinline__ uint32_t chunk_off(int r, int cb) { return r * 128 + ((((cb & 63) >> 3) ^ (r & 7)) << 4); }
+
+// Transposing read-outs of a [feature lanes][token columns] accumulator (dv, dq, dk): warp (wq, wg) reads
+// features 32 wq + ls .. + 15 (ls = 0, 16) and tokens c0 .. c0 + 15 as fragments (tmem_ld_frag2), so value
+// 2m + e of lane t is feature 32 wq + ls + 8 (m & 1) + t/4, token c0 + 8 (m >> 1) + 2 (t%4) + e; the four
+// 8 x 8 matrices m move between those fragments and a token-major [token][feature] tile (feature halves
+// `blk` bytes apart, 128-byte swizzled rows) by one ldmatrix / stmatrix .trans, for which lane t addresses
+// the 16 bytes of token c0 + 8 ((t/8) >> 1) + t%8, features from 32 wq + ls + 8 ((t/8) & 1).
+__device__ __forceinline__ uint32_t frag_addr(const uint8_t *base, int blk, int wq, int ls, int c0, int lane) {
+  const int m = lane >> 3;
+  const int tk = c0 + 8 * (m >> 1) + (lane & 7);
+  const int fs = 32 * wq + ls + 8 * (m & 1);
+  return smem_u32(base + (fs >> 6) * blk + chunk_off(tk, fs));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&b);
+}
+__device__ __forceinline__ float2 unpack_f16(uint32_t r) { return __half22float2(*reinterpret_cast<const __half2 *>(&r)); }
+// a per-token factor at this lane's four tokens c0 + 2 (t%4) + {0, 1, 8, 9} (16-byte aligned arrays)
+__device__ __forceinline__ void tok4(const float *p, int ta, float (&v)[4]) {
+  const float2 a = *reinterpret_cast<const float2 *>(p + ta), b = *reinterpret_cast<const float2 *>(p + ta + 8);
+  v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+}
 
 }  // namespace
 
@@ -196,10 +212,6 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
         *reinterpret_cast<uint4 *>(gp + ((size_t)(t0 + r) * H + hh) * D + cc * 8) =
             *reinterpret_cast<const uint4 *>(stg + (cc >> 3) * HT + r * 128 + (((cc & 7) ^ (r & 7)) << 4));
     }
-  };
-  // bf16 element (token, feature) of such a staging tile
-  auto stg_at = [&](uint8_t *stg, int tkn, int f) {
-    return reinterpret_cast<bf16 *>(stg + (f >> 6) * HT + sw128_offset(tkn, f & 63));
   };
 
   // Work items (chunk gc, head h) = (item / H, item % H), strided over the persistent CTAs; chunks past
@@ -448,22 +460,41 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
   }
   {  // under P6: dV^T (lanes d_v, columns token) staged as bf16 dv[token][d_v] in dob (dO is dead; <dV, v>
      // comes with R6 as colsum(X2 M2)); gam <Qa, q^> per token over d_k (Qa = S0^T dO^T: the dO S0 part
-     // of dq^ dotted with q^)
-    float t3 = 0.f;
+     // of dq^ dotted with q^).  Fragment read-outs: the transposes are ldmatrix / stmatrix
+    float s[4] = {0.f, 0.f, 0.f, 0.f};  // sums over this lane's features at its four tokens
 #pragma unroll 1
-    for (int q4 = 0; q4 < 2; ++q4) {
-      const int cb = c0 + q4 * 8;
-      float v[8], w[8], gm[8];
-      tmem_ld8x2(tm + tl + T6 + cb, w, tm + tl + T5 + cb, v);
+    for (int ls = 0; ls < 32; ls += 16) {
+      const uint32_t tq = tm + tl + ((uint32_t)ls << 16) + c0;
+      float w[8], v[8];
+      tmem_ld_frag2(tq + T6, w, tq + T5, v);
+      uint32_t pk[4], qf[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) *stg_at(sm.dob, cb + i, row) = __float2bfloat16_rn(w[i]);
-      ld8f(G.gam + cb, gm);
+      for (int m = 0; m < 4; ++m) pk[m] = pack_bf16(w[2 * m], w[2 * m + 1]);
+      stmatrix_x4_trans(frag_addr(sm.dob, HT, wq, ls, c0, lane), pk);
+      ldmatrix_x4_trans(frag_addr(sm.kq + HT, 2 * HT, wq, ls, c0, lane), qf);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] *= gm[i] * ld_f16(sm.kq + HT, cb + i, row, 2 * HT);
-      const float a3 = colsum8(v);
-      if ((lane >> 3) == q4) t3 = a3;
+      for (int m = 0; m < 4; ++m) {
+        const float2 q2 = unpack_f16(qf[m]);
+        s[(m >> 1) * 2] += v[2 * m] * q2.x;
+        s[(m >> 1) * 2 + 1] += v[2 * m + 1] * q2.y;
+      }
     }
-    if (lane < 16) sm.part[12 + wq][c0 + lane] = t3;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {  // over the eight lanes that share this lane's tokens
+      s[k] += __shfl_xor_sync(0xffffffffu, s[k], 4);
+      s[k] += __shfl_xor_sync(0xffffffffu, s[k], 8);
+      s[k] += __shfl_xor_sync(0xffffffffu, s[k], 16);
+    }
+    if (lane < 4) {
+      const int ta = c0 + 2 * lane;
+      float gm[4];
+      tok4(G.gam, ta, gm);
+      float *dst = sm.part[12 + wq];
+      dst[ta] = gm[0] * s[0];
+      dst[ta + 1] = gm[1] * s[1];
+      dst[ta + 8] = gm[2] * s[2];
+      dst[ta + 9] = gm[3] * s[3];
+    }
   }
   fence_before();
   fence_async_smem();
@@ -571,34 +602,41 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
   {  // under P8: dq raw = (scale dq^ - q^ (q^ . dq^) / scale) / |q|   (or scale dq^ without normalisation),
      // staged in ds (dS is dead: its last reader, Kb, completed under P6)
     const float rscale = 1.f / a.scale;
+    const int ta = c0 + 2 * (lane & 3);  // this lane's tokens ta, ta + 1, ta + 8, ta + 9
+    float gm[4], dt[4], nqv[4];
+    tok4(G.gam, ta, gm);
+    if (l2) {  // q^ . dq^ = gam <Qa, q^> + sum_s dP * P (the Qb part: row sums of dP * P)
+      float p1[4];
+      tok4(sm.acc[5], ta, dt);
+      tok4(sm.acc[2], ta, p1);
+      tok4(sm.nq, ta, nqv);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) dt[k] = (dt[k] + p1[k]) * rscale;
+    }
 #pragma unroll 1
-    for (int q4 = 0; q4 < 2; ++q4) {
-      const int cb = c0 + q4 * 8;
+    for (int ls = 0; ls < 32; ls += 16) {
+      const uint32_t tq = tm + tl + ((uint32_t)ls << 16) + c0;
       float qa[8], qb[8];
-      tmem_ld8x2(tm + tl + T5 + cb, qa, tm + tl + T7 + cb, qb);
-      float gm[8], dt[8], nqv[8];
-      ld8f(G.gam + cb, gm);
-      if (l2) {  // q^ . dq^ = gam <Qa, q^> + sum_s dP * P (the Qb part: row sums of dP * P)
-        float p0[8], p1[8];
-        ld8f(sm.acc[5] + cb, p0);
-        ld8f(sm.acc[2] + cb, p1);
-        ld8f(sm.nq + cb, nqv);
+      tmem_ld_frag2(tq + T5, qa, tq + T7, qb);
+      uint32_t qf[4], pk[4];
+      if (l2) ldmatrix_x4_trans(frag_addr(sm.kq + HT, 2 * HT, wq, ls, c0, lane), qf);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) dt[i] = p0[i] + p1[i];
-      }
+      for (int m = 0; m < 4; ++m) {
+        float o[2];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int tkn = cb + i;
-        const float dq = qb[i] + gm[i] * qa[i];
-        float o;
-        if (l2) {
-          const float qv = ld_f16(sm.kq + HT, tkn, row, 2 * HT);
-          o = (a.scale * dq - qv * dt[i] * rscale) * nqv[i];
-        } else {
-          o = a.scale * dq;
+        for (int e = 0; e < 2; ++e) {
+          const int i = 2 * m + e, k = (m >> 1) * 2 + e;
+          const float dq = qb[i] + gm[k] * qa[i];
+          if (l2) {
+            const float2 q2 = unpack_f16(qf[m]);
+            o[e] = (a.scale * dq - (e ? q2.y : q2.x) * dt[k]) * nqv[k];
+          } else {
+            o[e] = a.scale * dq;
+          }
         }
-        *stg_at(sm.ds, tkn, row) = __float2bfloat16_rn(o);
+        pk[m] = pack_bf16(o[0], o[1]);
       }
+      stmatrix_x4_trans(frag_addr(sm.ds, HT, wq, ls, c0, lane), pk);
     }
   }
   fence_before();
@@ -702,24 +740,35 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
   }
   {  // R9: dk^T = Ka + cdec * Kb (lanes d_k); Jacobian; dk out
     uint8_t *const stg = sm.x2;  // x2 + ah (16 KB, both dead after P8)
+    const int ta = c0 + 2 * (lane & 3);  // this lane's tokens ta, ta + 1, ta + 8, ta + 9
+    float cd[4], dt[4], nkv[4];
+    tok4(G.cdec, ta, cd);
+    if (l2) {
+      tok4(sm.acc[8], ta, dt);
+      tok4(sm.nk, ta, nkv);
+    }
 #pragma unroll 1
-    for (int q4 = 0; q4 < 2; ++q4) {
-      const int cb = c0 + q4 * 8;
+    for (int ls = 0; ls < 32; ls += 16) {
+      const uint32_t tq = tm + tl + ((uint32_t)ls << 16) + c0;
       float ka[8], kbv[8];
-      tmem_ld8x2(tm + tl + T3 + cb, ka, tm + tl + T2 + cb, kbv);
-      float cd[8], dt[8], nkv[8];
-      ld8f(G.cdec + cb, cd);
-      if (l2) {
-        ld8f(sm.acc[8] + cb, dt);
-        ld8f(sm.nk + cb, nkv);
-      }
+      tmem_ld_frag2(tq + T3, ka, tq + T2, kbv);
+      uint32_t kf[4], pk[4];
+      if (l2) ldmatrix_x4_trans(frag_addr(sm.wt, HT, wq, ls, c0, lane), kf);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int tkn = cb + i;
-        float o = ka[i] + cd[i] * kbv[i];
-        if (l2) o = (o - ld_f16(sm.wt, tkn, row, HT) * dt[i]) * nkv[i];
-        *stg_at(stg, tkn, row) = __float2bfloat16_rn(o);
+      for (int m = 0; m < 4; ++m) {
+        float o[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int i = 2 * m + e, k = (m >> 1) * 2 + e;
+          o[e] = ka[i] + cd[k] * kbv[i];
+          if (l2) {
+            const float2 k2 = unpack_f16(kf[m]);
+            o[e] = (o[e] - (e ? k2.y : k2.x) * dt[k]) * nkv[k];
+          }
+        }
+        pk[m] = pack_bf16(o[0], o[1]);
       }
+      stmatrix_x4_trans(frag_addr(stg, HT, wq, ls, c0, lane), pk);
     }
   }
   fence_before();

@@ -153,6 +153,39 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, float (&va)[16], uint32
     vb[i] = __uint_as_float(rb[i]);
   }
 }
+// Fragment loads for transposing read-outs: 16 lanes x 16 columns of fp32 per warp (two 16x256b blocks),
+// the accumulator fragment of a 16 x 8 MMA tile twice.  With lane base L and column base C (taddr), thread t
+// holds v[4x + 0..1] = lane L + t/4, columns C + 8x + 2(t%4) + {0, 1} and v[4x + 2..3] = lane L + 8 + t/4,
+// the same columns (x = 0, 1).  Two loads, one wait.
+__device__ __forceinline__ void tmem_ld_frag2(uint32_t ta, float (&va)[8], uint32_t tb, float (&vb)[8]) {
+  uint32_t ra[8], rb[8];
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+               : "=r"(ra[0]), "=r"(ra[1]), "=r"(ra[2]), "=r"(ra[3]), "=r"(ra[4]), "=r"(ra[5]), "=r"(ra[6]), "=r"(ra[7])
+               : "r"(ta));
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+               : "=r"(rb[0]), "=r"(rb[1]), "=r"(rb[2]), "=r"(rb[3]), "=r"(rb[4]), "=r"(rb[5]), "=r"(rb[6]), "=r"(rb[7])
+               : "r"(tb));
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    va[i] = __uint_as_float(ra[i]);
+    vb[i] = __uint_as_float(rb[i]);
+  }
+}
+// Four 8 x 8 b16 matrices between fragments and shared memory, transposed: register i holds fragment row
+// t/4, columns 2(t%4) and 2(t%4) + 1 (low half first) of matrix i; thread t gives the address of row t%8 of
+// matrix t/8, and that 16-byte row holds column t%8 of the fragment.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, const uint32_t (&r)[4]) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};\n" ::"r"(saddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3])
+               : "memory");
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t saddr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(saddr)
+               : "memory");
+}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
