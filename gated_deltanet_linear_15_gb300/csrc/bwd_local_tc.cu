@@ -3,8 +3,8 @@
 // items, each given the forward state S0 at the chunk start and dS at its end
 // (fp16, from the two serial passes); the next item's tiles stream in by TMA
 // while the current one finishes.  Every product
-// is a tcgen05 MMA with fp32 accumulation in TMEM; the 64 x 64 products use
-// M = 128 with the upper 64 rows unused.  The algebra is the hand-derived
+// is a tcgen05 MMA with fp32 accumulation in TMEM; the 64 x 64 products are
+// M = 64 MMAs, whose rows spread over all four TMEM lane quarters.  The algebra is the hand-derived
 // chunk backward (see bwd.cu); the WY part forms dA and dA^T as one symmetric
 // matrix multiplied with K once (onedev.kr FlashQLA talk summary, paragraph on
 // SFU load, last sentence).
@@ -140,6 +140,36 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t *>(&b);
 }
 __device__ __forceinline__ float2 unpack_f16(uint32_t r) { return __half22float2(*reinterpret_cast<const __half2 *>(&r)); }
+// The 64-row products (dP, M1, M2, Y1, dT) are M = 64 MMAs, whose row i sits on TMEM lane 32 (i / 16) + i % 16,
+// so all four lane quarters, and all 16 worker warps, share their read-outs: warp (wq, wg) reads rows 16 wq ..
+// + 15, columns c0 .. c0 + 15 as one fragment (value 2m + e of lane t: row 16 wq + 8 (m & 1) + t/4, column
+// c0 + 8 (m >> 1) + 2 (t%4) + e), and the row-major 64 x 64 fp16 tiles of those rows move to and from the
+// same fragments by ldmatrix / stmatrix, lane t addressing row 16 wq + 8 ((t/8) & 1) + t%8 from column
+// c0 + 8 ((t/8) >> 1).
+__device__ __forceinline__ uint32_t rfrag_addr(const uint8_t *base, int wq, int c0, int lane) {
+  const int m = lane >> 3;
+  return smem_u32(base + chunk_off(16 * wq + 8 * (m & 1) + (lane & 7), c0 + 8 * (m >> 1)));
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+// sums of a row pair over the four lanes of a quad and of four columns over the eight quads of a warp
+__device__ __forceinline__ void quad_sum2(float (&v)[2]) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    v[h] += __shfl_xor_sync(0xffffffffu, v[h], 1);
+    v[h] += __shfl_xor_sync(0xffffffffu, v[h], 2);
+  }
+}
+__device__ __forceinline__ void col_sum4(float (&v)[4]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    v[k] += __shfl_xor_sync(0xffffffffu, v[k], 4);
+    v[k] += __shfl_xor_sync(0xffffffffu, v[k], 8);
+    v[k] += __shfl_xor_sync(0xffffffffu, v[k], 16);
+  }
+}
 // a per-token factor at this lane's four tokens c0 + 2 (t%4) + {0, 1, 8, 9} (16-byte aligned arrays)
 __device__ __forceinline__ void tok4(const float *p, int ta, float (&v)[4]) {
   const float2 a = *reinterpret_cast<const float2 *>(p + ta), b = *reinterpret_cast<const float2 *>(p + ta + 8);
@@ -170,6 +200,8 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
   const int wg = warp >> 2, wq = warp & 3;
   const int row = (wq << 5) | lane;  // TMEM lane of this thread
   const int c0 = wg * 16;            // this warp's 16 columns of a 64-column region
+  const int ra = 16 * wq + (lane >> 2), ta = c0 + 2 * (lane & 3);  // rows ra, ra + 8 and columns ta, ta + 1,
+                                                                    // ta + 8, ta + 9 of its M = 64 fragments
   int *err = a.status;
 
   if (tid == 0) {
@@ -401,38 +433,44 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     break;
   }
   {
-    // dP rows (lanes 0-63): Z = dP * P row sums (thread-local) and column sums; dPm over P
-    if (row < 64) {
-      const int r = row;
-      float rs = 0.f, cs = 0.f;
+    // dP (M = 64 fragment): row and column sums of Z = dP * P; dPm = Gamma * dP (lower triangle) over P
+    {
       auto r5 = [&](auto pw) {
-#pragma unroll 1
-      for (int q4 = 0; q4 < 2; ++q4) {
-        const int cb = c0 + q4 * 8;
-        float v[8], zc[8], y[8];
-        tmem_ld8(tm + tl + T0 + cb, v);
-        uint8_t *pp = sm.p + chunk_off(r, cb);
-        const uint4 raw = *reinterpret_cast<const uint4 *>(pp);
-        const __half *ph = reinterpret_cast<const __half *>(&raw);
-        float rt[8];
-        ratio8<decltype(pw)::value>(G, r, cb, rt);
+        float v[8], rt[8];
+        uint32_t pf[4], out[4];
+        tmem_ld_frag1(tm + tl + T0 + c0, v);
+        const uint32_t pa = rfrag_addr(sm.p, wq, c0, lane);
+        ldmatrix_x4(pa, pf);
+        ratio_frag<decltype(pw)::value>(G, ra, ta, rt);
+        float rs[2] = {0.f, 0.f}, cs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float dpv = v[i];
-          const float zz = dpv * __half2float(ph[i]);
-          rs += zz;
-          zc[i] = zz;
-          y[i] = cb + i <= r ? dpv * rt[i] : 0.f;
+        for (int m = 0; m < 4; ++m) {
+          const float2 p2 = unpack_f16(pf[m]);
+          float y[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int i = 2 * m + e, h = m & 1, k = 2 * (m >> 1) + e;
+            const float zz = v[i] * (e ? p2.y : p2.x);
+            rs[h] += zz;
+            cs[k] += zz;
+            y[e] = ta + 8 * (m >> 1) + e <= ra + 8 * h ? v[i] * rt[i] : 0.f;
+          }
+          out[m] = pack_f16(y[0], y[1]);
         }
-        st_chunk_f16(pp, y);
-        const float a = colsum8(zc);
-        if ((lane >> 3) == q4) cs = a;
-      }
+        stmatrix_x4(pa, out);
+        quad_sum2(rs);
+        col_sum4(cs);
+        if ((lane & 3) == 0) {  // row sums of Z, per 16-column block
+          sm.part[16 + wg][ra] = rs[0];
+          sm.part[16 + wg][ra + 8] = rs[1];
+        }
+        if (lane < 4) {  // column sums of Z, per 16-row block
+          float *d = sm.part[8 + wq];
+          d[ta] = cs[0]; d[ta + 1] = cs[1]; d[ta + 8] = cs[2]; d[ta + 9] = cs[3];
+        }
       };
       if (G.pw) r5(std::true_type{});
       else r5(std::false_type{});
-      sm.part[16 + wg][r] = rs;          // row sums of Z, per 16-column block
-      if (lane < 16) sm.part[10 + wq][c0 + lane] = cs;  // column sums of Z, per row quarter (wq 0/1)
     }
     // dW'^T (lanes d_k) * gam -> s0 region (S0 is dead)
 #pragma unroll 1
@@ -456,7 +494,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
   if (tid < 64) {
     sm.acc[0][tid] = sm.part[0][tid] + sm.part[1][tid] + sm.part[2][tid] + sm.part[3][tid];      // <Ut, Y>
     sm.acc[2][tid] = sm.part[16][tid] + sm.part[17][tid] + sm.part[18][tid] + sm.part[19][tid];  // row sums of dP * P
-    sm.acc[3][tid] = sm.part[10][tid] + sm.part[11][tid];  // column sums of dP * P
+    sm.acc[3][tid] = sm.part[8][tid] + sm.part[9][tid] + sm.part[10][tid] + sm.part[11][tid];  // column sums of dP * P
   }
   {  // under P6: dV^T (lanes d_v, columns token) staged as bf16 dv[token][d_v] in dob (dO is dead; <dV, v>
      // comes with R6 as colsum(X2 M2)); gam <Qa, q^> per token over d_k (Qa = S0^T dO^T: the dO S0 part
@@ -486,7 +524,6 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
       s[k] += __shfl_xor_sync(0xffffffffu, s[k], 16);
     }
     if (lane < 4) {
-      const int ta = c0 + 2 * lane;
       float gm[4];
       tok4(G.gam, ta, gm);
       float *dst = sm.part[12 + wq];
@@ -509,57 +546,62 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     break;
   }
   {
-    // M1, M2 (lanes 0-63 = r): dAhat = beta_i (M1 + Gamma M2); beta column sums colsum_i(Ahat (M1 + Gamma M2));
-    // colsum_i(Ahat M1) (the dW'^T X1 part of dk^ dotted with k^).  Gate terms: <dW_r, W_r> =
+    // M1, M2 (M = 64 fragments, rows r): dAhat = beta_i (M1 + Gamma M2); beta column sums colsum_i(Ahat (M1 +
+    // Gamma M2)); colsum_i(Ahat M1) (the dW'^T X1 part of dk^ dotted with k^).  Gate terms: <dW_r, W_r> =
     // rowsum_r(beta Ahat M1) and the row and column sums of X2 * M2 (X2 = Gamma Ahat diag(beta), M2 =
     // dUt V^T) over the strictly lower triangle only: a diagonal ratio gamma_r / gamma_r does not depend
     // on the gates, and leaving it out of both sums keeps the small gate gradient of a strongly decaying
     // chunk from being the difference of two large, differently rounded numbers.  X2 is read before dAhat
     // replaces it
-    if (row < 64) {
-      const int r = row;
-      float cs = 0.f, ca = 0.f, cv = 0.f, rwx = 0.f;
-      auto r6 = [&](auto pw) {
-#pragma unroll 1
-      for (int q4 = 0; q4 < 2; ++q4) {
-        const int cb = c0 + q4 * 8;
-        float m1[8], m2[8];
-        tmem_ld8x2(tm + tl + T3 + cb, m1, tm + tl + T4 + cb, m2);
-        const uint4 raw = *reinterpret_cast<const uint4 *>(sm.ah + chunk_off(r, cb));
-        const __half *hh = reinterpret_cast<const __half *>(&raw);
-        const uint4 xraw = *reinterpret_cast<const uint4 *>(sm.x2 + chunk_off(r, cb));
-        const __half *xh = reinterpret_cast<const __half *>(&xraw);
-        float rt[8], bt[8];
-        ratio8<decltype(pw)::value>(G, r, cb, rt);
-        ld8f(gbeta + cb, bt);
-        float am[8], xm[8];
+    auto r6 = [&](auto pw) {
+      float m1[8], m2[8], rt[8], bt[4];
+      uint32_t af[4], xf[4], out[4];
+      tmem_ld_frag2(tm + tl + T3 + c0, m1, tm + tl + T4 + c0, m2);
+      const uint32_t xa = rfrag_addr(sm.x2, wq, c0, lane);
+      ldmatrix_x4(rfrag_addr(sm.ah, wq, c0, lane), af);
+      ldmatrix_x4(xa, xf);
+      ratio_frag<decltype(pw)::value>(G, ra, ta, rt);
+      tok4(gbeta, ta, bt);
+      float rw[2] = {0.f, 0.f}, cs[4] = {0.f, 0.f, 0.f, 0.f}, ca[4] = {0.f, 0.f, 0.f, 0.f},
+            cv[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int col = cb + i;
-          const float hv = __half2float(hh[i]);
+      for (int m = 0; m < 4; ++m) {
+        const float2 a2 = unpack_f16(af[m]), x2 = unpack_f16(xf[m]);
+        float o[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int i = 2 * m + e, h = m & 1, k = 2 * (m >> 1) + e;
+          const int r = ra + 8 * h, col = ta + 8 * (m >> 1) + e;
+          const float hv = e ? a2.y : a2.x;
           const float x = m1[i] + (col <= r ? m2[i] * rt[i] : 0.f);
-          am[i] = hv * m1[i];
-          xm[i] = col < r ? __half2float(xh[i]) * m2[i] : 0.f;
-          rwx += bt[i] * am[i] + xm[i];
-          m2[i] = hv * x;
-          m1[i] = bt[i] * x;
+          const float am = hv * m1[i];
+          const float xm = col < r ? (e ? x2.y : x2.x) * m2[i] : 0.f;
+          rw[h] += bt[k] * am + xm;
+          cs[k] += hv * x;
+          ca[k] += am;
+          cv[k] += xm;
+          o[e] = bt[k] * x;
         }
-        st_chunk_f16(sm.x2 + chunk_off(r, cb), m1);
-        const float a = colsum8(m2), b = colsum8(am), e = colsum8(xm);
-        if ((lane >> 3) == q4) {
-          cs = a;
-          ca = b;
-          cv = e;
-        }
+        out[m] = pack_f16(o[0], o[1]);
       }
-      };
-      if (G.pw) r6(std::true_type{});
-      else r6(std::false_type{});
-      if (lane < 16) sm.part[8 + wq][c0 + lane] = cs;
-      if (lane < 16) sm.part[10 + wq][c0 + lane] = ca;
-      if (lane < 16) sm.part[14 + wq][c0 + lane] = cv;
-      sm.part[4 + wg][r] = rwx;  // row terms, per 16-column block
-    }
+      stmatrix_x4(xa, out);
+      quad_sum2(rw);
+      col_sum4(cs);
+      col_sum4(ca);
+      col_sum4(cv);
+      if ((lane & 3) == 0) {  // row terms, per 16-column block
+        sm.part[4 + wg][ra] = rw[0];
+        sm.part[4 + wg][ra + 8] = rw[1];
+      }
+      if (lane < 4) {  // column terms, per 16-row block
+        float *d0 = sm.part[8 + wq], *d1 = sm.part[12 + wq], *d2 = sm.part[wq];
+        d0[ta] = cs[0]; d0[ta + 1] = cs[1]; d0[ta + 8] = cs[2]; d0[ta + 9] = cs[3];
+        d1[ta] = ca[0]; d1[ta + 1] = ca[1]; d1[ta + 8] = ca[2]; d1[ta + 9] = ca[3];
+        d2[ta] = cv[0]; d2[ta + 1] = cv[1]; d2[ta + 8] = cv[2]; d2[ta + 9] = cv[3];
+      }
+    };
+    if (G.pw) r6(std::true_type{});
+    else r6(std::false_type{});
   }
   if (tid < 128) (tid < 64 ? sm.g[gbuf ^ 1] : sm.beta[gbuf ^ 1])[tid & 63] = gb_next;  // next item's g, beta
   fence_before();
@@ -569,9 +611,9 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     break;
   }
   if (tid < 64) {
-    sm.acc[6][tid] = sm.part[8][tid] + sm.part[9][tid];    // beta col terms
-    sm.acc[7][tid] = sm.part[10][tid] + sm.part[11][tid];  // colsum(Ahat M1)
-    sm.acc[4][tid] = sm.part[14][tid] + sm.part[15][tid];  // strictly lower column sums of X2 * M2
+    sm.acc[6][tid] = sm.part[8][tid] + sm.part[9][tid] + sm.part[10][tid] + sm.part[11][tid];    // beta col terms
+    sm.acc[7][tid] = sm.part[12][tid] + sm.part[13][tid] + sm.part[14][tid] + sm.part[15][tid];  // colsum(Ahat M1)
+    sm.acc[4][tid] = sm.part[0][tid] + sm.part[1][tid] + sm.part[2][tid] + sm.part[3][tid];  // lower col sums of X2 * M2
     sm.acc[1][tid] = sm.part[4][tid] + sm.part[5][tid] + sm.part[6][tid] + sm.part[7][tid];  // <dW, W> + rows of X2 * M2
   }
   {  // K^ -> wt (dUt^T is dead): R9 reads k^ there, so the K/Q buffer is free once P9 is done
@@ -584,14 +626,13 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     failed = release = true;
     break;
   }
-  if (row < 64) {  // R7: Y1 -> v (first half; V is dead)
-#pragma unroll 1
-    for (int q4 = 0; q4 < 2; ++q4) {
-      const int cb = c0 + q4 * 8;
-      float v[8];
-      tmem_ld8(tm + tl + T0 + cb, v);
-      st_chunk_f16(sm.v + chunk_off(row, cb), v);
-    }
+  {  // R7: Y1 (M = 64 fragment) -> v (first half; V is dead)
+    float v[8];
+    uint32_t out[4];
+    tmem_ld_frag1(tm + tl + T0 + c0, v);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) out[m] = pack_f16(v[2 * m], v[2 * m + 1]);
+    stmatrix_x4(rfrag_addr(sm.v, wq, c0, lane), out);
   }
   fence_before();
   fence_async_smem();
@@ -602,7 +643,6 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
   {  // under P8: dq raw = (scale dq^ - q^ (q^ . dq^) / scale) / |q|   (or scale dq^ without normalisation),
      // staged in ds (dS is dead: its last reader, Kb, completed under P6)
     const float rscale = 1.f / a.scale;
-    const int ta = c0 + 2 * (lane & 3);  // this lane's tokens ta, ta + 1, ta + 8, ta + 9
     float gm[4], dt[4], nqv[4];
     tok4(G.gam, ta, gm);
     if (l2) {  // q^ . dq^ = gam <Qa, q^> + sum_s dP * P (the Qb part: row sums of dP * P)
@@ -650,33 +690,39 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     failed = release = true;
     break;
   }
-  if (row < 64) {  // R8: dN[r][i] = beta_r dT_ri (i < r), zero elsewhere; beta row sums of dT * N
-    const int r = row;
-    const float br = gbeta[r];
-    uint8_t *sg = sm.v + HT;
-    float rb = 0.f, cn = 0.f;  // row sums of dT * N; column sums of dN * N
-#pragma unroll 1
-    for (int q4 = 0; q4 < 2; ++q4) {
-      const int cb = c0 + q4 * 8;
-      float v[8], y[8], dn[8];
-      tmem_ld8(tm + tl + T1 + cb, v);
-      const uint4 nraw = *reinterpret_cast<const uint4 *>(sm.n16 + chunk_off(r, cb));
-      const __half *nh = reinterpret_cast<const __half *>(&nraw);
+  {  // R8 (M = 64 fragment of dT): dN[r][i] = beta_r dT_ri (i < r), zero elsewhere; beta row sums of dT * N
+    float v[8];
+    uint32_t nf[4], out[4];
+    tmem_ld_frag1(tm + tl + T1 + c0, v);
+    ldmatrix_x4(rfrag_addr(sm.n16, wq, c0, lane), nf);
+    const float br[2] = {gbeta[ra], gbeta[ra + 8]};
+    float rb[2] = {0.f, 0.f}, cn[4] = {0.f, 0.f, 0.f, 0.f};  // row sums of dT * N; column sums of dN * N
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int col = cb + i;
-        const bool lo = col < r;
-        const float nv = __half2float(nh[i]);
-        rb += lo ? v[i] * nv : 0.f;
-        y[i] = lo ? br * v[i] : 0.f;
-        dn[i] = y[i] * nv;
+    for (int m = 0; m < 4; ++m) {
+      const float2 n2 = unpack_f16(nf[m]);
+      float y[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int i = 2 * m + e, h = m & 1, k = 2 * (m >> 1) + e;
+        const bool lo = ta + 8 * (m >> 1) + e < ra + 8 * h;
+        const float nv = e ? n2.y : n2.x;
+        rb[h] += lo ? v[i] * nv : 0.f;
+        y[e] = lo ? br[h] * v[i] : 0.f;
+        cn[k] += y[e] * nv;
       }
-      st_chunk_f16(sg + chunk_off(r, cb), y);
-      const float a = colsum8(dn);
-      if ((lane >> 3) == q4) cn = a;
+      out[m] = pack_f16(y[0], y[1]);
     }
-    sm.part[16 + wg][r] = rb;
-    if (lane < 16) sm.part[12 + wq][c0 + lane] = cn;
+    stmatrix_x4(rfrag_addr(sm.v + HT, wq, c0, lane), out);
+    quad_sum2(rb);
+    col_sum4(cn);
+    if ((lane & 3) == 0) {
+      sm.part[16 + wg][ra] = rb[0];
+      sm.part[16 + wg][ra + 8] = rb[1];
+    }
+    if (lane < 4) {
+      float *d = sm.part[12 + wq];
+      d[ta] = cn[0]; d[ta + 1] = cn[1]; d[ta + 8] = cn[2]; d[ta + 9] = cn[3];
+    }
   }
   fence_before();
   fence_async_smem();
@@ -687,8 +733,8 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
   if (tid < 64) {  // k^ . dk^ per token: Q^T dPm, dW'^T X1, K^T (dN + dN^T) and cdec Kb parts, from sums above
     const int t = tid;
     const float rbs = sm.part[16][t] + sm.part[17][t] + sm.part[18][t] + sm.part[19][t];
-    sm.acc[8][t] = sm.acc[3][t] + gbeta[t] * (sm.acc[7][t] + rbs) + (sm.part[12][t] + sm.part[13][t]) +
-                   G.cdec[t] * sm.acc[0][t];
+    sm.acc[8][t] = sm.acc[3][t] + gbeta[t] * (sm.acc[7][t] + rbs) +
+                   (sm.part[12][t] + sm.part[13][t] + sm.part[14][t] + sm.part[15][t]) + G.cdec[t] * sm.acc[0][t];
   }
   // ---- gate and beta gradients
   if (warp == LWARPS - 1) {  // under P9 (the other warps' shadow work is the k^ . dk^ sum)
@@ -740,7 +786,6 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
   }
   {  // R9: dk^T = Ka + cdec * Kb (lanes d_k); Jacobian; dk out
     uint8_t *const stg = sm.x2;  // x2 + ah (16 KB, both dead after P8)
-    const int ta = c0 + 2 * (lane & 3);  // this lane's tokens ta, ta + 1, ta + 8, ta + 9
     float cd[4], dt[4], nkv[4];
     tok4(G.cdec, ta, cd);
     if (l2) {
@@ -827,16 +872,16 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
       pend_wy = false;
       if (f) break;
     }
-    // ---- P5: dP = dO Ut^T -> T0; dW'^T = -S0^T dUt^T -> T1; dV^T = dUt^T X2 -> T6;  Kb = dS^T Ut^T -> T2
+    // ---- P5: dP = dO Ut^T -> T0 (M = 64); dW'^T = -S0^T dUt^T -> T1; dV^T = dUt^T X2 -> T6;  Kb = dS^T Ut^T -> T2
     if (lane == 0) {
       fence_after();
-      const uint32_t id_kmn = idesc_f16(128, 64, false, true);
+      const uint32_t id_kmn = idesc_f16(128, 64, false, true), id_dp = idesc_f16(64, 64, false, true);
       const uint32_t id_mmn_neg = idesc_f16(128, 64, true, true, true);
       const uint32_t dob = u32(sm.dob), ub = u32(sm.ut), sb = u32(sm.s0), dub = u32(sm.wt), x2b = u32(sm.x2);
 #pragma unroll 1
       for (int kk = 0; kk < 8; ++kk) {
         mma_f16(tm + T0, sdesc(dob + (kk >> 2) * HT + (kk & 3) * 32, 16, 1024), sdesc(ub + kk * 2048, 2 * HT, 1024),
-                id_kmn, kk > 0);
+                id_dp, kk > 0);
         mma_f16(tm + T1, sdesc(sb + kk * 2048, 2 * HT, 1024), sdesc(dub + kk * 2048, 2 * HT, 1024), id_mmn_neg,
                 kk > 0);
       }
@@ -852,18 +897,18 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     }
     __syncwarp();
     if (__syncthreads_or(false)) break;  // B4
-    // ---- P6: M1 = dW' K^T -> T3;  M2 = dUt V^T -> T4;  then Qb = K^T dPm^T -> T7 (first read under P8: the
-    //      P7 commit covers it)
+    // ---- P6: M1 = dW' K^T -> T3;  M2 = dUt V^T -> T4 (both M = 64);  then Qb = K^T dPm^T -> T7 (first read
+    //      under P8: the P7 commit covers it)
     if (lane == 0) {
       fence_after();
-      const uint32_t id_mk = idesc_f16(128, 64, true, false);
+      const uint32_t id_mk = idesc_f16(128, 64, true, false), id_m64 = idesc_f16(64, 64, true, false);
       const uint32_t kb = u32(sm.kq), pb = u32(sm.p), dwb = u32(sm.s0), dub = u32(sm.wt), vb = u32(sm.v);
 #pragma unroll 1
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t boff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
-        mma_f16(tm + T3, sdesc(dwb + kk * 2048, 2 * HT, 1024), sdesc(kb + boff, 16, 1024), id_mk, kk > 0);
+        mma_f16(tm + T3, sdesc(dwb + kk * 2048, 2 * HT, 1024), sdesc(kb + boff, 16, 1024), id_m64, kk > 0);
         mma_f16(tm + T4, sdesc(dub + kk * 2048, 2 * HT, 1024), sdesc(vb + (kk >> 2) * HT + (kk & 3) * 32, 16, 1024),
-                id_mk, kk > 0);
+                id_m64, kk > 0);
       }
       mma_commit(u32(&sm.bar_mma));
 #pragma unroll 1
@@ -874,17 +919,17 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     if (__syncthreads_or(false)) break;  // B5
     if (lane == 0 && nvalid == CH) store_tma(&tmdv, sm.dob, h, tok0);
     if (__syncthreads_or(false)) break;  // B6
-    // ---- P7: Y1 = Ahat^T dAhat -> T0;  then Ka's context-only part Q^T dPm + dW'^T X1 -> T3 (first read in
+    // ---- P7: Y1 = Ahat^T dAhat -> T0 (M = 64);  then Ka's context-only part Q^T dPm + dW'^T X1 -> T3 (first read in
     //      R9: the P8 commit covers it; M1 in T3 was read above)
     if (lane == 0) {
       fence_after();
-      const uint32_t id = idesc_f16(128, 64, true, true);
+      const uint32_t id = idesc_f16(128, 64, true, true), id_y1 = idesc_f16(64, 64, true, true);
       const uint32_t id_km = idesc_f16(128, 64, false, true);
       const uint32_t ab = u32(sm.ah), dab = u32(sm.x2);
       const uint32_t kb = u32(sm.kq), pb = u32(sm.p), dwb = u32(sm.s0), x1b = u32(sm.x1);
 #pragma unroll 1
       for (int kk = 0; kk < 4; ++kk)
-        mma_f16(tm + T0, sdesc(ab + kk * 2048, HT, 1024), sdesc(dab + kk * 2048, HT, 1024), id, kk > 0);
+        mma_f16(tm + T0, sdesc(ab + kk * 2048, HT, 1024), sdesc(dab + kk * 2048, HT, 1024), id_y1, kk > 0);
       mma_commit(u32(&sm.bar_mma));
 #pragma unroll 1
       for (int kk = 0; kk < 4; ++kk) {
@@ -899,10 +944,10 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     __syncwarp();
     if (nitem < n_items) pend_do = true;
     if (__syncthreads_or(false)) break;  // B7
-    // ---- P8: dT = -Y1 Ahat^T -> T1
+    // ---- P8: dT = -Y1 Ahat^T -> T1 (M = 64)
     if (lane == 0) {
       fence_after();
-      const uint32_t id = idesc_f16(128, 64, false, false, true);
+      const uint32_t id = idesc_f16(64, 64, false, false, true);
       const uint32_t yb = u32(sm.v), ab = u32(sm.ah);
 #pragma unroll 1
       for (int kk = 0; kk < 4; ++kk) mma_f16(tm + T1, sdesc(yb + kk * 32, 16, 1024), sdesc(ab + kk * 32, 16, 1024), id, kk > 0);

@@ -211,6 +211,23 @@ template <bool PW> __device__ __forceinline__ void ratio8(const Gates &gt, int r
     for (int i = 0; i < 8; ++i) o[i] = cb + i <= r ? expf(two_diff(Gr, Grl, gt.Ghi[cb + i], gt.Glo[cb + i])) : 0.f;
   }
 }
+// The ratios at the eight entries of a 16 x 16 fragment that one lane holds (rows ra, ra + 8; columns ta,
+// ta + 1, ta + 8, ta + 9; ta even): o[4x + 2h + e] = gamma_{ra + 8h} / gamma_{ta + 8x + e}.  The factored form
+// does not zero the entries above the diagonal (the callers mask them); the pairwise form does.
+template <bool PW> __device__ __forceinline__ void ratio_frag(const Gates &gt, int ra, int ta, float (&o)[8]) {
+  if constexpr (!PW) {
+    const float2 a = *reinterpret_cast<const float2 *>(gt.rgp + ta), b = *reinterpret_cast<const float2 *>(gt.rgp + ta + 8);
+    const float g0 = gt.gp[ra], g1 = gt.gp[ra + 8];
+    o[0] = g0 * a.x; o[1] = g0 * a.y; o[2] = g1 * a.x; o[3] = g1 * a.y;
+    o[4] = g0 * b.x; o[5] = g0 * b.y; o[6] = g1 * b.x; o[7] = g1 * b.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = ra + 8 * ((i >> 1) & 1), c = ta + 8 * (i >> 2) + (i & 1);
+      o[i] = c <= r ? expf(two_diff(gt.Ghi[r], gt.Glo[r], gt.Ghi[c], gt.Glo[c])) : 0.f;
+    }
+  }
+}
 // the same with the form chosen at run time (the pairwise form element by element out of line)
 __device__ __forceinline__ void gratio8(const Gates &gt, int r, int cb, float (&o)[8]) {
   if (!gt.pw) {

@@ -172,6 +172,30 @@ __device__ __forceinline__ void tmem_ld_frag2(uint32_t ta, float (&va)[8], uint3
     vb[i] = __uint_as_float(rb[i]);
   }
 }
+// one fragment load (same layout as tmem_ld_frag2), then wait
+__device__ __forceinline__ void tmem_ld_frag1(uint32_t ta, float (&va)[8]) {
+  uint32_t ra[8];
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+               : "=r"(ra[0]), "=r"(ra[1]), "=r"(ra[2]), "=r"(ra[3]), "=r"(ra[4]), "=r"(ra[5]), "=r"(ra[6]), "=r"(ra[7])
+               : "r"(ta));
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) va[i] = __uint_as_float(ra[i]);
+}
+// Four 8 x 8 b16 matrices between fragments and shared memory, not transposed: register i holds row t/4,
+// columns 2(t%4) and 2(t%4) + 1 (low half first) of matrix i; thread t gives the address of row t%8 of
+// matrix t/8 (16 bytes).
+__device__ __forceinline__ void stmatrix_x4(uint32_t saddr, const uint32_t (&r)[4]) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};\n" ::"r"(saddr), "r"(r[0]), "r"(r[1]),
+               "r"(r[2]), "r"(r[3])
+               : "memory");
+}
+__device__ __forceinline__ void ldmatrix_x4(uint32_t saddr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(saddr)
+               : "memory");
+}
 // Four 8 x 8 b16 matrices between fragments and shared memory, transposed: register i holds fragment row
 // t/4, columns 2(t%4) and 2(t%4) + 1 (low half first) of matrix i; thread t gives the address of row t%8 of
 // matrix t/8, and that 16-byte row holds column t%8 of the fragment.
