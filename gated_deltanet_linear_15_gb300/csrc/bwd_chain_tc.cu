@@ -6,8 +6,9 @@
 // (TMA, with dO), so a chunk is dO's conversion and two tensor-core rounds:
 //   Y = dS K^T, Z = dO^T P, dS += (diag(gam) dO)^T Q;   dUt^T = Y diag(cdec) + Z (read-out)
 //   dS <- dS - dUt^T W                                    (after gam_C dS and the fp16 copy)
-// and the fp16 dS at every chunk end goes to the workspace (TMA store) for the
-// local-gradient kernel.  Pass 0 (reverse sequence parallelism) runs a
+// and the fp16 dS at every chunk end and the chunk's fp16 dUt^T (the operand of
+// round 2, which the local-gradient kernel would otherwise recompute from dS, K,
+// dO and P) go to the workspace by TMA store for the local-gradient kernel.  Pass 0 (reverse sequence parallelism) runs a
 // segment from zero (role 0) or the transition from I with dO = 0 (role 1);
 // pass 1 runs it from its exact end gradient and stores the per-chunk dS
 // (and dS0 for the first segment).  Layouts and primitives as in fwd_tc.cu.
@@ -55,7 +56,7 @@ __device__ __forceinline__ void st_chunk_f16(uint8_t *dst, const float *v) {
 // warm-up, role 1 the reverse transition; 1: the per-chunk dS).
 __device__ __forceinline__ void chain_tc_item(const BwdArgs &a, const CUtensorMap &tm3, const CUtensorMap &tmdo,
                                               const CUtensorMap &tmp, const CUtensorMap &tmw, const CUtensorMap &tmds,
-                                              int s, int h, int role, int pass) {
+                                              const CUtensorMap &tmdu, int s, int h, int role, int pass) {
   extern __shared__ unsigned char smraw[];
   ChainTcSmem &sm =
       *reinterpret_cast<ChainTcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
@@ -108,7 +109,10 @@ __device__ __forceinline__ void chain_tc_item(const BwdArgs &a, const CUtensorMa
     tma_prefetch_desc(&tmdo);
     tma_prefetch_desc(&tmp);
     tma_prefetch_desc(&tmw);
-    if (store) tma_prefetch_desc(&tmds);
+    if (store) {
+      tma_prefetch_desc(&tmds);
+      tma_prefetch_desc(&tmdu);
+    }
   }
   if (warp == 0) {
     tmem_alloc(u32(&sm.tmem_base), TM_COLS);
@@ -199,7 +203,7 @@ __device__ __forceinline__ void chain_tc_item(const BwdArgs &a, const CUtensorMa
         // round 2 of the previous chunk (the second of two commits per chunk: parity 1) has read its
         // ring stage, which takes the tiles of chunk c - 1 below
         if (it > 0) mbar_wait(u32(&sm.bar_mma), 1, err, 4);
-        if (store) tma_store_wait_read();  // the previous chunk's dS store has read ds16
+        if (store) tma_store_wait_read();  // the previous chunk's dS and dUt^T stores have read ds16 and kc
       }
       __syncwarp();
       named_bar_arrive<2, NTHREADS + 32>();
@@ -249,6 +253,10 @@ __device__ __forceinline__ void chain_tc_item(const BwdArgs &a, const CUtensorMa
         for (int kk = 0; kk < 4; ++kk)
           mma_f16(tm + TM_S, sdesc(dub + kk * 32, 16, 1024), sdesc(wb + kk * 32, 16, 1024), id_kk_neg, true);
         mma_commit(u32(&sm.bar_mma));
+        if (store && c < cend) {  // dUt^T of chunk c for the local-gradient kernel (read before the next
+          tma_store_3d(&tmdu, 0, ((chunk0 + c) * H + h) * D, 0, dub);  // chunk's read-out rewrites kc)
+          tma_store_commit();
+        }
       }
       __syncwarp();
       continue;
@@ -305,7 +313,7 @@ __device__ __forceinline__ void chain_tc_item(const BwdArgs &a, const CUtensorMa
         *reinterpret_cast<uint4 *>(rowg + off) = g4;
       }
     }
-    named_bar_sync<2, NTHREADS + 32>();  // the previous chunk's dS store has read ds16
+    named_bar_sync<2, NTHREADS + 32>();  // the previous chunk's stores have read ds16 and kc
     // ---- dS (end of chunk c) -> fp16 operand copy, gam_C dS back into TMEM
     {
       const float gC = G.gamC;
@@ -405,7 +413,7 @@ template <bool SCHED>
 __global__ void __launch_bounds__(NTHREADS + 32, 1)
     bwd_chain_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tm3, const __grid_constant__ CUtensorMap tmdo,
                         const __grid_constant__ CUtensorMap tmp, const __grid_constant__ CUtensorMap tmw,
-                        const __grid_constant__ CUtensorMap tmds) {
+                        const __grid_constant__ CUtensorMap tmds, const __grid_constant__ CUtensorMap tmdu) {
   pdl_trigger();
   pdl_wait();
   int s = blockIdx.x, h = blockIdx.y, role = blockIdx.z, pass = a.pass;
@@ -477,7 +485,7 @@ __global__ void __launch_bounds__(NTHREADS + 32, 1)
       return;  // a ticket past the lists: no work
     }
   }
-  chain_tc_item(a, tm3, tmdo, tmp, tmw, tmds, s, h, role, pass);
+  chain_tc_item(a, tm3, tmdo, tmp, tmw, tmds, tmdu, s, h, role, pass);
   if (doneA) {  // the start-gradient / transition stores of every thread are visible before the count
     __threadfence();
     __syncthreads();
@@ -492,7 +500,8 @@ int launch_bwd_chain_tc(const BwdArgs &a, const CUtensorMap *maps, dim3 grid, cu
   auto kern = a.sched_on ? bwd_chain_tc_kernel<true> : bwd_chain_tc_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  return (int)launch_pdl(kern, grid, dim3(NTHREADS + 32), smem, st, a, maps[0], maps[1], maps[2], maps[3], maps[4]);
+  return (int)launch_pdl(kern, grid, dim3(NTHREADS + 32), smem, st, a, maps[0], maps[1], maps[2], maps[3], maps[4],
+                         maps[5]);
 }
 
 }  // namespace gdn

@@ -10,18 +10,17 @@
 // SFU load, last sentence).
 //
 // Rounds (MMA group -> read-out), TMEM regions T0..T7 of 64 columns.  The forward's chunk context
-// supplies X1, X2, Ahat, P, N and Ut^T by TMA with the inputs, so nothing of the forward chunk is
-// recomputed here.  Each round commits once the products its read-out needs are issued; the products
-// read later (in brackets) are issued after that commit and covered by the next one, and the CUDA-core
-// work no following product needs runs while the next round computes:
-//   P2 Y = dS K^T->T3, Z = dO^T P->T4 [Qa = S0^T dO^T->T5]
-//                            R2: dUt^T = cdec*Y + Z
-//   P5 dP = dO Ut^T->T0, dW'^T = -S0^T dUt^T->T1, dV^T = dUt^T X2->T6 [Kb = dS^T Ut^T->T2]
-//                            under P5: sums <Ut,Y>, <dUt,Ut>;  R5: dPm (over P), dP*P sums; dW'^T tile
+// supplies X1, X2, Ahat, P, N and Ut^T, and the reverse chain dUt^T (the operand of its own second round),
+// so nothing of the forward chunk or of the chain is recomputed here.  Each round commits once the
+// products its read-out needs are issued; the products read later (in brackets) are issued after that
+// commit and covered by the next one, and the CUDA-core work no following product needs runs while the
+// next round computes:
+//   P5 dP = dO Ut^T->T0, dW'^T = -S0^T dUt^T->T1, dV^T = dUt^T X2->T6, Qa = S0^T dO^T->T5 [Kb = dS^T Ut^T->T2]
+//                            under P5: <dS, S0>;  R5: dPm (over P), dP*P sums; dW'^T tile
 //   P6 M1 = dW' K^T->T3, M2 = dUt V^T->T4 [Qb = K^T dPm^T->T7]
 //                            under P6: dv out, gam <Qa,q>;  R6: dAhat tile, beta column sums, <dV,v>
 //   P7 Y1 = Ahat^T dAhat->T0 [Ka = Q^T dPm + dW'^T X1->T3]
-//                            under P7: K^ copy, next item's gates;  R7: Y1 tile
+//                            under P7: <k, Kb>, next item's gates;  R7: Y1 tile
 //   P8 dT = -Y1 Ahat^T->T1   under P8: dq out;  R8: dN tile (strictly lower), beta row sums (with N)
 //   P9 Ka += K^T (dN + dN^T)->T3
 //                            R9: dk out (Ka + cdec Kb);  dg (reverse cumsum), dbeta
@@ -48,7 +47,7 @@ constexpr uint32_t T0 = 0, T1 = 64, T2 = 128, T3 = 192, T4 = 256, T5 = 320, T6 =
 
 struct __align__(1024) LocalTcSmem {
   uint8_t kq[4 * HT];   // [K0 | Q0 | K1 | Q1] half-tiles (feature blocks 0/1), rows = token
-  uint8_t v[2 * HT];    // V, later Y1 (first half) and dN (second half)
+  uint8_t v[2 * HT];    // V, later Y1 (first half) and dN (second half), then the dk staging
   uint8_t dob[2 * HT];  // dO, later output staging (bf16 [token][128])
   uint8_t s0[4 * HT];   // S0 [k-block][128 rows = d_v][64], later dW'^T [d_k][token]
   uint8_t ds[4 * HT];   // dS, same layout
@@ -56,7 +55,7 @@ struct __align__(1024) LocalTcSmem {
   uint8_t x1[HT];
   uint8_t x2[HT];       // X2, later dAhat
   uint8_t ah[HT];       // Ahat (fp16)
-  uint8_t wt[2 * HT];   // W^T [d_k][token], later dUt^T [d_v][token]
+  uint8_t wt[2 * HT];   // dUt^T [d_v][token] (the reverse chain's tile)
   uint8_t ut[2 * HT];   // Ut^T [d_v][token] (context tile)
   uint8_t n16[HT];      // N = K K^T (fp16, [r][i], context tile)
   float g[2][CH], beta[2][CH];  // per item parity: the next item's gates are prepared during this one
@@ -65,7 +64,8 @@ struct __align__(1024) LocalTcSmem {
   float part[20][CH];   // per-token partial sums (reused per round)
   float acc[9][CH];     // assembled per-token terms
   float red[LWARPS];
-  uint64_t bar_a, bar_b, bar_w, bar_mma;  // TMA: {K, Q, V, S0, dS, Ut^T, P, N}, {dO}, {X1, X2, Ahat}; tensor cores
+  uint64_t bar_a, bar_b, bar_w, bar_mma;  // TMA: {Ut^T, dUt^T, X2, S0, dS, P, N, X1, Ahat}, {dO}, {K, Q, norms, V};
+                                          // tensor cores
   uint32_t tmem_base;
 };
 
@@ -76,25 +76,6 @@ __device__ __forceinline__ void st_chunk_f16(uint8_t *dst, const float *v) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
   *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<uint4 *>(h);
-}
-
-// v[8] per lane -> lane l holds the sum over the warp's lanes of v[l % 8]
-__device__ __forceinline__ float colsum8(float (&v)[8]) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int s = 4; s >= 1; s >>= 1) {
-#pragma unroll
-    for (int i = 0; i < s; ++i) {
-      const bool up = (lane & s) != 0;
-      const float send = up ? v[i] : v[i + s];
-      const float recv = __shfl_xor_sync(0xffffffffu, send, s);
-      v[i] = (up ? v[i + s] : v[i]) + recv;
-    }
-  }
-  float t = v[0];
-  t += __shfl_xor_sync(0xffffffffu, t, 8);
-  t += __shfl_xor_sync(0xffffffffu, t, 16);
-  return t;
 }
 
 // 8 consecutive floats from 16-byte aligned shared memory (two vector loads, broadcast across the warp)
@@ -183,7 +164,8 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
                         const __grid_constant__ CUtensorMap tms0, const __grid_constant__ CUtensorMap tmds,
                         const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmdq,
                         const __grid_constant__ CUtensorMap tmdk, const __grid_constant__ CUtensorMap tmdv,
-                        const __grid_constant__ CUtensorMap tmu, int n_items) {
+                        const __grid_constant__ CUtensorMap tmu, const __grid_constant__ CUtensorMap tmdu,
+                        int n_items) {
   extern __shared__ unsigned char smraw[];
   LocalTcSmem &sm =
       *reinterpret_cast<LocalTcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
@@ -210,7 +192,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     mbar_init(u32(&sm.bar_w), 1);
     mbar_init(u32(&sm.bar_mma), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    for (const CUtensorMap *m : {&tm3, &tmdo, &tms0, &tmds, &tmw, &tmdq, &tmdk, &tmdv, &tmu}) tma_prefetch_desc(m);
+    for (const CUtensorMap *m : {&tm3, &tmdo, &tms0, &tmds, &tmw, &tmdq, &tmdk, &tmdv, &tmu, &tmdu}) tma_prefetch_desc(m);
   }
   if (warp == 0) {
     tmem_alloc(u32(&sm.tmem_base), 512);
@@ -247,8 +229,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
   };
 
   // Work items (chunk gc, head h) = (item / H, item % H), strided over the persistent CTAs; chunks past
-  // the plan's total are skipped.  The tiles of the next item are loaded by TMA while this one finishes:
-  // dO once the dq staging in its buffer is stored, everything else once the last product (P9) is done.
+  // the plan's total are skipped.  The tiles of the next item are loaded by TMA while this one finishes.
   auto next_valid = [&](int item) {
     while (item < n_items && a.plan.chunk_seq[item / H] < 0) item += gridDim.x;
     return item;
@@ -266,23 +247,39 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     }
     return r;
   };
-  auto issue_main = [&](int item) {  // K, Q, V operand tiles, S0, dS, Ut^T, P, N
-    const int srow = item * D, qrow = item * TQ_TILES * CH;  // state / operand-tile rows of (chunk, head)
+  // The tiles of an item (item = chunk * H + head) arrive in three groups, each on its own mbarrier, each
+  // part issued as soon as the previous item's last reader of its buffers is done:
+  //  A (bar_a, read from P5 on): Ut^T and the chain's dUt^T after that item's P6, X2 after its P7, S0, dS,
+  //    P, N, X1, Ahat after its P8 and its dq store;
+  //  B (bar_b): dO, after that item's dv store;
+  //  W (bar_w, read from P6 on): the K, Q operand tiles and the reciprocal norms after its dk read-out, V
+  //    after its dk store (dk is staged in V's buffer).
+  // The early parts of a group only raise the bytes its barrier expects; the last part arrives, so a phase
+  // completes once every part has been issued and has landed.
+  auto issue_a1 = [&](int item, bool arrive) {  // Ut^T, dUt^T
     const uint32_t bar = u32(&sm.bar_a);
-    mbar_expect_tx(bar, 18 * HT);
+    if (arrive) mbar_expect_tx(bar, 4 * HT);
+    else mbar_expect_tx_only(bar, 4 * HT);
     tma_load_3d(u32(sm.ut), &tmu, 0, (item * T128_TILES + T128_U) * D, 0, bar);
-    tma_load_3d(u32(sm.p), &tmw, 0, (item * T64_TILES + T64_P) * CH, 0, bar);
-    tma_load_3d(u32(sm.n16), &tmw, 0, (item * T64_TILES + T64_N) * CH, 0, bar);
-#pragma unroll
-    for (int hb = 0; hb < 2; ++hb) {
-      tma_load_3d(u32(sm.kq + 2 * hb * HT), &tm3, 64 * hb, qrow + TQ_K * CH, 0, bar);
-      tma_load_3d(u32(sm.kq + (2 * hb + 1) * HT), &tm3, 64 * hb, qrow + TQ_Q * CH, 0, bar);
-      tma_load_3d(u32(sm.v + hb * HT), &tm3, 64 * hb, qrow + TQ_V * CH, 0, bar);
-    }
+    tma_load_3d(u32(sm.wt), &tmdu, 0, item * D, 0, bar);
+  };
+  auto issue_a2 = [&](int item) {  // X2
+    const uint32_t bar = u32(&sm.bar_a);
+    mbar_expect_tx_only(bar, HT);
+    tma_load_3d(u32(sm.x2), &tmw, 0, (item * T64_TILES + T64_X2) * CH, 0, bar);
+  };
+  auto issue_a3 = [&](int item) {  // S0, dS, P, N, X1, Ahat; the group's arrival
+    const int srow = item * D, row = item * T64_TILES * CH;
+    const uint32_t bar = u32(&sm.bar_a);
+    mbar_expect_tx(bar, 12 * HT);
     tma_load_3d(u32(sm.s0), &tms0, 0, srow, 0, bar);
     tma_load_3d(u32(sm.s0 + 2 * HT), &tms0, 64, srow, 0, bar);
     tma_load_3d(u32(sm.ds), &tmds, 0, srow, 0, bar);
     tma_load_3d(u32(sm.ds + 2 * HT), &tmds, 64, srow, 0, bar);
+    tma_load_3d(u32(sm.p), &tmw, 0, row + T64_P * CH, 0, bar);
+    tma_load_3d(u32(sm.n16), &tmw, 0, row + T64_N * CH, 0, bar);
+    tma_load_3d(u32(sm.x1), &tmw, 0, row + T64_X1 * CH, 0, bar);
+    tma_load_3d(u32(sm.ah), &tmw, 0, row + T64_AH * CH, 0, bar);
   };
   auto issue_do = [&](int item, int t0) {
     const int hh = item % H;
@@ -291,23 +288,32 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     tma_load_3d(u32(sm.dob), &tmdo, 0, hh, t0, bar);
     tma_load_3d(u32(sm.dob + HT), &tmdo, 64, hh, t0, bar);
   };
-  // the WY tiles X1, X2, Ahat of an item (item = chunk * H + head): their buffers are free once the
-  // previous item's dk is stored
-  auto issue_wy = [&](int item) {
+  auto issue_w1 = [&](int item) {  // K, Q operand tiles, reciprocal norms
+    const int qrow = item * TQ_TILES * CH;
     const uint32_t bar = u32(&sm.bar_w);
-    const int row = item * T64_TILES * CH;
-    mbar_expect_tx(bar, 3 * HT + 2 * CH * 4);
-    // the reciprocal norms too: the previous item's dk read them until its dk was staged
+    mbar_expect_tx_only(bar, 4 * HT + 2 * CH * 4);
     bulk_load(u32(sm.nk), a.nrm + (size_t)item * 2 * CH, 2 * CH * 4, bar);
-    tma_load_3d(u32(sm.x1), &tmw, 0, row + T64_X1 * CH, 0, bar);
-    tma_load_3d(u32(sm.x2), &tmw, 0, row + T64_X2 * CH, 0, bar);
-    tma_load_3d(u32(sm.ah), &tmw, 0, row + T64_AH * CH, 0, bar);
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) {
+      tma_load_3d(u32(sm.kq + 2 * hb * HT), &tm3, 64 * hb, qrow + TQ_K * CH, 0, bar);
+      tma_load_3d(u32(sm.kq + (2 * hb + 1) * HT), &tm3, 64 * hb, qrow + TQ_Q * CH, 0, bar);
+    }
+  };
+  auto issue_w2 = [&](int item) {  // V; the group's arrival
+    const int qrow = item * TQ_TILES * CH;
+    const uint32_t bar = u32(&sm.bar_w);
+    mbar_expect_tx(bar, 2 * HT);
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) tma_load_3d(u32(sm.v + hb * HT), &tm3, 64 * hb, qrow + TQ_V * CH, 0, bar);
   };
   ItemInfo cur = info_of(next_valid(blockIdx.x));
   if (tid == PRODUCER && cur.item < n_items) {
-    issue_main(cur.item);
+    issue_a1(cur.item, false);
+    issue_a2(cur.item);
+    issue_a3(cur.item);
     issue_do(cur.item, cur.tok0);
-    issue_wy(cur.item);
+    issue_w1(cur.item);
+    issue_w2(cur.item);
   }
   // ---------------- worker warps 0-15: read-outs and the CUDA-core parts of every round
   bool failed = false, release = false;  // release: the producer still waits at a CTA-wide barrier
@@ -354,11 +360,16 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     }
   }
   fence_async_smem();
-  if (__syncthreads_or(false)) {  // B2: the producer issues P2
+  if (__syncthreads_or(false)) {  // B2: the producer issues P5
     failed = true;
     break;
   }
-  {  // meanwhile: <dS, S0> over the whole state (both tiles share one layout, so compare byte positions)
+  if (nitem < n_items && tid < 128) {  // the next item's g or beta, stored under P7 (its plan lookups have landed by now)
+    const int r = tid & 63, nh = nitem % H;
+    if (r < nxt.nvalid)
+      gb_next = tid < 64 ? a.g[(size_t)(nxt.tok0 + r) * H + nh] : a.beta[(size_t)(nxt.tok0 + r) * H + nh];
+  }
+  {  // under P5: <dS, S0> over the whole state (both tiles share one layout, so compare byte positions)
     float acc = 0.f;
     const uint4 *A4 = reinterpret_cast<const uint4 *>(sm.s0), *B4 = reinterpret_cast<const uint4 *>(sm.ds);
 #pragma unroll 2
@@ -373,60 +384,6 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     }
     acc = warp_sum(acc);
     if (lane == 0) sm.red[warp] = acc;
-  }
-  if (wbar_or(!mma_done())) {  // P2
-    failed = release = true;
-    break;
-  }
-  {  // R2: dUt^T = cdec*Y + Z -> wt (the per-token sums over Y and Z follow under P5)
-#pragma unroll 1
-    for (int q4 = 0; q4 < 2; ++q4) {
-      const int cb = c0 + q4 * 8;
-      float y[8], z[8], cd[8];
-      tmem_ld8x2(tm + tl + T3 + cb, y, tm + tl + T4 + cb, z);
-      ld8f(G.cdec + cb, cd);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) z[i] = cd[i] * y[i] + z[i];
-      st_chunk_f16(sm.wt + chunk_off(row, cb), z);
-    }
-  }
-  fence_before();
-  fence_async_smem();
-  {  // X1, X2, Ahat of this item (loaded at the end of the previous one)
-    const bool ok = mbar_wait(u32(&sm.bar_w), it & 1, err, 8);
-    if (__syncthreads_or(!ok)) {  // B3: the producer issues P5
-      failed = true;
-      break;
-    }
-  }
-  if (nitem < n_items && tid < 128) {  // the next item's g or beta, stored under P7 (its plan lookups have landed by now)
-    const int r = tid & 63, nh = nitem % H;
-    if (r < nxt.nvalid)
-      gb_next = tid < 64 ? a.g[(size_t)(nxt.tok0 + r) * H + nh] : a.beta[(size_t)(nxt.tok0 + r) * H + nh];
-  }
-  {  // under P5: per-token sums <Ut, Y> over d_v (Y stays in T3 until P6; Ut^T from its tile)
-    float t1 = 0.f;
-#pragma unroll 1
-    for (int q4 = 0; q4 < 2; ++q4) {
-      const int cb = c0 + q4 * 8;
-      float y[8], u[8];
-      tmem_ld8(tm + tl + T3 + cb, y);
-      {
-        const uint4 raw = *reinterpret_cast<const uint4 *>(sm.ut + chunk_off(row, cb));
-        const __half2 *uh = reinterpret_cast<const __half2 *>(&raw);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __half22float2(uh[i]);
-          u[2 * i] = f.x;
-          u[2 * i + 1] = f.y;
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) y[i] *= u[i];
-      const float a1 = colsum8(y);
-      if ((lane >> 3) == q4) t1 = a1;
-    }
-    if (lane < 16) sm.part[wq][c0 + lane] = t1;
   }
   if (wbar_or(!mma_done())) {  // P5
     failed = release = true;
@@ -487,12 +444,14 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
   }
   fence_before();
   fence_async_smem();
-  if (__syncthreads_or(false)) {  // B4: the producer issues P6
-    failed = true;
-    break;
+  {  // K, Q, V and the norms of this item (loaded at the end of the previous one)
+    const bool ok = mbar_wait(u32(&sm.bar_w), it & 1, err, 8);
+    if (__syncthreads_or(!ok)) {  // B4: the producer issues P6
+      failed = true;
+      break;
+    }
   }
   if (tid < 64) {
-    sm.acc[0][tid] = sm.part[0][tid] + sm.part[1][tid] + sm.part[2][tid] + sm.part[3][tid];      // <Ut, Y>
     sm.acc[2][tid] = sm.part[16][tid] + sm.part[17][tid] + sm.part[18][tid] + sm.part[19][tid];  // row sums of dP * P
     sm.acc[3][tid] = sm.part[8][tid] + sm.part[9][tid] + sm.part[10][tid] + sm.part[11][tid];  // column sums of dP * P
   }
@@ -616,16 +575,34 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     sm.acc[4][tid] = sm.part[0][tid] + sm.part[1][tid] + sm.part[2][tid] + sm.part[3][tid];  // lower col sums of X2 * M2
     sm.acc[1][tid] = sm.part[4][tid] + sm.part[5][tid] + sm.part[6][tid] + sm.part[7][tid];  // <dW, W> + rows of X2 * M2
   }
-  {  // K^ -> wt (dUt^T is dead): R9 reads k^ there, so the K/Q buffer is free once P9 is done
-    const uint4 *src = reinterpret_cast<const uint4 *>(sm.kq);
-    uint4 *dst = reinterpret_cast<uint4 *>(sm.wt);
-    for (int e = tid; e < 2 * HT / 16; e += LTHREADS) dst[e] = src[(e >= HT / 16 ? 2 * HT / 16 : 0) + (e % (HT / 16))];
+  {  // under P7: <k^_t, Kb[:, t]> per token over d_k (Kb = dS^T Ut^T, so this is <Ut_t, dS k^_t>: cdec_t times it
+     // is the state term y_t of the gate gradient and the cdec Kb part of k^ . dk^), Kb fragments against k^
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+    for (int ls = 0; ls < 32; ls += 16) {
+      float kbv[8];
+      uint32_t kf[4];
+      tmem_ld_frag1(tm + tl + ((uint32_t)ls << 16) + T2 + c0, kbv);
+      ldmatrix_x4_trans(frag_addr(sm.kq, 2 * HT, wq, ls, c0, lane), kf);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float2 k2 = unpack_f16(kf[m]);
+        s4[(m >> 1) * 2] += kbv[2 * m] * k2.x;
+        s4[(m >> 1) * 2 + 1] += kbv[2 * m + 1] * k2.y;
+      }
+    }
+    col_sum4(s4);
+    if (lane < 4) {
+      float *d = sm.part[16 + wq];
+      d[ta] = s4[0]; d[ta + 1] = s4[1]; d[ta + 8] = s4[2]; d[ta + 9] = s4[3];
+    }
   }
   if (warp == 1 && nitem < n_items) gate_prefix(sm.g[gbuf ^ 1], sm.gt[gbuf ^ 1]);  // next item's gates, under P7
   if (wbar_or(!mma_done())) {  // P7
     failed = release = true;
     break;
   }
+  if (tid < 64) sm.acc[0][tid] = sm.part[16][tid] + sm.part[17][tid] + sm.part[18][tid] + sm.part[19][tid];  // <k^, Kb>
   {  // R7: Y1 (M = 64 fragment) -> v (first half; V is dead)
     float v[8];
     uint32_t out[4];
@@ -740,8 +717,9 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
   if (warp == LWARPS - 1) {  // under P9 (the other warps' shadow work is the k^ . dk^ sum)
     // dg_t = sum_{r >= t} dG_r + gam_C <dS, S0> + sum_{r < t} y_r: dG_r holds the terms whose decay factor
     // starts or ends at r (gamma_r of the inter-chunk output and of W; the ratios of P and X2, diagonal
-    // excluded); the state terms y_r = cdec_r <Ut_r, Y_r> depend on g_t only for r < t (through cdec_r),
-    // so they enter by a forward exclusive scan (not as a total minus a reverse partial sum)
+    // excluded); the state terms y_r = cdec_r <Ut_r, dS k_r> (= cdec_r <k_r, Kb[:, r]>) depend on g_t only
+    // for r < t (through cdec_r), so they enter by a forward exclusive scan (not as a total minus a reverse
+    // partial sum)
     float dGv[2], yv[2];
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
@@ -785,7 +763,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     break;
   }
   {  // R9: dk^T = Ka + cdec * Kb (lanes d_k); Jacobian; dk out
-    uint8_t *const stg = sm.x2;  // x2 + ah (16 KB, both dead after P8)
+    uint8_t *const stg = sm.v;  // V's buffer (Y1 and dN are dead once P9 is done)
     float cd[4], dt[4], nkv[4];
     tok4(G.cdec, ta, cd);
     if (l2) {
@@ -798,7 +776,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
       float ka[8], kbv[8];
       tmem_ld_frag2(tq + T3, ka, tq + T2, kbv);
       uint32_t kf[4], pk[4];
-      if (l2) ldmatrix_x4_trans(frag_addr(sm.wt, HT, wq, ls, c0, lane), kf);
+      if (l2) ldmatrix_x4_trans(frag_addr(sm.kq, 2 * HT, wq, ls, c0, lane), kf);
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         float o[2];
@@ -823,8 +801,8 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     break;
   }
   if (nvalid < CH) {
-    store_rows(a.dk, sm.x2, h, tok0, nvalid);
-    if (__syncthreads_or(false)) {  // B11: x2 / ah read, the producer may load the next WY tiles
+    store_rows(a.dk, sm.v, h, tok0, nvalid);
+    if (__syncthreads_or(false)) {  // B11: the dk staging is read, the producer may load the next V
       failed = true;
       break;
     }
@@ -834,49 +812,28 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
   if (release) __syncthreads_or(true);  // meet the producer at its pending CTA-wide barrier: it stops there
   } else {
   // ---------------- producer warp 16 (lane 0): every tensor-core product, TMA load and TMA store
-  bool pend_main = cur.item < n_items, pend_do = pend_main, pend_wy = pend_main;  // loads in flight
+  // Loads in flight that the workers have not waited for (pend_*), groups partly issued whose barrier still
+  // lacks its arrival (open_*), and the parity of the phase each refers to.
+  bool pend_a = cur.item < n_items, pend_b = pend_a, pend_w = pend_a, open_a = false, open_w = false;
+  uint32_t par_a = 0, par_b = 0, par_w = 0;
   for (; cur.item < n_items; ++it) {
     const ItemInfo nxt = info_of(next_valid(cur.item + gridDim.x));
     const int nitem = nxt.item;
+    const bool more = nitem < n_items;
+    const uint32_t npar = (it + 1) & 1;  // phase parity of the next item's loads
     const int item = cur.item, h = item % H, tok0 = cur.tok0, nvalid = cur.nvalid;
     {
       const bool f = __syncthreads_or(false);  // B2
-      pend_main = pend_do = false;  // the workers waited for both (a failed wait is not repeated)
+      pend_a = pend_b = false;  // the workers waited for both (a failed wait is not repeated)
       if (f) break;
     }
-    // ---- P2: Y = dS K^T -> T3;  Qa = S0^T dO^T -> T5;  Z = dO^T P -> T4  (inputs and context only)
-    if (lane == 0) {
-      fence_after();
-      const uint32_t id_kk = idesc_f16(128, 64, false, false);
-      const uint32_t id_mk = idesc_f16(128, 64, true, false);
-      const uint32_t id_mm = idesc_f16(128, 64, true, true);
-      const uint32_t kb = u32(sm.kq), dsb = u32(sm.ds), dob = u32(sm.dob), sb = u32(sm.s0), pb = u32(sm.p);
-#pragma unroll 1
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
-        mma_f16(tm + T3, sdesc(dsb + aoff, 16, 1024), sdesc(kb + aoff, 16, 1024), id_kk, kk > 0);
-      }
-#pragma unroll 1
-      for (int kk = 0; kk < 4; ++kk)
-        mma_f16(tm + T4, sdesc(dob + kk * 2048, HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id_mm, kk > 0);
-      mma_commit(u32(&sm.bar_mma));
-      // Qa is first read under P6: the P5 commit covers it (the tensor cores run in issue order)
-#pragma unroll 1
-      for (int kk = 0; kk < 8; ++kk)
-        mma_f16(tm + T5, sdesc(sb + kk * 2048, 2 * HT, 1024), sdesc(dob + (kk >> 2) * HT + (kk & 3) * 32, 16, 1024),
-                id_mk, kk > 0);
-    }
-    __syncwarp();
-    {
-      const bool f = __syncthreads_or(false);  // B3
-      pend_wy = false;
-      if (f) break;
-    }
-    // ---- P5: dP = dO Ut^T -> T0 (M = 64); dW'^T = -S0^T dUt^T -> T1; dV^T = dUt^T X2 -> T6;  Kb = dS^T Ut^T -> T2
+    // ---- P5: dP = dO Ut^T -> T0 (M = 64); dW'^T = -S0^T dUt^T -> T1; dV^T = dUt^T X2 -> T6; Qa = S0^T dO^T -> T5
+    //      (all before the commit: R5 overwrites S0 with dW'^T); then Kb = dS^T Ut^T -> T2 (first read under P7:
+    //      the P6 commit covers it)
     if (lane == 0) {
       fence_after();
       const uint32_t id_kmn = idesc_f16(128, 64, false, true), id_dp = idesc_f16(64, 64, false, true);
-      const uint32_t id_mmn_neg = idesc_f16(128, 64, true, true, true);
+      const uint32_t id_mmn_neg = idesc_f16(128, 64, true, true, true), id_mk = idesc_f16(128, 64, true, false);
       const uint32_t dob = u32(sm.dob), ub = u32(sm.ut), sb = u32(sm.s0), dub = u32(sm.wt), x2b = u32(sm.x2);
 #pragma unroll 1
       for (int kk = 0; kk < 8; ++kk) {
@@ -888,15 +845,22 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
 #pragma unroll 1
       for (int kk = 0; kk < 4; ++kk)
         mma_f16(tm + T6, sdesc(dub + kk * 32, 16, 1024), sdesc(x2b + kk * 2048, HT, 1024), id_kmn, kk > 0);
+#pragma unroll 1
+      for (int kk = 0; kk < 8; ++kk)
+        mma_f16(tm + T5, sdesc(sb + kk * 2048, 2 * HT, 1024), sdesc(dob + (kk >> 2) * HT + (kk & 3) * 32, 16, 1024),
+                id_mk, kk > 0);
       mma_commit(u32(&sm.bar_mma));
-      // Kb is first read in R9: the P6 commit covers it
       const uint32_t id_mm = idesc_f16(128, 64, true, true), dsb = u32(sm.ds);
 #pragma unroll 1
       for (int kk = 0; kk < 8; ++kk)
         mma_f16(tm + T2, sdesc(dsb + kk * 2048, 2 * HT, 1024), sdesc(ub + kk * 2048, 2 * HT, 1024), id_mm, kk > 0);
     }
     __syncwarp();
-    if (__syncthreads_or(false)) break;  // B4
+    {
+      const bool f = __syncthreads_or(false);  // B4 (the workers waited for K, Q, V)
+      pend_w = false;
+      if (f) break;
+    }
     // ---- P6: M1 = dW' K^T -> T3;  M2 = dUt V^T -> T4 (both M = 64);  then Qb = K^T dPm^T -> T7 (first read
     //      under P8: the P7 commit covers it)
     if (lane == 0) {
@@ -920,7 +884,8 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     if (lane == 0 && nvalid == CH) store_tma(&tmdv, sm.dob, h, tok0);
     if (__syncthreads_or(false)) break;  // B6
     // ---- P7: Y1 = Ahat^T dAhat -> T0 (M = 64);  then Ka's context-only part Q^T dPm + dW'^T X1 -> T3 (first read in
-    //      R9: the P8 commit covers it; M1 in T3 was read above)
+    //      R9: the P8 commit covers it; M1 in T3 was read above).  Then the next item's dO (once the dv store has
+    //      read its staging) and its Ut^T, dUt^T (their last readers, P5 and P6, are done)
     if (lane == 0) {
       fence_after();
       const uint32_t id = idesc_f16(128, 64, true, true), id_y1 = idesc_f16(64, 64, true, true);
@@ -936,15 +901,19 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
         mma_f16(tm + T3, sdesc(kb + HT + kk * 2048, 2 * HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id, kk > 0);
         mma_f16(tm + T3, sdesc(dwb + kk * 32, 16, 1024), sdesc(x1b + kk * 2048, HT, 1024), id_km, true);
       }
-      if (nitem < n_items) {  // dO of the next item into its buffer, once the dv tile store has read it
+      if (more) {
         tma_store_wait_read();
         issue_do(nitem, nxt.tok0);
+        issue_a1(nitem, false);
       }
     }
     __syncwarp();
-    if (nitem < n_items) pend_do = true;
+    if (more) {
+      pend_b = open_a = true;
+      par_b = par_a = npar;
+    }
     if (__syncthreads_or(false)) break;  // B7
-    // ---- P8: dT = -Y1 Ahat^T -> T1 (M = 64)
+    // ---- P8: dT = -Y1 Ahat^T -> T1 (M = 64); then the next item's X2 (dAhat, its last reader Y1, is done)
     if (lane == 0) {
       fence_after();
       const uint32_t id = idesc_f16(64, 64, false, false, true);
@@ -952,12 +921,15 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
 #pragma unroll 1
       for (int kk = 0; kk < 4; ++kk) mma_f16(tm + T1, sdesc(yb + kk * 32, 16, 1024), sdesc(ab + kk * 32, 16, 1024), id, kk > 0);
       mma_commit(u32(&sm.bar_mma));
+      if (more) issue_a2(nitem);
     }
     __syncwarp();
     if (__syncthreads_or(false)) break;  // B8
     if (lane == 0 && nvalid == CH) store_tma(&tmdq, sm.ds, h, tok0);
     if (__syncthreads_or(false)) break;  // B9
-    // ---- P9: Ka += K^T (dN + dN^T) -> T3  (Ka's context-only part came with P7; Kb = dS^T Ut^T with P5, in T2)
+    // ---- P9: Ka += K^T (dN + dN^T) -> T3  (Ka's context-only part came with P7; Kb = dS^T Ut^T with P5, in T2);
+    //      then the rest of the next item's group A: S0, P, X1 (last read by Ka's context part, which the P8
+    //      commit covered), Ahat (P8), N (R8), dS once the dq store has read its staging
     if (lane == 0) {
       fence_after();
       const uint32_t id_mm = idesc_f16(128, 64, true, true);
@@ -970,33 +942,48 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
         mma_f16(tm + T3, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(sgb + kk * 32, 16, 1024), id_mk, true);
       }
       mma_commit(u32(&sm.bar_mma));
+      if (more) {
+        tma_store_wait_read();
+        issue_a3(nitem);
+      }
     }
     __syncwarp();
-    // K, Q, V, S0, dS, Ut^T, P, N of the next item once P9 is done (ds also once the dq store has read it);
-    // P9 is the sixth of six commits per item: its completion has parity 1
-    if (lane == 0 && nitem < n_items && mbar_wait(u32(&sm.bar_mma), 1, err, 4)) {
-      tma_store_wait_read();
-      issue_main(nitem);
-      pend_main = true;  // the flags are read by lane 0 only
+    if (more) {
+      open_a = false;
+      pend_a = true;
     }
-    __syncwarp();
     if (__syncthreads_or(false)) break;  // B10
-    if (lane == 0 && nvalid == CH) store_tma(&tmdk, sm.x2, h, tok0);
-    if (nvalid < CH && __syncthreads_or(false)) break;  // B11
-    if (lane == 0 && nitem < n_items) {  // X1, X2, Ahat of the next item once the dk staging is read
-      tma_store_wait_read();
-      issue_wy(nitem);
+    // dk (staged in V's buffer); the next item's K, Q and norms (R9 has read them), then its V once the dk
+    // staging is read
+    if (lane == 0) {
+      if (nvalid == CH) store_tma(&tmdk, sm.v, h, tok0);
+      if (more) issue_w1(nitem);
     }
     __syncwarp();
-    if (nitem < n_items) pend_wy = true;
+    if (more) {
+      open_w = true;
+      par_w = npar;
+    }
+    if (nvalid < CH && __syncthreads_or(false)) break;  // B11
+    if (lane == 0 && more) {
+      tma_store_wait_read();
+      issue_w2(nitem);
+    }
+    __syncwarp();
+    if (more) {
+      open_w = false;
+      pend_w = true;
+    }
     cur = nxt;
   }
   failed = cur.item < n_items;
   if (lane == 0) {
     if (failed) {  // let loads already in flight land before the CTA leaves (bounded waits)
-      if (pend_main) mbar_wait(u32(&sm.bar_a), (it + 1) & 1, err, 8);
-      if (pend_do) mbar_wait(u32(&sm.bar_b), (it + 1) & 1, err, 8);
-      if (pend_wy) mbar_wait(u32(&sm.bar_w), it & 1, err, 8);  // issued for the item of iteration it
+      if (open_a) mbar_arrive(u32(&sm.bar_a));  // a partly issued group completes on the parts issued
+      if (open_w) mbar_arrive(u32(&sm.bar_w));
+      if (pend_a || open_a) mbar_wait(u32(&sm.bar_a), par_a, err, 8);
+      if (pend_b) mbar_wait(u32(&sm.bar_b), par_b, err, 8);
+      if (pend_w || open_w) mbar_wait(u32(&sm.bar_w), par_w, err, 8);
     }
     tma_store_wait_all();  // output tiles written before the CTA leaves
   }
@@ -1028,7 +1015,7 @@ int launch_bwd_local_tc(const BwdArgs &a, const CUtensorMap *maps, int CH_max, c
   const int n_items = CH_max * a.H;
   const int grid = n_items < sms ? n_items : sms;  // persistent: one CTA per SM
   return (int)launch_pdl(bwd_local_tc_kernel, dim3(grid), dim3(LNTHREADS), smem, st, a, maps[0], maps[1], maps[2],
-                         maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], n_items);
+                         maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], maps[9], n_items);
 }
 
 }  // namespace gdn

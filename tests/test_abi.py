@@ -127,13 +127,15 @@ def test_forward_context_region(lib):
     (five fp16 64 x 64 tiles and three fp16 64 x 128 operand tiles per (chunk, head)); the backward's
     buffers start where that region starts.  With one segment per sequence (no sequence-parallel
     buffers) the forward and the saved-context backward share the same core, so the difference of
-    their workspaces is exactly that region minus the backward's fp16 per-chunk dS."""
+    their workspaces is exactly that region minus the backward's fp16 per-chunk dS (128 x 128) and the
+    reverse chain's fp16 per-chunk dUt^T (128 x 64), which the local-gradient kernel reads."""
     chunks, H = (1000 + 63) // 64, 3
     s = _shape(T=1000, H=H, flags=_lib.GDN_SP_OFF)
     ctx = chunks * H * (5 * 64 * 64 + 3 * 64 * 128) * 2
     dstates = chunks * H * 128 * 128 * 2
+    dut = chunks * H * 128 * 64 * 2
     fwd = lib.gdn_fwd_workspace_size(ctypes.byref(s))
-    assert fwd - lib.gdn_bwd_saved_workspace_size(ctypes.byref(s)) == ctx - dstates
+    assert fwd - lib.gdn_bwd_saved_workspace_size(ctypes.byref(s)) == ctx - dstates - dut
     # fp32, d = 64 runs the mma.sync kernels: no context region, fp32 per-chunk dS
     s = _shape(T=1000, H=H, Dk=64, Dv=64, dtype=_lib.GDN_FP32, flags=_lib.GDN_SP_OFF)
     fwd = lib.gdn_fwd_workspace_size(ctypes.byref(s))
