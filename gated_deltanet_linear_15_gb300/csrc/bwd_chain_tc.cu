@@ -227,16 +227,18 @@ __device__ __forceinline__ void chain_tc_item(const BwdArgs &a, const CUtensorMa
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * 2 * HT + (kk & 3) * 32;
-          mma_f16(tm + TM_Y, sdesc(dsb + off, 16, 1024), sdesc(kb + off, 16, 1024), id_kk, kk > 0);
+          mma_f16s(tm + TM_Y, sdesc_s(dsb, 16, 1024) + (off), sdesc_s(kb, 16, 1024) + (off), id_kk, kk > 0);
         }
         if (with_do) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_f16(tm + TM_DU, sdesc(dob + kk * 2048, HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id_mm, kk > 0);
+            mma_f16s(tm + TM_DU, sdesc_s(dob, HT, 1024) + (kk * 2048), sdesc_s(pb, HT, 1024) + (kk * 2048), id_mm,
+                     kk > 0);
           const uint32_t id_s = idesc_f16(128, 128, true, true), dgb = u32(sm.dog), qb = u32(st + HT);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_f16(tm + TM_S, sdesc(dgb + kk * 2048, HT, 1024), sdesc(qb + kk * 2048, 2 * HT, 1024), id_s, true);
+            mma_f16s(tm + TM_S, sdesc_s(dgb, HT, 1024) + (kk * 2048), sdesc_s(qb, 2 * HT, 1024) + (kk * 2048), id_s,
+                     true);
         }
         mma_commit(u32(&sm.bar_mma));
       }
@@ -251,7 +253,7 @@ __device__ __forceinline__ void chain_tc_item(const BwdArgs &a, const CUtensorMa
         const uint32_t dub = u32(sm.kc), wb = u32(st + 7 * HT);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_f16(tm + TM_S, sdesc(dub + kk * 32, 16, 1024), sdesc(wb + kk * 32, 16, 1024), id_kk_neg, true);
+          mma_f16s(tm + TM_S, sdesc_s(dub, 16, 1024) + (kk * 32), sdesc_s(wb, 16, 1024) + (kk * 32), id_kk_neg, true);
         mma_commit(u32(&sm.bar_mma));
         if (store && c < cend) {  // dUt^T of chunk c for the local-gradient kernel (read before the next
           tma_store_3d(&tmdu, 0, ((chunk0 + c) * H + h) * D, 0, dub);  // chunk's read-out rewrites kc)

@@ -17,12 +17,11 @@
 // next round computes:
 //   P5 dP = dO Ut^T->T0, dW'^T = -S0^T dUt^T->T1, dV^T = dUt^T X2->T6, Qa = S0^T dO^T->T5 [Kb = dS^T Ut^T->T2]
 //                            under P5: <dS, S0>;  R5: dPm (over P), dP*P sums; dW'^T tile
-//   P6 M1 = dW' K^T->T3, M2 = dUt V^T->T4 [Qb = K^T dPm^T->T7]
+//   P6 M1 = dW' K^T->T3, M2 = dUt V^T->T4 [Qb = K^T dPm^T->T7, Ka = Q^T dPm + dW'^T X1->T0]
 //                            under P6: dv out, gam <Qa,q>;  R6: dAhat tile, beta column sums, <dV,v>
-//   P7 Y1 = Ahat^T dAhat->T0 [Ka = Q^T dPm + dW'^T X1->T3]
-//                            under P7: <k, Kb>, next item's gates;  R7: Y1 tile
+//   P7 Y1 = Ahat^T dAhat->T3 under P7: <k, Kb>, next item's gates;  R7: Y1 tile
 //   P8 dT = -Y1 Ahat^T->T1   under P8: dq out;  R8: dN tile (strictly lower), beta row sums (with N)
-//   P9 Ka += K^T (dN + dN^T)->T3
+//   P9 Ka += K^T (dN + dN^T)->T0
 //                            R9: dk out (Ka + cdec Kb);  dg (reverse cumsum), dbeta
 #include <cstddef>
 #include <type_traits>
@@ -61,7 +60,7 @@ struct __align__(1024) LocalTcSmem {
   float g[2][CH], beta[2][CH];  // per item parity: the next item's gates are prepared during this one
   float nk[CH], nq[CH];         // reciprocal norms 1/|k|, 1/|q| (context, one bulk copy)
   Gates gt[2];
-  float part[20][CH];   // per-token partial sums (reused per round)
+  float part[24][CH];   // per-token partial sums (reused per round)
   float acc[9][CH];     // assembled per-token terms
   float red[LWARPS];
   uint64_t bar_a, bar_b, bar_w, bar_mma;  // TMA: {Ut^T, dUt^T, X2, S0, dS, P, N, X1, Ahat}, {dO}, {K, Q, norms, V};
@@ -249,36 +248,39 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
   };
   // The tiles of an item (item = chunk * H + head) arrive in three groups, each on its own mbarrier, each
   // part issued as soon as the previous item's last reader of its buffers is done:
-  //  A (bar_a, read from P5 on): Ut^T and the chain's dUt^T after that item's P6, X2 after its P7, S0, dS,
-  //    P, N, X1, Ahat after its P8 and its dq store;
+  //  A (bar_a, read from P5 on): Ut^T, the chain's dUt^T and dS after that item's P6 (and Kb); X2, the first
+  //    half of S0, P, X1 after its P7 (which covers Ka's context part); the second half of S0 (its dq
+  //    staging) after its dq store, Ahat and N after its P8 and R8;
   //  B (bar_b): dO, after that item's dv store;
   //  W (bar_w, read from P6 on): the K, Q operand tiles and the reciprocal norms after its dk read-out, V
   //    after its dk store (dk is staged in V's buffer).
   // The early parts of a group only raise the bytes its barrier expects; the last part arrives, so a phase
   // completes once every part has been issued and has landed.
-  auto issue_a1 = [&](int item, bool arrive) {  // Ut^T, dUt^T
+  auto issue_a1 = [&](int item, bool arrive) {  // Ut^T, dUt^T, dS
     const uint32_t bar = u32(&sm.bar_a);
-    if (arrive) mbar_expect_tx(bar, 4 * HT);
-    else mbar_expect_tx_only(bar, 4 * HT);
+    const int srow = item * D;
+    if (arrive) mbar_expect_tx(bar, 8 * HT);
+    else mbar_expect_tx_only(bar, 8 * HT);
     tma_load_3d(u32(sm.ut), &tmu, 0, (item * T128_TILES + T128_U) * D, 0, bar);
     tma_load_3d(u32(sm.wt), &tmdu, 0, item * D, 0, bar);
-  };
-  auto issue_a2 = [&](int item) {  // X2
-    const uint32_t bar = u32(&sm.bar_a);
-    mbar_expect_tx_only(bar, HT);
-    tma_load_3d(u32(sm.x2), &tmw, 0, (item * T64_TILES + T64_X2) * CH, 0, bar);
-  };
-  auto issue_a3 = [&](int item) {  // S0, dS, P, N, X1, Ahat; the group's arrival
-    const int srow = item * D, row = item * T64_TILES * CH;
-    const uint32_t bar = u32(&sm.bar_a);
-    mbar_expect_tx(bar, 12 * HT);
-    tma_load_3d(u32(sm.s0), &tms0, 0, srow, 0, bar);
-    tma_load_3d(u32(sm.s0 + 2 * HT), &tms0, 64, srow, 0, bar);
     tma_load_3d(u32(sm.ds), &tmds, 0, srow, 0, bar);
     tma_load_3d(u32(sm.ds + 2 * HT), &tmds, 64, srow, 0, bar);
+  };
+  auto issue_a2 = [&](int item) {  // X2, S0 (first feature block), P, X1
+    const uint32_t bar = u32(&sm.bar_a);
+    const int row = item * T64_TILES * CH;
+    mbar_expect_tx_only(bar, 5 * HT);
+    tma_load_3d(u32(sm.x2), &tmw, 0, row + T64_X2 * CH, 0, bar);
+    tma_load_3d(u32(sm.s0), &tms0, 0, item * D, 0, bar);
     tma_load_3d(u32(sm.p), &tmw, 0, row + T64_P * CH, 0, bar);
-    tma_load_3d(u32(sm.n16), &tmw, 0, row + T64_N * CH, 0, bar);
     tma_load_3d(u32(sm.x1), &tmw, 0, row + T64_X1 * CH, 0, bar);
+  };
+  auto issue_a3 = [&](int item) {  // S0 (second feature block), N, Ahat; the group's arrival
+    const uint32_t bar = u32(&sm.bar_a);
+    const int row = item * T64_TILES * CH;
+    mbar_expect_tx(bar, 4 * HT);
+    tma_load_3d(u32(sm.s0 + 2 * HT), &tms0, 64, item * D, 0, bar);
+    tma_load_3d(u32(sm.n16), &tmw, 0, row + T64_N * CH, 0, bar);
     tma_load_3d(u32(sm.ah), &tmw, 0, row + T64_AH * CH, 0, bar);
   };
   auto issue_do = [&](int item, int t0) {
@@ -485,7 +487,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     if (lane < 4) {
       float gm[4];
       tok4(G.gam, ta, gm);
-      float *dst = sm.part[12 + wq];
+      float *dst = sm.part[20 + wq];
       dst[ta] = gm[0] * s[0];
       dst[ta + 1] = gm[1] * s[1];
       dst[ta + 8] = gm[2] * s[2];
@@ -493,17 +495,19 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     }
   }
   fence_before();
-  fence_async_smem();
-  if (__syncthreads_or(false)) {  // B5: the producer stores a full dv tile
-    failed = true;
-    break;
+  fence_async_smem();  // the producer stores a full dv tile at B6
+  if (nvalid < CH) {  // a partial one: its valid rows, once every warp has staged its part
+    if (wbar_or(false)) {
+      failed = release = true;
+      break;
+    }
+    store_rows(a.dv, sm.dob, h, tok0, nvalid);
   }
-  if (nvalid < CH) store_rows(a.dv, sm.dob, h, tok0, nvalid);
-  if (tid < 64) sm.acc[5][tid] = sm.part[12][tid] + sm.part[13][tid] + sm.part[14][tid] + sm.part[15][tid];
   if (wbar_or(!mma_done())) {  // P6
     failed = release = true;
     break;
   }
+  if (tid < 64) sm.acc[5][tid] = sm.part[20][tid] + sm.part[21][tid] + sm.part[22][tid] + sm.part[23][tid];
   {
     // M1, M2 (M = 64 fragments, rows r): dAhat = beta_i (M1 + Gamma M2); beta column sums colsum_i(Ahat (M1 +
     // Gamma M2)); colsum_i(Ahat M1) (the dW'^T X1 part of dk^ dotted with k^).  Gate terms: <dW_r, W_r> =
@@ -606,7 +610,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
   {  // R7: Y1 (M = 64 fragment) -> v (first half; V is dead)
     float v[8];
     uint32_t out[4];
-    tmem_ld_frag1(tm + tl + T0 + c0, v);
+    tmem_ld_frag1(tm + tl + T3 + c0, v);
 #pragma unroll
     for (int m = 0; m < 4; ++m) out[m] = pack_f16(v[2 * m], v[2 * m + 1]);
     stmatrix_x4(rfrag_addr(sm.v, wq, c0, lane), out);
@@ -618,7 +622,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     break;
   }
   {  // under P8: dq raw = (scale dq^ - q^ (q^ . dq^) / scale) / |q|   (or scale dq^ without normalisation),
-     // staged in ds (dS is dead: its last reader, Kb, completed under P6)
+     // staged in the second half of S0's buffer (S0 is dead after P5; dW'^T fills the first half)
     const float rscale = 1.f / a.scale;
     float gm[4], dt[4], nqv[4];
     tok4(G.gam, ta, gm);
@@ -653,7 +657,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
         }
         pk[m] = pack_bf16(o[0], o[1]);
       }
-      stmatrix_x4_trans(frag_addr(sm.ds, HT, wq, ls, c0, lane), pk);
+      stmatrix_x4_trans(frag_addr(sm.s0 + 2 * HT, HT, wq, ls, c0, lane), pk);
     }
   }
   fence_before();
@@ -662,7 +666,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     failed = true;
     break;
   }
-  if (nvalid < CH) store_rows(a.dq, sm.ds, h, tok0, nvalid);
+  if (nvalid < CH) store_rows(a.dq, sm.s0 + 2 * HT, h, tok0, nvalid);
   if (wbar_or(!mma_done())) {  // P8
     failed = release = true;
     break;
@@ -774,7 +778,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     for (int ls = 0; ls < 32; ls += 16) {
       const uint32_t tq = tm + tl + ((uint32_t)ls << 16) + c0;
       float ka[8], kbv[8];
-      tmem_ld_frag2(tq + T3, ka, tq + T2, kbv);
+      tmem_ld_frag2(tq + T0, ka, tq + T2, kbv);
       uint32_t kf[4], pk[4];
       if (l2) ldmatrix_x4_trans(frag_addr(sm.kq, 2 * HT, wq, ls, c0, lane), kf);
 #pragma unroll
@@ -835,25 +839,26 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
       const uint32_t id_kmn = idesc_f16(128, 64, false, true), id_dp = idesc_f16(64, 64, false, true);
       const uint32_t id_mmn_neg = idesc_f16(128, 64, true, true, true), id_mk = idesc_f16(128, 64, true, false);
       const uint32_t dob = u32(sm.dob), ub = u32(sm.ut), sb = u32(sm.s0), dub = u32(sm.wt), x2b = u32(sm.x2);
-#pragma unroll 1
+#pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
-        mma_f16(tm + T0, sdesc(dob + (kk >> 2) * HT + (kk & 3) * 32, 16, 1024), sdesc(ub + kk * 2048, 2 * HT, 1024),
-                id_dp, kk > 0);
-        mma_f16(tm + T1, sdesc(sb + kk * 2048, 2 * HT, 1024), sdesc(dub + kk * 2048, 2 * HT, 1024), id_mmn_neg,
-                kk > 0);
+        mma_f16s(tm + T0, sdesc_s(dob, 16, 1024) + ((kk >> 2) * HT + (kk & 3) * 32),
+                 sdesc_s(ub, 2 * HT, 1024) + (kk * 2048), id_dp, kk > 0);
+        mma_f16s(tm + T1, sdesc_s(sb, 2 * HT, 1024) + (kk * 2048), sdesc_s(dub, 2 * HT, 1024) + (kk * 2048), id_mmn_neg,
+                 kk > 0);
       }
-#pragma unroll 1
+#pragma unroll
       for (int kk = 0; kk < 4; ++kk)
-        mma_f16(tm + T6, sdesc(dub + kk * 32, 16, 1024), sdesc(x2b + kk * 2048, HT, 1024), id_kmn, kk > 0);
-#pragma unroll 1
+        mma_f16s(tm + T6, sdesc_s(dub, 16, 1024) + (kk * 32), sdesc_s(x2b, HT, 1024) + (kk * 2048), id_kmn, kk > 0);
+#pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_f16(tm + T5, sdesc(sb + kk * 2048, 2 * HT, 1024), sdesc(dob + (kk >> 2) * HT + (kk & 3) * 32, 16, 1024),
-                id_mk, kk > 0);
+        mma_f16s(tm + T5, sdesc_s(sb, 2 * HT, 1024) + (kk * 2048),
+                 sdesc_s(dob, 16, 1024) + ((kk >> 2) * HT + (kk & 3) * 32), id_mk, kk > 0);
       mma_commit(u32(&sm.bar_mma));
       const uint32_t id_mm = idesc_f16(128, 64, true, true), dsb = u32(sm.ds);
-#pragma unroll 1
+#pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_f16(tm + T2, sdesc(dsb + kk * 2048, 2 * HT, 1024), sdesc(ub + kk * 2048, 2 * HT, 1024), id_mm, kk > 0);
+        mma_f16s(tm + T2, sdesc_s(dsb, 2 * HT, 1024) + (kk * 2048), sdesc_s(ub, 2 * HT, 1024) + (kk * 2048), id_mm,
+                 kk > 0);
     }
     __syncwarp();
     {
@@ -861,46 +866,47 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
       pend_w = false;
       if (f) break;
     }
-    // ---- P6: M1 = dW' K^T -> T3;  M2 = dUt V^T -> T4 (both M = 64);  then Qb = K^T dPm^T -> T7 (first read
-    //      under P8: the P7 commit covers it)
+    // ---- P6: M1 = dW' K^T -> T3;  M2 = dUt V^T -> T4 (both M = 64);  then Qb = K^T dPm^T -> T7 and Ka's
+    //      context-only part Q^T dPm + dW'^T X1 -> T0 (dP, read in R5, is dead), both first read after the P7
+    //      commit, which covers them
     if (lane == 0) {
       fence_after();
       const uint32_t id_mk = idesc_f16(128, 64, true, false), id_m64 = idesc_f16(64, 64, true, false);
+      const uint32_t id = idesc_f16(128, 64, true, true), id_km = idesc_f16(128, 64, false, true);
       const uint32_t kb = u32(sm.kq), pb = u32(sm.p), dwb = u32(sm.s0), dub = u32(sm.wt), vb = u32(sm.v);
-#pragma unroll 1
+      const uint32_t x1b = u32(sm.x1);
+#pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t boff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
-        mma_f16(tm + T3, sdesc(dwb + kk * 2048, 2 * HT, 1024), sdesc(kb + boff, 16, 1024), id_m64, kk > 0);
-        mma_f16(tm + T4, sdesc(dub + kk * 2048, 2 * HT, 1024), sdesc(vb + (kk >> 2) * HT + (kk & 3) * 32, 16, 1024),
-                id_m64, kk > 0);
+        mma_f16s(tm + T3, sdesc_s(dwb, 2 * HT, 1024) + (kk * 2048), sdesc_s(kb, 16, 1024) + (boff), id_m64, kk > 0);
+        mma_f16s(tm + T4, sdesc_s(dub, 2 * HT, 1024) + (kk * 2048),
+                 sdesc_s(vb, 16, 1024) + ((kk >> 2) * HT + (kk & 3) * 32), id_m64, kk > 0);
       }
       mma_commit(u32(&sm.bar_mma));
-#pragma unroll 1
+#pragma unroll
       for (int kk = 0; kk < 4; ++kk)
-        mma_f16(tm + T7, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(pb + kk * 32, 16, 1024), id_mk, kk > 0);
+        mma_f16s(tm + T7, sdesc_s(kb, 2 * HT, 1024) + (kk * 2048), sdesc_s(pb, 16, 1024) + (kk * 32), id_mk, kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        mma_f16s(tm + T0, sdesc_s(kb, 2 * HT, 1024) + (HT + kk * 2048), sdesc_s(pb, HT, 1024) + (kk * 2048), id,
+                 kk > 0);
+        mma_f16s(tm + T0, sdesc_s(dwb, 16, 1024) + (kk * 32), sdesc_s(x1b, HT, 1024) + (kk * 2048), id_km, true);
+      }
     }
     __syncwarp();
-    if (__syncthreads_or(false)) break;  // B5
-    if (lane == 0 && nvalid == CH) store_tma(&tmdv, sm.dob, h, tok0);
     if (__syncthreads_or(false)) break;  // B6
-    // ---- P7: Y1 = Ahat^T dAhat -> T0 (M = 64);  then Ka's context-only part Q^T dPm + dW'^T X1 -> T3 (first read in
-    //      R9: the P8 commit covers it; M1 in T3 was read above).  Then the next item's dO (once the dv store has
-    //      read its staging) and its Ut^T, dUt^T (their last readers, P5 and P6, are done)
+    // ---- P7: Y1 = Ahat^T dAhat -> T3 (M = 64; M1, read in R6, is dead).  Then the dv tile (staged under P6), the
+    //      next item's dO once that store has read its staging, and the next item's Ut^T, dUt^T, dS (their last
+    //      readers, P5, P6 and Kb, are done)
     if (lane == 0) {
       fence_after();
-      const uint32_t id = idesc_f16(128, 64, true, true), id_y1 = idesc_f16(64, 64, true, true);
-      const uint32_t id_km = idesc_f16(128, 64, false, true);
+      const uint32_t id_y1 = idesc_f16(64, 64, true, true);
       const uint32_t ab = u32(sm.ah), dab = u32(sm.x2);
-      const uint32_t kb = u32(sm.kq), pb = u32(sm.p), dwb = u32(sm.s0), x1b = u32(sm.x1);
-#pragma unroll 1
+#pragma unroll
       for (int kk = 0; kk < 4; ++kk)
-        mma_f16(tm + T0, sdesc(ab + kk * 2048, HT, 1024), sdesc(dab + kk * 2048, HT, 1024), id_y1, kk > 0);
+        mma_f16s(tm + T3, sdesc_s(ab, HT, 1024) + (kk * 2048), sdesc_s(dab, HT, 1024) + (kk * 2048), id_y1, kk > 0);
       mma_commit(u32(&sm.bar_mma));
-#pragma unroll 1
-      for (int kk = 0; kk < 4; ++kk) {
-        mma_f16(tm + T3, sdesc(kb + HT + kk * 2048, 2 * HT, 1024), sdesc(pb + kk * 2048, HT, 1024), id, kk > 0);
-        mma_f16(tm + T3, sdesc(dwb + kk * 32, 16, 1024), sdesc(x1b + kk * 2048, HT, 1024), id_km, true);
-      }
+      if (nvalid == CH) store_tma(&tmdv, sm.dob, h, tok0);
       if (more) {
         tma_store_wait_read();
         issue_do(nitem, nxt.tok0);
@@ -913,33 +919,35 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
       par_b = par_a = npar;
     }
     if (__syncthreads_or(false)) break;  // B7
-    // ---- P8: dT = -Y1 Ahat^T -> T1 (M = 64); then the next item's X2 (dAhat, its last reader Y1, is done)
+    // ---- P8: dT = -Y1 Ahat^T -> T1 (M = 64); then the next item's X2, first half of S0, P, X1 (last read by Y1,
+    //      M1 and Ka's context part, which the P7 commit covered)
     if (lane == 0) {
       fence_after();
       const uint32_t id = idesc_f16(64, 64, false, false, true);
       const uint32_t yb = u32(sm.v), ab = u32(sm.ah);
-#pragma unroll 1
-      for (int kk = 0; kk < 4; ++kk) mma_f16(tm + T1, sdesc(yb + kk * 32, 16, 1024), sdesc(ab + kk * 32, 16, 1024), id, kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) mma_f16s(tm + T1, sdesc_s(yb, 16, 1024) + (kk * 32),
+                                              sdesc_s(ab, 16, 1024) + (kk * 32), id, kk > 0);
       mma_commit(u32(&sm.bar_mma));
       if (more) issue_a2(nitem);
     }
     __syncwarp();
     if (__syncthreads_or(false)) break;  // B8
-    if (lane == 0 && nvalid == CH) store_tma(&tmdq, sm.ds, h, tok0);
+    if (lane == 0 && nvalid == CH) store_tma(&tmdq, sm.s0 + 2 * HT, h, tok0);
     if (__syncthreads_or(false)) break;  // B9
-    // ---- P9: Ka += K^T (dN + dN^T) -> T3  (Ka's context-only part came with P7; Kb = dS^T Ut^T with P5, in T2);
-    //      then the rest of the next item's group A: S0, P, X1 (last read by Ka's context part, which the P8
-    //      commit covered), Ahat (P8), N (R8), dS once the dq store has read its staging
+    // ---- P9: Ka += K^T (dN + dN^T) -> T0  (Ka's context-only part came with P6; Kb = dS^T Ut^T with P5, in T2);
+    //      then the rest of the next item's group A: Ahat (P8), N (R8), the second half of S0 once the dq store
+    //      has read its staging there
     if (lane == 0) {
       fence_after();
       const uint32_t id_mm = idesc_f16(128, 64, true, true);
       const uint32_t id_mk = idesc_f16(128, 64, true, false);
       const uint32_t kb = u32(sm.kq), sgb = u32(sm.v + HT);
-#pragma unroll 1
+#pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         // the dN tile read once as MN-major (dN) and once as K-major (dN^T)
-        mma_f16(tm + T3, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(sgb + kk * 2048, HT, 1024), id_mm, true);
-        mma_f16(tm + T3, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(sgb + kk * 32, 16, 1024), id_mk, true);
+        mma_f16s(tm + T0, sdesc_s(kb, 2 * HT, 1024) + (kk * 2048), sdesc_s(sgb, HT, 1024) + (kk * 2048), id_mm, true);
+        mma_f16s(tm + T0, sdesc_s(kb, 2 * HT, 1024) + (kk * 2048), sdesc_s(sgb, 16, 1024) + (kk * 32), id_mk, true);
       }
       mma_commit(u32(&sm.bar_mma));
       if (more) {

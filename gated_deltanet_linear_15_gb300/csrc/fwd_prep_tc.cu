@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(PT, 2)
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t koff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
-        mma_f16(tm, sdesc(base + koff, 16, 1024), sdesc(base + koff, 16, 1024), idesc, kk > 0);
+        mma_f16s(tm, sdesc_s(base, 16, 1024) + (koff), sdesc_s(base, 16, 1024) + (koff), idesc, kk > 0);
       }
       mma_commit(u32(&sm.bar_mma));
     }

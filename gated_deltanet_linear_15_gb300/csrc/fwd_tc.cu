@@ -180,11 +180,11 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
     const uint32_t x1b = u32(st + R_X1 * HT), x2b = u32(st + R_X2 * HT);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
-      mma_f16(tm + TM_W, sdesc(kb + kk * 2048, 2 * HT, 1024), sdesc(x1b + kk * 32, 16, 1024), idesc, kk > 0);
+      mma_f16s(tm + TM_W, sdesc_s(kb, 2 * HT, 1024) + (kk * 2048), sdesc_s(x1b, 16, 1024) + (kk * 32), idesc, kk > 0);
     if (need_v) {
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
-        mma_f16(tm + TM_U, sdesc(vb + kk * 2048, HT, 1024), sdesc(x2b + kk * 32, 16, 1024), idesc, kk > 0);
+        mma_f16s(tm + TM_U, sdesc_s(vb, HT, 1024) + (kk * 2048), sdesc_s(x2b, 16, 1024) + (kk * 32), idesc, kk > 0);
     }
     mma_commit(u32(&sm.bar_mma2));
   };
@@ -278,8 +278,8 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
-          mma_f16(tm + TM_U, sdesc(s0b + aoff, 16, 1024), sdesc(wb + kk * 2048, 2 * HT, 1024), id_u,
-                  need_v || kk > 0);
+          mma_f16s(tm + TM_U, sdesc_s(s0b, 16, 1024) + (aoff), sdesc_s(wb, 2 * HT, 1024) + (kk * 2048), id_u,
+                   need_v || kk > 0);
         }
         mma_commit(u32(&sm.bar_mma));
         if (save_c) tma_store_wait_read();  // the W^T store has read wu (Ut^T is written next)
@@ -300,7 +300,7 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
-            mma_f16(tm + TM_O, sdesc(s0b + aoff, 16, 1024), sdesc(qb + aoff, 16, 1024), id_o, kk > 0);
+            mma_f16s(tm + TM_O, sdesc_s(s0b, 16, 1024) + (aoff), sdesc_s(qb, 16, 1024) + (aoff), id_o, kk > 0);
           }
         }
       }
@@ -321,11 +321,11 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
         const uint32_t id_o = idesc_f16(128, 64, false, false);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_f16(tm + TM_S, sdesc(ucb + kk * 32, 16, 1024), sdesc(kb + kk * 2048, 2 * HT, 1024), id_s, true);
+          mma_f16s(tm + TM_S, sdesc_s(ucb, 16, 1024) + (kk * 32), sdesc_s(kb, 2 * HT, 1024) + (kk * 2048), id_s, true);
         if (emit_o) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_f16(tm + TM_OA, sdesc(ub + kk * 32, 16, 1024), sdesc(pb + kk * 32, 16, 1024), id_o, kk > 0);
+            mma_f16s(tm + TM_OA, sdesc_s(ub, 16, 1024) + (kk * 32), sdesc_s(pb, 16, 1024) + (kk * 32), id_o, kk > 0);
         }
         mma_commit(u32(&sm.bar_mma));
         if (save_c && emit_o) tma_store_wait_read();  // the Ut^T store has read wu (the O staging)

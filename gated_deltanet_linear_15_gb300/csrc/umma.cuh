@@ -67,16 +67,29 @@ __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::aft
 // generic-proxy shared-memory writes -> visible to the async proxy (MMA, TMA)
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                        bool accumulate) {
+// A shared-memory operand descriptor as its two 32-bit words.  The start address (>> 4) is the low 14 bits of
+// `lo` and every address of the CTA's shared memory window is below 256 KB, so moving the start by a byte
+// offset (a K step, another tile) is one add to `lo`: built once, stepped in the issue loops.
+struct SDesc {
+  uint32_t lo, hi;
+};
+__device__ __forceinline__ SDesc sdesc_s(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  const uint64_t d = sdesc(saddr, lbo_bytes, sbo_bytes);
+  return SDesc{(uint32_t)d, (uint32_t)(d >> 32)};
+}
+__device__ __forceinline__ SDesc operator+(SDesc d, uint32_t bytes) { return SDesc{d.lo + (bytes >> 4), d.hi}; }
+// D[tmem] (+)= A * B with descriptors in that form (accumulate: 0 overwrites D)
+__device__ __forceinline__ void mma_f16s(uint32_t d_tmem, SDesc a, SDesc b, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n"
+      ".reg .b64 da, db;\n"
       ".reg .pred p;\n"
-      "setp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      "mov.b64 da, {%1, %2};\n"
+      "mov.b64 db, {%3, %4};\n"
+      "setp.ne.b32 p, %6, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n"
       "}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate));
+      "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate));
 }
 // arrive on an mbarrier once all previously issued MMAs of this thread completed
 __device__ __forceinline__ void mma_commit(uint32_t mbar) {
