@@ -53,18 +53,19 @@ struct __align__(1024) LocalTcSmem {
   uint8_t p[HT];        // P, then dPm (in place)
   uint8_t x1[HT];
   uint8_t x2[HT];       // X2, later dAhat
-  uint8_t ah[HT];       // Ahat (fp16)
+  uint8_t ah[HT];       // Ahat (fp16); with n16, the dq staging once both are read
+  uint8_t n16[HT];      // N = K K^T (fp16, [r][i], context tile)
   uint8_t wt[2 * HT];   // dUt^T [d_v][token] (the reverse chain's tile)
   uint8_t ut[2 * HT];   // Ut^T [d_v][token] (context tile)
-  uint8_t n16[HT];      // N = K K^T (fp16, [r][i], context tile)
   float g[2][CH], beta[2][CH];  // per item parity: the next item's gates are prepared during this one
   float nk[CH], nq[CH];         // reciprocal norms 1/|k|, 1/|q| (context, one bulk copy)
   Gates gt[2];
   float part[24][CH];   // per-token partial sums (reused per round)
   float acc[9][CH];     // assembled per-token terms
   float red[LWARPS];
-  uint64_t bar_a, bar_b, bar_w, bar_mma;  // TMA: {Ut^T, dUt^T, X2, S0, dS, P, N, X1, Ahat}, {dO}, {K, Q, norms, V};
-                                          // tensor cores
+  int nxt_info[3];       // the next item and its first token and valid rows (the producer's plan look-ups)
+  uint64_t bar_a, bar_b, bar_w, bar_c, bar_mma;  // TMA: {Ut^T, dUt^T, dS, X2, S0, P, X1}, {dO}, {K, Q, norms,
+                                                 // V}, {Ahat, N}; tensor cores
   uint32_t tmem_base;
 };
 
@@ -189,6 +190,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     mbar_init(u32(&sm.bar_a), 1);
     mbar_init(u32(&sm.bar_b), 1);
     mbar_init(u32(&sm.bar_w), 1);
+    mbar_init(u32(&sm.bar_c), 1);
     mbar_init(u32(&sm.bar_mma), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     for (const CUtensorMap *m : {&tm3, &tmdo, &tms0, &tmds, &tmw, &tmdq, &tmdk, &tmdv, &tmu, &tmdu}) tma_prefetch_desc(m);
@@ -246,42 +248,41 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     }
     return r;
   };
-  // The tiles of an item (item = chunk * H + head) arrive in three groups, each on its own mbarrier, each
+  // The tiles of an item (item = chunk * H + head) arrive in four groups, each on its own mbarrier, each
   // part issued as soon as the previous item's last reader of its buffers is done:
-  //  A (bar_a, read from P5 on): Ut^T, the chain's dUt^T and dS after that item's P6 (and Kb); X2, the first
-  //    half of S0, P, X1 after its P7 (which covers Ka's context part); the second half of S0 (its dq
-  //    staging) after its dq store, Ahat and N after its P8 and R8;
+  //  A (bar_a, read from P5 on): Ut^T, the chain's dUt^T and dS after that item's P6 (and Kb); X2, S0, P,
+  //    X1 after its P7 (which covers Ka's context part);
   //  B (bar_b): dO, after that item's dv store;
   //  W (bar_w, read from P6 on): the K, Q operand tiles and the reciprocal norms after its dk read-out, V
-  //    after its dk store (dk is staged in V's buffer).
-  // The early parts of a group only raise the bytes its barrier expects; the last part arrives, so a phase
+  //    after its dk store (dk is staged in V's buffer);
+  //  C (bar_c, read from R6 on): Ahat and N after its dq store (dq is staged in their buffers).
+  // The early part of a group only raises the bytes its barrier expects; the last part arrives, so a phase
   // completes once every part has been issued and has landed.
-  auto issue_a1 = [&](int item, bool arrive) {  // Ut^T, dUt^T, dS
+  auto issue_a1 = [&](int item) {  // Ut^T, dUt^T, dS
     const uint32_t bar = u32(&sm.bar_a);
     const int srow = item * D;
-    if (arrive) mbar_expect_tx(bar, 8 * HT);
-    else mbar_expect_tx_only(bar, 8 * HT);
+    mbar_expect_tx_only(bar, 8 * HT);
     tma_load_3d(u32(sm.ut), &tmu, 0, (item * T128_TILES + T128_U) * D, 0, bar);
     tma_load_3d(u32(sm.wt), &tmdu, 0, item * D, 0, bar);
     tma_load_3d(u32(sm.ds), &tmds, 0, srow, 0, bar);
     tma_load_3d(u32(sm.ds + 2 * HT), &tmds, 64, srow, 0, bar);
   };
-  auto issue_a2 = [&](int item) {  // X2, S0 (first feature block), P, X1
+  auto issue_a2 = [&](int item) {  // X2, S0, P, X1; the group's arrival
     const uint32_t bar = u32(&sm.bar_a);
     const int row = item * T64_TILES * CH;
-    mbar_expect_tx_only(bar, 5 * HT);
+    mbar_expect_tx(bar, 7 * HT);
     tma_load_3d(u32(sm.x2), &tmw, 0, row + T64_X2 * CH, 0, bar);
     tma_load_3d(u32(sm.s0), &tms0, 0, item * D, 0, bar);
+    tma_load_3d(u32(sm.s0 + 2 * HT), &tms0, 64, item * D, 0, bar);
     tma_load_3d(u32(sm.p), &tmw, 0, row + T64_P * CH, 0, bar);
     tma_load_3d(u32(sm.x1), &tmw, 0, row + T64_X1 * CH, 0, bar);
   };
-  auto issue_a3 = [&](int item) {  // S0 (second feature block), N, Ahat; the group's arrival
-    const uint32_t bar = u32(&sm.bar_a);
+  auto issue_c = [&](int item) {  // Ahat, N
+    const uint32_t bar = u32(&sm.bar_c);
     const int row = item * T64_TILES * CH;
-    mbar_expect_tx(bar, 4 * HT);
-    tma_load_3d(u32(sm.s0 + 2 * HT), &tms0, 64, item * D, 0, bar);
-    tma_load_3d(u32(sm.n16), &tmw, 0, row + T64_N * CH, 0, bar);
+    mbar_expect_tx(bar, 2 * HT);
     tma_load_3d(u32(sm.ah), &tmw, 0, row + T64_AH * CH, 0, bar);
+    tma_load_3d(u32(sm.n16), &tmw, 0, row + T64_N * CH, 0, bar);
   };
   auto issue_do = [&](int item, int t0) {
     const int hh = item % H;
@@ -310,9 +311,9 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
   };
   ItemInfo cur = info_of(next_valid(blockIdx.x));
   if (tid == PRODUCER && cur.item < n_items) {
-    issue_a1(cur.item, false);
+    issue_a1(cur.item);
     issue_a2(cur.item);
-    issue_a3(cur.item);
+    issue_c(cur.item);
     issue_do(cur.item, cur.tok0);
     issue_w1(cur.item);
     issue_w2(cur.item);
@@ -322,8 +323,6 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
   uint32_t it = 0;  // parity of the TMA barriers: one completion per item
   if (warp < LWARPS) {
   for (; cur.item < n_items; ++it) {
-  const ItemInfo nxt = info_of(next_valid(cur.item + gridDim.x));  // consumed late in this item
-  const int nitem = nxt.item;
   const int item = cur.item, h = item % H, tok0 = cur.tok0, nvalid = cur.nvalid;
   const int gbuf = it & 1;
   Gates &G = sm.gt[gbuf];
@@ -366,6 +365,9 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     failed = true;
     break;
   }
+  // the next item, looked up by the producer before B2 (dependent global loads the workers do not wait for)
+  const ItemInfo nxt{sm.nxt_info[0], sm.nxt_info[1], sm.nxt_info[2]};
+  const int nitem = nxt.item;
   if (nitem < n_items && tid < 128) {  // the next item's g or beta, stored under P7 (its plan lookups have landed by now)
     const int r = tid & 63, nh = nitem % H;
     if (r < nxt.nvalid)
@@ -503,9 +505,12 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     }
     store_rows(a.dv, sm.dob, h, tok0, nvalid);
   }
-  if (wbar_or(!mma_done())) {  // P6
-    failed = release = true;
-    break;
+  {  // P6, and Ahat and N of this item (loaded at the end of the previous one)
+    const bool ok = mma_done() && mbar_wait(u32(&sm.bar_c), it & 1, err, 8);
+    if (wbar_or(!ok)) {
+      failed = release = true;
+      break;
+    }
   }
   if (tid < 64) sm.acc[5][tid] = sm.part[20][tid] + sm.part[21][tid] + sm.part[22][tid] + sm.part[23][tid];
   {
@@ -621,52 +626,6 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     failed = true;
     break;
   }
-  {  // under P8: dq raw = (scale dq^ - q^ (q^ . dq^) / scale) / |q|   (or scale dq^ without normalisation),
-     // staged in the second half of S0's buffer (S0 is dead after P5; dW'^T fills the first half)
-    const float rscale = 1.f / a.scale;
-    float gm[4], dt[4], nqv[4];
-    tok4(G.gam, ta, gm);
-    if (l2) {  // q^ . dq^ = gam <Qa, q^> + sum_s dP * P (the Qb part: row sums of dP * P)
-      float p1[4];
-      tok4(sm.acc[5], ta, dt);
-      tok4(sm.acc[2], ta, p1);
-      tok4(sm.nq, ta, nqv);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) dt[k] = (dt[k] + p1[k]) * rscale;
-    }
-#pragma unroll 1
-    for (int ls = 0; ls < 32; ls += 16) {
-      const uint32_t tq = tm + tl + ((uint32_t)ls << 16) + c0;
-      float qa[8], qb[8];
-      tmem_ld_frag2(tq + T5, qa, tq + T7, qb);
-      uint32_t qf[4], pk[4];
-      if (l2) ldmatrix_x4_trans(frag_addr(sm.kq + HT, 2 * HT, wq, ls, c0, lane), qf);
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        float o[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int i = 2 * m + e, k = (m >> 1) * 2 + e;
-          const float dq = qb[i] + gm[k] * qa[i];
-          if (l2) {
-            const float2 q2 = unpack_f16(qf[m]);
-            o[e] = (a.scale * dq - (e ? q2.y : q2.x) * dt[k]) * nqv[k];
-          } else {
-            o[e] = a.scale * dq;
-          }
-        }
-        pk[m] = pack_bf16(o[0], o[1]);
-      }
-      stmatrix_x4_trans(frag_addr(sm.s0 + 2 * HT, HT, wq, ls, c0, lane), pk);
-    }
-  }
-  fence_before();
-  fence_async_smem();
-  if (__syncthreads_or(false)) {  // B8: the producer stores a full dq tile
-    failed = true;
-    break;
-  }
-  if (nvalid < CH) store_rows(a.dq, sm.s0 + 2 * HT, h, tok0, nvalid);
   if (wbar_or(!mma_done())) {  // P8
     failed = release = true;
     break;
@@ -707,7 +666,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
   }
   fence_before();
   fence_async_smem();
-  if (__syncthreads_or(false)) {  // B9: the producer issues P9, then the next item's main tiles once P9 is done
+  if (__syncthreads_or(false)) {  // B9: the producer issues P9
     failed = true;
     break;
   }
@@ -762,6 +721,47 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
       }
     }
   }
+  {  // under P9: dq raw = (scale dq^ - q^ (q^ . dq^) / scale) / |q|   (or scale dq^ without normalisation),
+     // staged in the Ahat and N buffers (their last readers, P8 and R8, are done)
+    const float rscale = 1.f / a.scale;
+    float gm[4], dt[4], nqv[4];
+    tok4(G.gam, ta, gm);
+    if (l2) {  // q^ . dq^ = gam <Qa, q^> + sum_s dP * P (the Qb part: row sums of dP * P)
+      float p1[4];
+      tok4(sm.acc[5], ta, dt);
+      tok4(sm.acc[2], ta, p1);
+      tok4(sm.nq, ta, nqv);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) dt[k] = (dt[k] + p1[k]) * rscale;
+    }
+#pragma unroll 1
+    for (int ls = 0; ls < 32; ls += 16) {
+      const uint32_t tq = tm + tl + ((uint32_t)ls << 16) + c0;
+      float qa[8], qb[8];
+      tmem_ld_frag2(tq + T5, qa, tq + T7, qb);
+      uint32_t qf[4], pk[4];
+      if (l2) ldmatrix_x4_trans(frag_addr(sm.kq + HT, 2 * HT, wq, ls, c0, lane), qf);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        float o[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int i = 2 * m + e, k = (m >> 1) * 2 + e;
+          const float dq = qb[i] + gm[k] * qa[i];
+          if (l2) {
+            const float2 q2 = unpack_f16(qf[m]);
+            o[e] = (a.scale * dq - (e ? q2.y : q2.x) * dt[k]) * nqv[k];
+          } else {
+            o[e] = a.scale * dq;
+          }
+        }
+        pk[m] = pack_bf16(o[0], o[1]);
+      }
+      stmatrix_x4_trans(frag_addr(sm.ah, HT, wq, ls, c0, lane), pk);
+    }
+  }
+  fence_before();
+  fence_async_smem();  // the producer stores a full dq tile at B10
   if (wbar_or(!mma_done())) {  // P9
     failed = release = true;
     break;
@@ -800,13 +800,14 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
   }
   fence_before();
   fence_async_smem();
-  if (__syncthreads_or(false)) {  // B10: the producer stores a full dk tile
+  if (__syncthreads_or(false)) {  // B10: the producer stores full dq and dk tiles
     failed = true;
     break;
   }
   if (nvalid < CH) {
+    store_rows(a.dq, sm.ah, h, tok0, nvalid);
     store_rows(a.dk, sm.v, h, tok0, nvalid);
-    if (__syncthreads_or(false)) {  // B11: the dk staging is read, the producer may load the next V
+    if (__syncthreads_or(false)) {  // B11: the dq and dk staging are read, the producer may load the next V, Ahat, N
       failed = true;
       break;
     }
@@ -818,12 +819,19 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
   // ---------------- producer warp 16 (lane 0): every tensor-core product, TMA load and TMA store
   // Loads in flight that the workers have not waited for (pend_*), groups partly issued whose barrier still
   // lacks its arrival (open_*), and the parity of the phase each refers to.
-  bool pend_a = cur.item < n_items, pend_b = pend_a, pend_w = pend_a, open_a = false, open_w = false;
-  uint32_t par_a = 0, par_b = 0, par_w = 0;
+  bool pend_a = cur.item < n_items, pend_b = pend_a, pend_w = pend_a, pend_c = pend_a, open_a = false,
+       open_w = false;
+  uint32_t par_a = 0, par_b = 0, par_w = 0, par_c = 0;
+  // plan look-ups one item ahead: dependent global loads, done while the producer waits at B10
+  ItemInfo nxt = info_of(next_valid(cur.item + gridDim.x));
   for (; cur.item < n_items; ++it) {
-    const ItemInfo nxt = info_of(next_valid(cur.item + gridDim.x));
     const int nitem = nxt.item;
     const bool more = nitem < n_items;
+    if (lane == 0) {  // for the workers, who read it after B2
+      sm.nxt_info[0] = nxt.item;
+      sm.nxt_info[1] = nxt.tok0;
+      sm.nxt_info[2] = nxt.nvalid;
+    }
     const uint32_t npar = (it + 1) & 1;  // phase parity of the next item's loads
     const int item = cur.item, h = item % H, tok0 = cur.tok0, nvalid = cur.nvalid;
     {
@@ -894,7 +902,11 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
       }
     }
     __syncwarp();
-    if (__syncthreads_or(false)) break;  // B6
+    {
+      const bool f = __syncthreads_or(false);  // B6 (the workers waited for Ahat and N)
+      pend_c = false;
+      if (f) break;
+    }
     // ---- P7: Y1 = Ahat^T dAhat -> T3 (M = 64; M1, read in R6, is dead).  Then the dv tile (staged under P6), the
     //      next item's dO once that store has read its staging, and the next item's Ut^T, dUt^T, dS (their last
     //      readers, P5, P6 and Kb, are done)
@@ -910,7 +922,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
       if (more) {
         tma_store_wait_read();
         issue_do(nitem, nxt.tok0);
-        issue_a1(nitem, false);
+        issue_a1(nitem);
       }
     }
     __syncwarp();
@@ -919,8 +931,8 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
       par_b = par_a = npar;
     }
     if (__syncthreads_or(false)) break;  // B7
-    // ---- P8: dT = -Y1 Ahat^T -> T1 (M = 64); then the next item's X2, first half of S0, P, X1 (last read by Y1,
-    //      M1 and Ka's context part, which the P7 commit covered)
+    // ---- P8: dT = -Y1 Ahat^T -> T1 (M = 64); then the rest of the next item's group A: X2, S0, P, X1 (last read
+    //      by Y1, P5, M1 and Ka's context part, which the P7 commit covered)
     if (lane == 0) {
       fence_after();
       const uint32_t id = idesc_f16(64, 64, false, false, true);
@@ -932,12 +944,12 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
       if (more) issue_a2(nitem);
     }
     __syncwarp();
-    if (__syncthreads_or(false)) break;  // B8
-    if (lane == 0 && nvalid == CH) store_tma(&tmdq, sm.s0 + 2 * HT, h, tok0);
+    if (more) {
+      open_a = false;
+      pend_a = true;
+    }
     if (__syncthreads_or(false)) break;  // B9
-    // ---- P9: Ka += K^T (dN + dN^T) -> T0  (Ka's context-only part came with P6; Kb = dS^T Ut^T with P5, in T2);
-    //      then the rest of the next item's group A: Ahat (P8), N (R8), the second half of S0 once the dq store
-    //      has read its staging there
+    // ---- P9: Ka += K^T (dN + dN^T) -> T0  (Ka's context-only part came with P6; Kb = dS^T Ut^T with P5, in T2)
     if (lane == 0) {
       fence_after();
       const uint32_t id_mm = idesc_f16(128, 64, true, true);
@@ -950,21 +962,17 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
         mma_f16s(tm + T0, sdesc_s(kb, 2 * HT, 1024) + (kk * 2048), sdesc_s(sgb, 16, 1024) + (kk * 32), id_mk, true);
       }
       mma_commit(u32(&sm.bar_mma));
-      if (more) {
-        tma_store_wait_read();
-        issue_a3(nitem);
-      }
     }
     __syncwarp();
-    if (more) {
-      open_a = false;
-      pend_a = true;
-    }
+    const ItemInfo nn = info_of(next_valid(nitem + gridDim.x));  // the item after the next one
     if (__syncthreads_or(false)) break;  // B10
-    // dk (staged in V's buffer); the next item's K, Q and norms (R9 has read them), then its V once the dk
-    // staging is read
+    // dq (staged in the Ahat and N buffers) and dk (in V's buffer); the next item's K, Q and norms (R9 has read
+    // them), then its V, Ahat and N once the staging is read
     if (lane == 0) {
-      if (nvalid == CH) store_tma(&tmdk, sm.v, h, tok0);
+      if (nvalid == CH) {
+        store_tma(&tmdq, sm.ah, h, tok0);
+        store_tma(&tmdk, sm.v, h, tok0);
+      }
       if (more) issue_w1(nitem);
     }
     __syncwarp();
@@ -976,13 +984,16 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     if (lane == 0 && more) {
       tma_store_wait_read();
       issue_w2(nitem);
+      issue_c(nitem);
     }
     __syncwarp();
     if (more) {
       open_w = false;
-      pend_w = true;
+      pend_w = pend_c = true;
+      par_c = npar;
     }
     cur = nxt;
+    nxt = nn;
   }
   failed = cur.item < n_items;
   if (lane == 0) {
@@ -992,6 +1003,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
       if (pend_a || open_a) mbar_wait(u32(&sm.bar_a), par_a, err, 8);
       if (pend_b) mbar_wait(u32(&sm.bar_b), par_b, err, 8);
       if (pend_w || open_w) mbar_wait(u32(&sm.bar_w), par_w, err, 8);
+      if (pend_c) mbar_wait(u32(&sm.bar_c), par_c, err, 8);
     }
     tma_store_wait_all();  // output tiles written before the CTA leaves
   }
