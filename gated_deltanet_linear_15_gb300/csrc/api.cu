@@ -59,7 +59,7 @@ struct Layout {
   size_t off_E = 0, off_M = 0, off_S = 0;     // forward fix-up buffers
   size_t off_states = 0, off_dstates = 0;   // backward per-chunk states
   size_t off_F = 0, off_R = 0, off_dS = 0;  // reverse fix-up buffers
-  size_t off_dut = 0, dut_bytes = 0;        // the chain's per-chunk dUt^T tiles (bf16, d = 128)
+  size_t off_dut = 0, dut_bytes = 0;        // the chain's per-chunk dUt^T and fp16 dO tiles (bf16, d = 128)
   size_t off_t64 = 0, off_t128 = 0;        // recomputed chunk context tiles (bf16, d = 128)
   size_t t64_bytes = 0, t128_bytes = 0;
   size_t off_tqkv = 0, off_nrm = 0, tqkv_bytes = 0, nrm_bytes = 0;
@@ -257,7 +257,7 @@ int make_layout(const gdn_shape *s, Layout &L) {
   off += spbuf;
   L.off_dS = off;
   off += spbuf;
-  L.dut_bytes = tiles ? align256((size_t)L.CH_max * L.H * 128 * CH * 2) : 0;
+  L.dut_bytes = tiles ? align256((size_t)L.CH_max * L.H * TC_TILES * 128 * CH * 2) : 0;
   L.off_dut = off;
   off += L.dut_bytes;
   L.bwd_saved_total = off;
@@ -494,9 +494,10 @@ int t128_map(CUtensorMap *m, const Layout &L, const void *ptr) {
 int tqkv_map(CUtensorMap *m, const Layout &L, const void *ptr) {
   return tile_map(m, ptr, (long)L.CH_max * L.H * TQ_TILES * CH, 64, 128);
 }
-// the reverse chain's dUt^T tiles, [chunks, H, 128 (d_v), 64 (tokens)], one 128-row box per (chunk, head)
+// the reverse chain's tiles, [chunks, H, TC_TILES, 128, 64]: dUt^T (rows d_v, columns token) and the fp16 dO
+// (rows 0-63: tokens x features 0-63, rows 64-127: features 64-127), one 128-row box each
 int dut_map(CUtensorMap *m, const Layout &L, const void *ptr) {
-  return tile_map(m, ptr, (long)L.CH_max * L.H * 128, 128);
+  return tile_map(m, ptr, (long)L.CH_max * L.H * TC_TILES * 128, 128);
 }
 
 // The chunk forward kernel for this problem: tcgen05 for bf16 with d = 128 (its recurrent half, on the
@@ -774,13 +775,13 @@ int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
   {
     PROF("bwd_local");
     if (bf && L.D == 128 && L.Ttot > 0) {
-      CUtensorMap maps[10];
-      if ((rc = tqkv_map(&maps[0], L, tqkv)) || (rc = qkv_map(&maps[1], dO, L.Ttot, L.H)) ||
+      CUtensorMap maps[9];
+      if ((rc = tqkv_map(&maps[0], L, tqkv)) || (rc = dut_map(&maps[1], L, ws + L.off_dut)) ||
           (rc = state_map(&maps[2], states, (long)L.CH_max * L.H * 128)) ||
           (rc = state_map(&maps[3], ws + L.off_dstates, (long)L.CH_max * L.H * 128)) ||
           (rc = t64_map(&maps[4], L, t64)) || (rc = qkv_map(&maps[5], dq, L.Ttot, L.H)) ||
           (rc = qkv_map(&maps[6], dk, L.Ttot, L.H)) || (rc = qkv_map(&maps[7], dv, L.Ttot, L.H)) ||
-          (rc = t128_map(&maps[8], L, t128)) || (rc = dut_map(&maps[9], L, ws + L.off_dut)))
+          (rc = t128_map(&maps[8], L, t128)))
         return rc;
       CK(launch_bwd_local_tc(ba, maps, L.CH_max, st));
     } else {

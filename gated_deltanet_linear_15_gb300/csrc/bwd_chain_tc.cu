@@ -215,10 +215,11 @@ __device__ __forceinline__ void chain_tc_item(const BwdArgs &a, const CUtensorMa
       }
       if (lane == 0) {
         fence_after();
-        if (store && c < cend) {  // the fp16 dS at the end of chunk c, for the local-gradient kernel
+        if (store && c < cend) {  // the fp16 dS at the end of chunk c and its fp16 dO, for the local-gradient kernel
           const int srow = ((chunk0 + c) * H + h) * D;
           tma_store_3d(&tmds, 0, srow, 0, u32(sm.ds16));
           tma_store_3d(&tmds, 64, srow, 0, u32(sm.ds16 + 2 * HT));
+          tma_store_3d(&tmdu, 0, (((chunk0 + c) * H + h) * TC_TILES + TC_DO) * D, 0, u32(st + 4 * HT));
           tma_store_commit();
         }
         const uint32_t id_kk = idesc_f16(128, 64, false, false);
@@ -256,7 +257,8 @@ __device__ __forceinline__ void chain_tc_item(const BwdArgs &a, const CUtensorMa
           mma_f16s(tm + TM_S, sdesc_s(dub, 16, 1024) + (kk * 32), sdesc_s(wb, 16, 1024) + (kk * 32), id_kk_neg, true);
         mma_commit(u32(&sm.bar_mma));
         if (store && c < cend) {  // dUt^T of chunk c for the local-gradient kernel (read before the next
-          tma_store_3d(&tmdu, 0, ((chunk0 + c) * H + h) * D, 0, dub);  // chunk's read-out rewrites kc)
+                                  // chunk's read-out rewrites kc)
+          tma_store_3d(&tmdu, 0, (((chunk0 + c) * H + h) * TC_TILES + TC_DUT) * D, 0, dub);
           tma_store_commit();
         }
       }

@@ -47,7 +47,7 @@ constexpr uint32_t T0 = 0, T1 = 64, T2 = 128, T3 = 192, T4 = 256, T5 = 320, T6 =
 struct __align__(1024) LocalTcSmem {
   uint8_t kq[4 * HT];   // [K0 | Q0 | K1 | Q1] half-tiles (feature blocks 0/1), rows = token
   uint8_t v[2 * HT];    // V, later Y1 (first half) and dN (second half), then the dk staging
-  uint8_t dob[2 * HT];  // dO, later output staging (bf16 [token][128])
+  uint8_t dob[2 * HT];  // dO (fp16 operand form, from the chain), later the dv staging (bf16 [token][128])
   uint8_t s0[4 * HT];   // S0 [k-block][128 rows = d_v][64], later dW'^T [d_k][token]
   uint8_t ds[4 * HT];   // dS, same layout
   uint8_t p[HT];        // P, then dPm (in place)
@@ -160,12 +160,11 @@ __device__ __forceinline__ void tok4(const float *p, int ta, float (&v)[4]) {
 }  // namespace
 
 __global__ void __launch_bounds__(LNTHREADS, 1)
-    bwd_local_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tm3, const __grid_constant__ CUtensorMap tmdo,
+    bwd_local_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tm3, const __grid_constant__ CUtensorMap tmtc,
                         const __grid_constant__ CUtensorMap tms0, const __grid_constant__ CUtensorMap tmds,
                         const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmdq,
                         const __grid_constant__ CUtensorMap tmdk, const __grid_constant__ CUtensorMap tmdv,
-                        const __grid_constant__ CUtensorMap tmu, const __grid_constant__ CUtensorMap tmdu,
-                        int n_items) {
+                        const __grid_constant__ CUtensorMap tmu, int n_items) {
   extern __shared__ unsigned char smraw[];
   LocalTcSmem &sm =
       *reinterpret_cast<LocalTcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
@@ -193,7 +192,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     mbar_init(u32(&sm.bar_c), 1);
     mbar_init(u32(&sm.bar_mma), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    for (const CUtensorMap *m : {&tm3, &tmdo, &tms0, &tmds, &tmw, &tmdq, &tmdk, &tmdv, &tmu, &tmdu}) tma_prefetch_desc(m);
+    for (const CUtensorMap *m : {&tm3, &tmtc, &tms0, &tmds, &tmw, &tmdq, &tmdk, &tmdv, &tmu}) tma_prefetch_desc(m);
   }
   if (warp == 0) {
     tmem_alloc(u32(&sm.tmem_base), 512);
@@ -252,7 +251,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
   // part issued as soon as the previous item's last reader of its buffers is done:
   //  A (bar_a, read from P5 on): Ut^T, the chain's dUt^T and dS after that item's P6 (and Kb); X2, S0, P,
   //    X1 after its P7 (which covers Ka's context part);
-  //  B (bar_b): dO, after that item's dv store;
+  //  B (bar_b): dO (fp16, from the chain), after that item's dv store;
   //  W (bar_w, read from P6 on): the K, Q operand tiles and the reciprocal norms after its dk read-out, V
   //    after its dk store (dk is staged in V's buffer);
   //  C (bar_c, read from R6 on): Ahat and N after its dq store (dq is staged in their buffers).
@@ -263,7 +262,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     const int srow = item * D;
     mbar_expect_tx_only(bar, 8 * HT);
     tma_load_3d(u32(sm.ut), &tmu, 0, (item * T128_TILES + T128_U) * D, 0, bar);
-    tma_load_3d(u32(sm.wt), &tmdu, 0, item * D, 0, bar);
+    tma_load_3d(u32(sm.wt), &tmtc, 0, (item * TC_TILES + TC_DUT) * D, 0, bar);
     tma_load_3d(u32(sm.ds), &tmds, 0, srow, 0, bar);
     tma_load_3d(u32(sm.ds + 2 * HT), &tmds, 64, srow, 0, bar);
   };
@@ -284,12 +283,10 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     tma_load_3d(u32(sm.ah), &tmw, 0, row + T64_AH * CH, 0, bar);
     tma_load_3d(u32(sm.n16), &tmw, 0, row + T64_N * CH, 0, bar);
   };
-  auto issue_do = [&](int item, int t0) {
-    const int hh = item % H;
+  auto issue_do = [&](int item) {  // dO in its fp16 operand form (the chain converted it), both feature halves
     const uint32_t bar = u32(&sm.bar_b);
     mbar_expect_tx(bar, 2 * HT);
-    tma_load_3d(u32(sm.dob), &tmdo, 0, hh, t0, bar);
-    tma_load_3d(u32(sm.dob + HT), &tmdo, 64, hh, t0, bar);
+    tma_load_3d(u32(sm.dob), &tmtc, 0, (item * TC_TILES + TC_DO) * D, 0, bar);
   };
   auto issue_w1 = [&](int item) {  // K, Q operand tiles, reciprocal norms
     const int qrow = item * TQ_TILES * CH;
@@ -314,7 +311,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     issue_a1(cur.item);
     issue_a2(cur.item);
     issue_c(cur.item);
-    issue_do(cur.item, cur.tok0);
+    issue_do(cur.item);
     issue_w1(cur.item);
     issue_w2(cur.item);
   }
@@ -340,27 +337,6 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     }
   }
   if (it == 0 && warp == 0) gate_prefix(sm.g[0], sm.gt[0]);
-  // ---- prep: dO bf16 -> fp16 in place, rows >= nvalid zero (K, Q, V arrive as operand tiles, with
-  //      their norms, from the forward's context); thread t takes 2 of the 16 chunks of dO row t / 8
-  {
-    const int r = tid >> 3, part = tid & 7;
-    uint8_t *rowp = sm.dob + (part >> 2) * HT + r * 128;
-    const float mul = r < nvalid ? 1.f : 0.f;
-#pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-      const int off = (((part & 3) * 2 + cc) ^ (r & 7)) * 16;
-      uint4 q4 = *reinterpret_cast<const uint4 *>(rowp + off);
-      uint32_t *w = reinterpret_cast<uint32_t *>(&q4);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const __half2 a2 =
-            __floats2half2_rn(__uint_as_float(w[i] << 16) * mul, __uint_as_float(w[i] & 0xffff0000u) * mul);
-        w[i] = *reinterpret_cast<const uint32_t *>(&a2);
-      }
-      *reinterpret_cast<uint4 *>(rowp + off) = q4;
-    }
-  }
-  fence_async_smem();
   if (__syncthreads_or(false)) {  // B2: the producer issues P5
     failed = true;
     break;
@@ -824,6 +800,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
   uint32_t par_a = 0, par_b = 0, par_w = 0, par_c = 0;
   // plan look-ups one item ahead: dependent global loads, done while the producer waits at B10
   ItemInfo nxt = info_of(next_valid(cur.item + gridDim.x));
+  bool deferred = false;  // this item's V, Ahat and N wait for the previous item's output stores: issued after B2
   for (; cur.item < n_items; ++it) {
     const int nitem = nxt.item;
     const bool more = nitem < n_items;
@@ -839,9 +816,11 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
       pend_a = pend_b = false;  // the workers waited for both (a failed wait is not repeated)
       if (f) break;
     }
+
     // ---- P5: dP = dO Ut^T -> T0 (M = 64); dW'^T = -S0^T dUt^T -> T1; dV^T = dUt^T X2 -> T6; Qa = S0^T dO^T -> T5
-    //      (all before the commit: R5 overwrites S0 with dW'^T); then Kb = dS^T Ut^T -> T2 (first read under P7:
-    //      the P6 commit covers it)
+    //      (all before the commit: R5 overwrites S0 with dW'^T); then this item's V, Ahat, N once the previous item's
+    //      dq and dk stores have read their staging, and Kb = dS^T Ut^T -> T2 (first read under P7: the P6 commit
+    //      covers it)
     if (lane == 0) {
       fence_after();
       const uint32_t id_kmn = idesc_f16(128, 64, false, true), id_dp = idesc_f16(64, 64, false, true);
@@ -862,6 +841,11 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
         mma_f16s(tm + T5, sdesc_s(sb, 2 * HT, 1024) + (kk * 2048),
                  sdesc_s(dob, 16, 1024) + ((kk >> 2) * HT + (kk & 3) * 32), id_mk, kk > 0);
       mma_commit(u32(&sm.bar_mma));
+      if (deferred) {
+        tma_store_wait_read();
+        issue_w2(item);
+        issue_c(item);
+      }
       const uint32_t id_mm = idesc_f16(128, 64, true, true), dsb = u32(sm.ds);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
@@ -869,6 +853,12 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
                  kk > 0);
     }
     __syncwarp();
+    if (deferred) {
+      open_w = false;
+      pend_w = pend_c = true;
+      par_c = it & 1;
+      deferred = false;
+    }
     {
       const bool f = __syncthreads_or(false);  // B4 (the workers waited for K, Q, V)
       pend_w = false;
@@ -921,7 +911,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
       if (nvalid == CH) store_tma(&tmdv, sm.dob, h, tok0);
       if (more) {
         tma_store_wait_read();
-        issue_do(nitem, nxt.tok0);
+        issue_do(nitem);
         issue_a1(nitem);
       }
     }
@@ -967,7 +957,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     const ItemInfo nn = info_of(next_valid(nitem + gridDim.x));  // the item after the next one
     if (__syncthreads_or(false)) break;  // B10
     // dq (staged in the Ahat and N buffers) and dk (in V's buffer); the next item's K, Q and norms (R9 has read
-    // them), then its V, Ahat and N once the staging is read
+    // them); its V, Ahat and N follow after its B2, once the stores have read the staging
     if (lane == 0) {
       if (nvalid == CH) {
         store_tma(&tmdq, sm.ah, h, tok0);
@@ -981,17 +971,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
       par_w = npar;
     }
     if (nvalid < CH && __syncthreads_or(false)) break;  // B11
-    if (lane == 0 && more) {
-      tma_store_wait_read();
-      issue_w2(nitem);
-      issue_c(nitem);
-    }
-    __syncwarp();
-    if (more) {
-      open_w = false;
-      pend_w = pend_c = true;
-      par_c = npar;
-    }
+    deferred = more;
     cur = nxt;
     nxt = nn;
   }
@@ -1035,7 +1015,7 @@ int launch_bwd_local_tc(const BwdArgs &a, const CUtensorMap *maps, int CH_max, c
   const int n_items = CH_max * a.H;
   const int grid = n_items < sms ? n_items : sms;  // persistent: one CTA per SM
   return (int)launch_pdl(bwd_local_tc_kernel, dim3(grid), dim3(LNTHREADS), smem, st, a, maps[0], maps[1], maps[2],
-                         maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], maps[9], n_items);
+                         maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], n_items);
 }
 
 }  // namespace gdn

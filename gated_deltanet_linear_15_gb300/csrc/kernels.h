@@ -64,6 +64,10 @@ struct FwdArgs {
 constexpr int T64_X1 = 0, T64_X2 = 1, T64_AH = 2, T64_P = 3, T64_N = 4, T64_TILES = 5;
 constexpr int T128_W = 0, T128_U = 1, T128_TILES = 2;
 constexpr int TQ_K = 0, TQ_Q = 1, TQ_V = 2, TQ_TILES = 3;
+// Tiles the reverse chain leaves for the local-gradient kernel, fp16 row-major:
+//   tc   [CH_max, H, 2, 128, 64]: dUt^T (rows d_v, columns token) and dO in its operand form (rows 0-63: tokens x
+//                                 features 0-63, rows 64-127: tokens x features 64-127; zero past the sequence end)
+constexpr int TC_DUT = 0, TC_DO = 1, TC_TILES = 2;
 
 struct BwdArgs {
   const void *q, *k, *v, *dO;

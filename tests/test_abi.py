@@ -128,12 +128,12 @@ def test_forward_context_region(lib):
     buffers start where that region starts.  With one segment per sequence (no sequence-parallel
     buffers) the forward and the saved-context backward share the same core, so the difference of
     their workspaces is exactly that region minus the backward's fp16 per-chunk dS (128 x 128) and the
-    reverse chain's fp16 per-chunk dUt^T (128 x 64), which the local-gradient kernel reads."""
+    reverse chain's fp16 per-chunk dUt^T and dO tiles (2 x 128 x 64), which the local-gradient kernel reads."""
     chunks, H = (1000 + 63) // 64, 3
     s = _shape(T=1000, H=H, flags=_lib.GDN_SP_OFF)
     ctx = chunks * H * (5 * 64 * 64 + 3 * 64 * 128) * 2
     dstates = chunks * H * 128 * 128 * 2
-    dut = chunks * H * 128 * 64 * 2
+    dut = chunks * H * 2 * 128 * 64 * 2
     fwd = lib.gdn_fwd_workspace_size(ctypes.byref(s))
     assert fwd - lib.gdn_bwd_saved_workspace_size(ctypes.byref(s)) == ctx - dstates - dut
     # fp32, d = 64 runs the mma.sync kernels: no context region, fp32 per-chunk dS
