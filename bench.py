@@ -81,9 +81,9 @@ def job_throughput(total_ms, world, tokens_per_rank_step, steps):
 # keyed by (profiler name, workload); valid only while the kernel's sources hash to the value
 # recorded with it (otherwise the roofline reports traffic null).  Summaries: profiles/*.md.
 NCU_TRAFFIC = {
-    ("bwd_local", "prefill_h32_t8192"): (960259584, "bwd_local_tc.cu", "47a3d9e8f898bf14"),
-    ("fwd_prep", "prefill_h32_t8192"): (514429952, "fwd_prep_tc.cu", "6353d3e852b92fb8"),
-    ("bwd_chain", "prefill_h32_t8192"): (422545408, "bwd_chain_tc.cu", "a89b9bca45ef57e9"),
+    ("bwd_local", "prefill_h32_t8192"): (1026357248, "bwd_local_tc.cu", "b85f1a2cc0d5df7e"),
+    ("fwd_prep", "prefill_h32_t8192"): (514611712, "fwd_prep_tc.cu", "6ea2fa2817a58325"),
+    ("bwd_chain", "prefill_h32_t8192"): (537566976, "bwd_chain_tc.cu", "3e5b142bf37a323b"),
 }
 KERNEL_COMMON = ["chunk_common.cuh", "umma.cuh", "common.cuh", "kernels.h", "fixup.cuh"]
 
