@@ -101,26 +101,6 @@ __device__ __forceinline__ bool wbar_or(bool pred) {
   return r != 0;
 }
 
-// byte offset of the 16-byte chunk holding columns [cb, cb + 8) of row r in a swizzled tile
-__device__ __forceinline__ uint32_t chunk_off(int r, int cb) { return r * 128 + ((((cb & 63) >> 3) ^ (r & 7)) << 4); }
-
-// Transposing read-outs of a [feature lanes][token columns] accumulator (dv, dq, dk): warp (wq, wg) reads
-// features 32 wq + ls .. + 15 (ls = 0, 16) and tokens c0 .. c0 + 15 as fragments (tmem_ld_frag2), so value
-// 2m + e of lane t is feature 32 wq + ls + 8 (m & 1) + t/4, token c0 + 8 (m >> 1) + 2 (t%4) + e; the four
-// 8 x 8 matrices m move between those fragments and a token-major [token][feature] tile (feature halves
-// `blk` bytes apart, 128-byte swizzled rows) by one ldmatrix / stmatrix .trans, for which lane t addresses
-// the 16 bytes of token c0 + 8 ((t/8) >> 1) + t%8, features from 32 wq + ls + 8 ((t/8) & 1).
-__device__ __forceinline__ uint32_t frag_addr(const uint8_t *base, int blk, int wq, int ls, int c0, int lane) {
-  const int m = lane >> 3;
-  const int tk = c0 + 8 * (m >> 1) + (lane & 7);
-  const int fs = 32 * wq + ls + 8 * (m & 1);
-  return smem_u32(base + (fs >> 6) * blk + chunk_off(tk, fs));
-}
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t *>(&b);
-}
-__device__ __forceinline__ float2 unpack_f16(uint32_t r) { return __half22float2(*reinterpret_cast<const __half2 *>(&r)); }
 // The 64-row products (dP, M1, M2, Y1, dT) are M = 64 MMAs, whose row i sits on TMEM lane 32 (i / 16) + i % 16,
 // so all four lane quarters, and all 16 worker warps, share their read-outs: warp (wq, wg) reads rows 16 wq ..
 // + 15, columns c0 .. c0 + 15 as one fragment (value 2m + e of lane t: row 16 wq + 8 (m & 1) + t/4, column
@@ -150,11 +130,6 @@ __device__ __forceinline__ void col_sum4(float (&v)[4]) {
     v[k] += __shfl_xor_sync(0xffffffffu, v[k], 8);
     v[k] += __shfl_xor_sync(0xffffffffu, v[k], 16);
   }
-}
-// a per-token factor at this lane's four tokens c0 + 2 (t%4) + {0, 1, 8, 9} (16-byte aligned arrays)
-__device__ __forceinline__ void tok4(const float *p, int ta, float (&v)[4]) {
-  const float2 a = *reinterpret_cast<const float2 *>(p + ta), b = *reinterpret_cast<const float2 *>(p + ta + 8);
-  v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
 }
 
 }  // namespace

@@ -48,8 +48,6 @@ __device__ __forceinline__ void st_chunk_f16(uint8_t *dst, const float *v) {
   *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<uint4 *>(h);
 }
 
-__device__ __forceinline__ uint32_t chunk_off(int r, int cb) { return r * 128 + ((((cb & 63) >> 3) ^ (r & 7)) << 4); }
-
 }  // namespace
 
 __global__ void __launch_bounds__(PT, 2)

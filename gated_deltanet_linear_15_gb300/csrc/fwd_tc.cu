@@ -69,8 +69,6 @@ __device__ __forceinline__ void st_chunk_f16(uint8_t *dst, const float *v) {
   *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<uint4 *>(h);
 }
 
-// byte offset of the 16-byte chunk holding columns [cb, cb + 8) of row r in a swizzled [rows][64] tile
-__device__ __forceinline__ uint32_t chunk_off(int r, int cb) { return r * 128 + ((((cb & 63) >> 3) ^ (r & 7)) << 4); }
 
 }  // namespace
 
@@ -450,16 +448,23 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
 
     // ---- O^T = Oi^T diag(gam) + Oa^T -> bf16 staging in wu (two swizzled [64 token][64 feature] halves) ->
     // o by TMA (a full chunk, the producer) or coalesced rows (a partial one)
-    if (emit_o) {
-      const int c0 = wg * 16;
-      float v[16], va[16];
-      tmem_ld16x2(tm + tm_lane + TM_O + c0, v, tm + tm_lane + TM_OA + c0, va);
-      float gm[16];
-      ld16f(G.gam + c0, gm);
-      uint8_t *stg = sm.wu + (row >> 6) * HT;
+    if (emit_o) {  // fragments (rows d_v, columns token), transposed into the staging by stmatrix
+      const int c0 = wg * 16, wq = warp & 3, ta = c0 + 2 * (lane & 3);
+      float gm[4];
+      tok4(G.gam, ta, gm);
+#pragma unroll 1
+      for (int ls = 0; ls < 32; ls += 16) {
+        const uint32_t tq = tm + tm_lane + ((uint32_t)ls << 16) + c0;
+        float v[8], va[8];
+        tmem_ld_frag2(tq + TM_O, v, tq + TM_OA, va);
+        uint32_t pk[4];
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        *reinterpret_cast<bf16 *>(stg + sw128_offset(c0 + i, row & 63)) = __float2bfloat16_rn(fmaf(v[i], gm[i], va[i]));
+        for (int m = 0; m < 4; ++m) {
+          const int k = (m >> 1) * 2;
+          pk[m] = pack_bf16(fmaf(v[2 * m], gm[k], va[2 * m]), fmaf(v[2 * m + 1], gm[k + 1], va[2 * m + 1]));
+        }
+        stmatrix_x4_trans(frag_addr(sm.wu, HT, wq, ls, c0, lane), pk);
+      }
     }
     fence_before();
     fence_async_smem();

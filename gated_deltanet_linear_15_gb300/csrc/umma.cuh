@@ -30,6 +30,33 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t
   return row * 128u + chunk * 16u + (col_elem16 & 7u) * 2u;
 }
 
+// ------------------------------------------------------------------ fragments of [rows][64] tiles
+// byte offset of the 16-byte chunk holding columns [cb, cb + 8) of row r in a swizzled tile
+__device__ __forceinline__ uint32_t chunk_off(int r, int cb) { return r * 128 + ((((cb & 63) >> 3) ^ (r & 7)) << 4); }
+
+// Transposing read-outs of a [feature lanes][token columns] accumulator (o, dv, dq, dk): warp (wq, wg) reads
+// features 32 wq + ls .. + 15 (ls = 0, 16) and tokens c0 .. c0 + 15 as fragments (tmem_ld_frag2), so value
+// 2m + e of lane t is feature 32 wq + ls + 8 (m & 1) + t/4, token c0 + 8 (m >> 1) + 2 (t%4) + e; the four
+// 8 x 8 matrices m move between those fragments and a token-major [token][feature] tile (feature halves
+// `blk` bytes apart, 128-byte swizzled rows) by one ldmatrix / stmatrix .trans, for which lane t addresses
+// the 16 bytes of token c0 + 8 ((t/8) >> 1) + t%8, features from 32 wq + ls + 8 ((t/8) & 1).
+__device__ __forceinline__ uint32_t frag_addr(const uint8_t *base, int blk, int wq, int ls, int c0, int lane) {
+  const int m = lane >> 3;
+  const int tk = c0 + 8 * (m >> 1) + (lane & 7);
+  const int fs = 32 * wq + ls + 8 * (m & 1);
+  return smem_u32(base + (fs >> 6) * blk + chunk_off(tk, fs));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&b);
+}
+__device__ __forceinline__ float2 unpack_f16(uint32_t r) { return __half22float2(*reinterpret_cast<const __half2 *>(&r)); }
+// a per-token factor at this lane's four tokens c0 + 2 (t%4) + {0, 1, 8, 9} (16-byte aligned arrays)
+__device__ __forceinline__ void tok4(const float *p, int ta, float (&v)[4]) {
+  const float2 a = *reinterpret_cast<const float2 *>(p + ta), b = *reinterpret_cast<const float2 *>(p + ta + 8);
+  v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+}
+
 // ------------------------------------------------------------------ descriptors
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
   uint64_t d = 0;
