@@ -33,8 +33,8 @@ struct __align__(1024) PrepSmem {
   uint8_t x1[HT], x2[HT], ah[HT], p[HT];
   float nf[CH * LN];  // N (fp32) for the inverse, which also uses its upper triangle as scratch
   float ys[1152];
-  float g[CH], beta[CH];
-  Gates gt;
+  float g[2][CH], beta[2][CH];  // per item parity: the next item's are loaded during this one
+  Gates gt[2];
   uint64_t bar_tma, bar_mma;
   uint32_t tmem_base;
 };
@@ -72,17 +72,26 @@ __global__ void __launch_bounds__(PT, 2)
 
   // Work items (chunk gc, head h) = (item / H, item % H), strided over the persistent CTAs (two per SM);
   // chunks past the plan's total are skipped.  The next item's q, k, v are loaded by TMA once this
-  // item's Gram product is done and its operand tiles have left, under the read-out and the inverse.
+  // item's Gram product is done and its operand tiles have left, under the read-out and the inverse; its
+  // plan look-ups (dependent global loads) and its g, beta are fetched while this item's Gram product runs.
   auto next_valid = [&](int item) {
     while (item < n_items && a.plan.chunk_seq[item / H] < 0) item += gridDim.x;
     return item;
   };
-  auto tok0_of = [&](int item) {
-    const int gc = item / H, n = a.plan.chunk_seq[gc];
-    return a.plan.seq_bos[n] + (gc - a.plan.seq_chunk0[n]) * CH;
+  struct ItemInfo {
+    int item, tok0, nvalid;
   };
-  auto issue_qkv = [&](int item) {
-    const int hh = item % H, t0 = tok0_of(item);
+  auto info_of = [&](int item) {
+    ItemInfo r{item, 0, 0};
+    if (item < n_items) {
+      const int gc = item / H, n = a.plan.chunk_seq[gc], lc = gc - a.plan.seq_chunk0[n];
+      r.tok0 = a.plan.seq_bos[n] + lc * CH;
+      r.nvalid = min(CH, a.plan.seq_len[n] - lc * CH);
+    }
+    return r;
+  };
+  auto issue_qkv = [&](int item, int t0) {
+    const int hh = item % H;
     const uint32_t bar = u32(&sm.bar_tma);
     mbar_expect_tx(bar, 6 * HT);
 #pragma unroll
@@ -92,7 +101,12 @@ __global__ void __launch_bounds__(PT, 2)
       tma_load_3d(u32(sm.kqv + (4 + hb) * HT), &tmv, 64 * hb, hh, t0, bar);
     }
   };
-  int item = next_valid(blockIdx.x);
+  ItemInfo cur = info_of(next_valid(blockIdx.x));
+  if (tid < 2 * CH && cur.item < n_items) {  // the first item's g, beta (later items': fetched one item ahead)
+    const int r = tid & (CH - 1), hh = cur.item % H;
+    const float v = r < cur.nvalid ? (tid < CH ? a.g : a.beta)[(size_t)(cur.tok0 + r) * H + hh] : 0.f;
+    (tid < CH ? sm.g[0] : sm.beta[0])[r] = v;
+  }
   if (tid == 0) {
     mbar_init(u32(&sm.bar_tma), 1);
     mbar_init(u32(&sm.bar_mma), 1);
@@ -102,7 +116,7 @@ __global__ void __launch_bounds__(PT, 2)
     tma_prefetch_desc(&tmv);
     tma_prefetch_desc(&tmw);
     tma_prefetch_desc(&tm3);
-    if (item < n_items) issue_qkv(item);
+    if (cur.item < n_items) issue_qkv(cur.item, cur.tok0);
   }
   if (warp == 0) {
     tmem_alloc(u32(&sm.tmem_base), 64);
@@ -112,23 +126,15 @@ __global__ void __launch_bounds__(PT, 2)
   __syncthreads();
   fence_after();
   const uint32_t tm = sm.tmem_base;
-  bool pend = item < n_items;  // a q, k, v load in flight
+  bool pend = cur.item < n_items;  // a q, k, v load in flight
   bool nbad = false;           // numeric guard: a widened operand out of fp16 range
   uint32_t it = 0;             // parity of both barriers: one completion each per item
 
-  for (; item < n_items; ++it) {
-    const int gc = item / H, h = item % H, n = a.plan.chunk_seq[gc];
-    const int lc = gc - a.plan.seq_chunk0[n];
-    const int tok0 = a.plan.seq_bos[n] + lc * CH;
-    const int nvalid = min(CH, a.plan.seq_len[n] - lc * CH);
-    const int nitem = next_valid(item + gridDim.x);
+  for (; cur.item < n_items; ++it) {
+    const int item = cur.item, nvalid = cur.nvalid, gbuf = it & 1;
     const int t64row = item * T64_TILES * CH, qrow = item * TQ_TILES * CH;
-    if (tid < CH) sm.g[tid] = tid < nvalid ? a.g[(size_t)(tok0 + tid) * H + h] : 0.f;
-    else if (tid < 2 * CH) sm.beta[tid - CH] = tid - CH < nvalid ? a.beta[(size_t)(tok0 + tid - CH) * H + h] : 0.f;
-    // the previous item's X1, X2, Ahat, P stores have read their staging (rewritten below)
+    // the previous item's X1, X2, Ahat, P stores have read their staging (rewritten after the next barriers)
     if (tid == 0) tma_store_wait_read();
-    __syncthreads();
-    if (warp == 0) gate_prefix(sm.g, sm.gt);
     const bool tma_ok = mbar_wait(u32(&sm.bar_tma), it & 1, err, 8);
     pend = false;
     if (__syncthreads_or(!tma_ok)) break;
@@ -164,6 +170,9 @@ __global__ void __launch_bounds__(PT, 2)
         ss += __shfl_xor_sync(0xffffffffu, ss, 2);
         rn = rsqrtf(ss + 1e-6f);
         mul *= rn;
+        // normalised, every element is at most `scale` in magnitude: the fp16 range can only fail through a
+        // non-finite input, which makes the squared norm non-finite (one check per row, not per element)
+        nbad |= !(ss <= 3.0e38f);
       }
       if (nrm && qq == 0) nrm[(isq ? CH : 0) + r] = rn;  // 1/|k|, 1/|q| per token (1 without normalisation)
       if (r >= nvalid) mul = 0.f;
@@ -174,7 +183,7 @@ __global__ void __launch_bounds__(PT, 2)
         for (int i = 0; i < 4; ++i) {
           const uint32_t w = raw[4 * cc + i];
           const float lo = __uint_as_float(w << 16) * mul, hi = __uint_as_float(w & 0xffff0000u) * mul;
-          nbad |= f16_out(lo) | f16_out(hi);
+          if (!l2) nbad |= f16_out(lo) | f16_out(hi);
           const __half2 a2 = __floats2half2_rn(lo, hi);
           y[i] = *reinterpret_cast<const uint32_t *>(&a2);
         }
@@ -226,14 +235,24 @@ __global__ void __launch_bounds__(PT, 2)
       mma_commit(u32(&sm.bar_mma));
     }
     __syncwarp();
+    // under the Gram product: this item's gate prefix sums (warp 7; the read-out of P is their first
+    // reader), the next item's plan look-ups and its g, beta (kept in registers until the product is done)
+    if (warp == PT / 32 - 1) gate_prefix(sm.g[gbuf], sm.gt[gbuf]);
+    const ItemInfo nxt = info_of(next_valid(item + gridDim.x));
+    float gnext = 0.f;
+    if (tid < 2 * CH && nxt.item < n_items) {
+      const int r = tid & (CH - 1), hh = nxt.item % H;
+      if (r < nxt.nvalid) gnext = (tid < CH ? a.g : a.beta)[(size_t)(nxt.tok0 + r) * H + hh];
+    }
     const bool mok = mbar_wait(u32(&sm.bar_mma), it & 1, err, 4);
     fence_after();
     if (__syncthreads_or(!mok)) break;
-    if (tid == 0 && nitem < n_items) {  // kqv is free once the operand-tile stores have read it
+    if (tid < 2 * CH) (tid < CH ? sm.g[gbuf ^ 1] : sm.beta[gbuf ^ 1])[tid & (CH - 1)] = gnext;
+    if (tid == 0 && nxt.item < n_items) {  // kqv is free once the operand-tile stores have read it
       tma_store_wait_read();
-      issue_qkv(nitem);
+      issue_qkv(nxt.item, nxt.tok0);
     }
-    pend = nitem < n_items;
+    pend = nxt.item < n_items;
 
     // ---- read-out: warp w takes TMEM lanes 32 (w % 4).. and columns 32 (w / 4)..; N (fp32, rows 0-63,
     // also stored as fp16) and P (fp16, rows 64-127)
@@ -261,7 +280,7 @@ __global__ void __launch_bounds__(PT, 2)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             float w8[8], rt[8];
-            ratio8<decltype(pw)::value>(sm.gt, r, c0 + 8 * q, rt);
+            ratio8<decltype(pw)::value>(sm.gt[gbuf], r, c0 + 8 * q, rt);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const int c = c0 + 8 * q + i;
@@ -270,7 +289,7 @@ __global__ void __launch_bounds__(PT, 2)
             st_chunk_f16(sm.p + chunk_off(r, c0 + 8 * q), w8);
           }
         };
-        if (sm.gt.pw) pread(std::true_type{});
+        if (sm.gt[gbuf].pw) pread(std::true_type{});
         else pread(std::false_type{});
       }
     }
@@ -278,8 +297,8 @@ __global__ void __launch_bounds__(PT, 2)
     __syncthreads();
 
     // ---- Ahat -> X1, X2 (and Ahat) staging, fp16 K-major (rows = r)
-    const float *beta = sm.beta;
-    const Gates &G = sm.gt;
+    const float *beta = sm.beta[gbuf];
+    const Gates &G = sm.gt[gbuf];
     wy_inverse<false, false>(sm.nf, LN, beta, sm.ys, [&](int r, int c, float a0, float a1) {
       const float2 bb = *reinterpret_cast<const float2 *>(beta + c);
       const float x0 = a0 * bb.x, x1 = a1 * bb.y;
@@ -298,7 +317,7 @@ __global__ void __launch_bounds__(PT, 2)
       if (full) tma_store_3d(&tmw, 0, t64row + T64_AH * CH, 0, u32(sm.ah));
       tma_store_commit();
     }
-    item = nitem;
+    cur = nxt;
   }
   if (nbad && err) atomicOr(err, 1);
   if (tid == 0) {
