@@ -133,8 +133,6 @@ __global__ void __launch_bounds__(PT, 2)
   for (; cur.item < n_items; ++it) {
     const int item = cur.item, nvalid = cur.nvalid, gbuf = it & 1;
     const int t64row = item * T64_TILES * CH, qrow = item * TQ_TILES * CH;
-    // the previous item's X1, X2, Ahat, P stores have read their staging (rewritten after the next barriers)
-    if (tid == 0) tma_store_wait_read();
     const bool tma_ok = mbar_wait(u32(&sm.bar_tma), it & 1, err, 8);
     pend = false;
     if (__syncthreads_or(!tma_ok)) break;
@@ -233,6 +231,9 @@ __global__ void __launch_bounds__(PT, 2)
         mma_f16s(tm, sdesc_s(base, 16, 1024) + (koff), sdesc_s(base, 16, 1024) + (koff), idesc, kk > 0);
       }
       mma_commit(u32(&sm.bar_mma));
+      // the previous item's X1, X2, Ahat, P stores have read their staging (rewritten after the product):
+      // every store group but the operand tiles just issued
+      tma_store_wait_read_but_last();
     }
     __syncwarp();
     // under the Gram product: this item's gate prefix sums (warp 7; the read-out of P is their first

@@ -353,6 +353,10 @@ __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk
 __device__ __forceinline__ void tma_store_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
 }
+// the same for all but the most recent store group (which may still be reading its source)
+__device__ __forceinline__ void tma_store_wait_read_but_last() {
+  asm volatile("cp.async.bulk.wait_group.read 1;\n" ::: "memory");
+}
 // the issuing thread's stores are complete
 __device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
