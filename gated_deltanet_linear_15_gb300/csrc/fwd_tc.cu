@@ -38,8 +38,8 @@ constexpr int HT = 8192;  // one 64 x 64 fp16 half-tile, 128B-swizzled
 constexpr int FT = 512;   // worker threads (16 warps); warp 16 is the producer
 constexpr int FWARPS = FT / 32;
 
-// TMEM columns
-constexpr uint32_t TM_S = 0, TM_W = 128, TM_U = 192, TM_O = 256, TM_OA = 320, TM_COLS = 512;
+// TMEM columns; Oi, Oa are double-buffered by chunk parity (a chunk's o is read out during the next chunk)
+constexpr uint32_t TM_S = 0, TM_W = 128, TM_U = 192, TM_O = 256, TM_OA = 320, TM_OB = 128, TM_COLS = 512;
 
 // ring stage: [K0 | Q0 | K1 | Q1 | V0 | V1 | X1 | X2 | P] half-tiles (0/1 = feature block)
 constexpr int R_K = 0, R_Q = 1, R_V = 4, R_X1 = 6, R_X2 = 7, R_P = 8, R_TILES = 9;
@@ -217,6 +217,27 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
   __syncthreads();
   fence_after();
 
+  // O^T = Oi^T diag(gam) + Oa^T of a chunk (TMEM buffer at column offset obuf, its gates gt) -> bf16
+  // [token][d_v] staging in uc, two swizzled [64 token][64 feature] halves: fragments (rows d_v, columns
+  // token) transposed by stmatrix
+  auto stage_o = [&](const Gates &gt, uint32_t obuf) {
+    const int c0 = wg * 16, wq = warp & 3, ta = c0 + 2 * (lane & 3);
+    float gm[4];
+    tok4(gt.gam, ta, gm);
+#pragma unroll 1
+    for (int ls = 0; ls < 32; ls += 16) {
+      const uint32_t tq = tm + tm_lane + ((uint32_t)ls << 16) + c0 + obuf;
+      float v[8], va[8];
+      tmem_ld_frag2(tq + TM_O, v, tq + TM_OA, va);
+      uint32_t pk[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int k = (m >> 1) * 2;
+        pk[m] = pack_bf16(fmaf(v[2 * m], gm[k], va[2 * m]), fmaf(v[2 * m + 1], gm[k + 1], va[2 * m + 1]));
+      }
+      stmatrix_x4_trans(frag_addr(sm.uc, HT, wq, ls, c0, lane), pk);
+    }
+  };
   int *err = a.status;
   uint32_t mma_phase = 0, mma2_phase = 0;
   bool failed = false;
@@ -227,9 +248,11 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
     return ok;
   };
 
-  // Workers and producer meet at CTA-wide OR-barriers (A1, A3, A4, A5) that also carry a failed wait; the
-  // workers sync among themselves on barrier 2, and the producer tells them that a context store has
-  // read wu (barrier 3, arrive / sync).
+  // Workers and producer meet at CTA-wide OR-barriers (A1, A3, A4) that also carry a failed wait; the
+  // workers sync among themselves on barrier 2, tell the producer that the previous chunk's o is staged
+  // (barrier 4, arrive / sync), and the producer tells them that the W^T and o stores have read wu and
+  // uc (barrier 3, arrive / sync).  A chunk's o is read out under the next chunk's MMA 3, off the
+  // recurrence's critical path; the segment's last one after the loop.
   const bool producer = warp == FWARPS;
   for (int c = cfirst; c < cend; ++c) {
     const int it = c - cfirst;
@@ -244,6 +267,10 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
     const bool more = c + 1 < cend;
     const int nvn = more ? min(CH, len - (c + 1) * CH) : 0;
     Gates &G = sm.gt[stage];
+    const uint32_t ob = (uint32_t)stage * TM_OB;  // this chunk's Oi, Oa buffer
+    // the previous chunk's o, read out under this chunk's MMA 3 (a full chunk: only a segment's last chunk
+    // can be partial, and that one is read out after the loop)
+    const bool prev_o = want_o && outputs && it > 0 && c - 1 >= cbeg;
 
     if (producer) {
       // ================================================================ producer
@@ -280,7 +307,17 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
                    need_v || kk > 0);
         }
         mma_commit(u32(&sm.bar_mma));
-        if (save_c) tma_store_wait_read();  // the W^T store has read wu (Ut^T is written next)
+      }
+      __syncwarp();
+      named_bar_sync<4, FT + 32>();  // the workers staged the previous chunk's o in uc
+      if (lane == 0) {
+        if (prev_o) {  // the previous chunk's o (a full chunk) by two TMA stores
+          tma_store_3d(&tmo, 0, h, tok0 - CH, u32(sm.uc));
+          tma_store_3d(&tmo, 64, h, tok0 - CH, u32(sm.uc + HT));
+          tma_store_commit();
+        }
+        // the W^T and o stores have read wu and uc (Ut^T and Ut^T diag(cdec) are written next)
+        if (save_c || prev_o) tma_store_wait_read();
       }
       __syncwarp();
       named_bar_arrive<3, FT + 32>();
@@ -291,14 +328,14 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
           tma_store_3d(&tms, 64, srow, 0, u32(sm.s0 + 2 * HT));
           tma_store_commit();
         }
-        // Oi^T = S0 Q^T: read at the O read-out, after MMA 4's commit
+        // Oi^T = S0 Q^T: read out with Oa during the next chunk (MMA 4's commit covers it)
         if (emit_o) {
           const uint32_t s0b = u32(sm.s0), qb = u32(st + R_Q * HT);
           const uint32_t id_o = idesc_f16(128, 64, false, false);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t aoff = (kk >> 2) * 2 * HT + (kk & 3) * 32;
-            mma_f16s(tm + TM_O, sdesc_s(s0b, 16, 1024) + (aoff), sdesc_s(qb, 16, 1024) + (aoff), id_o, kk > 0);
+            mma_f16s(tm + TM_O + ob, sdesc_s(s0b, 16, 1024) + (aoff), sdesc_s(qb, 16, 1024) + (aoff), id_o, kk > 0);
           }
         }
       }
@@ -323,27 +360,16 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
         if (emit_o) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_f16s(tm + TM_OA, sdesc_s(ub, 16, 1024) + (kk * 32), sdesc_s(pb, 16, 1024) + (kk * 32), id_o, kk > 0);
+            mma_f16s(tm + TM_OA + ob, sdesc_s(ub, 16, 1024) + (kk * 32), sdesc_s(pb, 16, 1024) + (kk * 32), id_o,
+                     kk > 0);
         }
         mma_commit(u32(&sm.bar_mma));
-        if (save_c && emit_o) tma_store_wait_read();  // the Ut^T store has read wu (the O staging)
       }
       __syncwarp();
-      named_bar_arrive<3, FT + 32>();
       // MMA 2 of the next chunk once its tiles are in: TM_W and TM_U were read before A3 and A4
       if (lane == 0 && more && mbar_wait(u32(&sm.bar_tma[stage ^ 1]), ((it + 1) >> 1) & 1, err, 8)) {
         fence_after();
         issue_mma2(sm.ring[stage ^ 1]);
-      }
-      __syncwarp();
-      if (__syncthreads_or(false)) {  // A5: the O tile is staged
-        failed = true;
-        break;
-      }
-      if (lane == 0 && emit_o && nvalid == CH) {  // a full chunk of o by two TMA stores
-        tma_store_3d(&tmo, 0, h, tok0, u32(sm.wu));
-        tma_store_3d(&tmo, 64, h, tok0, u32(sm.wu + HT));
-        tma_store_commit();
       }
       __syncwarp();
       continue;
@@ -405,12 +431,16 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
     }
     fence_before();
     fence_async_smem();  // the state copy and W^T are operands of MMA 3 and Oi
-    if (__syncthreads_or(failed)) {  // A3: the producer stores the state and W^T, issues MMA 3 and Oi
+    if (__syncthreads_or(failed)) {  // A3: the producer stores W^T and issues MMA 3, then the state and Oi
       failed = true;
       break;
     }
+    // under MMA 3: the previous chunk's o into the uc staging (uc's last reader, that chunk's MMA 4, is done)
+    if (prev_o) stage_o(sm.gt[stage ^ 1], ob ^ TM_OB);
+    fence_async_smem();
+    named_bar_arrive<4, FT + 32>();  // the producer stores it
     failed |= !mma_wait();  // MMA 3
-    named_bar_sync<3, FT + 32>();  // the W^T store has read wu
+    named_bar_sync<3, FT + 32>();  // the W^T and o stores have read wu and uc
 
     // ---- Ut^T read-out -> fp16 K-major A (rows = d_v, k = token), and Ut^T diag(cdec)
     {
@@ -444,41 +474,29 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
       gate_prefix(gn, sm.gt[stage ^ 1]);
     }
     failed |= !mma_wait();  // MMA 4
-    named_bar_sync<3, FT + 32>();  // the Ut^T store has read wu
+  }
 
-    // ---- O^T = Oi^T diag(gam) + Oa^T -> bf16 staging in wu (two swizzled [64 token][64 feature] halves) ->
-    // o by TMA (a full chunk, the producer) or coalesced rows (a partial one)
-    if (emit_o) {  // fragments (rows d_v, columns token), transposed into the staging by stmatrix
-      const int c0 = wg * 16, wq = warp & 3, ta = c0 + 2 * (lane & 3);
-      float gm[4];
-      tok4(G.gam, ta, gm);
-#pragma unroll 1
-      for (int ls = 0; ls < 32; ls += 16) {
-        const uint32_t tq = tm + tm_lane + ((uint32_t)ls << 16) + c0;
-        float v[8], va[8];
-        tmem_ld_frag2(tq + TM_O, v, tq + TM_OA, va);
-        uint32_t pk[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const int k = (m >> 1) * 2;
-          pk[m] = pack_bf16(fmaf(v[2 * m], gm[k], va[2 * m]), fmaf(v[2 * m + 1], gm[k + 1], va[2 * m + 1]));
-        }
-        stmatrix_x4_trans(frag_addr(sm.wu, HT, wq, ls, c0, lane), pk);
-      }
-    }
+  // ---------------------------------------------------------------- the last chunk's o
+  {
+    const int cl = cend - 1;
+    const bool last_o = !failed && want_o && outputs && cl >= cbeg && cl >= cfirst;
+    const int tok0 = bos + cl * CH, nvalid = min(CH, len - cl * CH);
+    if (last_o && warp < FWARPS) stage_o(sm.gt[(cl - cfirst) & 1], (uint32_t)((cl - cfirst) & 1) * TM_OB);
     fence_before();
     fence_async_smem();
-    if (__syncthreads_or(failed)) {  // A5: the producer stores a full chunk of o
-      failed = true;
-      break;
+    __syncthreads();
+    if (last_o && nvalid == CH && tid == FT) {  // a full chunk by two TMA stores
+      tma_store_3d(&tmo, 0, h, tok0, u32(sm.uc));
+      tma_store_3d(&tmo, 64, h, tok0, u32(sm.uc + HT));
+      tma_store_commit();
     }
-    if (emit_o && nvalid < CH) {
+    if (last_o && nvalid < CH && warp < FWARPS) {  // a partial one by coalesced rows
       bf16 *og = static_cast<bf16 *>(a.o);
       for (int e = tid; e < CH * (D / 8); e += FT) {
         const int r = e >> 4, cc = e & 15;
         if (r < nvalid)
           *reinterpret_cast<uint4 *>(og + ((size_t)(tok0 + r) * H + h) * D + cc * 8) =
-              *reinterpret_cast<const uint4 *>(sm.wu + (cc >> 3) * HT + r * 128 + (((cc & 7) ^ (r & 7)) << 4));
+              *reinterpret_cast<const uint4 *>(sm.uc + (cc >> 3) * HT + r * 128 + (((cc & 7) ^ (r & 7)) << 4));
       }
     }
   }
