@@ -250,8 +250,8 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
 
   // Workers and producer meet at CTA-wide OR-barriers (A1, A3, A4) that also carry a failed wait; the
   // workers sync among themselves on barrier 2, tell the producer that the previous chunk's o is staged
-  // (barrier 4, arrive / sync), and the producer tells them that the W^T and o stores have read wu and
-  // uc (barrier 3, arrive / sync).  A chunk's o is read out under the next chunk's MMA 3, off the
+  // (barrier 4, arrive / sync), and the producer tells them that the W^T store has read wu (barrier 3)
+  // and the o store uc (barrier 5, arrive / sync).  A chunk's o is read out under the next chunk's MMA 3, off the
   // recurrence's critical path; the segment's last one after the loop.
   const bool producer = warp == FWARPS;
   for (int c = cfirst; c < cend; ++c) {
@@ -307,20 +307,19 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
                    need_v || kk > 0);
         }
         mma_commit(u32(&sm.bar_mma));
-      }
-      __syncwarp();
-      named_bar_sync<4, FT + 32>();  // the workers staged the previous chunk's o in uc
-      if (lane == 0) {
-        if (prev_o) {  // the previous chunk's o (a full chunk) by two TMA stores
-          tma_store_3d(&tmo, 0, h, tok0 - CH, u32(sm.uc));
-          tma_store_3d(&tmo, 64, h, tok0 - CH, u32(sm.uc + HT));
-          tma_store_commit();
-        }
-        // the W^T and o stores have read wu and uc (Ut^T and Ut^T diag(cdec) are written next)
-        if (save_c || prev_o) tma_store_wait_read();
+        if (save_c) tma_store_wait_read();  // the W^T store has read wu (Ut^T is written next)
       }
       __syncwarp();
       named_bar_arrive<3, FT + 32>();
+      named_bar_sync<4, FT + 32>();  // the workers staged the previous chunk's o in uc
+      if (lane == 0 && prev_o) {  // the previous chunk's o (a full chunk) by two TMA stores
+        tma_store_3d(&tmo, 0, h, tok0 - CH, u32(sm.uc));
+        tma_store_3d(&tmo, 64, h, tok0 - CH, u32(sm.uc + HT));
+        tma_store_commit();
+        tma_store_wait_read();  // it has read uc (Ut^T diag(cdec) is written next)
+      }
+      __syncwarp();
+      named_bar_arrive<5, FT + 32>();
       if (lane == 0) {
         if (save_states && c >= cbeg) {  // the fp16 chunk-start state, two 64-column blocks
           const int srow = ((chunk0 + c) * H + h) * D;
@@ -440,7 +439,7 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
     fence_async_smem();
     named_bar_arrive<4, FT + 32>();  // the producer stores it
     failed |= !mma_wait();  // MMA 3
-    named_bar_sync<3, FT + 32>();  // the W^T and o stores have read wu and uc
+    named_bar_sync<3, FT + 32>();  // the W^T store has read wu
 
     // ---- Ut^T read-out -> fp16 K-major A (rows = d_v, k = token), and Ut^T diag(cdec)
     {
@@ -457,6 +456,7 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
       ld16f(G.cdec + c0, cd);
 #pragma unroll
       for (int i = 0; i < 16; ++i) v[i] *= cd[i];
+      named_bar_sync<5, FT + 32>();  // the o store has read uc
       st_chunk_f16(sm.uc + chunk_off(row, c0), v);
       st_chunk_f16(sm.uc + chunk_off(row, c0 + 8), v + 8);
     }
