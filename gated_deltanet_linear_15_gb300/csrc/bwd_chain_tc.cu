@@ -267,11 +267,11 @@ __device__ __forceinline__ void chain_tc_item(const BwdArgs &a, const CUtensorMa
     }
 
     // ================================================================ workers
-    float gnext0 = 0.f, gnext1 = 0.f;  // log-gates of the next (previous in time) chunk
-    if (warp == 0 && c - 1 >= cbeg) {
-      const int tokn = bos + (c - 1) * CH;
-      gnext0 = a.g[(size_t)(tokn + lane) * H + h];
-      gnext1 = a.g[(size_t)(tokn + lane + 32) * H + h];
+    float gnext0 = 0.f, gnext1 = 0.f;  // log-gates of the next (previous in time) chunk, warps 0 and 1
+    if (warp < 2 && c - 1 >= cbeg) {
+      const int tokn = bos + (c - 1) * CH, nvn = min(CH, len - (c - 1) * CH);
+      if (lane < nvn) gnext0 = a.g[(size_t)(tokn + lane) * H + h];
+      if (lane + 32 < nvn) gnext1 = a.g[(size_t)(tokn + lane + 32) * H + h];
     }
     if (it == 0) cp_async_wait_all();  // the first chunk's gates; later ones come from gnext
     {
@@ -376,14 +376,8 @@ __device__ __forceinline__ void chain_tc_item(const BwdArgs &a, const CUtensorMa
       failed = true;
       break;
     }
-    if (warp == 0 && c - 1 >= cbeg) {  // gates of the next chunk, overlapping the last product
-      float *gn = sm.g[stage ^ 1];
-      const int nvn = min(CH, len - (c - 1) * CH);
-      gn[lane] = lane < nvn ? gnext0 : 0.f;
-      gn[lane + 32] = lane + 32 < nvn ? gnext1 : 0.f;
-      __syncwarp();
-      gate_prefix(gn, sm.gt[stage ^ 1]);
-    }
+    if (warp < 2 && c - 1 >= cbeg)  // gates of the next chunk, overlapping the last product: a half per warp
+      gate_prefix_part(gnext0, gnext1, sm.gt[stage ^ 1], 1 << warp);
     failed |= !mma_wait();  // round 2
   }
   if (release) __syncthreads_or(true);  // meet the producer at its pending CTA-wide barrier: it stops there

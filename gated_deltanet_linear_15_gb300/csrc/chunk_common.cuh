@@ -142,9 +142,14 @@ __device__ __forceinline__ void ld16f(const float *p, float (&v)[16]) {
   }
 }
 
-__device__ __forceinline__ bool gate_prefix(const float *g, Gates &gt) {
+// The in-chunk prefix sums and decay factors of a chunk (lane l of the calling warp holds the log-gates of
+// tokens l and l + 32), written for the tokens of `halves` (bit 0: tokens 0-31, bit 1: tokens 32-63); the
+// bit-0 writer also sets gamC and pw.  Every caller forms the full scans, so two warps can split the
+// exponentials (one half each) with no exchange; returns pw.
+__device__ __forceinline__ bool gate_prefix_part(float ga, float gb, Gates &gt, int halves) {
   const int lane = threadIdx.x & 31;
-  const float ga = fmaxf(g[lane], GATE_FLOOR), gb = fmaxf(g[lane + 32], GATE_FLOOR);
+  ga = fmaxf(ga, GATE_FLOOR);
+  gb = fmaxf(gb, GATE_FLOOR);
   float a = ga, b = gb, al = 0.f, bl = 0.f;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -174,26 +179,35 @@ __device__ __forceinline__ bool gate_prefix(const float *g, Gates &gt) {
     two_add(b, bl, Gm, Gml);
   }
   const float Gl = __shfl_sync(0xffffffffu, b, 31), Gll = __shfl_sync(0xffffffffu, bl, 31);
-  gt.Ghi[lane] = a;
-  gt.Glo[lane] = al;
-  gt.Ghi[lane + 32] = b;
-  gt.Glo[lane + 32] = bl;
-  gt.gam[lane] = expf(a + al);
-  gt.gam[lane + 32] = expf(b + bl);
   const float da = two_diff(a, al, Gm, Gml), db = two_diff(b, bl, Gm, Gml);
-  gt.gp[lane] = expf(da);
-  gt.gp[lane + 32] = expf(db);
-  gt.rgp[lane] = expf(-da);
-  gt.rgp[lane + 32] = expf(-db);
-  gt.cdec[lane] = expf(two_diff(Gl, Gll, a, al));
-  gt.cdec[lane + 32] = expf(two_diff(Gl, Gll, b, bl));
-  if (lane == 0) gt.gamC = expf(Gl + Gll);
+  if (halves & 1) {
+    gt.Ghi[lane] = a;
+    gt.Glo[lane] = al;
+    gt.gam[lane] = expf(a + al);
+    gt.gp[lane] = expf(da);
+    gt.rgp[lane] = expf(-da);
+    gt.cdec[lane] = expf(two_diff(Gl, Gll, a, al));
+    if (lane == 0) gt.gamC = expf(Gl + Gll);
+  }
+  if (halves & 2) {
+    gt.Ghi[lane + 32] = b;
+    gt.Glo[lane + 32] = bl;
+    gt.gam[lane + 32] = expf(b + bl);
+    gt.gp[lane + 32] = expf(db);
+    gt.rgp[lane + 32] = expf(-db);
+    gt.cdec[lane + 32] = expf(two_diff(Gl, Gll, b, bl));
+  }
   float rng = fmaxf(fabsf(da), fabsf(db));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) rng = fmaxf(rng, __shfl_xor_sync(0xffffffffu, rng, o));
   const bool pw = rng > FACTOR_RANGE;
-  if (lane == 0) gt.pw = pw;
+  if ((halves & 1) && lane == 0) gt.pw = pw;
   return pw;
+}
+// one warp, both halves, log-gates from shared memory
+__device__ __forceinline__ bool gate_prefix(const float *g, Gates &gt) {
+  const int lane = threadIdx.x & 31;
+  return gate_prefix_part(g[lane], g[lane + 32], gt, 3);
 }
 
 // o[i] = gamma_r / gamma_{cb + i} for cb + i <= r, 0 above the diagonal (eight columns from cb, a multiple of 8),

@@ -375,8 +375,8 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
     }
 
     // ================================================================ workers
-    float gnext0 = 0.f, gnext1 = 0.f;  // next chunk's log-gates (warp 0), consumed while MMA 4 runs
-    if (warp == 0 && more) {
+    float gnext0 = 0.f, gnext1 = 0.f;  // next chunk's log-gates (warps 0, 1), consumed while MMA 4 runs
+    if (warp < 2 && more) {
       const int tokn = bos + (c + 1) * CH;
       if (lane < nvn) gnext0 = a.g[(size_t)(tokn + lane) * H + h];
       if (lane + 32 < nvn) gnext1 = a.g[(size_t)(tokn + lane + 32) * H + h];
@@ -466,13 +466,8 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
       failed = true;
       break;
     }
-    if (warp == 0 && more) {  // gates of the next chunk, overlapping MMA 4
-      float *gn = sm.g[stage ^ 1];
-      gn[lane] = gnext0;
-      gn[lane + 32] = gnext1;
-      __syncwarp();
-      gate_prefix(gn, sm.gt[stage ^ 1]);
-    }
+    if (warp < 2 && more)  // gates of the next chunk, overlapping MMA 4: a half per warp
+      gate_prefix_part(gnext0, gnext1, sm.gt[stage ^ 1], 1 << warp);
     failed |= !mma_wait();  // MMA 4
   }
 
