@@ -81,9 +81,10 @@ def job_throughput(total_ms, world, tokens_per_rank_step, steps):
 # keyed by (profiler name, workload); valid only while the kernel's sources hash to the value
 # recorded with it (otherwise the roofline reports traffic null).  Summaries: profiles/*.md.
 NCU_TRAFFIC = {
-    ("bwd_local", "prefill_h32_t8192"): (1026357248, "bwd_local_tc.cu", "b85f1a2cc0d5df7e"),
-    ("fwd_prep", "prefill_h32_t8192"): (514611712, "fwd_prep_tc.cu", "6ea2fa2817a58325"),
-    ("bwd_chain", "prefill_h32_t8192"): (537566976, "bwd_chain_tc.cu", "3e5b142bf37a323b"),
+    ("bwd_local", "prefill_h32_t8192"): (1023317504, "bwd_local_tc.cu", "2b10173a98719041"),
+    ("fwd_chunk", "prefill_h32_t8192"): (596598784, "fwd_tc.cu", "25853474f9671c9b"),
+    ("fwd_prep", "prefill_h32_t8192"): (514280448, "fwd_prep_tc.cu", "1f85f4302ede08ed"),
+    ("bwd_chain", "prefill_h32_t8192"): (533453568, "bwd_chain_tc.cu", "f34997149f510216"),
 }
 KERNEL_COMMON = ["chunk_common.cuh", "umma.cuh", "common.cuh", "kernels.h", "fixup.cuh"]
 
