@@ -292,7 +292,7 @@ class ChunkGatedDeltaRuleFunction(torch.autograd.Function):
 def chunk_gated_delta_rule(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=None,
                            use_qk_l2norm_in_kernel=False, save_context=True):
     """Autograd entry: returns (o, final_state).  save_context=True keeps the per-chunk states
-    and WY tiles from the forward until the backward (gdn_saved_size bytes: 56 KB per chunk
+    and chunk context from the forward until the backward (gdn_saved_size bytes: about 152.5 KB per chunk
     and head at d = 128, bf16) instead of recomputing them there."""
     return ChunkGatedDeltaRuleFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, scale,
                                              use_qk_l2norm_in_kernel, save_context)

@@ -65,8 +65,8 @@ struct Layout {
   size_t off_tqkv = 0, off_nrm = 0, tqkv_bytes = 0, nrm_bytes = 0;
   size_t states_bytes = 0;                  // per-chunk start states
   size_t bwd_saved_total = 0;               // backward workspace when the forward saved its context
-  size_t saved_off_t64 = 0, saved_off_t128 = 0, saved_off_tqkv = 0, saved_off_nrm = 0;
-  size_t saved_total = 0;  // saved context: [states][t64][t128][tqkv][nrm]
+  size_t saved_off_t64 = 0, saved_off_t128 = 0, saved_off_tqkv = 0, saved_off_nrm = 0, saved_off_gsum = 0;
+  size_t saved_total = 0;  // saved context: [states][t64][t128][tqkv][nrm][gsum]
   size_t off_fctx_t64 = 0, off_fctx_tqkv = 0;  // the plain forward's chunk context (bf16, d = 128)
   size_t fwd_core = 0, fwd_total = 0, bwd_total = 0;
 };
@@ -276,7 +276,9 @@ int make_layout(const gdn_shape *s, Layout &L) {
   L.saved_off_t128 = L.states_bytes + L.t64_bytes;
   L.saved_off_tqkv = L.saved_off_t128 + L.t128_bytes;
   L.saved_off_nrm = L.saved_off_tqkv + L.tqkv_bytes;
-  L.saved_total = L.saved_off_nrm + L.nrm_bytes;
+  // the per-(chunk, head) gate sums: the saved-context backward takes them instead of rescanning g
+  L.saved_off_gsum = L.saved_off_nrm + L.nrm_bytes;
+  L.saved_total = L.saved_off_gsum + align256((size_t)L.CH_max * L.H * 4);
   return GDN_OK;
 }
 
@@ -403,8 +405,20 @@ void prof_drain_locked() {
     if (_e != 0) return fail(GDN_ERR_CUDA, "%s failed: %s", #expr, cudaGetErrorString((cudaError_t)_e)); \
   } while (0)
 
-// plan + gate scan, shared by both directions
-int prologue(const gdn_shape *s, const Layout &L, char *ws, const float *g, cudaStream_t st, Plan &pl) {
+// The chunk forward kernel for this problem: tcgen05 for bf16 with d = 128 (its recurrent half, on the
+// context that the chunk-local half stored), the mma.sync/CUDA-core kernel otherwise (d = 64, fp32
+// inputs, empty batches).
+bool tc_forward(const Layout &L, const gdn_shape *s) { return s->dtype == GDN_BF16 && L.D == 128 && L.Ttot > 0; }
+
+// Does the chunk-local half of the tcgen05 forward run in this call and take the gate scan's place (it writes
+// the per-chunk gate sums and its last CTA runs the fix-up mode scan)?  Not with the single-launch schedules,
+// which the gate scan builds.
+bool prep_scans(const Layout &L, const gdn_shape *s) { return tc_forward(L, s) && !single_launch_sp(L, s); }
+
+// plan + gate scan (gate sums to `gsum`), shared by both directions; `scan` false leaves the gate sums and
+// the fix-up modes to the chunk-local half (prep_scans)
+int prologue(const gdn_shape *s, const Layout &L, char *ws, const float *g, float *gsum, bool scan, cudaStream_t st,
+             Plan &pl) {
   pl = plan_of(L, ws);
   int *status = reinterpret_cast<int *>(ws + L.off_status);  // [0] status word, [1]/[2] fix-up flags
   const bool single = single_launch_sp(L, s);
@@ -413,12 +427,26 @@ int prologue(const gdn_shape *s, const Layout &L, char *ws, const float *g, cuda
     CK(launch_plan(pl, s->cu_seqlens, L.N, s->cu_seqlens ? s->T : L.Tseq, L.Lseg, L.S_max, L.CH_max, status,
                    single ? reinterpret_cast<int *>(ws + L.off_sched) : nullptr, L.sched_zero, st));
   }
-  {
+  if (scan) {
     PROF("gate_scan");
     const Sched sc[2] = {sched_of(L, ws, 0), sched_of(L, ws, 1)};
-    CK(launch_gate_scan(pl, g, L.H, L.CH_max, reinterpret_cast<float *>(ws + L.off_gsum), status, L.sp ? 1 : 0,
-                        L.Lseg, L.S_max, s->flags, single ? sc : nullptr, L.N * L.H, st));
+    CK(launch_gate_scan(pl, g, L.H, L.CH_max, gsum, status, L.sp ? 1 : 0, L.Lseg, L.S_max, s->flags,
+                        single ? sc : nullptr, L.N * L.H, st));
   }
+  return GDN_OK;
+}
+
+// The saved-context backward's prologue: the plan kernel alone, which also runs the fix-up mode scan (and
+// builds the schedules) from the gate sums that the forward left in the saved context.
+int prologue_saved(const gdn_shape *s, const Layout &L, char *ws, const float *gsum, cudaStream_t st, Plan &pl) {
+  pl = plan_of(L, ws);
+  int *status = reinterpret_cast<int *>(ws + L.off_status);
+  const bool single = single_launch_sp(L, s);
+  const Sched sc[2] = {sched_of(L, ws, 0), sched_of(L, ws, 1)};
+  PROF("plan");
+  CK(launch_plan(pl, s->cu_seqlens, L.N, s->cu_seqlens ? s->T : L.Tseq, L.Lseg, L.S_max, L.CH_max, status,
+                 single ? reinterpret_cast<int *>(ws + L.off_sched) : nullptr, L.sched_zero, st, gsum, L.H,
+                 L.sp ? 1 : 0, s->flags, single ? sc : nullptr));
   return GDN_OK;
 }
 
@@ -500,11 +528,6 @@ int dut_map(CUtensorMap *m, const Layout &L, const void *ptr) {
   return tile_map(m, ptr, (long)L.CH_max * L.H * TC_TILES * 128, 128);
 }
 
-// The chunk forward kernel for this problem: tcgen05 for bf16 with d = 128 (its recurrent half, on the
-// context that the chunk-local half stored), the mma.sync/CUDA-core kernel otherwise (d = 64, fp32
-// inputs, empty batches).
-bool tc_forward(const Layout &L, const gdn_shape *s) { return s->dtype == GDN_BF16 && L.D == 128 && L.Ttot > 0; }
-
 int launch_forward_kernel(const Layout &L, const gdn_shape *s, const FwdArgs &fa, dim3 grid, cudaStream_t st) {
   if (tc_forward(L, s)) {
     CUtensorMap t3, tw, ts, tt, to;
@@ -572,11 +595,17 @@ int forward_passes(const gdn_shape *s, const Layout &L, char *ws, FwdArgs fa, in
   return GDN_OK;
 }
 
-FwdArgs fwd_args(const gdn_shape *s, const Layout &L, char *ws, const Plan &pl) {
+// prep: the chunk-local half writes the gate sums to gsum and scans the fix-up modes (prep_scans)
+FwdArgs fwd_args(const gdn_shape *s, const Layout &L, char *ws, const Plan &pl, float *gsum, bool prep) {
   FwdArgs fa;
   std::memset(&fa, 0, sizeof fa);
   fa.plan = pl;
-  fa.gsum = reinterpret_cast<const float *>(ws + L.off_gsum);
+  fa.gsum = gsum;
+  if (prep) {
+    fa.gsum_out = gsum;
+    fa.modes = L.sp ? 1 : 0;
+    fa.S_max = L.S_max;
+  }
   fa.status = reinterpret_cast<int *>(ws + L.off_status);
   if (L.sp) {
     fa.Ebuf = reinterpret_cast<float *>(ws + L.off_E);
@@ -613,9 +642,13 @@ int fwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   char *ws = static_cast<char *>(workspace);
+  // the gate sums go with the saved context, for the saved-context backward
+  float *gsum = saved ? reinterpret_cast<float *>(static_cast<char *>(saved) + L.saved_off_gsum)
+                      : reinterpret_cast<float *>(ws + L.off_gsum);
+  const bool prep = prep_scans(L, s);
   Plan pl;
-  if ((rc = prologue(s, L, ws, g, st, pl))) return rc;
-  FwdArgs fa = fwd_args(s, L, ws, pl);
+  if ((rc = prologue(s, L, ws, g, gsum, !prep, st, pl))) return rc;
+  FwdArgs fa = fwd_args(s, L, ws, pl, gsum, prep);
   fa.q = q;
   fa.k = k;
   fa.v = v;
@@ -666,7 +699,15 @@ int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
   char *ws = static_cast<char *>(workspace);
   const bool bf = s->dtype == GDN_BF16;
   Plan pl;
-  if ((rc = prologue(s, L, ws, g, st, pl))) return rc;
+  // the saved-context backward takes the forward's gate sums; the recomputing one forms them again (with its
+  // forward's chunk-local half where that runs)
+  float *gsum = saved ? reinterpret_cast<float *>(const_cast<char *>(static_cast<const char *>(saved)) +
+                                                  L.saved_off_gsum)
+                      : reinterpret_cast<float *>(ws + L.off_gsum);
+  const bool prep = !saved && prep_scans(L, s);
+  if (saved) rc = prologue_saved(s, L, ws, gsum, st, pl);
+  else rc = prologue(s, L, ws, g, gsum, !prep, st, pl);
+  if (rc) return rc;
   const char *states = ws + L.off_states, *t64 = ws + L.off_t64, *t128 = ws + L.off_t128;
   const char *tqkv = ws + L.off_tqkv, *nrm = ws + L.off_nrm;
   if (saved) {  // the forward left the chunk-start states and context tiles: nothing to recompute
@@ -678,7 +719,7 @@ int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
   } else {
     // 1. forward states at every chunk start (and, bf16 with d = 128, the context tiles: a forward
     //    pass that writes no output)
-    FwdArgs fa = fwd_args(s, L, ws, pl);
+    FwdArgs fa = fwd_args(s, L, ws, pl, gsum, prep);
     fa.q = q;
     fa.k = k;
     fa.v = v;
@@ -712,7 +753,7 @@ int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
   ba.dbeta = dbeta;
   ba.dS0 = dS0;
   ba.plan = pl;
-  ba.gsum = reinterpret_cast<const float *>(ws + L.off_gsum);
+  ba.gsum = gsum;
   ba.status = reinterpret_cast<int *>(ws + L.off_status);
   if (L.sp) {
     ba.Fbuf = reinterpret_cast<float *>(ws + L.off_F);

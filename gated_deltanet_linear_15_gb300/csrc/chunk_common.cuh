@@ -98,6 +98,7 @@ struct __align__(16) Gates {
   float Ghi[CH], Glo[CH];
   float gam[CH], gp[CH], rgp[CH], cdec[CH];
   float gamC;  // exp(G_last)
+  float Glog;  // G_last, the chunk's summed log-gates
   int pw;      // nonzero: take decay ratios pairwise (the span leaves the factoring range)
 };
 
@@ -187,7 +188,10 @@ __device__ __forceinline__ bool gate_prefix_part(float ga, float gb, Gates &gt, 
     gt.gp[lane] = expf(da);
     gt.rgp[lane] = expf(-da);
     gt.cdec[lane] = expf(two_diff(Gl, Gll, a, al));
-    if (lane == 0) gt.gamC = expf(Gl + Gll);
+    if (lane == 0) {
+      gt.gamC = expf(Gl + Gll);
+      gt.Glog = Gl + Gll;
+    }
   }
   if (halves & 2) {
     gt.Ghi[lane + 32] = b;

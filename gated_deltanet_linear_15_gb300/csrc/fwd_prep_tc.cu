@@ -16,6 +16,7 @@
 // each loading its next item's inputs while it finishes the current one.
 #include "chunk_common.cuh"
 #include "kernels.h"
+#include "modes.cuh"
 #include "umma.cuh"
 
 namespace gdn {
@@ -238,7 +239,10 @@ __global__ void __launch_bounds__(PT, 2)
     __syncwarp();
     // under the Gram product: this item's gate prefix sums (warp 7; the read-out of P is their first
     // reader), the next item's plan look-ups and its g, beta (kept in registers until the product is done)
-    if (warp == PT / 32 - 1) gate_prefix(sm.g[gbuf], sm.gt[gbuf]);
+    if (warp == PT / 32 - 1) {
+      gate_prefix(sm.g[gbuf], sm.gt[gbuf]);
+      if (lane == 0 && a.gsum_out) a.gsum_out[item] = sm.gt[gbuf].Glog;  // this lane wrote Glog
+    }
     const ItemInfo nxt = info_of(next_valid(item + gridDim.x));
     float gnext = 0.f;
     if (tid < 2 * CH && nxt.item < n_items) {
@@ -329,6 +333,21 @@ __global__ void __launch_bounds__(PT, 2)
   __syncthreads();
   fence_after();
   if (warp == 0) tmem_dealloc(tm, 64);
+  if (a.modes && a.gsum_out && a.status) {
+    // the last CTA to finish (status[3] counts them; the plan kernel zeroed it) runs the fix-up mode scan
+    // over every CTA's gate sums, which each CTA made visible before counting itself
+    __shared__ int last;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) last = atomicAdd(a.status + 3, 1) == (int)gridDim.x - 1;
+    __syncthreads();
+    if (last) {
+      __threadfence();
+      Sched none;
+      memset(&none, 0, sizeof none);
+      fixup_modes(a.plan, a.gsum_out, H, a.Lseg, a.S_max, a.flags, a.status, tid, PT, none, none, 0);
+    }
+  }
 }
 
 size_t fwd_prep_tc_smem_bytes() { return sizeof(PrepSmem) + 1024; }

@@ -44,6 +44,10 @@ struct FwdArgs {
   float scale;
   unsigned flags;
   int pass;  // 0: segment end states / transitions, 1: outputs (+ saves if set), 2: states only
+  // bf16 with d = 128, in place of the gate scan: the chunk-local half writes the per-chunk gate sums to
+  // gsum_out (when set) and, with modes, its last CTA runs the fix-up mode scan over the S_max segments
+  float *gsum_out;
+  int modes, S_max;
   // bf16 with d = 128: the chunk context, see T64_*, T128_*, TQ_*.  t64 and tqkv are always set: the
   // chunk-local half writes them and the recurrent half reads them.  t128 and nrm are set when the
   // context is kept for the backward (then the chunk-local half also writes Ahat, N and the norms, and
@@ -111,9 +115,12 @@ struct RecArgs {
   unsigned flags;
 };
 
-// zero: `nzero` ints cleared with the status words (the schedules' counters), or NULL
+// zero: `nzero` ints cleared with the status words (the schedules' counters), or NULL.  With gsum and modes
+// set (the saved-context backward, which takes the forward's gate sums) the plan kernel also runs the fix-up
+// mode scan and builds the schedules in sched[0] / sched[1] (hdr NULL: none) instead of the gate scan.
 int launch_plan(const Plan &p, const int *cu, int N, int T, int Lseg, int S_max, int CH_max, int *status, int *zero,
-                int nzero, cudaStream_t st);
+                int nzero, cudaStream_t st, const float *gsum = nullptr, int H = 0, int modes = 0,
+                unsigned flags = 0, const Sched *sched = nullptr);
 // sched[0] / sched[1]: forward / reverse schedules to build (hdr NULL: none)
 int launch_gate_scan(const Plan &p, const float *g, int H, int CH_max, float *gsum, int *status, int modes, int Lseg,
                      int S_max, unsigned flags, const Sched *sched, int NH, cudaStream_t st);

@@ -15,14 +15,18 @@
 // state are independent in this composition, so CTAs split the rows.
 #include "fixup.cuh"
 #include "kernels.h"
+#include "modes.cuh"
 
 namespace gdn {
 
 // One block.  Builds the per-sequence and per-segment tables; a malformed
 // cu_seqlens (not starting at 0, decreasing, or not ending at T) sets status
 // bit 1 and leaves every sequence empty, so the chunk kernels do nothing.
+// Given the gate sums of a call whose forward computed them (modes != 0,
+// gsum set), it also runs the fix-up mode scan over the tables it built.
 __global__ void plan_kernel(Plan p, const int *cu, int N, int T, int Lseg, int S_max, int CH_max, int *status,
-                            int *zero, int nzero) {
+                            int *zero, int nzero, const float *gsum, int H, int modes, unsigned flags, Sched fs,
+                            Sched bs) {
   pdl_trigger();
   pdl_wait();
   __shared__ int carry_c, carry_s, bad;
@@ -135,21 +139,23 @@ __global__ void plan_kernel(Plan p, const int *cu, int N, int T, int Lseg, int S
     }
     p.seg_seq[s] = owner;
   }
+  if (!modes || !gsum) return;
+  __syncthreads();  // the tables above, the zeroed status words and counters
+  fixup_modes(p, gsum, H, Lseg, S_max, flags, status, tid, nt, fs, bs, N * H);
 }
 
 int launch_plan(const Plan &p, const int *cu, int N, int T, int Lseg, int S_max, int CH_max, int *status, int *zero,
-                int nzero, cudaStream_t st) {
+                int nzero, cudaStream_t st, const float *gsum, int H, int modes, unsigned flags, const Sched *sched) {
+  Sched none;
+  memset(&none, 0, sizeof none);
   return (int)launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, st, p, cu, N, T, Lseg, S_max, CH_max, status, zero,
-                         zero ? nzero : 0);
+                         zero ? nzero : 0, gsum, H, modes, flags, sched ? sched[0] : none, sched ? sched[1] : none);
 }
 
 // One block per global chunk: the chunk's log-gates of 32 heads at a time are
 // staged in shared memory with coalesced row loads (tokens are rows of H gates),
 // then one warp per head scans its 64 values: gsum[c, h] = sum of g over the
 // chunk's tokens (each g raised to GATE_FLOOR first, as in the chunk kernels).
-__device__ void fixup_modes(const Plan &p, const float *gsum, int H, int Lseg, int S_max, unsigned flags, int *status,
-                            int i0, int stride, Sched fs, Sched bs, int NH);
-
 // With modes != 0 (a call with segments) the last block to finish also runs the fix-up mode scan
 // over every (segment, head) (status[3] counts finished blocks; the plan kernel zeroed it).
 __global__ void __launch_bounds__(256) gate_scan_kernel(Plan p, const float *g, int H, float *gsum, int *status,
@@ -207,87 +213,6 @@ int launch_gate_scan(const Plan &p, const float *g, int H, int CH_max, float *gs
   memset(&none, 0, sizeof none);
   return (int)launch_pdl(gate_scan_kernel, dim3(CH_max), dim3(256), 0, st, p, g, H, gsum, status, modes, Lseg, S_max,
                          flags, sched ? sched[0] : none, sched ? sched[1] : none, NH);
-}
-
-// Does any segment start (forward) or end (reverse) need the exact fix-up?  status[1] / status[2]
-// become nonzero if so; the pass-A launches and the fix-ups of a direction without any such segment
-// return at once.  With schedules (fs.hdr / bs.hdr set) it also builds each direction's work lists of
-// the single-launch sequence parallelism (see Sched): pass A of segment j is needed when the start of
-// segment j + 1 (forward; the end of segment j - 1 reversed) takes the fix-up, with the transition role
-// too when segment j's own start (end) does.  (segment, head) pairs i0, i0 + stride, ...; gsum read
-// through L2 (other blocks wrote it in this launch).  Called by one block, which synchronises itself.
-__device__ __forceinline__ bool window_ok(const float *gsum, int H, int h, int chunk0, int first, int count) {
-  // the start-mode rule of the chunk kernels (fwd_start_mode / bwd_start_mode) on L2-coherent loads:
-  // some w <= min(WMAX, count) with sum_{chunks first - w + 1 .. first} (forward) <= ln eps; the caller
-  // passes the chunks in scan order through `first` and the direction through the sign of count
-  float gs[WMAX];
-  const int n = count < 0 ? -count : count;
-#pragma unroll
-  for (int ww = 1; ww <= WMAX; ++ww) {
-    const int c = count < 0 ? first + ww - 1 : first - ww;
-    gs[ww - 1] = ww <= n ? __ldcg(gsum + (size_t)(chunk0 + c) * H + h) : 0.f;
-  }
-  float acc = 0.f;
-  bool warm = false;
-#pragma unroll
-  for (int ww = 1; ww <= WMAX; ++ww) {
-    acc += gs[ww - 1];
-    warm |= ww <= n && acc <= LN_EPS_WINDOW;
-  }
-  return warm;
-}
-
-__device__ void fixup_modes(const Plan &p, const float *gsum, int H, int Lseg, int S_max, unsigned flags, int *status,
-                            int i0, int stride, Sched fs, Sched bs, int NH) {
-  const bool window = !(flags & kFlagWindowOff);
-  bool fwd_fix = false, bwd_fix = false;
-  // forward start of segment j needs the fix-up (j > 0 and no certified warm-up)
-  auto ffix = [&](int j, int chunk0, int h) { return j > 0 && !(window && window_ok(gsum, H, h, chunk0, j * Lseg, j * Lseg)); };
-  // reverse end of segment j needs the fix-up (j < nseg - 1 and no certified warm-up after it)
-  auto bfix = [&](int j, int nseg, int nchunks, int chunk0, int h) {
-    const int cend = min((j + 1) * Lseg, nchunks);
-    return j < nseg - 1 && !(window && window_ok(gsum, H, h, chunk0, cend, -(nchunks - cend)));
-  };
-  auto push = [](Sched &sc, int k, int v) {
-    int *list = k == 0 ? sc.listA : (k == 1 ? sc.listBn : sc.listBf);
-    list[atomicAdd(sc.hdr + 1 + (k == 0 ? 0 : (k == 1 ? 1 : 3)), 1)] = v;
-  };
-  for (int i = i0; i < S_max * H; i += stride) {
-    const int s = i / H, h = i % H;
-    const int n = __ldcg(p.seg_seq + s);
-    if (n < 0) continue;
-    const int j = s - __ldcg(p.seq_seg0 + n), nseg = __ldcg(p.seq_nseg + n), chunk0 = __ldcg(p.seq_chunk0 + n);
-    const int nchunks = (__ldcg(p.seq_len + n) + CH - 1) / CH;
-    const bool fj = ffix(j, chunk0, h), bj = bfix(j, nseg, nchunks, chunk0, h);
-    fwd_fix |= fj;
-    bwd_fix |= bj;
-    const int pair = n * H + h, sh = s * H + h;
-    if (fs.hdr) {
-      if (j < nseg - 1 && ffix(j + 1, chunk0, h)) {
-        push(fs, 0, sh * 2);
-        if (fj) push(fs, 0, sh * 2 + 1);
-        atomicAdd(fs.needA + pair, fj ? 2 : 1);
-      }
-      push(fs, fj ? 2 : 1, sh);
-    }
-    if (bs.hdr) {
-      if (j > 0 && bfix(j - 1, nseg, nchunks, chunk0, h)) {
-        push(bs, 0, sh * 2);
-        if (bj) push(bs, 0, sh * 2 + 1);
-        atomicAdd(bs.needA + pair, bj ? 2 : 1);
-      }
-      push(bs, bj ? 2 : 1, sh);
-    }
-  }
-  if (fwd_fix) atomicOr(status + 1, 1);
-  if (bwd_fix) atomicOr(status + 2, 1);
-  if (!fs.hdr && !bs.hdr) return;
-  __syncthreads();
-  // fix-up row blocks: every (sequence, head) with a pass-A item
-  for (int pair = i0; pair < NH; pair += stride) {
-    if (fs.hdr && __ldcg(fs.needA + pair) > 0) fs.listF[atomicAdd(fs.hdr + 3, 1)] = pair;
-    if (bs.hdr && __ldcg(bs.needA + pair) > 0) bs.listF[atomicAdd(bs.hdr + 3, 1)] = pair;
-  }
 }
 
 // grid (D / FIX_ROWS, H, N), 256 threads: one fix-up row block per CTA (see fixup_rows)

@@ -195,8 +195,10 @@ int gdn_chunk_bwd(const gdn_shape *shape,
  * gamma) and Ut^T = U^T - S0 W^T; the fp16 operand tiles [chunks, H, 3, 64,
  * 128] of K, Q (normalised, Q scaled) and V; fp32 [chunks, H, 2, 64]
  * reciprocal norms 1/|k|, 1/|q| (onedev.kr FlashQLA talk summary, paragraph
- * on the WY representation, which names these intra-chunk quantities).  The
- * backward then starts at the reverse chain.  This trades memory for time
+ * on the WY representation, which names these intra-chunk quantities).  Last,
+ * for every dtype and d, the fp32 sum of g over each chunk [chunks, H] (the
+ * gate scan's result, from which the backward decides its segment warm-ups
+ * without reading g again).  The backward then starts at the reverse chain.  This trades memory for time
  * (d = 128, bf16: 152.5 KB per chunk and head, 640 MB for 32 heads x 8192
  * tokens); the chunked algorithm as published recomputes these in the
  * backward instead, and gdn_chunk_bwd keeps that form.

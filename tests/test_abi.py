@@ -107,18 +107,20 @@ def test_workspace_checks(lib):
 def test_saved_context_sizes(lib):
     """Saved context = fp16 chunk-start states + five fp16 64 x 64 tiles (X1, X2, Ahat, P, N) + two
     fp16 128 x 64 tiles (scaled W^T, Ut^T) + three fp16 64 x 128 operand tiles (K, Q, V) + 2 x 64 fp32
-    reciprocal norms per (chunk, head) at bf16, d = 128; the saved-context backward needs the
-    recompute workspace minus exactly that."""
+    reciprocal norms per (chunk, head) at bf16, d = 128, then the fp32 gate sum of every (chunk, head)
+    (a 256-byte aligned region); the saved-context backward needs the recompute workspace minus
+    exactly the states and tiles (the gate sums replace no workspace region)."""
     s = _shape(T=1000, H=3)
     chunks = (1000 + 63) // 64
+    gsum = (chunks * 3 * 4 + 255) // 256 * 256
     states = chunks * 3 * 128 * 128 * 2
     tiles = chunks * 3 * ((5 * 64 * 64 + 2 * 128 * 64 + 3 * 64 * 128) * 2 + 2 * 64 * 4)
-    assert lib.gdn_saved_size(ctypes.byref(s)) == states + tiles
+    assert lib.gdn_saved_size(ctypes.byref(s)) == states + tiles + gsum
     full = lib.gdn_bwd_workspace_size(ctypes.byref(s))
     assert lib.gdn_bwd_saved_workspace_size(ctypes.byref(s)) == full - states - tiles
     # fp32, d = 64: fp32 states, no WY tiles
     s = _shape(T=1000, H=3, Dk=64, Dv=64, dtype=_lib.GDN_FP32)
-    assert lib.gdn_saved_size(ctypes.byref(s)) == chunks * 3 * 64 * 64 * 4
+    assert lib.gdn_saved_size(ctypes.byref(s)) == chunks * 3 * 64 * 64 * 4 + gsum
     assert lib.gdn_saved_size(ctypes.byref(_shape(Dk=96, Dv=96))) == 0
 
 
