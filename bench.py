@@ -220,8 +220,9 @@ def run_reference(args):
 # ----------------------------------------------------------------------------- segment-length sweep
 def run_sweep(args, g, x, dev):
     """Saved-context fwd + bwd timed per segment length (CUDA events around each call, 256 MB L2 flush
-    before every step, outside the events), with the per-kernel table of one profiled pass and the
-    library's own estimate for the plan (gdn_plan_estimate).  One JSON line per length."""
+    before every step, outside the events), with the mean time of the two recurrent passes (each
+    bracketed alone over K further steps) and the library's own estimate for the plan
+    (gdn_plan_estimate).  One JSON line per plan."""
     import torch
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -234,9 +235,10 @@ def run_sweep(args, g, x, dev):
     clocks = ClockSampler(dev.index or 0)
     clocks.start()
     time.sleep(0.3)
-    for L in [int(v) for v in args.sweep_seg_chunks.split(",")]:
+    for spec in args.sweep_seg_chunks.split(","):
+        L, F = (int(v) for v in spec.split(":")) if ":" in spec else (int(spec), 0)
         shape = g.make_shape(x["q"], x["v"], cu_seqlens=x["cu_seqlens"], scale=x["scale"], l2norm=x["l2norm"],
-                             seg_chunks=L)
+                             seg_chunks=L, seg_first=F)
         plan = g.gdn_plan_query(shape)
         est = g.gdn_plan_estimate(shape)
         ws_bytes = max(g.gdn_fwd_workspace_size(shape), g.gdn_bwd_saved_workspace_size(shape))
@@ -258,15 +260,20 @@ def run_sweep(args, g, x, dev):
             flush.zero_()
             fwd()
             bwd()
-        g.gdn_profile_report(reset=True)
+        # the recurrent passes, each bracketed alone (the other launches keep their overlap) over K steps
+        kern = {}
+        for name in ("fwd_chunk", "bwd_chain"):
+            g.gdn_profile_report(reset=True)
+            g.gdn_profile_only(name)
+            g.gdn_profile_enable(True)
+            for _ in range(args.steps):
+                flush.zero_()
+                fwd()
+                bwd()
+            torch.cuda.synchronize()
+            g.gdn_profile_enable(False)
+            kern.update(g.gdn_profile_report(reset=True))
         g.gdn_profile_only(None)
-        g.gdn_profile_enable(True)
-        flush.zero_()
-        fwd()
-        bwd()
-        torch.cuda.synchronize()
-        g.gdn_profile_enable(False)
-        kern = g.gdn_profile_report(reset=True)
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
         torch.cuda.synchronize()
         for e in evs:
@@ -279,7 +286,8 @@ def run_sweep(args, g, x, dev):
         torch.cuda.synchronize()
         fwd_ms = statistics.median(a.elapsed_time(b) for a, b, c in evs)
         bwd_ms = statistics.median(b.elapsed_time(c) for a, b, c in evs)
-        print(json.dumps({"sweep": args.workload, "seg_chunks_requested": L, "seg_chunks": plan["seg_chunks"],
+        print(json.dumps({"sweep": args.workload, "seg_chunks_requested": L, "seg_first": F,
+                          "seg_chunks": plan["seg_chunks"],
                           "max_segments": plan["max_segments"], "fwd_ms": round(fwd_ms, 4),
                           "bwd_ms": round(bwd_ms, 4), "step_ms": round(fwd_ms + bwd_ms, 4),
                           "estimate_us": est,
@@ -360,8 +368,9 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=None, help="tokens per sequence in the reference sample")
     ap.add_argument("--seg-chunks", type=int, default=0)
     ap.add_argument("--sweep-seg-chunks", default="",
-                    help="comma-separated segment lengths (0 = the automatic plan): time the saved-context pair "
-                         "for each and print one JSON line per length instead of the bench line")
+                    help="comma-separated segment lengths L or L:F (F = the first segment's length; 0 = the "
+                         "automatic plan): time the saved-context pair for each and print one JSON line per "
+                         "plan instead of the bench line")
     ap.add_argument("--recompute", action="store_true",
                     help="time the stateless pair (the backward recomputes the chunk states and WY tiles) "
                          "instead of the saved-context pair")

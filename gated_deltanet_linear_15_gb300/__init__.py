@@ -58,7 +58,7 @@ def _check(rc: int, what: str):
 
 def make_shape(q: torch.Tensor, v: torch.Tensor, *, cu_seqlens: Optional[torch.Tensor] = None,
                scale: Optional[float] = None, l2norm: bool = False, sp: bool = True, window: bool = True,
-               seg_chunks: int = 0, single_launch: bool = False) -> GdnShape:
+               seg_chunks: int = 0, single_launch: bool = False, seg_first: int = 0) -> GdnShape:
     B, T, H, Dk = q.shape
     s = GdnShape()
     s.B, s.T, s.H, s.Dk, s.Dv = B, T, H, Dk, v.shape[-1]
@@ -70,6 +70,7 @@ def make_shape(q: torch.Tensor, v: torch.Tensor, *, cu_seqlens: Optional[torch.T
     s.flags = (GDN_L2NORM_QK if l2norm else 0) | (0 if sp else GDN_SP_OFF) | (0 if window else GDN_WINDOW_OFF) | \
         (_lib.GDN_SP_SINGLE_LAUNCH if single_launch else 0)
     s.seg_chunks = int(seg_chunks)
+    s.seg_first = int(seg_first)
     return s
 
 
@@ -83,10 +84,10 @@ def gdn_bwd_workspace_size(shape: GdnShape) -> int:
 
 
 def gdn_plan_query(shape: GdnShape):
-    a, b, c = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
-    _check(_lib.load().gdn_plan_query(ctypes.byref(shape), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)),
-           "gdn_plan_query")
-    return dict(seg_chunks=a.value, max_segments=b.value, max_chunks=c.value)
+    a, b, c, f = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(_lib.load().gdn_plan_query(ctypes.byref(shape), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c),
+                                      ctypes.byref(f)), "gdn_plan_query")
+    return dict(seg_chunks=a.value, max_segments=b.value, max_chunks=c.value, seg_first=f.value)
 
 
 def gdn_plan_estimate(shape: GdnShape):
@@ -202,12 +203,12 @@ def _contig(*ts):
 
 def chunk_gated_delta_rule_fwd(q, k, v, g, beta, initial_state=None, output_final_state=True, cu_seqlens=None,
                                scale=None, use_qk_l2norm_in_kernel=False, sp=True, window=True, seg_chunks=0,
-                               workspace=None, save_context=False, single_launch=False):
+                               workspace=None, save_context=False, single_launch=False, seg_first=0):
     """o, S_T (S_T None unless output_final_state); with save_context=True also the saved
     context (a uint8 tensor) to pass to chunk_gated_delta_rule_bwd(saved=...)."""
     _contig(q, k, v, g, beta, initial_state)
     shape = make_shape(q, v, cu_seqlens=cu_seqlens, scale=scale, l2norm=use_qk_l2norm_in_kernel, sp=sp,
-                       window=window, seg_chunks=seg_chunks, single_launch=single_launch)
+                       window=window, seg_chunks=seg_chunks, single_launch=single_launch, seg_first=seg_first)
     N = shape.num_seqs if cu_seqlens is not None else q.shape[0]
     o = torch.empty_like(v)
     S_T = torch.empty(N, q.shape[2], v.shape[-1], q.shape[-1], dtype=torch.float32, device=q.device) \
@@ -245,12 +246,12 @@ def recurrent_gated_delta_rule(q, k, v, g, beta, initial_state=None, scale=None,
 
 def chunk_gated_delta_rule_bwd(q, k, v, g, beta, dO, initial_state=None, dS_T=None, cu_seqlens=None, scale=None,
                                use_qk_l2norm_in_kernel=False, sp=True, window=True, seg_chunks=0, workspace=None,
-                               saved=None, single_launch=False):
+                               saved=None, single_launch=False, seg_first=0):
     """dq, dk, dv, dg, dbeta, dS0 (dS0 None without an initial state).  `saved`: the context
     that chunk_gated_delta_rule_fwd(save_context=True) returned for these same inputs."""
     _contig(q, k, v, g, beta, dO, initial_state, dS_T)
     shape = make_shape(q, v, cu_seqlens=cu_seqlens, scale=scale, l2norm=use_qk_l2norm_in_kernel, sp=sp,
-                       window=window, seg_chunks=seg_chunks, single_launch=single_launch)
+                       window=window, seg_chunks=seg_chunks, single_launch=single_launch, seg_first=seg_first)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dg, db = torch.empty_like(g), torch.empty_like(beta)
     dS0 = torch.empty_like(initial_state) if initial_state is not None else None

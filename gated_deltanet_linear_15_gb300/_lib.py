@@ -28,7 +28,8 @@ class GdnShape(ctypes.Structure):
                 ("Dk", ctypes.c_int), ("Dv", ctypes.c_int),
                 ("cu_seqlens", ctypes.c_void_p), ("num_seqs", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("scale", ctypes.c_float), ("flags", ctypes.c_uint),
-                ("seg_chunks", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
+                ("seg_chunks", ctypes.c_int), ("seg_first", ctypes.c_int),
+                ("reserved", ctypes.c_int * 2)]
 
 
 _lock = threading.Lock()
@@ -77,7 +78,7 @@ def load():
         lib.gdn_device_status_code.argtypes = [ctypes.c_int]
         lib.gdn_device_status_code.restype = ctypes.c_int
         lib.gdn_plan_query.argtypes = [S, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
-                                       ctypes.POINTER(ctypes.c_int)]
+                                       ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
         lib.gdn_plan_query.restype = ctypes.c_int
         lib.gdn_plan_estimate.argtypes = [S, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
         lib.gdn_plan_estimate.restype = ctypes.c_int

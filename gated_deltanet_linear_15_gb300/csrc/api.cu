@@ -50,7 +50,7 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 struct Layout {
   int N = 0, H = 0, D = 0, Tseq = 0;  // Tseq: per-sequence length for uniform batches, 0 for packed
   long Ttot = 0;
-  int CH_max = 0, S_max = 0, Lseg = 1;
+  int CH_max = 0, S_max = 0, Lseg = 1, Lfirst = 1;  // segment lengths in chunks: the first, then Lseg each
   bool sp = false;  // more than one segment possible for some sequence
   size_t esize = 2;
   size_t off_status = 0, off_plan = 0, off_gsum = 0;
@@ -71,91 +71,143 @@ struct Layout {
   size_t fwd_core = 0, fwd_total = 0, bwd_total = 0;
 };
 
+// Does a plan of S segments per sequence over nh equal-length (sequence, head) pairs run the recurrent
+// passes on the balanced grid (later segments one CTA each, the first segments sharing the other SMs)?
+bool balanced_plan(long nh, int S, long slots) { return S >= 2 && nh * S > slots && nh * (S - 1) < slots; }
+
 // Modelled time of the two recurrent passes (the forward's state pass and the backward's reverse
-// chain) for L chunks per segment.  One CTA per (segment, head) walks its chunks serially and holds a
-// whole SM, and the hardware starts the CTAs in launch order (segments of a head, heads in turn) on
-// whichever SM frees first, so the pass takes the makespan of that list on the SMs.  An item costs a
-// fixed part plus its chunks, plus kWarmChunks warm-up chunks for a segment that does not start its
-// sequence (the window case of the gate scan; the exact case adds a pass A that the host cannot
-// foresee, since it depends on the gates).  The constants are a least-squares fit to GB300 timings of
-// the tcgen05 kernels over 23 segment lengths of the H = 32, T = 8192 prefill (bench.py
-// --sweep-seg-chunks: within 4 % of every measured length); the d = 64 and fp32 kernels are costed the
-// same way.  Packed batches, whose lengths the host does not see, are costed in whole waves of an
-// average item.
+// chain) for a first segment of F chunks and later ones of L.  One CTA per (segment, head) walks its
+// chunks serially and holds a whole SM; the hardware starts the CTAs in launch order (segments of a
+// head, heads in turn) on whichever SM frees first, so the pass takes the makespan of that list on the
+// SMs.  A segment costs a fixed part plus its chunks, plus kWarmChunks warm-up chunks where it does not
+// start (forward) or end (reverse) its sequence (the window case of the gate scan; the exact case adds a
+// pass A that the host cannot foresee, since it depends on the gates).  On the balanced grid the pass
+// takes the longer of a later segment and the first segments of the most loaded shared CTA, each of
+// which pays the fixed part of an item that follows another in the same CTA.  The constants fit GB300
+// timings of the tcgen05 kernels (bench.py --sweep-seg-chunks over 21 plans of the H = 32, T = 8192
+// prefill and 12 of the B = 4, H = 16, T = 4096 batch: one segment length 8 .. 128 chunks and first
+// segments of 2 .. 20 chunks); the d = 64 and fp32 kernels are costed the same way.  Packed batches,
+// whose lengths the host does not see, are costed in whole waves of an average item.
 struct PassCost {
-  double item_us, chunk_us, warm_us;
+  double item_us, chunk_us, next_item_us;  // next_item_us: an item after another one in the same CTA
 };
-constexpr PassCost kFwdPass = {3.0, 4.95, 5.0}, kChainPass = {11.0, 4.0, 0.5};
+constexpr PassCost kFwdPass = {20.0, 3.2, 24.0}, kChainPass = {12.0, 2.9, 17.0};
 constexpr int kWarmChunks = 2;
 
-void plan_cost_us(const gdn_shape &s, int N, int maxc, int CH_max, int L, double *fwd_us, double *bwd_us) {
+bool tc_shape(const gdn_shape &s) { return s.dtype == GDN_BF16 && s.Dk == 128; }
+
+void plan_cost_us(const gdn_shape &s, int N, int maxc, int CH_max, int L, int F, double *fwd_us, double *bwd_us) {
   const int slots = num_sms();
   L = std::max(1, std::min(L, maxc));
-  const int S = (maxc + L - 1) / L;
-  const long items = s.cu_seqlens ? (long)std::ceil(s.H * ((double)CH_max / L + 0.5 * N)) : (long)N * s.H * S;
+  F = std::max(1, std::min(F, maxc));
+  const int S = seg_count(maxc, F, L);
+  const long nh = (long)N * s.H;
+  const long items = s.cu_seqlens ? (long)std::ceil(s.H * ((double)CH_max / L + 0.5 * N)) : nh * S;
   if (s.cu_seqlens || items > 16L * slots) {
     const double waves = std::ceil((double)items / slots);
-    const double warm = L < maxc ? kWarmChunks : 0.0;
-    *fwd_us = waves * (kFwdPass.item_us + L * kFwdPass.chunk_us + warm * kFwdPass.warm_us);
-    *bwd_us = waves * (kChainPass.item_us + L * kChainPass.chunk_us + warm * kChainPass.warm_us);
+    const double steps = L + (L < maxc ? kWarmChunks : 0);
+    *fwd_us = waves * (kFwdPass.item_us + steps * kFwdPass.chunk_us);
+    *bwd_us = waves * (kChainPass.item_us + steps * kChainPass.chunk_us);
     return;
   }
+  // chunk steps of segment j, its warm-up included
+  auto seg_len = [&](int j) { return std::min(seg_begin(j + 1, F, L), maxc) - seg_begin(j, F, L); };
+  auto steps = [&](int pass, int j) {
+    if (pass == 0) return seg_len(j) + (j ? std::min(kWarmChunks, seg_begin(j, F, L)) : 0);
+    const int cend = std::min(seg_begin(j + 1, F, L), maxc);
+    return seg_len(j) + (j < S - 1 ? std::min(kWarmChunks, maxc - cend) : 0);
+  };
   double out[2];
-  for (int pass = 0; pass < 2; ++pass) {
-    const PassCost &pc = pass ? kChainPass : kFwdPass;
-    std::vector<double> sm(std::min<long>(slots, items), 0.0);  // a min-heap of the SMs' free times
-    for (long i = 0; i < items; ++i) {
-      const int j = (int)(i % S);  // launch order: the segments of one (sequence, head), then the next
-      const int len = std::min(L, maxc - j * L), warm = j ? std::min(kWarmChunks, j * L) : 0;
-      const double d = pc.item_us + len * pc.chunk_us + warm * pc.warm_us;
-      if ((long)i < (long)sm.size()) {
-        sm[i] = d;
-        std::push_heap(sm.begin(), sm.begin() + i + 1, std::greater<double>());
-      } else {
-        std::pop_heap(sm.begin(), sm.end(), std::greater<double>());
-        sm.back() += d;
-        std::push_heap(sm.begin(), sm.end(), std::greater<double>());
-      }
+  if (tc_shape(s) && balanced_plan(nh, S, slots)) {
+    const long shared = slots - nh * (S - 1), per_cta = (nh + shared - 1) / shared;
+    for (int pass = 0; pass < 2; ++pass) {
+      const PassCost &pc = pass ? kChainPass : kFwdPass;
+      double big = 0.0;
+      for (int j = 1; j < S; ++j) big = std::max(big, pc.item_us + steps(pass, j) * pc.chunk_us);
+      out[pass] = std::max(big, per_cta * (pc.next_item_us + steps(pass, 0) * pc.chunk_us));
     }
-    out[pass] = *std::max_element(sm.begin(), sm.end());
+  } else {
+    for (int pass = 0; pass < 2; ++pass) {
+      const PassCost &pc = pass ? kChainPass : kFwdPass;
+      std::vector<double> sm(std::min<long>(slots, items), 0.0);  // a min-heap of the SMs' free times
+      for (long i = 0; i < items; ++i) {
+        const int j = (int)(i % S);  // launch order: the segments of one (sequence, head), then the next
+        const double d = pc.item_us + steps(pass, j) * pc.chunk_us;
+        if ((long)i < (long)sm.size()) {
+          sm[i] = d;
+          std::push_heap(sm.begin(), sm.begin() + i + 1, std::greater<double>());
+        } else {
+          std::pop_heap(sm.begin(), sm.end(), std::greater<double>());
+          sm.back() += d;
+          std::push_heap(sm.begin(), sm.end(), std::greater<double>());
+        }
+      }
+      out[pass] = *std::max_element(sm.begin(), sm.end());
+    }
   }
   *fwd_us = out[0];
   *bwd_us = out[1];
 }
 
-// Chunks per segment.  With few (sequence, head) pairs the sequences are split until the work items
-// fill the SMs (onedev.kr FlashQLA talk summary, paragraph on parallelism: one head per SM leaves most
-// of a >100-SM card idle); the length minimises the modelled time of the two recurrent passes over the
-// lengths that give each segment count its shortest longest segment, up to 16 waves of items.  Results
-// are cached per shape class (the plan is chosen on every call).
-int choose_lseg(const gdn_shape &s, int N, int maxc, int CH_max) {
-  if (maxc <= 0) return 1;
-  if (s.flags & GDN_SP_OFF) return maxc;
-  if (s.seg_chunks > 0) return s.seg_chunks;
+// Segment lengths: L chunks per segment after a first segment of F.  With few (sequence, head) pairs the
+// sequences are split until the work items fill the SMs (onedev.kr FlashQLA talk summary, paragraph on
+// parallelism: one head per SM leaves most of a >100-SM card idle); the plan minimises the modelled time
+// of the two recurrent passes over the lengths that give each segment count its shortest longest segment,
+// up to 16 waves of items, and, for the tcgen05 kernels on equal-length sequences, over the balanced plans
+// (a shorter first segment of at least min(WMAX, L) chunks, so that the next segment's warm-up is never cut
+// short by it).  Results are cached per shape class (the plan is chosen on every call).
+void choose_plan(const gdn_shape &s, int N, int maxc, int CH_max, int &L, int &F) {
+  L = F = std::max(1, maxc);
+  if (maxc <= 0) return;
+  if (s.flags & GDN_SP_OFF) return;
+  if (s.seg_chunks > 0) {
+    L = s.seg_chunks;
+    F = s.seg_first > 0 ? s.seg_first : L;
+    return;
+  }
   const int slots = num_sms();
-  if ((long)N * s.H >= slots) return maxc;
+  const long nh = (long)N * s.H;
+  if (nh >= slots) return;
   static std::mutex mu;
-  static std::vector<std::array<long, 6>> cache;  // {N, H, maxc, CH_max, packed, SMs}
-  static std::vector<int> cached;
-  const std::array<long, 6> key = {N, s.H, maxc, CH_max, s.cu_seqlens != nullptr, slots};
+  static std::vector<std::array<long, 7>> cache;  // {N, H, maxc, CH_max, packed, SMs, tcgen05}
+  static std::vector<std::pair<int, int>> cached;
+  const std::array<long, 7> key = {N, s.H, maxc, CH_max, s.cu_seqlens != nullptr, slots, tc_shape(s)};
   {
     std::lock_guard<std::mutex> lk(mu);
     for (size_t i = 0; i < cache.size(); ++i)
-      if (cache[i] == key) return cached[i];
+      if (cache[i] == key) {
+        L = cached[i].first;
+        F = cached[i].second;
+        return;
+      }
   }
-  int best = maxc;
+  int bestL = maxc, bestF = maxc;
   double best_cost = 1e300;
+  auto consider = [&](int l, int f) {
+    double fw, bw;
+    plan_cost_us(s, N, maxc, CH_max, l, f, &fw, &bw);
+    if (fw + bw < best_cost - 1e-9) {
+      best_cost = fw + bw;
+      bestL = l;
+      bestF = f;
+    }
+  };
   int prevL = 0;
   for (int S = 1; S <= maxc; ++S) {
-    const int L = (maxc + S - 1) / S;
-    if (L == prevL) continue;
-    prevL = L;
-    if ((long)N * s.H * S > 16L * slots) break;
-    double f, b;
-    plan_cost_us(s, N, maxc, CH_max, L, &f, &b);
-    if (f + b < best_cost - 1e-9) {
-      best_cost = f + b;
-      best = L;
+    const int l = (maxc + S - 1) / S;
+    if (l == prevL) continue;
+    prevL = l;
+    if (nh * S > 16L * slots) break;
+    consider(l, l);
+  }
+  if (!s.cu_seqlens && tc_shape(s)) {
+    for (int S = 2; S <= maxc && nh * (S - 1) < slots; ++S) {
+      if (!balanced_plan(nh, S, slots)) continue;
+      for (int f = 1; f < maxc; ++f) {
+        const int l = (maxc - f + S - 2) / (S - 1);
+        if (l < 1 || f < std::min(WMAX, l) || seg_count(maxc, f, l) != S) continue;
+        consider(l, f);
+      }
     }
   }
   std::lock_guard<std::mutex> lk(mu);
@@ -164,19 +216,22 @@ int choose_lseg(const gdn_shape &s, int N, int maxc, int CH_max) {
     cached.clear();
   }
   cache.push_back(key);
-  cached.push_back(best);
-  return best;
+  cached.push_back({bestL, bestF});
+  L = bestL;
+  F = bestF;
 }
 
 int make_layout(const gdn_shape *s, Layout &L) {
   if (!s) return fail(GDN_ERR_INVALID_ARG, "shape is NULL");
-  if (s->reserved[0] || s->reserved[1] || s->reserved[2]) return fail(GDN_ERR_INVALID_ARG, "reserved fields must be 0");
+  if (s->reserved[0] || s->reserved[1]) return fail(GDN_ERR_INVALID_ARG, "reserved fields must be 0");
   if (s->B < 1 || s->T < 0 || s->H < 1) return fail(GDN_ERR_INVALID_ARG, "need B >= 1, T >= 0, H >= 1");
   if (s->Dk != s->Dv) return fail(GDN_ERR_UNSUPPORTED, "d_k != d_v is not supported");
   if (s->Dk != 64 && s->Dk != 128) return fail(GDN_ERR_UNSUPPORTED, "d must be 64 or 128 (got %d)", s->Dk);
   if (s->dtype != GDN_BF16 && s->dtype != GDN_FP32) return fail(GDN_ERR_INVALID_ARG, "unknown dtype");
   if (s->dtype == GDN_FP32 && s->Dk != 64) return fail(GDN_ERR_UNSUPPORTED, "fp32 mode supports d = 64 only");
   if (s->seg_chunks < 0) return fail(GDN_ERR_INVALID_ARG, "seg_chunks must be >= 0");
+  if (s->seg_first < 0) return fail(GDN_ERR_INVALID_ARG, "seg_first must be >= 0");
+  if (s->seg_first > 0 && s->seg_chunks == 0) return fail(GDN_ERR_INVALID_ARG, "seg_first needs seg_chunks > 0");
   if (!std::isfinite(s->scale) || s->scale == 0.f) return fail(GDN_ERR_INVALID_ARG, "scale must be finite and non-zero");
   if (s->cu_seqlens) {
     if (s->B != 1) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens requires B == 1");
@@ -205,10 +260,11 @@ int make_layout(const gdn_shape *s, Layout &L) {
   if (s->dtype == GDN_BF16 && L.D == 128 && (long)L.CH_max * L.H * T64_TILES * CH > (long)INT32_MAX)
     return fail(GDN_ERR_UNSUPPORTED, "too many (chunk, head) pairs for the context tiles (%ld, at most %ld)",
                 (long)L.CH_max * L.H, (long)INT32_MAX / (T64_TILES * CH));
-  L.Lseg = std::max(1, choose_lseg(*s, L.N, maxc, L.CH_max));
+  choose_plan(*s, L.N, maxc, L.CH_max, L.Lseg, L.Lfirst);
+  // a sequence of nc chunks has at most 2 + nc / Lseg segments
   if (s->cu_seqlens) L.S_max = L.CH_max / L.Lseg + 2 * L.N + 1;
-  else L.S_max = L.N * std::max(1, (maxc + L.Lseg - 1) / L.Lseg);
-  L.sp = L.Lseg < maxc;
+  else L.S_max = L.N * seg_count(maxc, L.Lfirst, L.Lseg);
+  L.sp = std::min(L.Lfirst, L.Lseg) < maxc;
   const size_t DD = (size_t)L.D * L.D;
   const size_t nplan = 5 * (size_t)L.N + L.S_max + L.CH_max + 2;
   size_t off = 0;
@@ -410,6 +466,25 @@ void prof_drain_locked() {
 // inputs, empty batches).
 bool tc_forward(const Layout &L, const gdn_shape *s) { return s->dtype == GDN_BF16 && L.D == 128 && L.Ttot > 0; }
 
+// The grid of a tcgen05 recurrent pass (pass 1 / 2 of the forward, the reverse chain).  With equal-length
+// sequences whose later segments fit the SMs one CTA each while all segments do not, the later segments take
+// one CTA each and the shorter first segments share the remaining SMs, several to a CTA (bal_* in the
+// kernel arguments); otherwise one CTA per (segment, head).
+dim3 recurrent_grid(const Layout &L, const gdn_shape *s, int &bal_pairs, int &bal_ns, int &bal_big) {
+  bal_pairs = bal_ns = bal_big = 0;
+  const long slots = num_sms();
+  if (!s->cu_seqlens && L.N > 0 && L.S_max % L.N == 0) {
+    const long nh = (long)L.N * L.H, ns = L.S_max / L.N;
+    if (balanced_plan(nh, (int)ns, slots)) {
+      bal_pairs = (int)nh;
+      bal_ns = (int)ns;
+      bal_big = (int)(nh * (ns - 1));
+      return dim3((unsigned)slots);
+    }
+  }
+  return dim3(L.S_max, L.H, 1);
+}
+
 // Does the chunk-local half of the tcgen05 forward run in this call and take the gate scan's place (it writes
 // the per-chunk gate sums and its last CTA runs the fix-up mode scan)?  Not with the single-launch schedules,
 // which the gate scan builds.
@@ -424,13 +499,13 @@ int prologue(const gdn_shape *s, const Layout &L, char *ws, const float *g, floa
   const bool single = single_launch_sp(L, s);
   {
     PROF("plan");
-    CK(launch_plan(pl, s->cu_seqlens, L.N, s->cu_seqlens ? s->T : L.Tseq, L.Lseg, L.S_max, L.CH_max, status,
+    CK(launch_plan(pl, s->cu_seqlens, L.N, s->cu_seqlens ? s->T : L.Tseq, L.Lseg, L.Lfirst, L.S_max, L.CH_max, status,
                    single ? reinterpret_cast<int *>(ws + L.off_sched) : nullptr, L.sched_zero, st));
   }
   if (scan) {
     PROF("gate_scan");
     const Sched sc[2] = {sched_of(L, ws, 0), sched_of(L, ws, 1)};
-    CK(launch_gate_scan(pl, g, L.H, L.CH_max, gsum, status, L.sp ? 1 : 0, L.Lseg, L.S_max, s->flags,
+    CK(launch_gate_scan(pl, g, L.H, L.CH_max, gsum, status, L.sp ? 1 : 0, L.Lseg, L.Lfirst, L.S_max, s->flags,
                         single ? sc : nullptr, L.N * L.H, st));
   }
   return GDN_OK;
@@ -444,7 +519,7 @@ int prologue_saved(const gdn_shape *s, const Layout &L, char *ws, const float *g
   const bool single = single_launch_sp(L, s);
   const Sched sc[2] = {sched_of(L, ws, 0), sched_of(L, ws, 1)};
   PROF("plan");
-  CK(launch_plan(pl, s->cu_seqlens, L.N, s->cu_seqlens ? s->T : L.Tseq, L.Lseg, L.S_max, L.CH_max, status,
+  CK(launch_plan(pl, s->cu_seqlens, L.N, s->cu_seqlens ? s->T : L.Tseq, L.Lseg, L.Lfirst, L.S_max, L.CH_max, status,
                  single ? reinterpret_cast<int *>(ws + L.off_sched) : nullptr, L.sched_zero, st, gsum, L.H,
                  L.sp ? 1 : 0, s->flags, single ? sc : nullptr));
   return GDN_OK;
@@ -583,6 +658,7 @@ int forward_passes(const gdn_shape *s, const Layout &L, char *ws, FwdArgs fa, in
     fx.H = L.H;
     fx.D = L.D;
     fx.Lseg = L.Lseg;
+    fx.Lfirst = L.Lfirst;
     fx.flags = fa.flags;
     fx.reverse = 0;
     fx.fixflag = fa.status + 1;
@@ -590,8 +666,10 @@ int forward_passes(const gdn_shape *s, const Layout &L, char *ws, FwdArgs fa, in
     CK(launch_fixup(fx, L.N, st));
   }
   fa.pass = pass;
+  dim3 grid(L.S_max, L.H, 1);
+  if (tc_forward(L, s)) grid = recurrent_grid(L, s, fa.bal_pairs, fa.bal_ns, fa.bal_big);
   PROF(pass == 1 ? "fwd_chunk" : "fwd_states");
-  CK(launch_forward_kernel(L, s, fa, dim3(L.S_max, L.H, 1), st));
+  CK(launch_forward_kernel(L, s, fa, grid, st));
   return GDN_OK;
 }
 
@@ -614,6 +692,7 @@ FwdArgs fwd_args(const gdn_shape *s, const Layout &L, char *ws, const Plan &pl, 
   }
   fa.H = L.H;
   fa.Lseg = L.Lseg;
+  fa.Lfirst = L.Lfirst;
   fa.scale = s->scale;
   fa.flags = s->flags;
   return fa;
@@ -765,6 +844,7 @@ int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
   ba.dstates = ws + L.off_dstates;
   ba.H = L.H;
   ba.Lseg = L.Lseg;
+  ba.Lfirst = L.Lfirst;
   ba.scale = s->scale;
   ba.flags = s->flags;
   // the reverse chain: tcgen05 for bf16 with d = 128, the mma.sync kernel otherwise
@@ -800,6 +880,7 @@ int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
     fx.H = L.H;
     fx.D = L.D;
     fx.Lseg = L.Lseg;
+    fx.Lfirst = L.Lfirst;
     fx.flags = s->flags;
     fx.reverse = 1;
     fx.fixflag = ba.status + 2;
@@ -808,8 +889,10 @@ int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
   }
   ba.pass = 1;
   {
+    dim3 grid(L.S_max, L.H, 1);
+    if (chain_tc) grid = recurrent_grid(L, s, ba.bal_pairs, ba.bal_ns, ba.bal_big);
     PROF("bwd_chain");
-    CK(chain(dim3(L.S_max, L.H, 1)));
+    CK(chain(grid));
   }
   }
   // 3. local gradients, every (chunk, head) in parallel
@@ -958,7 +1041,7 @@ int gdn_recurrent_fwd(const gdn_shape *s, const void *q, const void *k, const vo
                       const float *beta, const float *S_in, void *o, float *S_out, gdn_stream_t stream) {
   g_last_error.clear();
   if (!s) return fail(GDN_ERR_INVALID_ARG, "shape is NULL");
-  if (s->reserved[0] || s->reserved[1] || s->reserved[2]) return fail(GDN_ERR_INVALID_ARG, "reserved fields must be 0");
+  if (s->reserved[0] || s->reserved[1]) return fail(GDN_ERR_INVALID_ARG, "reserved fields must be 0");
   if (s->B < 1 || s->T < 0 || s->H < 1) return fail(GDN_ERR_INVALID_ARG, "need B >= 1, T >= 0, H >= 1");
   if (s->cu_seqlens) return fail(GDN_ERR_UNSUPPORTED, "the recurrent form takes B sequences of T tokens (cu_seqlens must be NULL)");
   if (s->Dk != s->Dv) return fail(GDN_ERR_UNSUPPORTED, "d_k != d_v is not supported");
@@ -1017,17 +1100,18 @@ int gdn_plan_estimate(const gdn_shape *shape, double *fwd_us, double *bwd_us) {
   if (rc) return rc;
   const int maxc = shape->cu_seqlens ? (int)((L.Ttot + CH - 1) / CH) : (shape->T + CH - 1) / CH;
   double f = 0.0, b = 0.0;
-  if (maxc > 0) plan_cost_us(*shape, L.N, maxc, L.CH_max, std::min(L.Lseg, maxc), &f, &b);
+  if (maxc > 0) plan_cost_us(*shape, L.N, maxc, L.CH_max, std::min(L.Lseg, maxc), std::min(L.Lfirst, maxc), &f, &b);
   if (fwd_us) *fwd_us = f;
   if (bwd_us) *bwd_us = b;
   return GDN_OK;
 }
 
-int gdn_plan_query(const gdn_shape *shape, int *seg_chunks, int *max_segments, int *max_chunks) {
+int gdn_plan_query(const gdn_shape *shape, int *seg_chunks, int *max_segments, int *max_chunks, int *seg_first) {
   Layout L;
   int rc = make_layout(shape, L);
   if (rc) return rc;
   if (seg_chunks) *seg_chunks = L.Lseg;
+  if (seg_first) *seg_first = L.Lfirst;
   if (max_segments) *max_segments = L.S_max;
   if (max_chunks) *max_chunks = L.CH_max;
   return GDN_OK;

@@ -53,10 +53,12 @@ __device__ __forceinline__ void st_chunk_f16(uint8_t *dst, const float *v) {
 }  // namespace
 
 // One work item: segment s of head h in pass `pass` (0: pass A, role 0 the start gradient from zero or its
-// warm-up, role 1 the reverse transition; 1: the per-chunk dS).
+// warm-up, role 1 the reverse transition; 1: the per-chunk dS).  A CTA may run several items in turn: the
+// first that does work allocates the TMEM columns (have_tm), which the caller frees after the last one.
 __device__ __forceinline__ void chain_tc_item(const BwdArgs &a, const CUtensorMap &tm3, const CUtensorMap &tmdo,
                                               const CUtensorMap &tmp, const CUtensorMap &tmw, const CUtensorMap &tmds,
-                                              const CUtensorMap &tmdu, int s, int h, int role, int pass) {
+                                              const CUtensorMap &tmdu, int s, int h, int role, int pass,
+                                              bool &have_tm) {
   extern __shared__ unsigned char smraw[];
   ChainTcSmem &sm =
       *reinterpret_cast<ChainTcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
@@ -69,7 +71,7 @@ __device__ __forceinline__ void chain_tc_item(const BwdArgs &a, const CUtensorMa
   const int len = a.plan.seq_len[n], chunk0 = a.plan.seq_chunk0[n];
   const int bos = a.plan.seq_bos[n];
   const int nchunks = (len + CH - 1) / CH;
-  const int cbeg = j * a.Lseg, cend = min(cbeg + a.Lseg, nchunks);
+  const int cbeg = seg_begin(j, a.Lfirst, a.Lseg), cend = min(seg_begin(j + 1, a.Lfirst, a.Lseg), nchunks);
   const bool window = !(a.flags & kFlagWindowOff);
   int w = 0;
   const int mode = bwd_start_mode(a.gsum, H, h, chunk0, cend, nchunks, j, nseg, window, &w);
@@ -114,10 +116,11 @@ __device__ __forceinline__ void chain_tc_item(const BwdArgs &a, const CUtensorMa
       tma_prefetch_desc(&tmdu);
     }
   }
-  if (warp == 0) {
+  if (!have_tm && warp == 0) {
     tmem_alloc(u32(&sm.tmem_base), TM_COLS);
     tmem_relinquish();
   }
+  have_tm = true;
   fence_before();
   __syncthreads();
   fence_after();
@@ -404,7 +407,23 @@ __device__ __forceinline__ void chain_tc_item(const BwdArgs &a, const CUtensorMa
   fence_before();
   __syncthreads();
   fence_after();
-  if (warp == 0) tmem_dealloc(tm, TM_COLS);
+  if (tid == 0) {  // the next item of this CTA initialises them again
+    mbar_inval(u32(&sm.bar_tma[0]));
+    mbar_inval(u32(&sm.bar_tma[1]));
+    mbar_inval(u32(&sm.bar_mma));
+  }
+}
+
+// The TMEM columns of the items a CTA ran, once all of them are done.
+__device__ __forceinline__ void chain_tc_release(bool have_tm) {
+  if (!have_tm) return;
+  extern __shared__ unsigned char smraw[];
+  ChainTcSmem &sm =
+      *reinterpret_cast<ChainTcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if ((threadIdx.x >> 5) == 0) tmem_dealloc(sm.tmem_base, TM_COLS);
 }
 
 template <bool SCHED>
@@ -416,6 +435,23 @@ __global__ void __launch_bounds__(NTHREADS + 32, 1)
   pdl_wait();
   int s = blockIdx.x, h = blockIdx.y, role = blockIdx.z, pass = a.pass;
   int *doneA = nullptr;  // a pass-A item reports its completion here
+  bool have_tm = false;
+  if (!SCHED && a.bal_pairs > 0 && pass != 0) {
+    // balanced chain over equal-length sequences of bal_ns segments each (1-D grid): CTA b < bal_big runs the
+    // b-th later segment (j >= 1) of the (sequence, head) pairs, every other CTA a share of the pairs' shorter
+    // first segments (pairs k, k + G - bal_big, ...)
+    const int ns = a.bal_ns, b = blockIdx.x, G = gridDim.x;
+    if (b < a.bal_big) {
+      const int pair = b / (ns - 1);
+      chain_tc_item(a, tm3, tmdo, tmp, tmw, tmds, tmdu, (pair / a.H) * ns + 1 + b % (ns - 1), pair % a.H, 0, pass,
+                    have_tm);
+    } else {
+      for (int k = b - a.bal_big; k < a.bal_pairs; k += G - a.bal_big)
+        chain_tc_item(a, tm3, tmdo, tmp, tmw, tmds, tmdu, (k / a.H) * ns, k % a.H, 0, pass, have_tm);
+    }
+    chain_tc_release(have_tm);
+    return;
+  }
   if (SCHED) {
     // single-launch sequence parallelism: this CTA runs the ticket-th item of the work lists (see Sched)
     __shared__ int tk, ok;
@@ -456,6 +492,7 @@ __global__ void __launch_bounds__(NTHREADS + 32, 1)
       fx.H = a.H;
       fx.D = D;
       fx.Lseg = a.Lseg;
+      fx.Lfirst = a.Lfirst;
       fx.flags = a.flags;
       fx.reverse = 1;
       fx.fixflag = nullptr;
@@ -483,7 +520,8 @@ __global__ void __launch_bounds__(NTHREADS + 32, 1)
       return;  // a ticket past the lists: no work
     }
   }
-  chain_tc_item(a, tm3, tmdo, tmp, tmw, tmds, tmdu, s, h, role, pass);
+  chain_tc_item(a, tm3, tmdo, tmp, tmw, tmds, tmdu, s, h, role, pass, have_tm);
+  chain_tc_release(have_tm);
   if (doneA) {  // the start-gradient / transition stores of every thread are visible before the count
     __threadfence();
     __syncthreads();

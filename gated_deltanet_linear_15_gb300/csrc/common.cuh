@@ -240,6 +240,16 @@ __device__ __forceinline__ bool f16_out(float x) { return !(fabsf(x) <= F16_MAX)
 
 enum StartMode { START_INIT = 0, START_WARMUP = 1, START_FIXUP = 2 };
 
+// Segment j of a sequence covers its chunks [seg_begin(j), seg_begin(j + 1)), capped at its chunk count:
+// the first segment Lfirst chunks, every later one Lseg.  A sequence of nchunks chunks has seg_count of
+// them (one for an empty sequence).
+__host__ __device__ __forceinline__ int seg_begin(int j, int Lfirst, int Lseg) {
+  return j == 0 ? 0 : Lfirst + (j - 1) * Lseg;
+}
+__host__ __device__ __forceinline__ int seg_count(int nchunks, int Lfirst, int Lseg) {
+  return nchunks <= Lfirst ? 1 : 1 + (nchunks - Lfirst + Lseg - 1) / Lseg;
+}
+
 // Forward: how segment (n, j) obtains its start state.  w = warm-up chunks.
 __device__ __forceinline__ int fwd_start_mode(const float *gsum, int H, int h, int chunk0, int cbeg, int j,
                                               bool window, int *w) {

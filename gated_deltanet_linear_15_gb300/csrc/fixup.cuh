@@ -45,8 +45,9 @@ __device__ __forceinline__ void fixup_rows(const FixupArgs &a, int rb, int h, in
   // the start (end, reversed) mode of segment j
   auto start_mode = [&](int j) {
     int w;
-    if (!a.reverse) return fwd_start_mode(a.gsum, H, h, chunk0, j * a.Lseg, j, window, &w);
-    return bwd_start_mode(a.gsum, H, h, chunk0, min((j + 1) * a.Lseg, nchunks), nchunks, j, nseg, window, &w);
+    if (!a.reverse) return fwd_start_mode(a.gsum, H, h, chunk0, seg_begin(j, a.Lfirst, a.Lseg), j, window, &w);
+    return bwd_start_mode(a.gsum, H, h, chunk0, min(seg_begin(j + 1, a.Lfirst, a.Lseg), nchunks), nchunks, j, nseg,
+                          window, &w);
   };
   const bool small = nseg <= FIX_MODES;
   if (small) {

@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_chunk_kernel(FwdArgs a) {
   const int len = a.plan.seq_len[n], chunk0 = a.plan.seq_chunk0[n];
   const long bos = a.plan.seq_bos[n];
   const int nchunks = (len + CH - 1) / CH;
-  const int cbeg = j * a.Lseg, cend = min(cbeg + a.Lseg, nchunks);
+  const int cbeg = seg_begin(j, a.Lfirst, a.Lseg), cend = min(seg_begin(j + 1, a.Lfirst, a.Lseg), nchunks);
   const bool window = !(a.flags & kFlagWindowOff);
   int w = 0;
   const int mode = fwd_start_mode(a.gsum, H, h, chunk0, cbeg, j, window, &w);

@@ -345,7 +345,7 @@ __global__ void __launch_bounds__(PT, 2)
       __threadfence();
       Sched none;
       memset(&none, 0, sizeof none);
-      fixup_modes(a.plan, a.gsum_out, H, a.Lseg, a.S_max, a.flags, a.status, tid, PT, none, none, 0);
+      fixup_modes(a.plan, a.gsum_out, H, a.Lseg, a.Lfirst, a.S_max, a.flags, a.status, tid, PT, none, none, 0);
     }
   }
 }

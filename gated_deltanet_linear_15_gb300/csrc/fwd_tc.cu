@@ -73,10 +73,11 @@ __device__ __forceinline__ void st_chunk_f16(uint8_t *dst, const float *v) {
 }  // namespace
 
 // One work item: segment s of head h in pass `pass` (0: pass A, role 0 the end state from zero or its
-// warm-up, role 1 the transition; 1: outputs; 2: states only).
+// warm-up, role 1 the transition; 1: outputs; 2: states only).  A CTA may run several items in turn: the
+// first that does work allocates the TMEM columns (have_tm), which the caller frees after the last one.
 __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap &tm3, const CUtensorMap &tmw,
                                             const CUtensorMap &tms, const CUtensorMap &tmt, const CUtensorMap &tmo,
-                                            int s, int h, int role, int pass) {
+                                            int s, int h, int role, int pass, bool &have_tm) {
   extern __shared__ unsigned char smraw[];
   TcSmem &sm = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
   // pass A of a call in which no segment needs the exact fix-up (status[1], set after the gate scan)
@@ -88,7 +89,7 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
   const int len = a.plan.seq_len[n], chunk0 = a.plan.seq_chunk0[n];
   const int bos = a.plan.seq_bos[n];
   const int nchunks = (len + CH - 1) / CH;
-  const int cbeg = j * a.Lseg, cend = min(cbeg + a.Lseg, nchunks);
+  const int cbeg = seg_begin(j, a.Lfirst, a.Lseg), cend = min(seg_begin(j + 1, a.Lfirst, a.Lseg), nchunks);
   const bool window = !(a.flags & kFlagWindowOff);
   int w = 0;
   const int mode = fwd_start_mode(a.gsum, H, h, chunk0, cbeg, j, window, &w);
@@ -137,10 +138,11 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
     if (save_states) tma_prefetch_desc(&tms);
     if (want_o) tma_prefetch_desc(&tmo);
   }
-  if (warp == 0) {
+  if (!have_tm && warp == 0) {
     tmem_alloc(u32(&sm.tmem_base), TM_COLS);
     tmem_relinquish();
   }
+  have_tm = true;
   fence_before();
   __syncthreads();
   fence_after();
@@ -517,7 +519,23 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
   fence_before();
   __syncthreads();
   fence_after();
-  if (warp == 0) tmem_dealloc(tm, TM_COLS);
+  if (tid == 0) {  // the next item of this CTA initialises them again
+    mbar_inval(u32(&sm.bar_tma[0]));
+    mbar_inval(u32(&sm.bar_tma[1]));
+    mbar_inval(u32(&sm.bar_mma));
+    mbar_inval(u32(&sm.bar_mma2));
+  }
+}
+
+// The TMEM columns of the items a CTA ran, once all of them are done.
+__device__ __forceinline__ void fwd_tc_release(bool have_tm) {
+  if (!have_tm) return;
+  extern __shared__ unsigned char smraw[];
+  TcSmem &sm = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if ((threadIdx.x >> 5) == 0) tmem_dealloc(sm.tmem_base, TM_COLS);
 }
 
 template <bool SCHED>
@@ -529,6 +547,22 @@ __global__ void __launch_bounds__(FT + 32, 1)
   pdl_wait();
   int s = blockIdx.x, h = blockIdx.y, role = blockIdx.z, pass = a.pass;
   int *doneA = nullptr;  // a pass-A item reports its completion here
+  bool have_tm = false;
+  if (!SCHED && a.bal_pairs > 0 && pass != 0) {
+    // balanced pass over equal-length sequences of bal_ns segments each (1-D grid): CTA b < bal_big runs the
+    // b-th later segment (j >= 1) of the (sequence, head) pairs, every other CTA a share of the pairs' shorter
+    // first segments (pairs k, k + G - bal_big, ...)
+    const int ns = a.bal_ns, b = blockIdx.x, G = gridDim.x;
+    if (b < a.bal_big) {
+      const int pair = b / (ns - 1);
+      fwd_tc_item(a, tm3, tmw, tms, tmt, tmo, (pair / a.H) * ns + 1 + b % (ns - 1), pair % a.H, 0, pass, have_tm);
+    } else {
+      for (int k = b - a.bal_big; k < a.bal_pairs; k += G - a.bal_big)
+        fwd_tc_item(a, tm3, tmw, tms, tmt, tmo, (k / a.H) * ns, k % a.H, 0, pass, have_tm);
+    }
+    fwd_tc_release(have_tm);
+    return;
+  }
   if (SCHED) {
     // single-launch sequence parallelism: this CTA runs the ticket-th item of the work lists (see Sched)
     __shared__ int tk, ok;
@@ -569,6 +603,7 @@ __global__ void __launch_bounds__(FT + 32, 1)
       fx.H = a.H;
       fx.D = D;
       fx.Lseg = a.Lseg;
+      fx.Lfirst = a.Lfirst;
       fx.flags = a.flags;
       fx.reverse = 0;
       fx.fixflag = nullptr;
@@ -596,7 +631,8 @@ __global__ void __launch_bounds__(FT + 32, 1)
       return;  // a ticket past the lists: no work
     }
   }
-  fwd_tc_item(a, tm3, tmw, tms, tmt, tmo, s, h, role, pass);
+  fwd_tc_item(a, tm3, tmw, tms, tmt, tmo, s, h, role, pass, have_tm);
+  fwd_tc_release(have_tm);
   if (doneA) {  // the end state / transition stores of every thread are visible before the count
     __threadfence();
     __syncthreads();

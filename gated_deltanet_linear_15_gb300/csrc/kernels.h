@@ -40,7 +40,7 @@ struct FwdArgs {
   int *status;
   float *Ebuf, *Mbuf, *Sstart;  // [S_max, H, D, D]
   void *states;                 // [CH_max, H, D, D] state at every chunk start (fp16 / fp32), or NULL
-  int H, Lseg;
+  int H, Lseg, Lfirst;  // segment lengths in chunks (seg_begin)
   float scale;
   unsigned flags;
   int pass;  // 0: segment end states / transitions, 1: outputs (+ saves if set), 2: states only
@@ -56,6 +56,10 @@ struct FwdArgs {
   float *nrm;
   Sched sched;  // single-launch sequence parallelism when sched_on (pass then names the pass-B kind, 1 or 2)
   int sched_on;
+  // bf16 with d = 128, pass 1 / 2 over bal_pairs (sequence, head) pairs of equal length with bal_ns segments each
+  // (bal_pairs = 0: one CTA per (segment, head), grid (S_max, H)): a 1-D grid whose first bal_big CTAs take the
+  // later segments one each and whose other CTAs share the first segments
+  int bal_pairs, bal_ns, bal_big;
 };
 
 // Chunk context tiles of every (chunk, head), fp16 row-major, written by the forward:
@@ -84,13 +88,14 @@ struct BwdArgs {
   float *Fbuf, *Rbuf, *dSend;  // [S_max, H, D, D]
   const void *states;          // [CH_max, H, D, D] forward state at each chunk start
   void *dstates;               // [CH_max, H, D, D] dS at each chunk end
-  int H, Lseg;
+  int H, Lseg, Lfirst;
   float scale;
   unsigned flags;
   int pass;  // reverse chain: 0 segment starts / transitions, 1 per-chunk dS
   const float *nrm;  // context reciprocal norms (bf16, d = 128), see FwdArgs
   Sched sched;       // single-launch sequence parallelism when sched_on, see FwdArgs
   int sched_on;
+  int bal_pairs, bal_ns, bal_big;  // balanced chain over equal-length sequences, see FwdArgs
 };
 
 struct FixupArgs {
@@ -98,7 +103,7 @@ struct FixupArgs {
   const float *gsum;
   const float *E, *M;  // end states / transitions per (segment, head)
   float *out;          // corrected start (forward) or end (reverse) states
-  int H, D, Lseg;
+  int H, D, Lseg, Lfirst;
   unsigned flags;
   int reverse;
   const int *fixflag;  // nonzero iff some segment of this direction needs the fix-up (NULL: always run)
@@ -118,12 +123,12 @@ struct RecArgs {
 // zero: `nzero` ints cleared with the status words (the schedules' counters), or NULL.  With gsum and modes
 // set (the saved-context backward, which takes the forward's gate sums) the plan kernel also runs the fix-up
 // mode scan and builds the schedules in sched[0] / sched[1] (hdr NULL: none) instead of the gate scan.
-int launch_plan(const Plan &p, const int *cu, int N, int T, int Lseg, int S_max, int CH_max, int *status, int *zero,
-                int nzero, cudaStream_t st, const float *gsum = nullptr, int H = 0, int modes = 0,
+int launch_plan(const Plan &p, const int *cu, int N, int T, int Lseg, int Lfirst, int S_max, int CH_max, int *status,
+                int *zero, int nzero, cudaStream_t st, const float *gsum = nullptr, int H = 0, int modes = 0,
                 unsigned flags = 0, const Sched *sched = nullptr);
 // sched[0] / sched[1]: forward / reverse schedules to build (hdr NULL: none)
 int launch_gate_scan(const Plan &p, const float *g, int H, int CH_max, float *gsum, int *status, int modes, int Lseg,
-                     int S_max, unsigned flags, const Sched *sched, int NH, cudaStream_t st);
+                     int Lfirst, int S_max, unsigned flags, const Sched *sched, int NH, cudaStream_t st);
 int launch_fixup(const FixupArgs &a, int N, cudaStream_t st);
 
 int launch_fwd_chunk(const FwdArgs &a, bool is_bf16, int D, dim3 grid, cudaStream_t st);

@@ -36,15 +36,19 @@ static __device__ __forceinline__ bool window_ok(const float *gsum, int H, int h
   return warm;
 }
 
-static __device__ void fixup_modes(const Plan &p, const float *gsum, int H, int Lseg, int S_max, unsigned flags, int *status,
+static __device__ void fixup_modes(const Plan &p, const float *gsum, int H, int Lseg, int Lfirst, int S_max, unsigned flags,
+                                   int *status,
                             int i0, int stride, Sched fs, Sched bs, int NH) {
   const bool window = !(flags & kFlagWindowOff);
   bool fwd_fix = false, bwd_fix = false;
   // forward start of segment j needs the fix-up (j > 0 and no certified warm-up)
-  auto ffix = [&](int j, int chunk0, int h) { return j > 0 && !(window && window_ok(gsum, H, h, chunk0, j * Lseg, j * Lseg)); };
+  auto ffix = [&](int j, int chunk0, int h) {
+    const int cbeg = seg_begin(j, Lfirst, Lseg);
+    return j > 0 && !(window && window_ok(gsum, H, h, chunk0, cbeg, cbeg));
+  };
   // reverse end of segment j needs the fix-up (j < nseg - 1 and no certified warm-up after it)
   auto bfix = [&](int j, int nseg, int nchunks, int chunk0, int h) {
-    const int cend = min((j + 1) * Lseg, nchunks);
+    const int cend = min(seg_begin(j + 1, Lfirst, Lseg), nchunks);
     return j < nseg - 1 && !(window && window_ok(gsum, H, h, chunk0, cend, -(nchunks - cend)));
   };
   auto push = [](Sched &sc, int k, int v) {

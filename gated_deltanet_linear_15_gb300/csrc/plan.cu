@@ -24,7 +24,7 @@ namespace gdn {
 // bit 1 and leaves every sequence empty, so the chunk kernels do nothing.
 // Given the gate sums of a call whose forward computed them (modes != 0,
 // gsum set), it also runs the fix-up mode scan over the tables it built.
-__global__ void plan_kernel(Plan p, const int *cu, int N, int T, int Lseg, int S_max, int CH_max, int *status,
+__global__ void plan_kernel(Plan p, const int *cu, int N, int T, int Lseg, int Lfirst, int S_max, int CH_max, int *status,
                             int *zero, int nzero, const float *gsum, int H, int modes, unsigned flags, Sched fs,
                             Sched bs) {
   pdl_trigger();
@@ -58,7 +58,7 @@ __global__ void plan_kernel(Plan p, const int *cu, int N, int T, int Lseg, int S
     }
     const int nc = (len + CH - 1) / CH;
     // an empty sequence still gets one (chunk-less) segment: it passes S0 to S_T
-    const int ns = (n < N && !isbad) ? max(1, (nc + Lseg - 1) / Lseg) : 0;
+    const int ns = (n < N && !isbad) ? seg_count(nc, Lfirst, Lseg) : 0;
     // block-wide exclusive scans of nc and ns
     const int lane = tid & 31, warp = tid >> 5;
     int ic = nc, is = ns;
@@ -141,15 +141,16 @@ __global__ void plan_kernel(Plan p, const int *cu, int N, int T, int Lseg, int S
   }
   if (!modes || !gsum) return;
   __syncthreads();  // the tables above, the zeroed status words and counters
-  fixup_modes(p, gsum, H, Lseg, S_max, flags, status, tid, nt, fs, bs, N * H);
+  fixup_modes(p, gsum, H, Lseg, Lfirst, S_max, flags, status, tid, nt, fs, bs, N * H);
 }
 
-int launch_plan(const Plan &p, const int *cu, int N, int T, int Lseg, int S_max, int CH_max, int *status, int *zero,
-                int nzero, cudaStream_t st, const float *gsum, int H, int modes, unsigned flags, const Sched *sched) {
+int launch_plan(const Plan &p, const int *cu, int N, int T, int Lseg, int Lfirst, int S_max, int CH_max, int *status,
+                int *zero, int nzero, cudaStream_t st, const float *gsum, int H, int modes, unsigned flags,
+                const Sched *sched) {
   Sched none;
   memset(&none, 0, sizeof none);
-  return (int)launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, st, p, cu, N, T, Lseg, S_max, CH_max, status, zero,
-                         zero ? nzero : 0, gsum, H, modes, flags, sched ? sched[0] : none, sched ? sched[1] : none);
+  return (int)launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, st, p, cu, N, T, Lseg, Lfirst, S_max, CH_max, status,
+                         zero, zero ? nzero : 0, gsum, H, modes, flags, sched ? sched[0] : none, sched ? sched[1] : none);
 }
 
 // One block per global chunk: the chunk's log-gates of 32 heads at a time are
@@ -159,7 +160,8 @@ int launch_plan(const Plan &p, const int *cu, int N, int T, int Lseg, int S_max,
 // With modes != 0 (a call with segments) the last block to finish also runs the fix-up mode scan
 // over every (segment, head) (status[3] counts finished blocks; the plan kernel zeroed it).
 __global__ void __launch_bounds__(256) gate_scan_kernel(Plan p, const float *g, int H, float *gsum, int *status,
-                                                        int modes, int Lseg, int S_max, unsigned flags, Sched fs,
+                                                        int modes, int Lseg, int Lfirst, int S_max, unsigned flags,
+                                                        Sched fs,
                                                         Sched bs, int NH) {
   pdl_trigger();
   pdl_wait();
@@ -203,16 +205,16 @@ __global__ void __launch_bounds__(256) gate_scan_kernel(Plan p, const float *g, 
   __syncthreads();
   if (!last) return;
   __threadfence();
-  fixup_modes(p, gsum, H, Lseg, S_max, flags, status, threadIdx.x, blockDim.x, fs, bs, NH);
+  fixup_modes(p, gsum, H, Lseg, Lfirst, S_max, flags, status, threadIdx.x, blockDim.x, fs, bs, NH);
 }
 
 int launch_gate_scan(const Plan &p, const float *g, int H, int CH_max, float *gsum, int *status, int modes, int Lseg,
-                     int S_max, unsigned flags, const Sched *sched, int NH, cudaStream_t st) {
+                     int Lfirst, int S_max, unsigned flags, const Sched *sched, int NH, cudaStream_t st) {
   if (CH_max == 0) return 0;
   Sched none;
   memset(&none, 0, sizeof none);
-  return (int)launch_pdl(gate_scan_kernel, dim3(CH_max), dim3(256), 0, st, p, g, H, gsum, status, modes, Lseg, S_max,
-                         flags, sched ? sched[0] : none, sched ? sched[1] : none, NH);
+  return (int)launch_pdl(gate_scan_kernel, dim3(CH_max), dim3(256), 0, st, p, g, H, gsum, status, modes, Lseg, Lfirst,
+                         S_max, flags, sched ? sched[0] : none, sched ? sched[1] : none, NH);
 }
 
 // grid (D / FIX_ROWS, H, N), 256 threads: one fix-up row block per CTA (see fixup_rows)

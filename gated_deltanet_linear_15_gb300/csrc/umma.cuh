@@ -272,6 +272,10 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
 __device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(mbar), "r"(count));
 }
+// retire an mbarrier whose phases are all complete, so that its word can be initialised again
+__device__ __forceinline__ void mbar_inval(uint32_t mbar) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];\n" ::"r"(mbar) : "memory");
+}
 __device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(mbar), "r"(bytes) : "memory");
 }

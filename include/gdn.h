@@ -94,7 +94,9 @@ typedef struct {
   float scale;                /* o_t = S_t (scale * q_t), applied after normalisation    */
   unsigned flags;             /* GDN_L2NORM_QK | GDN_SP_OFF | GDN_WINDOW_OFF | GDN_SP_SINGLE_LAUNCH */
   int seg_chunks;             /* chunks per segment for sequence parallelism; 0 = auto   */
-  int reserved[3];            /* must be 0                                               */
+  int seg_first;              /* chunks of each sequence's first segment (needs          */
+                              /* seg_chunks > 0); 0 = seg_chunks, or auto with it        */
+  int reserved[2];            /* must be 0                                               */
 } gdn_shape;
 
 /* Workspace bytes needed by gdn_chunk_fwd / gdn_chunk_bwd for this shape on the
@@ -282,8 +284,9 @@ int gdn_get_device_status(const gdn_shape *shape, const void *workspace, gdn_str
 int gdn_device_status_code(int word);
 
 /* The segment plan for this shape on the current device: chunks per segment,
- * an upper bound on the number of segments, and on the number of chunks. */
-int gdn_plan_query(const gdn_shape *shape, int *seg_chunks, int *max_segments, int *max_chunks);
+ * an upper bound on the number of segments, on the number of chunks, and the
+ * chunks of each sequence's first segment.  Any output pointer may be NULL. */
+int gdn_plan_query(const gdn_shape *shape, int *seg_chunks, int *max_segments, int *max_chunks, int *seg_first);
 
 /* The library's cost model of that plan: the modelled time in microseconds of the forward's state
  * pass and of the backward's reverse chain on the current device (the passes whose length the

@@ -38,15 +38,15 @@ MARGINS = []
 
 
 def run_gpu(x, *, bwd=True, sp=True, window=True, seg_chunks=0, with_final=True, saved=False, bwd_plan=None,
-            check_status=True, single_launch=False):
+            check_status=True, single_launch=False, seg_first=0):
     """Forward (+ backward) through the library.  saved=True: the forward keeps its per-chunk states
-    and WY tiles and the backward reads them; bwd_plan = dict(sp=, window=, seg_chunks=) gives the
+    and WY tiles and the backward reads them; bwd_plan = dict(sp=, window=, seg_chunks=, seg_first=) gives the
     backward another segment plan than the forward.  The device status word of each call must be 0
     (no numeric-guard hit, no expired wait, no malformed plan) unless check_status is False."""
     def shape_of(plan):
         return g.make_shape(x["q"], x["v"], cu_seqlens=x["cu_seqlens"], scale=x["scale"], l2norm=x["l2norm"], **plan)
 
-    fplan = dict(sp=sp, window=window, seg_chunks=seg_chunks, single_launch=single_launch)
+    fplan = dict(sp=sp, window=window, seg_chunks=seg_chunks, single_launch=single_launch, seg_first=seg_first)
     fshape = shape_of(fplan)
     fws = torch.empty(max(g.gdn_fwd_workspace_size(fshape), 256), dtype=torch.uint8, device=x["q"].device)
     res = g.chunk_gated_delta_rule_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], with_final,

@@ -74,6 +74,8 @@ def test_device_status_code(lib, word, code):
     (dict(T=-1), _lib.GDN_ERR_INVALID_ARG),
     (dict(dtype=7), _lib.GDN_ERR_INVALID_ARG),
     (dict(seg_chunks=-2), _lib.GDN_ERR_INVALID_ARG),
+    (dict(seg_chunks=2, seg_first=-1), _lib.GDN_ERR_INVALID_ARG),
+    (dict(seg_first=3), _lib.GDN_ERR_INVALID_ARG),              # seg_first needs seg_chunks
 ])
 def test_bad_shapes_rejected(lib, kw, code):
     s = _shape(**kw)
@@ -86,6 +88,26 @@ def test_reserved_must_be_zero(lib):
     s = _shape()
     s.reserved[1] = 3
     assert _fwd(lib, s) == _lib.GDN_ERR_INVALID_ARG
+
+
+def test_first_segment_length_in_plan(lib):
+    """seg_first sets the first segment of every sequence, seg_chunks the later ones: 130 chunks as
+    3 + 127 / 8 -> 1 + 16 segments per sequence (the sequence-parallel buffers grow with the count)."""
+    base = _shape(T=130 * 64, H=2, seg_chunks=8)
+    first = _shape(T=130 * 64, H=2, seg_chunks=8, seg_first=3)
+    a, b = ctypes.c_int(), ctypes.c_int()
+    c = ctypes.c_int()
+    assert lib.gdn_plan_query(ctypes.byref(base), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c), None) == 0
+    assert (a.value, b.value) == (8, 17)
+    assert lib.gdn_plan_query(ctypes.byref(first), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c), None) == 0
+    assert (a.value, b.value) == (8, 17)
+    assert lib.gdn_fwd_workspace_size(ctypes.byref(first)) > 0
+    first.seg_first = 2     # 2 + 128 / 8: 17 segments
+    assert lib.gdn_plan_query(ctypes.byref(first), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c), None) == 0
+    assert b.value == 17
+    first.seg_first = 10    # 10 + 120 / 8: 16 segments
+    assert lib.gdn_plan_query(ctypes.byref(first), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c), None) == 0
+    assert b.value == 16
 
 
 def test_null_and_misaligned_pointers(lib):
@@ -198,16 +220,16 @@ def test_plan_query_sp_policy(lib):
     with many (sequence, head) pairs no split happens."""
     a, b, c = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     s = _shape(T=8192, H=32, flags=_lib.GDN_SP_OFF)
-    assert lib.gdn_plan_query(ctypes.byref(s), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)) == 0
+    assert lib.gdn_plan_query(ctypes.byref(s), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c), None) == 0
     assert (a.value, b.value, c.value) == (128, 1, 128)
     s = _shape(T=8192, H=32, seg_chunks=10)
-    lib.gdn_plan_query(ctypes.byref(s), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c))
+    lib.gdn_plan_query(ctypes.byref(s), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c), None)
     assert (a.value, b.value) == (10, 13)
     s = _shape(B=64, T=4096, H=32)
-    lib.gdn_plan_query(ctypes.byref(s), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c))
+    lib.gdn_plan_query(ctypes.byref(s), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c), None)
     assert a.value == 64 and b.value == 64
     s = _shape(T=65536, H=8)           # long context, few heads: split
-    lib.gdn_plan_query(ctypes.byref(s), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c))
+    lib.gdn_plan_query(ctypes.byref(s), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c), None)
     assert 1 < a.value < 1024 and b.value * 8 >= 100
 
 

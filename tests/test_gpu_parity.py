@@ -57,6 +57,35 @@ def test_sequence_parallel_exact_and_window(seg_chunks, window, single_launch):
                 run_oracle(x), TOL["bf16"])
 
 
+@pytest.mark.parametrize("seg_chunks,seg_first", [(3, 1), (2, 4), (1, 2)])
+@pytest.mark.parametrize("window", [True, False])
+def test_first_segment_length(seg_chunks, seg_first, window):
+    """Segments of two lengths (each sequence's first segment seg_first chunks, the later ones seg_chunks):
+    the passes, the fix-up and the mode scan take the same boundaries; slow decay (alpha ~ 1) with the
+    window off exercises pass A + fix-up on them, the window on the warm-up path; both pairs."""
+    x = make_inputs("long_h8_t65536", DEV, T=64 * 7 + 9, H=8, with_S0=True, with_dST=True)
+    ref = run_oracle(x)
+    for saved in (False, True):
+        compare(run_gpu(x, seg_chunks=seg_chunks, seg_first=seg_first, window=window, saved=saved), ref,
+                TOL["bf16"])
+
+
+def test_balanced_recurrent_grid():
+    """More (segment, head) items than SMs while the later segments fit the SMs one each: the recurrent
+    passes and the reverse chain run on one CTA per SM, the later segments one per CTA and the one-chunk
+    first segments several to a CTA in turn (9 chunks: 1 + 4 x 2, 32 heads); window on and off, both
+    pairs, a ragged last chunk."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    H, ns = 32, 5
+    if not H * (ns - 1) < sms < H * ns:
+        pytest.skip(f"{sms} SMs: this plan would not take the balanced grid")
+    x = make_inputs("prefill_h32_t8192", DEV, T=64 * 8 + 40, H=H, with_S0=True, with_dST=True)
+    ref = run_oracle(x)
+    for window in (True, False):
+        for saved in (False, True):
+            compare(run_gpu(x, seg_chunks=2, seg_first=1, window=window, saved=saved), ref, TOL["bf16"])
+
+
 def test_sp_on_off_agree():
     x = make_inputs("long_h8_t65536", DEV, T=64 * 9, H=8, with_dST=True)
     a = run_gpu(x, sp=False)
