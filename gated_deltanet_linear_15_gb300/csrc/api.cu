@@ -266,7 +266,7 @@ int make_layout(const gdn_shape *s, Layout &L) {
   else L.S_max = L.N * seg_count(maxc, L.Lfirst, L.Lseg);
   L.sp = std::min(L.Lfirst, L.Lseg) < maxc;
   const size_t DD = (size_t)L.D * L.D;
-  const size_t nplan = 5 * (size_t)L.N + L.S_max + L.CH_max + 2;
+  const size_t nplan = 5 * (size_t)L.N + L.S_max + 3 * (size_t)L.CH_max + 2;
   size_t off = 0;
   L.off_status = off;
   off += 256;
@@ -366,8 +366,9 @@ unsigned sched_grid(const Layout &L) {
 }
 
 Plan plan_of(const Layout &L, char *ws) {
-  int *p = reinterpret_cast<int *>(ws + L.off_plan);
   Plan pl;
+  pl.chunk_info = reinterpret_cast<int2 *>(ws + L.off_plan);
+  int *p = reinterpret_cast<int *>(pl.chunk_info + L.CH_max);
   pl.seq_bos = p;
   pl.seq_len = p + L.N;
   pl.seq_chunk0 = p + 2 * L.N;

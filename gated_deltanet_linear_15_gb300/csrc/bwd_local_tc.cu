@@ -203,22 +203,22 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     }
   };
 
-  // Work items (chunk gc, head h) = (item / H, item % H), strided over the persistent CTAs; chunks past
-  // the plan's total are skipped.  The tiles of the next item are loaded by TMA while this one finishes.
-  auto next_valid = [&](int item) {
-    while (item < n_items && a.plan.chunk_seq[item / H] < 0) item += gridDim.x;
-    return item;
-  };
-  // first token and valid rows of a work item (plan lookups, done one item ahead)
+  // Work items (chunk gc, head h) = (item / H, item % H), strided over the persistent CTAs; the chunks in
+  // use are the plan's first totals[0] (all of them, or none for a malformed plan).  The tiles of the next
+  // item are loaded by TMA while this one finishes.
+  const int tot_c = a.plan.totals[0];
+  const int lim = tot_c <= n_items / H ? tot_c * H : 0;  // items of the chunks in use
+  auto next_valid = [&](int item) { return item < lim ? item : n_items; };
+  // first token and valid rows of a work item (one plan look-up, done one item ahead)
   struct ItemInfo {
     int item, tok0, nvalid;
   };
   auto info_of = [&](int item) {
     ItemInfo r{item, 0, 0};
     if (item < n_items) {
-      const int gc = item / H, n = a.plan.chunk_seq[gc], lc = gc - a.plan.seq_chunk0[n];
-      r.tok0 = a.plan.seq_bos[n] + lc * CH;
-      r.nvalid = min(CH, a.plan.seq_len[n] - lc * CH);
+      const int2 ci = a.plan.chunk_info[item / H];
+      r.tok0 = ci.x;
+      r.nvalid = ci.y;
     }
     return r;
   };

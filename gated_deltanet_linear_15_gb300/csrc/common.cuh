@@ -225,6 +225,7 @@ struct Plan {
   int *seg_seq;     // [S_max] sequence of segment s, -1 if unused
   int *chunk_seq;   // [CH_max] sequence of global chunk c, -1 if unused
   int *totals;      // [2] total chunks, total segments
+  int2 *chunk_info; // [CH_max] first token and valid rows of global chunk c ({0, 0} if unused)
 };
 
 constexpr float LN_EPS_WINDOW = -16.635532f;  // ln(2^-24)

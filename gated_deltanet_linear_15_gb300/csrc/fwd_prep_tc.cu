@@ -72,22 +72,22 @@ __global__ void __launch_bounds__(PT, 2)
   int *err = a.status;
 
   // Work items (chunk gc, head h) = (item / H, item % H), strided over the persistent CTAs (two per SM);
-  // chunks past the plan's total are skipped.  The next item's q, k, v are loaded by TMA once this
-  // item's Gram product is done and its operand tiles have left, under the read-out and the inverse; its
-  // plan look-ups (dependent global loads) and its g, beta are fetched while this item's Gram product runs.
-  auto next_valid = [&](int item) {
-    while (item < n_items && a.plan.chunk_seq[item / H] < 0) item += gridDim.x;
-    return item;
-  };
+  // the chunks in use are the plan's first totals[0] (all of them, or none for a malformed plan).  The next
+  // item's q, k, v are loaded by TMA once this item's Gram product is done and its operand tiles have left,
+  // under the read-out and the inverse; its g, beta are fetched while this item's Gram product runs, from
+  // its first token and valid rows, which were loaded one item earlier.
+  const int tot_c = a.plan.totals[0];
+  const int lim = tot_c <= n_items / H ? tot_c * H : 0;  // items of the chunks in use
+  auto next_valid = [&](int item) { return item < lim ? item : n_items; };
   struct ItemInfo {
     int item, tok0, nvalid;
   };
   auto info_of = [&](int item) {
     ItemInfo r{item, 0, 0};
     if (item < n_items) {
-      const int gc = item / H, n = a.plan.chunk_seq[gc], lc = gc - a.plan.seq_chunk0[n];
-      r.tok0 = a.plan.seq_bos[n] + lc * CH;
-      r.nvalid = min(CH, a.plan.seq_len[n] - lc * CH);
+      const int2 ci = a.plan.chunk_info[item / H];
+      r.tok0 = ci.x;
+      r.nvalid = ci.y;
     }
     return r;
   };
@@ -103,6 +103,7 @@ __global__ void __launch_bounds__(PT, 2)
     }
   };
   ItemInfo cur = info_of(next_valid(blockIdx.x));
+  ItemInfo nxt = info_of(next_valid(cur.item + gridDim.x));
   if (tid < 2 * CH && cur.item < n_items) {  // the first item's g, beta (later items': fetched one item ahead)
     const int r = tid & (CH - 1), hh = cur.item % H;
     const float v = r < cur.nvalid ? (tid < CH ? a.g : a.beta)[(size_t)(cur.tok0 + r) * H + hh] : 0.f;
@@ -238,12 +239,11 @@ __global__ void __launch_bounds__(PT, 2)
     }
     __syncwarp();
     // under the Gram product: this item's gate prefix sums (warp 7; the read-out of P is their first
-    // reader), the next item's plan look-ups and its g, beta (kept in registers until the product is done)
+    // reader) and the next item's g, beta (kept in registers until the product is done)
     if (warp == PT / 32 - 1) {
       gate_prefix(sm.g[gbuf], sm.gt[gbuf]);
       if (lane == 0 && a.gsum_out) a.gsum_out[item] = sm.gt[gbuf].Glog;  // this lane wrote Glog
     }
-    const ItemInfo nxt = info_of(next_valid(item + gridDim.x));
     float gnext = 0.f;
     if (tid < 2 * CH && nxt.item < n_items) {
       const int r = tid & (CH - 1), hh = nxt.item % H;
@@ -258,6 +258,10 @@ __global__ void __launch_bounds__(PT, 2)
       issue_qkv(nxt.item, nxt.tok0);
     }
     pend = nxt.item < n_items;
+    // the first token and valid rows of the item after the next one, first read at the end of this item
+    const int item2 = next_valid(nxt.item + gridDim.x);
+    int2 ci2 = make_int2(0, 0);
+    if (item2 < n_items) ci2 = a.plan.chunk_info[item2 / H];
 
     // ---- read-out: warp w takes TMEM lanes 32 (w % 4).. and columns 32 (w / 4)..; N (fp32, rows 0-63,
     // also stored as fp16) and P (fp16, rows 64-127)
@@ -323,6 +327,7 @@ __global__ void __launch_bounds__(PT, 2)
       tma_store_commit();
     }
     cur = nxt;
+    nxt = ItemInfo{item2, ci2.x, ci2.y};
   }
   if (nbad && err) atomicOr(err, 1);
   if (tid == 0) {

@@ -126,6 +126,13 @@ __global__ void plan_kernel(Plan p, const int *cu, int N, int T, int Lseg, int L
       owner = lo;
     }
     p.chunk_seq[c] = owner;
+    int2 ci = make_int2(0, 0);
+    if (owner >= 0) {
+      const int lc = c - p.seq_chunk0[owner];
+      ci.x = p.seq_bos[owner] + lc * CH;
+      ci.y = min(CH, p.seq_len[owner] - lc * CH);
+    }
+    p.chunk_info[c] = ci;
   }
   for (int s = tid; s < S_max; s += nt) {
     int owner = -1;
