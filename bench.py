@@ -81,12 +81,12 @@ def job_throughput(total_ms, world, tokens_per_rank_step, steps):
 # keyed by (profiler name, workload); valid only while the kernel's sources hash to the value
 # recorded with it (otherwise the roofline reports traffic null).  Summaries: profiles/*.md.
 NCU_TRAFFIC = {
-    ("bwd_local", "prefill_h32_t8192"): (1023317504, "bwd_local_tc.cu", "2b10173a98719041"),
-    ("fwd_chunk", "prefill_h32_t8192"): (596598784, "fwd_tc.cu", "25853474f9671c9b"),
-    ("fwd_prep", "prefill_h32_t8192"): (514280448, "fwd_prep_tc.cu", "1f85f4302ede08ed"),
-    ("bwd_chain", "prefill_h32_t8192"): (533453568, "bwd_chain_tc.cu", "f34997149f510216"),
+    ("bwd_local", "prefill_h32_t8192"): (1022339328, "bwd_local_tc.cu", "d6dc67b66c8c8162"),
+    ("fwd_chunk", "prefill_h32_t8192"): (600946432, "fwd_tc.cu", "e6eb3984ae98a05a"),
+    ("fwd_prep", "prefill_h32_t8192"): (514387200, "fwd_prep_tc.cu", "fbd4b2d30d963b99"),
+    ("bwd_chain", "prefill_h32_t8192"): (537454080, "bwd_chain_tc.cu", "bc219a07a1b3f541"),
 }
-KERNEL_COMMON = ["chunk_common.cuh", "umma.cuh", "common.cuh", "kernels.h", "fixup.cuh"]
+KERNEL_COMMON = ["chunk_common.cuh", "umma.cuh", "common.cuh", "kernels.h", "fixup.cuh", "modes.cuh"]
 
 
 def measured_traffic(kernel, workload):
