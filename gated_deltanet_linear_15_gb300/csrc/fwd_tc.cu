@@ -410,7 +410,7 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
         v[i] *= gC;
       }
       if (bad && err) atomicOr(err, 1);
-      tmem_st32(tm + tm_lane + TM_S + c0, v);
+      tmem_st32_issue(tm + tm_lane + TM_S + c0, v);  // completed before A4 (MMA 4 accumulates onto it)
     }
     {  // MMA 2 (its own barrier, one completion per chunk)
       failed |= !mbar_wait(u32(&sm.bar_mma2), mma2_phase, err, 4);
@@ -462,6 +462,7 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
       st_chunk_f16(sm.uc + chunk_off(row, c0), v);
       st_chunk_f16(sm.uc + chunk_off(row, c0 + 8), v + 8);
     }
+    tmem_wait_st();  // gam_C * S0, written back by the state copy
     fence_before();
     fence_async_smem();
     if (__syncthreads_or(failed)) {  // A4: the producer stores Ut^T and issues MMA 4
@@ -473,6 +474,7 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
     failed |= !mma_wait();  // MMA 4
   }
 
+  tmem_wait_st();  // a loop left early may leave the state write-back in flight
   // ---------------------------------------------------------------- the last chunk's o
   {
     const int cl = cend - 1;

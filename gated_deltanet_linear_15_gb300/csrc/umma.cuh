@@ -250,7 +250,9 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t saddr, uint32_t (&r)[
                : "r"(saddr)
                : "memory");
 }
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+// 32 lanes x 32 columns of fp32 into TMEM; tmem_st32_issue leaves the store in flight (tmem_wait_st completes
+// every store this thread issued), tmem_st32 waits for it
+__device__ __forceinline__ void tmem_st32_issue(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
       "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
@@ -265,7 +267,11 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
       "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])),
       "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
       : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  tmem_st32_issue(taddr, v);
+  tmem_wait_st();
 }
 
 // ------------------------------------------------------------------ mbarriers
