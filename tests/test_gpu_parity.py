@@ -84,6 +84,9 @@ def test_balanced_recurrent_grid():
     for window in (True, False):
         for saved in (False, True):
             compare(run_gpu(x, seg_chunks=2, seg_first=1, window=window, saved=saved), ref, TOL["bf16"])
+    # two sequences of 16 heads: the same 32 (sequence, head) pairs, segment indices across sequences
+    x = make_inputs("train_b4_h16_t4096", DEV, B=2, T=64 * 8 + 40, H=H // 2, with_S0=True, with_dST=True, seed=7)
+    compare(run_gpu(x, seg_chunks=2, seg_first=1, saved=True), run_oracle(x), TOL["bf16"])
 
 
 def test_sp_on_off_agree():
