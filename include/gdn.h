@@ -111,10 +111,15 @@ size_t gdn_bwd_workspace_size(const gdn_shape *shape);
  * Steps (all in sm_103a kernels on `stream`): segment plan from cu_seqlens;
  * gate scan (per-chunk log-decay sums, which mark segment starts inside an
  * effective sliding window -- onedev.kr talk summary, paragraph on the
- * effective sliding window); pass A over segments whose start must be
- * corrected (state from zero plus the composed d_k x d_k transition --
- * paragraph on parallelism); the sequential start-state fix-up; pass B, the
- * fused WY + state pass + output over every segment.  With bf16, d = 128 and
+ * effective sliding window; with bf16 and d = 128 the chunk-local half of the
+ * forward forms these sums and decisions itself, no separate launch); pass A
+ * over segments whose start must be corrected (state from zero plus the
+ * composed d_k x d_k transition -- paragraph on parallelism); the sequential
+ * start-state fix-up; pass B, the WY + state pass + output over every
+ * segment (bf16, d = 128: the chunk-local half of every chunk, then the
+ * recurrent half; equal-length batches may give each sequence a shorter
+ * first segment, see seg_first, so that the recurrent passes fill the SMs in
+ * one wave).  With bf16, d = 128 and
  * GDN_SP_SINGLE_LAUNCH, pass A, the fix-up and pass B are one launch: its CTAs
  * take work items in start order from lists the gate scan builds, and an item
  * that needs others' results (a fix-up, a fixed-up segment) waits for them
