@@ -663,6 +663,7 @@ int forward_passes(const gdn_shape *s, const Layout &L, char *ws, FwdArgs fa, in
     fx.flags = fa.flags;
     fx.reverse = 0;
     fx.fixflag = fa.status + 1;
+    fx.status = fa.status;
     PROF("fixup_fwd");
     CK(launch_fixup(fx, L.N, st));
   }
@@ -885,6 +886,7 @@ int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
     fx.flags = s->flags;
     fx.reverse = 1;
     fx.fixflag = ba.status + 2;
+    fx.status = ba.status;
     PROF("fixup_bwd");
     CK(launch_fixup(fx, L.N, st));
   }

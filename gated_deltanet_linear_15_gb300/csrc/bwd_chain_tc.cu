@@ -496,6 +496,7 @@ __global__ void __launch_bounds__(NTHREADS + 32, 1)
       fx.flags = a.flags;
       fx.reverse = 1;
       fx.fixflag = nullptr;
+      fx.status = a.status;
       extern __shared__ unsigned char smraw[];
       fixup_rows<D>(fx, t % NRB, pair % a.H, pair / a.H,
                     reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023));

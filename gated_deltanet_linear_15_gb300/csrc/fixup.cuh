@@ -3,27 +3,30 @@
 // summaries (onedev.kr FlashQLA talk summary, paragraph on parallelism).  One row block (FIX_ROWS rows
 // of the state) per call, run by threads 0-255 of a CTA, which synchronise on named barrier 1.  The
 // composition is serial over segments, but every step's inputs (M_j and E_j's rows) are independent of
-// the chain, so they stream through a two-stage shared-memory ring by cp.async: step i computes while
-// step i + 1's transition lands.  The segment start modes (which segments take the fix-up at all) are
+// the chain, so they stream through a two-stage shared-memory ring, two bulk copies per step issued by
+// one thread on the stage's mbarrier: step i computes while step i + 1's transition lands.  The segment start modes (which segments take the fix-up at all) are
 // decided up front, one segment per thread.  Used by the stand-alone fix-up kernel and, as a work item
 // of the single-launch sequence parallelism, by the tcgen05 recurrent kernels.
 #pragma once
 #include "kernels.h"
+#include "umma.cuh"
 
 namespace gdn {
 
 constexpr int FIX_MODES = 2048;  // segments per sequence whose modes are kept in shared memory
 
-// shared memory of one fix-up row block: the ring, cur, the working steps and the modes
+// shared memory of one fix-up row block: the ring, cur, the working steps, the modes, the step count and
+// the ring's two mbarriers
 template <int D> constexpr size_t fixup_smem_bytes() {
   return 2 * ((size_t)D * D + FIX_ROWS * D) * sizeof(float) + FIX_ROWS * D * sizeof(float) + FIX_MODES * 2 +
-         FIX_MODES + 16;
+         FIX_MODES + 32;
 }
 
 __device__ __forceinline__ void fix_bar() { asm volatile("bar.sync 1, 256;\n" ::: "memory"); }
 
 template <int D>
 __device__ __forceinline__ void fixup_rows(const FixupArgs &a, int rb, int h, int n, unsigned char *smem) {
+  using namespace umma;
   const int H = a.H;
   const int tid = threadIdx.x;
   const size_t DD = (size_t)D * D;
@@ -32,6 +35,7 @@ __device__ __forceinline__ void fixup_rows(const FixupArgs &a, int rb, int h, in
   short *work = reinterpret_cast<short *>(ring + 2 * (DD + FIX_ROWS * D) + FIX_ROWS * D);
   signed char *fix_mode = reinterpret_cast<signed char *>(work + FIX_MODES);
   int *nwork = reinterpret_cast<int *>(fix_mode + FIX_MODES);
+  uint64_t *fbar = reinterpret_cast<uint64_t *>(fix_mode + FIX_MODES + 8);  // stage s lands on fbar[s]
   if (a.fixflag && *a.fixflag == 0) return;  // no segment of this direction needs the exact fix-up
   const int nseg = a.plan.seq_nseg[n];
   if (nseg <= 1) return;
@@ -77,19 +81,31 @@ __device__ __forceinline__ void fixup_rows(const FixupArgs &a, int rb, int h, in
     withM = start_mode(a.reverse ? jt + 1 : jt - 1) == START_FIXUP;
     return true;
   };
-  auto issue = [&](int i) {  // cp.async of step i's M (if used) and E rows into stage i & 1
+  if (tid == 0) {
+    mbar_init(smem_u32(&fbar[0]), 1);
+    mbar_init(smem_u32(&fbar[1]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  fix_bar();
+  // thread 0: step i's M (if used) and E rows into stage i & 1 by two bulk copies; a step with nothing to
+  // load completes its stage's phase by a plain arrival
+  auto issue = [&](int i) {
+    if (tid != 0 || i >= nw) return;
     int jt;
     bool withM;
-    if (i < nw && step_of(i, jt, withM)) {
+    const uint32_t bar = smem_u32(&fbar[i & 1]);
+    if (step_of(i, jt, withM)) {
       const int js = a.reverse ? jt + 1 : jt - 1;
       const size_t src = ((size_t)(seg0 + js) * H + h) * DD;
       float *st = ring + (size_t)(i & 1) * (DD + FIX_ROWS * D);
-      if (withM)
-        for (int e = tid; e < (int)(DD / 4); e += 256) cp_async16(st + 4 * e, a.M + src + 4 * e, true);
-      for (int e = tid; e < FIX_ROWS * D / 4; e += 256)
-        cp_async16(st + DD + 4 * e, a.E + src + (size_t)rb * FIX_ROWS * D + 4 * e, true);
+      fence_async_smem();  // the stage's last generic reads (before the caller's barrier) precede the copies
+      mbar_expect_tx(bar, (uint32_t)(((withM ? DD : 0) + FIX_ROWS * D) * sizeof(float)));
+      if (withM) bulk_load(smem_u32(st), a.M + src, (uint32_t)(DD * sizeof(float)), bar);
+      bulk_load(smem_u32(st + DD), a.E + src + (size_t)rb * FIX_ROWS * D, (uint32_t)(FIX_ROWS * D * sizeof(float)),
+                bar);
+    } else {
+      mbar_arrive(bar);
     }
-    cp_async_commit();  // one group per step, empty or not
   };
   issue(0);
   issue(1);
@@ -97,7 +113,9 @@ __device__ __forceinline__ void fixup_rows(const FixupArgs &a, int rb, int h, in
     int jt;
     bool withM;
     const bool active = step_of(i, jt, withM);
-    asm volatile("cp.async.wait_group 1;\n" ::: "memory");  // step i's group has landed (i + 1's may be in flight)
+    // step i's inputs have landed (step i + 1's may be in flight); an expired wait is recorded and the
+    // composition goes on (its result is then not to be trusted)
+    mbar_wait(smem_u32(&fbar[i & 1]), (i >> 1) & 1, a.status, 4);
     fix_bar();
     if (active) {
       const float *st = ring + (size_t)(i & 1) * (DD + FIX_ROWS * D);
@@ -136,7 +154,11 @@ __device__ __forceinline__ void fixup_rows(const FixupArgs &a, int rb, int h, in
     }
     issue(i + 2);  // into the stage just read
   }
-  asm volatile("cp.async.wait_all;\n" ::: "memory");
+  fix_bar();  // every wait on the ring's barriers is done (every issued step was awaited)
+  if (tid == 0) {
+    mbar_inval(smem_u32(&fbar[0]));
+    mbar_inval(smem_u32(&fbar[1]));
+  }
 }
 
 }  // namespace gdn

@@ -107,6 +107,7 @@ struct FixupArgs {
   unsigned flags;
   int reverse;
   const int *fixflag;  // nonzero iff some segment of this direction needs the fix-up (NULL: always run)
+  int *status;         // status word (an expired wait for a step's inputs sets value 4), or NULL
 };
 
 struct RecArgs {
