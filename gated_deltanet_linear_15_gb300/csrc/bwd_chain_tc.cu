@@ -62,7 +62,7 @@ __device__ __forceinline__ void chain_tc_item(const BwdArgs &a, const CUtensorMa
   extern __shared__ unsigned char smraw[];
   ChainTcSmem &sm =
       *reinterpret_cast<ChainTcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
-  // pass A of a call in which no segment needs the exact fix-up (status[2], set after the gate scan)
+  // pass A of a call in which no segment needs the exact fix-up (status[2], set by the fix-up mode scan)
   if (pass == 0 && a.status && a.status[2] == 0) return;
   const int H = a.H;
   const int n = a.plan.seg_seq[s];

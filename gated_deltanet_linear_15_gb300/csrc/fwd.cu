@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_chunk_kernel(FwdArgs a) {
   SM &sm = *reinterpret_cast<SM *>(smraw);
 
   const int s = blockIdx.x, h = blockIdx.y, role = blockIdx.z;
-  // pass A of a call in which no segment needs the exact fix-up (status[1], set after the gate scan)
+  // pass A of a call in which no segment needs the exact fix-up (status[1], set by the fix-up mode scan)
   if (a.pass == 0 && a.status && a.status[1] == 0) return;
   const int H = a.H;
   const int n = a.plan.seg_seq[s];

@@ -80,7 +80,7 @@ __device__ __forceinline__ void fwd_tc_item(const FwdArgs &a, const CUtensorMap 
                                             int s, int h, int role, int pass, bool &have_tm) {
   extern __shared__ unsigned char smraw[];
   TcSmem &sm = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
-  // pass A of a call in which no segment needs the exact fix-up (status[1], set after the gate scan)
+  // pass A of a call in which no segment needs the exact fix-up (status[1], set by the fix-up mode scan)
   if (pass == 0 && a.status && a.status[1] == 0) return;
   const int H = a.H;
   const int n = a.plan.seg_seq[s];

@@ -16,7 +16,7 @@ constexpr unsigned kFlagDebugPeerTimeout = 0x40000000u;  // test hook, see gdn.h
 
 // Single-launch sequence parallelism (bf16, d = 128): one launch of a recurrent kernel runs pass A, the
 // start-state fix-up and pass B.  Each CTA takes a ticket (an atomic counter) when it starts and runs the
-// ticket-th item of the work lists that the gate scan built on the device, in this order: the pass-A items
+// ticket-th item of the work lists that the fix-up mode scan built on the device, in this order: the pass-A items
 // that some fix-up needs, the pass-B items whose start needs no fix-up, the fix-up row blocks, the pass-B
 // items whose start is fixed up.  An item waits (bounded) only for items of lower tickets, which belong to
 // CTAs that started earlier: fix-up blocks for their (sequence, head)'s pass-A items, fixed-up pass-B items
