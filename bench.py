@@ -81,10 +81,10 @@ def job_throughput(total_ms, world, tokens_per_rank_step, steps):
 # keyed by (profiler name, workload); valid only while the kernel's sources hash to the value
 # recorded with it (otherwise the roofline reports traffic null).  Summaries: profiles/*.md.
 NCU_TRAFFIC = {
-    ("bwd_local", "prefill_h32_t8192"): (1022503680, "bwd_local_tc.cu", "910d9e4f6b81a7e0"),
-    ("fwd_chunk", "prefill_h32_t8192"): (600303104, "fwd_tc.cu", "5f54f4827e12f2e0"),
-    ("fwd_prep", "prefill_h32_t8192"): (514050304, "fwd_prep_tc.cu", "942073167d14c1f8"),
-    ("bwd_chain", "prefill_h32_t8192"): (537549568, "bwd_chain_tc.cu", "ee36be83652d766f"),
+    ("bwd_local", "prefill_h32_t8192"): (1022306048, "bwd_local_tc.cu", "99864d8a2a3336ea"),
+    ("fwd_chunk", "prefill_h32_t8192"): (600349184, "fwd_tc.cu", "9623116358409c74"),
+    ("fwd_prep", "prefill_h32_t8192"): (514352128, "fwd_prep_tc.cu", "362db0708daf7616"),
+    ("bwd_chain", "prefill_h32_t8192"): (537823744, "bwd_chain_tc.cu", "1908e0d22e2f500f"),
 }
 KERNEL_COMMON = ["chunk_common.cuh", "umma.cuh", "common.cuh", "kernels.h", "fixup.cuh", "modes.cuh"]
 
