@@ -11,7 +11,9 @@
 // dot products per token are warp butterflies.  Grid: (sequence x head,
 // D / (8 * RPW)) CTAs of 8 warps.  HBM traffic is the state read and written
 // once per call plus the token inputs, all in coalesced 16-byte (or 8-byte)
-// accesses.
+// accesses.  The token inputs are staged in shared memory 16 tokens at a time
+// (k normalised and q scaled once per CTA), so the token loop waits on shared
+// memory, not on global loads.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -20,6 +22,7 @@ namespace gdn {
 namespace {
 
 constexpr int RPW = 8;  // state rows per warp (the joint reductions below assume eight)
+constexpr int TB = 16;  // tokens staged in shared memory at a time
 
 __device__ __forceinline__ float bsum(float x) {
 #pragma unroll
@@ -78,13 +81,18 @@ __global__ void __launch_bounds__(256) recurrent_kernel(RecArgs a) {
   constexpr int EPL = D / 32;
   const int nh = blockIdx.x, H = a.H, n = nh / H, h = nh % H;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row0 = (blockIdx.y * 8 + warp) * RPW;
+  const int rowc = blockIdx.y * 8 * RPW;  // this CTA's first state row
+  const int row0 = rowc + warp * RPW;     // this warp's
   const size_t sbase = (size_t)nh * D * D;
   const bool l2 = (a.flags & kFlagL2Norm) != 0;
   const I *q = static_cast<const I *>(a.q);
   const I *k = static_cast<const I *>(a.k);
   const I *v = static_cast<const I *>(a.v);
   I *o = static_cast<I *>(a.o);
+  // the token inputs of TB tokens at a time, staged in shared memory with k normalised and q scaled once
+  // per CTA (not once per warp), so that the token loop reads them at shared-memory latency
+  __shared__ __align__(16) float ks[TB][D], qs[TB][D], vs[TB][8 * RPW];
+  __shared__ float as[TB], bs[TB];
 
   float s[RPW][EPL];
 #pragma unroll
@@ -97,68 +105,80 @@ __global__ void __launch_bounds__(256) recurrent_kernel(RecArgs a) {
     }
   }
 
-  // token inputs one token ahead, so their load latency hides behind the previous token's work
-  float kn[EPL], qn[EPL], vn[RPW], gn = 0.f, bn = 0.f;
-  auto fetch = [&](int t) {
-    const size_t tok = ((size_t)n * a.T + t) * H + h;
-    load_vec<I, EPL>(k + tok * D + lane * EPL, kn);
-    load_vec<I, EPL>(q + tok * D + lane * EPL, qn);
+  for (int t0 = 0; t0 < a.T; t0 += TB) {
+    const int nt = min(TB, a.T - t0);
+    // ---- stage tokens t0 .. t0 + nt - 1: warp w takes tokens w, w + 8 (k, q and their norms); every
+    // thread four of the CTA's v entries; threads 0 .. nt - 1 the gates
+    for (int tt = warp; tt < nt; tt += 8) {
+      const size_t tok = ((size_t)n * a.T + t0 + tt) * H + h;
+      float kk[EPL], qq[EPL];
+      load_vec<I, EPL>(k + tok * D + lane * EPL, kk);
+      load_vec<I, EPL>(q + tok * D + lane * EPL, qq);
+      float km = 1.f, qm = a.scale;
+      if (l2) {
+        float sk = 0.f, sq = 0.f;
 #pragma unroll
-    for (int r = 0; r < RPW; ++r) vn[r] = tof(v[tok * D + row0 + r]);
-    gn = a.g[tok];
-    bn = a.beta[tok];
-  };
-  if (a.T > 0) fetch(0);
-  for (int t = 0; t < a.T; ++t) {
-    const size_t tok = ((size_t)n * a.T + t) * H + h;
-    float kk[EPL], qq[EPL], vv[RPW];
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      kk[e] = kn[e];
-      qq[e] = qn[e];
-    }
-#pragma unroll
-    for (int r = 0; r < RPW; ++r) vv[r] = vn[r];
-    const float alpha = expf(gn), bt = bn;
-    if (t + 1 < a.T) fetch(t + 1);
-    float qmul = a.scale;
-    if (l2) {
-      float sk = 0.f, sq = 0.f;
+        for (int e = 0; e < EPL; ++e) {
+          sk = fmaf(kk[e], kk[e], sk);
+          sq = fmaf(qq[e], qq[e], sq);
+        }
+        km = rsqrtf(bsum(sk) + 1e-6f);
+        qm *= rsqrtf(bsum(sq) + 1e-6f);
+      }
 #pragma unroll
       for (int e = 0; e < EPL; ++e) {
-        sk = fmaf(kk[e], kk[e], sk);
-        sq = fmaf(qq[e], qq[e], sq);
-      }
-      const float rk = rsqrtf(bsum(sk) + 1e-6f);
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) kk[e] *= rk;
-      qmul *= rsqrtf(bsum(sq) + 1e-6f);
-    }
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) qq[e] *= qmul;
-    float dk[RPW], dq[RPW];
-#pragma unroll
-    for (int r = 0; r < RPW; ++r) {
-      dk[r] = 0.f;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        s[r][e] *= alpha;
-        dk[r] = fmaf(s[r][e], kk[e], dk[r]);
+        ks[tt][lane * EPL + e] = kk[e] * km;
+        qs[tt][lane * EPL + e] = qq[e] * qm;
       }
     }
-    const float dkr = tsum8(dk);  // row (lane >> 2)'s S k, then broadcast to every lane
-#pragma unroll
-    for (int r = 0; r < RPW; ++r) {
-      const float u = bt * (vv[r] - __shfl_sync(0xffffffffu, dkr, 4 * r));
-      dq[r] = 0.f;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        s[r][e] = fmaf(u, kk[e], s[r][e]);
-        dq[r] = fmaf(s[r][e], qq[e], dq[r]);
-      }
+    for (int i = threadIdx.x; i < nt * 8 * RPW; i += blockDim.x) {
+      const int tt = i / (8 * RPW), r = i % (8 * RPW);
+      vs[tt][r] = tof(v[(((size_t)n * a.T + t0 + tt) * H + h) * D + rowc + r]);
     }
-    const float out = tsum8(dq);  // row (lane >> 2)'s S q
-    if ((lane & 3) == 0) o[tok * D + row0 + (lane >> 2)] = fromf<I>(out);
+    if (threadIdx.x < nt) {
+      const size_t tok = ((size_t)n * a.T + t0 + threadIdx.x) * H + h;
+      as[threadIdx.x] = expf(a.g[tok]);
+      bs[threadIdx.x] = a.beta[tok];
+    }
+    __syncthreads();
+    for (int tt = 0; tt < nt; ++tt) {
+      float kk[EPL], qq[EPL], vv[RPW];
+      load_row<D>(&ks[tt][lane * EPL], kk);
+      load_row<D>(&qs[tt][lane * EPL], qq);
+#pragma unroll
+      for (int r = 0; r < RPW; r += 4) {
+        const float4 t4 = *reinterpret_cast<const float4 *>(&vs[tt][warp * RPW + r]);
+        vv[r] = t4.x;
+        vv[r + 1] = t4.y;
+        vv[r + 2] = t4.z;
+        vv[r + 3] = t4.w;
+      }
+      const float alpha = as[tt], bt = bs[tt];
+      float dk[RPW], dq[RPW];
+#pragma unroll
+      for (int r = 0; r < RPW; ++r) {
+        dk[r] = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          s[r][e] *= alpha;
+          dk[r] = fmaf(s[r][e], kk[e], dk[r]);
+        }
+      }
+      const float dkr = tsum8(dk);  // row (lane >> 2)'s S k, then broadcast to every lane
+#pragma unroll
+      for (int r = 0; r < RPW; ++r) {
+        const float u = bt * (vv[r] - __shfl_sync(0xffffffffu, dkr, 4 * r));
+        dq[r] = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          s[r][e] = fmaf(u, kk[e], s[r][e]);
+          dq[r] = fmaf(s[r][e], qq[e], dq[r]);
+        }
+      }
+      const float out = tsum8(dq);  // row (lane >> 2)'s S q
+      if ((lane & 3) == 0) o[(((size_t)n * a.T + t0 + tt) * H + h) * D + row0 + (lane >> 2)] = fromf<I>(out);
+    }
+    __syncthreads();  // the staged block is read before the next one overwrites it
   }
 
 #pragma unroll

@@ -25,7 +25,7 @@ def _check(o, S, ref_o, ref_S, dtype):
 
 
 @pytest.mark.parametrize("dtype,D", [("bf16", 128), ("bf16", 64), ("fp32", 64), ("fp32", 128)])
-@pytest.mark.parametrize("T", [1, 5])
+@pytest.mark.parametrize("T", [1, 5, 37])  # 37: tokens staged in blocks of 16 with a ragged last block
 @pytest.mark.parametrize("with_S0", [True, False])
 @pytest.mark.parametrize("unit_keys", [False, True])
 def test_recurrent_matches_oracle(dtype, D, T, with_S0, unit_keys):
