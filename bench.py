@@ -621,7 +621,8 @@ def main():
             "data": "synthetic (seeded gdn_inputs; q,k raw Gaussian with in-kernel L2 norm)",
             "config": {"workload": args.workload, "B": x["q"].shape[0], "T": x["q"].shape[1], "H": H, "d": D,
                        "chunk": 64, "l2norm_in_kernel": x["l2norm"], "initial_state": x["S0"] is not None,
-                       "seg_chunks": plan["seg_chunks"], "l2": "256 MB flush before every step, outside the events",
+                       "seg_chunks": plan["seg_chunks"], "seg_first": plan["seg_first"],
+                       "l2": "256 MB flush before every step, outside the events",
                        "pair": "recompute" if args.recompute else "saved_context",
                        "saved_bytes": 0 if args.recompute else saved_bytes,
                        "parallelism": f"replica x{world}"},
