@@ -90,6 +90,29 @@ def test_reserved_must_be_zero(lib):
     assert _fwd(lib, s) == _lib.GDN_ERR_INVALID_ARG
 
 
+def test_automatic_plan_balances_the_prefill_shape(lib):
+    """H=32, T=8192 (128 chunks per head) on a GPU of 129-159 SMs: four segments per head leave SMs
+    idle and five do not fit one wave, so the automatic plan gives each sequence a shorter first segment
+    (at least 8 chunks, so the next segment's warm-up is never cut short) and four later ones that fill
+    the rest, 5 segments in all; the model's estimate is finite and positive."""
+    import torch
+    if torch.cuda.is_available():  # without a GPU the library plans for 148 SMs
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        if not 128 < sms < 160:
+            pytest.skip(f"{sms} SMs: another plan is the right one")
+    s = _shape(T=8192, H=32)
+    L, S, C, F = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    assert lib.gdn_plan_query(ctypes.byref(s), ctypes.byref(L), ctypes.byref(S), ctypes.byref(C), ctypes.byref(F)) == 0
+    assert S.value == 5 and 8 <= F.value < L.value and F.value + 4 * L.value >= 128 > F.value + 3 * L.value
+    f, b = ctypes.c_double(), ctypes.c_double()
+    assert lib.gdn_plan_estimate(ctypes.byref(s), ctypes.byref(f), ctypes.byref(b)) == 0
+    assert 0 < f.value < 1e4 and 0 < b.value < 1e4
+    # the d = 64 / fp32 kernels keep one segment length
+    s = _shape(T=8192, H=32, Dk=64, Dv=64, dtype=_lib.GDN_FP32)
+    assert lib.gdn_plan_query(ctypes.byref(s), ctypes.byref(L), ctypes.byref(S), ctypes.byref(C), ctypes.byref(F)) == 0
+    assert F.value == L.value
+
+
 def test_first_segment_length_in_plan(lib):
     """seg_first sets the first segment of every sequence, seg_chunks the later ones: 130 chunks as
     3 + 127 / 8 -> 1 + 16 segments per sequence (the sequence-parallel buffers grow with the count)."""
