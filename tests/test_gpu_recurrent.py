@@ -1,8 +1,9 @@
 """GPU parity of the token-by-token (decode) entry point gdn_recurrent_fwd against
 the fp64 oracle: output o and final state for B sequences of T tokens, in bf16
 and fp32, d = 64 and 128, with and without an initial state and the in-kernel
-L2 norm; the in-place state update; T = 0; and a chunked prefill continued by
-recurrent decode steps, against the oracle run over the whole sequence."""
+L2 norm; gates at the extremes (strong decay, alpha = 0, alpha ~ 1 runs); the
+in-place state update; T = 0; and a chunked prefill continued by recurrent decode
+steps, against the oracle run over the whole sequence."""
 import pytest
 import torch
 
@@ -34,6 +35,22 @@ def test_recurrent_matches_oracle(dtype, D, T, with_S0, unit_keys):
     o, S = g.recurrent_gated_delta_rule(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], x["scale"],
                                         x["l2norm"])
     torch.cuda.synchronize()
+    ref_o, ref_S = _oracle(x, x["S0"])
+    _check(o, S, ref_o, ref_S, dtype)
+
+
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("bf16", 64), ("fp32", 128)])
+@pytest.mark.parametrize("gate", ["uniform_8_2", "alpha0_heads", "runs_0_6"])
+def test_recurrent_gate_extremes(dtype, D, gate):
+    """Strong decay (g ~ U[-8, -2]: the running gate product leaves fp32's normal range within a few
+    tokens), alpha = 0 in even heads, and runs of alpha ~ 1 broken by g = -6, over 70 tokens (five staged
+    blocks, the last one ragged), with an initial state."""
+    x = make_inputs("train_b4_h16_t4096", "cuda", T=70, B=2, H=4, D=D, dtype=dtype, with_S0=True, gate=gate,
+                    seed=23)
+    o, S = g.recurrent_gated_delta_rule(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], x["scale"],
+                                        x["l2norm"])
+    torch.cuda.synchronize()
+    assert torch.isfinite(o).all() and torch.isfinite(S).all()
     ref_o, ref_S = _oracle(x, x["S0"])
     _check(o, S, ref_o, ref_S, dtype)
 
