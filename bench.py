@@ -78,32 +78,52 @@ def job_throughput(total_ms, world, tokens_per_rank_step, steps):
 
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture,
-# keyed by (profiler name, workload); valid only while the kernel's sources hash to the value
-# recorded with it (otherwise the roofline reports traffic null).  Summaries: profiles/*.md.
+# keyed by (profiler name, workload); valid only while the kernel's translation unit (its .cu file and
+# the local headers it includes, transitively) hashes to the value recorded with it (otherwise the
+# roofline reports traffic null).  Summaries: profiles/*.md.
 NCU_TRAFFIC = {
-    ("bwd_local", "prefill_h32_t8192"): (1022306048, "bwd_local_tc.cu", "99864d8a2a3336ea"),
-    ("fwd_chunk", "prefill_h32_t8192"): (600349184, "fwd_tc.cu", "9623116358409c74"),
-    ("fwd_prep", "prefill_h32_t8192"): (514352128, "fwd_prep_tc.cu", "362db0708daf7616"),
-    ("bwd_chain", "prefill_h32_t8192"): (537823744, "bwd_chain_tc.cu", "1908e0d22e2f500f"),
+    ("bwd_local", "prefill_h32_t8192"): (1022306048, "bwd_local_tc.cu", "57964d101249e66e"),
+    ("fwd_chunk", "prefill_h32_t8192"): (600349184, "fwd_tc.cu", "e8168e6a4ba20a9d"),
+    ("fwd_prep", "prefill_h32_t8192"): (514352128, "fwd_prep_tc.cu", "3037a1075ea78ed0"),
+    ("bwd_chain", "prefill_h32_t8192"): (537823744, "bwd_chain_tc.cu", "ca7f3649f44b73f8"),
 }
-KERNEL_COMMON = ["chunk_common.cuh", "umma.cuh", "common.cuh", "kernels.h", "fixup.cuh", "modes.cuh"]
+
+
+def kernel_sources(src):
+    """The files of a kernel's translation unit: src and the local headers it includes, transitively."""
+    import re
+    csrc = os.path.join(ROOT, "gated_deltanet_linear_15_gb300", "csrc")
+    seen, todo = set(), [src]
+    while todo:
+        f = todo.pop()
+        if f in seen:
+            continue
+        seen.add(f)
+        with open(os.path.join(csrc, f)) as fh:
+            todo += re.findall(r'^\s*#include "([^"]+)"', fh.read(), flags=re.M)
+    return sorted(seen)
+
+
+def source_digest(src):
+    import hashlib
+    m = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gated_deltanet_linear_15_gb300", "csrc")
+    for f in kernel_sources(src):
+        m.update(f.encode())
+        with open(os.path.join(csrc, f), "rb") as fh:
+            m.update(fh.read())
+    return m.hexdigest()[:16]
 
 
 def measured_traffic(kernel, workload):
-    import hashlib
     ent = NCU_TRAFFIC.get((kernel, workload))
     if ent is None:
         return None
     nbytes, src, digest = ent
-    m = hashlib.sha256()
-    csrc = os.path.join(ROOT, "gated_deltanet_linear_15_gb300", "csrc")
     try:
-        for f in [src] + KERNEL_COMMON:
-            with open(os.path.join(csrc, f), "rb") as fh:
-                m.update(fh.read())
+        return nbytes if source_digest(src) == digest else None
     except OSError:
         return None
-    return nbytes if m.hexdigest()[:16] == digest else None
 
 
 def load_peaks():

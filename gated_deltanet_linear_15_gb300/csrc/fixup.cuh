@@ -15,11 +15,17 @@ namespace gdn {
 
 constexpr int FIX_MODES = 2048;  // segments per sequence whose modes are kept in shared memory
 
-// shared memory of one fix-up row block: the ring, cur, the working steps, the modes, the step count and
-// the ring's two mbarriers
+// The product cur M of a step: thread t takes the column pair t % (D/2) of all FIX_ROWS rows over one of
+// the 512 / D parts of the k range, so that every element of M read from shared memory serves all
+// FIX_ROWS rows; the parts' sums meet in shared memory.
+static_assert(FIX_ROWS == 8, "the product reads a column of cur as two float4");
+template <int D> __host__ __device__ constexpr int fix_kparts() { return 256 / (D / 2); }
+
+// shared memory of one fix-up row block: the ring, cur (transposed: [k][row]), the partial sums, the
+// working steps, the modes, the step count and the ring's two mbarriers
 template <int D> constexpr size_t fixup_smem_bytes() {
-  return 2 * ((size_t)D * D + FIX_ROWS * D) * sizeof(float) + FIX_ROWS * D * sizeof(float) + FIX_MODES * 2 +
-         FIX_MODES + 32;
+  return 2 * ((size_t)D * D + FIX_ROWS * D) * sizeof(float) + FIX_ROWS * D * sizeof(float) +
+         (size_t)fix_kparts<D>() * FIX_ROWS * D * sizeof(float) + FIX_MODES * 2 + FIX_MODES + 32;
 }
 
 __device__ __forceinline__ void fix_bar() { asm volatile("bar.sync 1, 256;\n" ::: "memory"); }
@@ -31,8 +37,10 @@ __device__ __forceinline__ void fixup_rows(const FixupArgs &a, int rb, int h, in
   const int tid = threadIdx.x;
   const size_t DD = (size_t)D * D;
   float *ring = reinterpret_cast<float *>(smem);                  // 2 stages of [M (D x D) | E rows]
-  float (*cur)[D] = reinterpret_cast<float (*)[D]>(ring + 2 * (DD + FIX_ROWS * D));
-  short *work = reinterpret_cast<short *>(ring + 2 * (DD + FIX_ROWS * D) + FIX_ROWS * D);
+  constexpr int NKP = fix_kparts<D>();  // parts of the k range
+  float *curT = ring + 2 * (DD + FIX_ROWS * D);  // [k][row]: the source segment's corrected rows
+  float *red = curT + FIX_ROWS * D;             // [part][row][column] partial sums
+  short *work = reinterpret_cast<short *>(red + NKP * FIX_ROWS * D);
   signed char *fix_mode = reinterpret_cast<signed char *>(work + FIX_MODES);
   int *nwork = reinterpret_cast<int *>(fix_mode + FIX_MODES);
   uint64_t *fbar = reinterpret_cast<uint64_t *>(fix_mode + FIX_MODES + 8);  // stage s lands on fbar[s]
@@ -42,10 +50,10 @@ __device__ __forceinline__ void fixup_rows(const FixupArgs &a, int rb, int h, in
   const int seg0 = a.plan.seq_seg0[n], chunk0 = a.plan.seq_chunk0[n];
   const int nchunks = (a.plan.seq_len[n] + CH - 1) / CH;
   const bool window = !(a.flags & kFlagWindowOff);
-  constexpr int CPT = D / 32;  // columns per thread
-  const int r = tid >> 5;
-  const int c0 = (tid & 31) * CPT;
-  const int row = rb * FIX_ROWS + r;
+  constexpr int NCP = D / 2, KPP = D / NKP;  // column pairs; k per part
+  const int cp = tid % NCP, kp = tid / NCP;   // product: columns 2 cp, 2 cp + 1, k in [kp KPP, kp KPP + KPP)
+  constexpr int RPT = FIX_ROWS * D / 256;     // sums: rows fr0 .. fr0 + RPT - 1 of column fc
+  const int fc = tid % D, fr0 = (tid / D) * RPT;
   // the start (end, reversed) mode of segment j
   auto start_mode = [&](int j) {
     int w;
@@ -119,35 +127,41 @@ __device__ __forceinline__ void fixup_rows(const FixupArgs &a, int rb, int h, in
     fix_bar();
     if (active) {
       const float *st = ring + (size_t)(i & 1) * (DD + FIX_ROWS * D);
-      float acc[CPT];
+      float v[RPT];  // E's rows, read before the barrier that lets the stage be refilled
 #pragma unroll
-      for (int t = 0; t < CPT; ++t) acc[t] = st[DD + r * D + c0 + t];
-      if (withM) {  // cur holds the corrected state of the source segment (the previous working step)
-#pragma unroll 8
-        for (int k = 0; k < D; ++k) {
-          const float x = cur[r][k];
-          float m[CPT];
-          if constexpr (CPT == 4) {
-            const float4 t4 = *reinterpret_cast<const float4 *>(st + (size_t)k * D + c0);
-            m[0] = t4.x;
-            m[1] = t4.y;
-            m[2] = t4.z;
-            m[3] = t4.w;
-          } else {
-            const float2 t2 = *reinterpret_cast<const float2 *>(st + (size_t)k * D + c0);
-            m[0] = t2.x;
-            m[1] = t2.y;
+      for (int t = 0; t < RPT; ++t) v[t] = st[DD + (fr0 + t) * D + fc];
+      if (withM) {  // curT holds the corrected state of the source segment (the previous working step)
+        float acc[FIX_ROWS][2] = {};
+        const float *mk = st + (size_t)kp * KPP * D + 2 * cp;
+        const float *xk = curT + kp * KPP * FIX_ROWS;
+#pragma unroll 4
+        for (int kk = 0; kk < KPP; ++kk) {
+          const float2 m = *reinterpret_cast<const float2 *>(mk + (size_t)kk * D);
+          const float4 x0 = *reinterpret_cast<const float4 *>(xk + kk * FIX_ROWS);
+          const float4 x1 = *reinterpret_cast<const float4 *>(xk + kk * FIX_ROWS + 4);
+          const float x[FIX_ROWS] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+          for (int r = 0; r < FIX_ROWS; ++r) {
+            acc[r][0] = fmaf(x[r], m.x, acc[r][0]);
+            acc[r][1] = fmaf(x[r], m.y, acc[r][1]);
           }
-#pragma unroll
-          for (int t = 0; t < CPT; ++t) acc[t] = fmaf(x, m[t], acc[t]);
         }
-      }
-      fix_bar();  // every thread has read cur and this stage
-      float *out = a.out + ((size_t)(seg0 + jt) * H + h) * DD + (size_t)row * D;
 #pragma unroll
-      for (int t = 0; t < CPT; ++t) {
-        cur[r][c0 + t] = acc[t];
-        out[c0 + t] = acc[t];
+        for (int r = 0; r < FIX_ROWS; ++r)
+          *reinterpret_cast<float2 *>(red + (kp * FIX_ROWS + r) * D + 2 * cp) = make_float2(acc[r][0], acc[r][1]);
+      }
+      fix_bar();  // every thread has read curT and this stage; the partial sums are written
+      if (withM) {
+#pragma unroll
+        for (int q = 0; q < NKP; ++q)
+#pragma unroll
+          for (int t = 0; t < RPT; ++t) v[t] += red[(q * FIX_ROWS + fr0 + t) * D + fc];
+      }
+      float *out = a.out + ((size_t)(seg0 + jt) * H + h) * DD + (size_t)(rb * FIX_ROWS + fr0) * D + fc;
+#pragma unroll
+      for (int t = 0; t < RPT; ++t) {
+        curT[fc * FIX_ROWS + fr0 + t] = v[t];
+        out[(size_t)t * D] = v[t];
       }
     } else {
       fix_bar();
