@@ -83,9 +83,9 @@ def job_throughput(total_ms, world, tokens_per_rank_step, steps):
 # roofline reports traffic null).  Summaries: profiles/*.md.
 NCU_TRAFFIC = {
     ("bwd_local", "prefill_h32_t8192"): (1022306048, "bwd_local_tc.cu", "57964d101249e66e"),
-    ("fwd_chunk", "prefill_h32_t8192"): (600349184, "fwd_tc.cu", "e8168e6a4ba20a9d"),
+    ("fwd_chunk", "prefill_h32_t8192"): (600421120, "fwd_tc.cu", "bdbd57d0cf46daba"),
     ("fwd_prep", "prefill_h32_t8192"): (514352128, "fwd_prep_tc.cu", "3037a1075ea78ed0"),
-    ("bwd_chain", "prefill_h32_t8192"): (537823744, "bwd_chain_tc.cu", "ca7f3649f44b73f8"),
+    ("bwd_chain", "prefill_h32_t8192"): (537797888, "bwd_chain_tc.cu", "1dbc4ee01d1e8903"),
 }
 
 
