@@ -648,7 +648,13 @@ int forward_passes(const gdn_shape *s, const Layout &L, char *ws, FwdArgs fa, in
     fa.pass = 0;
     {
       PROF("fwd_segment_pass_a");
-      CK(launch_forward_kernel(L, s, fa, dim3(L.S_max, L.H, 2), st));
+      dim3 grid(L.S_max, L.H, 2);
+      if (tc_forward(L, s)) {  // the (segment, head, role) items by ticket, at most one CTA per SM
+        fa.passA_items = 2 * L.S_max * L.H;
+        grid = dim3(std::min(fa.passA_items, num_sms()));
+      }
+      CK(launch_forward_kernel(L, s, fa, grid, st));
+      fa.passA_items = 0;
     }
     FixupArgs fx;
     fx.plan = fa.plan;
@@ -664,8 +670,9 @@ int forward_passes(const gdn_shape *s, const Layout &L, char *ws, FwdArgs fa, in
     fx.reverse = 0;
     fx.fixflag = fa.status + 1;
     fx.status = fa.status;
+    fx.ticket = fa.status + 6;  // the row blocks by ticket, at most one CTA per SM
     PROF("fixup_fwd");
-    CK(launch_fixup(fx, L.N, st));
+    CK(launch_fixup(fx, L.N, num_sms(), st));
   }
   fa.pass = pass;
   dim3 grid(L.S_max, L.H, 1);
@@ -871,7 +878,13 @@ int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
     ba.pass = 0;
     {
       PROF("bwd_chain_pass_a");
-      CK(chain(dim3(L.S_max, L.H, 2)));
+      dim3 grid(L.S_max, L.H, 2);
+      if (chain_tc) {  // the (segment, head, role) items by ticket, at most one CTA per SM
+        ba.passA_items = 2 * L.S_max * L.H;
+        grid = dim3(std::min(ba.passA_items, num_sms()));
+      }
+      CK(chain(grid));
+      ba.passA_items = 0;
     }
     FixupArgs fx;
     fx.plan = pl;
@@ -887,8 +900,9 @@ int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
     fx.reverse = 1;
     fx.fixflag = ba.status + 2;
     fx.status = ba.status;
+    fx.ticket = ba.status + 7;  // the row blocks by ticket, at most one CTA per SM
     PROF("fixup_bwd");
-    CK(launch_fixup(fx, L.N, st));
+    CK(launch_fixup(fx, L.N, num_sms(), st));
   }
   ba.pass = 1;
   {

@@ -565,6 +565,23 @@ __global__ void __launch_bounds__(FT + 32, 1)
     fwd_tc_release(have_tm);
     return;
   }
+  if (!SCHED && pass == 0 && a.passA_items > 0) {
+    // pass A by ticket (1-D grid of at most one CTA per SM): item t is role t & 1 of segment (t / 2) % S,
+    // head (t / 2) / S (S segments); a call whose segments need no exact fix-up returns at once
+    if (a.status && a.status[1] == 0) return;
+    const int S = a.passA_items / (2 * a.H);  // segments
+    __shared__ int tk;
+    for (;;) {
+      if (threadIdx.x == 0) tk = atomicAdd(a.status + 4, 1);
+      __syncthreads();
+      const int t = tk;
+      __syncthreads();  // every thread has its ticket before thread 0 takes the next one
+      if (t >= a.passA_items) break;
+      fwd_tc_item(a, tm3, tmw, tms, tmt, tmo, (t >> 1) % S, (t >> 1) / S, t & 1, 0, have_tm);
+    }
+    fwd_tc_release(have_tm);
+    return;
+  }
   if (SCHED) {
     // single-launch sequence parallelism: this CTA runs the ticket-th item of the work lists (see Sched)
     __shared__ int tk, ok;
@@ -597,6 +614,7 @@ __global__ void __launch_bounds__(FT + 32, 1)
       }
       __threadfence();
       FixupArgs fx;
+      fx.ticket = nullptr;
       fx.plan = a.plan;
       fx.gsum = a.gsum;
       fx.E = a.Ebuf;

@@ -60,6 +60,10 @@ struct FwdArgs {
   // (bal_pairs = 0: one CTA per (segment, head), grid (S_max, H)): a 1-D grid whose first bal_big CTAs take the
   // later segments one each and whose other CTAs share the first segments
   int bal_pairs, bal_ns, bal_big;
+  // bf16 with d = 128, pass 0 with passA_items = 2 S_max H > 0: a 1-D grid of at most one CTA per SM whose
+  // CTAs take the (segment, head, role) items t (role t & 1, segment (t / 2) % S_max, head (t / 2) / S_max)
+  // by ticket (status word 4), so that a pass with no work, or little, is one short wave
+  int passA_items;
 };
 
 // Chunk context tiles of every (chunk, head), fp16 row-major, written by the forward:
@@ -96,6 +100,7 @@ struct BwdArgs {
   Sched sched;       // single-launch sequence parallelism when sched_on, see FwdArgs
   int sched_on;
   int bal_pairs, bal_ns, bal_big;  // balanced chain over equal-length sequences, see FwdArgs
+  int passA_items;                 // pass A by ticket (status word 5), see FwdArgs
 };
 
 struct FixupArgs {
@@ -108,6 +113,9 @@ struct FixupArgs {
   int reverse;
   const int *fixflag;  // nonzero iff some segment of this direction needs the fix-up (NULL: always run)
   int *status;         // status word (an expired wait for a step's inputs sets value 4), or NULL
+  // NULL: grid (D / FIX_ROWS, H, N), one row block per CTA; else a 1-D grid whose CTAs take the row blocks
+  // t (rb = t % (D / FIX_ROWS), then head, then sequence) by ticket from this zeroed counter
+  int *ticket;
 };
 
 struct RecArgs {
@@ -130,7 +138,8 @@ int launch_plan(const Plan &p, const int *cu, int N, int T, int Lseg, int Lfirst
 // sched[0] / sched[1]: forward / reverse schedules to build (hdr NULL: none)
 int launch_gate_scan(const Plan &p, const float *g, int H, int CH_max, float *gsum, int *status, int modes, int Lseg,
                      int Lfirst, int S_max, unsigned flags, const Sched *sched, int NH, cudaStream_t st);
-int launch_fixup(const FixupArgs &a, int N, cudaStream_t st);
+// ctas > 0 (with a.ticket set): that many CTAs take the row blocks by ticket
+int launch_fixup(const FixupArgs &a, int N, int ctas, cudaStream_t st);
 
 int launch_fwd_chunk(const FwdArgs &a, bool is_bf16, int D, dim3 grid, cudaStream_t st);
 // tcgen05 forward for bf16 inputs and d = 128, chunk-local half: one CTA per (chunk, head) over CH_max x H;

@@ -32,7 +32,7 @@ __global__ void plan_kernel(Plan p, const int *cu, int N, int T, int Lseg, int L
   __shared__ int carry_c, carry_s, bad;
   __shared__ int wsum_c[32], wsum_s[32];
   const int tid = threadIdx.x, nt = blockDim.x;
-  if (tid < 4 && status) status[tid] = 0;  // status word and the fix-up flags of this call
+  if (tid < 8 && status) status[tid] = 0;  // status word, fix-up flags, counters and tickets of this call
   for (int i = tid; i < nzero; i += nt) zero[i] = 0;  // the schedules' counters
   __syncthreads();
   if (tid == 0) {
@@ -224,29 +224,46 @@ int launch_gate_scan(const Plan &p, const float *g, int H, int CH_max, float *gs
                          S_max, flags, sched ? sched[0] : none, sched ? sched[1] : none, NH);
 }
 
-// grid (D / FIX_ROWS, H, N), 256 threads: one fix-up row block per CTA (see fixup_rows)
+// 256 threads; grid (D / FIX_ROWS, H, N), one fix-up row block per CTA (see fixup_rows), or, with a ticket
+// counter, a 1-D grid whose CTAs take the row blocks in turn: a call whose segments need no fix-up (or
+// few) then costs one short wave of CTAs instead of one CTA per row block
 template <int D>
-__global__ void __launch_bounds__(256, 1) fixup_kernel(FixupArgs a) {
+__global__ void __launch_bounds__(256, 1) fixup_kernel(FixupArgs a, int nitems) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ __align__(16) unsigned char fx_smem[];
-  fixup_rows<D>(a, blockIdx.x, blockIdx.y, blockIdx.z, fx_smem);
+  if (!a.ticket) {
+    fixup_rows<D>(a, blockIdx.x, blockIdx.y, blockIdx.z, fx_smem);
+    return;
+  }
+  if (a.fixflag && *a.fixflag == 0) return;  // no segment of this direction needs the exact fix-up
+  constexpr int NRB = D / FIX_ROWS;
+  __shared__ int tk;
+  for (;;) {
+    if (threadIdx.x == 0) tk = atomicAdd(a.ticket, 1);
+    __syncthreads();
+    const int t = tk;
+    __syncthreads();  // every thread has its ticket before thread 0 takes the next one
+    if (t >= nitems) break;
+    fixup_rows<D>(a, t % NRB, (t / NRB) % a.H, t / (NRB * a.H), fx_smem);
+  }
 }
 
-int launch_fixup(const FixupArgs &a, int N, cudaStream_t st) {
+int launch_fixup(const FixupArgs &a, int N, int ctas, cudaStream_t st) {
   if (N == 0) return 0;
-  dim3 grid(a.D / FIX_ROWS, a.H, N);
+  const int nitems = a.D / FIX_ROWS * a.H * N;
+  const dim3 grid = (a.ticket && ctas > 0) ? dim3(min(ctas, nitems)) : dim3(a.D / FIX_ROWS, a.H, N);
   if (a.D == 128) {
     const size_t smem = fixup_smem_bytes<128>();
     cudaError_t e = cudaFuncSetAttribute(fixup_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
-    return (int)launch_pdl(fixup_kernel<128>, grid, dim3(256), smem, st, a);
+    return (int)launch_pdl(fixup_kernel<128>, grid, dim3(256), smem, st, a, nitems);
   }
   if (a.D == 64) {
     const size_t smem = fixup_smem_bytes<64>();
     cudaError_t e = cudaFuncSetAttribute(fixup_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
-    return (int)launch_pdl(fixup_kernel<64>, grid, dim3(256), smem, st, a);
+    return (int)launch_pdl(fixup_kernel<64>, grid, dim3(256), smem, st, a, nitems);
   }
   return -1;
 }
