@@ -82,10 +82,10 @@ def job_throughput(total_ms, world, tokens_per_rank_step, steps):
 # the local headers it includes, transitively) hashes to the value recorded with it (otherwise the
 # roofline reports traffic null).  Summaries: profiles/*.md.
 NCU_TRAFFIC = {
-    ("bwd_local", "prefill_h32_t8192"): (1022306048, "bwd_local_tc.cu", "57964d101249e66e"),
-    ("fwd_chunk", "prefill_h32_t8192"): (600421120, "fwd_tc.cu", "bdbd57d0cf46daba"),
-    ("fwd_prep", "prefill_h32_t8192"): (514352128, "fwd_prep_tc.cu", "3037a1075ea78ed0"),
-    ("bwd_chain", "prefill_h32_t8192"): (537797888, "bwd_chain_tc.cu", "1dbc4ee01d1e8903"),
+    ("bwd_local", "prefill_h32_t8192"): (1022408448, "bwd_local_tc.cu", "f15506e0ea430b99"),
+    ("fwd_chunk", "prefill_h32_t8192"): (600498432, "fwd_tc.cu", "b3a39be3664ecd47"),
+    ("fwd_prep", "prefill_h32_t8192"): (514248192, "fwd_prep_tc.cu", "77e78cd414c8d8f3"),
+    ("bwd_chain", "prefill_h32_t8192"): (538007552, "bwd_chain_tc.cu", "62b3c316657cdd71"),
 }
 
 
