@@ -854,6 +854,10 @@ int bwd_impl(const gdn_shape *s, const void *q, const void *k, const void *v, co
   ba.H = L.H;
   ba.Lseg = L.Lseg;
   ba.Lfirst = L.Lfirst;
+  if (!s->cu_seqlens && L.Tseq > 0) {  // equal-length sequences: the local kernel's chunk order
+    ba.ord_n = L.N;
+    ba.ord_nc = (L.Tseq + CH - 1) / CH;
+  }
   ba.scale = s->scale;
   ba.flags = s->flags;
   // the reverse chain: tcgen05 for bf16 with d = 128, the mma.sync kernel otherwise

@@ -71,6 +71,58 @@ struct __align__(1024) LocalTcSmem {
 
 __device__ __forceinline__ uint32_t u32(const void *p) { return smem_u32(p); }
 
+// The r-th chunk (0 <= r < N nc) of N equal-length sequences of nc chunks, segments of F then L chunks,
+// in the order of the chunk's offset within its segment, then sequence, then segment.  The reverse chain
+// walks every segment at once from its last chunk to its first, so the chunks it hands over last, whose
+// tiles are the likeliest to be still in L2, come first (the order changes no result: every item of the
+// local kernel is independent).  Per sequence: a first segment of len0 chunks, nfull of L and a last of
+// llast, so the number of segments with a chunk at offset o changes only at len0, L and llast: the
+// offsets fall into at most three runs of equal width, walked here in closed form.
+struct LifoOrder {
+  int N, S, len0, nfull, llast, cut[3];  // cut: len0, L, llast in ascending order
+};
+__device__ __forceinline__ LifoOrder lifo_order(int N, int nc, int F, int L) {
+  LifoOrder q;
+  q.N = N;
+  q.S = seg_count(nc, F, L);
+  q.len0 = min(F, nc);
+  q.nfull = q.S > 2 ? q.S - 2 : 0;
+  q.llast = q.S > 1 ? nc - seg_begin(q.S - 1, F, L) : 0;
+  int a = q.len0, b = L, c = q.llast, t;
+  if (a > b) { t = a; a = b; b = t; }
+  if (b > c) { t = b; b = c; c = t; }
+  if (a > b) { t = a; a = b; b = t; }
+  q.cut[0] = a;
+  q.cut[1] = b;
+  q.cut[2] = c;
+  return q;
+}
+__device__ __forceinline__ int lifo_chunk(const LifoOrder &q, int r, int nc, int F, int L) {
+  int lo = 0, base = 0;
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+    const int hi = q.cut[i];
+    if (hi > lo) {
+      const int m = (lo < q.len0) + (lo < L ? q.nfull : 0) + (lo < q.llast);  // segments per offset in [lo, hi)
+      const int per = q.N * m, cnt = per * (hi - lo);
+      if (r < base + cnt) {
+        const int rr = r - base, o = lo + rr / per, idx = rr - (o - lo) * per, n = idx / m;
+        int k = idx - n * m, j;
+        if (o < q.len0 && k == 0) {
+          j = 0;
+        } else {
+          k -= o < q.len0;
+          j = (o < L && k < q.nfull) ? 1 + k : q.S - 1;
+        }
+        return n * nc + seg_begin(j, F, L) + o;
+      }
+      base += cnt;
+      lo = hi;
+    }
+  }
+  return r;  // not reached for r < N nc
+}
+
 __device__ __forceinline__ void st_chunk_f16(uint8_t *dst, const float *v) {
   __half2 h[4];
 #pragma unroll
@@ -203,20 +255,25 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     }
   };
 
-  // Work items (chunk gc, head h) = (item / H, item % H), strided over the persistent CTAs; the chunks in
-  // use are the plan's first totals[0] (all of them, or none for a malformed plan).  The tiles of the next
-  // item are loaded by TMA while this one finishes.
+  // Work items (chunk gc, head h): item = gc H + h; the CTAs take the ranks b, b + G, ... and rank r is
+  // head r % H of chunk lifo_chunk(r / H) for equal-length sequences (the chunks the reverse chain handed
+  // over last first), of chunk r / H otherwise; the chunks in use are the plan's first totals[0] (all of
+  // them, or none for a malformed plan).  The tiles of the next item are loaded by TMA while this one
+  // finishes.
   const int tot_c = a.plan.totals[0];
-  const int lim = tot_c <= n_items / H ? tot_c * H : 0;  // items of the chunks in use
-  auto next_valid = [&](int item) { return item < lim ? item : n_items; };
-  // first token and valid rows of a work item (one plan look-up, done one item ahead)
+  const int lim = tot_c <= n_items / H ? tot_c * H : 0;  // ranks of the chunks in use
+  auto next_valid = [&](int rank) { return rank < lim ? rank : n_items; };
+  const LifoOrder lq = lifo_order(a.ord_n, a.ord_nc, a.Lfirst, a.Lseg);
+  // the item, first token and valid rows of a rank (one plan look-up, done one item ahead)
   struct ItemInfo {
-    int item, tok0, nvalid;
+    int item, tok0, nvalid, rank;
   };
-  auto info_of = [&](int item) {
-    ItemInfo r{item, 0, 0};
-    if (item < n_items) {
-      const int2 ci = a.plan.chunk_info[item / H];
+  auto info_of = [&](int rank) {
+    ItemInfo r{n_items, 0, 0, rank};
+    if (rank < n_items) {
+      const int gc = a.ord_nc > 0 ? lifo_chunk(lq, rank / H, a.ord_nc, a.Lfirst, a.Lseg) : rank / H;
+      const int2 ci = a.plan.chunk_info[gc];
+      r.item = gc * H + rank % H;
       r.tok0 = ci.x;
       r.nvalid = ci.y;
     }
@@ -317,7 +374,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
     break;
   }
   // the next item, looked up by the producer before B2 (dependent global loads the workers do not wait for)
-  const ItemInfo nxt{sm.nxt_info[0], sm.nxt_info[1], sm.nxt_info[2]};
+  const ItemInfo nxt{sm.nxt_info[0], sm.nxt_info[1], sm.nxt_info[2], 0};
   const int nitem = nxt.item;
   if (nitem < n_items && tid < 128) {  // the next item's g or beta, stored under P7 (its plan lookups have landed by now)
     const int r = tid & 63, nh = nitem % H;
@@ -774,7 +831,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
        open_w = false;
   uint32_t par_a = 0, par_b = 0, par_w = 0, par_c = 0;
   // plan look-ups one item ahead: dependent global loads, done while the producer waits at B10
-  ItemInfo nxt = info_of(next_valid(cur.item + gridDim.x));
+  ItemInfo nxt = info_of(next_valid(cur.rank + gridDim.x));
   bool deferred = false;  // this item's V, Ahat and N wait for the previous item's output stores: issued after B2
   for (; cur.item < n_items; ++it) {
     const int nitem = nxt.item;
@@ -929,7 +986,7 @@ __global__ void __launch_bounds__(LNTHREADS, 1)
       mma_commit(u32(&sm.bar_mma));
     }
     __syncwarp();
-    const ItemInfo nn = info_of(next_valid(nitem + gridDim.x));  // the item after the next one
+    const ItemInfo nn = info_of(next_valid(nxt.rank + gridDim.x));  // the item after the next one
     if (__syncthreads_or(false)) break;  // B10
     // dq (staged in the Ahat and N buffers) and dk (in V's buffer); the next item's K, Q and norms (R9 has read
     // them); its V, Ahat and N follow after its B2, once the stores have read the staging

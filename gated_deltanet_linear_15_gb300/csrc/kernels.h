@@ -101,6 +101,9 @@ struct BwdArgs {
   int sched_on;
   int bal_pairs, bal_ns, bal_big;  // balanced chain over equal-length sequences, see FwdArgs
   int passA_items;                 // pass A by ticket (status word 5), see FwdArgs
+  // local gradients over ord_n equal-length sequences of ord_nc chunks each: the chunks in the order of
+  // their offset within the segment (lifo_chunk in bwd_local_tc.cu); 0: in chunk order
+  int ord_n, ord_nc;
 };
 
 struct FixupArgs {
