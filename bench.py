@@ -82,10 +82,10 @@ def job_throughput(total_ms, world, tokens_per_rank_step, steps):
 # the local headers it includes, transitively) hashes to the value recorded with it (otherwise the
 # roofline reports traffic null).  Summaries: profiles/*.md.
 NCU_TRAFFIC = {
-    ("bwd_local", "prefill_h32_t8192"): (1022408448, "bwd_local_tc.cu", "f15506e0ea430b99"),
-    ("fwd_chunk", "prefill_h32_t8192"): (600498432, "fwd_tc.cu", "b3a39be3664ecd47"),
-    ("fwd_prep", "prefill_h32_t8192"): (514248192, "fwd_prep_tc.cu", "77e78cd414c8d8f3"),
-    ("bwd_chain", "prefill_h32_t8192"): (538007552, "bwd_chain_tc.cu", "62b3c316657cdd71"),
+    ("bwd_local", "prefill_h32_t8192"): (1022568192, "bwd_local_tc.cu", "f974d11495cedf5e"),
+    ("fwd_chunk", "prefill_h32_t8192"): (599764224, "fwd_tc.cu", "1f89580d4ef10f85"),
+    ("fwd_prep", "prefill_h32_t8192"): (513900800, "fwd_prep_tc.cu", "40c0954d21fe6409"),
+    ("bwd_chain", "prefill_h32_t8192"): (537678080, "bwd_chain_tc.cu", "ec98eaa20e34262a"),
 }
 
 
